@@ -1,0 +1,468 @@
+"""Benchmark of the NVFP4 rollout linear layer on one GB300 (or N replicas).
+
+Workload (one step): a Qwen2.5-7B-shaped decoder layer in W4A16 decode --
+hidden 3584; q/o 3584x3584, gate/up 18944x3584, down 3584x18944 bf16 weights
+~N(0, 0.02) with 1% outlier columns x8; M = 64 bf16 tokens; LoRA r = 32 on every
+linear; AQN sigma schedule 1e-2 -> 5e-4 over K = 10. One step runs every stage of
+the path on that layer:
+  1. AQN sigma_k (host) and RMSNorm-AQN of the 64 tokens (input norm), then again
+     (post-attention norm);
+  2. the rollout weight refresh: per weight, the tensor amax and the NVFP4
+     encoding (codes, E4M3 block scales, fp32 g);
+  3. the five W4A16 LoRA linears at M = 64.
+Inputs are synthetic, generated on the device from a seed, and larger than L2
+(the five bf16 weights are 458 MB); L2 is also flushed between steps.
+
+Prints one JSON line. `value` is algorithmic bytes per step (what the method must
+move, each tensor once) over the device time of a step, summed over ranks.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 LoRA-linear TFLOP/s & HBM GB/s (% roofline); quantize GB/s, 1×GB300"
+WORKLOAD = ("qwen2.5-7b-shaped decode layer, W4A16: hidden 3584, q/o 3584x3584, gate/up 18944x3584, "
+            "down 3584x18944, M=64 tokens, LoRA r=32 s=2, AQN sigma 1e-2->5e-4 over K=10, "
+            "weight refresh (amax + NVFP4 encode) of all five weights each step")
+HIDDEN, INTER, M_TOK, RANK, S_LORA = 3584, 18944, 64, 32, 2.0
+LINEARS = [("q", 3584, 3584), ("o", 3584, 3584), ("gate", 18944, 3584), ("up", 18944, 3584), ("down", 3584, 18944)]
+SIGMA0, SIGMAK, KSCHED = 1e-2, 5e-4, 10
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- byte / flop counts
+
+def bytes_rmsnorm(M, H):
+    return M * H * 2 * 2 + H * 8
+
+
+def bytes_quantize(n):
+    return n * (2 + 0.5 + 0.0625)
+
+
+def bytes_linear(M, N, K, r):
+    return N * K * 0.5625 + 2 * M * K + 2 * M * N + 2 * r * (K + N)
+
+
+def flops_linear(M, N, K, r):
+    return 2 * M * N * K + 2 * M * r * (K + N)
+
+
+def step_bytes():
+    b = 2 * bytes_rmsnorm(M_TOK, HIDDEN)
+    b += sum(bytes_quantize(n * k) for _, n, k in LINEARS)
+    b += sum(bytes_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
+    return b
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons in the background."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+
+    def __init__(self, index=0):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                parts = [p.strip() for p in out.stdout.strip().split(",")]
+                if len(parts) == 3:
+                    self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [s[0] for s in self.samples]
+        mask = 0
+        for s in self.samples:
+            mask |= s[2]
+        reasons = [name for bit, name in self.REASONS.items() if mask & bit and name != "gpu_idle"]
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(s[1] for s in self.samples), "reasons": reasons,
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def source_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[kernel]
+        if d.get("source_hash") != source_hash(*d["sources"]):
+            return None
+        return d
+    except Exception:
+        return None
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    import nvfp4_quantized_rl_gb300 as nv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+
+    def randn(*shape, std=1.0):
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).mul_(std)
+
+    # weights: bf16 ~N(0, 0.02), 1% of the input columns x8
+    W = {}
+    for name, n, k in LINEARS:
+        w = randn(n, k, std=0.02)
+        cols = torch.randperm(k, generator=gen, device=dev)[: round(0.01 * k)]
+        w[:, cols] *= 8
+        W[name] = w.to(torch.bfloat16)
+        del w
+    lora = {name: (randn(RANK, k, std=0.02).to(torch.bfloat16), randn(n, RANK, std=0.02).to(torch.bfloat16))
+            for name, n, k in LINEARS}
+    x_in = randn(M_TOK, HIDDEN).to(torch.bfloat16)
+    x_res = randn(M_TOK, HIDDEN).to(torch.bfloat16)
+    attn = randn(M_TOK, HIDDEN).to(torch.bfloat16)
+    act = randn(M_TOK, INTER).to(torch.bfloat16)
+    w1, w2 = (1 + randn(HIDDEN, std=0.1)), (1 + randn(HIDDEN, std=0.1))
+    eps = [randn(HIDDEN) for _ in range(KSCHED + 1)]
+
+    # outputs and workspaces, allocated once
+    Q = {name: (torch.empty(n, k // 2, dtype=torch.uint8, device=dev), torch.empty(n, k // 16, dtype=torch.uint8, device=dev),
+                torch.empty(1, dtype=torch.float32, device=dev), torch.empty(1, dtype=torch.float32, device=dev))
+         for name, n, k in LINEARS}
+    Y = {name: torch.empty(M_TOK, n, dtype=torch.bfloat16, device=dev) for name, n, k in LINEARS}
+    h1 = torch.empty(M_TOK, HIDDEN, dtype=torch.bfloat16, device=dev)
+    h2 = torch.empty_like(h1)
+    ws_bytes = max(nv.workspace_bytes(nv.OP_LINEAR_W4A16, M_TOK, n, k, RANK) for _, n, k in LINEARS)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    inputs = {"q": h1, "o": attn, "gate": h2, "up": h2, "down": act}
+    stream = torch.cuda.current_stream(dev)
+
+    # per-op CUDA events (all launches go to the current stream)
+    ops = ["rmsnorm_aqn"] + [f"amax_{n}" for n, _, _ in LINEARS] + [f"quantize_{n}" for n, _, _ in LINEARS] + \
+          [f"linear_{n}" for n, _, _ in LINEARS]
+
+    def step(k, ev=None):
+        def mark(name, fn):
+            if ev is None:
+                fn()
+                return
+            a, b = ev[name]
+            a.record(stream)
+            fn()
+            b.record(stream)
+        sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
+        mark("rmsnorm_aqn", lambda: nv.rmsnorm_aqn(x_in, w1, eps[k], sigma, 1e-6, out=h1))
+        for name, n, kk in LINEARS:
+            c, s, g, a = Q[name]
+            mark(f"amax_{name}", lambda: nv.nvfp4_amax(W[name], out=a))
+            mark(f"quantize_{name}", lambda: nv.nvfp4_quantize(W[name], amax_in=a, codes=c, scales=s, g=g))
+        nv.rmsnorm_aqn(x_res, w2, eps[k], sigma, 1e-6, out=h2)
+        for name, n, kk in LINEARS:
+            c, s, g, _ = Q[name]
+            A, B = lora[name]
+            mark(f"linear_{name}", lambda: nv.nvfp4_lora_linear(inputs[name], c, s, g, A, B, S_LORA, out=Y[name],
+                                                                 workspace=ws))
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i % (KSCHED + 1))
+    torch.cuda.synchronize()
+
+    evs = [{name: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for name in ops}
+           for _ in range(args.steps)]
+    bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = nv.kernel_launches()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps, outside the step's events
+            bounds[i][0].record(stream)
+            step(i % (KSCHED + 1), evs[i])
+            bounds[i][1].record(stream)
+        torch.cuda.synchronize()
+    launches = nv.kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in bounds]
+    total_ms = float(sum(step_ms))
+    op_ms = {name: float(np.mean([e[name][0].elapsed_time(e[name][1]) for e in evs])) for name in ops}
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end: host buffers in, host result out, through the same public API
+    e2e = run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, Q, Y, h1, h2, ws, flush,
+                  inputs, world)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    hbm, bf16_tf, peak_src = peaks()
+    sb = step_bytes()
+    value = sb * world / (total_ms / args.steps / 1e3) / 1e9
+
+    # parts
+    q_bytes = sum(bytes_quantize(n * k) for _, n, k in LINEARS)
+    q_ms = sum(op_ms[f"quantize_{n}"] for n, _, _ in LINEARS)
+    a_ms = sum(op_ms[f"amax_{n}"] for n, _, _ in LINEARS)
+    l_bytes = sum(bytes_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
+    l_flops = sum(flops_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
+    l_ms = sum(op_ms[f"linear_{n}"] for n, _, _ in LINEARS)
+    parts = {
+        "rmsnorm_aqn": {"us": op_ms["rmsnorm_aqn"] * 1e3,
+                        "GB/s": bytes_rmsnorm(M_TOK, HIDDEN) / op_ms["rmsnorm_aqn"] / 1e6},
+        "amax": {"us": a_ms * 1e3, "GB/s": sum(2 * n * k for _, n, k in LINEARS) / a_ms / 1e6},
+        "quantize_encode": {"us": q_ms * 1e3, "GB/s": q_bytes / q_ms / 1e6},
+        "quantize_op": {"us": (q_ms + a_ms) * 1e3, "GB/s": q_bytes / (q_ms + a_ms) / 1e6},
+        "lora_linear_w4a16": {"us": l_ms * 1e3, "GB/s": l_bytes / l_ms / 1e6, "TFLOP/s": l_flops / l_ms / 1e9,
+                              "frac_hbm": l_bytes / l_ms / 1e6 / hbm},
+        "per_linear_us": {n: op_ms[f"linear_{n}"] * 1e3 for n, _, _ in LINEARS},
+    }
+    # dominant kernel by device time
+    groups = {"quantize_kernel": q_ms, "amax_kernel": a_ms, "lora_linear_w4a16": l_ms,
+              "rmsnorm_aqn_kernel": op_ms["rmsnorm_aqn"]}
+    dom = max(groups, key=groups.get)
+    if dom == "quantize_kernel":
+        ach, launches_per = q_bytes / q_ms / 1e6, len(LINEARS)
+        per_launch_bytes = q_bytes / len(LINEARS)
+    elif dom == "amax_kernel":
+        ach = parts["amax"]["GB/s"]
+        per_launch_bytes = sum(2 * n * k for _, n, k in LINEARS) / len(LINEARS)
+    elif dom == "lora_linear_w4a16":
+        ach = l_bytes / l_ms / 1e6
+        per_launch_bytes = l_bytes / len(LINEARS)
+    else:
+        ach = parts["rmsnorm_aqn"]["GB/s"]
+        per_launch_bytes = bytes_rmsnorm(M_TOK, HIDDEN)
+    tr = recorded_traffic(dom)
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+                "algorithmic_bytes_per_launch": per_launch_bytes,
+                "traffic": None if tr is None else tr["dram_bytes_per_launch"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, generated on device)",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 and a 256 MB write between timed steps",
+                   "replicas": world, "algorithmic_bytes_per_step": sb},
+        "parts": parts, "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, Q, Y, h1, h2, ws, flush, inputs,
+            world):
+    """Same step through the public API, with each step's inputs copied from pinned host memory and every
+    output read back to pinned host memory inside the timed region."""
+    host_in = {name: W[name].cpu().pin_memory() for name, _, _ in LINEARS}
+    host_x = {"x_in": x_in.cpu().pin_memory(), "x_res": x_res.cpu().pin_memory(), "attn": attn.cpu().pin_memory(),
+              "act": act.cpu().pin_memory()}
+    dev_x = {"x_in": x_in, "x_res": x_res, "attn": attn, "act": act}
+    host_out = {name: torch.empty(Y[name].shape, dtype=torch.bfloat16).pin_memory() for name, _, _ in LINEARS}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+        sum(t.numel() * t.element_size() for t in host_x.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    stream = torch.cuda.current_stream(dev)
+    inputs_e2e = {"q": h1, "o": dev_x["attn"], "gate": h2, "up": h2, "down": dev_x["act"]}
+
+    def step(k):
+        for name, _, _ in LINEARS:
+            W[name].copy_(host_in[name], non_blocking=True)
+        for key in host_x:
+            dev_x[key].copy_(host_x[key], non_blocking=True)
+        sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
+        nv.rmsnorm_aqn(dev_x["x_in"], w1, eps[k], sigma, 1e-6, out=h1)
+        for name, _, _ in LINEARS:
+            c, s, g, a = Q[name]
+            nv.nvfp4_amax(W[name], out=a)
+            nv.nvfp4_quantize(W[name], amax_in=a, codes=c, scales=s, g=g)
+        nv.rmsnorm_aqn(dev_x["x_res"], w2, eps[k], sigma, 1e-6, out=h2)
+        for name, _, _ in LINEARS:
+            c, s, g, _ = Q[name]
+            A, B = lora[name]
+            nv.nvfp4_lora_linear(inputs_e2e[name], c, s, g, A, B, S_LORA, out=Y[name], workspace=ws)
+        for name, _, _ in LINEARS:
+            host_out[name].copy_(Y[name], non_blocking=True)
+
+    for i in range(max(1, args.warmup)):
+        step(i % (KSCHED + 1))
+    torch.cuda.synchronize()
+    n = max(1, args.steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(n):
+        step(i % (KSCHED + 1))
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": step_bytes() * world / (ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample(seconds_budget: float):
+    """A bounded sample of the same step, run by the CPU oracle: RMSNorm of all 64 tokens, the NVFP4
+    encoding of a seeded 1/64 of each weight's rows, and every linear's outputs for 1/64 of its output
+    columns (all 64 tokens). Returns (algorithmic bytes of the sample, seconds, threads)."""
+    import oracle
+    import synth
+    t_total, bytes_total = 0.0, 0.0
+    nthreads = oracle.threads()
+    x = synth.activation_bf16(M_TOK, HIDDEN, 9, 0)
+    w = synth.aqn_weight(HIDDEN, 9, 1)
+    e = synth.aqn_eps(HIDDEN, 9, 2)
+    t0 = time.perf_counter()
+    oracle.rmsnorm_aqn(x, w, e, np.float32(SIGMA0), 1e-6)
+    oracle.rmsnorm_aqn(x, w, e, np.float32(SIGMA0), 1e-6)
+    t_total += time.perf_counter() - t0
+    bytes_total += 2 * bytes_rmsnorm(M_TOK, HIDDEN)
+    for i, (name, n, k) in enumerate(LINEARS):
+        rows = n // 64
+        Wb = synth.weight_bf16(rows, k, 0.02, 9, 10 + i, outlier_frac=0.01)
+        t0 = time.perf_counter()
+        codes, scales, g = oracle.quantize(Wb)
+        t_total += time.perf_counter() - t0
+        bytes_total += bytes_quantize(rows * k)
+        A, B = synth.lora_factors(RANK, k, rows, 9, 20 + i)
+        xi = synth.activation_bf16(M_TOK, k, 9, 30 + i)
+        t0 = time.perf_counter()
+        oracle.lora_linear_w4a16(xi, codes, scales, g, A, B, S_LORA)
+        t_total += time.perf_counter() - t0
+        bytes_total += bytes_linear(M_TOK, rows, k, RANK)
+    return bytes_total, t_total, nthreads
+
+
+SAMPLE_DESC = ("RMSNorm-AQN of the 64x3584 tokens twice; NVFP4 encoding of 1/64 of each weight's rows; "
+               "each LoRA linear on 1/64 of its output columns for all 64 tokens (fp64 oracle)")
+
+
+def cpu_baseline(seconds_budget=20.0):
+    b, t, th = oracle_sample(seconds_budget)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": SAMPLE_DESC,
+            "sample_seconds": t}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(0)
+    tot_b, tot_t, th = 0.0, 0.0, 1
+    for _ in range(args.steps):
+        b, t, th = oracle_sample(0)
+        tot_b += b
+        tot_t += t
+    v = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_t / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "sample": SAMPLE_DESC},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": SAMPLE_DESC},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

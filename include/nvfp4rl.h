@@ -1,0 +1,208 @@
+/*
+ * nvfp4rl.h -- C ABI of the NVFP4 rollout-linear library (one GB300 GPU, sm_103a).
+ *
+ * The library implements the quantized rollout linear layer of QeRL-style
+ * low-precision RL: NVFP4 block quantization (plain and rollout-guided),
+ * AQN-noised RMSNorm, and the NVFP4-weight linear layer with a fused LoRA
+ * branch, with 16-bit activations (W4A16) or activations quantized on the fly
+ * (W4A4, optionally grouped per MoE expert).
+ *
+ * Sources of the operations (the pages describe them in prose; the concrete
+ * recipe is stated with each entry point):
+ *   - "QeRL: Beyond Efficiency -- Quantization-enhanced Reinforcement Learning
+ *     for LLMs" explainer (lifetechia.com), sections "NVFP4量子化とLoRA",
+ *     "AQNの仕組み" and "ゼロオーバーヘッド：レイヤー正規化への統合";
+ *   - "TRACE: rollout-guided quantization-aware training" summary (sns.style),
+ *     sections "TRACE の中心的なアイデア" and "仕組みの工学的な理解".
+ *
+ * Conventions shared by every entry point:
+ *   - Memory: every pointer argument is DEVICE memory, allocated and owned by
+ *     the caller, and must be 16-byte aligned. The library allocates nothing;
+ *     it keeps only per-device cached attributes and kernel resources.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Calls are asynchronous on that stream; outputs are complete when
+ *     the stream reaches the call. Inputs are never written.
+ *   - bf16 tensors are passed as uint16_t bit patterns, row-major.
+ *   - Errors: arguments are validated on the host before any launch; a failed
+ *     check returns its status and launches nothing. A launch failure returns
+ *     NVFP4RL_ERR_CUDA. Inputs must be finite (not checked on the device).
+ *   - Outputs must not overlap inputs (NVFP4RL_ERR_ALIAS).
+ *   - Zero-sized problems (rows == 0, M == 0) are valid no-ops.
+ */
+#ifndef NVFP4RL_H_
+#define NVFP4RL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4RL_API __attribute__((visibility("default")))
+#else
+#define NVFP4RL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4rl_status {
+  NVFP4RL_OK = 0,
+  NVFP4RL_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad dtype, r or groups out of range */
+  NVFP4RL_ERR_MISALIGNED = 2,        /* a pointer is not 16-byte aligned */
+  NVFP4RL_ERR_UNSUPPORTED_SHAPE = 3, /* a dimension is not a multiple of what the kernel needs */
+  NVFP4RL_ERR_WORKSPACE = 4,         /* workspace missing or smaller than nvfp4rl_workspace_bytes() */
+  NVFP4RL_ERR_CUDA = 5,              /* a CUDA runtime call or a kernel launch failed */
+  NVFP4RL_ERR_TIMEOUT = 6,           /* a bounded device-side wait ran out (reported by nvfp4rl_device_status) */
+  NVFP4RL_ERR_ALIAS = 7,             /* an output buffer overlaps an input buffer */
+  NVFP4RL_ERR_DEVICE = 8             /* the current device is not a compute-capability 10.3 GPU */
+} nvfp4rl_status;
+
+/* Element types of quantizer inputs. */
+enum { NVFP4RL_BF16 = 0, NVFP4RL_F32 = 1 };
+
+/* Operations for nvfp4rl_workspace_bytes(). */
+enum { NVFP4RL_OP_QUANTIZE = 0, NVFP4RL_OP_LINEAR_W4A16 = 1, NVFP4RL_OP_LINEAR_W4A4 = 2 };
+
+/*
+ * nvfp4_amax -- per-tensor absolute maximum, the input of the NVFP4 per-tensor
+ *   scale g = amax / (6 * 448) (QeRL explainer, "NVFP4量子化とLoRA"; TRACE summary,
+ *   "仕組みの工学的な理解": block scaling under one tensor-level scale).
+ *   x      [n] bf16 bits or fp32 (dtype), n multiple of 16.
+ *   amax   out, one fp32 = max |x_i| (0 for n == 0). Its result can be passed as
+ *          amax_in to nvfp4_quantize / nvfp4_quantize_guided.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_amax(const void* x, int32_t dtype, int64_t n, float* amax, void* stream);
+
+/*
+ * nvfp4_quantize -- NVFP4 block quantization of a rows x cols tensor.
+ *   QeRL explainer, "NVFP4量子化とLoRA" (4-bit weights with hardware support);
+ *   TRACE summary, "仕組みの工学的な理解" (a few values share one scale, each
+ *   value is 4 bits).
+ * Recipe: g = fl32(amax / 2688) with amax = max |x| over the tensor (or *amax_in);
+ *   for each 16-element block b along a row, s_b = the E4M3 byte nearest to
+ *   bamax_b / (6 g) (ties to the even byte, saturating at 448, 0 when g == 0);
+ *   each element's 4-bit code = sign bit (bit 3) | the index of the E2M1 grid
+ *   point {0,.5,1,1.5,2,3,4,6} nearest to |x| / (E4M3(s_b) g) (ties to the even
+ *   index, saturating at 6; code sign|0 when the scale is 0). Both roundings
+ *   apply to the exact real quotient.
+ * Arguments:
+ *   x        [rows][cols] bf16 bits (dtype NVFP4RL_BF16) or fp32 (NVFP4RL_F32).
+ *   cols     multiple of 16.
+ *   codes    out, [rows][cols/2] bytes; element 2j in the low nibble of byte j.
+ *   scales   out, [rows][cols/16] E4M3 bytes.
+ *   g        out, one fp32.
+ *   amax_in  optional device fp32; when non-NULL it replaces the computed
+ *            amax and the tensor is read once (workspace may then be NULL).
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_QUANTIZE, ...) bytes when
+ *            amax_in is NULL; scratch, contents undefined between calls.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_quantize(const void* x, int32_t dtype, int64_t rows, int64_t cols,
+                              uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * nvfp4_quantize_guided -- NVFP4 quantization whose rounding direction comes
+ *   from a cached 1-bit-per-element mask (TRACE summary, "TRACE の中心的なアイデア":
+ *   the trainer reproduces the rollout's rounding decisions from cached mantissa
+ *   and scale information; "仕組みの工学的な理解": the rounding direction is a
+ *   per-value choice between the two neighbouring grid points).
+ * Same as nvfp4_quantize, except for each element's magnitude code: with
+ *   a = |x| / (E4M3(s_b) g): a >= 6 gives 6; a grid point a is kept; otherwise
+ *   mask bit 1 takes the larger-magnitude neighbour, bit 0 the smaller one.
+ *   Scale bytes and g are those of nvfp4_quantize.
+ *   mask     [ceil(rows*cols/32)] uint32 words; element i (flat row-major index)
+ *            uses bit (i % 32) of word i / 32.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_quantize_guided(const void* x, int32_t dtype, int64_t rows, int64_t cols,
+                                     const uint32_t* mask, uint8_t* codes, uint8_t* scales, float* g,
+                                     const float* amax_in, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * aqn_sigma -- AQN exponential noise schedule (QeRL explainer, "AQNの仕組み":
+ *   large noise early, small noise late): sigma_k = sigma0 * (sigmaK/sigma0)^(k/K),
+ *   k = 0..K. Host function, no device work. Returns NaN for K <= 0 or
+ *   non-positive sigmas.
+ */
+NVFP4RL_API double aqn_sigma(double sigma0, double sigmaK, int64_t k, int64_t K);
+
+/*
+ * rmsnorm_aqn -- RMSNorm with adaptive quantization noise folded into its
+ *   weight (QeRL explainer, "ゼロオーバーヘッド：レイヤー正規化への統合":
+ *   X_noise = (Z_noise + w) * X / sqrt(sum(X^2) + delta); the mean of squares is
+ *   used, as in standard RMSNorm).
+ *   y[m][j] = bf16( (w[j] + sigma * eps[j]) * x[m][j] / sqrt(mean_j x[m][j]^2 + delta) )
+ *   x    [M][H] bf16 bits; H multiple of 8.
+ *   w    [H] fp32 norm weight.  eps [H] fp32 standard-normal draws, or NULL (no noise).
+ *   y    out, [M][H] bf16 bits.
+ *   w + sigma*eps and the statistics are formed in fp32.
+ */
+NVFP4RL_API nvfp4rl_status rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
+                           float sigma, float delta, uint16_t* y, void* stream);
+
+/*
+ * nvfp4_lora_linear -- W4A16 linear layer with the LoRA branch fused
+ *   (QeRL explainer, "NVFP4量子化とLoRA": frozen NVFP4 base weights plus
+ *   trainable low-rank factors):
+ *   Y = x deq(W)^T + s (x A^T) B^T,  deq(W)[n][k] = e2m1(code) * E4M3(s_b) * w_g.
+ *   x        [M][K] bf16 bits; K multiple of 256.
+ *   w_codes  [N][K/2], w_scales [N][K/16]: as written by nvfp4_quantize; N multiple of 128.
+ *   w_g      one fp32 (device), the tensor's g.
+ *   lora_A   [r][K] bf16 bits, lora_B [N][r] bf16 bits; r in [0, 256] (0: no LoRA,
+ *            A and B may then be NULL).
+ *   y        out, [M][N] bf16 bits.
+ *   group_offsets, num_groups: must be NULL / 0 (grouped W4A16 is not provided).
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, M, N, K, r, 0).
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_lora_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
+                                 const uint8_t* w_scales, const float* w_g, int64_t N,
+                                 const uint16_t* lora_A, const uint16_t* lora_B, int32_t r, float s,
+                                 const int32_t* group_offsets, int32_t num_groups, uint16_t* y,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * nvfp4_lora_linear_w4a4 -- the W4A4 variant: x is quantized on the fly with
+ *   the nvfp4_quantize recipe (one per-tensor g_x over all M rows), the base
+ *   GEMM runs on FP4 x FP4 with the block scales, and the LoRA branch uses the
+ *   unquantized bf16 x (TRACE summary, "論文が取り組む課題" and "実験結果と性能":
+ *   FP4 weights and activations in the rollout):
+ *   Y = deq(quant(x)) deq(W)^T + s (x A^T) B^T.
+ *   Arguments as nvfp4_lora_linear, plus grouping:
+ *   group_offsets  NULL (dense) or device int32 [num_groups + 1], non-decreasing,
+ *                  offsets[0] == 0, offsets[num_groups] == M: rows
+ *                  [offsets[e], offsets[e+1]) use expert e's weights
+ *                  w_codes + e*N*K/2, w_scales + e*N*K/16, w_g[e].
+ *                  Grouped calls take r == 0 (no LoRA). num_groups in [1, 1024].
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A4, M, N, K, r, num_groups).
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_w4a4(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
+                                      const uint8_t* w_scales, const float* w_g, int64_t N,
+                                      const uint16_t* lora_A, const uint16_t* lora_B, int32_t r, float s,
+                                      const int32_t* group_offsets, int32_t num_groups, uint16_t* y,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes an operation needs for these sizes (0 on invalid sizes). */
+NVFP4RL_API size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r, int32_t num_groups);
+
+/* Static, human-readable name of a status code. */
+NVFP4RL_API const char* nvfp4rl_status_string(nvfp4rl_status status);
+
+/*
+ * nvfp4rl_device_status -- synchronizes the current device and reports the
+ *   library's device-side error word: NVFP4RL_ERR_TIMEOUT if a bounded wait in
+ *   a kernel ran out since the last clear, else NVFP4RL_OK. *word_out (may be
+ *   NULL) receives the raw word; clear != 0 resets it.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t clear);
+
+/*
+ * nvfp4rl_kernel_launches -- diagnostic: number of kernels this library has
+ *   launched in this process (all devices, all streams). Host only.
+ */
+NVFP4RL_API uint64_t nvfp4rl_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4RL_H_ */

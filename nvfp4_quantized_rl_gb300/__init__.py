@@ -1,0 +1,231 @@
+"""Python binding of libnvfp4rl.so, the NVFP4 rollout-linear C ABI (include/nvfp4rl.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels. PyTorch provides device memory (outputs and workspaces are torch
+tensors) and the current CUDA stream. The library must have been built
+(``nvfp4_quantized_rl_gb300._build.build()`` or ``__graft_entry__.build()``);
+importing the binding does not build it, and every call fails loudly when the
+library or a GPU is missing -- there is no CPU fallback.
+
+Functions carry the C names: nvfp4_amax, nvfp4_quantize, nvfp4_quantize_guided, aqn_sigma,
+rmsnorm_aqn, nvfp4_lora_linear, nvfp4_lora_linear_w4a4.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+OK = 0
+BF16, F32 = 0, 1
+OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4 = 0, 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+# Every symbol include/nvfp4rl.h declares, with its C signature.
+_SIGNATURES = None
+
+
+def _signatures():
+    c = ctypes
+    p, i32, i64, f32, f64, sz = c.c_void_p, c.c_int32, c.c_int64, c.c_float, c.c_double, c.c_size_t
+    return {
+        "nvfp4_amax": (c.c_int, [p, i32, i64, p, p]),
+        "nvfp4_quantize": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, sz, p]),
+        "nvfp4_quantize_guided": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
+        "aqn_sigma": (f64, [f64, f64, i64, i64]),
+        "rmsnorm_aqn": (c.c_int, [p, i64, i64, p, p, f32, f32, p, p]),
+        "nvfp4_lora_linear": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
+        "nvfp4_lora_linear_w4a4": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
+        "nvfp4rl_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
+        "nvfp4rl_status_string": (c.c_char_p, [c.c_int]),
+        "nvfp4rl_device_status": (c.c_int, [p, i32]),
+        "nvfp4rl_kernel_launches": (c.c_uint64, []),
+    }
+
+
+class Nvfp4rlError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libnvfp4rl.so is not built ({LIB_PATH}); run nvfp4_quantized_rl_gb300._build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _signatures().items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().nvfp4rl_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise Nvfp4rlError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t, stream=None):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("nvfp4rl works on CUDA tensors only (no CPU path)")
+
+
+def workspace_bytes(op: int, M: int, N: int, K: int, r: int = 0, groups: int = 0) -> int:
+    return int(lib().nvfp4rl_workspace_bytes(op, M, N, K, r, groups))
+
+
+def kernel_launches() -> int:
+    return int(lib().nvfp4rl_kernel_launches())
+
+
+def device_status(clear: bool = True) -> int:
+    word = ctypes.c_uint32(0)
+    st = lib().nvfp4rl_device_status(ctypes.byref(word), 1 if clear else 0)
+    return st, int(word.value)
+
+
+def aqn_sigma(sigma0: float, sigmaK: float, k: int, K: int) -> float:
+    """AQN exponential schedule sigma_k = sigma0 * (sigmaK / sigma0)^(k / K) (host)."""
+    return float(lib().aqn_sigma(float(sigma0), float(sigmaK), int(k), int(K)))
+
+
+def _empty(shape, dtype, device):
+    import torch
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def _bits16(t):
+    """bf16 tensors are passed as their bit patterns; any 2-byte dtype view works."""
+    import torch
+    if t is None:
+        return None
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"expected a bf16 tensor, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t
+
+
+def nvfp4_amax(x, out=None, stream=None):
+    """max |x| of a bf16 or fp32 CUDA tensor (numel multiple of 16) -> fp32 [1]."""
+    import torch
+    _require_cuda(x)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    dt = BF16 if x.dtype == torch.bfloat16 else F32 if x.dtype == torch.float32 else None
+    if dt is None:
+        raise TypeError("x must be bf16 or fp32")
+    out = _empty((1,), torch.float32, x.device) if out is None else out
+    _check(lib().nvfp4_amax(_ptr(x), dt, x.numel(), _ptr(out), _stream(x, stream)), "nvfp4_amax")
+    return out
+
+
+def nvfp4_quantize(x, amax_in=None, codes=None, scales=None, g=None, workspace=None, stream=None):
+    """NVFP4 block quantization of a 2-D bf16 or fp32 CUDA tensor -> (codes u8 [R, C/2], scales u8 [R, C/16], g f32 [1])."""
+    return _quantize(x, None, amax_in, codes, scales, g, workspace, stream)
+
+
+def nvfp4_quantize_guided(x, mask, amax_in=None, codes=None, scales=None, g=None, workspace=None, stream=None):
+    """Guided NVFP4 quantization: mask (int32/uint32 words, bit i%32 of word i//32) picks the rounding direction."""
+    return _quantize(x, mask, amax_in, codes, scales, g, workspace, stream)
+
+
+def _quantize(x, mask, amax_in, codes, scales, g, workspace, stream):
+    import torch
+    _require_cuda(x, mask, amax_in)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    if x.dtype == torch.bfloat16:
+        dt = BF16
+    elif x.dtype == torch.float32:
+        dt = F32
+    else:
+        raise TypeError("x must be bf16 or fp32")
+    rows, cols = x.shape
+    dev = x.device
+    codes = _empty((rows, cols // 2), torch.uint8, dev) if codes is None else codes
+    scales = _empty((rows, cols // 16), torch.uint8, dev) if scales is None else scales
+    g = _empty((1,), torch.float32, dev) if g is None else g
+    if workspace is None and amax_in is None:
+        workspace = _empty((workspace_bytes(OP_QUANTIZE, 0, 0, 0),), torch.uint8, dev)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    L = lib()
+    if mask is None:
+        st = L.nvfp4_quantize(_ptr(x), dt, rows, cols, _ptr(codes), _ptr(scales), _ptr(g), _ptr(amax_in),
+                              _ptr(workspace), wsb, _stream(x, stream))
+        _check(st, "nvfp4_quantize")
+    else:
+        st = L.nvfp4_quantize_guided(_ptr(x), dt, rows, cols, _ptr(mask), _ptr(codes), _ptr(scales), _ptr(g),
+                                     _ptr(amax_in), _ptr(workspace), wsb, _stream(x, stream))
+        _check(st, "nvfp4_quantize_guided")
+    return codes, scales, g
+
+
+def rmsnorm_aqn(x, w, eps=None, sigma: float = 0.0, delta: float = 1e-6, out=None, stream=None):
+    """y = (w + sigma*eps) * x / sqrt(mean(x^2) + delta), bf16 x [M, H] -> bf16 y."""
+    import torch
+    _require_cuda(x, w, eps)
+    _bits16(x)
+    M, H = x.shape
+    out = _empty((M, H), torch.bfloat16, x.device) if out is None else out
+    st = lib().rmsnorm_aqn(_ptr(x), M, H, _ptr(w), _ptr(eps), float(sigma), float(delta), _ptr(out), _stream(x, stream))
+    _check(st, "rmsnorm_aqn")
+    return out
+
+
+def _linear(fn_name, op, x, codes, scales, g, A, B, s, group_offsets, num_groups, out, workspace, stream):
+    import torch
+    _require_cuda(x, codes, scales, g, A, B, group_offsets)
+    _bits16(x), _bits16(A), _bits16(B)
+    M, K = x.shape
+    N = codes.shape[-2]
+    r = 0 if A is None else A.shape[0]
+    G = 0 if group_offsets is None else (num_groups if num_groups else group_offsets.numel() - 1)
+    out = _empty((M, N), torch.bfloat16, x.device) if out is None else out
+    if workspace is None:
+        workspace = _empty((max(workspace_bytes(op, M, N, K, r, G), 16),), torch.uint8, x.device)
+    wsb = workspace.numel() * workspace.element_size()
+    st = getattr(lib(), fn_name)(_ptr(x), M, K, _ptr(codes), _ptr(scales), _ptr(g), N, _ptr(A), _ptr(B), r,
+                                 float(s), _ptr(group_offsets), G, _ptr(out), _ptr(workspace), wsb, _stream(x, stream))
+    _check(st, fn_name)
+    return out
+
+
+def nvfp4_lora_linear(x, codes, scales, g, A=None, B=None, s: float = 1.0, out=None, workspace=None, stream=None):
+    """W4A16: Y = x deq(W)^T + s (x A^T) B^T (bf16 x [M, K]; codes [N, K/2], scales [N, K/16], g [1])."""
+    return _linear("nvfp4_lora_linear", OP_LINEAR_W4A16, x, codes, scales, g, A, B, s, None, 0, out, workspace, stream)
+
+
+def nvfp4_lora_linear_w4a4(x, codes, scales, g, A=None, B=None, s: float = 1.0, group_offsets=None,
+                           num_groups: int = 0, out=None, workspace=None, stream=None):
+    """W4A4: x quantized on the fly (per-tensor g_x); grouped when group_offsets (int32 [G+1]) is given,
+    with codes [G, N, K/2], scales [G, N, K/16], g [G]."""
+    return _linear("nvfp4_lora_linear_w4a4", OP_LINEAR_W4A4, x, codes, scales, g, A, B, s, group_offsets,
+                   num_groups, out, workspace, stream)

@@ -1,0 +1,233 @@
+// C ABI of the NVFP4 rollout-linear library: argument validation and dispatch.
+// Every check runs on the host before any launch; see include/nvfp4rl.h for the contract.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace nvfp4rl {
+
+// Device-side error word (bounded waits set bits here instead of hanging).
+__device__ uint32_t g_device_status;
+
+namespace {
+std::mutex g_dev_mutex;
+DeviceInfo g_dev_cache[64];
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+nvfp4rl_status current_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return NVFP4RL_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev_cache[dev];
+  if (d.device != dev) {
+    DeviceInfo n;
+    n.device = dev;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return NVFP4RL_ERR_CUDA;
+    n.smem_optin = static_cast<size_t>(v);
+    d = n;
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3) return NVFP4RL_ERR_DEVICE;
+  *out = d;
+  return NVFP4RL_OK;
+}
+
+int64_t rmsnorm_max_h();
+
+}  // namespace nvfp4rl
+
+using namespace nvfp4rl;
+
+namespace {
+
+nvfp4rl_status quantize_common(const void* x, int32_t dtype, int64_t rows, int64_t cols, const uint32_t* mask,
+                               bool guided, uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
+                               void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !codes || !scales || !g || (guided && !mask)) return NVFP4RL_ERR_INVALID_ARG;
+  if (dtype != NVFP4RL_BF16 && dtype != NVFP4RL_F32) return NVFP4RL_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0) return NVFP4RL_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (mask && !aligned16(mask)) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u) || (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)))
+    return NVFP4RL_ERR_MISALIGNED;
+  if (!amax_in) {
+    if (!ws || ws_bytes < kQuantizeWorkspace) return NVFP4RL_ERR_WORKSPACE;
+    if (!aligned16(ws)) return NVFP4RL_ERR_MISALIGNED;
+  }
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
+  const size_t xbytes = n * (dtype == NVFP4RL_BF16 ? 2 : 4);
+  const size_t mbytes = guided ? (n + 31) / 32 * 4 : 0;
+  const void* outs[3] = {codes, scales, g};
+  const size_t osz[3] = {n / 2, n / 16, 4};
+  for (int i = 0; i < 3; ++i) {
+    if (overlap(outs[i], osz[i], x, xbytes) || (guided && overlap(outs[i], osz[i], mask, mbytes)) ||
+        (amax_in && overlap(outs[i], osz[i], amax_in, 4)) || (!amax_in && overlap(outs[i], osz[i], ws, kQuantizeWorkspace)))
+      return NVFP4RL_ERR_ALIAS;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], osz[i], outs[j], osz[j])) return NVFP4RL_ERR_ALIAS;
+  }
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_quantize(x, dtype, rows, cols, guided ? mask : nullptr, codes, scales, g, amax_in,
+                         static_cast<uint32_t*>(ws), dev, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
+                             const uint8_t* w_scales, const float* w_g, int64_t N, const uint16_t* A,
+                             const uint16_t* B, int32_t r, float s, const int32_t* offsets, int32_t groups,
+                             uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !w_codes || !w_scales || !w_g || !y) return NVFP4RL_ERR_INVALID_ARG;
+  if (M < 0 || K <= 0 || N <= 0 || r < 0 || r > 256) return NVFP4RL_ERR_INVALID_ARG;
+  if (r > 0 && (!A || !B)) return NVFP4RL_ERR_INVALID_ARG;
+  if (!std::isfinite(s)) return NVFP4RL_ERR_INVALID_ARG;
+  if (offsets) {
+    if (!w4a4) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+    if (groups < 1 || groups > 1024 || r != 0) return NVFP4RL_ERR_INVALID_ARG;
+  } else if (groups != 0 && groups != 1) {
+    return NVFP4RL_ERR_INVALID_ARG;
+  }
+  if (K % 256 != 0 || N % 128 != 0 || M > 65535) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  const void* arrays[] = {x, w_codes, w_scales, A, B, offsets, y, ws};
+  for (const void* p : arrays)
+    if (p && !aligned16(p)) return NVFP4RL_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(w_g) & 3u) return NVFP4RL_ERR_MISALIGNED;
+  const int G = offsets ? groups : 1;
+  const size_t need = linear_workspace_bytes(w4a4, M, N, K, r, G);
+  if (M > 0 && (!ws || ws_bytes < need)) return NVFP4RL_ERR_WORKSPACE;
+  const size_t ybytes = static_cast<size_t>(M) * N * 2;
+  const void* ins[] = {x, w_codes, w_scales, w_g, A, B, offsets, ws};
+  const size_t isz[] = {static_cast<size_t>(M) * K * 2, static_cast<size_t>(G) * N * K / 2,
+                        static_cast<size_t>(G) * N * K / 16, static_cast<size_t>(G) * 4,
+                        A ? static_cast<size_t>(r) * K * 2 : 0, B ? static_cast<size_t>(N) * r * 2 : 0,
+                        offsets ? static_cast<size_t>(groups + 1) * 4 : 0, ws ? need : 0};
+  for (int i = 0; i < 8; ++i)
+    if (ins[i] && overlap(y, ybytes, ins[i], isz[i])) return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  LinearArgs a{x, M, K, N, w_codes, w_scales, w_g, A, B, r, s, offsets, G, y, w4a4};
+  return launch_linear(a, ws, ws_bytes, dev, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+nvfp4rl_status nvfp4_amax(const void* x, int32_t dtype, int64_t n, float* amax, void* stream) {
+  if (!x || !amax) return NVFP4RL_ERR_INVALID_ARG;
+  if (dtype != NVFP4RL_BF16 && dtype != NVFP4RL_F32) return NVFP4RL_ERR_INVALID_ARG;
+  if (n < 0) return NVFP4RL_ERR_INVALID_ARG;
+  if (n % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(amax) & 3u)) return NVFP4RL_ERR_MISALIGNED;
+  if (overlap(amax, 4, x, static_cast<size_t>(n) * (dtype == NVFP4RL_BF16 ? 2 : 4))) return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_amax(x, dtype, n, reinterpret_cast<uint32_t*>(amax), dev, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4rl_status nvfp4_quantize(const void* x, int32_t dtype, int64_t rows, int64_t cols, uint8_t* codes,
+                              uint8_t* scales, float* g, const float* amax_in, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return quantize_common(x, dtype, rows, cols, nullptr, false, codes, scales, g, amax_in, workspace,
+                         workspace_bytes, stream);
+}
+
+nvfp4rl_status nvfp4_quantize_guided(const void* x, int32_t dtype, int64_t rows, int64_t cols,
+                                     const uint32_t* mask, uint8_t* codes, uint8_t* scales, float* g,
+                                     const float* amax_in, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return quantize_common(x, dtype, rows, cols, mask, true, codes, scales, g, amax_in, workspace, workspace_bytes,
+                         stream);
+}
+
+double aqn_sigma(double sigma0, double sigmaK, int64_t k, int64_t K) {
+  if (K <= 0 || !(sigma0 > 0.0) || !(sigmaK > 0.0)) return NAN;
+  return sigma0 * std::pow(sigmaK / sigma0, static_cast<double>(k) / static_cast<double>(K));
+}
+
+nvfp4rl_status rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps, float sigma,
+                           float delta, uint16_t* y, void* stream) {
+  if (!x || !w || !y) return NVFP4RL_ERR_INVALID_ARG;
+  if (M < 0 || H <= 0 || !std::isfinite(sigma) || !(delta >= 0.0f) || !std::isfinite(delta))
+    return NVFP4RL_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > rmsnorm_max_h() || M > 2147483647LL) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (eps && !aligned16(eps))) return NVFP4RL_ERR_MISALIGNED;
+  const size_t yb = static_cast<size_t>(M) * H * 2;
+  if (overlap(y, yb, x, yb) || overlap(y, yb, w, H * 4) || (eps && overlap(y, yb, eps, H * 4)))
+    return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_rmsnorm_aqn(x, M, H, w, eps, sigma, delta, y, dev, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4rl_status nvfp4_lora_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
+                                 const uint8_t* w_scales, const float* w_g, int64_t N, const uint16_t* lora_A,
+                                 const uint16_t* lora_B, int32_t r, float s, const int32_t* group_offsets,
+                                 int32_t num_groups, uint16_t* y, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  return linear_common(false, x, M, K, w_codes, w_scales, w_g, N, lora_A, lora_B, r, s, group_offsets, num_groups,
+                       y, workspace, workspace_bytes, stream);
+}
+
+nvfp4rl_status nvfp4_lora_linear_w4a4(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
+                                      const uint8_t* w_scales, const float* w_g, int64_t N,
+                                      const uint16_t* lora_A, const uint16_t* lora_B, int32_t r, float s,
+                                      const int32_t* group_offsets, int32_t num_groups, uint16_t* y,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return linear_common(true, x, M, K, w_codes, w_scales, w_g, N, lora_A, lora_B, r, s, group_offsets, num_groups,
+                       y, workspace, workspace_bytes, stream);
+}
+
+size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r, int32_t num_groups) {
+  if (M < 0 || N < 0 || K < 0 || r < 0 || r > 256 || num_groups < 0 || num_groups > 1024) return 0;
+  switch (op) {
+    case NVFP4RL_OP_QUANTIZE: return kQuantizeWorkspace;
+    case NVFP4RL_OP_LINEAR_W4A16: return linear_workspace_bytes(false, M, N, K, r, 1);
+    case NVFP4RL_OP_LINEAR_W4A4: return linear_workspace_bytes(true, M, N, K, r, num_groups > 0 ? num_groups : 1);
+    default: return 0;
+  }
+}
+
+const char* nvfp4rl_status_string(nvfp4rl_status status) {
+  switch (status) {
+    case NVFP4RL_OK: return "ok";
+    case NVFP4RL_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4RL_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case NVFP4RL_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case NVFP4RL_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4RL_ERR_CUDA: return "CUDA error";
+    case NVFP4RL_ERR_TIMEOUT: return "device-side wait timed out";
+    case NVFP4RL_ERR_ALIAS: return "output overlaps an input";
+    case NVFP4RL_ERR_DEVICE: return "device is not compute capability 10.3";
+  }
+  return "unknown status";
+}
+
+uint64_t nvfp4rl_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_device_status, sizeof(w)) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  if (word_out) *word_out = w;
+  if (clear) {
+    const uint32_t z = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &z, sizeof(z)) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  }
+  return w ? NVFP4RL_ERR_TIMEOUT : NVFP4RL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// Shared device helpers of the NVFP4 rollout-linear library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4rl.h"
+
+namespace nvfp4rl {
+
+constexpr int kNumSMsHint = 152;  // GB300: 2 dies x 76 SMs; the real count is queried at run time
+
+// ---- bf16 / fp32 bit helpers ------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t bf16_lo_bits(uint32_t pair) { return pair << 16; }
+__device__ __forceinline__ uint32_t bf16_hi_bits(uint32_t pair) { return pair & 0xFFFF0000u; }
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs)
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+// E4M3 (OCP FP8 E4M3FN) value of a non-negative byte 0x00..0x7E, built from its bits.
+__device__ __forceinline__ float e4m3_decode_pos(uint32_t b) {
+  const uint32_t e = b >> 3, m = b & 7u;
+  // normal: (1 + m/8) 2^(e-7) -> fp32 exponent field e + 120, mantissa m << 20
+  const float normal = __uint_as_float(((e + 120u) << 23) | (m << 20));
+  const float sub = static_cast<float>(m) * 0.001953125f;  // m * 2^-9
+  return e ? normal : sub;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  size_t smem_optin = 0;
+};
+
+// Cached attributes of the current device; NVFP4RL_ERR_DEVICE unless compute capability 10.3.
+nvfp4rl_status current_device(DeviceInfo* out);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na && nb && x < y + nb && y < x + na;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Counts one kernel launch (diagnostic, see nvfp4rl_kernel_launches) and reports its status.
+void count_launch();
+inline nvfp4rl_status launch_status() {
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? NVFP4RL_OK : NVFP4RL_ERR_CUDA;
+}
+
+// ---- internal launchers (quantize.cu, rmsnorm.cu, linear.cu) -------------------------------
+
+// Quantization scratch: one 32-bit word holding the running amax bits.
+constexpr size_t kQuantizeWorkspace = 256;
+
+nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
+                           cudaStream_t st);
+
+nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
+                               uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
+                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st);
+
+nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
+                                  float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st);
+
+struct LinearArgs {
+  const uint16_t* x;
+  int64_t M, K, N;
+  const uint8_t* w_codes;
+  const uint8_t* w_scales;
+  const float* w_g;
+  const uint16_t* A;
+  const uint16_t* B;
+  int r;
+  float s;
+  const int32_t* offsets;
+  int groups;
+  uint16_t* y;
+  bool w4a4;
+};
+
+size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups);
+nvfp4rl_status launch_linear(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st);
+
+}  // namespace nvfp4rl

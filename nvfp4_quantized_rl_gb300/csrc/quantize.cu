@@ -1,0 +1,253 @@
+// NVFP4 block quantization, plain and rollout-guided (sm_103a).
+//
+// Format: QeRL explainer, section "NVFP4量子化とLoRA" (4-bit weights with hardware
+// support); TRACE summary, section "仕組みの工学的な理解" (a few values share one
+// scale, each value is 4 bits; the rounding direction is a per-value choice between
+// the two neighbouring grid points). Recipe: g = fl32(amax / 2688); the 16-element
+// block scale is the E4M3 byte nearest to bamax / (6 g); each element's code is the
+// E2M1 grid index nearest to |x| / (E4M3(s) g) with its sign in bit 3; both roundings
+// apply to the exact real quotient, ties to the even encoding, saturating.
+//
+// Kernels:
+//   amax_kernel      one HBM read of x, 128-bit non-caching loads, packed 16-bit max
+//                    for bf16, warp/CTA reduction, one atomicMax per CTA.
+//   quantize_kernel  one thread per 16-element block: two (bf16) or four (fp32)
+//                    128-bit loads, the exact E4M3 scale byte, seven per-block
+//                    thresholds, and per element seven unsigned compares.
+//
+// Exactness without division per element: for an fp32 value a and a real P,
+//   a > P  <=>  a > RD(P)      a >= P  <=>  a >= RU(P)
+// where RD/RU are P rounded down/up to fp32. Every P used here is T * dec(s) * g
+// with T * dec(s) exact in fp32 (at most 7 significant bits), so RD/RU are single
+// directed-rounding multiplies (__fmul_rd / __fmul_ru). Non-negative fp32 values
+// order like their bit patterns, so the compares run on integers.
+#include "common.cuh"
+
+namespace nvfp4rl {
+namespace {
+
+// Approximate E4M3 byte of v (round to nearest, saturating): a starting point that is
+// within one byte of the exact answer; the caller corrects it exactly.
+__device__ __forceinline__ uint32_t e4m3_estimate(float v) {
+  uint16_t pair;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(pair) : "f"(v));
+  return pair & 0x7Fu;
+}
+
+// Exact E4M3 byte nearest to bamax / (6 g), ties to the even byte, saturating at 0x7E.
+// g > 0. `est` is a fp32 approximation of the quotient.
+__device__ __forceinline__ uint32_t scale_byte(float bamax, float g, float est) {
+  uint32_t b = e4m3_estimate(est);
+  uint32_t dec = 0, inc = 0;
+  if (b > 0) {
+    // 6 * midpoint(b-1, b) = 3 * (E4M3(b-1) + E4M3(b)), exact in fp32
+    const float t = 3.0f * (e4m3_decode_pos(b - 1) + e4m3_decode_pos(b));
+    const float ru = __fmul_ru(t, g), rd = __fmul_rd(t, g);
+    if (bamax < ru) dec = 1;
+    else if (rd == ru && bamax == ru && (b & 1u)) dec = 1;  // exact tie: to the even byte b-1
+  }
+  if (b < 0x7Eu) {
+    const float t = 3.0f * (e4m3_decode_pos(b) + e4m3_decode_pos(b + 1));
+    const float ru = __fmul_ru(t, g), rd = __fmul_rd(t, g);
+    if (bamax > rd) inc = 1;
+    else if (rd == ru && bamax == rd && (b & 1u)) inc = 1;  // exact tie: to the even byte b+1
+  }
+  return b - dec + inc;
+}
+
+// Strict-compare thresholds (fp32 bit patterns) of the seven E2M1 midpoints for the real
+// scale S = dec * g: |x| bits > th[i] exactly when |x| rounds above midpoint i.
+// Midpoints 0.25, 1.25, 2.5 and 5 round down on a tie (to the even code below),
+// 0.75, 1.75 and 3.5 round up on a tie (to the even code above).
+__device__ __forceinline__ void plain_thresholds(float dec, float g, uint32_t th[7]) {
+  th[0] = __float_as_uint(__fmul_rd(0.25f * dec, g));
+  th[1] = __float_as_uint(__fmul_ru(0.75f * dec, g)) - 1u;
+  th[2] = __float_as_uint(__fmul_rd(1.25f * dec, g));
+  th[3] = __float_as_uint(__fmul_ru(1.75f * dec, g)) - 1u;
+  th[4] = __float_as_uint(__fmul_rd(2.5f * dec, g));
+  th[5] = __float_as_uint(__fmul_ru(3.5f * dec, g)) - 1u;
+  th[6] = __float_as_uint(__fmul_rd(5.0f * dec, g));
+}
+
+// Guided thresholds at the grid points 0.5 .. 6 (k = 1..7):
+//   ge[k-1]: |x| bits > ge  <=>  |x| >= grid[k] S      gt[k-1]: |x| bits > gt  <=>  |x| > grid[k] S
+__device__ __forceinline__ void guided_thresholds(float dec, float g, uint32_t ge[7], uint32_t gt[7]) {
+  const float grid[7] = {0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    ge[k] = __float_as_uint(__fmul_ru(grid[k] * dec, g)) - 1u;
+    gt[k] = __float_as_uint(__fmul_rd(grid[k] * dec, g));
+  }
+}
+
+template <int kDtype>
+__global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, int64_t nvec,
+                                                   uint32_t* __restrict__ amax_bits) {
+  uint32_t m = 0;
+  const uint4* p = static_cast<const uint4*>(x);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  if (kDtype == NVFP4RL_BF16) {
+    uint32_t m2 = 0;  // two running 16-bit maxima of |bf16| bit patterns
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+      const uint4 v = ld_nc_v4(p + i);
+      m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+    }
+    m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+  } else {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+      const uint4 v = ld_nc_v4(p + i);
+      m = max(m, max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu)));
+    }
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (threadIdx.x == 0) atomicMax(amax_bits, m);
+  }
+}
+
+template <int kDtype, bool kGuided>
+__global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ x, int64_t nblocks,
+                                                       const uint32_t* __restrict__ amax_bits,
+                                                       const float* __restrict__ amax_in,
+                                                       const uint32_t* __restrict__ mask,
+                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                       float* __restrict__ g_out) {
+  const float amax = amax_in ? *amax_in : __uint_as_float(*amax_bits);
+  const float g = __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  // The estimate of bamax / (6 g) is taken on operands scaled by 2^64 when g is tiny,
+  // so that 6 g keeps full precision; the exact correction uses the unscaled values.
+  const bool tiny = g < 0x1p-60f;
+  const float est_scale = tiny ? 0x1p64f : 1.0f;
+  const float g6 = 6.0f * (g * est_scale);
+
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < nblocks; blk += stride) {
+    uint32_t ax[16];
+    uint32_t sgn = 0;
+    if (kDtype == NVFP4RL_BF16) {
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + blk * 16);
+      const uint4 v0 = ld_nc_v4(p), v1 = ld_nc_v4(p + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = w[i] << 16, hi = w[i] & 0xFFFF0000u;
+        ax[2 * i] = lo & 0x7FFFFFFFu;
+        ax[2 * i + 1] = hi & 0x7FFFFFFFu;
+        sgn |= ((lo >> 31) << (2 * i)) | ((hi >> 31) << (2 * i + 1));
+      }
+    } else {
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(x) + blk * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = ld_nc_v4(p + q);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ax[4 * q + i] = w[i] & 0x7FFFFFFFu;
+          sgn |= (w[i] >> 31) << (4 * q + i);
+        }
+      }
+    }
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx = max(mx, ax[i]);
+    const float bamax = __uint_as_float(mx);
+
+    uint32_t b = 0;
+    if (g > 0.0f) b = scale_byte(bamax, g, __fdiv_rn(bamax * est_scale, g6));
+    const float dec = e4m3_decode_pos(b);
+
+    uint32_t lo32 = 0, hi32 = 0;
+    if (!kGuided) {
+      uint32_t th[7];
+      plain_thresholds(dec, g, th);
+      if (b == 0) {
+#pragma unroll
+        for (int k = 0; k < 7; ++k) th[k] = 0x7F800000u;  // zero scale: every code is sign|0
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint32_t mag = 0;
+#pragma unroll
+        for (int k = 0; k < 7; ++k) mag += ax[i] > th[k] ? 1u : 0u;
+        const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
+        if (i < 8) lo32 |= code << (4 * i);
+        else hi32 |= code << (4 * (i - 8));
+      }
+    } else {
+      uint32_t ge[7], gt[7];
+      guided_thresholds(dec, g, ge, gt);
+      const uint32_t up_bits = (mask[blk >> 1] >> ((blk & 1) * 16)) & (b ? 0xFFFFu : 0u);
+      if (b == 0) {
+#pragma unroll
+        for (int k = 0; k < 7; ++k) ge[k] = gt[k] = 0x7F800000u;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint32_t c_ge = 0, c_gt = 0;
+#pragma unroll
+        for (int k = 0; k < 7; ++k) {
+          c_ge += ax[i] > ge[k] ? 1u : 0u;
+          c_gt += ax[i] > gt[k] ? 1u : 0u;
+        }
+        const bool on_grid = (c_ge != c_gt) || ax[i] == 0u;
+        const uint32_t up = (up_bits >> i) & 1u;
+        const uint32_t mag = (c_ge == 7u) ? 7u : c_ge + ((up && !on_grid) ? 1u : 0u);
+        const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
+        if (i < 8) lo32 |= code << (4 * i);
+        else hi32 |= code << (4 * (i - 8));
+      }
+    }
+    *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo32, hi32);
+    scales[blk] = static_cast<uint8_t>(b);
+  }
+}
+
+}  // namespace
+
+nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
+                           cudaStream_t st) {
+  if (cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), st) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  if (n == 0) return NVFP4RL_OK;
+  const int threads = 256;
+  const int64_t nvec = n * (dtype == NVFP4RL_BF16 ? 2 : 4) / 16;
+  const int64_t want = (nvec + threads - 1) / threads;
+  const int grid = static_cast<int>(want < dev.sm_count * 4 ? want : dev.sm_count * 4);
+  if (dtype == NVFP4RL_BF16) amax_kernel<NVFP4RL_BF16><<<grid, threads, 0, st>>>(x, nvec, amax_bits);
+  else amax_kernel<NVFP4RL_F32><<<grid, threads, 0, st>>>(x, nvec, amax_bits);
+  return launch_status();
+}
+
+nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
+                               uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
+                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st) {
+  const int64_t n = rows * cols;
+  const int64_t nblocks = n / 16;
+  if (nblocks == 0) return NVFP4RL_OK;
+  const int threads = 256;
+  if (amax_in == nullptr) {
+    const nvfp4rl_status sa = launch_amax(x, dtype, n, amax_scratch, dev, st);
+    if (sa != NVFP4RL_OK) return sa;
+  }
+  const int64_t want = (nblocks + threads - 1) / threads;
+  const int grid = static_cast<int>(want < dev.sm_count * 8 ? want : dev.sm_count * 8);
+  if (dtype == NVFP4RL_BF16) {
+    if (mask) quantize_kernel<NVFP4RL_BF16, true><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
+    else quantize_kernel<NVFP4RL_BF16, false><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
+  } else {
+    if (mask) quantize_kernel<NVFP4RL_F32, true><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
+    else quantize_kernel<NVFP4RL_F32, false><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
+  }
+  return launch_status();
+}
+
+}  // namespace nvfp4rl

@@ -1,0 +1,118 @@
+"""The C-ABI library builds, loads and exports every symbol include/nvfp4rl.h declares;
+host-side validation rejects bad arguments before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4rl.h")
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_quantized_rl_gb300 import _build
+    _build.build()
+    import nvfp4_quantized_rl_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"NVFP4RL_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "rmsnorm_aqn", "nvfp4_lora_linear",
+                     "nvfp4_lora_linear_w4a4", "aqn_sigma"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(nv):
+    L = ctypes.CDLL(nv.LIB_PATH)
+    names = declared_functions()
+    assert names
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in the header but not exported"
+    # and the binding declares a ctypes signature for each of them
+    assert set(names) == set(nv._signatures())
+
+
+def test_aqn_sigma_matches_the_oracle(nv):
+    for k in range(11):
+        assert nv.aqn_sigma(1e-2, 5e-4, k, 10) == pytest.approx(oracle.aqn_sigma(1e-2, 5e-4, k, 10), rel=1e-15)
+    assert np.isnan(nv.aqn_sigma(1e-2, 5e-4, 0, 0))
+
+
+def test_status_strings(nv):
+    for s in range(9):
+        assert nv.status_string(s) and nv.status_string(s) != "unknown status"
+
+
+def test_workspace_bytes(nv):
+    assert nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0) >= 4
+    w16 = nv.workspace_bytes(nv.OP_LINEAR_W4A16, 64, 3584, 3584, 32)
+    w4 = nv.workspace_bytes(nv.OP_LINEAR_W4A4, 64, 3584, 3584, 32)
+    assert w16 >= 64 * 3584 * 4 and w4 > w16
+    assert nv.workspace_bytes(7, 1, 1, 1) == 0 and nv.workspace_bytes(nv.OP_LINEAR_W4A16, -1, 1, 1) == 0
+
+
+# Fake, never-dereferenced addresses: validation fails before any device access.
+A0, A1, A2, A3, A4 = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+
+
+def _q(nv, x=A0, dtype=0, rows=4, cols=32, codes=A1, scales=A2, g=A3, amax=None, ws=A4, wsb=256):
+    return nv.lib().nvfp4_quantize(x, dtype, rows, cols, codes, scales, g, amax, ws, wsb, None)
+
+
+def test_quantize_validation(nv):
+    assert _q(nv, x=None) == 1                 # null input
+    assert _q(nv, dtype=3) == 1                # bad dtype
+    assert _q(nv, rows=-1) == 1
+    assert _q(nv, cols=24) == 3                # not a multiple of 16
+    assert _q(nv, x=A0 + 8) == 2               # misaligned
+    assert _q(nv, codes=A0) == 7               # output overlaps input
+    assert _q(nv, ws=None) == 4                # no workspace and no amax_in
+    assert _q(nv, wsb=8) == 4                  # workspace too small
+    g = nv.lib().nvfp4_quantize_guided(A0, 0, 4, 32, None, A1, A2, A3, None, A4, 256, None)
+    assert g == 1                              # guided without a mask
+
+
+def _lin(nv, fn="nvfp4_lora_linear", x=A0, M=8, K=512, codes=A1, scales=A2, g=A3, N=256, A=None, B=None, r=0,
+         s=2.0, off=None, G=0, y=A4, ws=0x60000, wsb=1 << 30):
+    return getattr(nv.lib(), fn)(x, M, K, codes, scales, g, N, A, B, r, s, off, G, y, ws, wsb, None)
+
+
+def test_linear_validation(nv):
+    assert _lin(nv, x=None) == 1
+    assert _lin(nv, r=16) == 1                 # r > 0 without A, B
+    assert _lin(nv, r=300, A=0x70000, B=0x80000) == 1
+    assert _lin(nv, K=500) == 3                # K not a multiple of 256
+    assert _lin(nv, N=200) == 3                # N not a multiple of 128
+    assert _lin(nv, x=A0 + 4) == 2
+    assert _lin(nv, y=A0) == 7                 # y overlaps x
+    assert _lin(nv, wsb=16) == 4
+    assert _lin(nv, off=0x90000, G=4) == 3     # grouped W4A16 is not provided
+    assert _lin(nv, fn="nvfp4_lora_linear_w4a4", off=0x90000, G=0) == 1
+    assert _lin(nv, fn="nvfp4_lora_linear_w4a4", off=0x90000, G=4, r=16, A=0x70000, B=0x80000) == 1
+    assert _lin(nv, s=float("nan")) == 1
+
+
+def test_rmsnorm_validation(nv):
+    L = nv.lib()
+    assert L.rmsnorm_aqn(None, 4, 64, A1, None, 0.0, 1e-6, A2, None) == 1
+    assert L.rmsnorm_aqn(A0, 4, 60, A1, None, 0.0, 1e-6, A2, None) == 3
+    assert L.rmsnorm_aqn(A0, 4, 64, A1, None, 0.0, -1.0, A2, None) == 1
+    assert L.rmsnorm_aqn(A0, 4, 64, A1 + 4, None, 0.0, 1e-6, A2, None) == 2
+    assert L.rmsnorm_aqn(A0, 4, 64, A1, None, 0.0, 1e-6, A0, None) == 7
+
+
+def test_binding_refuses_cpu_tensors(nv):
+    import torch
+    with pytest.raises(ValueError):
+        nv.nvfp4_quantize(torch.zeros(4, 32))

@@ -1,0 +1,325 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Quantization (codes, scale bytes, g) is compared bit for bit; RMSNorm and the
+GEMMs within the tolerances of tests/_parity.py. Inputs come from synth; every
+expected value comes from the oracle. Sizes span several tiles with ragged
+tails, plus the full workload shapes (the 7B decode layer the benchmark times,
+checked on every output; the larger ones on sampled rows).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_quantized_rl_gb300 import _build
+    _build.build()
+    import nvfp4_quantized_rl_gb300 as m
+    assert torch.cuda.is_available(), "GPU parity tests need a CUDA device"
+    return m
+
+
+def gpu_quantize(nv, x_np, mask=None, amax_in=None):
+    x = P.dev_bf16(x_np) if x_np.dtype == np.uint16 else P.dev(x_np)
+    m = None if mask is None else P.dev(mask.view(np.int32))
+    a = None if amax_in is None else torch.tensor([amax_in], dtype=torch.float32, device="cuda")
+    fn = nv.nvfp4_quantize if mask is None else (lambda t, **k: nv.nvfp4_quantize_guided(t, m, **k))
+    c, s, g = fn(x, amax_in=a)
+    torch.cuda.synchronize()
+    return c.cpu().numpy(), s.cpu().numpy(), np.float32(g.cpu().numpy()[0])
+
+
+def assert_quant_equal(got, want, what=""):
+    (c1, s1, g1), (c2, s2, g2) = got, want
+    assert np.float32(g1).view(np.uint32) == np.float32(g2).view(np.uint32), f"{what}: g {g1!r} vs {g2!r}"
+    assert np.array_equal(s1, s2), f"{what}: {int((s1 != s2).sum())} scale bytes differ"
+    assert np.array_equal(c1, c2), f"{what}: {int((c1 != c2).sum())} code bytes differ"
+
+
+# ---------------------------------------------------------------- quantization
+
+def test_quantize_tiny_fp32(nv):
+    W = synth.tiny_config(0)["W"]
+    assert_quant_equal(gpu_quantize(nv, W), oracle.quantize(W), "tiny fp32 256x512")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(1, 16), (37, 48), (300, 1040), (129, 4096)])
+def test_quantize_ragged(nv, dtype, shape):
+    W = synth.weight_f32(*shape, 0.02, 1, shape[0], outlier_frac=0.02)
+    x = synth.bf16_bits(W) if dtype == "bf16" else W
+    assert_quant_equal(gpu_quantize(nv, x), oracle.quantize(x), f"{dtype} {shape}")
+
+
+def _edge_tensor():
+    """Exact grid values, every E2M1 midpoint, +-0, zero blocks, tiny blocks (subnormal scale bytes)."""
+    rng = np.random.default_rng(5)
+    rows, cols = 64, 256
+    g = np.float32(2.0 ** -6)
+    x = np.zeros((rows, cols), np.float32)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    for r in range(rows):
+        for b in range(cols // 16):
+            s = np.float32(2.0 ** rng.integers(-9, 8))  # power-of-two block scales, some subnormal in E4M3
+            vals = np.concatenate([mids, grid[1:], [0.0, 0.0]]) if (r + b) % 3 else rng.uniform(-7, 7, 16)
+            vals = (vals * s * g).astype(np.float32) * np.where(rng.random(16) < 0.5, -1, 1).astype(np.float32)
+            vals[0] = np.float32(6 * s * g)  # the block amax makes the scale byte exactly s
+            x[r, 16 * b:16 * b + 16] = vals
+    x[3] = 0.0
+    x[4, :16] = -0.0
+    x[0, 0] = np.float32(6 * 448 * g)  # tensor amax -> g exactly
+    return x
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_quantize_edge_values(nv, dtype):
+    x = _edge_tensor()
+    x = synth.bf16_bits(x) if dtype == "bf16" else x
+    want = oracle.quantize(x)
+    assert_quant_equal(gpu_quantize(nv, x), want, "edge values")
+    # saturation: a caller amax below the true one drives scale bytes to 0x7E and codes to 6
+    a = float(np.float32(np.abs(synth.bf16_to_f32(x) if dtype == "bf16" else x).max()) / 5)
+    assert_quant_equal(gpu_quantize(nv, x, amax_in=a), oracle.quantize(x, amax_in=a), "amax_in saturation")
+
+
+def test_quantize_zero_tiny_and_huge(nv):
+    z = np.zeros((8, 64), np.float32)
+    z[2, 5] = -0.0
+    assert_quant_equal(gpu_quantize(nv, z), oracle.quantize(z), "all zero")
+    one = np.zeros((8, 64), np.float32)
+    one[7, 63] = -3.0
+    assert_quant_equal(gpu_quantize(nv, one), oracle.quantize(one), "single nonzero")
+    tiny = (synth.weight_f32(16, 64, 1.0, 3, 1) * np.float32(1e-36)).astype(np.float32)  # g is subnormal
+    assert_quant_equal(gpu_quantize(nv, tiny), oracle.quantize(tiny), "tiny g")
+    huge = (synth.weight_f32(16, 64, 1.0, 3, 2) * np.float32(1e37)).astype(np.float32)
+    assert_quant_equal(gpu_quantize(nv, huge), oracle.quantize(huge), "huge values")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_quantize_guided(nv, dtype):
+    W = synth.weight_f32(200, 768, 0.02, 4, 1, outlier_frac=0.01)
+    x = synth.bf16_bits(W) if dtype == "bf16" else W
+    mask = synth.guided_mask(W.size, 4, 2)
+    assert_quant_equal(gpu_quantize(nv, x, mask=mask), oracle.quantize(x, mask=mask), "guided")
+    e = _edge_tensor()
+    e = synth.bf16_bits(e) if dtype == "bf16" else e
+    m2 = synth.guided_mask(e.size, 4, 3)
+    assert_quant_equal(gpu_quantize(nv, e, mask=m2), oracle.quantize(e, mask=m2), "guided edge values")
+
+
+def test_quantize_empty_is_a_noop(nv):
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    c, s, g = nv.nvfp4_quantize(x)
+    torch.cuda.synchronize()
+    assert c.shape == (0, 32) and s.shape == (0, 4)
+
+
+def test_quantize_qwen7b_layer_full(nv):
+    """All five weights of a Qwen2.5-7B-shaped layer (bf16, 1% outlier columns x8), every output byte."""
+    for i, (name, (n, k)) in enumerate(synth.QWEN25_7B["linears"].items()):
+        W = synth.weight_bf16(n, k, 0.02, 2, i, outlier_frac=0.01)
+        assert_quant_equal(gpu_quantize(nv, W), oracle.quantize(W), f"7B {name}")
+
+
+def test_quantize_moe_experts_guided(nv):
+    """MoE expert weights (768x2048 gate/up, 2048x768 down); guided with a Bernoulli(1/2) mask, as for the
+    deepest layers, and plain, on a seeded set of experts."""
+    rng = np.random.default_rng(6)
+    for e in rng.choice(128, 6, replace=False):
+        for j, (n, k) in enumerate([(768, 2048), (768, 2048), (2048, 768)]):
+            W = synth.weight_bf16(n, k, 0.02, 47, int(e), j)
+            mask = synth.guided_mask(W.size, 47, int(e), j, 99)
+            assert_quant_equal(gpu_quantize(nv, W, mask=mask), oracle.quantize(W, mask=mask), f"expert {e}.{j} guided")
+            assert_quant_equal(gpu_quantize(nv, W), oracle.quantize(W), f"expert {e}.{j} plain")
+
+
+# ---------------------------------------------------------------- RMSNorm with AQN
+
+def gpu_rmsnorm(nv, x, w, eps, sigma, delta):
+    y = nv.rmsnorm_aqn(P.dev_bf16(x), P.dev(w), None if eps is None else P.dev(eps), sigma, delta)
+    torch.cuda.synchronize()
+    return P.host_bits(y)
+
+
+def test_rmsnorm_tiny(nv):
+    c = synth.tiny_config(0)
+    s = np.float32(c["sigma"])
+    y = gpu_rmsnorm(nv, c["x"], c["w"], c["eps"], s, c["delta"])
+    P.assert_rmsnorm_close(y, oracle.rmsnorm_aqn(c["x"], c["w"], c["eps"], s, c["delta"]), "tiny")
+
+
+def test_rmsnorm_schedule_qwen7b_decode(nv):
+    x = synth.activation_bf16(64, 3584, 7, 1)
+    w = synth.aqn_weight(3584, 7, 2)
+    eps = synth.aqn_eps(3584, 7, 3)
+    for k in range(11):
+        s = np.float32(nv.aqn_sigma(1e-2, 5e-4, k, 10))
+        y = gpu_rmsnorm(nv, x, w, eps, s, 1e-6)
+        P.assert_rmsnorm_close(y, oracle.rmsnorm_aqn(x, w, eps, s, 1e-6), f"k={k}")
+
+
+@pytest.mark.parametrize("shape", [(1, 8), (3, 520), (4096, 3584), (256, 5120), (8192, 5120)])
+def test_rmsnorm_shapes(nv, shape):
+    M, H = shape
+    x = synth.activation_bf16(M, H, 8, M)
+    w = synth.aqn_weight(H, 8, 2)
+    eps = synth.aqn_eps(H, 8, 3)
+    y = gpu_rmsnorm(nv, x, w, eps, np.float32(3e-3), 1e-6)
+    P.assert_rmsnorm_close(y, oracle.rmsnorm_aqn(x, w, eps, np.float32(3e-3), 1e-6), f"{shape}")
+    y0 = gpu_rmsnorm(nv, x, w, None, 0.0, 1e-6)
+    P.assert_rmsnorm_close(y0, oracle.rmsnorm_aqn(x, w, None, 0.0, 1e-6), f"{shape} no noise")
+
+
+# ---------------------------------------------------------------- LoRA linear
+
+def _weights(n, k, seed, *stream, std=0.02, outliers=0.01, mask=None):
+    W = synth.weight_bf16(n, k, std, seed, *stream, outlier_frac=outliers)
+    return oracle.quantize(W, mask=mask)
+
+
+def gpu_linear(nv, w4a4, x, q, A, B, s, offsets=None):
+    codes, scales, g = q
+    fn = nv.nvfp4_lora_linear_w4a4 if w4a4 else nv.nvfp4_lora_linear
+    gd = P.dev(np.atleast_1d(np.asarray(g, np.float32)))
+    kw = {}
+    if offsets is not None:
+        kw = dict(group_offsets=P.dev(offsets.astype(np.int32)), num_groups=len(offsets) - 1)
+    y = fn(P.dev_bf16(x), P.dev(codes), P.dev(scales), gd, None if A is None else P.dev_bf16(A),
+           None if B is None else P.dev_bf16(B), s, **kw)
+    torch.cuda.synchronize()
+    return P.host_bits(y)
+
+
+def ref_linear(w4a4, x, q, A, B, s, rows=None):
+    if w4a4:
+        return oracle.lora_linear_w4a4(x, *q, A, B, s, rows=rows)[0]
+    return oracle.lora_linear_w4a16(x, *q, A, B, s, rows=rows)
+
+
+@pytest.mark.parametrize("w4a4", [False, True], ids=["w4a16", "w4a4"])
+def test_linear_tiny(nv, w4a4):
+    c = synth.tiny_config(0)
+    q = oracle.quantize(c["W"])
+    y = gpu_linear(nv, w4a4, c["x"], q, c["A"], c["B"], c["s"])
+    P.assert_gemm_close(y, ref_linear(w4a4, c["x"], q, c["A"], c["B"], c["s"]), "tiny")
+
+
+@pytest.mark.parametrize("w4a4", [False, True], ids=["w4a16", "w4a4"])
+@pytest.mark.parametrize("M,N,K,r,s", [(100, 384, 768, 32, 2.0), (1, 128, 256, 0, 2.0), (65, 256, 512, 16, 0.0),
+                                       (200, 640, 1024, 64, 0.5)])
+def test_linear_multi_tile_ragged(nv, w4a4, M, N, K, r, s):
+    q = _weights(N, K, 11, M, N)
+    x = synth.heavy_tail_activation_bf16(M, K, 12, M) if w4a4 else synth.activation_bf16(M, K, 12, M)
+    A, B = synth.lora_factors(r, K, N, 13, M) if r else (None, None)
+    y = gpu_linear(nv, w4a4, x, q, A, B, s)
+    P.assert_gemm_close(y, ref_linear(w4a4, x, q, A, B, s), f"{M}x{N}x{K} r={r}")
+
+
+def test_linear_empty_is_a_noop(nv):
+    q = _weights(128, 256, 1)
+    x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    y = nv.nvfp4_lora_linear(x, P.dev(q[0]), P.dev(q[1]), P.dev(np.atleast_1d(q[2])))
+    torch.cuda.synchronize()
+    assert y.shape == (0, 128)
+
+
+def test_linear_qwen7b_decode_full(nv):
+    """The 7B decode layer the benchmark times: M=64 bf16 tokens, every linear, r=32, every output."""
+    x = synth.activation_bf16(64, 3584, 21, 0)
+    x_int = synth.activation_bf16(64, 18944, 21, 1)
+    for i, (name, (n, k)) in enumerate(synth.QWEN25_7B["linears"].items()):
+        q = _weights(n, k, 2, i)
+        A, B = synth.lora_factors(32, k, n, 22, i)
+        xi = x_int if k == 18944 else x
+        y = gpu_linear(nv, False, xi, q, A, B, 2.0)
+        P.assert_gemm_close(y, ref_linear(False, xi, q, A, B, 2.0), f"7B {name}")
+
+
+def test_w4a4_qwen7b_prefill_sampled(nv):
+    """W4A4 at M=4096 with heavy-tailed channels; sampled rows (g_x still over all of x)."""
+    x = synth.heavy_tail_activation_bf16(4096, 3584, 31, 0)
+    x_int = synth.heavy_tail_activation_bf16(4096, 18944, 31, 1)
+    rows = np.sort(np.random.default_rng(32).choice(4096, 48, replace=False))
+    for i, (name, (n, k)) in enumerate(synth.QWEN25_7B["linears"].items()):
+        if name in ("o", "up"):
+            continue  # same shapes as q and gate
+        q = _weights(n, k, 2, i)
+        A, B = synth.lora_factors(32, k, n, 33, i)
+        xi = x_int if k == 18944 else x
+        y = gpu_linear(nv, True, xi, q, A, B, 2.0)
+        P.assert_gemm_close(y[rows], ref_linear(True, xi, q, A, B, 2.0, rows=rows), f"7B W4A4 {name}")
+
+
+def test_qwen32b_decode_and_prefill_sampled(nv):
+    rows256 = np.arange(0, 256, 8)
+    rows8k = np.sort(np.random.default_rng(41).choice(8192, 24, replace=False))
+    x256 = synth.activation_bf16(256, 5120, 40, 0)
+    x8k = synth.heavy_tail_activation_bf16(8192, 5120, 40, 1)
+    for i, name in enumerate(["q", "k", "gate"]):
+        n, k = synth.QWEN25_32B["linears"][name]
+        q = _weights(n, k, 3, i, std=0.015, outliers=0.0)
+        A, B = synth.lora_factors(64, k, n, 42, i)
+        y = gpu_linear(nv, False, x256, q, A, B, 2.0)
+        P.assert_gemm_close(y[rows256], ref_linear(False, x256, q, A, B, 2.0, rows=rows256), f"32B M=256 {name}")
+        y = gpu_linear(nv, True, x8k, q, A, B, 2.0)
+        P.assert_gemm_close(y[rows8k], ref_linear(True, x8k, q, A, B, 2.0, rows=rows8k), f"32B M=8192 {name}")
+
+
+# ---------------------------------------------------------------- grouped (MoE) W4A4
+
+def _grouped_ref(x, qs, offsets, rows):
+    """Per-expert dense oracle on the sampled rows (the grouped definition)."""
+    out = []
+    gx = oracle.global_scale(oracle.amax(x))
+    xc, xs = oracle.quantize_rows_given_g(x, gx, rows)
+    xq = oracle.dequantize(xc, xs, gx)
+    for i, r in enumerate(rows):
+        e = int(np.searchsorted(offsets, r, side="right") - 1)
+        out.append(oracle.linear(xq[i:i + 1], None, *qs[e], None, None, 0.0)[0])
+    return np.stack(out)
+
+
+def _stack(qs):
+    return (np.stack([q[0] for q in qs]), np.stack([q[1] for q in qs]), np.array([q[2] for q in qs], np.float32))
+
+
+def test_grouped_small_with_empty_experts(nv):
+    E, N, K = 8, 256, 512
+    tok, off = synth.moe_routing(96, E, 2, 5, 1)
+    off = off.copy()
+    # force expert 3 to be empty
+    counts = np.diff(off)
+    counts[4] += counts[3]
+    counts[3] = 0
+    off[1:] = np.cumsum(counts)
+    x = synth.activation_bf16(int(off[-1]), K, 51, 0)
+    qs = [_weights(N, K, 52, e) for e in range(E)]
+    y = gpu_linear(nv, True, x, _stack(qs), None, None, 0.0, offsets=off)
+    rows = np.arange(int(off[-1]))
+    P.assert_gemm_close(y, _grouped_ref(x, qs, off, rows), "grouped small")
+
+
+def test_grouped_moe_layer_sampled(nv):
+    """One MoE layer: 4096 tokens top-8 over 128 experts (32768 routed rows); guided-quantized expert
+    weights of the deepest layer; gate/up (768x2048) and down (2048x768); sampled rows."""
+    cfg = synth.MOE
+    E, H, I = cfg["experts"], cfg["hidden"], cfg["intermediate"]
+    _, off = synth.moe_routing(cfg["tokens"], E, cfg["top_k"], 47, 0)
+    M = int(off[-1])
+    rows = np.sort(np.random.default_rng(61).choice(M, 64, replace=False))
+    for j, (n, k) in enumerate([(I, H), (H, I)]):
+        qs = []
+        for e in range(E):
+            W = synth.weight_bf16(n, k, 0.02, 47, e, j)
+            qs.append(oracle.quantize(W, mask=synth.guided_mask(W.size, 47, e, j, 99)))
+        x = synth.activation_bf16(M, k, 62, j)
+        y = gpu_linear(nv, True, x, _stack(qs), None, None, 0.0, offsets=off)
+        P.assert_gemm_close(y[rows], _grouped_ref(x, qs, off, rows), f"MoE {'gate' if j == 0 else 'down'}")
