@@ -35,6 +35,9 @@ nvfp4rl_status current_device(DeviceInfo* out) {
         cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return NVFP4RL_ERR_CUDA;
     n.smem_optin = static_cast<size_t>(v);
+    void* sp = nullptr;
+    if (cudaGetSymbolAddress(&sp, g_device_status) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+    n.status = static_cast<uint32_t*>(sp);
     d = n;
   }
   if (d.cc_major != 10 || d.cc_minor != 3) return NVFP4RL_ERR_DEVICE;
@@ -53,10 +56,11 @@ namespace {
 nvfp4rl_status quantize_common(const void* x, int32_t dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                bool guided, uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
                                void* ws, size_t ws_bytes, void* stream) {
-  if (!x || !codes || !scales || !g || (guided && !mask)) return NVFP4RL_ERR_INVALID_ARG;
   if (dtype != NVFP4RL_BF16 && dtype != NVFP4RL_F32) return NVFP4RL_ERR_INVALID_ARG;
   if (rows < 0 || cols <= 0) return NVFP4RL_ERR_INVALID_ARG;
   if (cols % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return NVFP4RL_OK;  // empty tensor: nothing to read or write (g is left as is)
+  if (!x || !codes || !scales || !g || (guided && !mask)) return NVFP4RL_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (mask && !aligned16(mask)) ||
       (reinterpret_cast<uintptr_t>(g) & 3u) || (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)))
     return NVFP4RL_ERR_MISALIGNED;
@@ -87,8 +91,9 @@ nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K,
                              const uint8_t* w_scales, const float* w_g, int64_t N, const uint16_t* A,
                              const uint16_t* B, int32_t r, float s, const int32_t* offsets, int32_t groups,
                              uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
-  if (!x || !w_codes || !w_scales || !w_g || !y) return NVFP4RL_ERR_INVALID_ARG;
   if (M < 0 || K <= 0 || N <= 0 || r < 0 || r > 256) return NVFP4RL_ERR_INVALID_ARG;
+  if (M == 0) return NVFP4RL_OK;  // no activation rows: nothing to read or write
+  if (!x || !w_codes || !w_scales || !w_g || !y) return NVFP4RL_ERR_INVALID_ARG;
   if (r > 0 && (!A || !B)) return NVFP4RL_ERR_INVALID_ARG;
   if (!std::isfinite(s)) return NVFP4RL_ERR_INVALID_ARG;
   if (offsets) {
@@ -125,9 +130,9 @@ nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K,
 extern "C" {
 
 nvfp4rl_status nvfp4_amax(const void* x, int32_t dtype, int64_t n, float* amax, void* stream) {
-  if (!x || !amax) return NVFP4RL_ERR_INVALID_ARG;
+  if (!amax) return NVFP4RL_ERR_INVALID_ARG;
   if (dtype != NVFP4RL_BF16 && dtype != NVFP4RL_F32) return NVFP4RL_ERR_INVALID_ARG;
-  if (n < 0) return NVFP4RL_ERR_INVALID_ARG;
+  if (n < 0 || (n > 0 && !x)) return NVFP4RL_ERR_INVALID_ARG;
   if (n % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(amax) & 3u)) return NVFP4RL_ERR_MISALIGNED;
   if (overlap(amax, 4, x, static_cast<size_t>(n) * (dtype == NVFP4RL_BF16 ? 2 : 4))) return NVFP4RL_ERR_ALIAS;
@@ -159,9 +164,10 @@ double aqn_sigma(double sigma0, double sigmaK, int64_t k, int64_t K) {
 
 nvfp4rl_status rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps, float sigma,
                            float delta, uint16_t* y, void* stream) {
-  if (!x || !w || !y) return NVFP4RL_ERR_INVALID_ARG;
   if (M < 0 || H <= 0 || !std::isfinite(sigma) || !(delta >= 0.0f) || !std::isfinite(delta))
     return NVFP4RL_ERR_INVALID_ARG;
+  if (M == 0) return NVFP4RL_OK;
+  if (!x || !w || !y) return NVFP4RL_ERR_INVALID_ARG;
   if (H % 8 != 0 || H > rmsnorm_max_h() || M > 2147483647LL) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (eps && !aligned16(eps))) return NVFP4RL_ERR_MISALIGNED;
   const size_t yb = static_cast<size_t>(M) * H * 2;

@@ -57,6 +57,7 @@ struct DeviceInfo {
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
   size_t smem_optin = 0;
+  uint32_t* status = nullptr;  // device address of the library's error word on this device
 };
 
 // Cached attributes of the current device; NVFP4RL_ERR_DEVICE unless compute capability 10.3.
@@ -110,6 +111,15 @@ struct LinearArgs {
 };
 
 size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups);
+
+// Split-K planning uses at most this many SMs, so workspace sizes do not depend on the device.
+constexpr int kPlanSMs = 152;
+
+// tcgen05 W4A16 path (linear_tc.cu).
+bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r);
+size_t w4a16_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int sm_count);
+nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev,
+                               cudaStream_t st);
 nvfp4rl_status launch_linear(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st);
 
 }  // namespace nvfp4rl

@@ -6,7 +6,9 @@ Tolerances (floating point; integer/byte results are compared bit for bit):
     1e-2 * rms is the stated bar; a large element's bf16 rounding alone can exceed it
     (half an ulp is 2^-9 |Y|), so one bf16 ulp of the element is also allowed.
   * RMSNorm: per element |y_gpu - y_ref| <= 1 bf16 ulp of y_ref, and
-    rms(y_gpu - y_ref) / rms(y_ref) <= 1e-3.
+    rms(y_gpu - bf16(y_ref)) / rms(y_ref) <= 1e-3. The bf16 output's own rounding is
+    about 1.5e-3 of rms, so the 1e-3 bar is read against the bf16-rounded reference,
+    as for the GEMM.
 """
 import numpy as np
 import torch
@@ -60,6 +62,7 @@ def assert_rmsnorm_close(y_gpu_bits: np.ndarray, y_ref: np.ndarray, what: str = 
     ulp = bf16_ulp(y_ref)
     bad = err > ulp
     assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond 1 bf16 ulp; worst {err[bad].max()!r}"
-    rel = float(np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(y_ref ** 2)))
+    err_b = np.abs(y - bf16_round(y_ref))
+    rel = float(np.sqrt(np.mean(err_b ** 2)) / np.sqrt(np.mean(y_ref ** 2)))
     assert rel <= 1e-3, f"{what}: rms error ratio {rel}"
     return rel
