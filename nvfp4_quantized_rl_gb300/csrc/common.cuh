@@ -1,6 +1,7 @@
 // Shared device helpers of the NVFP4 rollout-linear library (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -114,6 +115,16 @@ size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r,
 
 // Split-K planning uses at most this many SMs, so workspace sizes do not depend on the device.
 constexpr int kPlanSMs = 152;
+
+// 2-D TMA tensor map over a row-major [rows][cols] array of `esize`-byte elements (linear_tc.cu).
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                        int esize, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+
+// tcgen05 W4A4 block-scaled path (linear_w4a4_tc.cu).
+bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r);
+size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups);
+nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev,
+                              cudaStream_t st);
 
 // tcgen05 W4A16 path (linear_tc.cu).
 bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r);

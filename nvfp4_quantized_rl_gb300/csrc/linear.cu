@@ -279,12 +279,14 @@ WsLayout layout(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups) {
 
 size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups) {
   if (!w4a4 && w4a16_tc_supported(M, N, K, r)) return w4a16_tc_workspace_bytes(M, N, K, r, kPlanSMs);
+  if (w4a4 && w4a4_tc_supported(M, N, K, r)) return w4a4_tc_workspace_bytes(M, N, K, r, groups);
   return layout(w4a4, M, N, K, r, groups).total;
 }
 
 nvfp4rl_status launch_linear(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
   if (a.M == 0) return NVFP4RL_OK;
   if (!a.w4a4 && w4a16_tc_supported(a.M, a.N, a.K, a.r)) return launch_w4a16_tc(a, ws, ws_bytes, dev, st);
+  if (a.w4a4 && w4a4_tc_supported(a.M, a.N, a.K, a.r)) return launch_w4a4_tc(a, ws, ws_bytes, dev, st);
   const int groups = a.offsets ? a.groups : 1;
   const WsLayout L = layout(a.w4a4, a.M, a.N, a.K, a.r, groups);
   if (ws_bytes < L.total) return NVFP4RL_ERR_WORKSPACE;

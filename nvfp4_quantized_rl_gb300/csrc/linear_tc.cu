@@ -245,11 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     for (int j = 0; j < nst && ok; ++j) {
       const int s = j % S, a = j % kAbuf;
-      if (!mbar_wait(smem_addr(&full[s]), (j / S) & 1, p.status, kStatusTimeoutDequant) ||
-          !mbar_wait(smem_addr(&aempty[a]), ((j / kAbuf) & 1) ^ 1, p.status, kStatusTimeoutDequant)) {
-        ok = false;
-        break;
-      }
+      // every lane waits; the warp leaves together if any lane ran out of time
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (j / S) & 1, p.status, kStatusTimeoutDequant) &&
+                                       mbar_wait(smem_addr(&aempty[a]), ((j / kAbuf) & 1) ^ 1, p.status,
+                                                 kStatusTimeoutDequant));
+      if (!ok) break;
       const uint8_t* st = smem + s * sb;
       const uint8_t* crow = st + row * 128;
       const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + x_stage_bytes(MBOX) + row * 16 + half * 8);
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---------------------------------------------------------------- epilogue
-    if (!mbar_wait(smem_addr(dfull), 0, p.status, kStatusTimeoutEpilogue)) ok = false;
+    ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait(smem_addr(dfull), 0, p.status, kStatusTimeoutEpilogue));
     tc_fence_after();
     if (ok) {
       const float g = *p.w_g;
@@ -315,14 +315,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (*last_flag) {
         __threadfence();
-        const int64_t n = n0 + row;
-        constexpr int kTokHalf = MBOX / 2;
-        for (int i = 0; i < kTokHalf; ++i) {
-          const int64_t m = m0 + half * kTokHalf + i;
-          if (m >= p.M) break;
-          float v = 0.0f;
-          for (int sp = 0; sp < p.splits; ++sp) v += __ldcg(p.slabs + (static_cast<int64_t>(sp) * p.M + m) * p.N + n);
-          p.y[m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(v));
+        // 256 threads over the MBOX x 128 output tile: thread -> one row, a run of kCols columns
+        constexpr int kThreadsPerRow = 256 / MBOX, kCols = kRows / kThreadsPerRow;
+        const int t = dw * 32 + lane;
+        const int64_t m = m0 + t / kThreadsPerRow;
+        const int64_t nb = n0 + (t % kThreadsPerRow) * kCols;
+        if (m < p.M) {
+          float acc[kCols];
+#pragma unroll
+          for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
+          for (int sp = 0; sp < p.splits; ++sp) {
+            const float4* src = reinterpret_cast<const float4*>(p.slabs + (static_cast<int64_t>(sp) * p.M + m) * p.N + nb);
+#pragma unroll
+            for (int i = 0; i < kCols / 4; ++i) {
+              const float4 v = __ldcg(src + i);
+              acc[4 * i] += v.x;
+              acc[4 * i + 1] += v.y;
+              acc[4 * i + 2] += v.z;
+              acc[4 * i + 3] += v.w;
+            }
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.y + m * p.N + nb);
+#pragma unroll
+          for (int i = 0; i < kCols / 8; ++i) {
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              o[q] = f32_to_bf16_bits(acc[8 * i + 2 * q]) | (f32_to_bf16_bits(acc[8 * i + 2 * q + 1]) << 16);
+            dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+          }
         }
       }
     }
@@ -336,18 +357,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Prep: x_perm (K permuted inside groups of 8 as 0,4,1,5,2,6,3,7), U = bf16(x A^T), and zeroed
-// split-K counters. One CTA per activation row.
-__global__ void __launch_bounds__(256) w4a16_prep_kernel(const uint16_t* __restrict__ x, int64_t K,
+constexpr int kPrepChunk = 1024;  // K per prep CTA
+
+// Prep: x_perm (K permuted inside groups of 8 as 0,4,1,5,2,6,3,7) and the LoRA down-projection
+// U = bf16(x A^T). CTA (chunk, m) handles 1024 K of row m: it writes that slice of x_perm and
+// adds its partial dot products into the fp32 accumulator U32 (zeroed by the caller); the last
+// chunk of a row (per-row arrival counter) converts the row of U to bf16.
+__global__ void __launch_bounds__(128) w4a16_prep_kernel(const uint16_t* __restrict__ x, int64_t K,
                                                          const uint16_t* __restrict__ A, int r,
-                                                         uint16_t* __restrict__ xp, uint16_t* __restrict__ U,
-                                                         uint32_t* __restrict__ counters, int ncounters) {
-  const int64_t m = blockIdx.x;
-  if (m == 0)
-    for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
+                                                         uint16_t* __restrict__ xp, float* __restrict__ U32,
+                                                         uint16_t* __restrict__ U, uint32_t* __restrict__ rowcnt) {
+  const int64_t m = blockIdx.y;
+  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * (kPrepChunk / 8);
+  const int64_t v1 = min(K / 8, v0 + kPrepChunk / 8);
   const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
   uint4* pr = reinterpret_cast<uint4*>(xp + m * K);
-  for (int64_t v = threadIdx.x; v < K / 8; v += blockDim.x) {
+  for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
     const uint4 a = xr[v];
     // elements e0..e7 (two per word) -> e0 e4 | e1 e5 | e2 e6 | e3 e7
     uint4 o;
@@ -357,11 +382,13 @@ __global__ void __launch_bounds__(256) w4a16_prep_kernel(const uint16_t* __restr
     o.w = __byte_perm(a.y, a.w, 0x7632);
     pr[v] = o;
   }
+  if (r == 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int j = warp; j < r; j += 8) {
+  for (int j = warp; j < r; j += 4) {
     const uint4* ar = reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j) * K);
     float acc = 0.0f;
-    for (int64_t v = lane; v < K / 8; v += 32) {
+#pragma unroll 4
+    for (int64_t v = v0 + lane; v < v1; v += 32) {
       const uint4 xv = xr[v], av = __ldg(ar + v);
       const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w}, aq[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
@@ -371,7 +398,17 @@ __global__ void __launch_bounds__(256) w4a16_prep_kernel(const uint16_t* __restr
       }
     }
     acc = warp_sum(acc);
-    if (lane == 0) U[m * r + j] = static_cast<uint16_t>(f32_to_bf16_bits(acc));
+    if (lane == 0) atomicAdd(U32 + m * r + j, acc);
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ uint32_t last;
+  if (threadIdx.x == 0) last = (atomicAdd(rowcnt + m, 1u) == gridDim.x - 1) ? 1u : 0u;
+  __syncthreads();
+  if (last) {
+    __threadfence();
+    for (int j = threadIdx.x; j < r; j += blockDim.x)
+      U[m * r + j] = static_cast<uint16_t>(f32_to_bf16_bits(__ldcg(U32 + m * r + j)));
   }
 }
 
@@ -390,18 +427,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D tensor map over a row-major [rows][cols] array of `esize`-byte elements.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows, int esize,
-              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(esize)};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
 
 CUtensorMapSwizzle swizzle_for(int box_bytes) {
   return box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -411,7 +438,8 @@ CUtensorMapSwizzle swizzle_for(int box_bytes) {
 
 struct TcPlan {
   int mbox, tiles_m, tiles_n, splits, stages_per_split, smem_stages;
-  size_t smem_bytes, ws_xperm, ws_u, ws_counters, ws_slabs, ws_total;
+  // ws_zero .. ws_zero + zero_bytes is cleared every call: U32, per-row and per-tile counters
+  size_t smem_bytes, ws_xperm, ws_u, ws_zero, zero_bytes, ws_u32, ws_rowcnt, ws_counters, ws_slabs, ws_total;
 };
 
 TcPlan plan(int64_t M, int64_t N, int64_t K, int r, int sm_count) {
@@ -433,13 +461,35 @@ TcPlan plan(int64_t M, int64_t N, int64_t K, int r, int sm_count) {
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
   t.ws_xperm = take(static_cast<size_t>(M) * K * 2);
   t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
+  t.ws_u32 = take(static_cast<size_t>(M) * std::max(r, 1) * 4);
+  t.ws_rowcnt = take(static_cast<size_t>(M) * 4);
   t.ws_counters = take(static_cast<size_t>(t.tiles_m) * t.tiles_n * 4);
+  t.ws_zero = t.ws_u32;
+  t.zero_bytes = o - t.ws_u32;
   t.ws_slabs = take(t.splits > 1 ? static_cast<size_t>(t.splits) * M * N * 4 : 0);
   t.ws_total = o;
   return t;
 }
 
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows, int esize,
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  return make_tensor_map_2d(m, dt, base, cols, rows, esize, box_cols, box_rows, sw);
+}
+
 }  // namespace
+
+// 2-D tensor map over a row-major [rows][cols] array of `esize`-byte elements; zero fill outside.
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                        int esize, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(esize)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // True when the tcgen05 W4A16 path takes this shape.
 bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
@@ -462,8 +512,10 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   uint32_t* counters = reinterpret_cast<uint32_t*>(base + t.ws_counters);
   float* slabs = reinterpret_cast<float*>(base + t.ws_slabs);
 
-  w4a16_prep_kernel<<<static_cast<unsigned>(a.M), 256, 0, st>>>(a.x, a.K, a.A, a.r, xp, U, counters,
-                                                                  t.tiles_m * t.tiles_n);
+  if (cudaMemsetAsync(base + t.ws_zero, 0, t.zero_bytes, st) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  dim3 pgrid(static_cast<unsigned>((a.K + kPrepChunk - 1) / kPrepChunk), static_cast<unsigned>(a.M));
+  w4a16_prep_kernel<<<pgrid, 128, 0, st>>>(a.x, a.K, a.A, a.r, xp, reinterpret_cast<float*>(base + t.ws_u32), U,
+                                           reinterpret_cast<uint32_t*>(base + t.ws_rowcnt));
   if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
 
   CUtensorMap mc, ms, mx, mb, mu;

@@ -1,0 +1,478 @@
+// W4A4 NVFP4 LoRA linear on tcgen05 block-scaled FP4 MMA (kind::mxf4nvf4), sm_103a.
+//
+// TRACE summary, sections "論文が取り組む課題" and "実験結果と性能": the rollout runs with
+// FP4 weights and FP4 activations. The activations are quantized on the fly with the
+// NVFP4 recipe (one per-tensor g_x, 16-element E4M3 block scales); the tensor cores then
+// take both operands as packed E2M1 with their block scales, and the epilogue applies
+// g_x * g_w and adds the LoRA branch s (x A^T) B^T computed from the bf16 activations
+// (QeRL explainer, section "NVFP4量子化とLoRA"). Grouped mode runs one weight matrix per
+// MoE expert over that expert's contiguous block of routed rows.
+//
+// Persistent kernel, one CTA per SM, tile = 128 activation rows x 128 weight rows:
+//   warp 0      TMA producer: per 256-K stage the activation and weight code tiles
+//               (128 x 128 bytes each, 128-byte swizzle) and both 128 x 16-byte scale tiles.
+//   warp 1      MMA warp: re-lays the stage's scale bytes into the 32 x 16-byte groups
+//               tcgen05.cp expects (row r of a 128-row block goes to group row r % 32, word
+//               r / 32), copies them to TMEM, and one thread issues four
+//               tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each); at the
+//               end of a tile the LoRA up-projection (U tile x B_lora tile^T, kind::f16)
+//               goes to a separate accumulator.
+//   warps 2-5   epilogue: TMEM -> registers, Y = g_x g_w D + s D_lora, bf16 stores; the
+//               accumulator is double buffered so it overlaps the next tile's main loop.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace nvfp4rl {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTile = 128;
+constexpr int kKStage = 256;
+constexpr int kCodeBytes = kTile * kKStage / 2;   // 16 KB per operand
+constexpr int kSfBytes = kTile * kKStage / 16;    // 2 KB per operand
+constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSfBytes;
+constexpr int kAtomBytes = 2 * 4 * 512;           // per stage: A and B, 4 K-steps x 512 bytes
+constexpr int kThreads = 192;
+constexpr uint32_t kD0 = 0, kD1 = 128, kDL = 256, kSF = 384;  // TMEM columns
+
+struct W4a4Params {
+  int64_t M, N, K;
+  int tiles_n;
+  int total_tiles;         // dense: tiles_m * tiles_n; grouped: read from tile_start[groups] * tiles_n
+  int r, lora_box_bytes;
+  float s;
+  const float* g_x;
+  const float* w_g;        // [groups]
+  const int32_t* offsets;  // grouped row offsets or null
+  const int32_t* tile_start;
+  int groups;
+  uint16_t* y;
+  uint32_t* status;
+  int stages;
+};
+
+__device__ __forceinline__ int find_group(const int32_t* starts, int groups, int64_t v) {
+  int lo = 0, hi = groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (starts[mid] <= v) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct TileInfo {
+  int e;          // expert (0 when dense)
+  int64_t m0;     // first activation row
+  int64_t m_end;  // one past the last row this tile may write
+  int n0;         // first weight row within the expert
+};
+
+__device__ __forceinline__ TileInfo tile_info(const W4a4Params& p, int t) {
+  TileInfo ti;
+  const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+  ti.n0 = tn * kTile;
+  if (p.offsets) {
+    ti.e = find_group(p.tile_start, p.groups, tm);
+    ti.m0 = p.offsets[ti.e] + static_cast<int64_t>(tm - p.tile_start[ti.e]) * kTile;
+    ti.m_end = p.offsets[ti.e + 1];
+  } else {
+    ti.e = 0;
+    ti.m0 = static_cast<int64_t>(tm) * kTile;
+    ti.m_end = p.M;
+  }
+  return ti;
+}
+
+__device__ __forceinline__ int total_tiles(const W4a4Params& p) {
+  return p.offsets ? p.tile_start[p.groups] * p.tiles_n : p.total_tiles;
+}
+
+__device__ __forceinline__ uint32_t lora_swizzle(int box_bytes) {
+  return box_bytes == 128 ? 2u : box_bytes == 64 ? 4u : 6u;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a4_tc_kernel(const __grid_constant__ CUtensorMap map_xc, const __grid_constant__ CUtensorMap map_xs,
+                   const __grid_constant__ CUtensorMap map_wc, const __grid_constant__ CUtensorMap map_ws,
+                   const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_bl,
+                   const W4a4Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  uint8_t* atoms = smem + S * kStageBytes;          // S x kAtomBytes
+  uint8_t* lora_u = atoms + S * kAtomBytes;         // 128 x 2r
+  const int lbytes = p.r ? kTile * 2 * p.r : 0;
+  uint8_t* lora_b = lora_u + lbytes;                // 128 x 2r
+  uint64_t* full = reinterpret_cast<uint64_t*>(lora_b + lbytes);
+  uint64_t* empty = full + S;
+  uint64_t* dfull = empty + S;      // [2]
+  uint64_t* dempty = dfull + 2;     // [2]
+  uint64_t* lfull = dempty + 2;     // LoRA operands landed
+  uint64_t* lempty = lfull + 1;     // LoRA operand smem + D_lora free
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lempty + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ksteps = static_cast<int>(p.K / kKStage);
+  const int ntiles = total_tiles(p);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&dfull[i]), 1);
+      mbar_init(smem_addr(&dempty[i]), 4);
+    }
+    mbar_init(smem_addr(lfull), 1);
+    mbar_init(smem_addr(lempty), 4);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_xc);
+      prefetch_tensormap(&map_xs);
+      prefetch_tensormap(&map_wc);
+      prefetch_tensormap(&map_ws);
+      int it = 0, li = 0, last_issued = 0, lora_issued = 0;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
+        const TileInfo ti = tile_info(p, t);
+        const int wrow = ti.e * static_cast<int>(p.N) + ti.n0;
+        for (int k = 0; k < ksteps; ++k, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(smem_addr(&empty[s]), ((it / S) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kStageBytes;
+          const uint32_t bar = smem_addr(&full[s]);
+          mbar_arrive_expect_tx(bar, kStageBytes);
+          tma_load_2d(smem_addr(st), &map_xc, k * (kKStage / 2), static_cast<int32_t>(ti.m0), bar);
+          tma_load_2d(smem_addr(st + kCodeBytes), &map_wc, k * (kKStage / 2), wrow, bar);
+          tma_load_2d(smem_addr(st + 2 * kCodeBytes), &map_xs, k * (kKStage / 16), static_cast<int32_t>(ti.m0), bar);
+          tma_load_2d(smem_addr(st + 2 * kCodeBytes + kSfBytes), &map_ws, k * (kKStage / 16), wrow, bar);
+          last_issued = it + 1;
+        }
+        if (ok && p.r) {
+          // LoRA operands of this tile (U rows m0.., B_lora rows n0..), needed after its main loop,
+          // once the epilogue of the previous tile has read the LoRA accumulator
+          if (!mbar_wait(smem_addr(lempty), (li & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_addr(lfull);
+          mbar_arrive_expect_tx(bar, 2 * lbytes);
+          const int nbox = 2 * p.r / p.lora_box_bytes, box_el = p.lora_box_bytes / 2;
+          for (int b = 0; b < nbox; ++b) {
+            tma_load_2d(smem_addr(lora_u + b * kTile * p.lora_box_bytes), &map_u, b * box_el,
+                        static_cast<int32_t>(ti.m0), bar);
+            tma_load_2d(smem_addr(lora_b + b * kTile * p.lora_box_bytes), &map_bl, b * box_el, ti.n0, bar);
+          }
+          lora_issued = li + 1;
+        }
+      }
+      for (int j = max(0, last_issued - S); j < last_issued; ++j)
+        mbar_wait(smem_addr(&full[j % S]), (j / S) & 1, p.status, kStatusTimeoutDrain);
+      if (lora_issued) mbar_wait(smem_addr(lfull), (lora_issued - 1) & 1, p.status, kStatusTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA (+ scale-factor relayout)
+    const uint32_t idesc = idesc_nvf4_f32(kTile, kTile);
+    const uint32_t idesc_l = idesc_bf16_f32(kTile, kTile);
+    int it = 0, li = 0;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
+      const int buf = li & 1;
+      const uint32_t dcol = buf ? kD1 : kD0;
+      // every lane waits; the warp leaves together if any lane ran out of time
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&dempty[buf]), ((li >> 1) & 1) ^ 1, p.status, kStatusTimeoutMma));
+      if (!ok) break;
+      tc_fence_after();
+      for (int k = 0; k < ksteps; ++k, ++it) {
+        const int s = it % S;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (it / S) & 1, p.status, kStatusTimeoutMma));
+        if (!ok) break;
+        // scale factors: [128 rows][16 bytes] row-major -> per K-step t a 512-byte group where
+        // group row i holds the 4 bytes of rows i, 32+i, 64+i, 96+i
+        const uint8_t* st = smem + s * kStageBytes;
+        uint8_t* at = atoms + s * kAtomBytes;
+#pragma unroll
+        for (int op = 0; op < 2; ++op) {
+          const uint4* sf = reinterpret_cast<const uint4*>(st + 2 * kCodeBytes + op * kSfBytes);
+          const uint4 r0 = sf[lane], r1 = sf[32 + lane], r2 = sf[64 + lane], r3 = sf[96 + lane];
+          uint4* dst = reinterpret_cast<uint4*>(at + op * 2048);
+          dst[0 * 32 + lane] = make_uint4(r0.x, r1.x, r2.x, r3.x);
+          dst[1 * 32 + lane] = make_uint4(r0.y, r1.y, r2.y, r3.y);
+          dst[2 * 32 + lane] = make_uint4(r0.z, r1.z, r2.z, r3.z);
+          dst[3 * 32 + lane] = make_uint4(r0.w, r1.w, r2.w, r3.w);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          // each pipeline stage owns 32 scale-factor columns: stage s is refilled (and its columns
+          // rewritten) only after the MMAs that read them have completed (empty[s])
+          const uint32_t sfcol = kSF + s * 32;
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt) {
+            tmem_cp_32x128b_x4(tmem + sfcol + tt * 4, smem_desc(smem_addr(at + tt * 512), 0, 128, 0));
+            tmem_cp_32x128b_x4(tmem + sfcol + 16 + tt * 4, smem_desc(smem_addr(at + 2048 + tt * 512), 0, 128, 0));
+          }
+          const uint32_t xa = smem_addr(st), wa = smem_addr(st + kCodeBytes);
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt) {
+            const uint64_t ad = smem_desc(xa + tt * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(wa + tt * 32, 16, 1024, 2);
+            mma_nvf4_ss(tmem + dcol, ad, bd, idesc, tmem + sfcol + tt * 4, tmem + sfcol + 16 + tt * 4,
+                        (k | tt) ? 1u : 0u);
+          }
+          mma_commit(smem_addr(&empty[s]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (p.r) {
+        if (lane == 0) {
+          const bool got = mbar_wait(smem_addr(lfull), li & 1, p.status, kStatusTimeoutMma);
+          if (got) {
+            tc_fence_after();
+            const uint32_t sw = lora_swizzle(p.lora_box_bytes), sbo = 8 * p.lora_box_bytes;
+            const uint32_t ua = smem_addr(lora_u), ba = smem_addr(lora_b);
+            for (int kk = 0; kk < p.r / 16; ++kk) {
+              const int off = kk * 32, box = off / p.lora_box_bytes, in = off % p.lora_box_bytes;
+              mma_f16_ss(tmem + kDL, smem_desc(ua + box * kTile * p.lora_box_bytes + in, 16, sbo, sw),
+                         smem_desc(ba + box * kTile * p.lora_box_bytes + in, 16, sbo, sw), idesc_l, kk ? 1u : 0u);
+            }
+          } else {
+            ok = false;
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      }
+      if (lane == 0) mma_commit(smem_addr(&dfull[buf]));
+      __syncwarp();
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const float gx = *p.g_x;
+    int li = 0;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
+      const int buf = li & 1;
+      const uint32_t dcol = buf ? kD1 : kD0;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&dfull[buf]), (li >> 1) & 1, p.status, kStatusTimeoutEpilogue));
+      if (!ok) break;
+      tc_fence_after();
+      const TileInfo ti = tile_info(p, t);
+      const float alpha = gx * p.w_g[ti.e];
+      const int64_t m = ti.m0 + quarter * 32 + lane;
+      const bool live = m < ti.m_end;
+      uint16_t* yrow = p.y + m * p.N + ti.n0;
+#pragma unroll 1
+      for (int c = 0; c < kTile; c += 16) {
+        uint32_t d[16], l[16];
+        tmem_ld16(tmem + lane_base + dcol + c, d);
+        if (p.r) tmem_ld16(tmem + lane_base + kDL + c, l);
+        tmem_ld_wait();
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float a = __uint_as_float(d[2 * i]) * alpha, b = __uint_as_float(d[2 * i + 1]) * alpha;
+          if (p.r) {
+            a = fmaf(p.s, __uint_as_float(l[2 * i]), a);
+            b = fmaf(p.s, __uint_as_float(l[2 * i + 1]), b);
+          }
+          o[i] = f32_to_bf16_bits(a) | (f32_to_bf16_bits(b) << 16);
+        }
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&dempty[buf]));
+        if (p.r) mbar_arrive(smem_addr(lempty));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// U = bf16(x A^T) (LoRA down-projection from the bf16 activations). One CTA per row.
+__global__ void __launch_bounds__(256) lora_down_bf16_kernel(const uint16_t* __restrict__ x, int64_t K,
+                                                             const uint16_t* __restrict__ A, int r,
+                                                             uint16_t* __restrict__ U) {
+  const int64_t m = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
+  for (int j = warp; j < r; j += 8) {
+    const uint4* ar = reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j) * K);
+    float acc = 0.0f;
+    for (int64_t v = lane; v < K / 8; v += 32) {
+      const uint4 xv = xr[v], av = __ldg(ar + v);
+      const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w}, aq[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc = fmaf(__uint_as_float(bf16_lo_bits(xq[q])), __uint_as_float(bf16_lo_bits(aq[q])), acc);
+        acc = fmaf(__uint_as_float(bf16_hi_bits(xq[q])), __uint_as_float(bf16_hi_bits(aq[q])), acc);
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) U[m * r + j] = static_cast<uint16_t>(f32_to_bf16_bits(acc));
+  }
+}
+
+// tile_start[e] = sum over e' < e of ceil(rows(e') / 128); tile_start[groups] = total row tiles.
+__global__ void __launch_bounds__(1024) tile_map128_kernel(const int32_t* __restrict__ offsets, int groups,
+                                                           int32_t* __restrict__ tile_start) {
+  __shared__ int32_t s[1024];
+  const int e = threadIdx.x;
+  s[e] = e < groups ? (offsets[e + 1] - offsets[e] + kTile - 1) / kTile : 0;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {
+    const int32_t add = e >= o ? s[e - o] : 0;
+    __syncthreads();
+    s[e] += add;
+    __syncthreads();
+  }
+  if (e < groups) tile_start[e + 1] = s[e];
+  if (e == 0) tile_start[0] = 0;
+}
+
+struct W4a4Plan {
+  int stages;
+  size_t smem, ws_codes, ws_scales, ws_amax, ws_gx, ws_u, ws_tiles, ws_total;
+};
+
+W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups) {
+  W4a4Plan t{};
+  const size_t lora = r ? 2 * static_cast<size_t>(kTile) * 2 * r : 0;
+  const size_t fixed = 1024 + lora + 512;
+  // at most 4 stages: TMEM holds 2 x 128 accumulator + 128 LoRA + 4 x 32 scale-factor columns
+  t.stages = static_cast<int>(std::min<size_t>(4, (227 * 1024 - fixed) / (kStageBytes + kAtomBytes)));
+  t.smem = fixed + t.stages * (kStageBytes + kAtomBytes);
+  size_t o = 0;
+  auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
+  t.ws_codes = take(static_cast<size_t>(M) * K / 2);
+  t.ws_scales = take(static_cast<size_t>(M) * K / 16);
+  t.ws_amax = take(kQuantizeWorkspace);
+  t.ws_gx = take(16);
+  t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
+  t.ws_tiles = take(static_cast<size_t>(groups + 2) * 4);
+  t.ws_total = o;
+  return t;
+}
+
+CUtensorMapSwizzle lora_map_swizzle(int box_bytes) {
+  return box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                           : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+}  // namespace
+
+bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
+  return M > 0 && N % kTile == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= 128)) &&
+         w4a4_plan(M, K, r, 1).stages >= 2;
+}
+
+size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups) {
+  (void)N;
+  return w4a4_plan(M, K, r, groups).ws_total;
+}
+
+nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev,
+                              cudaStream_t st) {
+  const int groups = a.offsets ? a.groups : 1;
+  const W4a4Plan t = w4a4_plan(a.M, a.K, a.r, groups);
+  if (ws_bytes < t.ws_total) return NVFP4RL_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  uint8_t* xc = reinterpret_cast<uint8_t*>(base + t.ws_codes);
+  uint8_t* xs = reinterpret_cast<uint8_t*>(base + t.ws_scales);
+  float* gx = reinterpret_cast<float*>(base + t.ws_gx);
+  uint16_t* U = reinterpret_cast<uint16_t*>(base + t.ws_u);
+  int32_t* tiles = reinterpret_cast<int32_t*>(base + t.ws_tiles);
+
+  nvfp4rl_status sq = launch_quantize(a.x, NVFP4RL_BF16, a.M, a.K, nullptr, xc, xs, gx, nullptr,
+                                      reinterpret_cast<uint32_t*>(base + t.ws_amax), dev, st);
+  if (sq != NVFP4RL_OK) return sq;
+  if (a.r) {
+    lora_down_bf16_kernel<<<static_cast<unsigned>(a.M), 256, 0, st>>>(a.x, a.K, a.A, a.r, U);
+    if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  }
+  if (a.offsets) {
+    tile_map128_kernel<<<1, 1024, 0, st>>>(a.offsets, groups, tiles);
+    if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  }
+  CUtensorMap mxc, mxs, mwc, mws, mu, mb;
+  const int lbox = a.r ? std::min(2 * a.r, 128) : 128;
+  const uint64_t wrows = static_cast<uint64_t>(groups) * a.N;
+  if (!make_tensor_map_2d(&mxc, CU_TENSOR_MAP_DATA_TYPE_UINT8, xc, a.K / 2, a.M, 1, 128, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map_2d(&mxs, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, a.K / 16, a.M, 1, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_tensor_map_2d(&mwc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, a.K / 2, wrows, 1, 128, kTile,
+                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map_2d(&mws, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_scales, a.K / 16, wrows, 1, 16, kTile,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+    return NVFP4RL_ERR_CUDA;
+  if (a.r) {
+    if (!make_tensor_map_2d(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, U, a.r, a.M, 2, lbox / 2, kTile,
+                            lora_map_swizzle(lbox)) ||
+        !make_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, a.r, a.N, 2, lbox / 2, kTile,
+                            lora_map_swizzle(lbox)))
+      return NVFP4RL_ERR_CUDA;
+  } else {
+    mu = mxc;
+    mb = mxc;
+  }
+  W4a4Params p{};
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.tiles_n = static_cast<int>(a.N / kTile);
+  const int64_t tiles_m_bound = a.offsets ? (a.M + kTile - 1) / kTile + groups : (a.M + kTile - 1) / kTile;
+  p.total_tiles = static_cast<int>(((a.M + kTile - 1) / kTile) * p.tiles_n);
+  p.r = a.r;
+  p.lora_box_bytes = lbox;
+  p.s = a.s;
+  p.g_x = gx;
+  p.w_g = a.w_g;
+  p.offsets = a.offsets;
+  p.tile_start = tiles;
+  p.groups = groups;
+  p.y = a.y;
+  p.status = dev.status;
+  p.stages = t.stages;
+  const int64_t max_tiles = tiles_m_bound * p.tiles_n;
+  const int grid = static_cast<int>(std::min<int64_t>(max_tiles, dev.sm_count));
+  if (cudaFuncSetAttribute(w4a4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(t.smem)) !=
+      cudaSuccess)
+    return NVFP4RL_ERR_CUDA;
+  w4a4_tc_kernel<<<grid, kThreads, t.smem, st>>>(mxc, mxs, mwc, mws, mu, mb, p);
+  return launch_status();
+}
+
+}  // namespace nvfp4rl

@@ -168,20 +168,55 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
 
     uint32_t lo32 = 0, hi32 = 0;
     if (!kGuided) {
-      uint32_t th[7];
-      plain_thresholds(dec, g, th);
-      if (b == 0) {
+      // Fast path: t = |x| * fl(1 / fl(dec g)) differs from the exact quotient by at most 3 ulps,
+      // so the hardware round-to-nearest E2M1 conversion of t decides exactly unless t lies
+      // within 8 ulps of a multiple of a quarter of its binade (every decision boundary
+      // 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 is such a point). Such blocks, zero scales and
+      // scales far from 1 take the exact threshold path below.
+      const float S = dec * g;
+      bool exact = (b == 0) || !(S >= 0x1p-100f && S <= 0x1p100f);
+      if (!exact) {
+        const float inv = __frcp_rn(S);
+        uint32_t near = 0xFFFFFFFFu;
+        uint32_t mags[8];
 #pragma unroll
-        for (int k = 0; k < 7; ++k) th[k] = 0x7F800000u;  // zero scale: every code is sign|0
+        for (int i = 0; i < 8; ++i) {
+          const float t0 = __uint_as_float(ax[2 * i]) * inv, t1 = __uint_as_float(ax[2 * i + 1]) * inv;
+          near = min(near, (__float_as_uint(t0) + 8u) & 0x1FFFFFu);
+          near = min(near, (__float_as_uint(t1) + 8u) & 0x1FFFFFu);
+          uint16_t pair;  // code(t1) in the high nibble, code(t0) in the low nibble
+          asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.u16.u8 %0, q;\n\t}"
+              : "=h"(pair)
+              : "f"(t1), "f"(t0));
+          mags[i] = pair & 0x77u;
+        }
+        exact = near < 16u;
+        if (!exact) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t code2 = mags[i] | (((sgn >> (2 * i)) & 1u) << 3) | (((sgn >> (2 * i + 1)) & 1u) << 7);
+            if (i < 4) lo32 |= code2 << (8 * i);
+            else hi32 |= code2 << (8 * (i - 4));
+          }
+        }
       }
+      if (exact) {
+        uint32_t th[7];
+        plain_thresholds(dec, g, th);
+        if (b == 0) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        uint32_t mag = 0;
+          for (int k = 0; k < 7; ++k) th[k] = 0x7F800000u;  // zero scale: every code is sign|0
+        }
+        lo32 = hi32 = 0;
 #pragma unroll
-        for (int k = 0; k < 7; ++k) mag += ax[i] > th[k] ? 1u : 0u;
-        const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
-        if (i < 8) lo32 |= code << (4 * i);
-        else hi32 |= code << (4 * (i - 8));
+        for (int i = 0; i < 16; ++i) {
+          uint32_t mag = 0;
+#pragma unroll
+          for (int k = 0; k < 7; ++k) mag += ax[i] > th[k] ? 1u : 0u;
+          const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
+          if (i < 8) lo32 |= code << (4 * i);
+          else hi32 |= code << (4 * (i - 8));
+        }
       }
     } else {
       uint32_t ge[7], gt[7];
