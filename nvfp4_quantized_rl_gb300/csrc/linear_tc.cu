@@ -45,6 +45,7 @@ constexpr int kCodeBytes = kRows * kKStage / 2;   // 16 KB
 constexpr int kScaleBytes = kRows * kKStage / 16;  // 2 KB
 constexpr int kThreads = 320;     // 10 warps
 constexpr int kDeqWarps = 8;
+constexpr int kMaxSplits = 8;     // split-K factor cap (the last CTA keeps one load per split in flight)
 
 struct TcParams {
   int64_t M, N, K;
@@ -202,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kRows, MBOX);
       for (int j = 0; j < nst && ok; ++j) {
         const int s = j % S, a = j % kAbuf;
-        if (!mbar_wait(smem_addr(&afull[a]), (j / kAbuf) & 1, p.status, kStatusTimeoutMma) ||
-            !mbar_wait(smem_addr(&full[s]), (j / S) & 1, p.status, kStatusTimeoutMma)) {
+        // the dequant warps arrive on afull only after waiting for this stage's full barrier, so
+        // afull also orders the activation tile the MMAs read
+        if (!mbar_wait(smem_addr(&afull[a]), (j / kAbuf) & 1, p.status, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
@@ -321,28 +323,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t m = m0 + t / kThreadsPerRow;
         const int64_t nb = n0 + (t % kThreadsPerRow) * kCols;
         if (m < p.M) {
-          float acc[kCols];
-#pragma unroll
-          for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
-          for (int sp = 0; sp < p.splits; ++sp) {
-            const float4* src = reinterpret_cast<const float4*>(p.slabs + (static_cast<int64_t>(sp) * p.M + m) * p.N + nb);
-#pragma unroll
-            for (int i = 0; i < kCols / 4; ++i) {
-              const float4 v = __ldcg(src + i);
-              acc[4 * i] += v.x;
-              acc[4 * i + 1] += v.y;
-              acc[4 * i + 2] += v.z;
-              acc[4 * i + 3] += v.w;
-            }
-          }
           uint4* dst = reinterpret_cast<uint4*>(p.y + m * p.N + nb);
+#pragma unroll 1
+          for (int c8 = 0; c8 < kCols; c8 += 8) {
+            // all splits' loads of these 8 columns are issued before any is summed
+            float4 va[kMaxSplits], vb[kMaxSplits];
 #pragma unroll
-          for (int i = 0; i < kCols / 8; ++i) {
+            for (int sp = 0; sp < kMaxSplits; ++sp) {
+              if (sp < p.splits) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(p.slabs + (static_cast<int64_t>(sp) * p.M + m) * p.N + nb + c8);
+                va[sp] = __ldcg(src);
+                vb[sp] = __ldcg(src + 1);
+              }
+            }
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplits; ++sp) {
+              if (sp < p.splits) {
+                acc[0] += va[sp].x; acc[1] += va[sp].y; acc[2] += va[sp].z; acc[3] += va[sp].w;
+                acc[4] += vb[sp].x; acc[5] += vb[sp].y; acc[6] += vb[sp].z; acc[7] += vb[sp].w;
+              }
+            }
             uint32_t o[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              o[q] = f32_to_bf16_bits(acc[8 * i + 2 * q]) | (f32_to_bf16_bits(acc[8 * i + 2 * q + 1]) << 16);
-            dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int q = 0; q < 4; ++q) o[q] = f32_to_bf16_bits(acc[2 * q]) | (f32_to_bf16_bits(acc[2 * q + 1]) << 16);
+            dst[c8 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
       }
@@ -357,58 +363,103 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr int kPrepChunk = 1024;  // K per prep CTA
+constexpr int kPrepK = 128;   // K per prep CTA
+constexpr int kPrepM = 64;    // activation rows per prep CTA
+constexpr int kPrepPad = 8;   // bf16 row padding (conflict-free ldmatrix)
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
 // Prep: x_perm (K permuted inside groups of 8 as 0,4,1,5,2,6,3,7) and the LoRA down-projection
-// U = bf16(x A^T). CTA (chunk, m) handles 1024 K of row m: it writes that slice of x_perm and
-// adds its partial dot products into the fp32 accumulator U32 (zeroed by the caller); the last
-// chunk of a row (per-row arrival counter) converts the row of U to bf16.
-__global__ void __launch_bounds__(128) w4a16_prep_kernel(const uint16_t* __restrict__ x, int64_t K,
+// U = bf16(x A^T). CTA (k chunk, row tile) stages a 64 x 128 slice of x and a 32 x 128 slice of A
+// in shared memory, writes its slice of x_perm, and runs the small GEMM on mma.sync (warp w:
+// rows 16w..16w+15, 32 ranks per pass); partial sums go to the fp32 accumulator U32 (zeroed by
+// the caller); the last chunk of a row tile (arrival counter) converts its rows of U to bf16.
+__global__ void __launch_bounds__(128) w4a16_prep_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                          const uint16_t* __restrict__ A, int r,
                                                          uint16_t* __restrict__ xp, float* __restrict__ U32,
-                                                         uint16_t* __restrict__ U, uint32_t* __restrict__ rowcnt) {
-  const int64_t m = blockIdx.y;
-  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * (kPrepChunk / 8);
-  const int64_t v1 = min(K / 8, v0 + kPrepChunk / 8);
-  const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
-  uint4* pr = reinterpret_cast<uint4*>(xp + m * K);
-  for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-    const uint4 a = xr[v];
-    // elements e0..e7 (two per word) -> e0 e4 | e1 e5 | e2 e6 | e3 e7
-    uint4 o;
-    o.x = __byte_perm(a.x, a.z, 0x5410);
-    o.y = __byte_perm(a.x, a.z, 0x7632);
-    o.z = __byte_perm(a.y, a.w, 0x5410);
-    o.w = __byte_perm(a.y, a.w, 0x7632);
-    pr[v] = o;
+                                                         uint16_t* __restrict__ U, uint32_t* __restrict__ tilecnt) {
+  __shared__ __align__(16) uint16_t xs[kPrepM][kPrepK + kPrepPad];
+  __shared__ __align__(16) uint16_t as[32][kPrepK + kPrepPad];
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kPrepM;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.x) * kPrepK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // 64 rows x 16 vectors of 8 bf16: 8 per thread
+#pragma unroll
+  for (int i = 0; i < (kPrepM * kPrepK / 8) / 128; ++i) {
+    const int idx = tid + i * 128, row = idx >> 4, vec = idx & 15;
+    const int64_t m = m0 + row;
+    uint4 a = make_uint4(0, 0, 0, 0);
+    if (m < M) {
+      a = *reinterpret_cast<const uint4*>(x + m * K + k0 + vec * 8);
+      uint4 o;  // elements e0..e7 (two per word) -> e0 e4 | e1 e5 | e2 e6 | e3 e7
+      o.x = __byte_perm(a.x, a.z, 0x5410);
+      o.y = __byte_perm(a.x, a.z, 0x7632);
+      o.z = __byte_perm(a.y, a.w, 0x5410);
+      o.w = __byte_perm(a.y, a.w, 0x7632);
+      *reinterpret_cast<uint4*>(xp + m * K + k0 + vec * 8) = o;
+    }
+    *reinterpret_cast<uint4*>(&xs[row][vec * 8]) = a;
   }
   if (r == 0) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int j = warp; j < r; j += 4) {
-    const uint4* ar = reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j) * K);
-    float acc = 0.0f;
-#pragma unroll 4
-    for (int64_t v = v0 + lane; v < v1; v += 32) {
-      const uint4 xv = xr[v], av = __ldg(ar + v);
-      const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w}, aq[4] = {av.x, av.y, av.z, av.w};
+  for (int j0 = 0; j0 < r; j0 += 32) {
+    __syncthreads();
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        acc = fmaf(__uint_as_float(bf16_lo_bits(xq[t])), __uint_as_float(bf16_lo_bits(aq[t])), acc);
-        acc = fmaf(__uint_as_float(bf16_hi_bits(xq[t])), __uint_as_float(bf16_hi_bits(aq[t])), acc);
+    for (int i = 0; i < (32 * kPrepK / 8) / 128; ++i) {
+      const int idx = tid + i * 128, jr = idx >> 4, vec = idx & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (j0 + jr < r) v = __ldg(reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j0 + jr) * K + k0 + vec * 8));
+      *reinterpret_cast<uint4*>(&as[jr][vec * 8]) = v;
+    }
+    __syncthreads();
+    float c[4][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < kPrepK / 16; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&xs[warp * 16 + (lane & 15)][ks * 16 + (lane >> 4) * 8])),
+              a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {
+        const int q = lane >> 3;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&as[jp * 16 + (q >> 1) * 8 + (lane & 7)][ks * 16 + (q & 1) * 8])),
+                b0, b1, b2, b3);
+        mma16816(c[2 * jp], a, b0, b1);
+        mma16816(c[2 * jp + 1], a, b2, b3);
       }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) atomicAdd(U32 + m * r + j, acc);
+    // C fragment: c0,c1 at (row lane/4, cols 2(lane%4), +1); c2,c3 at row + 8
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t m = m0 + warp * 16 + (lane >> 2) + (q >> 1) * 8;
+        const int j = j0 + nt * 8 + 2 * (lane & 3) + (q & 1);
+        if (m < M && j < r) atomicAdd(U32 + m * r + j, c[nt][q]);
+      }
   }
   __threadfence();
   __syncthreads();
   __shared__ uint32_t last;
-  if (threadIdx.x == 0) last = (atomicAdd(rowcnt + m, 1u) == gridDim.x - 1) ? 1u : 0u;
+  if (tid == 0) last = (atomicAdd(tilecnt + blockIdx.y, 1u) == gridDim.x - 1) ? 1u : 0u;
   __syncthreads();
   if (last) {
     __threadfence();
-    for (int j = threadIdx.x; j < r; j += blockDim.x)
-      U[m * r + j] = static_cast<uint16_t>(f32_to_bf16_bits(__ldcg(U32 + m * r + j)));
+    for (int i = tid; i < kPrepM * r; i += blockDim.x) {
+      const int64_t m = m0 + i / r;
+      if (m < M) U[m * r + i % r] = static_cast<uint16_t>(f32_to_bf16_bits(__ldcg(U32 + m * r + i % r)));
+    }
   }
 }
 
@@ -449,7 +500,7 @@ TcPlan plan(int64_t M, int64_t N, int64_t K, int r, int sm_count) {
   t.tiles_n = static_cast<int>(N / kRows);
   const int kst = static_cast<int>(K / kKStage);
   const int ctas = t.tiles_n * t.tiles_m;
-  int splits = std::max(1, std::min(kst, sm_count / std::max(1, ctas)));
+  int splits = std::max(1, std::min({kst, sm_count / std::max(1, ctas), kMaxSplits}));
   t.stages_per_split = (kst + splits - 1) / splits;
   t.splits = (kst + t.stages_per_split - 1) / t.stages_per_split;
   const size_t lora = r ? static_cast<size_t>(kRows + t.mbox) * 2 * r : 0;
@@ -513,8 +564,8 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   float* slabs = reinterpret_cast<float*>(base + t.ws_slabs);
 
   if (cudaMemsetAsync(base + t.ws_zero, 0, t.zero_bytes, st) != cudaSuccess) return NVFP4RL_ERR_CUDA;
-  dim3 pgrid(static_cast<unsigned>((a.K + kPrepChunk - 1) / kPrepChunk), static_cast<unsigned>(a.M));
-  w4a16_prep_kernel<<<pgrid, 128, 0, st>>>(a.x, a.K, a.A, a.r, xp, reinterpret_cast<float*>(base + t.ws_u32), U,
+  dim3 pgrid(static_cast<unsigned>(a.K / kPrepK), static_cast<unsigned>((a.M + kPrepM - 1) / kPrepM));
+  w4a16_prep_kernel<<<pgrid, 128, 0, st>>>(a.x, a.M, a.K, a.A, a.r, xp, reinterpret_cast<float*>(base + t.ws_u32), U,
                                            reinterpret_cast<uint32_t*>(base + t.ws_rowcnt));
   if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
 

@@ -11,9 +11,9 @@
 // Kernels:
 //   amax_kernel      one HBM read of x, 128-bit non-caching loads, packed 16-bit max
 //                    for bf16, warp/CTA reduction, one atomicMax per CTA.
-//   quantize_kernel  one thread per 16-element block: two (bf16) or four (fp32)
-//                    128-bit loads, the exact E4M3 scale byte, seven per-block
-//                    thresholds, and per element seven unsigned compares.
+//   quantize_kernel  one thread per 16-element block (two blocks in flight per thread):
+//                    two (bf16) or four (fp32) 128-bit loads, the exact E4M3 scale byte,
+//                    seven per-block thresholds, and per element seven unsigned compares.
 //
 // Exactness without division per element: for an fp32 value a and a real P,
 //   a > P  <=>  a > RD(P)      a >= P  <=>  a >= RU(P)
@@ -86,20 +86,31 @@ __global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, i
   uint32_t m = 0;
   const uint4* p = static_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // four 128-bit loads in flight per thread and iteration
+  constexpr int kU = 4;
   if (kDtype == NVFP4RL_BF16) {
     uint32_t m2 = 0;  // two running 16-bit maxima of |bf16| bit patterns
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-      const uint4 v = ld_nc_v4(p + i);
-      m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += kU * stride) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) v[u] = (i + u * stride < nvec) ? ld_nc_v4(p + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        m2 = __vmaxu2(m2, v[u].x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[u].y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[u].z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[u].w & 0x7FFF7FFFu);
+      }
     }
     m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
   } else {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-      const uint4 v = ld_nc_v4(p + i);
-      m = max(m, max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu)));
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += kU * stride) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) v[u] = (i + u * stride < nvec) ? ld_nc_v4(p + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        m = max(m, max(max(v[u].x & 0x7FFFFFFFu, v[u].y & 0x7FFFFFFFu), max(v[u].z & 0x7FFFFFFFu, v[u].w & 0x7FFFFFFFu)));
     }
   }
   m = __reduce_max_sync(0xFFFFFFFFu, m);
@@ -111,6 +122,168 @@ __global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, i
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if (threadIdx.x == 0) atomicMax(amax_bits, m);
   }
+}
+
+// Raw 128-bit words of one 16-element block: 2 (bf16) or 4 (fp32).
+template <int kDtype>
+struct BlockWords {
+  uint4 v[kDtype == NVFP4RL_BF16 ? 2 : 4];
+};
+
+template <int kDtype>
+__device__ __forceinline__ void load_block(const void* __restrict__ x, int64_t blk, BlockWords<kDtype>& w) {
+  const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(x) +
+                                                  blk * 16 * (kDtype == NVFP4RL_BF16 ? 2 : 4));
+#pragma unroll
+  for (int q = 0; q < (kDtype == NVFP4RL_BF16 ? 2 : 4); ++q) w.v[q] = ld_nc_v4(p + q);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_gt(uint32_t a, uint32_t b) {  // per half: 1.0 if a > b else 0.0
+  uint32_t d;
+  asm("set.gt.bf16x2.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// bf16 pattern of the largest bf16 <= v (v >= 0 finite fp32): truncation.
+__device__ __forceinline__ uint32_t bf16_rd(float v) { return __float_as_uint(v) >> 16; }
+// bf16 pattern of the smallest bf16 >= v (v >= 0 finite fp32).
+__device__ __forceinline__ uint32_t bf16_ru(float v) { return (__float_as_uint(v) + 0xFFFFu) >> 16; }
+
+// Plain encoding of one block of bf16 values, two elements per instruction. For bf16 x and a
+// real P: x > P <=> x > RD_bf16(P) and x >= P <=> x > pred(RU_bf16(P)), with RD_bf16(P) =
+// RD_bf16(RD_fp32(P)) and RU_bf16(P) = RU_bf16(RU_fp32(P)); so the seven midpoint thresholds
+// become bf16 values compared with set.gt.bf16x2, and the magnitude code is the number of
+// thresholds exceeded, accumulated with add.bf16x2 on 128.0 (128 + c is exact and its low
+// three bits are c).
+__device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
+                                                  float est_scale, uint8_t* __restrict__ codes,
+                                                  uint8_t* __restrict__ scales) {
+  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+  uint32_t aw[8];
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    aw[i] = w[i] & 0x7FFF7FFFu;
+    m2 = __vmaxu2(m2, aw[i]);
+  }
+  const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+  uint32_t b = 0;
+  if (g > 0.0f) b = scale_byte(bamax, g, (bamax * est_scale) * inv_g6);
+  const float dec = e4m3_decode_pos(b);
+  uint32_t t2[7];
+  if (b) {
+    const uint32_t t[7] = {bf16_rd(__fmul_rd(0.25f * dec, g)), bf16_ru(__fmul_ru(0.75f * dec, g)) - 1u,
+                           bf16_rd(__fmul_rd(1.25f * dec, g)), bf16_ru(__fmul_ru(1.75f * dec, g)) - 1u,
+                           bf16_rd(__fmul_rd(2.5f * dec, g)),  bf16_ru(__fmul_ru(3.5f * dec, g)) - 1u,
+                           bf16_rd(__fmul_rd(5.0f * dec, g))};
+#pragma unroll
+    for (int k = 0; k < 7; ++k) t2[k] = t[k] | (t[k] << 16);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 7; ++k) t2[k] = 0x7F807F80u;  // zero scale: every code is sign|0
+  }
+  uint32_t byte[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t acc = 0x43004300u;  // bf16x2 (128, 128)
+#pragma unroll
+    for (int k = 0; k < 7; ++k) acc = bf16x2_add(acc, bf16x2_gt(aw[i], t2[k]));
+    const uint32_t m = acc & 0x00070007u;
+    const uint32_t s = w[i] & 0x80008000u;
+    // low byte: magnitude of element 2i in bits 0-2, its sign in bit 3, element 2i+1 in bits 4-7
+    byte[i] = m | (m >> 12) | (s >> 12) | (s >> 24);
+  }
+  const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
+  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo, hi);
+  scales[blk] = static_cast<uint8_t>(b);
+}
+
+// Scale byte and codes of one block, written to scales[blk] and codes[8 blk .. 8 blk + 7].
+template <int kDtype, bool kGuided>
+__device__ __forceinline__ void encode_block(const BlockWords<kDtype>& w, int64_t blk, float g, float est_scale,
+                                             float g6, const uint32_t* __restrict__ mask,
+                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  uint32_t ax[16];
+  uint32_t sgn = 0;
+  if (kDtype == NVFP4RL_BF16) {
+    const uint32_t words[8] = {w.v[0].x, w.v[0].y, w.v[0].z, w.v[0].w, w.v[1].x, w.v[1].y, w.v[1].z, w.v[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = words[i] << 16, hi = words[i] & 0xFFFF0000u;
+      ax[2 * i] = lo & 0x7FFFFFFFu;
+      ax[2 * i + 1] = hi & 0x7FFFFFFFu;
+      sgn |= ((lo >> 31) << (2 * i)) | ((hi >> 31) << (2 * i + 1));
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t words[4] = {w.v[q].x, w.v[q].y, w.v[q].z, w.v[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ax[4 * q + i] = words[i] & 0x7FFFFFFFu;
+        sgn |= (words[i] >> 31) << (4 * q + i);
+      }
+    }
+  }
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mx = max(mx, ax[i]);
+  const float bamax = __uint_as_float(mx);
+
+  uint32_t b = 0;
+  if (g > 0.0f) b = scale_byte(bamax, g, __fdiv_rn(bamax * est_scale, g6));
+  const float dec = e4m3_decode_pos(b);
+
+  uint32_t lo32 = 0, hi32 = 0;
+  if (!kGuided) {
+    uint32_t th[7];
+    plain_thresholds(dec, g, th);
+    if (b == 0) {
+#pragma unroll
+      for (int k = 0; k < 7; ++k) th[k] = 0x7F800000u;  // zero scale: every code is sign|0
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint32_t mag = 0;
+#pragma unroll
+      for (int k = 0; k < 7; ++k) mag += ax[i] > th[k] ? 1u : 0u;
+      const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
+      if (i < 8) lo32 |= code << (4 * i);
+      else hi32 |= code << (4 * (i - 8));
+    }
+  } else {
+    uint32_t ge[7], gt[7];
+    guided_thresholds(dec, g, ge, gt);
+    const uint32_t up_bits = (mask[blk >> 1] >> ((blk & 1) * 16)) & (b ? 0xFFFFu : 0u);
+    if (b == 0) {
+#pragma unroll
+      for (int k = 0; k < 7; ++k) ge[k] = gt[k] = 0x7F800000u;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint32_t c_ge = 0, c_gt = 0;
+#pragma unroll
+      for (int k = 0; k < 7; ++k) {
+        c_ge += ax[i] > ge[k] ? 1u : 0u;
+        c_gt += ax[i] > gt[k] ? 1u : 0u;
+      }
+      const bool on_grid = (c_ge != c_gt) || ax[i] == 0u;
+      const uint32_t up = (up_bits >> i) & 1u;
+      const uint32_t mag = (c_ge == 7u) ? 7u : c_ge + ((up && !on_grid) ? 1u : 0u);
+      const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
+      if (i < 8) lo32 |= code << (4 * i);
+      else hi32 |= code << (4 * (i - 8));
+    }
+  }
+  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo32, hi32);
+  scales[blk] = static_cast<uint8_t>(b);
 }
 
 template <int kDtype, bool kGuided>
@@ -128,122 +301,22 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   const bool tiny = g < 0x1p-60f;
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float g6 = 6.0f * (g * est_scale);
+  const float inv_g6 = 1.0f / g6;
 
+  // two blocks per iteration, both loaded before either is encoded (more bytes in flight)
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < nblocks; blk += stride) {
-    uint32_t ax[16];
-    uint32_t sgn = 0;
-    if (kDtype == NVFP4RL_BF16) {
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + blk * 16);
-      const uint4 v0 = ld_nc_v4(p), v1 = ld_nc_v4(p + 1);
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t lo = w[i] << 16, hi = w[i] & 0xFFFF0000u;
-        ax[2 * i] = lo & 0x7FFFFFFFu;
-        ax[2 * i + 1] = hi & 0x7FFFFFFFu;
-        sgn |= ((lo >> 31) << (2 * i)) | ((hi >> 31) << (2 * i + 1));
-      }
+  for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < nblocks; blk += 2 * stride) {
+    const int64_t blk2 = blk + stride;
+    BlockWords<kDtype> a, b;
+    load_block<kDtype>(x, blk, a);
+    if (blk2 < nblocks) load_block<kDtype>(x, blk2, b);
+    if constexpr (kDtype == NVFP4RL_BF16 && !kGuided) {
+      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, codes, scales);
+      if (blk2 < nblocks) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, codes, scales);
     } else {
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(x) + blk * 16);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = ld_nc_v4(p + q);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          ax[4 * q + i] = w[i] & 0x7FFFFFFFu;
-          sgn |= (w[i] >> 31) << (4 * q + i);
-        }
-      }
+      encode_block<kDtype, kGuided>(a, blk, g, est_scale, g6, mask, codes, scales);
+      if (blk2 < nblocks) encode_block<kDtype, kGuided>(b, blk2, g, est_scale, g6, mask, codes, scales);
     }
-    uint32_t mx = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mx = max(mx, ax[i]);
-    const float bamax = __uint_as_float(mx);
-
-    uint32_t b = 0;
-    if (g > 0.0f) b = scale_byte(bamax, g, __fdiv_rn(bamax * est_scale, g6));
-    const float dec = e4m3_decode_pos(b);
-
-    uint32_t lo32 = 0, hi32 = 0;
-    if (!kGuided) {
-      // Fast path: t = |x| * fl(1 / fl(dec g)) differs from the exact quotient by at most 3 ulps,
-      // so the hardware round-to-nearest E2M1 conversion of t decides exactly unless t lies
-      // within 8 ulps of a multiple of a quarter of its binade (every decision boundary
-      // 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 is such a point). Such blocks, zero scales and
-      // scales far from 1 take the exact threshold path below.
-      const float S = dec * g;
-      bool exact = (b == 0) || !(S >= 0x1p-100f && S <= 0x1p100f);
-      if (!exact) {
-        const float inv = __frcp_rn(S);
-        uint32_t near = 0xFFFFFFFFu;
-        uint32_t mags[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float t0 = __uint_as_float(ax[2 * i]) * inv, t1 = __uint_as_float(ax[2 * i + 1]) * inv;
-          near = min(near, (__float_as_uint(t0) + 8u) & 0x1FFFFFu);
-          near = min(near, (__float_as_uint(t1) + 8u) & 0x1FFFFFu);
-          uint16_t pair;  // code(t1) in the high nibble, code(t0) in the low nibble
-          asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.u16.u8 %0, q;\n\t}"
-              : "=h"(pair)
-              : "f"(t1), "f"(t0));
-          mags[i] = pair & 0x77u;
-        }
-        exact = near < 16u;
-        if (!exact) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t code2 = mags[i] | (((sgn >> (2 * i)) & 1u) << 3) | (((sgn >> (2 * i + 1)) & 1u) << 7);
-            if (i < 4) lo32 |= code2 << (8 * i);
-            else hi32 |= code2 << (8 * (i - 4));
-          }
-        }
-      }
-      if (exact) {
-        uint32_t th[7];
-        plain_thresholds(dec, g, th);
-        if (b == 0) {
-#pragma unroll
-          for (int k = 0; k < 7; ++k) th[k] = 0x7F800000u;  // zero scale: every code is sign|0
-        }
-        lo32 = hi32 = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          uint32_t mag = 0;
-#pragma unroll
-          for (int k = 0; k < 7; ++k) mag += ax[i] > th[k] ? 1u : 0u;
-          const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
-          if (i < 8) lo32 |= code << (4 * i);
-          else hi32 |= code << (4 * (i - 8));
-        }
-      }
-    } else {
-      uint32_t ge[7], gt[7];
-      guided_thresholds(dec, g, ge, gt);
-      const uint32_t up_bits = (mask[blk >> 1] >> ((blk & 1) * 16)) & (b ? 0xFFFFu : 0u);
-      if (b == 0) {
-#pragma unroll
-        for (int k = 0; k < 7; ++k) ge[k] = gt[k] = 0x7F800000u;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        uint32_t c_ge = 0, c_gt = 0;
-#pragma unroll
-        for (int k = 0; k < 7; ++k) {
-          c_ge += ax[i] > ge[k] ? 1u : 0u;
-          c_gt += ax[i] > gt[k] ? 1u : 0u;
-        }
-        const bool on_grid = (c_ge != c_gt) || ax[i] == 0u;
-        const uint32_t up = (up_bits >> i) & 1u;
-        const uint32_t mag = (c_ge == 7u) ? 7u : c_ge + ((up && !on_grid) ? 1u : 0u);
-        const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
-        if (i < 8) lo32 |= code << (4 * i);
-        else hi32 |= code << (4 * (i - 8));
-      }
-    }
-    *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo32, hi32);
-    scales[blk] = static_cast<uint8_t>(b);
   }
 }
 
