@@ -196,6 +196,30 @@ NVFP4RL_API const char* nvfp4rl_status_string(nvfp4rl_status status);
 NVFP4RL_API nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t clear);
 
 /*
+ * nvfp4_lora_linear_noalloc -- nvfp4_lora_linear without a caller-supplied workspace, for
+ *   callers that cannot allocate device memory (code inside another framework's memory
+ *   planner, restricted runtimes that forbid cudaMalloc, code that must not grow its device
+ *   footprint after start-up). The pages have no counterpart: this is a deployment entry
+ *   point of this library, not part of the method.
+ *   Same arguments and result as nvfp4_lora_linear (dense only). The scratch lives in a fixed
+ *   array of nvfp4rl_noalloc_scratch_bytes() (16 MiB) that every GPU loading this library
+ *   holds until the process exits. Nothing is allocated by the call.
+ *   - Returns NVFP4RL_ERR_WORKSPACE when the problem needs more scratch than the array
+ *     (nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, ...) > 16 MiB).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the array and each overwrites it: calls that may overlap
+ *     on the GPU (unordered streams) race and must not be issued.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_noalloc(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
+                                                     const uint8_t* w_scales, const float* w_g, int64_t N,
+                                                     const uint16_t* lora_A, const uint16_t* lora_B, int32_t r,
+                                                     float s, uint16_t* y, void* stream);
+
+/* Bytes of the fixed scratch array nvfp4_lora_linear_noalloc uses (16 MiB). Host only. */
+NVFP4RL_API size_t nvfp4rl_noalloc_scratch_bytes(void);
+
+/*
  * nvfp4rl_kernel_launches -- diagnostic: number of kernels this library has
  *   launched in this process (all devices, all streams). Host only.
  */

@@ -42,6 +42,8 @@ def _signatures():
         "rmsnorm_aqn": (c.c_int, [p, i64, i64, p, p, f32, f32, p, p]),
         "nvfp4_lora_linear": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
         "nvfp4_lora_linear_w4a4": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
+        "nvfp4_lora_linear_noalloc": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, p]),
+        "nvfp4rl_noalloc_scratch_bytes": (sz, []),
         "nvfp4rl_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
         "nvfp4rl_status_string": (c.c_char_p, [c.c_int]),
         "nvfp4rl_device_status": (c.c_int, [p, i32]),
@@ -229,3 +231,20 @@ def nvfp4_lora_linear_w4a4(x, codes, scales, g, A=None, B=None, s: float = 1.0, 
     with codes [G, N, K/2], scales [G, N, K/16], g [G]."""
     return _linear("nvfp4_lora_linear_w4a4", OP_LINEAR_W4A4, x, codes, scales, g, A, B, s, group_offsets,
                    num_groups, out, workspace, stream)
+
+
+def nvfp4_lora_linear_noalloc(x, codes, scales, g, A=None, B=None, s: float = 1.0, out=None, stream=None):
+    """W4A16 LoRA linear without a workspace argument, for callers that cannot allocate device memory:
+    the library's fixed 16 MiB device array serves as scratch (see include/nvfp4rl.h). Outputs are still
+    the caller's (allocated here with torch only when `out` is None)."""
+    import torch
+    _require_cuda(x, codes, scales, g, A, B)
+    _bits16(x), _bits16(A), _bits16(B)
+    M, K = x.shape
+    N = codes.shape[-2]
+    r = 0 if A is None else A.shape[0]
+    out = _empty((M, N), torch.bfloat16, x.device) if out is None else out
+    st = lib().nvfp4_lora_linear_noalloc(_ptr(x), M, K, _ptr(codes), _ptr(scales), _ptr(g), N, _ptr(A), _ptr(B), r,
+                                         float(s), _ptr(out), _stream(x, stream))
+    _check(st, "nvfp4_lora_linear_noalloc")
+    return out
