@@ -10,8 +10,8 @@ the path on that layer:
   2. the rollout weight refresh: per weight, the tensor amax and the NVFP4
      encoding (codes, E4M3 block scales, fp32 g);
   3. the five W4A16 LoRA linears at M = 64.
-Inputs are synthetic, generated on the device from a seed, and larger than L2
-(the five bf16 weights are 458 MB); L2 is also flushed between steps.
+Inputs are synthetic, generated on the device from a seed, and larger than L2:
+every step streams the five bf16 weights (458 MB) and their NVFP4 codes (122 MB).
 
 Prints one JSON line. `value` is algorithmic bytes per step (what the method must
 move, each tensor once) over the device time of a step, summed over ranks.
@@ -239,10 +239,12 @@ def run_gpu(args):
     ops = ["rmsnorm_aqn", "rmsnorm_aqn_2"] + [f"amax_{n}" for n, _, _ in LINEARS] + \
           [f"quantize_{n}" for n, _, _ in LINEARS] + [f"linear_{n}" for n, _, _ in LINEARS]
 
-    def step(k, ev=None):
+    def step(k, ev=None, only=None):
         st = torch.cuda.current_stream(dev)
 
         def mark(name, fn):
+            if only is not None and name not in only:
+                return
             if ev is None:
                 fn()
                 return
@@ -268,43 +270,53 @@ def run_gpu(args):
     for i in range(2):
         step(i % (KSCHED + 1))
     torch.cuda.synchronize()
-    graphs = []
+    if args.op:
+        return run_ops(args, torch, step, ops, flush, stream, rank)
+    graphs, ev_graphs = [], []
     launches_per_step = None
     for k in range(KSCHED + 1):
-        ev = {name: (torch.cuda.Event(enable_timing=True, external=True),
-                     torch.cuda.Event(enable_timing=True, external=True)) for name in ops}
         g = torch.cuda.CUDAGraph()
         l0 = nv.kernel_launches()
         with torch.cuda.graph(g):
-            step(k, ev)
+            step(k)
         if launches_per_step is None:
             launches_per_step = nv.kernel_launches() - l0
-        graphs.append((g, ev))
+        graphs.append(g)
+        # the same step with CUDA events around every op, replayed only for the per-op breakdown
+        ev = {name: (torch.cuda.Event(enable_timing=True, external=True),
+                     torch.cuda.Event(enable_timing=True, external=True)) for name in ops}
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge):
+            step(k, ev)
+        ev_graphs.append((ge, ev))
     torch.cuda.synchronize()
     for i in range(args.warmup):
-        flush.zero_()
-        graphs[i % (KSCHED + 1)][0].replay()
+        graphs[i % (KSCHED + 1)].replay()
     torch.cuda.synchronize()
 
     bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    op_samples = {name: [] for name in ops}
-    step_ms = []
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(dev)
     pci = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    # Steps run back to back: every step streams 458 MB of bf16 weights and 122 MB of codes,
+    # several times the 129 MB L2, so nothing one step leaves in L2 serves the next.
     with ClockSampler(pci) as clocks:
         for i in range(args.steps):
-            flush.zero_()  # L2 flush between timed steps, outside the step's events
-            g, ev = graphs[i % (KSCHED + 1)]
             bounds[i][0].record(stream)
-            g.replay()
+            graphs[i % (KSCHED + 1)].replay()
             bounds[i][1].record(stream)
-            torch.cuda.synchronize()  # per-op events of this replay are read before the graph runs again
-            step_ms.append(bounds[i][0].elapsed_time(bounds[i][1]))
-            for name in ops:
-                op_samples[name].append(ev[name][0].elapsed_time(ev[name][1]))
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in bounds]
+    # per-op breakdown (not part of the timed region): event-instrumented replays
+    op_samples = {name: [] for name in ops}
+    for i in range(max(3, min(args.steps, 10))):
+        ge, ev = ev_graphs[i % (KSCHED + 1)]
+        ge.replay()
+        torch.cuda.synchronize()
+        for name in ops:
+            op_samples[name].append(ev[name][0].elapsed_time(ev[name][1]))
     launches = launches_per_step * args.steps
     if world > 1:
         dist.barrier()
@@ -370,7 +382,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, generated on device)",
-        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 and a 256 MB write between timed steps",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2: each step streams 458 MB of bf16 weights and 122 MB of NVFP4 codes (L2 129 MB); no flush",
                    "replicas": world, "algorithmic_bytes_per_step": sb},
         "parts": parts, "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clocks.summary(),
@@ -380,6 +392,52 @@ def run_gpu(args):
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def select_ops(spec, ops):
+    """--op names: op names of the step (e.g. linear_gate, amax_q, rmsnorm_aqn) or the groups
+    linears, amax, quantize, rmsnorm, all; comma-separated."""
+    groups = {"linears": [o for o in ops if o.startswith("linear_")], "amax": [o for o in ops if o.startswith("amax_")],
+              "quantize": [o for o in ops if o.startswith("quantize_")], "rmsnorm": [o for o in ops if "rmsnorm" in o],
+              "all": list(ops)}
+    out = []
+    for part in spec.split(","):
+        part = part.strip()
+        sel = groups.get(part, [part] if part in ops else None)
+        if sel is None:
+            raise SystemExit(f"unknown op {part!r}; ops: {', '.join(ops)}; groups: {', '.join(groups)}")
+        out += [o for o in sel if o not in out]
+    return out
+
+
+def run_ops(args, torch, step, ops, flush, stream, rank):
+    """Single-op timing (eager launches; before every op a 256 MB read evicts L2): W warm-up and K timed runs of
+    each selected op of the step; one JSON line of per-op device microseconds. Serves per-kernel
+    measurement and profiler captures of one op on the step's full-size inputs."""
+    sel = select_ops(args.op, ops)
+    flush64 = flush.view(torch.int64)
+
+    def evict():  # read a buffer twice the L2 size: L2 then holds clean lines only (no write-backs later)
+        flush64.sum()
+
+    res = {}
+    for name in sel:
+        for i in range(args.warmup):
+            evict()
+            step(i % (KSCHED + 1), only={name})
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(args.steps):
+            evict()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step(i % (KSCHED + 1), only={name})
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        res[name] = {"us_median": float(np.median(ts)), "us_min": float(np.min(ts)), "runs": len(ts)}
+    if rank == 0:
+        print(json.dumps({"mode": "ops", "workload": WORKLOAD, "steps": args.steps, "warmup": args.warmup, "ops": res}))
 
 
 def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, Q, Y, h1, h2, ws, flush, inputs,
@@ -438,10 +496,10 @@ def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
 
-def oracle_sample(seconds_budget: float):
-    """A bounded sample of the same step, run by the CPU oracle: RMSNorm of all 64 tokens, the NVFP4
-    encoding of a seeded 1/64 of each weight's rows, and every linear's outputs for 1/64 of its output
-    columns (all 64 tokens). Returns (algorithmic bytes of the sample, seconds, threads)."""
+def oracle_sample(den: int):
+    """A bounded sample of the same step, run by the CPU oracle: RMSNorm of all 64 tokens twice, the NVFP4
+    encoding of 1/den of each weight's rows, and every linear's outputs for those 1/den of its output rows
+    (all 64 tokens). Returns (algorithmic bytes of the sample, seconds, threads)."""
     import oracle
     import synth
     t_total, bytes_total = 0.0, 0.0
@@ -455,7 +513,7 @@ def oracle_sample(seconds_budget: float):
     t_total += time.perf_counter() - t0
     bytes_total += 2 * bytes_rmsnorm(M_TOK, HIDDEN)
     for i, (name, n, k) in enumerate(LINEARS):
-        rows = n // 64
+        rows = n // den
         Wb = synth.weight_bf16(rows, k, 0.02, 9, 10 + i, outlier_frac=0.01)
         t0 = time.perf_counter()
         codes, scales, g = oracle.quantize(Wb)
@@ -470,13 +528,26 @@ def oracle_sample(seconds_budget: float):
     return bytes_total, t_total, nthreads
 
 
-SAMPLE_DESC = ("RMSNorm-AQN of the 64x3584 tokens twice; NVFP4 encoding of 1/64 of each weight's rows; "
-               "each LoRA linear on 1/64 of its output columns for all 64 tokens (fp64 oracle)")
+def sample_den(seconds_budget: float) -> int:
+    """The smallest sampling denominator (1/den of every weight) whose oracle run fits the budget,
+    extrapolated from a 1/64 probe run."""
+    _, t64, _ = oracle_sample(64)
+    for den in (1, 2, 4, 8, 16, 32):
+        if t64 * 64 / den <= seconds_budget:
+            return den
+    return 64
+
+
+def sample_desc(den: int) -> str:
+    frac = "all" if den == 1 else f"1/{den}"
+    return (f"RMSNorm-AQN of the 64x3584 tokens twice; NVFP4 encoding of {frac} of each weight's rows; "
+            f"each LoRA linear on those rows' outputs for all 64 tokens (fp64 oracle)")
 
 
 def cpu_baseline(seconds_budget=20.0):
-    b, t, th = oracle_sample(seconds_budget)
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": SAMPLE_DESC,
+    den = sample_den(seconds_budget)
+    b, t, th = oracle_sample(den)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": sample_desc(den),
             "sample_seconds": t}
 
 
@@ -485,20 +556,23 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return
+    # each step is a sample sized so that warm-up and timed steps together take about two minutes
+    den = sample_den(120.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(0)
+        oracle_sample(den)
     tot_b, tot_t, th = 0.0, 0.0, 1
     for _ in range(args.steps):
-        b, t, th = oracle_sample(0)
+        b, t, th = oracle_sample(den)
         tot_b += b
         tot_t += t
     v = tot_b / tot_t / 1e9
+    desc = sample_desc(den)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_t / max(1, args.steps) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD, "sample": SAMPLE_DESC},
-        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": SAMPLE_DESC},
+        "config": {"workload": WORKLOAD, "sample": desc},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -512,6 +586,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--op", default=None, help="time single ops of the step instead (see select_ops)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -4,32 +4,44 @@
 // plus trainable LoRA factors, Y = x deq(W)^T + s (x A^T) B^T. In decode the layer is bound
 // by the HBM stream of 4-bit weights (0.5625 bytes per weight with the block scales).
 //
-// Structure (one CTA = 128 weight rows x one K range x up to 128 tokens):
+// One call = two kernels on the caller's stream:
+//   w4a16_lora_down_kernel  U = bf16(x A^T) for the LoRA up-projection: a cluster of CTAs
+//                           splits K, each runs mma.sync on its chunks, and the partial sums
+//                           meet in distributed shared memory (fixed order, no atomics).
+//   w4a16_tc_kernel         launched as a programmatic dependent of the first: it starts while
+//                           the LoRA-down runs and waits for it (griddepcontrol.wait) only
+//                           before loading U, after its whole weight stream has been issued.
+//
+// w4a16_tc_kernel (one CTA = 128 weight rows x one K range x up to 128 tokens):
 //   warp 0      TMA producer: per 256-K stage, the 128 x 128-byte code tile (128-byte
 //               swizzle), the 128 x 16-byte scale tile and the activation tile (4 boxes of
-//               64 bf16 x tokens, 128-byte swizzle) into a ring of shared-memory stages.
+//               64 bf16 x tokens, 128-byte swizzle, read straight from x) into a ring of
+//               shared-memory stages.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::f16 with A (the
 //               dequantized weights) in TMEM and B (activations) in shared memory, then the
 //               LoRA up-projection (B_lora tile x U^T) into a second accumulator.
 //   warps 2-9   dequantize: thread = one weight row and half of the stage's K; 4-bit codes
 //               are expanded to bf16 with integer ops (sign and magnitude bits moved into a
-//               bf16 bit pattern, then one bf16x2 FMA by E4M3(s) * 2^94), written to TMEM
-//               with tcgen05.st; then the epilogue: TMEM -> registers, g and s applied,
-//               bf16 stores (or fp32 split-K partial slabs, reduced by the last CTA).
+//               bf16 bit pattern, one bf16x2 FMA by E4M3(s) * 2^94, a byte permute into K
+//               order), written to TMEM with tcgen05.st; then the epilogue: TMEM -> registers,
+//               g and s applied, bf16 stores.
+// When K is split across CTAs, the CTAs of one output tile form a cluster: each leaves its
+// fp32 partial tile in its own shared memory, and after a cluster barrier each CTA sums one
+// slice of the tokens over all partials (in split order) through distributed shared memory.
 //
 // The bf16 pattern of a code magnitude m = (e1 e0 m0) placed in bits 8..6 is the value
 // grid(m) * 2^-126 (a subnormal when e = 0), so multiplying by E4M3(s) * 2^94 gives
 // grid(m) * E4M3(s) * 2^-32 exactly (at most 6 significant bits); the epilogue multiplies
 // the fp32 accumulator by 2^32 and then by g. A code word's nibbles j and j+4 (16 bits
-// apart) share their shifts, so each 32-bit TMEM column holds elements (8q+j, 8q+j+4);
-// the activations are stored with the same permutation of K inside each group of 8
-// (the product over K is unchanged), written by the prep kernel next to the LoRA
-// down-projection U = x A^T.
+// apart) share their shifts, so they are expanded together and then re-paired by byte
+// permutes into the K order (2c, 2c+1) of TMEM column c.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -45,19 +57,23 @@ constexpr int kCodeBytes = kRows * kKStage / 2;   // 16 KB
 constexpr int kScaleBytes = kRows * kKStage / 16;  // 2 KB
 constexpr int kThreads = 320;     // 10 warps
 constexpr int kDeqWarps = 8;
-constexpr int kMaxSplits = 8;     // split-K factor cap (the last CTA keeps one load per split in flight)
+constexpr int kMaxSplits = 8;     // split-K factor cap = the portable cluster size
+
+constexpr int kDownK = 128;       // K per LoRA-down chunk
+constexpr int kDownM = 64;        // activation rows per LoRA-down cluster
+constexpr int kDownPad = 8;       // bf16 row padding (conflict-free ldmatrix)
+constexpr int kDownCluster = 8;   // CTAs per LoRA-down cluster (K split)
+constexpr int kDownSmem = (kDownM + 32) * (kDownK + kDownPad) * 2 + kDownM * 32 * 4;
 
 struct TcParams {
   int64_t M, N, K;
   int stages_per_split;  // 256-K stages per CTA
-  int splits;
+  int splits;            // CTAs per cluster along K (1: no split)
   int r;                 // LoRA rank (0 or a multiple of 16)
   int lora_box_bytes;    // min(2r, 128)
   float s;
   const float* w_g;
   uint16_t* y;
-  float* slabs;          // [splits][M][N] fp32 when splits > 1
-  uint32_t* counters;    // [tiles_m * tiles_n]
   uint32_t* status;
   int smem_stages;
 };
@@ -76,24 +92,57 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Four TMEM columns from one word of 8 codes: column j = (code j, code j+4), each a bf16
-// pattern of grid(m) * 2^-126 with the code's sign, times the bf16x2 scale.
+// Four TMEM columns from one word of 8 codes (K order e0..e7): column c = (e_2c, e_2c+1),
+// each a bf16 of grid(m) * E4M3(s) * 2^-32 with the code's sign (scale2 = E4M3(s) * 2^94).
 __device__ __forceinline__ void expand_word(uint32_t w, uint32_t scale2, uint32_t* out) {
+  // swap nibbles 1<->4 and 3<->6 (one delta swap): nibbles p and p+4 of v, 16 bits apart,
+  // are then the K-adjacent pairs (e0, e1), (e4, e5), (e2, e3), (e6, e7) for p = 0..3
+  const uint32_t t = (w ^ (w >> 12)) & 0x0000F0F0u;
+  const uint32_t v = w ^ t ^ (t << 12);
   const uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u;
-  const uint32_t p0 = ((w << 6) & kMag) | ((w << 12) & kSign);
-  const uint32_t p1 = ((w << 2) & kMag) | ((w << 8) & kSign);
-  const uint32_t p2 = ((w >> 2) & kMag) | ((w << 4) & kSign);
-  const uint32_t p3 = ((w >> 6) & kMag) | (w & kSign);
-  out[0] = bf16x2_mul(p0, scale2);
-  out[1] = bf16x2_mul(p1, scale2);
-  out[2] = bf16x2_mul(p2, scale2);
-  out[3] = bf16x2_mul(p3, scale2);
+  out[0] = bf16x2_mul(((v << 6) & kMag) | ((v << 12) & kSign), scale2);  // (e0, e1)
+  out[2] = bf16x2_mul(((v << 2) & kMag) | ((v << 8) & kSign), scale2);   // (e4, e5)
+  out[1] = bf16x2_mul(((v >> 2) & kMag) | ((v << 4) & kSign), scale2);   // (e2, e3)
+  out[3] = bf16x2_mul(((v >> 6) & kMag) | (v & kSign), scale2);          // (e6, e7)
 }
 
-// bf16x2 of E4M3(s) * 2^94 (exact: at most 4 significant bits).
+// bf16x2 of E4M3(s) * 2^94 for a normal scale byte s (8 <= s <= 0x7E): the bf16 bits are
+// (s << 4) + (214 << 7), i.e. exponent e + 214 and mantissa m << 4; one multiply-add writes
+// both halves.
+__device__ __forceinline__ uint32_t scale_bf16x2_normal(uint32_t s) { return (s & 0x7Fu) * 0x00100010u + 0x6B006B00u; }
+
+// bf16x2 of E4M3(s) * 2^94 for any scale byte (exact: at most 4 significant bits).
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t s) {
   const uint32_t b = __float_as_uint(e4m3_decode_pos(s & 0x7Fu) * 0x1p94f) >> 16;
   return b | (b << 16);
+}
+
+// True when any of the eight scale bytes is below 8 (zero or subnormal E4M3).
+__device__ __forceinline__ bool has_small_scale(uint2 sc) {
+  const uint32_t y0 = sc.x & 0x78787878u, y1 = sc.y & 0x78787878u;
+  return (((y0 - 0x01010101u) & ~y0) | ((y1 - 0x01010101u) & ~y1)) & 0x80808080u;
+}
+
+// Dequantizes one thread's half-stage (row `row`, 128 K) into TMEM columns `col0`..`col0`+63.
+template <bool kAnyScale>
+__device__ __forceinline__ void dequant_half_stage(const uint8_t* crow, int row, int half, uint2 sc, uint32_t taddr) {
+  const uint32_t sbytes[2] = {sc.x, sc.y};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // 16-byte chunk = 32 codes = two MMA K-steps
+    const int chunk = half * 4 + c;
+    const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((chunk ^ (row & 7)) << 4));
+    const uint32_t b0 = (sbytes[c >> 1] >> (16 * (c & 1))) & 0xFFu;
+    const uint32_t b1 = (sbytes[c >> 1] >> (16 * (c & 1) + 8)) & 0xFFu;
+    const uint32_t s0 = kAnyScale ? scale_bf16x2(b0) : scale_bf16x2_normal(b0);
+    const uint32_t s1 = kAnyScale ? scale_bf16x2(b1) : scale_bf16x2_normal(b1);
+    uint32_t col[8];
+    expand_word(cw.x, s0, col);
+    expand_word(cw.y, s0, col + 4);
+    tmem_st8(taddr + chunk * 16, col);
+    expand_word(cw.z, s1, col);
+    expand_word(cw.w, s1, col + 4);
+    tmem_st8(taddr + chunk * 16 + 8, col);
+  }
 }
 
 template <int MBOX>
@@ -107,23 +156,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kAbuf = MBOX <= 64 ? 3 : 2;
   constexpr uint32_t kDcol = 0, kLcol = MBOX, kAcol0 = 2 * MBOX;
 
-  // layout: stages | lora A tile | lora U tile | barriers
+  // layout: stages (reused as the fp32 partial tile after the K loop) | lora A tile | lora U tile | barriers
   const int sb = stage_bytes(MBOX);
   uint8_t* lora_a = smem + S * sb;
   const int lora_a_bytes = p.r ? kRows * 2 * p.r : 0;
   uint8_t* lora_u = lora_a + lora_a_bytes;
   const int lora_u_bytes = p.r ? MBOX * 2 * p.r : 0;
   uint64_t* bars = reinterpret_cast<uint64_t*>(lora_u + lora_u_bytes);
-  // full[S], empty[S], afull[kAbuf], aempty[kAbuf], dfull, lfull, drain
+  // full[S], empty[S], afull[kAbuf], aempty[kAbuf], dfull, lfull
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* afull = empty + S;
   uint64_t* aempty = afull + kAbuf;
   uint64_t* dfull = aempty + kAbuf;
   uint64_t* lfull = dfull + 1;
-  uint64_t* drain = lfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile uint32_t* last_flag = tmem_slot + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lfull + 1);
+  float* part = reinterpret_cast<float*>(smem);  // [MBOX][kRows] fp32 partial tile (split K)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, split = blockIdx.y, tile_m = blockIdx.z;
@@ -144,8 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_addr(dfull), 1);
     mbar_init(smem_addr(lfull), 1);
-    mbar_init(smem_addr(drain), 1);
-    *last_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 512);
@@ -161,17 +207,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&map_codes);
       prefetch_tensormap(&map_scales);
       prefetch_tensormap(&map_x);
+      const int nbox = do_lora ? 2 * p.r / p.lora_box_bytes : 0;
+      const int box_el = p.lora_box_bytes / 2;
       if (do_lora) {
+        // B_lora is an input of the call; U comes from the LoRA-down kernel (loaded at the end)
         prefetch_tensormap(&map_blora);
         prefetch_tensormap(&map_u);
-        const uint32_t bar = smem_addr(lfull);
-        mbar_arrive_expect_tx(bar, lora_a_bytes + lora_u_bytes);
-        const int nbox = 2 * p.r / p.lora_box_bytes;
-        const int box_el = p.lora_box_bytes / 2;
-        for (int b = 0; b < nbox; ++b) {
-          tma_load_2d(smem_addr(lora_a + b * kRows * p.lora_box_bytes), &map_blora, b * box_el, n0, bar);
-          tma_load_2d(smem_addr(lora_u + b * MBOX * p.lora_box_bytes), &map_u, b * box_el, m0, bar);
-        }
+        mbar_arrive_expect_tx(smem_addr(lfull), lora_a_bytes + lora_u_bytes);
+        for (int b = 0; b < nbox; ++b)
+          tma_load_2d(smem_addr(lora_a + b * kRows * p.lora_box_bytes), &map_blora, b * box_el, n0, smem_addr(lfull));
       }
       int issued = 0;
       for (int j = 0; j < nst && ok; ++j) {
@@ -192,7 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(smem_addr(st + kCodeBytes + q * MBOX * 128), &map_x, kst * kKStage + q * 64, m0, bar);
         issued = j + 1;
       }
-      // drain: every issued stage has landed before the CTA can exit
+      if (do_lora) {
+        griddep_wait();  // the LoRA-down kernel has completed and its U is visible
+        for (int b = 0; b < nbox; ++b)
+          tma_load_2d(smem_addr(lora_u + b * MBOX * p.lora_box_bytes), &map_u, b * box_el, m0, smem_addr(lfull));
+      }
+      // drain: every issued copy has landed before the shared memory is reused or the CTA exits
       for (int j = max(0, issued - S); j < issued; ++j)
         mbar_wait(smem_addr(&full[j % S]), (j / S) & 1, p.status, kStatusTimeoutDrain);
       if (do_lora) mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutDrain);
@@ -255,21 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* st = smem + s * sb;
       const uint8_t* crow = st + row * 128;
       const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + x_stage_bytes(MBOX) + row * 16 + half * 8);
-      const uint32_t sbytes[2] = {sc.x, sc.y};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 16-byte chunk = 32 codes = two MMA K-steps
-        const int chunk = half * 4 + c;
-        const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((chunk ^ (row & 7)) << 4));
-        const uint32_t s0 = scale_bf16x2((sbytes[c >> 1] >> (16 * (c & 1))) & 0xFFu);
-        const uint32_t s1 = scale_bf16x2((sbytes[c >> 1] >> (16 * (c & 1) + 8)) & 0xFFu);
-        uint32_t col[8];
-        expand_word(cw.x, s0, col);
-        expand_word(cw.y, s0, col + 4);
-        tmem_st8(tmem + lane_base + kAcol0 + a * 128 + chunk * 16, col);
-        expand_word(cw.z, s1, col);
-        expand_word(cw.w, s1, col + 4);
-        tmem_st8(tmem + lane_base + kAcol0 + a * 128 + chunk * 16 + 8, col);
-      }
+      const uint32_t taddr = tmem + lane_base + kAcol0 + a * 128;
+      // scale bytes below 8 (zero or subnormal E4M3) take the general decode (warp-uniform branch)
+      if (__any_sync(0xFFFFFFFFu, has_small_scale(sc))) dequant_half_stage<true>(crow, row, half, sc, taddr);
+      else dequant_half_stage<false>(crow, row, half, sc, taddr);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -286,7 +324,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t n = n0 + row;
       constexpr int kTokHalf = MBOX / 2;
       const int t0 = half * kTokHalf;
-      float* slab = p.splits > 1 ? p.slabs + static_cast<int64_t>(split) * p.M * p.N : nullptr;
 #pragma unroll
       for (int c = 0; c < kTokHalf; c += 16) {
         uint32_t d[16], l[16];
@@ -295,64 +332,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int64_t m = m0 + t0 + c + i;
-          if (m >= p.M) break;
           float v = (__uint_as_float(d[i]) * 0x1p32f) * g;
           if (do_lora) v = fmaf(p.s, __uint_as_float(l[i]), v);
-          if (slab) slab[m * p.N + n] = v;
-          else p.y[m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(v));
-        }
-      }
-    }
-    if (p.splits > 1) {
-      // last CTA of this output tile sums the fp32 partials in split order
-      __threadfence();
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (dw == 0 && lane == 0) {
-        const uint32_t cidx = tile_m * gridDim.x + tile_n;
-        const uint32_t old = atomicAdd(&p.counters[cidx], 1u);
-        *last_flag = (old == static_cast<uint32_t>(p.splits - 1)) ? 1u : 0u;
-        if (old == static_cast<uint32_t>(p.splits - 1)) p.counters[cidx] = 0;
-      }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (*last_flag) {
-        __threadfence();
-        // 256 threads over the MBOX x 128 output tile: thread -> one row, a run of kCols columns
-        constexpr int kThreadsPerRow = 256 / MBOX, kCols = kRows / kThreadsPerRow;
-        const int t = dw * 32 + lane;
-        const int64_t m = m0 + t / kThreadsPerRow;
-        const int64_t nb = n0 + (t % kThreadsPerRow) * kCols;
-        if (m < p.M) {
-          uint4* dst = reinterpret_cast<uint4*>(p.y + m * p.N + nb);
-#pragma unroll 1
-          for (int c8 = 0; c8 < kCols; c8 += 8) {
-            // all splits' loads of these 8 columns are issued before any is summed
-            float4 va[kMaxSplits], vb[kMaxSplits];
-#pragma unroll
-            for (int sp = 0; sp < kMaxSplits; ++sp) {
-              if (sp < p.splits) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(p.slabs + (static_cast<int64_t>(sp) * p.M + m) * p.N + nb + c8);
-                va[sp] = __ldcg(src);
-                vb[sp] = __ldcg(src + 1);
-              }
-            }
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int sp = 0; sp < kMaxSplits; ++sp) {
-              if (sp < p.splits) {
-                acc[0] += va[sp].x; acc[1] += va[sp].y; acc[2] += va[sp].z; acc[3] += va[sp].w;
-                acc[4] += vb[sp].x; acc[5] += vb[sp].y; acc[6] += vb[sp].z; acc[7] += vb[sp].w;
-              }
-            }
-            uint32_t o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = f32_to_bf16_bits(acc[2 * q]) | (f32_to_bf16_bits(acc[2 * q + 1]) << 16);
-            dst[c8 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+          if (p.splits > 1) {
+            part[(t0 + c + i) * kRows + row] = v;  // every token of the tile, rows in lanes
+          } else {
+            const int64_t m = m0 + t0 + c + i;
+            if (m < p.M) p.y[m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(v));
           }
         }
       }
     }
+  }
+  if (p.splits > 1) {
+    // ---------------------------------------------------------------- split-K reduction
+    // All threads of the cluster meet twice: the partial tiles are complete before any CTA
+    // reads them, and no CTA leaves (its shared memory) while a peer may still read it.
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2) {
+      const int C = p.splits;
+      const int q = static_cast<int>(cluster_ctarank());
+      const int tb = q * MBOX / C, te = (q + 1) * MBOX / C;  // this CTA's slice of the tokens
+      constexpr int kPerTok = kRows / 8;                    // 8 rows (two float4) per item
+      for (int idx = (warp - 2) * 32 + lane; idx < (te - tb) * kPerTok; idx += kDeqWarps * 32) {
+        const int tok = tb + idx / kPerTok, r8 = (idx % kPerTok) * 8;
+        const int64_t m = m0 + tok;
+        if (m >= p.M) continue;
+        const uint32_t local = smem_addr(part + tok * kRows + r8);
+        float4 va[kMaxSplits], vb[kMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp) {
+          if (sp < C) {
+            const uint32_t ra = dsmem_map(local, static_cast<uint32_t>(sp));
+            va[sp] = dsmem_ld_v4(ra);
+            vb[sp] = dsmem_ld_v4(ra + 16);
+          }
+        }
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp) {
+          if (sp < C) {
+            acc[0] += va[sp].x; acc[1] += va[sp].y; acc[2] += va[sp].z; acc[3] += va[sp].w;
+            acc[4] += vb[sp].x; acc[5] += vb[sp].y; acc[6] += vb[sp].z; acc[7] += vb[sp].w;
+          }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = f32_to_bf16_bits(acc[2 * i]) | (f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4*>(p.y + m * p.N + n0 + r8) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -362,10 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, 512);
   }
 }
-
-constexpr int kPrepK = 128;   // K per prep CTA
-constexpr int kPrepM = 64;    // activation rows per prep CTA
-constexpr int kPrepPad = 8;   // bf16 row padding (conflict-free ldmatrix)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -381,85 +409,90 @@ __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Prep: x_perm (K permuted inside groups of 8 as 0,4,1,5,2,6,3,7) and the LoRA down-projection
-// U = bf16(x A^T). CTA (k chunk, row tile) stages a 64 x 128 slice of x and a 32 x 128 slice of A
-// in shared memory, writes its slice of x_perm, and runs the small GEMM on mma.sync (warp w:
-// rows 16w..16w+15, 32 ranks per pass); partial sums go to the fp32 accumulator U32 (zeroed by
-// the caller); the last chunk of a row tile (arrival counter) converts its rows of U to bf16.
-__global__ void __launch_bounds__(128) w4a16_prep_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
-                                                         const uint16_t* __restrict__ A, int r,
-                                                         uint16_t* __restrict__ xp, float* __restrict__ U32,
-                                                         uint16_t* __restrict__ U, uint32_t* __restrict__ tilecnt) {
-  __shared__ __align__(16) uint16_t xs[kPrepM][kPrepK + kPrepPad];
-  __shared__ __align__(16) uint16_t as[32][kPrepK + kPrepPad];
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kPrepM;
-  const int64_t k0 = static_cast<int64_t>(blockIdx.x) * kPrepK;
+// LoRA down-projection U = bf16(x A^T), [M][r]. A cluster of kDownCluster CTAs (blockIdx.x)
+// covers 64 rows of x (blockIdx.y); CTA q takes a contiguous range of the 128-K chunks. Per
+// chunk it stages 64 x 128 of x and 32 x 128 of A in shared memory and runs mma.sync
+// m16n8k16 (warp w: rows 16w..16w+15, 32 ranks per pass), accumulating in registers. The
+// fp32 partial [64][32] goes to shared memory; after a cluster barrier, CTA q sums its
+// eighth of the rows over all CTAs' partials in rank order (distributed shared memory)
+// and writes U. Rows past M read as zero and are not written.
+__global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                              const uint16_t* __restrict__ A, int r,
+                                                              uint16_t* __restrict__ U) {
+  // the main kernel may start now: it waits (griddepcontrol.wait) before reading U
+  griddep_launch_dependents();
+  __shared__ __align__(16) uint16_t xs[kDownM][kDownK + kDownPad];
+  __shared__ __align__(16) uint16_t as[32][kDownK + kDownPad];
+  __shared__ __align__(16) float part[kDownM][32];
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kDownM;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // 64 rows x 16 vectors of 8 bf16: 8 per thread
-#pragma unroll
-  for (int i = 0; i < (kPrepM * kPrepK / 8) / 128; ++i) {
-    const int idx = tid + i * 128, row = idx >> 4, vec = idx & 15;
-    const int64_t m = m0 + row;
-    uint4 a = make_uint4(0, 0, 0, 0);
-    if (m < M) {
-      a = *reinterpret_cast<const uint4*>(x + m * K + k0 + vec * 8);
-      uint4 o;  // elements e0..e7 (two per word) -> e0 e4 | e1 e5 | e2 e6 | e3 e7
-      o.x = __byte_perm(a.x, a.z, 0x5410);
-      o.y = __byte_perm(a.x, a.z, 0x7632);
-      o.z = __byte_perm(a.y, a.w, 0x5410);
-      o.w = __byte_perm(a.y, a.w, 0x7632);
-      *reinterpret_cast<uint4*>(xp + m * K + k0 + vec * 8) = o;
-    }
-    *reinterpret_cast<uint4*>(&xs[row][vec * 8]) = a;
-  }
-  if (r == 0) return;
+  const int C = static_cast<int>(gridDim.x);
+  const int q = static_cast<int>(cluster_ctarank());
+  const int nchunks = static_cast<int>(K / kDownK);
+  const int cb = q * nchunks / C, ce = (q + 1) * nchunks / C;
   for (int j0 = 0; j0 < r; j0 += 32) {
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < (32 * kPrepK / 8) / 128; ++i) {
-      const int idx = tid + i * 128, jr = idx >> 4, vec = idx & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (j0 + jr < r) v = __ldg(reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j0 + jr) * K + k0 + vec * 8));
-      *reinterpret_cast<uint4*>(&as[jr][vec * 8]) = v;
-    }
-    __syncthreads();
     float c[4][4] = {};
+    for (int ch = cb; ch < ce; ++ch) {
+      const int64_t k0 = static_cast<int64_t>(ch) * kDownK;
+      __syncthreads();  // the previous chunk's fragments have been read
 #pragma unroll
-    for (int ks = 0; ks < kPrepK / 16; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&xs[warp * 16 + (lane & 15)][ks * 16 + (lane >> 4) * 8])),
-              a[0], a[1], a[2], a[3]);
+      for (int i = 0; i < (kDownM * kDownK / 8) / 128; ++i) {  // 64 rows x 16 vectors of 8 bf16
+        const int idx = tid + i * 128, row = idx >> 4, vec = idx & 15;
+        const int64_t m = m0 + row;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (m < M) v = __ldg(reinterpret_cast<const uint4*>(x + m * K + k0 + vec * 8));
+        *reinterpret_cast<uint4*>(&xs[row][vec * 8]) = v;
+      }
 #pragma unroll
-      for (int jp = 0; jp < 2; ++jp) {
-        const int q = lane >> 3;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&as[jp * 16 + (q >> 1) * 8 + (lane & 7)][ks * 16 + (q & 1) * 8])),
-                b0, b1, b2, b3);
-        mma16816(c[2 * jp], a, b0, b1);
-        mma16816(c[2 * jp + 1], a, b2, b3);
+      for (int i = 0; i < (32 * kDownK / 8) / 128; ++i) {
+        const int idx = tid + i * 128, jr = idx >> 4, vec = idx & 15;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (j0 + jr < r) v = __ldg(reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j0 + jr) * K + k0 + vec * 8));
+        *reinterpret_cast<uint4*>(&as[jr][vec * 8]) = v;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int ks = 0; ks < kDownK / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&xs[warp * 16 + (lane & 15)][ks * 16 + (lane >> 4) * 8])),
+                a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {
+          const int g8 = lane >> 3;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&as[jp * 16 + (g8 >> 1) * 8 + (lane & 7)][ks * 16 + (g8 & 1) * 8])),
+                  b0, b1, b2, b3);
+          mma16816(c[2 * jp], a, b0, b1);
+          mma16816(c[2 * jp + 1], a, b2, b3);
+        }
       }
     }
     // C fragment: c0,c1 at (row lane/4, cols 2(lane%4), +1); c2,c3 at row + 8
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int64_t m = m0 + warp * 16 + (lane >> 2) + (q >> 1) * 8;
-        const int j = j0 + nt * 8 + 2 * (lane & 3) + (q & 1);
-        if (m < M && j < r) atomicAdd(U32 + m * r + j, c[nt][q]);
+      for (int e = 0; e < 4; ++e)
+        part[warp * 16 + (lane >> 2) + (e >> 1) * 8][nt * 8 + 2 * (lane & 3) + (e & 1)] = c[nt][e];
+    cluster_sync_all();
+    // CTA q: rows [q*64/C, (q+1)*64/C), four ranks per thread and step
+    const int rb = q * kDownM / C, re = (q + 1) * kDownM / C;
+    for (int idx = tid; idx < (re - rb) * 8; idx += 128) {
+      const int row = rb + idx / 8, j4 = (idx % 8) * 4;
+      const int64_t m = m0 + row;
+      const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(&part[row][j4]));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sp = 0; sp < C; ++sp) {
+        const float4 v = dsmem_ld_v4(dsmem_map(local, static_cast<uint32_t>(sp)));
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
-  }
-  __threadfence();
-  __syncthreads();
-  __shared__ uint32_t last;
-  if (tid == 0) last = (atomicAdd(tilecnt + blockIdx.y, 1u) == gridDim.x - 1) ? 1u : 0u;
-  __syncthreads();
-  if (last) {
-    __threadfence();
-    for (int i = tid; i < kPrepM * r; i += blockDim.x) {
-      const int64_t m = m0 + i / r;
-      if (m < M) U[m * r + i % r] = static_cast<uint16_t>(f32_to_bf16_bits(__ldcg(U32 + m * r + i % r)));
+      if (m < M) {
+        const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j0 + j4 + e < r) U[m * r + j0 + j4 + e] = static_cast<uint16_t>(f32_to_bf16_bits(av[e]));
+      }
     }
+    cluster_sync_all();  // partials read by every peer before the next pass overwrites them
   }
 }
 
@@ -488,38 +521,77 @@ CUtensorMapSwizzle swizzle_for(int box_bytes) {
 }
 
 struct TcPlan {
-  int mbox, tiles_m, tiles_n, splits, stages_per_split, smem_stages;
-  // ws_zero .. ws_zero + zero_bytes is cleared every call: U32, per-row and per-tile counters
-  size_t smem_bytes, ws_xperm, ws_u, ws_zero, zero_bytes, ws_u32, ws_rowcnt, ws_counters, ws_slabs, ws_total;
+  int mbox, tiles_m, tiles_n, smem_stages;
+  size_t smem_bytes, ws_u, ws_total;
 };
 
-TcPlan plan(int64_t M, int64_t N, int64_t K, int r, int sm_count) {
+// Tile shape, shared-memory ring and workspace (U only). The ring leaves room for one
+// LoRA-down CTA on the same SM, so that kernel never delays a CTA of this one.
+TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
   TcPlan t{};
   t.mbox = M <= 64 ? 64 : 128;
   t.tiles_m = static_cast<int>((M + t.mbox - 1) / t.mbox);
   t.tiles_n = static_cast<int>(N / kRows);
-  const int kst = static_cast<int>(K / kKStage);
-  const int ctas = t.tiles_n * t.tiles_m;
-  int splits = std::max(1, std::min({kst, sm_count / std::max(1, ctas), kMaxSplits}));
-  t.stages_per_split = (kst + splits - 1) / splits;
-  t.splits = (kst + t.stages_per_split - 1) / t.stages_per_split;
   const size_t lora = r ? static_cast<size_t>(kRows + t.mbox) * 2 * r : 0;
   const size_t fixed = 1024 + lora + 256;
   const size_t sb = stage_bytes(t.mbox);
-  t.smem_stages = static_cast<int>(std::min<size_t>(4, (227 * 1024 - fixed) / sb));
+  const size_t budget = 227 * 1024 - (r ? kDownSmem + 1024 : 0);
+  t.smem_stages = budget > fixed ? static_cast<int>(std::min<size_t>(4, (budget - fixed) / sb)) : 0;
   t.smem_bytes = fixed + t.smem_stages * sb;
   size_t o = 0;
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
-  t.ws_xperm = take(static_cast<size_t>(M) * K * 2);
   t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
-  t.ws_u32 = take(static_cast<size_t>(M) * std::max(r, 1) * 4);
-  t.ws_rowcnt = take(static_cast<size_t>(M) * 4);
-  t.ws_counters = take(static_cast<size_t>(t.tiles_m) * t.tiles_n * 4);
-  t.ws_zero = t.ws_u32;
-  t.zero_bytes = o - t.ws_u32;
-  t.ws_slabs = take(t.splits > 1 ? static_cast<size_t>(t.splits) * M * N * 4 : 0);
   t.ws_total = o;
   return t;
+}
+
+template <int MBOX>
+void* tc_kernel_ptr() {
+  return reinterpret_cast<void*>(w4a16_tc_kernel<MBOX>);
+}
+
+// Clusters of `c` CTAs of the tcgen05 kernel that can be resident at once on this device.
+int cluster_capacity(int device, int mbox, size_t smem, int c) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(device, mbox, smem, c);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, c, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = c;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const void* fn = mbox == 64 ? tc_kernel_ptr<64>() : tc_kernel_ptr<128>();
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
+// Split-K factor: 1 when the output tiles alone fill half the SMs; otherwise the largest
+// cluster size (<= 8, <= the number of 256-K stages) whose clusters all fit at once.
+int choose_splits(int device, const TcPlan& t, int64_t K, int sm_count) {
+  const int tiles = t.tiles_n * t.tiles_m;
+  const int kst = static_cast<int>(K / kKStage);
+  if (2 * tiles > sm_count) return 1;
+  for (int c = std::min(kMaxSplits, kst); c >= 2; --c) {
+    const int sps = (kst + c - 1) / c;
+    const int used = (kst + sps - 1) / sps;  // splits after rounding the stages per split
+    if (used != c) continue;
+    if (tiles <= cluster_capacity(device, t.mbox, t.smem_bytes, c)) return c;
+  }
+  return 1;
 }
 
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows, int esize,
@@ -545,35 +617,55 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 // True when the tcgen05 W4A16 path takes this shape.
 bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
   if (!(M > 0 && N % kRows == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= 128)))) return false;
-  return plan(M, N, K, r, kPlanSMs).smem_stages >= 2;
+  return plan(M, N, K, r).smem_stages >= 2;
 }
 
-size_t w4a16_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int sm_count) {
-  return plan(M, N, K, r, sm_count).ws_total;
+size_t w4a16_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int) {
+  return plan(M, N, K, r).ws_total;
 }
 
 nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev,
                                cudaStream_t st) {
-  const TcPlan t = plan(a.M, a.N, a.K, a.r, std::min(dev.sm_count, kPlanSMs));
+  const TcPlan t = plan(a.M, a.N, a.K, a.r);
   if (ws_bytes < t.ws_total) return NVFP4RL_ERR_WORKSPACE;
   if (t.smem_stages < 2) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
-  char* base = static_cast<char*>(ws);
-  uint16_t* xp = reinterpret_cast<uint16_t*>(base + t.ws_xperm);
-  uint16_t* U = reinterpret_cast<uint16_t*>(base + t.ws_u);
-  uint32_t* counters = reinterpret_cast<uint32_t*>(base + t.ws_counters);
-  float* slabs = reinterpret_cast<float*>(base + t.ws_slabs);
+  uint16_t* U = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + t.ws_u);
+  const int smem = static_cast<int>(t.smem_bytes);
+  cudaError_t e = t.mbox == 64
+                      ? cudaFuncSetAttribute(w4a16_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                      : cudaFuncSetAttribute(w4a16_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  const int splits = choose_splits(dev.device, t, a.K, std::min(dev.sm_count, kPlanSMs));
+  const int kst = static_cast<int>(a.K / kKStage);
 
-  if (cudaMemsetAsync(base + t.ws_zero, 0, t.zero_bytes, st) != cudaSuccess) return NVFP4RL_ERR_CUDA;
-  dim3 pgrid(static_cast<unsigned>(a.K / kPrepK), static_cast<unsigned>((a.M + kPrepM - 1) / kPrepM));
-  w4a16_prep_kernel<<<pgrid, 128, 0, st>>>(a.x, a.M, a.K, a.A, a.r, xp, reinterpret_cast<float*>(base + t.ws_u32), U,
-                                           reinterpret_cast<uint32_t*>(base + t.ws_rowcnt));
-  if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  if (a.r) {
+    // LoRA down-projection: one cluster per 64 rows of x, K split over the cluster
+    const int nchunks = static_cast<int>(a.K / kDownK);
+    const int cd = std::min(kDownCluster, nchunks);
+    cudaLaunchConfig_t dcfg = {};
+    dcfg.gridDim = dim3(cd, static_cast<unsigned>((a.M + kDownM - 1) / kDownM), 1);
+    dcfg.blockDim = dim3(128);
+    dcfg.stream = st;
+    cudaLaunchAttribute dattr[1];
+    dattr[0].id = cudaLaunchAttributeClusterDimension;
+    dattr[0].val.clusterDim.x = cd;
+    dattr[0].val.clusterDim.y = 1;
+    dattr[0].val.clusterDim.z = 1;
+    dcfg.attrs = dattr;
+    dcfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return NVFP4RL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel, a.x, a.M, a.K, a.A, a.r, U) != cudaSuccess)
+      return NVFP4RL_ERR_CUDA;
+    if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  }
 
   CUtensorMap mc, ms, mx, mb, mu;
   const int lbox = a.r ? std::min(2 * a.r, 128) : 128;
   if (!make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, a.K / 2, a.N, 1, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_scales, a.K / 16, a.N, 1, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xp, a.K, a.M, 2, 64, t.mbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, 2, 64, t.mbox, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4RL_ERR_CUDA;
   if (a.r) {
     if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, a.r, a.N, 2, lbox / 2, kRows, swizzle_for(lbox)) ||
@@ -587,28 +679,36 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
-  p.stages_per_split = t.stages_per_split;
-  p.splits = t.splits;
+  p.stages_per_split = (kst + splits - 1) / splits;
+  p.splits = splits;
   p.r = a.r;
   p.lora_box_bytes = lbox;
   p.s = a.s;
   p.w_g = a.w_g;
   p.y = a.y;
-  p.slabs = slabs;
-  p.counters = counters;
   p.status = dev.status;
   p.smem_stages = t.smem_stages;
-  dim3 grid(t.tiles_n, t.splits, t.tiles_m);
-  cudaError_t e;
-  if (t.mbox == 64) {
-    e = cudaFuncSetAttribute(w4a16_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(t.smem_bytes));
-    if (e == cudaSuccess) w4a16_tc_kernel<64><<<grid, kThreads, t.smem_bytes, st>>>(mc, ms, mx, mb, mu, p);
-  } else {
-    e = cudaFuncSetAttribute(w4a16_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(t.smem_bytes));
-    if (e == cudaSuccess) w4a16_tc_kernel<128><<<grid, kThreads, t.smem_bytes, st>>>(mc, ms, mx, mb, mu, p);
-  }
+  // Split K runs as clusters of `splits` CTAs along y. With LoRA, the launch is a programmatic
+  // dependent of the LoRA-down kernel: it runs alongside it and waits for it only before loading
+  // U. Everything else it reads (x, weights, B_lora, g) was complete before the LoRA-down kernel
+  // started. Without LoRA the launch is an ordinary one (nothing would order it after the
+  // caller's previous kernel).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(t.tiles_n, splits, t.tiles_m);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = t.smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = splits;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.r ? 2 : 1;
+  e = t.mbox == 64 ? cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<64>, mc, ms, mx, mb, mu, p)
+                   : cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<128>, mc, ms, mx, mb, mu, p);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }

@@ -47,7 +47,7 @@ extern "C" nvfp4rl_status nvfp4_lora_linear_noalloc(const uint16_t* x, int64_t M
     }
     scratch = g_noalloc_ptr[dev];
   }
-  // The workspace path clears what must start at zero on every call (stream-ordered memset).
+  // Nothing in the workspace has to start at zero: every call writes what it later reads.
   return nvfp4_lora_linear(x, M, K, w_codes, w_scales, w_g, N, lora_A, lora_B, r, s, nullptr, 0, y, scratch,
                            kNoallocScratchBytes, stream);
 }

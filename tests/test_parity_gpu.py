@@ -90,6 +90,27 @@ def test_quantize_edge_values(nv, dtype):
     assert_quant_equal(gpu_quantize(nv, x, amax_in=a), oracle.quantize(x, amax_in=a), "amax_in saturation")
 
 
+def test_quantize_midpoints_with_general_scales(nv):
+    """bf16 values exactly on E2M1 midpoints (and on grid points) of blocks whose E4M3 scale has a
+    nonzero mantissa: every element is a rounding tie of the quotient x / (E4M3(s) g)."""
+    rng = np.random.default_rng(11)
+    rows, cols = 48, 512
+    g = np.float32(2.0 ** -7)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    grid = np.array([.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    x = np.zeros((rows, cols), np.float32)
+    for r in range(rows):
+        for b in range(cols // 16):
+            s = np.float32(2.0 ** int(rng.integers(-5, 7)) * (1 + int(rng.integers(0, 8)) / 8))
+            vals = np.concatenate([[6.0], mids, grid[rng.integers(0, 7, 8)]])[:16].astype(np.float32)
+            vals = vals * s * g * np.where(rng.random(16) < 0.5, -1, 1).astype(np.float32)
+            x[r, 16 * b:16 * b + 16] = vals
+    x[0, 0] = np.float32(6 * 448 * g)  # tensor amax -> g exactly
+    xb = synth.bf16_bits(x)
+    assert np.array_equal(synth.bf16_to_f32(xb), x)  # every value is exact in bf16
+    assert_quant_equal(gpu_quantize(nv, xb), oracle.quantize(xb), "midpoint ties, general scales")
+
+
 def test_quantize_zero_tiny_and_huge(nv):
     z = np.zeros((8, 64), np.float32)
     z[2, 5] = -0.0

@@ -63,9 +63,10 @@ def test_noalloc_matches_workspace_entry_point(nv, M, N, K, r):
 def test_noalloc_rejects_problems_beyond_its_scratch(nv):
     L = nv.lib()
     cap = L.nvfp4rl_noalloc_scratch_bytes()
-    M, N, K = 64, 128, 1 << 17  # x_perm alone (M*K*2 bytes) exceeds the fixed array
-    assert nv.workspace_bytes(nv.OP_LINEAR_W4A16, M, N, K, 0) > cap
+    # rank 136 (> 128) takes the general path, whose fp32 accumulator (M*N*4 bytes) exceeds the array
+    M, N, K, r = 8192, 1024, 256, 136
+    assert nv.workspace_bytes(nv.OP_LINEAR_W4A16, M, N, K, r) > cap
     dummy = torch.empty(16, dtype=torch.uint8, device="cuda")
     p = ctypes.c_void_p(dummy.data_ptr())
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    assert L.nvfp4_lora_linear_noalloc(p, M, K, p, p, p, N, None, None, 0, 1.0, p, st) == 4  # NVFP4RL_ERR_WORKSPACE
+    assert L.nvfp4_lora_linear_noalloc(p, M, K, p, p, p, N, p, p, r, 1.0, p, st) == 4  # NVFP4RL_ERR_WORKSPACE
