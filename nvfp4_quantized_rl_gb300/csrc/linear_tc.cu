@@ -6,25 +6,31 @@
 //
 // One call = two kernels on the caller's stream:
 //   w4a16_lora_down_kernel  U = bf16(x A^T) for the LoRA up-projection: a cluster of CTAs
-//                           splits K, each runs mma.sync on its chunks, and the partial sums
-//                           meet in distributed shared memory (fixed order, no atomics).
+//                           splits K, each streams its chunks through a cp.async ring into
+//                           mma.sync, and the partial sums meet in distributed shared memory
+//                           (fixed order, no atomics).
 //   w4a16_tc_kernel         launched as a programmatic dependent of the first: it starts while
 //                           the LoRA-down runs and waits for it (griddepcontrol.wait) only
 //                           before loading U, after its whole weight stream has been issued.
 //
 // w4a16_tc_kernel (one CTA = 128 weight rows x one K range x up to 128 tokens):
-//   warp 0      TMA producer: per 256-K stage, the 128 x 128-byte code tile (128-byte
-//               swizzle), the 128 x 16-byte scale tile and the activation tile (4 boxes of
-//               64 bf16 x tokens, 128-byte swizzle, read straight from x) into a ring of
-//               shared-memory stages.
+//   warp 0      weight producer (TMA): per 256-K stage the 128 x 128-byte code tile (128-byte
+//               swizzle) and the 128 x 16-byte scale tile, into a deep weight ring.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::f16 with A (the
 //               dequantized weights) in TMEM and B (activations) in shared memory, then the
 //               LoRA up-projection (B_lora tile x U^T) into a second accumulator.
-//   warps 2-9   dequantize: thread = one weight row and half of the stage's K; 4-bit codes
-//               are expanded to bf16 with integer ops (sign and magnitude bits moved into a
-//               bf16 bit pattern, one bf16x2 FMA by E4M3(s) * 2^94, a byte permute into K
-//               order), written to TMEM with tcgen05.st; then the epilogue: TMEM -> registers,
-//               g and s applied, bf16 stores.
+//   warp 2      activation producer (TMA): per 128-K sub-stage two boxes of 64 bf16 x tokens
+//               (128-byte swizzle, read straight from x) into a separate, shallower ring;
+//               plus the LoRA tiles.
+//   warps 3-10  dequantize: thread = one weight row and half of the stage's K; 4-bit codes
+//               are expanded to bf16 with integer ops (a nibble swap, sign and magnitude bits
+//               moved into a bf16 bit pattern, one bf16x2 FMA by E4M3(s) * 2^94), written to
+//               TMEM with tcgen05.st; then the epilogue: TMEM -> registers, g and s applied,
+//               bf16 stores.
+// The weight ring is released by the dequant warps and the activation ring by the MMAs, so
+// the HBM weight stream runs ahead independently of the L2-resident activation tiles. Each
+// output tile starts its K range at a different stage (the CTAs then read different
+// activation tiles at any one time).
 // When K is split across CTAs, the CTAs of one output tile form a cluster: each leaves its
 // fp32 partial tile in its own shared memory, and after a cluster barrier each CTA sums one
 // slice of the tokens over all partials (in split order) through distributed shared memory.
@@ -32,9 +38,9 @@
 // The bf16 pattern of a code magnitude m = (e1 e0 m0) placed in bits 8..6 is the value
 // grid(m) * 2^-126 (a subnormal when e = 0), so multiplying by E4M3(s) * 2^94 gives
 // grid(m) * E4M3(s) * 2^-32 exactly (at most 6 significant bits); the epilogue multiplies
-// the fp32 accumulator by 2^32 and then by g. A code word's nibbles j and j+4 (16 bits
-// apart) share their shifts, so they are expanded together and then re-paired by byte
-// permutes into the K order (2c, 2c+1) of TMEM column c.
+// the fp32 accumulator by 2^32 and then by g. Two codes 16 bits apart in a code word share
+// their shifts and are expanded together; one delta swap of nibbles beforehand makes those
+// two codes K-adjacent, the pair (2c, 2c+1) of TMEM column c.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -55,15 +61,17 @@ constexpr int kRows = 128;        // weight rows per CTA (MMA M)
 constexpr int kKStage = 256;      // K per pipeline stage
 constexpr int kCodeBytes = kRows * kKStage / 2;   // 16 KB
 constexpr int kScaleBytes = kRows * kKStage / 16;  // 2 KB
-constexpr int kThreads = 320;     // 10 warps
-constexpr int kDeqWarps = 8;
+constexpr int kWStageBytes = kCodeBytes + kScaleBytes;  // one weight stage: codes + scales
+constexpr int kFirstDeqWarp = 3;  // warps 0-2: weight producer, MMA issuer, activation producer
 constexpr int kMaxSplits = 8;     // split-K factor cap = the portable cluster size
 
-constexpr int kDownK = 128;       // K per LoRA-down chunk
+constexpr int kDownK = 64;        // K per LoRA-down chunk
 constexpr int kDownM = 64;        // activation rows per LoRA-down cluster
 constexpr int kDownPad = 8;       // bf16 row padding (conflict-free ldmatrix)
-constexpr int kDownCluster = 8;   // CTAs per LoRA-down cluster (K split)
-constexpr int kDownSmem = (kDownM + 32) * (kDownK + kDownPad) * 2 + kDownM * 32 * 4;
+constexpr int kDownStages = 3;    // chunks in flight (cp.async ring)
+constexpr int kDownCluster = 16;  // CTAs per LoRA-down cluster (K split); 8 where 16 is not available
+constexpr int kDownStageElems = (kDownM + 32) * (kDownK + kDownPad);
+constexpr int kDownSmem = kDownStages * kDownStageElems * 2 + kDownM * 32 * 4;
 
 struct TcParams {
   int64_t M, N, K;
@@ -75,11 +83,13 @@ struct TcParams {
   const float* w_g;
   uint16_t* y;
   uint32_t* status;
-  int smem_stages;
+  int w_stages;          // weight ring depth (256-K stages)
+  int x_stages;          // activation ring depth (128-K sub-stages)
 };
 
-__host__ __device__ constexpr int x_stage_bytes(int mbox) { return 4 * mbox * 128; }
-__host__ __device__ constexpr int stage_bytes(int mbox) { return kCodeBytes + x_stage_bytes(mbox) + kScaleBytes; }
+// activation sub-stage: 128 K (two boxes of 64 bf16) x tokens; two per 256-K weight stage
+__host__ __device__ constexpr int x_stage_bytes(int mbox) { return 2 * mbox * 128; }
+__host__ __device__ constexpr int threads_for(int deq_warps) { return 32 * (kFirstDeqWarp + deq_warps); }
 
 __device__ __forceinline__ uint32_t swizzle_mode_for(int box_bytes) {
   return box_bytes == 128 ? 2u : box_bytes == 64 ? 4u : 6u;
@@ -123,13 +133,15 @@ __device__ __forceinline__ bool has_small_scale(uint2 sc) {
   return (((y0 - 0x01010101u) & ~y0) | ((y1 - 0x01010101u) & ~y1)) & 0x80808080u;
 }
 
-// Dequantizes one thread's half-stage (row `row`, 128 K) into TMEM columns `col0`..`col0`+63.
-template <bool kAnyScale>
-__device__ __forceinline__ void dequant_half_stage(const uint8_t* crow, int row, int half, uint2 sc, uint32_t taddr) {
+// Dequantizes one thread's share of a stage (row `row`, chunks c0 .. c0 + NCH - 1 of 32 codes)
+// into TMEM columns starting at taddr + 16 * chunk. sc holds the chunks' scale bytes, two per
+// chunk, in order.
+template <bool kAnyScale, int NCH>
+__device__ __forceinline__ void dequant_chunks(const uint8_t* crow, int row, int c0, uint2 sc, uint32_t taddr) {
   const uint32_t sbytes[2] = {sc.x, sc.y};
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {  // 16-byte chunk = 32 codes = two MMA K-steps
-    const int chunk = half * 4 + c;
+  for (int c = 0; c < NCH; ++c) {  // 16-byte chunk = 32 codes = two MMA K-steps
+    const int chunk = c0 + c;
     const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((chunk ^ (row & 7)) << 4));
     const uint32_t b0 = (sbytes[c >> 1] >> (16 * (c & 1))) & 0xFFu;
     const uint32_t b1 = (sbytes[c >> 1] >> (16 * (c & 1) + 8)) & 0xFFu;
@@ -145,33 +157,39 @@ __device__ __forceinline__ void dequant_half_stage(const uint8_t* crow, int row,
   }
 }
 
-template <int MBOX>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MBOX, int DW>
+__global__ void __launch_bounds__(threads_for(DW), 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                     const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_blora,
                     const __grid_constant__ CUtensorMap map_u, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.smem_stages;
+  const int SW = p.w_stages, SX = p.x_stages;
   constexpr int kAbuf = MBOX <= 64 ? 3 : 2;
+  constexpr int kWarpsPerQuarter = DW / 4;           // dequant warps sharing one TMEM lane quarter
+  constexpr int kChunks = 8 / kWarpsPerQuarter;      // 16-byte code chunks per thread and stage
   constexpr uint32_t kDcol = 0, kLcol = MBOX, kAcol0 = 2 * MBOX;
+  constexpr int kXBytes = x_stage_bytes(MBOX);
 
-  // layout: stages (reused as the fp32 partial tile after the K loop) | lora A tile | lora U tile | barriers
-  const int sb = stage_bytes(MBOX);
-  uint8_t* lora_a = smem + S * sb;
+  // layout: activation ring (reused as the fp32 partial tile after the K loop) | weight ring |
+  //         lora A tile | lora U tile | barriers
+  uint8_t* xring = smem;
+  uint8_t* wring = xring + SX * kXBytes;
+  uint8_t* lora_a = wring + SW * kWStageBytes;
   const int lora_a_bytes = p.r ? kRows * 2 * p.r : 0;
   uint8_t* lora_u = lora_a + lora_a_bytes;
   const int lora_u_bytes = p.r ? MBOX * 2 * p.r : 0;
   uint64_t* bars = reinterpret_cast<uint64_t*>(lora_u + lora_u_bytes);
-  // full[S], empty[S], afull[kAbuf], aempty[kAbuf], dfull, lfull
-  uint64_t* full = bars;
-  uint64_t* empty = full + S;
-  uint64_t* afull = empty + S;
-  uint64_t* aempty = afull + kAbuf;
+  uint64_t* wfull = bars;             // [SW] weight stage landed
+  uint64_t* wempty = wfull + SW;      // [SW] weight stage dequantized (DW arrivals)
+  uint64_t* xfull = wempty + SW;      // [SX] activation sub-stage landed
+  uint64_t* xempty = xfull + SX;      // [SX] activation sub-stage read by the MMAs (commit)
+  uint64_t* afull = xempty + SX;      // [kAbuf] A buffer written (DW arrivals)
+  uint64_t* aempty = afull + kAbuf;   // [kAbuf] A buffer read by the MMAs (commit)
   uint64_t* dfull = aempty + kAbuf;
   uint64_t* lfull = dfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lfull + 1);
-  float* part = reinterpret_cast<float*>(smem);  // [MBOX][kRows] fp32 partial tile (split K)
+  float* part = reinterpret_cast<float*>(xring);  // [MBOX][kRows] fp32 partial tile (split K)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, split = blockIdx.y, tile_m = blockIdx.z;
@@ -182,12 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool do_lora = p.r > 0 && split == 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(smem_addr(&full[i]), 1);
-      mbar_init(smem_addr(&empty[i]), kDeqWarps + 1);
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(smem_addr(&wfull[i]), 1);
+      mbar_init(smem_addr(&wempty[i]), DW);
+    }
+    for (int i = 0; i < SX; ++i) {
+      mbar_init(smem_addr(&xfull[i]), 1);
+      mbar_init(smem_addr(&xempty[i]), 1);
     }
     for (int i = 0; i < kAbuf; ++i) {
-      mbar_init(smem_addr(&afull[i]), kDeqWarps);
+      mbar_init(smem_addr(&afull[i]), DW);
       mbar_init(smem_addr(&aempty[i]), 1);
     }
     mbar_init(smem_addr(dfull), 1);
@@ -200,12 +222,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Each output tile starts its K range at a different stage, so that the CTAs do not all read
+  // the same activation tile from L2 at the same time. Producers and consumers all walk the
+  // stages in this order.
+  auto kstage = [&](int j) { return st0 + (j + tile_n) % nst; };
+
   bool ok = true;
   if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+    // ------------------------------------------------------------------ weight producer
     if (lane == 0) {
       prefetch_tensormap(&map_codes);
       prefetch_tensormap(&map_scales);
+      int issued = 0;
+      for (int j = 0; j < nst && ok; ++j) {
+        const int s = j % SW;
+        if (!mbar_wait(smem_addr(&wempty[s]), ((j / SW) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = wring + s * kWStageBytes;
+        const uint32_t bar = smem_addr(&wfull[s]);
+        mbar_arrive_expect_tx(bar, kWStageBytes);
+        const int kst = kstage(j);
+        tma_load_2d(smem_addr(st), &map_codes, kst * (kKStage / 2), n0, bar);
+        tma_load_2d(smem_addr(st + kCodeBytes), &map_scales, kst * (kKStage / 16), n0, bar);
+        issued = j + 1;
+      }
+      // drain: every issued copy has landed before the CTA exits
+      for (int j = max(0, issued - SW); j < issued; ++j)
+        mbar_wait(smem_addr(&wfull[j % SW]), (j / SW) & 1, p.status, kStatusTimeoutDrain);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ activation + LoRA producer
+    if (lane == 0) {
       prefetch_tensormap(&map_x);
       const int nbox = do_lora ? 2 * p.r / p.lora_box_bytes : 0;
       const int box_el = p.lora_box_bytes / 2;
@@ -218,23 +267,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(smem_addr(lora_a + b * kRows * p.lora_box_bytes), &map_blora, b * box_el, n0, smem_addr(lfull));
       }
       int issued = 0;
-      for (int j = 0; j < nst && ok; ++j) {
-        const int s = j % S;
-        const uint32_t ph = (j / S) & 1;
-        if (!mbar_wait(smem_addr(&empty[s]), ph ^ 1, p.status, kStatusTimeoutProducer)) {
+      for (int u = 0; u < 2 * nst && ok; ++u) {  // sub-stage u = half u % 2 of stage u / 2
+        const int s = u % SX;
+        if (!mbar_wait(smem_addr(&xempty[s]), ((u / SX) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * sb;
-        const uint32_t bar = smem_addr(&full[s]);
-        mbar_arrive_expect_tx(bar, sb);
-        const int kst = st0 + j;
-        tma_load_2d(smem_addr(st), &map_codes, kst * (kKStage / 2), n0, bar);
-        tma_load_2d(smem_addr(st + kCodeBytes + x_stage_bytes(MBOX)), &map_scales, kst * (kKStage / 16), n0, bar);
+        uint8_t* st = xring + s * kXBytes;
+        const uint32_t bar = smem_addr(&xfull[s]);
+        mbar_arrive_expect_tx(bar, kXBytes);
+        const int k0 = kstage(u >> 1) * kKStage + (u & 1) * (kKStage / 2);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_addr(st + kCodeBytes + q * MBOX * 128), &map_x, kst * kKStage + q * 64, m0, bar);
-        issued = j + 1;
+        for (int q = 0; q < 2; ++q) tma_load_2d(smem_addr(st + q * MBOX * 128), &map_x, k0 + q * 64, m0, bar);
+        issued = u + 1;
       }
       if (do_lora) {
         griddep_wait();  // the LoRA-down kernel has completed and its U is visible
@@ -242,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(smem_addr(lora_u + b * MBOX * p.lora_box_bytes), &map_u, b * box_el, m0, smem_addr(lfull));
       }
       // drain: every issued copy has landed before the shared memory is reused or the CTA exits
-      for (int j = max(0, issued - S); j < issued; ++j)
-        mbar_wait(smem_addr(&full[j % S]), (j / S) & 1, p.status, kStatusTimeoutDrain);
+      for (int u = max(0, issued - SX); u < issued; ++u)
+        mbar_wait(smem_addr(&xfull[u % SX]), (u / SX) & 1, p.status, kStatusTimeoutDrain);
       if (do_lora) mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
@@ -251,22 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kRows, MBOX);
       for (int j = 0; j < nst && ok; ++j) {
-        const int s = j % S, a = j % kAbuf;
-        // the dequant warps arrive on afull only after waiting for this stage's full barrier, so
-        // afull also orders the activation tile the MMAs read
+        const int a = j % kAbuf;
+        // the dequant warps arrive on afull only after waiting for the weight stage, and the
+        // activation sub-stages have their own barriers
         if (!mbar_wait(smem_addr(&afull[a]), (j / kAbuf) & 1, p.status, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t xs = smem_addr(smem + s * sb + kCodeBytes);
+        for (int h = 0; h < 2 && ok; ++h) {
+          const int u = 2 * j + h, sx = u % SX;
+          if (!mbar_wait(smem_addr(&xfull[sx]), (u / SX) & 1, p.status, kStatusTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xs = smem_addr(xring + sx * kXBytes);
 #pragma unroll
-        for (int kk = 0; kk < kKStage / 16; ++kk) {
-          const uint64_t bdesc = smem_desc(xs + (kk >> 2) * MBOX * 128 + (kk & 3) * 32, 16, 1024, 2);
-          mma_f16_ts(tmem + kDcol, tmem + kAcol0 + a * 128 + kk * 8, bdesc, idesc, (j | kk) ? 1u : 0u);
+          for (int kk = 0; kk < kKStage / 32; ++kk) {
+            const uint64_t bdesc = smem_desc(xs + (kk >> 2) * MBOX * 128 + (kk & 3) * 32, 16, 1024, 2);
+            mma_f16_ts(tmem + kDcol, tmem + kAcol0 + a * 128 + (h * 8 + kk) * 8, bdesc, idesc, (j | h | kk) ? 1u : 0u);
+          }
+          mma_commit(smem_addr(&xempty[sx]));
         }
         mma_commit(smem_addr(&aempty[a]));
-        mma_commit(smem_addr(&empty[s]));
       }
       if (ok && do_lora) {
         if (mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutMma)) {
@@ -289,31 +341,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
-    const int dw = warp - 2;             // 0..7
-    const int quarter = warp & 3;        // TMEM lane quarter this warp may access
-    const int half = dw >> 2;            // which 128-K half of the stage
+    const int dw = warp - kFirstDeqWarp;  // 0..DW-1
+    const int quarter = warp & 3;         // TMEM lane quarter this warp may access
+    const int part_k = dw >> 2;           // which share of the stage's K (and of the tile's tokens)
     const int row = quarter * 32 + lane;  // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     for (int j = 0; j < nst && ok; ++j) {
-      const int s = j % S, a = j % kAbuf;
+      const int s = j % SW, a = j % kAbuf;
       // every lane waits; the warp leaves together if any lane ran out of time
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (j / S) & 1, p.status, kStatusTimeoutDequant) &&
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&wfull[s]), (j / SW) & 1, p.status, kStatusTimeoutDequant) &&
                                        mbar_wait(smem_addr(&aempty[a]), ((j / kAbuf) & 1) ^ 1, p.status,
                                                  kStatusTimeoutDequant));
       if (!ok) break;
-      const uint8_t* st = smem + s * sb;
+      const uint8_t* st = wring + s * kWStageBytes;
       const uint8_t* crow = st + row * 128;
-      const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + x_stage_bytes(MBOX) + row * 16 + half * 8);
+      const uint32_t* srow = reinterpret_cast<const uint32_t*>(st + kCodeBytes + row * 16);
       const uint32_t taddr = tmem + lane_base + kAcol0 + a * 128;
+      // this thread's scale bytes: two per chunk
+      const uint2 sc = kChunks == 4 ? *reinterpret_cast<const uint2*>(srow + part_k * 2)
+                                    : make_uint2(srow[part_k], 0x08080808u);
       // scale bytes below 8 (zero or subnormal E4M3) take the general decode (warp-uniform branch)
-      if (__any_sync(0xFFFFFFFFu, has_small_scale(sc))) dequant_half_stage<true>(crow, row, half, sc, taddr);
-      else dequant_half_stage<false>(crow, row, half, sc, taddr);
+      if (__any_sync(0xFFFFFFFFu, has_small_scale(sc)))
+        dequant_chunks<true, kChunks>(crow, row, part_k * kChunks, sc, taddr);
+      else
+        dequant_chunks<false, kChunks>(crow, row, part_k * kChunks, sc, taddr);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_addr(&afull[a]));
-        mbar_arrive(smem_addr(&empty[s]));
+        mbar_arrive(smem_addr(&wempty[s]));
       }
     }
     // ---------------------------------------------------------------- epilogue
@@ -322,10 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       const float g = *p.w_g;
       const int64_t n = n0 + row;
-      constexpr int kTokHalf = MBOX / 2;
-      const int t0 = half * kTokHalf;
+      constexpr int kTok = MBOX / kWarpsPerQuarter;  // tokens per warp (multiple of 16)
+      const int t0 = part_k * kTok;
 #pragma unroll
-      for (int c = 0; c < kTokHalf; c += 16) {
+      for (int c = 0; c < kTok; c += 16) {
         uint32_t d[16], l[16];
         tmem_ld16(tmem + lane_base + kDcol + t0 + c, d);
         if (do_lora) tmem_ld16(tmem + lane_base + kLcol + t0 + c, l);
@@ -350,12 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // reads them, and no CTA leaves (its shared memory) while a peer may still read it.
     __syncwarp();
     cluster_sync_all();
-    if (warp >= 2) {
+    if (warp >= kFirstDeqWarp) {
       const int C = p.splits;
       const int q = static_cast<int>(cluster_ctarank());
       const int tb = q * MBOX / C, te = (q + 1) * MBOX / C;  // this CTA's slice of the tokens
       constexpr int kPerTok = kRows / 8;                    // 8 rows (two float4) per item
-      for (int idx = (warp - 2) * 32 + lane; idx < (te - tb) * kPerTok; idx += kDeqWarps * 32) {
+      for (int idx = (warp - kFirstDeqWarp) * 32 + lane; idx < (te - tb) * kPerTok; idx += DW * 32) {
         const int tok = tb + idx / kPerTok, r8 = (idx % kPerTok) * 8;
         const int64_t m = m0 + tok;
         if (m >= p.M) continue;
@@ -409,64 +466,86 @@ __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// LoRA down-projection U = bf16(x A^T), [M][r]. A cluster of kDownCluster CTAs (blockIdx.x)
-// covers 64 rows of x (blockIdx.y); CTA q takes a contiguous range of the 128-K chunks. Per
-// chunk it stages 64 x 128 of x and 32 x 128 of A in shared memory and runs mma.sync
-// m16n8k16 (warp w: rows 16w..16w+15, 32 ranks per pass), accumulating in registers. The
-// fp32 partial [64][32] goes to shared memory; after a cluster barrier, CTA q sums its
-// eighth of the rows over all CTAs' partials in rank order (distributed shared memory)
-// and writes U. Rows past M read as zero and are not written.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// LoRA down-projection U = bf16(x A^T), [M][r]. A cluster of CTAs (blockIdx.x, 16 or 8) covers 64
+// rows of x (blockIdx.y); CTA q takes a contiguous range of the 64-K chunks. A ring of three
+// chunk buffers is filled with cp.async (x: 64 x 64, A: 32 x 64 bf16) while mma.sync m16n8k16
+// runs on the oldest (warp w: rows 16w..16w+15, 32 ranks per pass), accumulating in registers.
+// The fp32 partial [64][32] goes to shared memory; after a cluster barrier, CTA q sums its share
+// of the rows over all CTAs' partials in rank order (distributed shared memory) and writes U.
+// Rows past M read as zero and are not written.
 __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                               const uint16_t* __restrict__ A, int r,
                                                               uint16_t* __restrict__ U) {
   // the main kernel may start now: it waits (griddepcontrol.wait) before reading U
   griddep_launch_dependents();
-  __shared__ __align__(16) uint16_t xs[kDownM][kDownK + kDownPad];
-  __shared__ __align__(16) uint16_t as[32][kDownK + kDownPad];
-  __shared__ __align__(16) float part[kDownM][32];
+  extern __shared__ __align__(16) uint8_t down_smem[];
+  uint16_t* ring = reinterpret_cast<uint16_t*>(down_smem);  // [kDownStages][96][kDownK + kDownPad]
+  float(*part)[32] = reinterpret_cast<float(*)[32]>(down_smem + kDownStages * kDownStageElems * 2);
+  constexpr int kRow = kDownK + kDownPad;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kDownM;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = static_cast<int>(gridDim.x);
   const int q = static_cast<int>(cluster_ctarank());
   const int nchunks = static_cast<int>(K / kDownK);
-  const int cb = q * nchunks / C, ce = (q + 1) * nchunks / C;
+  const int cb = q * nchunks / C, n = (q + 1) * nchunks / C - cb;
   for (int j0 = 0; j0 < r; j0 += 32) {
+    // one chunk: rows 0..63 of the buffer hold x, rows 64..95 hold A (ranks j0..j0+31)
+    auto load = [&](int i, int buf) {
+      uint16_t* b = ring + buf * kDownStageElems;
+      const int64_t k0 = static_cast<int64_t>(cb + i) * kDownK;
+#pragma unroll
+      for (int u = 0; u < (96 * kDownK / 8) / 128; ++u) {  // 96 rows x 8 vectors of 8 bf16
+        const int idx = tid + u * 128, row = idx >> 3, vec = idx & 7;
+        uint16_t* dst = b + row * kRow + vec * 8;
+        const uint16_t* src = nullptr;
+        if (row < kDownM) {
+          if (m0 + row < M) src = x + (m0 + row) * K + k0 + vec * 8;
+        } else if (j0 + row - kDownM < r) {
+          src = A + static_cast<int64_t>(j0 + row - kDownM) * K + k0 + vec * 8;
+        }
+        if (src) cp_async16(dst, src);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      }
+    };
     float c[4][4] = {};
-    for (int ch = cb; ch < ce; ++ch) {
-      const int64_t k0 = static_cast<int64_t>(ch) * kDownK;
-      __syncthreads();  // the previous chunk's fragments have been read
 #pragma unroll
-      for (int i = 0; i < (kDownM * kDownK / 8) / 128; ++i) {  // 64 rows x 16 vectors of 8 bf16
-        const int idx = tid + i * 128, row = idx >> 4, vec = idx & 15;
-        const int64_t m = m0 + row;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (m < M) v = __ldg(reinterpret_cast<const uint4*>(x + m * K + k0 + vec * 8));
-        *reinterpret_cast<uint4*>(&xs[row][vec * 8]) = v;
-      }
-#pragma unroll
-      for (int i = 0; i < (32 * kDownK / 8) / 128; ++i) {
-        const int idx = tid + i * 128, jr = idx >> 4, vec = idx & 15;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (j0 + jr < r) v = __ldg(reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j0 + jr) * K + k0 + vec * 8));
-        *reinterpret_cast<uint4*>(&as[jr][vec * 8]) = v;
-      }
-      __syncthreads();
+    for (int st = 0; st < kDownStages - 1; ++st) {
+      if (st < n) load(st, st);
+      cp_async_commit();
+    }
+    for (int i = 0; i < n; ++i) {
+      cp_async_wait<kDownStages - 2>();
+      __syncthreads();  // chunk i is visible to all threads; buffer (i - 1) % kDownStages is free
+      if (i + kDownStages - 1 < n) load(i + kDownStages - 1, (i + kDownStages - 1) % kDownStages);
+      cp_async_commit();
+      const uint16_t* xs = ring + (i % kDownStages) * kDownStageElems;
+      const uint16_t* as = xs + kDownM * kRow;
 #pragma unroll
       for (int ks = 0; ks < kDownK / 16; ++ks) {
         uint32_t a[4];
-        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&xs[warp * 16 + (lane & 15)][ks * 16 + (lane >> 4) * 8])),
+        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(xs + (warp * 16 + (lane & 15)) * kRow + ks * 16 + (lane >> 4) * 8)),
                 a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int jp = 0; jp < 2; ++jp) {
           const int g8 = lane >> 3;
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&as[jp * 16 + (g8 >> 1) * 8 + (lane & 7)][ks * 16 + (g8 & 1) * 8])),
+          ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(as + (jp * 16 + (g8 >> 1) * 8 + (lane & 7)) * kRow + ks * 16 + (g8 & 1) * 8)),
                   b0, b1, b2, b3);
           mma16816(c[2 * jp], a, b0, b1);
           mma16816(c[2 * jp + 1], a, b2, b3);
         }
       }
     }
+    cp_async_wait<0>();
     // C fragment: c0,c1 at (row lane/4, cols 2(lane%4), +1); c2,c3 at row + 8
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -520,24 +599,31 @@ CUtensorMapSwizzle swizzle_for(int box_bytes) {
                            : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
+constexpr int kDW = 8;  // dequant warps of the tcgen05 kernel
+
 struct TcPlan {
-  int mbox, tiles_m, tiles_n, smem_stages;
+  int mbox, tiles_m, tiles_n, w_stages, x_stages;
   size_t smem_bytes, ws_u, ws_total;
 };
 
-// Tile shape, shared-memory ring and workspace (U only). The ring leaves room for one
-// LoRA-down CTA on the same SM, so that kernel never delays a CTA of this one.
+// Tile shape, shared-memory rings and workspace (U only). For decode tiles (64 tokens) the rings
+// leave room for one LoRA-down CTA on the same SM, so that kernel never delays a CTA of this one.
+// The activation ring (128-K sub-stages) takes 4 sub-stages when the weight ring still gets at
+// least 5 stages, else 3 when it gets 4, else 2; the weight ring takes the rest (at most 8).
 TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
   TcPlan t{};
   t.mbox = M <= 64 ? 64 : 128;
   t.tiles_m = static_cast<int>((M + t.mbox - 1) / t.mbox);
   t.tiles_n = static_cast<int>(N / kRows);
   const size_t lora = r ? static_cast<size_t>(kRows + t.mbox) * 2 * r : 0;
-  const size_t fixed = 1024 + lora + 256;
-  const size_t sb = stage_bytes(t.mbox);
-  const size_t budget = 227 * 1024 - (r ? kDownSmem + 1024 : 0);
-  t.smem_stages = budget > fixed ? static_cast<int>(std::min<size_t>(4, (budget - fixed) / sb)) : 0;
-  t.smem_bytes = fixed + t.smem_stages * sb;
+  const size_t fixed = 1024 + lora + 512;
+  const size_t xb = x_stage_bytes(t.mbox);
+  const size_t budget = 227 * 1024 - (r && t.mbox == 64 ? kDownSmem + 1024 : 0);
+  const size_t avail = budget > fixed ? budget - fixed : 0;
+  t.x_stages = avail >= 4 * xb + 5 * kWStageBytes ? 4 : avail >= 3 * xb + 4 * kWStageBytes ? 3 : 2;
+  t.w_stages =
+      avail > t.x_stages * xb ? static_cast<int>(std::min<size_t>(8, (avail - t.x_stages * xb) / kWStageBytes)) : 0;
+  t.smem_bytes = fixed + t.x_stages * xb + t.w_stages * kWStageBytes;
   size_t o = 0;
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
   t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
@@ -547,7 +633,7 @@ TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
 
 template <int MBOX>
 void* tc_kernel_ptr() {
-  return reinterpret_cast<void*>(w4a16_tc_kernel<MBOX>);
+  return reinterpret_cast<void*>(w4a16_tc_kernel<MBOX, kDW>);
 }
 
 // Clusters of `c` CTAs of the tcgen05 kernel that can be resident at once on this device.
@@ -560,7 +646,7 @@ int cluster_capacity(int device, int mbox, size_t smem, int c) {
   if (it != cache.end()) return it->second;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, c, 1);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(kDW));
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -599,6 +685,44 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
   return make_tensor_map_2d(m, dt, base, cols, rows, esize, box_cols, box_rows, sw);
 }
 
+// Cluster size of the LoRA-down kernel on this device: 16 (non-portable) where a 16-CTA cluster
+// of it can be resident, else 8. Also sets the kernel's attributes (once per device).
+int down_cluster_size(int device) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(device);
+  if (it != cache.end()) return it->second;
+  int c = 8;
+  const bool attrs =
+      cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDownSmem) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           static_cast<int>(cudaSharedmemCarveoutMaxShared)) == cudaSuccess;
+  if (attrs &&
+      cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kDownCluster, 1, 1);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kDownSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kDownCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(w4a16_lora_down_kernel), &cfg) == cudaSuccess &&
+        n > 0)
+      c = kDownCluster;
+  }
+  cudaGetLastError();
+  if (!attrs) c = 0;  // the kernel cannot be launched with its shared memory
+  cache[device] = c;
+  return c;
+}
+
 }  // namespace
 
 // 2-D tensor map over a row-major [rows][cols] array of `esize`-byte elements; zero fill outside.
@@ -617,7 +741,8 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 // True when the tcgen05 W4A16 path takes this shape.
 bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
   if (!(M > 0 && N % kRows == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= 128)))) return false;
-  return plan(M, N, K, r).smem_stages >= 2;
+  const TcPlan t = plan(M, N, K, r);
+  return t.w_stages >= 2 && t.x_stages >= 2;
 }
 
 size_t w4a16_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int) {
@@ -628,12 +753,12 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
                                cudaStream_t st) {
   const TcPlan t = plan(a.M, a.N, a.K, a.r);
   if (ws_bytes < t.ws_total) return NVFP4RL_ERR_WORKSPACE;
-  if (t.smem_stages < 2) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (t.w_stages < 2 || t.x_stages < 2) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   uint16_t* U = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + t.ws_u);
   const int smem = static_cast<int>(t.smem_bytes);
-  cudaError_t e = t.mbox == 64
-                      ? cudaFuncSetAttribute(w4a16_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                      : cudaFuncSetAttribute(w4a16_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      t.mbox == 64 ? cudaFuncSetAttribute(w4a16_tc_kernel<64, kDW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                   : cudaFuncSetAttribute(w4a16_tc_kernel<128, kDW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   const int splits = choose_splits(dev.device, t, a.K, std::min(dev.sm_count, kPlanSMs));
   const int kst = static_cast<int>(a.K / kKStage);
@@ -641,10 +766,13 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   if (a.r) {
     // LoRA down-projection: one cluster per 64 rows of x, K split over the cluster
     const int nchunks = static_cast<int>(a.K / kDownK);
-    const int cd = std::min(kDownCluster, nchunks);
+    const int dc = down_cluster_size(dev.device);
+    if (dc == 0) return NVFP4RL_ERR_CUDA;
+    const int cd = std::min(dc, nchunks);
     cudaLaunchConfig_t dcfg = {};
     dcfg.gridDim = dim3(cd, static_cast<unsigned>((a.M + kDownM - 1) / kDownM), 1);
     dcfg.blockDim = dim3(128);
+    dcfg.dynamicSmemBytes = kDownSmem;
     dcfg.stream = st;
     cudaLaunchAttribute dattr[1];
     dattr[0].id = cudaLaunchAttributeClusterDimension;
@@ -653,9 +781,6 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
     dattr[0].val.clusterDim.z = 1;
     dcfg.attrs = dattr;
     dcfg.numAttrs = 1;
-    if (cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
-      return NVFP4RL_ERR_CUDA;
     if (cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel, a.x, a.M, a.K, a.A, a.r, U) != cudaSuccess)
       return NVFP4RL_ERR_CUDA;
     if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
@@ -687,7 +812,8 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   p.w_g = a.w_g;
   p.y = a.y;
   p.status = dev.status;
-  p.smem_stages = t.smem_stages;
+  p.w_stages = t.w_stages;
+  p.x_stages = t.x_stages;
   // Split K runs as clusters of `splits` CTAs along y. With LoRA, the launch is a programmatic
   // dependent of the LoRA-down kernel: it runs alongside it and waits for it only before loading
   // U. Everything else it reads (x, weights, B_lora, g) was complete before the LoRA-down kernel
@@ -695,7 +821,7 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   // caller's previous kernel).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(t.tiles_n, splits, t.tiles_m);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(kDW));
   cfg.dynamicSmemBytes = t.smem_bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -707,8 +833,8 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.r ? 2 : 1;
-  e = t.mbox == 64 ? cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<64>, mc, ms, mx, mb, mu, p)
-                   : cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<128>, mc, ms, mx, mb, mu, p);
+  e = t.mbox == 64 ? cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<64, kDW>, mc, ms, mx, mb, mu, p)
+                   : cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<128, kDW>, mc, ms, mx, mb, mu, p);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }

@@ -251,32 +251,14 @@ __device__ __forceinline__ uint32_t bf16_rd(float v) { return __float_as_uint(v)
 // bf16 pattern of the smallest bf16 >= v (v >= 0 finite fp32).
 __device__ __forceinline__ uint32_t bf16_ru(float v) { return (__float_as_uint(v) + 0xFFFFu) >> 16; }
 
-// E2M1 codes of two fp32 values, rounded to nearest (ties to even), saturating: code(hi) in
-// bits 4-7, code(lo) in bits 0-3, the sign kept on zero.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
-  uint32_t d;
-  asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.u32.u8 %0, q;\n\t}" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-// Plain encoding of one block of bf16 values.
-//
-// Fast path (fast_ok: g within [2^-100, 2^100], block finite, scale nonzero): with
-// S = E4M3(b) * g, inv = RN(1 / RN(S)) and inv(1 +- 2^-20) rounded to nearest, the products
-// x * inv(1 + 2^-20) and x * inv(1 - 2^-20) bracket the exact quotient x / S strictly (the
-// four roundings move it by less than 4 * 2^-24 relative). When the hardware conversion of
-// both ends gives the same code, so does x / S: rounding to the E2M1 grid is monotonic.
-// When any pair differs (x / S at or within 2^-20 of a midpoint), the block is encoded by
-// the exact path below.
-//
-// Exact path, two elements per instruction. For bf16 x and a
+// Plain encoding of one block of bf16 values, two elements per instruction. For bf16 x and a
 // real P: x > P <=> x > RD_bf16(P) and x >= P <=> x > pred(RU_bf16(P)), with RD_bf16(P) =
 // RD_bf16(RD_fp32(P)) and RU_bf16(P) = RU_bf16(RU_fp32(P)); so the seven midpoint thresholds
 // become bf16 values compared with set.gt.bf16x2, and the magnitude code is the number of
 // thresholds exceeded, accumulated with add.bf16x2 on 128.0 (128 + c is exact and its low
 // three bits are c).
 __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
-                                                  float est_scale, bool fast_ok, uint8_t* __restrict__ codes,
+                                                  float est_scale, uint8_t* __restrict__ codes,
                                                   uint8_t* __restrict__ scales) {
   const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
   uint32_t aw[8];
@@ -286,31 +268,10 @@ __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t b
     aw[i] = w[i] & 0x7FFF7FFFu;
     m2 = __vmaxu2(m2, aw[i]);
   }
-  const uint32_t mbits = max(m2 & 0xFFFFu, m2 >> 16);
-  const float bamax = __uint_as_float(mbits << 16);
+  const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
   uint32_t b = 0;
   if (g > 0.0f) b = scale_byte(bamax, g, (bamax * est_scale) * inv_g6);
   const float dec = e4m3_decode_pos(b);
-  if (fast_ok && b != 0 && mbits < 0x7F80u) {
-    const float inv = __frcp_rn(dec * g);
-    const float ih = inv * (1.0f + 0x1p-20f), il = inv * (1.0f - 0x1p-20f);
-    uint32_t mism = 0, byte[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
-      const uint32_t up = cvt_e2m1x2(hi * ih, lo * ih);
-      const uint32_t dn = cvt_e2m1x2(hi * il, lo * il);
-      mism |= up ^ dn;
-      byte[i] = up;
-    }
-    if (mism == 0) {
-      const uint32_t lo32 = byte[0] | (byte[1] << 8) | (byte[2] << 16) | (byte[3] << 24);
-      const uint32_t hi32 = byte[4] | (byte[5] << 8) | (byte[6] << 16) | (byte[7] << 24);
-      *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo32, hi32);
-      scales[blk] = static_cast<uint8_t>(b);
-      return;
-    }
-  }
   uint32_t t2[7];
   if (b) {
     const uint32_t t[7] = {bf16_rd(__fmul_rd(0.25f * dec, g)), bf16_ru(__fmul_ru(0.75f * dec, g)) - 1u,
@@ -437,7 +398,6 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float g6 = 6.0f * (g * est_scale);
   const float inv_g6 = 1.0f / g6;
-  const bool fast_ok = g >= 0x1p-100f && g <= 0x1p100f;
 
   // Two blocks per iteration, both loaded before either is encoded (more bytes in flight).
   // The blocks are visited from the end of the tensor to its start: the amax pass that
@@ -451,8 +411,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
     load_block<kDtype>(x, blk, a);
     if (two) load_block<kDtype>(x, blk2, b);
     if constexpr (kDtype == NVFP4RL_BF16 && !kGuided) {
-      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, fast_ok, codes, scales);
-      if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, fast_ok, codes, scales);
+      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, codes, scales);
+      if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, codes, scales);
     } else {
       encode_block<kDtype, kGuided>(a, blk, g, est_scale, g6, mask, codes, scales);
       if (two) encode_block<kDtype, kGuided>(b, blk2, g, est_scale, g6, mask, codes, scales);
