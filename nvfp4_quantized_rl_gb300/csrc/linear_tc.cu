@@ -22,7 +22,7 @@
 //   warp 2      activation producer (TMA): per 128-K sub-stage two boxes of 64 bf16 x tokens
 //               (128-byte swizzle, read straight from x) into a separate, shallower ring;
 //               plus the LoRA tiles.
-//   warps 3-10  dequantize: thread = one weight row and half of the stage's K; 4-bit codes
+//   warps 3-18  dequantize: thread = one weight row and a quarter of the stage's K; 4-bit codes
 //               are expanded to bf16 with integer ops (a nibble swap, sign and magnitude bits
 //               moved into a bf16 bit pattern, one bf16x2 FMA by E4M3(s) * 2^94), written to
 //               TMEM with tcgen05.st; then the epilogue: TMEM -> registers, g and s applied,
@@ -84,11 +84,12 @@ struct TcParams {
   uint16_t* y;
   uint32_t* status;
   int w_stages;          // weight ring depth (256-K stages)
-  int x_stages;          // activation ring depth (128-K sub-stages)
 };
 
-// activation sub-stage: 128 K (two boxes of 64 bf16) x tokens; two per 256-K weight stage
-__host__ __device__ constexpr int x_stage_bytes(int mbox) { return 2 * mbox * 128; }
+// activation stage: 256 K (four boxes of 64 bf16) x tokens
+__host__ __device__ constexpr int x_stage_bytes(int mbox) { return 4 * mbox * 128; }
+// depth of the A-buffer / activation / stage-ready rings
+__host__ __device__ constexpr int ring_depth(int mbox) { return mbox <= 64 ? 3 : 2; }
 __host__ __device__ constexpr int threads_for(int deq_warps) { return 32 * (kFirstDeqWarp + deq_warps); }
 
 __device__ __forceinline__ uint32_t swizzle_mode_for(int box_bytes) {
@@ -133,6 +134,44 @@ __device__ __forceinline__ bool has_small_scale(uint2 sc) {
   return (((y0 - 0x01010101u) & ~y0) | ((y1 - 0x01010101u) & ~y1)) & 0x80808080u;
 }
 
+// The 16 MMAs of one 256-K stage (M = 128 weight rows, N = MBOX tokens, K = 16 each), issued
+// from one instruction sequence: K-step kk reads A from TMEM columns a_tmem + 8 kk and B from the
+// activation stage at desc0 advanced by ((kk / 4) MBOX 128 + (kk % 4) 32) bytes (128-byte
+// swizzled boxes of 64 bf16 K). The first MMA accumulates only if `accumulate`; the other 15
+// always do. Two integer adds per MMA keep the issuing thread's instruction count low.
+template <int MBOX>
+__device__ __forceinline__ void mma_stage16(uint32_t d_tmem, uint32_t a_tmem, uint64_t desc0, uint32_t idesc,
+                                            uint32_t accumulate) {
+#define NVFP4RL_BOFF(kk) ((((kk) >> 2) * MBOX * 128 + ((kk)&3) * 32) >> 4)
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b32 ta;\n\t.reg .b64 bd;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.u64 bd, %2, %5;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 16;\n\tadd.u64 bd, %2, %6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 24;\n\tadd.u64 bd, %2, %7;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 32;\n\tadd.u64 bd, %2, %8;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 40;\n\tadd.u64 bd, %2, %9;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 48;\n\tadd.u64 bd, %2, %10;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 56;\n\tadd.u64 bd, %2, %11;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 64;\n\tadd.u64 bd, %2, %12;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 72;\n\tadd.u64 bd, %2, %13;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 80;\n\tadd.u64 bd, %2, %14;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 88;\n\tadd.u64 bd, %2, %15;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 96;\n\tadd.u64 bd, %2, %16;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 104;\n\tadd.u64 bd, %2, %17;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 112;\n\tadd.u64 bd, %2, %18;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "add.u32 ta, %1, 120;\n\tadd.u64 bd, %2, %19;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(desc0), "r"(idesc), "r"(accumulate), "n"(NVFP4RL_BOFF(1)), "n"(NVFP4RL_BOFF(2)),
+      "n"(NVFP4RL_BOFF(3)), "n"(NVFP4RL_BOFF(4)), "n"(NVFP4RL_BOFF(5)), "n"(NVFP4RL_BOFF(6)), "n"(NVFP4RL_BOFF(7)),
+      "n"(NVFP4RL_BOFF(8)), "n"(NVFP4RL_BOFF(9)), "n"(NVFP4RL_BOFF(10)), "n"(NVFP4RL_BOFF(11)),
+      "n"(NVFP4RL_BOFF(12)), "n"(NVFP4RL_BOFF(13)), "n"(NVFP4RL_BOFF(14)), "n"(NVFP4RL_BOFF(15))
+      : "memory");
+#undef NVFP4RL_BOFF
+}
+
 // Dequantizes one thread's share of a stage (row `row`, chunks c0 .. c0 + NCH - 1 of 32 codes)
 // into TMEM columns starting at taddr + 16 * chunk. sc holds the chunks' scale bytes, two per
 // chunk, in order.
@@ -157,15 +196,17 @@ __device__ __forceinline__ void dequant_chunks(const uint8_t* crow, int row, int
   }
 }
 
+// 88 registers per thread: 608 threads of this kernel and a 128-thread LoRA-down CTA (72 registers)
+// fit the 64K-register file of one SM together.
 template <int MBOX, int DW>
-__global__ void __launch_bounds__(threads_for(DW), 1)
+__global__ void __maxnreg__(88)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                     const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_blora,
                     const __grid_constant__ CUtensorMap map_u, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int SW = p.w_stages, SX = p.x_stages;
-  constexpr int kAbuf = MBOX <= 64 ? 3 : 2;
+  const int SW = p.w_stages;
+  constexpr int R = ring_depth(MBOX);                // A buffers = activation stages = ready slots
   constexpr int kWarpsPerQuarter = DW / 4;           // dequant warps sharing one TMEM lane quarter
   constexpr int kChunks = 8 / kWarpsPerQuarter;      // 16-byte code chunks per thread and stage
   constexpr uint32_t kDcol = 0, kLcol = MBOX, kAcol0 = 2 * MBOX;
@@ -174,7 +215,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   // layout: activation ring (reused as the fp32 partial tile after the K loop) | weight ring |
   //         lora A tile | lora U tile | barriers
   uint8_t* xring = smem;
-  uint8_t* wring = xring + SX * kXBytes;
+  uint8_t* wring = xring + R * kXBytes;
   uint8_t* lora_a = wring + SW * kWStageBytes;
   const int lora_a_bytes = p.r ? kRows * 2 * p.r : 0;
   uint8_t* lora_u = lora_a + lora_a_bytes;
@@ -182,11 +223,12 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(lora_u + lora_u_bytes);
   uint64_t* wfull = bars;             // [SW] weight stage landed
   uint64_t* wempty = wfull + SW;      // [SW] weight stage dequantized (DW arrivals)
-  uint64_t* xfull = wempty + SW;      // [SX] activation sub-stage landed
-  uint64_t* xempty = xfull + SX;      // [SX] activation sub-stage read by the MMAs (commit)
-  uint64_t* afull = xempty + SX;      // [kAbuf] A buffer written (DW arrivals)
-  uint64_t* aempty = afull + kAbuf;   // [kAbuf] A buffer read by the MMAs (commit)
-  uint64_t* dfull = aempty + kAbuf;
+  // Stage j of the MMAs needs its A buffer written and its activation tile landed: one barrier
+  // per slot collects both (DW dequant arrivals + the activation producer's arrival and bytes),
+  // so the MMA issuer waits once per stage. One commit per stage releases both again.
+  uint64_t* ready = wempty + SW;      // [R]
+  uint64_t* consumed = ready + R;     // [R] the stage's MMAs have completed (commit)
+  uint64_t* dfull = consumed + R;
   uint64_t* lfull = dfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lfull + 1);
   float* part = reinterpret_cast<float*>(xring);  // [MBOX][kRows] fp32 partial tile (split K)
@@ -204,13 +246,9 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       mbar_init(smem_addr(&wfull[i]), 1);
       mbar_init(smem_addr(&wempty[i]), DW);
     }
-    for (int i = 0; i < SX; ++i) {
-      mbar_init(smem_addr(&xfull[i]), 1);
-      mbar_init(smem_addr(&xempty[i]), 1);
-    }
-    for (int i = 0; i < kAbuf; ++i) {
-      mbar_init(smem_addr(&afull[i]), DW);
-      mbar_init(smem_addr(&aempty[i]), 1);
+    for (int i = 0; i < R; ++i) {
+      mbar_init(smem_addr(&ready[i]), DW + 1);
+      mbar_init(smem_addr(&consumed[i]), 1);
     }
     mbar_init(smem_addr(dfull), 1);
     mbar_init(smem_addr(lfull), 1);
@@ -267,28 +305,29 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
           tma_load_2d(smem_addr(lora_a + b * kRows * p.lora_box_bytes), &map_blora, b * box_el, n0, smem_addr(lfull));
       }
       int issued = 0;
-      for (int u = 0; u < 2 * nst && ok; ++u) {  // sub-stage u = half u % 2 of stage u / 2
-        const int s = u % SX;
-        if (!mbar_wait(smem_addr(&xempty[s]), ((u / SX) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
+      for (int j = 0; j < nst && ok; ++j) {
+        const int s = j % R;
+        if (!mbar_wait(smem_addr(&consumed[s]), ((j / R) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
           ok = false;
           break;
         }
         uint8_t* st = xring + s * kXBytes;
-        const uint32_t bar = smem_addr(&xfull[s]);
+        const uint32_t bar = smem_addr(&ready[s]);
         mbar_arrive_expect_tx(bar, kXBytes);
-        const int k0 = kstage(u >> 1) * kKStage + (u & 1) * (kKStage / 2);
+        const int k0 = kstage(j) * kKStage;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) tma_load_2d(smem_addr(st + q * MBOX * 128), &map_x, k0 + q * 64, m0, bar);
-        issued = u + 1;
+        for (int q = 0; q < 4; ++q) tma_load_2d(smem_addr(st + q * MBOX * 128), &map_x, k0 + q * 64, m0, bar);
+        issued = j + 1;
       }
       if (do_lora) {
         griddep_wait();  // the LoRA-down kernel has completed and its U is visible
         for (int b = 0; b < nbox; ++b)
           tma_load_2d(smem_addr(lora_u + b * MBOX * p.lora_box_bytes), &map_u, b * box_el, m0, smem_addr(lfull));
       }
-      // drain: every issued copy has landed before the shared memory is reused or the CTA exits
-      for (int u = max(0, issued - SX); u < issued; ++u)
-        mbar_wait(smem_addr(&xfull[u % SX]), (u / SX) & 1, p.status, kStatusTimeoutDrain);
+      // drain: the last stages' activation copies have landed (their ready phases completed)
+      // before the shared memory is reused or the CTA exits
+      for (int j = max(0, issued - R); j < issued; ++j)
+        mbar_wait(smem_addr(&ready[j % R]), (j / R) & 1, p.status, kStatusTimeoutDrain);
       if (do_lora) mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
@@ -296,29 +335,15 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kRows, MBOX);
       for (int j = 0; j < nst && ok; ++j) {
-        const int a = j % kAbuf;
-        // the dequant warps arrive on afull only after waiting for the weight stage, and the
-        // activation sub-stages have their own barriers
-        if (!mbar_wait(smem_addr(&afull[a]), (j / kAbuf) & 1, p.status, kStatusTimeoutMma)) {
+        const int a = j % R;
+        if (!mbar_wait(smem_addr(&ready[a]), (j / R) & 1, p.status, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
-        for (int h = 0; h < 2 && ok; ++h) {
-          const int u = 2 * j + h, sx = u % SX;
-          if (!mbar_wait(smem_addr(&xfull[sx]), (u / SX) & 1, p.status, kStatusTimeoutMma)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t xs = smem_addr(xring + sx * kXBytes);
-#pragma unroll
-          for (int kk = 0; kk < kKStage / 32; ++kk) {
-            const uint64_t bdesc = smem_desc(xs + (kk >> 2) * MBOX * 128 + (kk & 3) * 32, 16, 1024, 2);
-            mma_f16_ts(tmem + kDcol, tmem + kAcol0 + a * 128 + (h * 8 + kk) * 8, bdesc, idesc, (j | h | kk) ? 1u : 0u);
-          }
-          mma_commit(smem_addr(&xempty[sx]));
-        }
-        mma_commit(smem_addr(&aempty[a]));
+        tc_fence_after();
+        mma_stage16<MBOX>(tmem + kDcol, tmem + kAcol0 + a * 128, smem_desc(smem_addr(xring + a * kXBytes), 16, 1024, 2),
+                          idesc, j ? 1u : 0u);
+        mma_commit(smem_addr(&consumed[a]));
       }
       if (ok && do_lora) {
         if (mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutMma)) {
@@ -347,10 +372,10 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     const int row = quarter * 32 + lane;  // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     for (int j = 0; j < nst && ok; ++j) {
-      const int s = j % SW, a = j % kAbuf;
+      const int s = j % SW, a = j % R;
       // every lane waits; the warp leaves together if any lane ran out of time
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&wfull[s]), (j / SW) & 1, p.status, kStatusTimeoutDequant) &&
-                                       mbar_wait(smem_addr(&aempty[a]), ((j / kAbuf) & 1) ^ 1, p.status,
+                                       mbar_wait(smem_addr(&consumed[a]), ((j / R) & 1) ^ 1, p.status,
                                                  kStatusTimeoutDequant));
       if (!ok) break;
       const uint8_t* st = wring + s * kWStageBytes;
@@ -369,7 +394,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_addr(&afull[a]));
+        mbar_arrive(smem_addr(&ready[a]));
         mbar_arrive(smem_addr(&wempty[s]));
       }
     }
@@ -599,17 +624,16 @@ CUtensorMapSwizzle swizzle_for(int box_bytes) {
                            : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
-constexpr int kDW = 8;  // dequant warps of the tcgen05 kernel
+constexpr int kDW = 16;  // dequant warps of the tcgen05 kernel (4 per TMEM lane quarter)
 
 struct TcPlan {
-  int mbox, tiles_m, tiles_n, w_stages, x_stages;
+  int mbox, tiles_m, tiles_n, w_stages;
   size_t smem_bytes, ws_u, ws_total;
 };
 
 // Tile shape, shared-memory rings and workspace (U only). For decode tiles (64 tokens) the rings
 // leave room for one LoRA-down CTA on the same SM, so that kernel never delays a CTA of this one.
-// The activation ring (128-K sub-stages) takes 4 sub-stages when the weight ring still gets at
-// least 5 stages, else 3 when it gets 4, else 2; the weight ring takes the rest (at most 8).
+// The activation ring has ring_depth stages; the weight ring takes the rest (at most 8 stages).
 TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
   TcPlan t{};
   t.mbox = M <= 64 ? 64 : 128;
@@ -617,13 +641,10 @@ TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
   t.tiles_n = static_cast<int>(N / kRows);
   const size_t lora = r ? static_cast<size_t>(kRows + t.mbox) * 2 * r : 0;
   const size_t fixed = 1024 + lora + 512;
-  const size_t xb = x_stage_bytes(t.mbox);
+  const size_t xring = static_cast<size_t>(ring_depth(t.mbox)) * x_stage_bytes(t.mbox);
   const size_t budget = 227 * 1024 - (r && t.mbox == 64 ? kDownSmem + 1024 : 0);
-  const size_t avail = budget > fixed ? budget - fixed : 0;
-  t.x_stages = avail >= 4 * xb + 5 * kWStageBytes ? 4 : avail >= 3 * xb + 4 * kWStageBytes ? 3 : 2;
-  t.w_stages =
-      avail > t.x_stages * xb ? static_cast<int>(std::min<size_t>(8, (avail - t.x_stages * xb) / kWStageBytes)) : 0;
-  t.smem_bytes = fixed + t.x_stages * xb + t.w_stages * kWStageBytes;
+  t.w_stages = budget > fixed + xring ? static_cast<int>(std::min<size_t>(8, (budget - fixed - xring) / kWStageBytes)) : 0;
+  t.smem_bytes = fixed + xring + t.w_stages * kWStageBytes;
   size_t o = 0;
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
   t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
@@ -742,7 +763,7 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
   if (!(M > 0 && N % kRows == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= 128)))) return false;
   const TcPlan t = plan(M, N, K, r);
-  return t.w_stages >= 2 && t.x_stages >= 2;
+  return t.w_stages >= 2;
 }
 
 size_t w4a16_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int) {
@@ -753,7 +774,7 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
                                cudaStream_t st) {
   const TcPlan t = plan(a.M, a.N, a.K, a.r);
   if (ws_bytes < t.ws_total) return NVFP4RL_ERR_WORKSPACE;
-  if (t.w_stages < 2 || t.x_stages < 2) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (t.w_stages < 2) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   uint16_t* U = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + t.ws_u);
   const int smem = static_cast<int>(t.smem_bytes);
   cudaError_t e =
@@ -813,7 +834,6 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   p.y = a.y;
   p.status = dev.status;
   p.w_stages = t.w_stages;
-  p.x_stages = t.x_stages;
   // Split K runs as clusters of `splits` CTAs along y. With LoRA, the launch is a programmatic
   // dependent of the LoRA-down kernel: it runs alongside it and waits for it only before loading
   // U. Everything else it reads (x, weights, B_lora, g) was complete before the LoRA-down kernel

@@ -251,15 +251,70 @@ __device__ __forceinline__ uint32_t bf16_rd(float v) { return __float_as_uint(v)
 // bf16 pattern of the smallest bf16 >= v (v >= 0 finite fp32).
 __device__ __forceinline__ uint32_t bf16_ru(float v) { return (__float_as_uint(v) + 0xFFFFu) >> 16; }
 
-// Plain encoding of one block of bf16 values, two elements per instruction. For bf16 x and a
+// Per-tensor lookup tables for the bf16 plain encoding, built in shared memory by every CTA
+// (they depend only on g):
+//   mid[i]  = (RD, RU) of 3 g (E4M3(i) + E4M3(i + 1)): six times the midpoint between scale
+//             bytes i and i + 1, rounded down and up (i = 0 .. 0x7D), for the exact scale byte;
+//   thr[b]  = for scale byte b, the seven element thresholds as bf16 patterns in both halves of a
+//             word, ready for the two-element compares (b = 0: +inf).
+struct EncodeTables {
+  float2 mid[0x7E];
+  uint4 thr[0x7F][2];
+};
+
+__device__ void build_encode_tables(EncodeTables& t, float g) {
+  for (int i = threadIdx.x; i < 0x7E; i += blockDim.x) {
+    const float m3 = 3.0f * (e4m3_decode_pos(i) + e4m3_decode_pos(i + 1));  // exact in fp32
+    t.mid[i] = make_float2(__fmul_rd(m3, g), __fmul_ru(m3, g));
+  }
+  for (int b = threadIdx.x; b < 0x7F; b += blockDim.x) {
+    uint32_t tk[8];
+    if (b == 0 || !(g > 0.0f)) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) tk[k] = 0x7F807F80u;  // zero scale: every code is sign|0
+    } else {
+      const float dec = e4m3_decode_pos(b);
+      const uint32_t t[7] = {bf16_rd(__fmul_rd(0.25f * dec, g)), bf16_ru(__fmul_ru(0.75f * dec, g)) - 1u,
+                             bf16_rd(__fmul_rd(1.25f * dec, g)), bf16_ru(__fmul_ru(1.75f * dec, g)) - 1u,
+                             bf16_rd(__fmul_rd(2.5f * dec, g)),  bf16_ru(__fmul_ru(3.5f * dec, g)) - 1u,
+                             bf16_rd(__fmul_rd(5.0f * dec, g))};
+#pragma unroll
+      for (int k = 0; k < 7; ++k) tk[k] = t[k] | (t[k] << 16);
+      tk[7] = 0u;
+    }
+    t.thr[b][0] = make_uint4(tk[0], tk[1], tk[2], tk[3]);
+    t.thr[b][1] = make_uint4(tk[4], tk[5], tk[6], tk[7]);
+  }
+}
+
+// Exact E4M3 scale byte of bamax / (6 g) from the estimate `est` and the midpoint table: the
+// same decision as scale_byte, with the midpoint products looked up instead of computed.
+__device__ __forceinline__ uint32_t scale_byte_tab(float bamax, float est, const EncodeTables& t) {
+  const uint32_t b = min(e4m3_estimate(est), 0x7Eu);
+  uint32_t dec = 0, inc = 0;
+  if (b > 0) {
+    const float2 m = t.mid[b - 1];
+    if (bamax < m.y) dec = 1;
+    else if (m.x == m.y && bamax == m.y && (b & 1u)) dec = 1;  // exact tie: to the even byte b-1
+  }
+  if (b < 0x7Eu) {
+    const float2 m = t.mid[b];
+    if (bamax > m.x) inc = 1;
+    else if (m.x == m.y && bamax == m.x && (b & 1u)) inc = 1;  // exact tie: to the even byte b+1
+  }
+  return b - dec + inc;
+}
+
+// Plain encoding of one block of bf16 values (finite), two elements per instruction. For bf16 x and a
 // real P: x > P <=> x > RD_bf16(P) and x >= P <=> x > pred(RU_bf16(P)), with RD_bf16(P) =
 // RD_bf16(RD_fp32(P)) and RU_bf16(P) = RU_bf16(RU_fp32(P)); so the seven midpoint thresholds
 // become bf16 values compared with set.gt.bf16x2, and the magnitude code is the number of
 // thresholds exceeded, accumulated with add.bf16x2 on 128.0 (128 + c is exact and its low
-// three bits are c).
+// three bits are c). The scale byte's midpoint products and the thresholds of every scale
+// byte come from per-tensor tables in shared memory.
 __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
-                                                  float est_scale, uint8_t* __restrict__ codes,
-                                                  uint8_t* __restrict__ scales) {
+                                                  float est_scale, const EncodeTables& tab,
+                                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
   uint32_t aw[8];
   uint32_t m2 = 0;
@@ -270,26 +325,15 @@ __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t b
   }
   const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
   uint32_t b = 0;
-  if (g > 0.0f) b = scale_byte(bamax, g, (bamax * est_scale) * inv_g6);
-  const float dec = e4m3_decode_pos(b);
-  uint32_t t2[7];
-  if (b) {
-    const uint32_t t[7] = {bf16_rd(__fmul_rd(0.25f * dec, g)), bf16_ru(__fmul_ru(0.75f * dec, g)) - 1u,
-                           bf16_rd(__fmul_rd(1.25f * dec, g)), bf16_ru(__fmul_ru(1.75f * dec, g)) - 1u,
-                           bf16_rd(__fmul_rd(2.5f * dec, g)),  bf16_ru(__fmul_ru(3.5f * dec, g)) - 1u,
-                           bf16_rd(__fmul_rd(5.0f * dec, g))};
-#pragma unroll
-    for (int k = 0; k < 7; ++k) t2[k] = t[k] | (t[k] << 16);
-  } else {
-#pragma unroll
-    for (int k = 0; k < 7; ++k) t2[k] = 0x7F807F80u;  // zero scale: every code is sign|0
-  }
+  if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, tab);
+  const uint4 ta = tab.thr[b][0], tb = tab.thr[b][1];
+  const uint32_t T2[7] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z};
   uint32_t byte[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     uint32_t acc = 0x43004300u;  // bf16x2 (128, 128)
 #pragma unroll
-    for (int k = 0; k < 7; ++k) acc = bf16x2_add(acc, bf16x2_gt(aw[i], t2[k]));
+    for (int k = 0; k < 7; ++k) acc = bf16x2_add(acc, bf16x2_gt(aw[i], T2[k]));
     const uint32_t m = acc & 0x00070007u;
     const uint32_t s = w[i] & 0x80008000u;
     // low byte: magnitude of element 2i in bits 0-2, its sign in bit 3, element 2i+1 in bits 4-7
@@ -398,6 +442,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float g6 = 6.0f * (g * est_scale);
   const float inv_g6 = 1.0f / g6;
+  __shared__ EncodeTables tab;
+  if (kDtype == NVFP4RL_BF16 && !kGuided) {
+    build_encode_tables(tab, g);
+    __syncthreads();
+  }
 
   // Two blocks per iteration, both loaded before either is encoded (more bytes in flight).
   // The blocks are visited from the end of the tensor to its start: the amax pass that
@@ -411,8 +460,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
     load_block<kDtype>(x, blk, a);
     if (two) load_block<kDtype>(x, blk2, b);
     if constexpr (kDtype == NVFP4RL_BF16 && !kGuided) {
-      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, codes, scales);
-      if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, codes, scales);
+      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
+      if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
     } else {
       encode_block<kDtype, kGuided>(a, blk, g, est_scale, g6, mask, codes, scales);
       if (two) encode_block<kDtype, kGuided>(b, blk2, g, est_scale, g6, mask, codes, scales);
