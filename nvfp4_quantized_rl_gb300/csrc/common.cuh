@@ -3,6 +3,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stdint.h>
 
 #include "../../include/nvfp4rl.h"
@@ -72,6 +74,34 @@ inline bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Programmatic dependent launch. A kernel launched with launch_pdl may start once every CTA of
+// the preceding kernel on the stream has called griddep_launch_dependents (or exited).
+// griddep_wait blocks until that preceding kernel has completed and its memory is visible (a
+// no-op for a kernel launched without the attribute). The library's kernels on the decode path
+// call griddep_wait before touching global memory and only then griddep_launch_dependents, so
+// every kernel still observes all earlier kernels complete, while the next launch overlaps the
+// current kernel's tail.
+#ifdef __CUDACC__
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Counts one kernel launch (diagnostic, see nvfp4rl_kernel_launches) and reports its status.
 void count_launch();

@@ -510,7 +510,10 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                               const uint16_t* __restrict__ A, int r,
                                                               uint16_t* __restrict__ U) {
-  // the main kernel may start now: it waits (griddepcontrol.wait) before reading U
+  // Earlier kernels on the stream (which may have written x) have completed once griddep_wait
+  // returns; only then may the main kernel start: it reads x and the weights without waiting,
+  // and waits (griddepcontrol.wait) for this kernel before reading U.
+  griddep_wait();
   griddep_launch_dependents();
   extern __shared__ __align__(16) uint8_t down_smem[];
   uint16_t* ring = reinterpret_cast<uint16_t*>(down_smem);  // [kDownStages][96][kDownK + kDownPad]
@@ -795,13 +798,15 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
     dcfg.blockDim = dim3(128);
     dcfg.dynamicSmemBytes = kDownSmem;
     dcfg.stream = st;
-    cudaLaunchAttribute dattr[1];
+    cudaLaunchAttribute dattr[2];
     dattr[0].id = cudaLaunchAttributeClusterDimension;
     dattr[0].val.clusterDim.x = cd;
     dattr[0].val.clusterDim.y = 1;
     dattr[0].val.clusterDim.z = 1;
+    dattr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the previous kernel's tail
+    dattr[1].val.programmaticStreamSerializationAllowed = 1;
     dcfg.attrs = dattr;
-    dcfg.numAttrs = 1;
+    dcfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel, a.x, a.M, a.K, a.A, a.r, U) != cudaSuccess)
       return NVFP4RL_ERR_CUDA;
     if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;

@@ -92,6 +92,8 @@ __device__ __forceinline__ uint32_t max4_abs_bf16(uint4 v) {
 template <int kDtype>
 __global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, int64_t nvec,
                                                    uint32_t* __restrict__ amax_bits) {
+  griddep_wait();
+  griddep_launch_dependents();
   uint32_t m = 0;
   const uint4* p = static_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -151,6 +153,8 @@ template <int kDtype>
 __global__ void __launch_bounds__(32 * (kAmaxWarps + 1), 1)
     amax_bulk_kernel(const uint8_t* __restrict__ x, int64_t bytes, uint32_t* __restrict__ amax_bits,
                      uint32_t* __restrict__ status) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kAmaxStages], empty[kAmaxStages];
   __shared__ uint32_t red[kAmaxWarps];
@@ -433,6 +437,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
                                                        const uint32_t* __restrict__ mask,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                        float* __restrict__ g_out) {
+  griddep_wait();
+  griddep_launch_dependents();
   const float amax = amax_in ? *amax_in : __uint_as_float(*amax_bits);
   const float g = __fdiv_rn(amax, 2688.0f);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
@@ -469,11 +475,20 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   }
 }
 
+// Clears the amax accumulator word (a kernel rather than a memset, so that it chains with the
+// neighbouring kernels by programmatic dependent launch).
+__global__ void zero_word_kernel(uint32_t* __restrict__ p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) *p = 0u;
+}
+
 }  // namespace
 
 nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
                            cudaStream_t st) {
-  if (cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), st) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  if (launch_pdl(zero_word_kernel, dim3(1), dim3(32), 0, st, amax_bits) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
   if (n == 0) return NVFP4RL_OK;
   const int64_t bytes = n * (dtype == NVFP4RL_BF16 ? 2 : 4);
   const int64_t nchunks = (bytes + kAmaxChunk - 1) / kAmaxChunk;
@@ -516,13 +531,19 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
   }
   const int64_t want = (nblocks + threads - 1) / threads;
   const int grid = static_cast<int>(want < dev.sm_count * 8 ? want : dev.sm_count * 8);
+  cudaError_t e;
   if (dtype == NVFP4RL_BF16) {
-    if (mask) quantize_kernel<NVFP4RL_BF16, true><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
-    else quantize_kernel<NVFP4RL_BF16, false><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
+    e = mask ? launch_pdl(quantize_kernel<NVFP4RL_BF16, true>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
+                          amax_in, mask, codes, scales, g)
+             : launch_pdl(quantize_kernel<NVFP4RL_BF16, false>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
+                          amax_in, mask, codes, scales, g);
   } else {
-    if (mask) quantize_kernel<NVFP4RL_F32, true><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
-    else quantize_kernel<NVFP4RL_F32, false><<<grid, threads, 0, st>>>(x, nblocks, amax_scratch, amax_in, mask, codes, scales, g);
+    e = mask ? launch_pdl(quantize_kernel<NVFP4RL_F32, true>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
+                          amax_in, mask, codes, scales, g)
+             : launch_pdl(quantize_kernel<NVFP4RL_F32, false>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
+                          amax_in, mask, codes, scales, g);
   }
+  if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }
 

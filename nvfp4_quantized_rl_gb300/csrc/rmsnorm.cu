@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_aqn_kernel(const uint16_t* _
                                                                const float* __restrict__ w,
                                                                const float* __restrict__ eps, float sigma,
                                                                float delta, uint16_t* __restrict__ y) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t row = blockIdx.x;
   const int nvec = static_cast<int>(H / 8);
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
@@ -85,8 +87,12 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_aqn_kernel(const uint16_t* _
 nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
                                   float sigma, float delta, uint16_t* y, const DeviceInfo&, cudaStream_t st) {
   if (M == 0) return NVFP4RL_OK;
-  if (eps) rmsnorm_aqn_kernel<true><<<static_cast<unsigned>(M), kThreads, 0, st>>>(x, H, w, eps, sigma, delta, y);
-  else rmsnorm_aqn_kernel<false><<<static_cast<unsigned>(M), kThreads, 0, st>>>(x, H, w, eps, sigma, delta, y);
+  const cudaError_t e =
+      eps ? launch_pdl(rmsnorm_aqn_kernel<true>, dim3(static_cast<unsigned>(M)), dim3(kThreads), 0, st, x, H, w, eps,
+                       sigma, delta, y)
+          : launch_pdl(rmsnorm_aqn_kernel<false>, dim3(static_cast<unsigned>(M)), dim3(kThreads), 0, st, x, H, w, eps,
+                       sigma, delta, y);
+  if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }
 

@@ -42,12 +42,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-// Programmatic dependent launch: a grid launched with programmatic stream serialization may start
-// once every CTA of the preceding grid has called launch_dependents (or exited); griddep_wait blocks
-// until that preceding grid has completed and its memory operations are visible. Both are no-ops
-// for a grid launched without the attribute.
-__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- thread-block clusters: rank, distributed shared memory, cluster-wide barrier ----------
 
