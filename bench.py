@@ -440,6 +440,170 @@ def run_ops(args, torch, step, ops, flush, stream, rank):
         print(json.dumps({"mode": "ops", "workload": WORKLOAD, "steps": args.steps, "warmup": args.warmup, "ops": res}))
 
 
+def run_suite(args):
+    """Secondary measurements of the other configurations on the path (not the headline step):
+    W4A4 prefill (7B shapes, 4096 tokens; 32B gate, 8192 tokens), W4A16 at 256 tokens on the 32B
+    shapes, the grouped MoE layer (128 experts, 32768 routed rows), and the NVFP4 encode of one 32B
+    layer. One JSON line per case: device time per call through the public API (eager, a 256 MB
+    read evicts L2 before each call), achieved TFLOP/s and GB/s, and the fraction of the binding
+    roof (FP4 tensor peak = the measured bf16 peak x 6, the nominal 13.5 / 2.25 ratio)."""
+    import torch
+    import nvfp4_quantized_rl_gb300 as nv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4321)
+    hbm, bf16_tf, src = peaks()
+    fp4_tf = bf16_tf * 6.0
+    flush64 = torch.empty(256 << 20, dtype=torch.uint8, device=dev).view(torch.int64)
+
+    def randn(*shape, std=1.0):
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).mul_(std)
+
+    def weight(n, k, std=0.02):
+        w = randn(n, k, std=std)
+        cols = torch.randperm(k, generator=gen, device=dev)[: round(0.01 * k)]
+        w[:, cols] *= 8
+        return w.to(torch.bfloat16)
+
+    def activations(m, k, heavy=True):
+        x = randn(m, k)
+        if heavy:  # 1% of the channels Student-t(4)
+            ch = torch.randperm(k, generator=gen, device=dev)[: max(1, round(0.01 * k))]
+            z = randn(m, ch.numel())
+            chi = (randn(m, ch.numel()) ** 2 + randn(m, ch.numel()) ** 2 + randn(m, ch.numel()) ** 2 +
+                   randn(m, ch.numel()) ** 2) / 4
+            x[:, ch] = z / chi.sqrt()
+        return x.to(torch.bfloat16)
+
+    def timed(fn, reps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush64.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return float(np.median(ts))
+
+    def emit(case, us, flops, nbytes, bound, extra=None):
+        tf = flops / us / 1e6 if flops else None
+        gbs = nbytes / us / 1e3
+        if bound == "fp4":
+            roof = {"bound": "tensor", "dtype": "fp4", "achieved": tf, "peak": fp4_tf, "unit": "TFLOP/s",
+                    "frac": tf / fp4_tf, "peak_source": f"{src} bf16 x 6 (nominal fp4/bf16 ratio)"}
+        elif bound == "bf16":
+            roof = {"bound": "tensor", "dtype": "bf16", "achieved": tf, "peak": bf16_tf, "unit": "TFLOP/s",
+                    "frac": tf / bf16_tf, "peak_source": src}
+        else:
+            roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "peak_source": src}
+        line = {"mode": "suite", "case": case, "us": us, "TFLOP/s": tf, "GB/s": gbs, "roofline": roof}
+        if extra:
+            line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    r = RANK
+    cases = set((args.suite or "all").split(","))
+
+    def want(name):
+        return "all" in cases or name in cases
+
+    # ---- W4A4 prefill, 7B shapes, 4096 tokens (LoRA r = 32)
+    if want("w4a4_7b"):
+        M = 4096
+        for name, n, k in [("q", 3584, 3584), ("gate", 18944, 3584), ("down", 3584, 18944)]:
+            W = weight(n, k)
+            c, sc, g = nv.nvfp4_quantize(W)
+            del W
+            x = activations(M, k)
+            A, B = randn(r, k, std=0.02).to(torch.bfloat16), randn(n, r, std=0.02).to(torch.bfloat16)
+            y = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(nv.workspace_bytes(nv.OP_LINEAR_W4A4, M, n, k, r), dtype=torch.uint8, device=dev)
+            us = timed(lambda: nv.nvfp4_lora_linear_w4a4(x, c, sc, g, A, B, S_LORA, out=y, workspace=ws), 10)
+            emit(f"w4a4_7b_{name}_m{M}", us, flops_linear(M, n, k, r),
+                 n * k * 0.5625 + 2 * M * k + 2 * M * n + 2 * r * (k + n), "fp4",
+                 {"shape": [M, n, k], "note": "full API: activation amax + NVFP4 encode, LoRA down, FP4 GEMM + LoRA up"})
+            del c, sc, g, x, A, B, y, ws
+            torch.cuda.empty_cache()
+    # ---- 32B shapes: W4A16 at 256 tokens (r = 64), W4A4 gate at 8192 tokens
+    if want("w4a16_32b") or want("w4a4_32b"):
+        r32 = 64
+        for name, n, k in [("q", 5120, 5120), ("gate", 27648, 5120), ("down", 5120, 27648)]:
+            W = weight(n, k, 0.015)
+            c, sc, g = nv.nvfp4_quantize(W)
+            del W
+            A, B = randn(r32, k, std=0.02).to(torch.bfloat16), randn(n, r32, std=0.02).to(torch.bfloat16)
+            if want("w4a16_32b"):
+                M = 256
+                x = activations(M, k, heavy=False)
+                y = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
+                ws = torch.empty(nv.workspace_bytes(nv.OP_LINEAR_W4A16, M, n, k, r32), dtype=torch.uint8, device=dev)
+                us = timed(lambda: nv.nvfp4_lora_linear(x, c, sc, g, A, B, S_LORA, out=y, workspace=ws), 10)
+                emit(f"w4a16_32b_{name}_m{M}", us, flops_linear(M, n, k, r32),
+                     n * k * 0.5625 + 2 * M * k + 2 * M * n + 2 * r32 * (k + n), "bf16", {"shape": [M, n, k]})
+                del x, y, ws
+            if want("w4a4_32b") and name == "gate":
+                M = 8192
+                x = activations(M, k)
+                y = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
+                ws = torch.empty(nv.workspace_bytes(nv.OP_LINEAR_W4A4, M, n, k, r32), dtype=torch.uint8, device=dev)
+                us = timed(lambda: nv.nvfp4_lora_linear_w4a4(x, c, sc, g, A, B, S_LORA, out=y, workspace=ws), 5)
+                emit(f"w4a4_32b_{name}_m{M}", us, flops_linear(M, n, k, r32),
+                     n * k * 0.5625 + 2 * M * k + 2 * M * n + 2 * r32 * (k + n), "fp4", {"shape": [M, n, k]})
+                del x, y, ws
+            del c, sc, g, A, B
+            torch.cuda.empty_cache()
+    # ---- MoE layer: 128 experts, H = 2048, I = 768, 4096 tokens x top-8 = 32768 rows, grouped W4A4
+    if want("moe"):
+        E, H, I, T, TOPK = 128, 2048, 768, 4096, 8
+        logits = randn(T, E)
+        top = torch.topk(torch.softmax(logits, dim=1), TOPK, dim=1).indices.reshape(-1)
+        counts = torch.bincount(top, minlength=E)
+        offsets = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+        offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+        rows = int(offsets[-1].item())
+        for name, n, k in [("gate", I, H), ("down", H, I)]:
+            codes = torch.empty(E, n, k // 2, dtype=torch.uint8, device=dev)
+            scales = torch.empty(E, n, k // 16, dtype=torch.uint8, device=dev)
+            gs = torch.empty(E, dtype=torch.float32, device=dev)
+            for e in range(E):
+                W = (randn(n, k, std=0.02)).to(torch.bfloat16)
+                nv.nvfp4_quantize(W, codes=codes[e], scales=scales[e], g=gs[e:e + 1])
+            x = activations(rows, k, heavy=False)
+            y = torch.empty(rows, n, dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(nv.workspace_bytes(nv.OP_LINEAR_W4A4, rows, n, k, 0, E), dtype=torch.uint8, device=dev)
+            us = timed(lambda: nv.nvfp4_lora_linear_w4a4(x, codes, scales, gs, group_offsets=offsets, num_groups=E,
+                                                         out=y, workspace=ws), 10)
+            emit(f"moe_{name}_rows{rows}", us, 2 * rows * n * k, E * n * k * 0.5625 + 2 * rows * k + 2 * rows * n,
+                 "hbm", {"shape": [rows, n, k], "experts": E})
+            del codes, scales, gs, x, y, ws
+            torch.cuda.empty_cache()
+    # ---- NVFP4 encode of one 32B layer's weights (q, k, v, o, gate, up, down; bf16)
+    if want("quantize_32b"):
+        tot_us, tot_bytes = 0.0, 0.0
+        for name, n, k in [("q", 5120, 5120), ("k", 1024, 5120), ("v", 1024, 5120), ("o", 5120, 5120),
+                           ("gate", 27648, 5120), ("up", 27648, 5120), ("down", 5120, 27648)]:
+            W = weight(n, k, 0.015)
+            c = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+            sc = torch.empty(n, k // 16, dtype=torch.uint8, device=dev)
+            g = torch.empty(1, dtype=torch.float32, device=dev)
+            wsq = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
+            us = timed(lambda: nv.nvfp4_quantize(W, codes=c, scales=sc, g=g, workspace=wsq), 5)
+            tot_us += us
+            tot_bytes += bytes_quantize(n * k)
+            del W, c, sc, g
+            torch.cuda.empty_cache()
+        emit("quantize_32b_layer", tot_us, 0, tot_bytes, "hbm",
+             {"note": "amax + encode of the seven weights, each call timed separately and summed; bytes count each "
+                      "element once (2 B in, 0.5625 B out)"})
+
+
 def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, Q, Y, h1, h2, ws, flush, inputs,
             world):
     """Same step through the public API, with each step's inputs copied from pinned host memory and every
@@ -587,11 +751,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--op", default=None, help="time single ops of the step instead (see select_ops)")
+    ap.add_argument("--suite", default=None,
+                    help="secondary measurements instead: all or any of w4a4_7b,w4a16_32b,w4a4_32b,moe,quantize_32b")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.suite:
+        run_suite(args)
     else:
         run_gpu(args)
 

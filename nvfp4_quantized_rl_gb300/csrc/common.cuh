@@ -150,6 +150,12 @@ constexpr int kPlanSMs = 152;
 bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                         int esize, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
 
+// LoRA down-projection U = bf16(x A^T), [M][r] row-major, K a multiple of 64 (linear_tc.cu):
+// clusters of CTAs split K and reduce in distributed shared memory. Launched as a programmatic
+// dependent of the previous kernel on the stream; it waits for that kernel before reading x.
+nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
+                                const DeviceInfo& dev, cudaStream_t st);
+
 // tcgen05 W4A4 block-scaled path (linear_w4a4_tc.cu).
 bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r);
 size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups);

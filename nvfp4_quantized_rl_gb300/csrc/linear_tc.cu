@@ -762,6 +762,31 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// LoRA down-projection: one cluster per 64 rows of x, K (a multiple of 64) split over the cluster.
+nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
+                                const DeviceInfo& dev, cudaStream_t st) {
+  const int nchunks = static_cast<int>(K / kDownK);
+  const int dc = down_cluster_size(dev.device);
+  if (dc == 0) return NVFP4RL_ERR_CUDA;
+  const int cd = std::min(dc, nchunks);
+  cudaLaunchConfig_t dcfg = {};
+  dcfg.gridDim = dim3(cd, static_cast<unsigned>((M + kDownM - 1) / kDownM), 1);
+  dcfg.blockDim = dim3(128);
+  dcfg.dynamicSmemBytes = kDownSmem;
+  dcfg.stream = st;
+  cudaLaunchAttribute dattr[2];
+  dattr[0].id = cudaLaunchAttributeClusterDimension;
+  dattr[0].val.clusterDim.x = cd;
+  dattr[0].val.clusterDim.y = 1;
+  dattr[0].val.clusterDim.z = 1;
+  dattr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the previous kernel's tail
+  dattr[1].val.programmaticStreamSerializationAllowed = 1;
+  dcfg.attrs = dattr;
+  dcfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel, x, M, K, A, r, U) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  return launch_status();
+}
+
 // True when the tcgen05 W4A16 path takes this shape.
 bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
   if (!(M > 0 && N % kRows == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= 128)))) return false;
@@ -788,28 +813,8 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   const int kst = static_cast<int>(a.K / kKStage);
 
   if (a.r) {
-    // LoRA down-projection: one cluster per 64 rows of x, K split over the cluster
-    const int nchunks = static_cast<int>(a.K / kDownK);
-    const int dc = down_cluster_size(dev.device);
-    if (dc == 0) return NVFP4RL_ERR_CUDA;
-    const int cd = std::min(dc, nchunks);
-    cudaLaunchConfig_t dcfg = {};
-    dcfg.gridDim = dim3(cd, static_cast<unsigned>((a.M + kDownM - 1) / kDownM), 1);
-    dcfg.blockDim = dim3(128);
-    dcfg.dynamicSmemBytes = kDownSmem;
-    dcfg.stream = st;
-    cudaLaunchAttribute dattr[2];
-    dattr[0].id = cudaLaunchAttributeClusterDimension;
-    dattr[0].val.clusterDim.x = cd;
-    dattr[0].val.clusterDim.y = 1;
-    dattr[0].val.clusterDim.z = 1;
-    dattr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the previous kernel's tail
-    dattr[1].val.programmaticStreamSerializationAllowed = 1;
-    dcfg.attrs = dattr;
-    dcfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel, a.x, a.M, a.K, a.A, a.r, U) != cudaSuccess)
-      return NVFP4RL_ERR_CUDA;
-    if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+    const nvfp4rl_status sd = launch_lora_down(a.x, a.M, a.K, a.A, a.r, U, dev, st);
+    if (sd != NVFP4RL_OK) return sd;
   }
 
   CUtensorMap mc, ms, mx, mb, mu;

@@ -6,19 +6,24 @@
 // take both operands as packed E2M1 with their block scales, and the epilogue applies
 // g_x * g_w and adds the LoRA branch s (x A^T) B^T computed from the bf16 activations
 // (QeRL explainer, section "NVFP4量子化とLoRA"). Grouped mode runs one weight matrix per
-// MoE expert over that expert's contiguous block of routed rows.
+// MoE expert over that expert's contiguous block of routed rows. U = bf16(x A^T) comes from the
+// cluster LoRA-down kernel that the W4A16 path uses (linear_tc.cu), launched before this one.
 //
 // Persistent kernel, one CTA per SM, tile = 128 activation rows x 128 weight rows:
 //   warp 0      TMA producer: per 256-K stage the activation and weight code tiles
 //               (128 x 128 bytes each, 128-byte swizzle) and both 128 x 16-byte scale tiles.
-//   warp 1      MMA warp: re-lays the stage's scale bytes into the 32 x 16-byte groups
-//               tcgen05.cp expects (row r of a 128-row block goes to group row r % 32, word
-//               r / 32), copies them to TMEM, and one thread issues four
-//               tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each); at the
-//               end of a tile the LoRA up-projection (U tile x B_lora tile^T, kind::f16)
-//               goes to a separate accumulator.
+//   warp 1      allocates TMEM; one thread issues four tcgen05.mma
+//               kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each) per stage; at the end of
+//               a tile the LoRA up-projection (U tile x B_lora tile^T, kind::f16) goes to a
+//               separate accumulator.
 //   warps 2-5   epilogue: TMEM -> registers, Y = g_x g_w D + s D_lora, bf16 stores; the
 //               accumulator is double buffered so it overlaps the next tile's main loop.
+//   warps 6-9   scale factors: each warp writes the stage's scale bytes of both operands into
+//               its own TMEM lane quarter with tcgen05.st (lane i, column 4t + w holds the four
+//               bytes of row 32w + i for K step t: the four lane quarters hold the same copy).
+//               This keeps the scale traffic off the tensor pipe, where a shared-memory ->
+//               TMEM copy per K step and operand would cost about as much as the MMAs.
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,8 +42,8 @@ constexpr int kKStage = 256;
 constexpr int kCodeBytes = kTile * kKStage / 2;   // 16 KB per operand
 constexpr int kSfBytes = kTile * kKStage / 16;    // 2 KB per operand
 constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSfBytes;
-constexpr int kAtomBytes = 2 * 4 * 512;           // per stage: A and B, 4 K-steps x 512 bytes
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kFirstSfWarp = 6;
 constexpr uint32_t kD0 = 0, kD1 = 128, kDL = 256, kSF = 384;  // TMEM columns
 
 struct W4a4Params {
@@ -106,12 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  uint8_t* atoms = smem + S * kStageBytes;          // S x kAtomBytes
-  uint8_t* lora_u = atoms + S * kAtomBytes;         // 128 x 2r
+  uint8_t* lora_u = smem + S * kStageBytes;         // 128 x 2r
   const int lbytes = p.r ? kTile * 2 * p.r : 0;
   uint8_t* lora_b = lora_u + lbytes;                // 128 x 2r
   uint64_t* full = reinterpret_cast<uint64_t*>(lora_b + lbytes);
-  uint64_t* empty = full + S;
+  uint64_t* sfready = full + S;     // stage's scale factors in TMEM (4 scale warps)
+  uint64_t* empty = sfready + S;    // stage's MMAs done: shared memory and scale columns free
   uint64_t* dfull = empty + S;      // [2]
   uint64_t* dempty = dfull + 2;     // [2]
   uint64_t* lfull = dempty + 2;     // LoRA operands landed
@@ -125,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&sfready[i]), 4);
       mbar_init(smem_addr(&empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -191,48 +197,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lora_issued) mbar_wait(smem_addr(lfull), (lora_issued - 1) & 1, p.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA (+ scale-factor relayout)
-    const uint32_t idesc = idesc_nvf4_f32(kTile, kTile);
-    const uint32_t idesc_l = idesc_bf16_f32(kTile, kTile);
-    int it = 0, li = 0;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
-      const int buf = li & 1;
-      const uint32_t dcol = buf ? kD1 : kD0;
-      // every lane waits; the warp leaves together if any lane ran out of time
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&dempty[buf]), ((li >> 1) & 1) ^ 1, p.status, kStatusTimeoutMma));
-      if (!ok) break;
-      tc_fence_after();
-      for (int k = 0; k < ksteps; ++k, ++it) {
-        const int s = it % S;
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (it / S) & 1, p.status, kStatusTimeoutMma));
-        if (!ok) break;
-        // scale factors: [128 rows][16 bytes] row-major -> per K-step t a 512-byte group where
-        // group row i holds the 4 bytes of rows i, 32+i, 64+i, 96+i
-        const uint8_t* st = smem + s * kStageBytes;
-        uint8_t* at = atoms + s * kAtomBytes;
-#pragma unroll
-        for (int op = 0; op < 2; ++op) {
-          const uint4* sf = reinterpret_cast<const uint4*>(st + 2 * kCodeBytes + op * kSfBytes);
-          const uint4 r0 = sf[lane], r1 = sf[32 + lane], r2 = sf[64 + lane], r3 = sf[96 + lane];
-          uint4* dst = reinterpret_cast<uint4*>(at + op * 2048);
-          dst[0 * 32 + lane] = make_uint4(r0.x, r1.x, r2.x, r3.x);
-          dst[1 * 32 + lane] = make_uint4(r0.y, r1.y, r2.y, r3.y);
-          dst[2 * 32 + lane] = make_uint4(r0.z, r1.z, r2.z, r3.z);
-          dst[3 * 32 + lane] = make_uint4(r0.w, r1.w, r2.w, r3.w);
+    // ---------------------------------------------------------------- MMA issuer (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_nvf4_f32(kTile, kTile);
+      const uint32_t idesc_l = idesc_bf16_f32(kTile, kTile);
+      int it = 0, li = 0;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
+        const int buf = li & 1;
+        const uint32_t dcol = buf ? kD1 : kD0;
+        if (!mbar_wait(smem_addr(&dempty[buf]), ((li >> 1) & 1) ^ 1, p.status, kStatusTimeoutMma)) {
+          ok = false;
+          break;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
+        tc_fence_after();
+        for (int k = 0; k < ksteps; ++k, ++it) {
+          const int s = it % S;
+          // the scale warps arrive only after the stage's TMA bytes have landed (they wait on full[s])
+          if (!mbar_wait(smem_addr(&sfready[s]), (it / S) & 1, p.status, kStatusTimeoutMma)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           // each pipeline stage owns 32 scale-factor columns: stage s is refilled (and its columns
           // rewritten) only after the MMAs that read them have completed (empty[s])
           const uint32_t sfcol = kSF + s * 32;
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            tmem_cp_32x128b_x4(tmem + sfcol + tt * 4, smem_desc(smem_addr(at + tt * 512), 0, 128, 0));
-            tmem_cp_32x128b_x4(tmem + sfcol + 16 + tt * 4, smem_desc(smem_addr(at + 2048 + tt * 512), 0, 128, 0));
-          }
-          const uint32_t xa = smem_addr(st), wa = smem_addr(st + kCodeBytes);
+          const uint32_t xa = smem_addr(smem + s * kStageBytes), wa = xa + kCodeBytes;
 #pragma unroll
           for (int tt = 0; tt < 4; ++tt) {
             const uint64_t ad = smem_desc(xa + tt * 32, 16, 1024, 2);
@@ -242,29 +231,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(smem_addr(&empty[s]));
         }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (p.r) {
-        if (lane == 0) {
-          const bool got = mbar_wait(smem_addr(lfull), li & 1, p.status, kStatusTimeoutMma);
-          if (got) {
-            tc_fence_after();
-            const uint32_t sw = lora_swizzle(p.lora_box_bytes), sbo = 8 * p.lora_box_bytes;
-            const uint32_t ua = smem_addr(lora_u), ba = smem_addr(lora_b);
-            for (int kk = 0; kk < p.r / 16; ++kk) {
-              const int off = kk * 32, box = off / p.lora_box_bytes, in = off % p.lora_box_bytes;
-              mma_f16_ss(tmem + kDL, smem_desc(ua + box * kTile * p.lora_box_bytes + in, 16, sbo, sw),
-                         smem_desc(ba + box * kTile * p.lora_box_bytes + in, 16, sbo, sw), idesc_l, kk ? 1u : 0u);
-            }
-          } else {
+        if (!ok) break;
+        if (p.r) {
+          if (!mbar_wait(smem_addr(lfull), li & 1, p.status, kStatusTimeoutMma)) {
             ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sw = lora_swizzle(p.lora_box_bytes), sbo = 8 * p.lora_box_bytes;
+          const uint32_t ua = smem_addr(lora_u), ba = smem_addr(lora_b);
+          for (int kk = 0; kk < p.r / 16; ++kk) {
+            const int off = kk * 32, box = off / p.lora_box_bytes, in = off % p.lora_box_bytes;
+            mma_f16_ss(tmem + kDL, smem_desc(ua + box * kTile * p.lora_box_bytes + in, 16, sbo, sw),
+                       smem_desc(ba + box * kTile * p.lora_box_bytes + in, 16, sbo, sw), idesc_l, kk ? 1u : 0u);
           }
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        mma_commit(smem_addr(&dfull[buf]));
       }
-      if (lane == 0) mma_commit(smem_addr(&dfull[buf]));
-      __syncwarp();
+    }
+    __syncwarp();
+  } else if (warp >= kFirstSfWarp) {
+    // ---------------------------------------------------------------- scale factors -> TMEM
+    // Scale tile in shared memory: [128 rows][16 bytes], word t = the four block scales of K
+    // step t. Lane i gathers rows i, 32 + i, 64 + i, 96 + i and writes, per operand, 16 columns:
+    // column 4t + w = row 32w + i, K step t (the layout the MMA reads for M = 128).
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int k = 0; k < ksteps; ++k, ++it) {
+        const int s = it % S;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (it / S) & 1, p.status, kStatusTimeoutMma));
+        if (!ok) break;
+        const uint8_t* st = smem + s * kStageBytes + 2 * kCodeBytes;
+        const uint32_t sfcol = kSF + s * 32;
+#pragma unroll
+        for (int op = 0; op < 2; ++op) {
+          const uint4* sf = reinterpret_cast<const uint4*>(st + op * kSfBytes);
+          const uint4 r0 = sf[lane], r1 = sf[32 + lane], r2 = sf[64 + lane], r3 = sf[96 + lane];
+          const uint32_t v[16] = {r0.x, r1.x, r2.x, r3.x, r0.y, r1.y, r2.y, r3.y,
+                                  r0.z, r1.z, r2.z, r3.z, r0.w, r1.w, r2.w, r3.w};
+          tmem_st16(tmem + lane_base + sfcol + op * 16, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sfready[s]));
+      }
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
@@ -322,30 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// U = bf16(x A^T) (LoRA down-projection from the bf16 activations). One CTA per row.
-__global__ void __launch_bounds__(256) lora_down_bf16_kernel(const uint16_t* __restrict__ x, int64_t K,
-                                                             const uint16_t* __restrict__ A, int r,
-                                                             uint16_t* __restrict__ U) {
-  const int64_t m = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
-  for (int j = warp; j < r; j += 8) {
-    const uint4* ar = reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j) * K);
-    float acc = 0.0f;
-    for (int64_t v = lane; v < K / 8; v += 32) {
-      const uint4 xv = xr[v], av = __ldg(ar + v);
-      const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w}, aq[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc = fmaf(__uint_as_float(bf16_lo_bits(xq[q])), __uint_as_float(bf16_lo_bits(aq[q])), acc);
-        acc = fmaf(__uint_as_float(bf16_hi_bits(xq[q])), __uint_as_float(bf16_hi_bits(aq[q])), acc);
-      }
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) U[m * r + j] = static_cast<uint16_t>(f32_to_bf16_bits(acc));
-  }
-}
-
 // tile_start[e] = sum over e' < e of ceil(rows(e') / 128); tile_start[groups] = total row tiles.
 __global__ void __launch_bounds__(1024) tile_map128_kernel(const int32_t* __restrict__ offsets, int groups,
                                                            int32_t* __restrict__ tile_start) {
@@ -373,8 +361,8 @@ W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups) {
   const size_t lora = r ? 2 * static_cast<size_t>(kTile) * 2 * r : 0;
   const size_t fixed = 1024 + lora + 512;
   // at most 4 stages: TMEM holds 2 x 128 accumulator + 128 LoRA + 4 x 32 scale-factor columns
-  t.stages = static_cast<int>(std::min<size_t>(4, (227 * 1024 - fixed) / (kStageBytes + kAtomBytes)));
-  t.smem = fixed + t.stages * (kStageBytes + kAtomBytes);
+  t.stages = static_cast<int>(std::min<size_t>(4, (227 * 1024 - fixed) / kStageBytes));
+  t.smem = fixed + t.stages * kStageBytes;
   size_t o = 0;
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
   t.ws_codes = take(static_cast<size_t>(M) * K / 2);
@@ -421,8 +409,8 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
                                       reinterpret_cast<uint32_t*>(base + t.ws_amax), dev, st);
   if (sq != NVFP4RL_OK) return sq;
   if (a.r) {
-    lora_down_bf16_kernel<<<static_cast<unsigned>(a.M), 256, 0, st>>>(a.x, a.K, a.A, a.r, U);
-    if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+    const nvfp4rl_status sd = launch_lora_down(a.x, a.M, a.K, a.A, a.r, U, dev, st);
+    if (sd != NVFP4RL_OK) return sd;
   }
   if (a.offsets) {
     tile_map128_kernel<<<1, 1024, 0, st>>>(a.offsets, groups, tiles);
