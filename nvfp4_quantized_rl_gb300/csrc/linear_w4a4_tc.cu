@@ -9,9 +9,13 @@
 // MoE expert over that expert's contiguous block of routed rows. U = bf16(x A^T) comes from the
 // cluster LoRA-down kernel that the W4A16 path uses (linear_tc.cu), launched before this one.
 //
-// Persistent kernel, one CTA per SM, tile = 128 activation rows x 128 weight rows:
-//   warp 0      TMA producer: per 256-K stage the activation and weight code tiles
-//               (128 x 128 bytes each, 128-byte swizzle) and both 128 x 16-byte scale tiles.
+// Persistent kernel, one CTA per SM, tile = 128 activation rows x 128 weight rows, 256-K
+// stages. The MMAs of a stage take ~0.13 us while one trip through a shared-memory ring (TMA,
+// scale factors to TMEM, MMA issue, MMA completion back to the producer) takes well over
+// 1 us, so the operand codes have a deep ring of their own and the small scale tiles a
+// separate one that runs ahead:
+//   warp 0      code producer (TMA): per stage the activation and weight code tiles (128 x 128
+//               bytes each, 128-byte swizzle) into the code ring.
 //   warp 1      allocates TMEM; one thread issues four tcgen05.mma
 //               kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each) per stage; at the end of
 //               a tile the LoRA up-projection (U tile x B_lora tile^T, kind::f16) goes to a
@@ -20,9 +24,12 @@
 //               accumulator is double buffered so it overlaps the next tile's main loop.
 //   warps 6-9   scale factors: each warp writes the stage's scale bytes of both operands into
 //               its own TMEM lane quarter with tcgen05.st (lane i, column 4t + w holds the four
-//               bytes of row 32w + i for K step t: the four lane quarters hold the same copy).
-//               This keeps the scale traffic off the tensor pipe, where a shared-memory ->
-//               TMEM copy per K step and operand would cost about as much as the MMAs.
+//               bytes of row 32w + i for K step t: the four lane quarters hold the same copy),
+//               into one of four TMEM slots that the MMAs release. This keeps the scale traffic
+//               off the tensor pipe, where a shared-memory -> TMEM copy per K step and operand
+//               would cost about as much as the MMAs.
+//   warp 10     scale producer (TMA): both 128 x 16-byte scale tiles per stage into the scale
+//               ring, which the scale warps release as soon as they have read it.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -41,9 +48,15 @@ constexpr int kTile = 128;
 constexpr int kKStage = 256;
 constexpr int kCodeBytes = kTile * kKStage / 2;   // 16 KB per operand
 constexpr int kSfBytes = kTile * kKStage / 16;    // 2 KB per operand
-constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSfBytes;
-constexpr int kThreads = 320;
+constexpr int kCodeStageBytes = 2 * kCodeBytes;  // code ring stage: activation + weight codes
+constexpr int kSfStageBytes = 2 * kSfBytes;      // scale ring stage: activation + weight scales
+constexpr int kSfRing = 4;                       // scale ring stages
+constexpr int kSfSlots = 4;                      // TMEM scale-factor slots (32 columns each)
+constexpr int kMaxCodeStages = 6;
+constexpr int kDoneRing = 8;                     // "stage's MMAs done" barriers, > kMaxCodeStages, kSfSlots
+constexpr int kThreads = 352;
 constexpr int kFirstSfWarp = 6;
+constexpr int kSfProducerWarp = 10;
 constexpr uint32_t kD0 = 0, kD1 = 128, kDL = 256, kSF = 384;  // TMEM columns
 
 struct W4a4Params {
@@ -103,6 +116,26 @@ __device__ __forceinline__ uint32_t lora_swizzle(int box_bytes) {
   return box_bytes == 128 ? 2u : box_bytes == 64 ? 4u : 6u;
 }
 
+// Four block-scaled MMAs over one 256-K stage from one instruction sequence: K step t reads the
+// operand tiles 32 bytes further along the swizzled rows (descriptor start address + 2) and
+// scale-factor columns 4t further on.
+__device__ __forceinline__ void mma_stage_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 a1, b1;\n\t.reg .b32 s1, s2;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t"
+      "add.u64 a1, %1, 2;\n\tadd.u64 b1, %2, 2;\n\tadd.u32 s1, %4, 4;\n\tadd.u32 s2, %5, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [s1], [s2], t;\n\t"
+      "add.u64 a1, %1, 4;\n\tadd.u64 b1, %2, 4;\n\tadd.u32 s1, %4, 8;\n\tadd.u32 s2, %5, 8;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [s1], [s2], t;\n\t"
+      "add.u64 a1, %1, 6;\n\tadd.u64 b1, %2, 6;\n\tadd.u32 s1, %4, 12;\n\tadd.u32 s2, %5, 12;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [s1], [s2], t;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     w4a4_tc_kernel(const __grid_constant__ CUtensorMap map_xc, const __grid_constant__ CUtensorMap map_xs,
                    const __grid_constant__ CUtensorMap map_wc, const __grid_constant__ CUtensorMap map_ws,
@@ -110,17 +143,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const W4a4Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.stages;
-  uint8_t* lora_u = smem + S * kStageBytes;         // 128 x 2r
+  const int S = p.stages;                           // code ring stages
+  uint8_t* sfring = smem + S * kCodeStageBytes;     // kSfRing x kSfStageBytes
+  uint8_t* lora_u = sfring + kSfRing * kSfStageBytes;  // 128 x 2r
   const int lbytes = p.r ? kTile * 2 * p.r : 0;
   uint8_t* lora_b = lora_u + lbytes;                // 128 x 2r
-  uint64_t* full = reinterpret_cast<uint64_t*>(lora_b + lbytes);
-  uint64_t* sfready = full + S;     // stage's scale factors in TMEM (4 scale warps)
-  uint64_t* empty = sfready + S;    // stage's MMAs done: shared memory and scale columns free
-  uint64_t* dfull = empty + S;      // [2]
-  uint64_t* dempty = dfull + 2;     // [2]
-  uint64_t* lfull = dempty + 2;     // LoRA operands landed
-  uint64_t* lempty = lfull + 1;     // LoRA operand smem + D_lora free
+  // mdone[i % kDoneRing]: one tcgen05.commit per stage i. The code producer waits for stage
+  // i - S before refilling its code slot, the scale warps for stage i - kSfSlots before
+  // rewriting its TMEM scale slot. Neither can fall kDoneRing stages behind the MMAs (those
+  // stages would need operands that the waiter has not provided yet), so the parity of the
+  // phase a waiter looks for is never ambiguous.
+  uint64_t* cfull = reinterpret_cast<uint64_t*>(lora_b + lbytes);
+  uint64_t* mdone = cfull + kMaxCodeStages;         // [kDoneRing]
+  uint64_t* ffull = mdone + kDoneRing;              // scale tiles landed
+  uint64_t* fempty = ffull + kSfRing;               // scale tiles read by the 4 scale warps
+  uint64_t* sfready = fempty + kSfRing;             // TMEM scale slot written by the 4 scale warps
+  uint64_t* dfull = sfready + kSfSlots;             // [2]
+  uint64_t* dempty = dfull + 2;                     // [2]
+  uint64_t* lfull = dempty + 2;                     // LoRA operands landed
+  uint64_t* lempty = lfull + 1;                     // LoRA operand smem + D_lora free
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lempty + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,11 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = total_tiles(p);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(smem_addr(&full[i]), 1);
-      mbar_init(smem_addr(&sfready[i]), 4);
-      mbar_init(smem_addr(&empty[i]), 1);
+    for (int i = 0; i < S; ++i) mbar_init(smem_addr(&cfull[i]), 1);
+    for (int i = 0; i < kDoneRing; ++i) mbar_init(smem_addr(&mdone[i]), 1);
+    for (int i = 0; i < kSfRing; ++i) {
+      mbar_init(smem_addr(&ffull[i]), 1);
+      mbar_init(smem_addr(&fempty[i]), 4);
     }
+    for (int i = 0; i < kSfSlots; ++i) mbar_init(smem_addr(&sfready[i]), 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&dfull[i]), 1);
       mbar_init(smem_addr(&dempty[i]), 4);
@@ -149,30 +192,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------------- code producer
     if (lane == 0) {
       prefetch_tensormap(&map_xc);
-      prefetch_tensormap(&map_xs);
       prefetch_tensormap(&map_wc);
-      prefetch_tensormap(&map_ws);
-      int it = 0, li = 0, last_issued = 0, lora_issued = 0;
+      int c = 0, li = 0, issued = 0, lora_issued = 0;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
         const TileInfo ti = tile_info(p, t);
         const int wrow = ti.e * static_cast<int>(p.N) + ti.n0;
-        for (int k = 0; k < ksteps; ++k, ++it) {
-          const int s = it % S;
-          if (!mbar_wait(smem_addr(&empty[s]), ((it / S) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
+        for (int k = 0; k < ksteps; ++k) {
+          const int prev = issued - S;  // the stage that last used code slot c
+          if (prev >= 0 && !mbar_wait(smem_addr(&mdone[prev % kDoneRing]), (prev / kDoneRing) & 1, p.status,
+                                      kStatusTimeoutProducer)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * kStageBytes;
-          const uint32_t bar = smem_addr(&full[s]);
-          mbar_arrive_expect_tx(bar, kStageBytes);
+          uint8_t* st = smem + c * kCodeStageBytes;
+          const uint32_t bar = smem_addr(&cfull[c]);
+          mbar_arrive_expect_tx(bar, kCodeStageBytes);
           tma_load_2d(smem_addr(st), &map_xc, k * (kKStage / 2), static_cast<int32_t>(ti.m0), bar);
           tma_load_2d(smem_addr(st + kCodeBytes), &map_wc, k * (kKStage / 2), wrow, bar);
-          tma_load_2d(smem_addr(st + 2 * kCodeBytes), &map_xs, k * (kKStage / 16), static_cast<int32_t>(ti.m0), bar);
-          tma_load_2d(smem_addr(st + 2 * kCodeBytes + kSfBytes), &map_ws, k * (kKStage / 16), wrow, bar);
-          last_issued = it + 1;
+          ++issued;
+          if (++c == S) c = 0;
         }
         if (ok && p.r) {
           // LoRA operands of this tile (U rows m0.., B_lora rows n0..), needed after its main loop,
@@ -192,16 +233,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           lora_issued = li + 1;
         }
       }
-      for (int j = max(0, last_issued - S); j < last_issued; ++j)
-        mbar_wait(smem_addr(&full[j % S]), (j / S) & 1, p.status, kStatusTimeoutDrain);
+      // do not exit with copies in flight: wait for the last S stages to land
+      for (int j = max(0, issued - S); j < issued; ++j)
+        mbar_wait(smem_addr(&cfull[j % S]), (j / S) & 1, p.status, kStatusTimeoutDrain);
       if (lora_issued) mbar_wait(smem_addr(lfull), (lora_issued - 1) & 1, p.status, kStatusTimeoutDrain);
+    }
+  } else if (warp == kSfProducerWarp) {
+    // ---------------------------------------------------------------- scale producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_xs);
+      prefetch_tensormap(&map_ws);
+      int f = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = tile_info(p, t);
+        const int wrow = ti.e * static_cast<int>(p.N) + ti.n0;
+        for (int k = 0; k < ksteps; ++k) {
+          if (!mbar_wait(smem_addr(&fempty[f]), ph ^ 1u, p.status, kStatusTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = sfring + f * kSfStageBytes;
+          const uint32_t bar = smem_addr(&ffull[f]);
+          mbar_arrive_expect_tx(bar, kSfStageBytes);
+          tma_load_2d(smem_addr(st), &map_xs, k * (kKStage / 16), static_cast<int32_t>(ti.m0), bar);
+          tma_load_2d(smem_addr(st + kSfBytes), &map_ws, k * (kKStage / 16), wrow, bar);
+          ++issued;
+          if (++f == kSfRing) {
+            f = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      for (int j = max(0, issued - kSfRing); j < issued; ++j)
+        mbar_wait(smem_addr(&ffull[j % kSfRing]), (j / kSfRing) & 1, p.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
     if (lane == 0) {
       const uint32_t idesc = idesc_nvf4_f32(kTile, kTile);
       const uint32_t idesc_l = idesc_bf16_f32(kTile, kTile);
-      int it = 0, li = 0;
+      // code stage 0's operand descriptors; stage c adds c * kCodeStageBytes to the start address field
+      const uint64_t xdesc0 = smem_desc(smem_addr(smem), 16, 1024, 2);
+      const uint64_t wdesc0 = smem_desc(smem_addr(smem + kCodeBytes), 16, 1024, 2);
+      int c = 0, j = 0, li = 0, it = 0;
+      uint32_t cph = 0, jph = 0;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
         const int buf = li & 1;
         const uint32_t dcol = buf ? kD1 : kD0;
@@ -210,26 +286,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int k = 0; k < ksteps; ++k, ++it) {
-          const int s = it % S;
-          // the scale warps arrive only after the stage's TMA bytes have landed (they wait on full[s])
-          if (!mbar_wait(smem_addr(&sfready[s]), (it / S) & 1, p.status, kStatusTimeoutMma)) {
+        for (int k = 0; k < ksteps; ++k) {
+          // scale slot j written (tcgen05.st + fence by the scale warps), code stage c landed
+          if (!mbar_wait(smem_addr(&sfready[j]), jph, p.status, kStatusTimeoutMma) ||
+              !mbar_wait(smem_addr(&cfull[c]), cph, p.status, kStatusTimeoutMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // each pipeline stage owns 32 scale-factor columns: stage s is refilled (and its columns
-          // rewritten) only after the MMAs that read them have completed (empty[s])
-          const uint32_t sfcol = kSF + s * 32;
-          const uint32_t xa = smem_addr(smem + s * kStageBytes), wa = xa + kCodeBytes;
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const uint64_t ad = smem_desc(xa + tt * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(wa + tt * 32, 16, 1024, 2);
-            mma_nvf4_ss(tmem + dcol, ad, bd, idesc, tmem + sfcol + tt * 4, tmem + sfcol + 16 + tt * 4,
-                        (k | tt) ? 1u : 0u);
+          const uint32_t sfcol = kSF + j * 32;
+          const uint64_t soff = static_cast<uint64_t>(c * (kCodeStageBytes >> 4));
+          mma_stage_nvf4(tmem + dcol, xdesc0 + soff, wdesc0 + soff, idesc, tmem + sfcol, tmem + sfcol + 16,
+                         k ? 1u : 0u);
+          mma_commit(smem_addr(&mdone[it % kDoneRing]));
+          ++it;
+          if (++c == S) {
+            c = 0;
+            cph ^= 1u;
           }
-          mma_commit(smem_addr(&empty[s]));
+          if (++j == kSfSlots) {
+            j = 0;
+            jph ^= 1u;
+          }
         }
         if (!ok) break;
         if (p.r) {
@@ -256,26 +334,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     // step t. Lane i gathers rows i, 32 + i, 64 + i, 96 + i and writes, per operand, 16 columns:
     // column 4t + w = row 32w + i, K step t (the layout the MMA reads for M = 128).
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int it = 0;
+    int f = 0, j = 0, it = 0;
+    uint32_t fph = 0;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       for (int k = 0; k < ksteps; ++k, ++it) {
-        const int s = it % S;
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (it / S) & 1, p.status, kStatusTimeoutMma));
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&ffull[f]), fph, p.status, kStatusTimeoutMma));
         if (!ok) break;
-        const uint8_t* st = smem + s * kStageBytes + 2 * kCodeBytes;
-        const uint32_t sfcol = kSF + s * 32;
+        const uint8_t* st = sfring + f * kSfStageBytes;
+        uint32_t v[2][16];
 #pragma unroll
         for (int op = 0; op < 2; ++op) {
           const uint4* sf = reinterpret_cast<const uint4*>(st + op * kSfBytes);
           const uint4 r0 = sf[lane], r1 = sf[32 + lane], r2 = sf[64 + lane], r3 = sf[96 + lane];
-          const uint32_t v[16] = {r0.x, r1.x, r2.x, r3.x, r0.y, r1.y, r2.y, r3.y,
+          const uint32_t w[16] = {r0.x, r1.x, r2.x, r3.x, r0.y, r1.y, r2.y, r3.y,
                                   r0.z, r1.z, r2.z, r3.z, r0.w, r1.w, r2.w, r3.w};
-          tmem_st16(tmem + lane_base + sfcol + op * 16, v);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[op][q] = w[q];
         }
+        // TMEM slot j is free once the MMAs of the stage that last used it have completed
+        const int prev = it - kSfSlots;
+        if (prev >= 0) {
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&mdone[prev % kDoneRing]), (prev / kDoneRing) & 1,
+                                                 p.status, kStatusTimeoutMma));
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t sfcol = kSF + j * 32;
+        tmem_st16(tmem + lane_base + sfcol, v[0]);
+        tmem_st16(tmem + lane_base + sfcol + 16, v[1]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sfready[s]));
+        if (lane == 0) {
+          mbar_arrive(smem_addr(&sfready[j]));
+          mbar_arrive(smem_addr(&fempty[f]));  // the shared-memory scale tiles may be refilled
+        }
+        if (++f == kSfRing) {
+          f = 0;
+          fph ^= 1u;
+        }
+        if (++j == kSfSlots) j = 0;
       }
     }
   } else {
@@ -359,10 +457,9 @@ struct W4a4Plan {
 W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups) {
   W4a4Plan t{};
   const size_t lora = r ? 2 * static_cast<size_t>(kTile) * 2 * r : 0;
-  const size_t fixed = 1024 + lora + 512;
-  // at most 4 stages: TMEM holds 2 x 128 accumulator + 128 LoRA + 4 x 32 scale-factor columns
-  t.stages = static_cast<int>(std::min<size_t>(4, (227 * 1024 - fixed) / kStageBytes));
-  t.smem = fixed + t.stages * kStageBytes;
+  const size_t fixed = 1024 + lora + kSfRing * kSfStageBytes + 512;
+  t.stages = static_cast<int>(std::min<size_t>(kMaxCodeStages, (227 * 1024 - fixed) / kCodeStageBytes));
+  t.smem = fixed + t.stages * kCodeStageBytes;
   size_t o = 0;
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
   t.ws_codes = take(static_cast<size_t>(M) * K / 2);
