@@ -7,8 +7,8 @@ linear; AQN sigma schedule 1e-2 -> 5e-4 over K = 10. One step runs every stage o
 the path on that layer:
   1. AQN sigma_k (host) and RMSNorm-AQN of the 64 tokens (input norm), then again
      (post-attention norm);
-  2. the rollout weight refresh: per weight, the tensor amax and the NVFP4
-     encoding (codes, E4M3 block scales, fp32 g);
+  2. the rollout weight refresh: the tensor amax and the NVFP4 encoding (codes,
+     E4M3 block scales, fp32 g) of all five weights, in one nvfp4_quantize_batch call;
   3. the five W4A16 LoRA linears at M = 64.
 Inputs are synthetic, generated on the device from a seed, and larger than L2:
 every step streams the five bf16 weights (458 MB) and their NVFP4 codes (122 MB).
@@ -231,13 +231,15 @@ def run_gpu(args):
     h2 = torch.empty_like(h1)
     ws_bytes = max(nv.workspace_bytes(nv.OP_LINEAR_W4A16, M_TOK, n, k, RANK) for _, n, k in LINEARS)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    wsq = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, len(LINEARS), 0, 0), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    refresh_args = ([W[n] for n, _, _ in LINEARS], [Q[n][0] for n, _, _ in LINEARS], [Q[n][1] for n, _, _ in LINEARS],
+                    [Q[n][2] for n, _, _ in LINEARS])
     inputs = {"q": h1, "o": attn, "gate": h2, "up": h2, "down": act}
     stream = torch.cuda.current_stream(dev)
 
     # per-op CUDA events (all launches go to the current stream)
-    ops = ["rmsnorm_aqn", "rmsnorm_aqn_2"] + [f"amax_{n}" for n, _, _ in LINEARS] + \
-          [f"quantize_{n}" for n, _, _ in LINEARS] + [f"linear_{n}" for n, _, _ in LINEARS]
+    ops = ["rmsnorm_aqn", "rmsnorm_aqn_2", "weight_refresh"] + [f"linear_{n}" for n, _, _ in LINEARS]
 
     def step(k, ev=None, only=None):
         st = torch.cuda.current_stream(dev)
@@ -254,10 +256,8 @@ def run_gpu(args):
             b.record(st)
         sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
         mark("rmsnorm_aqn", lambda: nv.rmsnorm_aqn(x_in, w1, eps[k], sigma, 1e-6, out=h1))
-        for name, n, kk in LINEARS:
-            c, s, g, a = Q[name]
-            mark(f"amax_{name}", lambda: nv.nvfp4_amax(W[name], out=a))
-            mark(f"quantize_{name}", lambda: nv.nvfp4_quantize(W[name], amax_in=a, codes=c, scales=s, g=g))
+        mark("weight_refresh", lambda: nv.nvfp4_quantize_batch(refresh_args[0], codes=refresh_args[1],
+                                                               scales=refresh_args[2], g=refresh_args[3], workspace=wsq))
         mark("rmsnorm_aqn_2", lambda: nv.rmsnorm_aqn(x_res, w2, eps[k], sigma, 1e-6, out=h2))
         for name, n, kk in LINEARS:
             c, s, g, _ = Q[name]
@@ -342,31 +342,26 @@ def run_gpu(args):
 
     # parts
     q_bytes = sum(bytes_quantize(n * k) for _, n, k in LINEARS)
-    q_ms = sum(op_ms[f"quantize_{n}"] for n, _, _ in LINEARS)
-    a_ms = sum(op_ms[f"amax_{n}"] for n, _, _ in LINEARS)
+    q_ms = op_ms["weight_refresh"]
     l_bytes = sum(bytes_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
     l_flops = sum(flops_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
     l_ms = sum(op_ms[f"linear_{n}"] for n, _, _ in LINEARS)
     r_ms = op_ms["rmsnorm_aqn"] + op_ms["rmsnorm_aqn_2"]
     parts = {
         "rmsnorm_aqn": {"us": r_ms * 1e3, "GB/s": 2 * bytes_rmsnorm(M_TOK, HIDDEN) / r_ms / 1e6},
-        "amax": {"us": a_ms * 1e3, "GB/s": sum(2 * n * k for _, n, k in LINEARS) / a_ms / 1e6},
-        "quantize_encode": {"us": q_ms * 1e3, "GB/s": q_bytes / q_ms / 1e6},
-        "quantize_op": {"us": (q_ms + a_ms) * 1e3, "GB/s": q_bytes / (q_ms + a_ms) / 1e6},
+        "weight_refresh": {"us": q_ms * 1e3, "GB/s": q_bytes / q_ms / 1e6,
+                           "note": "amax + NVFP4 encode of the five weights, one nvfp4_quantize_batch call; bytes: each "
+                                   "weight read once, codes and scales written (the amax pass reads each weight again)"},
         "lora_linear_w4a16": {"us": l_ms * 1e3, "GB/s": l_bytes / l_ms / 1e6, "TFLOP/s": l_flops / l_ms / 1e9,
                               "frac_hbm": l_bytes / l_ms / 1e6 / hbm},
         "per_linear_us": {n: op_ms[f"linear_{n}"] * 1e3 for n, _, _ in LINEARS},
     }
     # dominant kernel by device time
-    groups = {"quantize_kernel": q_ms, "amax_kernel": a_ms, "lora_linear_w4a16": l_ms,
-              "rmsnorm_aqn_kernel": op_ms["rmsnorm_aqn"]}
+    groups = {"weight_refresh": q_ms, "lora_linear_w4a16": l_ms, "rmsnorm_aqn_kernel": op_ms["rmsnorm_aqn"]}
     dom = max(groups, key=groups.get)
-    if dom == "quantize_kernel":
-        ach, launches_per = q_bytes / q_ms / 1e6, len(LINEARS)
-        per_launch_bytes = q_bytes / len(LINEARS)
-    elif dom == "amax_kernel":
-        ach = parts["amax"]["GB/s"]
-        per_launch_bytes = sum(2 * n * k for _, n, k in LINEARS) / len(LINEARS)
+    if dom == "weight_refresh":
+        ach = q_bytes / q_ms / 1e6
+        per_launch_bytes = q_bytes
     elif dom == "lora_linear_w4a16":
         ach = l_bytes / l_ms / 1e6
         per_launch_bytes = l_bytes / len(LINEARS)
@@ -395,11 +390,10 @@ def run_gpu(args):
 
 
 def select_ops(spec, ops):
-    """--op names: op names of the step (e.g. linear_gate, amax_q, rmsnorm_aqn) or the groups
-    linears, amax, quantize, rmsnorm, all; comma-separated."""
-    groups = {"linears": [o for o in ops if o.startswith("linear_")], "amax": [o for o in ops if o.startswith("amax_")],
-              "quantize": [o for o in ops if o.startswith("quantize_")], "rmsnorm": [o for o in ops if "rmsnorm" in o],
-              "all": list(ops)}
+    """--op names: op names of the step (e.g. linear_gate, weight_refresh, rmsnorm_aqn) or the groups
+    linears, refresh, rmsnorm, all; comma-separated."""
+    groups = {"linears": [o for o in ops if o.startswith("linear_")], "refresh": ["weight_refresh"],
+              "rmsnorm": [o for o in ops if "rmsnorm" in o], "all": list(ops)}
     out = []
     for part in spec.split(","):
         part = part.strip()
@@ -618,6 +612,7 @@ def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, 
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     stream = torch.cuda.current_stream(dev)
     inputs_e2e = {"q": h1, "o": dev_x["attn"], "gate": h2, "up": h2, "down": dev_x["act"]}
+    wsq_e2e = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, len(LINEARS), 0, 0), dtype=torch.uint8, device=dev)
 
     def step(k):
         for name, _, _ in LINEARS:
@@ -626,10 +621,9 @@ def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, 
             dev_x[key].copy_(host_x[key], non_blocking=True)
         sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
         nv.rmsnorm_aqn(dev_x["x_in"], w1, eps[k], sigma, 1e-6, out=h1)
-        for name, _, _ in LINEARS:
-            c, s, g, a = Q[name]
-            nv.nvfp4_amax(W[name], out=a)
-            nv.nvfp4_quantize(W[name], amax_in=a, codes=c, scales=s, g=g)
+        nv.nvfp4_quantize_batch([W[n] for n, _, _ in LINEARS], codes=[Q[n][0] for n, _, _ in LINEARS],
+                                scales=[Q[n][1] for n, _, _ in LINEARS], g=[Q[n][2] for n, _, _ in LINEARS],
+                                workspace=wsq_e2e)
         nv.rmsnorm_aqn(dev_x["x_res"], w2, eps[k], sigma, 1e-6, out=h2)
         for name, _, _ in LINEARS:
             c, s, g, _ = Q[name]

@@ -61,7 +61,12 @@ typedef enum nvfp4rl_status {
 enum { NVFP4RL_BF16 = 0, NVFP4RL_F32 = 1 };
 
 /* Operations for nvfp4rl_workspace_bytes(). */
-enum { NVFP4RL_OP_QUANTIZE = 0, NVFP4RL_OP_LINEAR_W4A16 = 1, NVFP4RL_OP_LINEAR_W4A4 = 2 };
+enum {
+  NVFP4RL_OP_QUANTIZE = 0,
+  NVFP4RL_OP_LINEAR_W4A16 = 1,
+  NVFP4RL_OP_LINEAR_W4A4 = 2,
+  NVFP4RL_OP_QUANTIZE_BATCH = 3 /* M = number of tensors */
+};
 
 /*
  * nvfp4_amax -- per-tensor absolute maximum, the input of the NVFP4 per-tensor
@@ -99,6 +104,32 @@ NVFP4RL_API nvfp4rl_status nvfp4_amax(const void* x, int32_t dtype, int64_t n, f
 NVFP4RL_API nvfp4rl_status nvfp4_quantize(const void* x, int32_t dtype, int64_t rows, int64_t cols,
                               uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * nvfp4_quantize_batch -- nvfp4_quantize of `count` independent tensors in one call: the
+ *   re-quantization of a model's linear weights after a training step, before the next
+ *   rollout (QeRL explainer, "NVFP4量子化とLoRA": the rollout reads the base weights in
+ *   NVFP4). Each tensor has its own amax and g; tensor i's codes, scales and g are exactly
+ *   what nvfp4_quantize(x[i], ..., amax_in = NULL) writes for it.
+ * Arguments:
+ *   count    number of tensors, in [0, 4096].
+ *   x, rows, cols, codes, scales, g
+ *            HOST arrays of `count` entries (owned by the caller, read during the call only);
+ *            entry i describes tensor i with nvfp4_quantize's layout, alignment and shape
+ *            rules; the pointers in them are device pointers. rows[i] == 0: tensor i is
+ *            skipped (g[i] is left as is).
+ *   dtype    NVFP4RL_BF16 or NVFP4RL_F32, for every tensor.
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_QUANTIZE_BATCH, count, 0, 0, 0, 0) bytes,
+ *            device, 16-byte aligned; scratch.
+ * No output may overlap an input, another output or the workspace (NVFP4RL_ERR_ALIAS).
+ * For bf16 one kernel encodes a tensor while it reduces the amax of the next one (the
+ * encoding is bound by arithmetic, the amax pass by memory), largest tensors first; the
+ * order changes no result.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_quantize_batch(int32_t count, const void* const* x, const int64_t* rows,
+                                                const int64_t* cols, int32_t dtype, uint8_t* const* codes,
+                                                uint8_t* const* scales, float* const* g, void* workspace,
+                                                size_t workspace_bytes, void* stream);
 
 /*
  * nvfp4_quantize_guided -- NVFP4 quantization whose rounding direction comes

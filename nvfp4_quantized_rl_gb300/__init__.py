@@ -7,8 +7,8 @@ tensors) and the current CUDA stream. The library must have been built
 importing the binding does not build it, and every call fails loudly when the
 library or a GPU is missing -- there is no CPU fallback.
 
-Functions carry the C names: nvfp4_amax, nvfp4_quantize, nvfp4_quantize_guided, aqn_sigma,
-rmsnorm_aqn, nvfp4_lora_linear, nvfp4_lora_linear_w4a4.
+Functions carry the C names: nvfp4_amax, nvfp4_quantize, nvfp4_quantize_guided,
+nvfp4_quantize_batch, aqn_sigma, rmsnorm_aqn, nvfp4_lora_linear, nvfp4_lora_linear_w4a4.
 """
 from __future__ import annotations
 
@@ -22,7 +22,7 @@ LIB_PATH = _build.LIB
 
 OK = 0
 BF16, F32 = 0, 1
-OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4 = 0, 1, 2
+OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH = 0, 1, 2, 3
 
 _lock = threading.Lock()
 _lib = None
@@ -38,6 +38,7 @@ def _signatures():
         "nvfp4_amax": (c.c_int, [p, i32, i64, p, p]),
         "nvfp4_quantize": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, sz, p]),
         "nvfp4_quantize_guided": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
+        "nvfp4_quantize_batch": (c.c_int, [i32, p, p, p, i32, p, p, p, p, sz, p]),
         "aqn_sigma": (f64, [f64, f64, i64, i64]),
         "rmsnorm_aqn": (c.c_int, [p, i64, i64, p, p, f32, f32, p, p]),
         "nvfp4_lora_linear": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
@@ -157,6 +158,37 @@ def nvfp4_quantize(x, amax_in=None, codes=None, scales=None, g=None, workspace=N
 def nvfp4_quantize_guided(x, mask, amax_in=None, codes=None, scales=None, g=None, workspace=None, stream=None):
     """Guided NVFP4 quantization: mask (int32/uint32 words, bit i%32 of word i//32) picks the rounding direction."""
     return _quantize(x, mask, amax_in, codes, scales, g, workspace, stream)
+
+
+def nvfp4_quantize_batch(xs, codes=None, scales=None, g=None, workspace=None, stream=None):
+    """NVFP4 quantization of a list of contiguous 2-D CUDA tensors of one dtype (bf16 or fp32) in one
+    call, each with its own g -> (codes list, scales list, g list); outputs may be given as lists."""
+    import torch
+    xs = list(xs)
+    n = len(xs)
+    if n == 0:
+        return [], [], []
+    _require_cuda(*xs)
+    dt = {torch.bfloat16: BF16, torch.float32: F32}.get(xs[0].dtype)
+    if dt is None or any(t.dtype != xs[0].dtype for t in xs):
+        raise TypeError("all tensors must be bf16, or all fp32")
+    for t in xs:
+        if t.dim() != 2 or not t.is_contiguous():
+            raise ValueError("every tensor must be contiguous and 2-D")
+    dev = xs[0].device
+    codes = [_empty((t.shape[0], t.shape[1] // 2), torch.uint8, dev) for t in xs] if codes is None else list(codes)
+    scales = [_empty((t.shape[0], t.shape[1] // 16), torch.uint8, dev) for t in xs] if scales is None else list(scales)
+    g = [_empty((1,), torch.float32, dev) for _ in xs] if g is None else list(g)
+    if workspace is None:
+        workspace = _empty((workspace_bytes(OP_QUANTIZE_BATCH, n, 0, 0),), torch.uint8, dev)
+    P = ctypes.c_void_p * n
+    I64 = ctypes.c_int64 * n
+    st = lib().nvfp4_quantize_batch(n, P(*[t.data_ptr() for t in xs]), I64(*[t.shape[0] for t in xs]),
+                                    I64(*[t.shape[1] for t in xs]), dt, P(*[t.data_ptr() for t in codes]),
+                                    P(*[t.data_ptr() for t in scales]), P(*[t.data_ptr() for t in g]), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(xs[0], stream))
+    _check(st, "nvfp4_quantize_batch")
+    return codes, scales, g
 
 
 def _quantize(x, mask, amax_in, codes, scales, g, workspace, stream):

@@ -1,8 +1,10 @@
 // C ABI of the NVFP4 rollout-linear library: argument validation and dispatch.
 // Every check runs on the host before any launch; see include/nvfp4rl.h for the contract.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -87,6 +89,20 @@ nvfp4rl_status quantize_common(const void* x, int32_t dtype, int64_t rows, int64
                          static_cast<uint32_t*>(ws), dev, static_cast<cudaStream_t>(stream));
 }
 
+// True when any two of the [begin, end) ranges overlap (n log n).
+bool any_overlap(std::vector<std::pair<uintptr_t, uintptr_t>>& r) {
+  std::sort(r.begin(), r.end());
+  for (size_t i = 1; i < r.size(); ++i)
+    if (r[i].first < r[i - 1].second) return true;
+  return false;
+}
+
+// True when [a, b) overlaps one of the sorted, disjoint ranges r.
+bool hits(const std::vector<std::pair<uintptr_t, uintptr_t>>& r, uintptr_t a, uintptr_t b) {
+  auto it = std::lower_bound(r.begin(), r.end(), std::make_pair(b, uintptr_t(0)));
+  return it != r.begin() && std::prev(it)->second > a;
+}
+
 nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
                              const uint8_t* w_scales, const float* w_g, int64_t N, const uint16_t* A,
                              const uint16_t* B, int32_t r, float s, const int32_t* offsets, int32_t groups,
@@ -157,6 +173,48 @@ nvfp4rl_status nvfp4_quantize_guided(const void* x, int32_t dtype, int64_t rows,
                          stream);
 }
 
+nvfp4rl_status nvfp4_quantize_batch(int32_t count, const void* const* x, const int64_t* rows, const int64_t* cols,
+                                    int32_t dtype, uint8_t* const* codes, uint8_t* const* scales, float* const* g,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (count < 0 || count > kQuantizeBatchMax) return NVFP4RL_ERR_INVALID_ARG;
+  if (dtype != NVFP4RL_BF16 && dtype != NVFP4RL_F32) return NVFP4RL_ERR_INVALID_ARG;
+  if (count == 0) return NVFP4RL_OK;
+  if (!x || !rows || !cols || !codes || !scales || !g) return NVFP4RL_ERR_INVALID_ARG;
+  const size_t esz = dtype == NVFP4RL_BF16 ? 2 : 4;
+  std::vector<std::pair<uintptr_t, uintptr_t>> outs, ins;
+  int live = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    if (rows[i] < 0 || cols[i] <= 0) return NVFP4RL_ERR_INVALID_ARG;
+    if (cols[i] % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+    if (rows[i] == 0) continue;
+    if (!x[i] || !codes[i] || !scales[i] || !g[i]) return NVFP4RL_ERR_INVALID_ARG;
+    if (!aligned16(x[i]) || !aligned16(codes[i]) || !aligned16(scales[i]) || (reinterpret_cast<uintptr_t>(g[i]) & 3u))
+      return NVFP4RL_ERR_MISALIGNED;
+    const size_t n = static_cast<size_t>(rows[i]) * static_cast<size_t>(cols[i]);
+    const auto rng = [](const void* p, size_t b) {
+      return std::make_pair(reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + b);
+    };
+    ins.push_back(rng(x[i], n * esz));
+    outs.push_back(rng(codes[i], n / 2));
+    outs.push_back(rng(scales[i], n / 16));
+    outs.push_back(rng(g[i], 4));
+    ++live;
+  }
+  if (live == 0) return NVFP4RL_OK;
+  const size_t need = quantize_batch_workspace_bytes(count);
+  if (!workspace || workspace_bytes < need) return NVFP4RL_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NVFP4RL_ERR_MISALIGNED;
+  if (any_overlap(outs)) return NVFP4RL_ERR_ALIAS;
+  ins.push_back(std::make_pair(reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need));
+  for (const auto& r : ins)
+    if (hits(outs, r.first, r.second)) return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_quantize_batch(count, x, rows, cols, dtype, codes, scales, g, static_cast<uint32_t*>(workspace), dev,
+                               static_cast<cudaStream_t>(stream));
+}
+
 double aqn_sigma(double sigma0, double sigmaK, int64_t k, int64_t K) {
   if (K <= 0 || !(sigma0 > 0.0) || !(sigmaK > 0.0)) return NAN;
   return sigma0 * std::pow(sigmaK / sigma0, static_cast<double>(k) / static_cast<double>(K));
@@ -201,6 +259,7 @@ size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int3
   if (M < 0 || N < 0 || K < 0 || r < 0 || r > 256 || num_groups < 0 || num_groups > 1024) return 0;
   switch (op) {
     case NVFP4RL_OP_QUANTIZE: return kQuantizeWorkspace;
+    case NVFP4RL_OP_QUANTIZE_BATCH: return M <= kQuantizeBatchMax ? quantize_batch_workspace_bytes(M) : 0;
     case NVFP4RL_OP_LINEAR_W4A16: return linear_workspace_bytes(false, M, N, K, r, 1);
     case NVFP4RL_OP_LINEAR_W4A4: return linear_workspace_bytes(true, M, N, K, r, num_groups > 0 ? num_groups : 1);
     default: return 0;

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <utility>
 #include <stdint.h>
 
@@ -118,9 +119,19 @@ constexpr size_t kQuantizeWorkspace = 256;
 nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
                            cudaStream_t st);
 
+// Batched quantization: at most this many tensors per call; one amax word (16 bytes) each.
+constexpr int64_t kQuantizeBatchMax = 4096;
+inline size_t quantize_batch_workspace_bytes(int64_t count) {
+  return static_cast<size_t>(((std::max<int64_t>(count, 1) * 16 + 255) / 256) * 256);
+}
+nvfp4rl_status launch_quantize_batch(int count, const void* const* x, const int64_t* rows, const int64_t* cols,
+                                     int dtype, uint8_t* const* codes, uint8_t* const* scales, float* const* g,
+                                     uint32_t* amax_words, const DeviceInfo& dev, cudaStream_t st);
+
+// amax_done: *amax_scratch already holds the tensor's amax bits (no amax pass is launched).
 nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
-                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st);
+                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done = false);
 
 nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
                                   float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st);

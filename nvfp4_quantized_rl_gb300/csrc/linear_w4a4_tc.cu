@@ -14,8 +14,10 @@
 // scale factors to TMEM, MMA issue, MMA completion back to the producer) takes well over
 // 1 us, so the operand codes have a deep ring of their own and the small scale tiles a
 // separate one that runs ahead:
-//   warp 0      code producer (TMA): per stage the activation and weight code tiles (128 x 128
-//               bytes each, 128-byte swizzle) into the code ring.
+//   warps 0, 11 code producers (TMA): per stage the activation (warp 0) and the weight (warp 11)
+//               code tile, 128 x 128 bytes each with 128-byte swizzle, into the code ring; warp 0
+//               also loads the LoRA tiles. One issuing thread completes only about three
+//               copies per microsecond (wait, expect_tx, copy), so each stream has its own.
 //   warp 1      allocates TMEM; one thread issues four tcgen05.mma
 //               kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each) per stage; at the end of
 //               a tile the LoRA up-projection (U tile x B_lora tile^T, kind::f16) goes to a
@@ -28,8 +30,9 @@
 //               into one of four TMEM slots that the MMAs release. This keeps the scale traffic
 //               off the tensor pipe, where a shared-memory -> TMEM copy per K step and operand
 //               would cost about as much as the MMAs.
-//   warp 10     scale producer (TMA): both 128 x 16-byte scale tiles per stage into the scale
-//               ring, which the scale warps release as soon as they have read it.
+//   warps 10,12 scale producers (TMA): the activation (warp 10) and weight (warp 12) 128 x 16-byte
+//               scale tiles per stage into the scale ring, which the scale warps release once the
+//               scales are in TMEM.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -54,9 +57,10 @@ constexpr int kSfRing = 4;                       // scale ring stages
 constexpr int kSfSlots = 4;                      // TMEM scale-factor slots (32 columns each)
 constexpr int kMaxCodeStages = 6;
 constexpr int kDoneRing = 8;                     // "stage's MMAs done" barriers, > kMaxCodeStages, kSfSlots
-constexpr int kThreads = 352;
+constexpr int kThreads = 416;
 constexpr int kFirstSfWarp = 6;
-constexpr int kSfProducerWarp = 10;
+constexpr int kSfProducerWarp = 10;   // activation scales; weight scales: warp 12
+constexpr int kWCodeWarp = 11;
 constexpr uint32_t kD0 = 0, kD1 = 128, kDL = 256, kSF = 384;  // TMEM columns
 
 struct W4a4Params {
@@ -169,10 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = total_tiles(p);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) mbar_init(smem_addr(&cfull[i]), 1);
+    for (int i = 0; i < S; ++i) mbar_init(smem_addr(&cfull[i]), 2);  // activation + weight producer
     for (int i = 0; i < kDoneRing; ++i) mbar_init(smem_addr(&mdone[i]), 1);
     for (int i = 0; i < kSfRing; ++i) {
-      mbar_init(smem_addr(&ffull[i]), 1);
+      mbar_init(smem_addr(&ffull[i]), 2);
       mbar_init(smem_addr(&fempty[i]), 4);
     }
     for (int i = 0; i < kSfSlots; ++i) mbar_init(smem_addr(&sfready[i]), 4);
@@ -191,11 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- code producer
+  if (warp == 0 || warp == kWCodeWarp) {
+    // ---------------------------------------------------------------- code producers
     if (lane == 0) {
-      prefetch_tensormap(&map_xc);
-      prefetch_tensormap(&map_wc);
+      const bool wside = warp == kWCodeWarp;
+      const CUtensorMap* map = wside ? &map_wc : &map_xc;
+      prefetch_tensormap(map);
       int c = 0, li = 0, issued = 0, lora_issued = 0;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
         const TileInfo ti = tile_info(p, t);
@@ -207,15 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* st = smem + c * kCodeStageBytes;
           const uint32_t bar = smem_addr(&cfull[c]);
-          mbar_arrive_expect_tx(bar, kCodeStageBytes);
-          tma_load_2d(smem_addr(st), &map_xc, k * (kKStage / 2), static_cast<int32_t>(ti.m0), bar);
-          tma_load_2d(smem_addr(st + kCodeBytes), &map_wc, k * (kKStage / 2), wrow, bar);
+          mbar_arrive_expect_tx(bar, kCodeBytes);
+          tma_load_2d(smem_addr(smem + c * kCodeStageBytes + (wside ? kCodeBytes : 0)), map, k * (kKStage / 2),
+                      wside ? wrow : static_cast<int32_t>(ti.m0), bar);
           ++issued;
           if (++c == S) c = 0;
         }
-        if (ok && p.r) {
+        if (ok && p.r && !wside) {
           // LoRA operands of this tile (U rows m0.., B_lora rows n0..), needed after its main loop,
           // once the epilogue of the previous tile has read the LoRA accumulator
           if (!mbar_wait(smem_addr(lempty), (li & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
@@ -238,11 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_addr(&cfull[j % S]), (j / S) & 1, p.status, kStatusTimeoutDrain);
       if (lora_issued) mbar_wait(smem_addr(lfull), (lora_issued - 1) & 1, p.status, kStatusTimeoutDrain);
     }
-  } else if (warp == kSfProducerWarp) {
-    // ---------------------------------------------------------------- scale producer
+  } else if (warp == kSfProducerWarp || warp == kSfProducerWarp + 2) {
+    // ---------------------------------------------------------------- scale producers
     if (lane == 0) {
-      prefetch_tensormap(&map_xs);
-      prefetch_tensormap(&map_ws);
+      const bool wside = warp != kSfProducerWarp;
+      const CUtensorMap* map = wside ? &map_ws : &map_xs;
+      prefetch_tensormap(map);
       int f = 0, issued = 0;
       uint32_t ph = 0;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -253,11 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* st = sfring + f * kSfStageBytes;
           const uint32_t bar = smem_addr(&ffull[f]);
-          mbar_arrive_expect_tx(bar, kSfStageBytes);
-          tma_load_2d(smem_addr(st), &map_xs, k * (kKStage / 16), static_cast<int32_t>(ti.m0), bar);
-          tma_load_2d(smem_addr(st + kSfBytes), &map_ws, k * (kKStage / 16), wrow, bar);
+          mbar_arrive_expect_tx(bar, kSfBytes);
+          tma_load_2d(smem_addr(sfring + f * kSfStageBytes + (wside ? kSfBytes : 0)), map, k * (kKStage / 16),
+                      wside ? wrow : static_cast<int32_t>(ti.m0), bar);
           ++issued;
           if (++f == kSfRing) {
             f = 0;
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= kFirstSfWarp) {
+  } else if (warp >= kFirstSfWarp && warp < kFirstSfWarp + 4) {
     // ---------------------------------------------------------------- scale factors -> TMEM
     // Scale tile in shared memory: [128 rows][16 bytes], word t = the four block scales of K
     // step t. Lane i gathers rows i, 32 + i, 64 + i, 96 + i and writes, per operand, 16 columns:
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++j == kSfSlots) j = 0;
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 6) {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;

@@ -21,6 +21,10 @@
 // with T * dec(s) exact in fp32 (at most 7 significant bits), so RD/RU are single
 // directed-rounding multiplies (__fmul_rd / __fmul_ru). Non-negative fp32 values
 // order like their bit patterns, so the compares run on integers.
+#include <map>
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -475,6 +479,71 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   }
 }
 
+// Encoding of one bf16 tensor (plain rounding) fused with the amax pass over the next tensor
+// of a batch. The encoding is bound by arithmetic and the amax pass by memory, so each thread
+// interleaves the two: per iteration two blocks of this tensor (loaded, then encoded) and Q
+// 128-bit words of the next one (loaded with them, reduced after), Q chosen by the host so
+// that both streams end together; words left over are reduced after the encoding loop. The
+// encoding is quantize_kernel's (same blocks, same tables, same order).
+template <int Q>
+__global__ void __launch_bounds__(256) encode_amax_next_kernel(const void* __restrict__ x, int64_t nblocks,
+                                                               const uint32_t* __restrict__ amax_bits,
+                                                               uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ scales, float* __restrict__ g_out,
+                                                               const uint4* __restrict__ xn, int64_t nvec_n,
+                                                               uint32_t* __restrict__ amax_next) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const float amax = __uint_as_float(*amax_bits);
+  const float g = __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  const bool tiny = g < 0x1p-60f;
+  const float est_scale = tiny ? 0x1p64f : 1.0f;
+  const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
+  __shared__ EncodeTables tab;
+  build_encode_tables(tab, g);
+  __syncthreads();
+
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // next word of the next tensor
+  uint32_t m2 = 0;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < nblocks; j += 2 * stride) {
+    uint4 an[Q];
+#pragma unroll
+    for (int u = 0; u < Q; ++u) an[u] = v + u * stride < nvec_n ? ld_nc_v4(xn + v + u * stride) : make_uint4(0, 0, 0, 0);
+    v += Q * stride;
+    const int64_t blk = nblocks - 1 - j;
+    const bool two = j + stride < nblocks;
+    const int64_t blk2 = blk - stride;
+    BlockWords<NVFP4RL_BF16> a, b;
+    load_block<NVFP4RL_BF16>(x, blk, a);
+    if (two) load_block<NVFP4RL_BF16>(x, blk2, b);
+    encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
+    if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
+#pragma unroll
+    for (int u = 0; u < Q; ++u) m2 = __vmaxu2(m2, max4_abs_bf16(an[u]));
+  }
+  for (; v + 3 * stride < nvec_n; v += 4 * stride) {
+    const uint4 v0 = ld_nc_v4(xn + v), v1 = ld_nc_v4(xn + v + stride);
+    const uint4 v2 = ld_nc_v4(xn + v + 2 * stride), v3 = ld_nc_v4(xn + v + 3 * stride);
+    m2 = __vmaxu2(m2, max4_abs_bf16(v0));
+    m2 = __vmaxu2(m2, max4_abs_bf16(v1));
+    m2 = __vmaxu2(m2, max4_abs_bf16(v2));
+    m2 = __vmaxu2(m2, max4_abs_bf16(v3));
+  }
+  for (; v < nvec_n; v += stride) m2 = __vmaxu2(m2, max4_abs_bf16(ld_nc_v4(xn + v)));
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (threadIdx.x == 0) atomicMax(amax_next, m);
+  }
+}
+
 // Clears the amax accumulator word (a kernel rather than a memset, so that it chains with the
 // neighbouring kernels by programmatic dependent launch).
 __global__ void zero_word_kernel(uint32_t* __restrict__ p) {
@@ -483,12 +552,21 @@ __global__ void zero_word_kernel(uint32_t* __restrict__ p) {
   if (threadIdx.x == 0) *p = 0u;
 }
 
+// Clears n amax accumulator words, 4 words (16 bytes) apart.
+__global__ void zero_words_kernel(uint32_t* __restrict__ p, int n) {
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[4 * i] = 0u;
+}
+
 }  // namespace
 
-nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
-                           cudaStream_t st) {
-  if (launch_pdl(zero_word_kernel, dim3(1), dim3(32), 0, st, amax_bits) != cudaSuccess) return NVFP4RL_ERR_CUDA;
-  if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+namespace {
+
+// amax of n elements accumulated (atomicMax of the bit pattern) into *amax_bits, which the
+// caller has zeroed.
+nvfp4rl_status launch_amax_accumulate(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
+                                      cudaStream_t st) {
   if (n == 0) return NVFP4RL_OK;
   const int64_t bytes = n * (dtype == NVFP4RL_BF16 ? 2 : 4);
   const int64_t nchunks = (bytes + kAmaxChunk - 1) / kAmaxChunk;
@@ -518,14 +596,23 @@ nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_b
   return launch_status();
 }
 
+}  // namespace
+
+nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
+                           cudaStream_t st) {
+  if (launch_pdl(zero_word_kernel, dim3(1), dim3(32), 0, st, amax_bits) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  return launch_amax_accumulate(x, dtype, n, amax_bits, dev, st);
+}
+
 nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
-                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st) {
+                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done) {
   const int64_t n = rows * cols;
   const int64_t nblocks = n / 16;
   if (nblocks == 0) return NVFP4RL_OK;
   const int threads = 256;
-  if (amax_in == nullptr) {
+  if (amax_in == nullptr && !amax_done) {
     const nvfp4rl_status sa = launch_amax(x, dtype, n, amax_scratch, dev, st);
     if (sa != NVFP4RL_OK) return sa;
   }
@@ -545,6 +632,95 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
   }
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
+}
+
+namespace {
+
+// CTAs per SM of the fused kernel at full residency (once per device and Q).
+template <int Q>
+int encode_amax_ctas_per_sm(int device) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(device);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_amax_next_kernel<Q>, 256, 0) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  cache[device] = n;
+  return n;
+}
+
+template <int Q>
+cudaError_t launch_encode_amax(const void* x, int64_t nblocks, const uint32_t* amax_bits, uint8_t* codes,
+                               uint8_t* scales, float* g, const void* xn, int64_t nvec_n, uint32_t* amax_next,
+                               int grid, cudaStream_t st) {
+  return launch_pdl(encode_amax_next_kernel<Q>, dim3(grid), dim3(256), 0, st, x, nblocks, amax_bits, codes, scales, g,
+                    static_cast<const uint4*>(xn), nvec_n, amax_next);
+}
+
+}  // namespace
+
+nvfp4rl_status launch_quantize_batch(int count, const void* const* x, const int64_t* rows, const int64_t* cols,
+                                     int dtype, uint8_t* const* codes, uint8_t* const* scales, float* const* g,
+                                     uint32_t* amax_words, const DeviceInfo& dev, cudaStream_t st) {
+  // non-empty tensors, largest first (the fused kernels then pair tensors of similar size)
+  std::vector<int> order;
+  for (int i = 0; i < count; ++i)
+    if (rows[i] > 0) order.push_back(i);
+  if (order.empty()) return NVFP4RL_OK;
+  const auto numel = [&](int i) { return rows[i] * cols[i]; };
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return numel(a) > numel(b); });
+  uint32_t* word = amax_words;  // tensor i: word[4 i]
+  if (launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>((count + 255) / 256)), dim3(256), 0, st, amax_words,
+                 count) != cudaSuccess)
+    return NVFP4RL_ERR_CUDA;
+  if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  if (dtype != NVFP4RL_BF16) {
+    for (int i : order) {
+      const nvfp4rl_status s1 = launch_amax_accumulate(x[i], dtype, numel(i), word + 4 * i, dev, st);
+      if (s1 != NVFP4RL_OK) return s1;
+      const nvfp4rl_status s2 = launch_quantize(x[i], dtype, rows[i], cols[i], nullptr, codes[i], scales[i], g[i],
+                                                nullptr, word + 4 * i, dev, st, /*amax_done=*/true);
+      if (s2 != NVFP4RL_OK) return s2;
+    }
+    return NVFP4RL_OK;
+  }
+  const int first = order[0];
+  nvfp4rl_status sa = launch_amax_accumulate(x[first], dtype, numel(first), word + 4 * first, dev, st);
+  if (sa != NVFP4RL_OK) return sa;
+  for (size_t k = 0; k + 1 < order.size(); ++k) {
+    const int i = order[k], n = order[k + 1];
+    const int64_t nblocks = numel(i) / 16, nvec_n = numel(n) * 2 / 16;
+    // words of the next tensor per encoding iteration so that both streams end together
+    const int64_t iters_bound = (nblocks + 1) / 2;  // iterations of the whole grid x threads, times stride
+    const int64_t qwant = (nvec_n + iters_bound - 1) / std::max<int64_t>(iters_bound, 1);
+    cudaError_t e;
+    if (qwant <= 1) {
+      const int grid = static_cast<int>(std::min<int64_t>(dev.sm_count * encode_amax_ctas_per_sm<1>(dev.device),
+                                                          (nblocks + 255) / 256));
+      e = launch_encode_amax<1>(x[i], nblocks, word + 4 * i, codes[i], scales[i], g[i], x[n], nvec_n, word + 4 * n,
+                                grid, st);
+    } else if (qwant <= 2) {
+      const int grid = static_cast<int>(std::min<int64_t>(dev.sm_count * encode_amax_ctas_per_sm<2>(dev.device),
+                                                          (nblocks + 255) / 256));
+      e = launch_encode_amax<2>(x[i], nblocks, word + 4 * i, codes[i], scales[i], g[i], x[n], nvec_n, word + 4 * n,
+                                grid, st);
+    } else {
+      // largest first: the next tensor is never larger, so at most 4 words per iteration
+      const int grid = static_cast<int>(std::min<int64_t>(dev.sm_count * encode_amax_ctas_per_sm<4>(dev.device),
+                                                          (nblocks + 255) / 256));
+      e = launch_encode_amax<4>(x[i], nblocks, word + 4 * i, codes[i], scales[i], g[i], x[n], nvec_n, word + 4 * n,
+                                grid, st);
+    }
+    if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
+    if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  }
+  const int last = order.back();
+  return launch_quantize(x[last], dtype, rows[last], cols[last], nullptr, codes[last], scales[last], g[last], nullptr,
+                         word + 4 * last, dev, st, /*amax_done=*/true);
 }
 
 }  // namespace nvfp4rl

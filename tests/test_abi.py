@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
-    for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "rmsnorm_aqn", "nvfp4_lora_linear",
+    for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "nvfp4_quantize_batch", "rmsnorm_aqn", "nvfp4_lora_linear",
                      "nvfp4_lora_linear_w4a4", "aqn_sigma"):
         assert required in names
 
@@ -81,6 +81,31 @@ def test_quantize_validation(nv):
     assert _q(nv, wsb=8) == 4                  # workspace too small
     g = nv.lib().nvfp4_quantize_guided(A0, 0, 4, 32, None, A1, A2, A3, None, A4, 256, None)
     assert g == 1                              # guided without a mask
+
+
+def _qb(nv, n=2, xs=(A0, A0 + 0x1000), rows=(4, 8), cols=(32, 64), dtype=0, codes=(A1, A1 + 0x1000),
+        scales=(A2, A2 + 0x1000), g=(A3, A3 + 0x100), ws=A4, wsb=256):
+    P, I = ctypes.c_void_p * len(xs), ctypes.c_int64 * len(xs)
+    return nv.lib().nvfp4_quantize_batch(n, P(*xs), I(*rows), I(*cols), dtype, P(*codes), P(*scales), P(*g), ws,
+                                         wsb, None)
+
+
+def test_quantize_batch_validation(nv):
+    assert nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, 300, 0, 0) >= 300 * 4
+    assert nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, 5000, 0, 0) == 0  # more than 4096 tensors
+    assert _qb(nv, n=-1) == 1
+    assert _qb(nv, n=0) == 0                                           # nothing to do
+    assert _qb(nv, dtype=2) == 1
+    assert _qb(nv, rows=(4, -1)) == 1
+    assert _qb(nv, cols=(32, 40)) == 3                                 # not a multiple of 16
+    assert _qb(nv, xs=(A0, A0 + 8)) == 2                               # misaligned input
+    assert _qb(nv, g=(A3, A3 + 2)) == 2                                # misaligned g
+    assert _qb(nv, ws=None) == 4
+    assert _qb(nv, wsb=16) == 4
+    assert _qb(nv, codes=(A1, A1)) == 7                                # two outputs in one place
+    assert _qb(nv, scales=(A2, A0 + 0x1000)) == 7                      # an output over an input
+    assert _qb(nv, g=(A3, A4)) == 7                                    # an output over the workspace
+    assert _qb(nv, rows=(0, 0)) == 0                                   # all tensors empty: no-op
 
 
 def _lin(nv, fn="nvfp4_lora_linear", x=A0, M=8, K=512, codes=A1, scales=A2, g=A3, N=256, A=None, B=None, r=0,

@@ -150,6 +150,40 @@ def test_quantize_qwen7b_layer_full(nv):
         assert_quant_equal(gpu_quantize(nv, W), oracle.quantize(W), f"7B {name}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_quantize_batch_mixed(nv, dtype):
+    """nvfp4_quantize_batch on tensors of mixed sizes (so the fused encode + next-amax kernel runs
+    with every share of the next tensor per iteration), an all-zero tensor, a tiny-g tensor and an
+    empty one: each tensor's bytes equal the oracle's for that tensor alone."""
+    mats = [synth.weight_f32(129, 4096, 0.02, 7, 1, outlier_frac=0.02), synth.weight_f32(300, 1040, 0.02, 7, 2),
+            synth.weight_f32(37, 48, 1.0, 7, 3), np.zeros((8, 64), np.float32),
+            (synth.weight_f32(16, 64, 1.0, 7, 4) * np.float32(1e-36)).astype(np.float32),
+            synth.weight_f32(200, 2048, 0.05, 7, 5, outlier_frac=0.01), np.zeros((0, 64), np.float32),
+            synth.weight_f32(1, 16, 3.0, 7, 6)]
+    xs = [synth.bf16_bits(m) if dtype == "bf16" else m for m in mats]
+    dev = [P.dev_bf16(x) if dtype == "bf16" else P.dev(x) for x in xs]
+    codes, scales, gs = nv.nvfp4_quantize_batch(dev)
+    torch.cuda.synchronize()
+    for i, x in enumerate(xs):
+        if x.shape[0] == 0:
+            assert codes[i].shape == (0, 32)
+            continue
+        got = (codes[i].cpu().numpy(), scales[i].cpu().numpy(), np.float32(gs[i].cpu().numpy()[0]))
+        assert_quant_equal(got, oracle.quantize(x), f"batch {dtype} tensor {i} {x.shape}")
+
+
+def test_quantize_batch_qwen7b_layer(nv):
+    """The weight refresh of the bench: all five Qwen2.5-7B-shaped weights in one batched call, every
+    output byte against the oracle."""
+    Ws = [synth.weight_bf16(n, k, 0.02, 2, i, outlier_frac=0.01)
+          for i, (name, (n, k)) in enumerate(synth.QWEN25_7B["linears"].items())]
+    codes, scales, gs = nv.nvfp4_quantize_batch([P.dev_bf16(W) for W in Ws])
+    torch.cuda.synchronize()
+    for i, W in enumerate(Ws):
+        got = (codes[i].cpu().numpy(), scales[i].cpu().numpy(), np.float32(gs[i].cpu().numpy()[0]))
+        assert_quant_equal(got, oracle.quantize(W), f"batch 7B weight {i}")
+
+
 def test_quantize_moe_experts_guided(nv):
     """MoE expert weights (768x2048 gate/up, 2048x768 down); guided with a Bernoulli(1/2) mask, as for the
     deepest layers, and plain, on a seeded set of experts."""
