@@ -235,11 +235,15 @@ def run_gpu(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     refresh_args = ([W[n] for n, _, _ in LINEARS], [Q[n][0] for n, _, _ in LINEARS], [Q[n][1] for n, _, _ in LINEARS],
                     [Q[n][2] for n, _, _ in LINEARS])
+    for name, _, _ in LINEARS:  # each weight's amax, the input of the single-op encode (quantize_<w>)
+        nv.nvfp4_amax(W[name], out=Q[name][3])
     inputs = {"q": h1, "o": attn, "gate": h2, "up": h2, "down": act}
     stream = torch.cuda.current_stream(dev)
 
     # per-op CUDA events (all launches go to the current stream)
     ops = ["rmsnorm_aqn", "rmsnorm_aqn_2", "weight_refresh"] + [f"linear_{n}" for n, _, _ in LINEARS]
+    # single-op mode only (not part of the step): the per-weight amax and encode kernels alone
+    solo_ops = [f"amax_{n}" for n, _, _ in LINEARS] + [f"quantize_{n}" for n, _, _ in LINEARS]
 
     def step(k, ev=None, only=None):
         st = torch.cuda.current_stream(dev)
@@ -258,6 +262,13 @@ def run_gpu(args):
         mark("rmsnorm_aqn", lambda: nv.rmsnorm_aqn(x_in, w1, eps[k], sigma, 1e-6, out=h1))
         mark("weight_refresh", lambda: nv.nvfp4_quantize_batch(refresh_args[0], codes=refresh_args[1],
                                                                scales=refresh_args[2], g=refresh_args[3], workspace=wsq))
+        if only is not None:
+            for name, n, kk in LINEARS:
+                c, s, g, a = Q[name]
+                if f"amax_{name}" in only:
+                    nv.nvfp4_amax(W[name], out=a)
+                if f"quantize_{name}" in only:
+                    nv.nvfp4_quantize(W[name], amax_in=a, codes=c, scales=s, g=g)
         mark("rmsnorm_aqn_2", lambda: nv.rmsnorm_aqn(x_res, w2, eps[k], sigma, 1e-6, out=h2))
         for name, n, kk in LINEARS:
             c, s, g, _ = Q[name]
@@ -271,7 +282,7 @@ def run_gpu(args):
         step(i % (KSCHED + 1))
     torch.cuda.synchronize()
     if args.op:
-        return run_ops(args, torch, step, ops, flush, stream, rank)
+        return run_ops(args, torch, step, ops + solo_ops, flush, stream, rank)
     graphs, ev_graphs = [], []
     launches_per_step = None
     for k in range(KSCHED + 1):
@@ -390,10 +401,13 @@ def run_gpu(args):
 
 
 def select_ops(spec, ops):
-    """--op names: op names of the step (e.g. linear_gate, weight_refresh, rmsnorm_aqn) or the groups
-    linears, refresh, rmsnorm, all; comma-separated."""
+    """--op names: op names of the step (e.g. linear_gate, weight_refresh, rmsnorm_aqn), the single-weight
+    amax_<w> / quantize_<w> (the per-tensor amax and encode kernels alone; not part of the step) or the
+    groups linears, refresh, rmsnorm, amax, quantize, all (= the step's ops); comma-separated."""
     groups = {"linears": [o for o in ops if o.startswith("linear_")], "refresh": ["weight_refresh"],
-              "rmsnorm": [o for o in ops if "rmsnorm" in o], "all": list(ops)}
+              "rmsnorm": [o for o in ops if "rmsnorm" in o], "amax": [o for o in ops if o.startswith("amax_")],
+              "quantize": [o for o in ops if o.startswith("quantize_")],
+              "all": [o for o in ops if not o.startswith(("amax_", "quantize_"))]}
     out = []
     for part in spec.split(","):
         part = part.strip()
