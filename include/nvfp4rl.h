@@ -123,8 +123,8 @@ NVFP4RL_API nvfp4rl_status nvfp4_quantize(const void* x, int32_t dtype, int64_t 
  *            device, 16-byte aligned; scratch.
  * No output may overlap an input, another output or the workspace (NVFP4RL_ERR_ALIAS).
  * For bf16 one kernel encodes a tensor while it reduces the amax of the next one (the
- * encoding is bound by arithmetic, the amax pass by memory), largest tensors first; the
- * order changes no result.
+ * encoding is bound by arithmetic, the amax pass by memory): the smallest tensor first, then
+ * the others largest first; the order changes no result.
  */
 NVFP4RL_API nvfp4rl_status nvfp4_quantize_batch(int32_t count, const void* const* x, const int64_t* rows,
                                                 const int64_t* cols, int32_t dtype, uint8_t* const* codes,

@@ -479,69 +479,102 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   }
 }
 
-// Encoding of one bf16 tensor (plain rounding) fused with the amax pass over the next tensor
-// of a batch. The encoding is bound by arithmetic and the amax pass by memory, so each thread
-// interleaves the two: per iteration two blocks of this tensor (loaded, then encoded) and Q
-// 128-bit words of the next one (loaded with them, reduced after), Q chosen by the host so
-// that both streams end together; words left over are reduced after the encoding loop. The
-// encoding is quantize_kernel's (same blocks, same tables, same order).
-template <int Q>
-__global__ void __launch_bounds__(256) encode_amax_next_kernel(const void* __restrict__ x, int64_t nblocks,
-                                                               const uint32_t* __restrict__ amax_bits,
-                                                               uint8_t* __restrict__ codes,
-                                                               uint8_t* __restrict__ scales, float* __restrict__ g_out,
-                                                               const uint4* __restrict__ xn, int64_t nvec_n,
-                                                               uint32_t* __restrict__ amax_next) {
+// Encoding of one bf16 tensor (plain rounding) fused with the amax pass over the next tensor of
+// a batch: the encoding is bound by arithmetic and the amax pass by memory. Two CTAs per SM:
+// warp 0 streams the next tensor through a ring of 16 KB shared-memory stages with
+// cp.async.bulk (the amax_bulk_kernel scheme), warps 1-2 reduce it from shared memory, and
+// warps 3-19 encode this tensor exactly as quantize_kernel does (same blocks, tables and
+// order). The amax stream costs the encoding warps neither registers nor load slots.
+constexpr int kFusedThreads = 640;   // two CTAs per SM
+constexpr int kFusedEncodeWarps = 17;
+constexpr int kFusedStages = 4;
+constexpr int kFusedSmem = kAmaxChunk * kFusedStages;
+
+__global__ void __launch_bounds__(kFusedThreads, 2)
+    encode_amax_ring_kernel(const void* __restrict__ x, int64_t nblocks, const uint32_t* __restrict__ amax_bits,
+                            uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ g_out,
+                            const uint8_t* __restrict__ xn, int64_t bytes_n, uint32_t* __restrict__ amax_next,
+                            uint32_t* __restrict__ status) {
   griddep_wait();
   griddep_launch_dependents();
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kFusedStages], empty[kFusedStages];
+  __shared__ uint32_t red[2];
+  __shared__ EncodeTables tab;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float amax = __uint_as_float(*amax_bits);
   const float g = __fdiv_rn(amax, 2688.0f);
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
   const bool tiny = g < 0x1p-60f;
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
-  __shared__ EncodeTables tab;
   build_encode_tables(tab, g);
-  __syncthreads();
-
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // next word of the next tensor
-  uint32_t m2 = 0;
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < nblocks; j += 2 * stride) {
-    uint4 an[Q];
-#pragma unroll
-    for (int u = 0; u < Q; ++u) an[u] = v + u * stride < nvec_n ? ld_nc_v4(xn + v + u * stride) : make_uint4(0, 0, 0, 0);
-    v += Q * stride;
-    const int64_t blk = nblocks - 1 - j;
-    const bool two = j + stride < nblocks;
-    const int64_t blk2 = blk - stride;
-    BlockWords<NVFP4RL_BF16> a, b;
-    load_block<NVFP4RL_BF16>(x, blk, a);
-    if (two) load_block<NVFP4RL_BF16>(x, blk2, b);
-    encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
-    if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
-#pragma unroll
-    for (int u = 0; u < Q; ++u) m2 = __vmaxu2(m2, max4_abs_bf16(an[u]));
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kFusedStages; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&empty[i]), 2);
+    }
+    fence_barrier_init();
   }
-  for (; v + 3 * stride < nvec_n; v += 4 * stride) {
-    const uint4 v0 = ld_nc_v4(xn + v), v1 = ld_nc_v4(xn + v + stride);
-    const uint4 v2 = ld_nc_v4(xn + v + 2 * stride), v3 = ld_nc_v4(xn + v + 3 * stride);
-    m2 = __vmaxu2(m2, max4_abs_bf16(v0));
-    m2 = __vmaxu2(m2, max4_abs_bf16(v1));
-    m2 = __vmaxu2(m2, max4_abs_bf16(v2));
-    m2 = __vmaxu2(m2, max4_abs_bf16(v3));
-  }
-  for (; v < nvec_n; v += stride) m2 = __vmaxu2(m2, max4_abs_bf16(ld_nc_v4(xn + v)));
-  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
-  m = __reduce_max_sync(0xFFFFFFFFu, m);
-  __shared__ uint32_t red[8];
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+  const int64_t nchunks = (bytes_n + kAmaxChunk - 1) / kAmaxChunk;
+  const int64_t mine = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (warp == 0) {
+    // ---------------------------------------------------------------- next tensor -> ring
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t j = 0; j < mine; ++j) {
+        const int s = static_cast<int>(j % kFusedStages);
+        if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>((j / kFusedStages) & 1) ^ 1u, status,
+                       kStatusTimeoutProducer))
+          break;
+        const int64_t off = (blockIdx.x + j * gridDim.x) * static_cast<int64_t>(kAmaxChunk);
+        const uint32_t size = static_cast<uint32_t>(min(static_cast<int64_t>(kAmaxChunk), bytes_n - off));
+        mbar_arrive_expect_tx(smem_addr(&full[s]), size);
+        bulk_load(smem_addr(ring + s * kAmaxChunk), xn + off, size, smem_addr(&full[s]));
+        issued = j + 1;
+      }
+      for (int64_t j = max(int64_t(0), issued - kFusedStages); j < issued; ++j)
+        mbar_wait(smem_addr(&full[j % kFusedStages]), static_cast<uint32_t>((j / kFusedStages) & 1), status,
+                  kStatusTimeoutDrain);
+    }
+  } else if (warp <= 2) {
+    // ---------------------------------------------------------------- amax of the next tensor
+    const int t = threadIdx.x - 32;
+    uint32_t m2 = 0;
+    for (int64_t j = 0; j < mine; ++j) {
+      const int s = static_cast<int>(j % kFusedStages);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((j / kFusedStages) & 1),
+                                             status, kStatusTimeoutDequant)))
+        break;
+      const int64_t off = (blockIdx.x + j * gridDim.x) * static_cast<int64_t>(kAmaxChunk);
+      const int nvec = static_cast<int>(min(static_cast<int64_t>(kAmaxChunk), bytes_n - off) / 16);
+      const uint4* v = reinterpret_cast<const uint4*>(ring + s * kAmaxChunk);
+#pragma unroll 8
+      for (int i = t; i < nvec; i += 64) m2 = __vmaxu2(m2, max4_abs_bf16(v[i]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
     m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if (threadIdx.x == 0) atomicMax(amax_next, m);
+    if (lane == 0) red[warp - 1] = m;
+  } else {
+    // ---------------------------------------------------------------- encode this tensor
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * (kFusedEncodeWarps * 32);
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * (kFusedEncodeWarps * 32) + (threadIdx.x - 96); j < nblocks;
+         j += 2 * stride) {
+      const int64_t blk = nblocks - 1 - j;
+      const bool two = j + stride < nblocks;
+      const int64_t blk2 = blk - stride;
+      BlockWords<NVFP4RL_BF16> a, b;
+      load_block<NVFP4RL_BF16>(x, blk, a);
+      if (two) load_block<NVFP4RL_BF16>(x, blk2, b);
+      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
+      if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
+    }
   }
+  __syncthreads();
+  if (threadIdx.x == 0) atomicMax(amax_next, max(red[0], red[1]));
 }
 
 // Clears the amax accumulator word (a kernel rather than a memset, so that it chains with the
@@ -634,45 +667,19 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
   return launch_status();
 }
 
-namespace {
-
-// CTAs per SM of the fused kernel at full residency (once per device and Q).
-template <int Q>
-int encode_amax_ctas_per_sm(int device) {
-  static std::mutex mu;
-  static std::map<int, int> cache;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(device);
-  if (it != cache.end()) return it->second;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_amax_next_kernel<Q>, 256, 0) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    n = 1;
-  }
-  cache[device] = n;
-  return n;
-}
-
-template <int Q>
-cudaError_t launch_encode_amax(const void* x, int64_t nblocks, const uint32_t* amax_bits, uint8_t* codes,
-                               uint8_t* scales, float* g, const void* xn, int64_t nvec_n, uint32_t* amax_next,
-                               int grid, cudaStream_t st) {
-  return launch_pdl(encode_amax_next_kernel<Q>, dim3(grid), dim3(256), 0, st, x, nblocks, amax_bits, codes, scales, g,
-                    static_cast<const uint4*>(xn), nvec_n, amax_next);
-}
-
-}  // namespace
-
 nvfp4rl_status launch_quantize_batch(int count, const void* const* x, const int64_t* rows, const int64_t* cols,
                                      int dtype, uint8_t* const* codes, uint8_t* const* scales, float* const* g,
                                      uint32_t* amax_words, const DeviceInfo& dev, cudaStream_t st) {
-  // non-empty tensors, largest first (the fused kernels then pair tensors of similar size)
+  // Non-empty tensors: the smallest first (its amax pass is the one that runs alone), then the
+  // rest largest first (the fused kernels then pair tensors of similar size, and the encoding
+  // that runs alone at the end is that of the smallest remaining tensor).
   std::vector<int> order;
   for (int i = 0; i < count; ++i)
     if (rows[i] > 0) order.push_back(i);
   if (order.empty()) return NVFP4RL_OK;
   const auto numel = [&](int i) { return rows[i] * cols[i]; };
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return numel(a) > numel(b); });
+  std::rotate(order.begin(), order.end() - 1, order.end());
   uint32_t* word = amax_words;  // tensor i: word[4 i]
   if (launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>((count + 255) / 256)), dim3(256), 0, st, amax_words,
                  count) != cudaSuccess)
@@ -691,31 +698,21 @@ nvfp4rl_status launch_quantize_batch(int count, const void* const* x, const int6
   const int first = order[0];
   nvfp4rl_status sa = launch_amax_accumulate(x[first], dtype, numel(first), word + 4 * first, dev, st);
   if (sa != NVFP4RL_OK) return sa;
+  static std::mutex attr_mu;
+  {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (cudaFuncSetAttribute(encode_amax_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmem) !=
+        cudaSuccess)
+      return NVFP4RL_ERR_CUDA;
+  }
   for (size_t k = 0; k + 1 < order.size(); ++k) {
     const int i = order[k], n = order[k + 1];
-    const int64_t nblocks = numel(i) / 16, nvec_n = numel(n) * 2 / 16;
-    // words of the next tensor per encoding iteration so that both streams end together
-    const int64_t iters_bound = (nblocks + 1) / 2;  // iterations of the whole grid x threads, times stride
-    const int64_t qwant = (nvec_n + iters_bound - 1) / std::max<int64_t>(iters_bound, 1);
-    cudaError_t e;
-    if (qwant <= 1) {
-      const int grid = static_cast<int>(std::min<int64_t>(dev.sm_count * encode_amax_ctas_per_sm<1>(dev.device),
-                                                          (nblocks + 255) / 256));
-      e = launch_encode_amax<1>(x[i], nblocks, word + 4 * i, codes[i], scales[i], g[i], x[n], nvec_n, word + 4 * n,
-                                grid, st);
-    } else if (qwant <= 2) {
-      const int grid = static_cast<int>(std::min<int64_t>(dev.sm_count * encode_amax_ctas_per_sm<2>(dev.device),
-                                                          (nblocks + 255) / 256));
-      e = launch_encode_amax<2>(x[i], nblocks, word + 4 * i, codes[i], scales[i], g[i], x[n], nvec_n, word + 4 * n,
-                                grid, st);
-    } else {
-      // largest first: the next tensor is never larger, so at most 4 words per iteration
-      const int grid = static_cast<int>(std::min<int64_t>(dev.sm_count * encode_amax_ctas_per_sm<4>(dev.device),
-                                                          (nblocks + 255) / 256));
-      e = launch_encode_amax<4>(x[i], nblocks, word + 4 * i, codes[i], scales[i], g[i], x[n], nvec_n, word + 4 * n,
-                                grid, st);
-    }
-    if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
+    const int64_t nblocks = numel(i) / 16, bytes_n = numel(n) * 2;
+    if (launch_pdl(encode_amax_ring_kernel, dim3(static_cast<unsigned>(2 * dev.sm_count)), dim3(kFusedThreads),
+                   static_cast<size_t>(kFusedSmem), st, x[i], nblocks, static_cast<const uint32_t*>(word + 4 * i),
+                   codes[i], scales[i], g[i], static_cast<const uint8_t*>(x[n]), bytes_n, word + 4 * n,
+                   dev.status) != cudaSuccess)
+      return NVFP4RL_ERR_CUDA;
     if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
   }
   const int last = order.back();
