@@ -638,6 +638,28 @@ nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_b
   return launch_amax_accumulate(x, dtype, n, amax_bits, dev, st);
 }
 
+namespace {
+
+// CTAs of quantize_kernel resident per SM (once per device and variant).
+template <int kDtype, bool kGuided>
+int quantize_ctas_per_sm(int device) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(device);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<kDtype, kGuided>, 256, 0) != cudaSuccess ||
+      n < 1) {
+    cudaGetLastError();
+    n = 8;
+  }
+  cache[device] = n;
+  return n;
+}
+
+}  // namespace
+
 nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
                                uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done) {
@@ -649,8 +671,13 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
     const nvfp4rl_status sa = launch_amax(x, dtype, n, amax_scratch, dev, st);
     if (sa != NVFP4RL_OK) return sa;
   }
+  // one wave: as many CTAs as can be resident at once (each loops over its share of the blocks)
   const int64_t want = (nblocks + threads - 1) / threads;
-  const int grid = static_cast<int>(want < dev.sm_count * 8 ? want : dev.sm_count * 8);
+  const int per_sm = dtype == NVFP4RL_BF16 ? (mask ? quantize_ctas_per_sm<NVFP4RL_BF16, true>(dev.device)
+                                                   : quantize_ctas_per_sm<NVFP4RL_BF16, false>(dev.device))
+                                          : (mask ? quantize_ctas_per_sm<NVFP4RL_F32, true>(dev.device)
+                                                  : quantize_ctas_per_sm<NVFP4RL_F32, false>(dev.device));
+  const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(dev.sm_count) * per_sm));
   cudaError_t e;
   if (dtype == NVFP4RL_BF16) {
     e = mask ? launch_pdl(quantize_kernel<NVFP4RL_BF16, true>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
