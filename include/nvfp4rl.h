@@ -215,6 +215,16 @@ NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_w4a4(const uint16_t* x, int64_t M, 
 /* Workspace bytes an operation needs for these sizes (0 on invalid sizes). */
 NVFP4RL_API size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r, int32_t num_groups);
 
+/*
+ * nvfp4rl_selftest_wait_timeout -- failure-path self-test (the pages have no counterpart):
+ *   launches one small kernel on `stream` in which a thread waits, through the same bounded
+ *   wait every pipeline kernel uses, on a barrier that nothing ever completes. After 1 ms
+ *   the wait gives up, sets its bit in the device status word and the kernel returns, so
+ *   the next nvfp4rl_device_status() reports NVFP4RL_ERR_TIMEOUT and the context stays
+ *   usable. Returns the launch status.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4rl_selftest_wait_timeout(void* stream);
+
 /* Static, human-readable name of a status code. */
 NVFP4RL_API const char* nvfp4rl_status_string(nvfp4rl_status status);
 

@@ -48,6 +48,7 @@ def _signatures():
         "nvfp4rl_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
         "nvfp4rl_status_string": (c.c_char_p, [c.c_int]),
         "nvfp4rl_device_status": (c.c_int, [p, i32]),
+        "nvfp4rl_selftest_wait_timeout": (c.c_int, [p]),
         "nvfp4rl_kernel_launches": (c.c_uint64, []),
     }
 

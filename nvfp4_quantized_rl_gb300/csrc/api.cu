@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace nvfp4rl {
 
@@ -48,6 +49,19 @@ nvfp4rl_status current_device(DeviceInfo* out) {
 }
 
 int64_t rmsnorm_max_h();
+
+// One thread waits, through the kernels' bounded wait, on a fresh mbarrier that nothing ever
+// arrives on; after 1 ms the wait gives up, sets kStatusTimeoutProducer and the kernel returns.
+__global__ void wait_timeout_probe_kernel(uint32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    sm100::mbar_init(sm100::smem_addr(&bar), 1);
+    sm100::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sm100::mbar_wait<1000000ull>(sm100::smem_addr(&bar), 0, status, sm100::kStatusTimeoutProducer);
+  __syncthreads();
+}
 
 }  // namespace nvfp4rl
 
@@ -282,6 +296,14 @@ const char* nvfp4rl_status_string(nvfp4rl_status status) {
 }
 
 uint64_t nvfp4rl_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+nvfp4rl_status nvfp4rl_selftest_wait_timeout(void* stream) {
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev.status);
+  return launch_status();
+}
 
 nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4RL_ERR_CUDA;

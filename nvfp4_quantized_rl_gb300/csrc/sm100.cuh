@@ -94,8 +94,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed, for at most kWaitLimitNs.
+// Waits until the phase with the given parity has completed, for at most kLimitNs (every
+// kernel uses the default; the library's self-test of this path uses a short limit).
 // On timeout: sets `code` in *status and returns false.
+template <uint64_t kLimitNs = kWaitLimitNs>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status, uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -103,7 +105,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > kLimitNs) {
       atomicOr(status, code);
       return false;
     }
