@@ -451,8 +451,8 @@ def run_ops(args, torch, step, ops, flush, stream, rank):
 def run_suite(args):
     """Secondary measurements of the other configurations on the path (not the headline step):
     W4A4 prefill (7B shapes, 4096 tokens; 32B gate, 8192 tokens), W4A16 at 256 tokens on the 32B
-    shapes, the grouped MoE layer (128 experts, 32768 routed rows), and the NVFP4 encode of one 32B
-    layer. One JSON line per case: device time per call through the public API (eager, a 256 MB
+    shapes, the grouped MoE layer (128 experts, 32768 routed rows), the NVFP4 encode of one 32B
+    layer (per tensor and batched), the guided encode, and RMSNorm-AQN at prefill sizes. One JSON line per case: device time per call through the public API (eager, a 256 MB
     read evicts L2 before each call), achieved TFLOP/s and GB/s, and the fraction of the binding
     roof (FP4 tensor peak = the measured bf16 peak x 6, the nominal 13.5 / 2.25 ratio)."""
     import torch
@@ -610,6 +610,49 @@ def run_suite(args):
         emit("quantize_32b_layer", tot_us, 0, tot_bytes, "hbm",
              {"note": "amax + encode of the seven weights, each call timed separately and summed; bytes count each "
                       "element once (2 B in, 0.5625 B out)"})
+    # ---- the same seven 32B weights in one nvfp4_quantize_batch call (the weight refresh)
+    if want("quantize_batch_32b"):
+        shapes = [(5120, 5120), (1024, 5120), (1024, 5120), (5120, 5120), (27648, 5120), (27648, 5120), (5120, 27648)]
+        Ws = [weight(n, k, 0.015) for n, k in shapes]
+        cs = [torch.empty(n, k // 2, dtype=torch.uint8, device=dev) for n, k in shapes]
+        ss = [torch.empty(n, k // 16, dtype=torch.uint8, device=dev) for n, k in shapes]
+        gs = [torch.empty(1, dtype=torch.float32, device=dev) for _ in shapes]
+        wsb = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, len(shapes), 0, 0), dtype=torch.uint8, device=dev)
+        us = timed(lambda: nv.nvfp4_quantize_batch(Ws, codes=cs, scales=ss, g=gs, workspace=wsb), 5)
+        emit("quantize_batch_32b_layer", us, 0, sum(bytes_quantize(n * k) for n, k in shapes), "hbm",
+             {"note": "amax + encode of the seven weights in one nvfp4_quantize_batch call; bytes count each element "
+                      "once (2 B in, 0.5625 B out)"})
+        del Ws, cs, ss, gs, wsb
+        torch.cuda.empty_cache()
+    # ---- guided encode (a 1-bit mask per element picks the rounding direction) of the 7B gate weight
+    if want("quantize_guided"):
+        n, k = 18944, 3584
+        W = weight(n, k)
+        mask = torch.randint(-2 ** 31, 2 ** 31 - 1, ((n * k + 31) // 32,), generator=gen, device=dev,
+                             dtype=torch.int64).to(torch.int32)  # Bernoulli(1/2) bits
+        c = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(n, k // 16, dtype=torch.uint8, device=dev)
+        g = torch.empty(1, dtype=torch.float32, device=dev)
+        wsq = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
+        us_g = timed(lambda: nv.nvfp4_quantize_guided(W, mask, codes=c, scales=sc, g=g, workspace=wsq), 10)
+        emit("quantize_guided_7b_gate", us_g, 0, n * k * (2 + 0.5625 + 0.125), "hbm",
+             {"shape": [n, k], "note": "amax + guided encode; bytes: 2 B in, 0.5625 B out, 0.125 B of mask per element"})
+        us_p = timed(lambda: nv.nvfp4_quantize(W, codes=c, scales=sc, g=g, workspace=wsq), 10)
+        emit("quantize_plain_7b_gate", us_p, 0, n * k * (2 + 0.5625), "hbm",
+             {"shape": [n, k], "note": "amax + plain encode, same weight"})
+        del W, mask, c, sc, g
+        torch.cuda.empty_cache()
+    # ---- RMSNorm-AQN at prefill sizes (HBM-bound there; M = 64 in the step is bound by launch latency)
+    if want("rmsnorm_prefill"):
+        for m, h in [(4096, 3584), (8192, 5120)]:
+            x = activations(m, h, heavy=False)
+            w = (1.0 + randn(h, std=0.1)).float()
+            z = randn(h)
+            y = torch.empty(m, h, dtype=torch.bfloat16, device=dev)
+            us = timed(lambda: nv.rmsnorm_aqn(x, w, z, 0.01, 1e-6, out=y), 10)
+            emit(f"rmsnorm_aqn_m{m}_h{h}", us, 0, bytes_rmsnorm(m, h), "hbm", {"shape": [m, h]})
+            del x, w, z, y
+            torch.cuda.empty_cache()
 
 
 def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, Q, Y, h1, h2, ws, flush, inputs,
@@ -774,7 +817,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--op", default=None, help="time single ops of the step instead (see select_ops)")
-    ap.add_argument("--suite", default=None,
+    ap.add_argument("--suite", default=None, nargs="?", const="all",
                     help="secondary measurements instead: all or any of w4a4_7b,w4a16_32b,w4a4_32b,moe,quantize_32b")
     args = ap.parse_args()
     if args.warmup < 3:
