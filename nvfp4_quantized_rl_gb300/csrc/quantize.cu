@@ -22,6 +22,7 @@
 // directed-rounding multiplies (__fmul_rd / __fmul_ru). Non-negative fp32 values
 // order like their bit patterns, so the compares run on integers.
 #include <map>
+#include <type_traits>
 #include <mutex>
 #include <vector>
 
@@ -295,6 +296,39 @@ __device__ void build_encode_tables(EncodeTables& t, float g) {
   }
 }
 
+// Per-tensor thresholds of the guided encoding for bf16 input, built in shared memory like
+// EncodeTables: for scale byte b and grid point G_k (0.5, 1, 1.5, 2, 3, 4, 6), in both halves of
+// a word, ge: x >= G_k E4M3(b) g <=> x > ge (pred of the bf16 rounded up), gt: x > G_k E4M3(b) g
+// <=> x > gt (the bf16 rounded down); b = 0: +inf.
+struct GuidedTables {
+  uint4 ge[0x7F][2];
+  uint4 gt[0x7F][2];
+};
+
+__device__ void build_guided_tables(GuidedTables& t, float g) {
+  const float grid[7] = {0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+  for (int b = threadIdx.x; b < 0x7F; b += blockDim.x) {
+    uint32_t e[8], u[8];
+    if (b == 0 || !(g > 0.0f)) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) e[k] = u[k] = 0x7F807F80u;
+    } else {
+      const float dec = e4m3_decode_pos(b);
+#pragma unroll
+      for (int k = 0; k < 7; ++k) {
+        const uint32_t te = bf16_ru(__fmul_ru(grid[k] * dec, g)) - 1u, tu = bf16_rd(__fmul_rd(grid[k] * dec, g));
+        e[k] = te | (te << 16);
+        u[k] = tu | (tu << 16);
+      }
+      e[7] = u[7] = 0u;
+    }
+    t.ge[b][0] = make_uint4(e[0], e[1], e[2], e[3]);
+    t.ge[b][1] = make_uint4(e[4], e[5], e[6], e[7]);
+    t.gt[b][0] = make_uint4(u[0], u[1], u[2], u[3]);
+    t.gt[b][1] = make_uint4(u[4], u[5], u[6], u[7]);
+  }
+}
+
 // Exact E4M3 scale byte of bamax / (6 g) from the estimate `est` and the midpoint table: the
 // same decision as scale_byte, with the midpoint products looked up instead of computed.
 __device__ __forceinline__ uint32_t scale_byte_tab(float bamax, float est, const EncodeTables& t) {
@@ -345,6 +379,55 @@ __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t b
     const uint32_t m = acc & 0x00070007u;
     const uint32_t s = w[i] & 0x80008000u;
     // low byte: magnitude of element 2i in bits 0-2, its sign in bit 3, element 2i+1 in bits 4-7
+    byte[i] = m | (m >> 12) | (s >> 12) | (s >> 24);
+  }
+  const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
+  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo, hi);
+  scales[blk] = static_cast<uint8_t>(b);
+}
+
+// Guided encoding of one block of bf16 values (finite), two elements per instruction: c_ge and
+// c_gt count the grid points below-or-at and strictly below |x| (bf16x2 compares against the
+// tables), x is on the grid when they differ or x = 0, and the magnitude is c_ge, plus one when
+// the element's mask bit is set, x is off the grid and c_ge < 7. The scale byte is the plain one.
+__device__ __forceinline__ void encode_block_bf16_guided(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
+                                                         float est_scale, const EncodeTables& tab,
+                                                         const GuidedTables& gtab, const uint32_t* __restrict__ mask,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+  uint32_t aw[8];
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    aw[i] = w[i] & 0x7FFF7FFFu;
+    m2 = __vmaxu2(m2, aw[i]);
+  }
+  const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+  uint32_t b = 0;
+  if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, tab);
+  const uint4 ea = gtab.ge[b][0], eb = gtab.ge[b][1], ua = gtab.gt[b][0], ub = gtab.gt[b][1];
+  const uint32_t GE[7] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z};
+  const uint32_t GT[7] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z};
+  const uint32_t up_bits = (mask[blk >> 1] >> ((blk & 1) * 16)) & (b ? 0xFFFFu : 0u);
+  uint32_t byte[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t ce = 0x43004300u, cu = 0x43004300u;  // bf16x2 (128, 128): the counts land in bits 0-2
+#pragma unroll
+    for (int k = 0; k < 7; ++k) {
+      ce = bf16x2_add(ce, bf16x2_gt(aw[i], GE[k]));
+      cu = bf16x2_add(cu, bf16x2_gt(aw[i], GT[k]));
+    }
+    const uint32_t c = ce & 0x00070007u;
+    // per 16-bit half, as 0/1 in bit 0: on the grid (the counts differ), x != 0, c == 7
+    const uint32_t on = (((ce ^ cu) & 0x00070007u) + 0x00070007u) >> 3 & 0x00010001u;
+    const uint32_t nz = ((aw[i] + 0x7FFF7FFFu) >> 15) & 0x00010001u;
+    const uint32_t c7 = ((c + 0x00010001u) >> 3) & 0x00010001u;
+    const uint32_t t = up_bits >> (2 * i);
+    const uint32_t up = (t & 1u) | ((t & 2u) << 15);
+    const uint32_t m = c + (up & nz & ~on & ~c7 & 0x00010001u);
+    const uint32_t s = w[i] & 0x80008000u;
     byte[i] = m | (m >> 12) | (s >> 12) | (s >> 24);
   }
   const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
@@ -453,8 +536,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   const float g6 = 6.0f * (g * est_scale);
   const float inv_g6 = 1.0f / g6;
   __shared__ EncodeTables tab;
-  if (kDtype == NVFP4RL_BF16 && !kGuided) {
+  // the guided tables exist only in the bf16 guided kernel
+  __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kGuided, GuidedTables, char> gtab;
+  if constexpr (kDtype == NVFP4RL_BF16) {
     build_encode_tables(tab, g);
+    if constexpr (kGuided) build_guided_tables(gtab, g);
     __syncthreads();
   }
 
@@ -472,6 +558,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
     if constexpr (kDtype == NVFP4RL_BF16 && !kGuided) {
       encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
       if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
+    } else if constexpr (kDtype == NVFP4RL_BF16) {
+      encode_block_bf16_guided(a.v, blk, g, inv_g6, est_scale, tab, gtab, mask, codes, scales);
+      if (two) encode_block_bf16_guided(b.v, blk2, g, inv_g6, est_scale, tab, gtab, mask, codes, scales);
     } else {
       encode_block<kDtype, kGuided>(a, blk, g, est_scale, g6, mask, codes, scales);
       if (two) encode_block<kDtype, kGuided>(b, blk2, g, est_scale, g6, mask, codes, scales);
