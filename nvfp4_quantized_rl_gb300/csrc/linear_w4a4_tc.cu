@@ -24,7 +24,8 @@
 //               separate accumulator.
 //   warps 2-5   epilogue: TMEM -> registers, Y = g_x g_w D + s D_lora, bf16 stores; the
 //               accumulator is double buffered so it overlaps the next tile's main loop.
-//   warps 6-9   scale factors: each warp writes the stage's scale bytes of both operands into
+//   warps 6-9, 13-16  scale factors (two groups, alternate stages): each warp writes the
+//               stage's scale bytes of both operands into
 //               its own TMEM lane quarter with tcgen05.st (lane i, column 4t + w holds the four
 //               bytes of row 32w + i for K step t: the four lane quarters hold the same copy),
 //               into one of four TMEM slots that the MMAs release. This keeps the scale traffic
@@ -57,8 +58,9 @@ constexpr int kSfRing = 4;                       // scale ring stages
 constexpr int kSfSlots = 4;                      // TMEM scale-factor slots (32 columns each)
 constexpr int kMaxCodeStages = 6;
 constexpr int kDoneRing = 8;                     // "stage's MMAs done" barriers, > kMaxCodeStages, kSfSlots
-constexpr int kThreads = 416;
-constexpr int kFirstSfWarp = 6;
+constexpr int kThreads = 544;
+constexpr int kFirstSfWarp = 6;        // scale warps 6-9 take the even stages, 13-16 the odd ones
+constexpr int kSecondSfWarp = 13;
 constexpr int kSfProducerWarp = 10;   // activation scales; weight scales: warp 12
 constexpr int kWCodeWarp = 11;
 constexpr uint32_t kD0 = 0, kD1 = 128, kDL = 256, kSF = 384;  // TMEM columns
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t xdesc0 = smem_desc(smem_addr(smem), 16, 1024, 2);
       const uint64_t wdesc0 = smem_desc(smem_addr(smem + kCodeBytes), 16, 1024, 2);
       int c = 0, j = 0, li = 0, it = 0;
-      uint32_t cph = 0, jph = 0;
+      uint32_t jph = 0;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
         const int buf = li & 1;
         const uint32_t dcol = buf ? kD1 : kD0;
@@ -291,9 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         for (int k = 0; k < ksteps; ++k) {
-          // scale slot j written (tcgen05.st + fence by the scale warps), code stage c landed
-          if (!mbar_wait(smem_addr(&sfready[j]), jph, p.status, kStatusTimeoutMma) ||
-              !mbar_wait(smem_addr(&cfull[c]), cph, p.status, kStatusTimeoutMma)) {
+          // scale slot j written (tcgen05.st + fence by the scale warps), which the scale warps
+          // signal only after they have seen code stage c land: one wait per stage here
+          if (!mbar_wait(smem_addr(&sfready[j]), jph, p.status, kStatusTimeoutMma)) {
             ok = false;
             break;
           }
@@ -304,10 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          k ? 1u : 0u);
           mma_commit(smem_addr(&mdone[it % kDoneRing]));
           ++it;
-          if (++c == S) {
-            c = 0;
-            cph ^= 1u;
-          }
+          if (++c == S) c = 0;
           if (++j == kSfSlots) {
             j = 0;
             jph ^= 1u;
@@ -332,16 +331,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= kFirstSfWarp && warp < kFirstSfWarp + 4) {
+  } else if ((warp >= kFirstSfWarp && warp < kFirstSfWarp + 4) || (warp >= kSecondSfWarp && warp < kSecondSfWarp + 4)) {
     // ---------------------------------------------------------------- scale factors -> TMEM
     // Scale tile in shared memory: [128 rows][16 bytes], word t = the four block scales of K
     // step t. Lane i gathers rows i, 32 + i, 64 + i, 96 + i and writes, per operand, 16 columns:
-    // column 4t + w = row 32w + i, K step t (the layout the MMA reads for M = 128).
+    // column 4t + w = row 32w + i, K step t (the layout the MMA reads for M = 128). Two groups of
+    // four warps (one per lane quarter) take alternate stages; ring slots and TMEM slots are
+    // stage mod 4, so each group keeps its own slots.
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int f = 0, j = 0, it = 0;
-    uint32_t fph = 0;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      for (int k = 0; k < ksteps; ++k, ++it) {
+    const int grp = warp >= kSecondSfWarp ? 1 : 0;
+    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int total = my_tiles * ksteps;
+    for (int it = grp; it < total && ok; it += 2) {
+      const int f = it % kSfRing, j = it % kSfSlots;
+      const uint32_t fph = static_cast<uint32_t>((it / kSfRing) & 1);
+      {
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&ffull[f]), fph, p.status, kStatusTimeoutMma));
         if (!ok) break;
         const uint8_t* st = sfring + f * kSfStageBytes;
@@ -368,16 +372,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(tmem + lane_base + sfcol + 16, v[1]);
         tmem_st_wait();
         tc_fence_before();
+        // the stage's code tiles have landed too (the MMA issuer then waits on sfready alone)
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&cfull[it % S]), static_cast<uint32_t>((it / S) & 1),
+                                               p.status, kStatusTimeoutMma));
+        if (!ok) break;
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(smem_addr(&sfready[j]));
           mbar_arrive(smem_addr(&fempty[f]));  // the shared-memory scale tiles may be refilled
         }
-        if (++f == kSfRing) {
-          f = 0;
-          fph ^= 1u;
-        }
-        if (++j == kSfSlots) j = 0;
       }
     }
   } else if (warp >= 2 && warp < 6) {
