@@ -642,6 +642,32 @@ def run_suite(args):
              {"shape": [n, k], "note": "amax + plain encode, same weight"})
         del W, mask, c, sc, g
         torch.cuda.empty_cache()
+    # ---- RMSNorm-AQN fused with the NVFP4 quantization of its output (the W4A4 activation operand)
+    if want("rmsnorm_quantize"):
+        m, h = 4096, 3584
+        x = activations(m, h)
+        w = (1.0 + randn(h, std=0.1)).float()
+        z = randn(h)
+        y = torch.empty(m, h, dtype=torch.bfloat16, device=dev)
+        c = torch.empty(m, h // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(m, h // 16, dtype=torch.uint8, device=dev)
+        g = torch.empty(1, dtype=torch.float32, device=dev)
+        wsq = torch.empty(nv.workspace_bytes(nv.OP_RMSNORM_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
+        us_f = timed(lambda: nv.rmsnorm_aqn_quantize(x, w, z, 0.01, 1e-6, out=y, codes=c, scales=sc, g=g,
+                                                     workspace=wsq), 10)
+        fused_bytes = m * h * (2 + 2 + 0.5625)  # x in; y, codes and scales out
+        emit(f"rmsnorm_quantize_m{m}_h{h}", us_f, 0, fused_bytes, "hbm",
+             {"shape": [m, h], "note": "rmsnorm_aqn_quantize: one cooperative kernel keeps y on chip"})
+
+        def separate():
+            nv.rmsnorm_aqn(x, w, z, 0.01, 1e-6, out=y)
+            nv.nvfp4_quantize(y, codes=c, scales=sc, g=g, workspace=wsq)
+        us_s = timed(separate, 10)
+        emit(f"rmsnorm_then_quantize_m{m}_h{h}", us_s, 0, fused_bytes, "hbm",
+             {"shape": [m, h], "note": "rmsnorm_aqn, then nvfp4_quantize of y (amax pass + encode pass): same bytes "
+                                       "counted, for comparison"})
+        del x, w, z, y, c, sc, g, wsq
+        torch.cuda.empty_cache()
     # ---- RMSNorm-AQN at prefill sizes (HBM-bound there; M = 64 in the step is bound by launch latency)
     if want("rmsnorm_prefill"):
         for m, h in [(4096, 3584), (8192, 5120)]:

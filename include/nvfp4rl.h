@@ -65,7 +65,8 @@ enum {
   NVFP4RL_OP_QUANTIZE = 0,
   NVFP4RL_OP_LINEAR_W4A16 = 1,
   NVFP4RL_OP_LINEAR_W4A4 = 2,
-  NVFP4RL_OP_QUANTIZE_BATCH = 3 /* M = number of tensors */
+  NVFP4RL_OP_QUANTIZE_BATCH = 3, /* M = number of tensors */
+  NVFP4RL_OP_RMSNORM_QUANTIZE = 4
 };
 
 /*
@@ -170,6 +171,23 @@ NVFP4RL_API double aqn_sigma(double sigma0, double sigmaK, int64_t k, int64_t K)
  */
 NVFP4RL_API nvfp4rl_status rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
                            float sigma, float delta, uint16_t* y, void* stream);
+
+/*
+ * rmsnorm_aqn_quantize -- rmsnorm_aqn followed by nvfp4_quantize of its output, the activation
+ *   operand of a W4A4 linear (TRACE summary, "論文が取り組む課題": FP4 activations; QeRL
+ *   explainer, "ゼロオーバーヘッド：レイヤー正規化への統合": the noise lives in the norm).
+ *   y is exactly what rmsnorm_aqn writes; codes, scales and g are exactly what
+ *   nvfp4_quantize(y, ...) writes (amax over all of y).
+ *   Arguments as rmsnorm_aqn and nvfp4_quantize; H a multiple of 16, at most 8192.
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_RMSNORM_QUANTIZE, 0, 0, 0, 0, 0) bytes.
+ *   When every SM's share of y fits in its shared memory (e.g. 4096 x 3584), one cooperative
+ *   kernel keeps y on chip between the norm and the encoding (x read once, y and the codes
+ *   written once); otherwise RMSNorm-AQN, the amax and the encoding run one after another.
+ */
+NVFP4RL_API nvfp4rl_status rmsnorm_aqn_quantize(const uint16_t* x, int64_t M, int64_t H, const float* w,
+                                                const float* eps, float sigma, float delta, uint16_t* y,
+                                                uint8_t* codes, uint8_t* scales, float* g, void* workspace,
+                                                size_t workspace_bytes, void* stream);
 
 /*
  * nvfp4_lora_linear -- W4A16 linear layer with the LoRA branch fused

@@ -8,7 +8,8 @@ importing the binding does not build it, and every call fails loudly when the
 library or a GPU is missing -- there is no CPU fallback.
 
 Functions carry the C names: nvfp4_amax, nvfp4_quantize, nvfp4_quantize_guided,
-nvfp4_quantize_batch, aqn_sigma, rmsnorm_aqn, nvfp4_lora_linear, nvfp4_lora_linear_w4a4.
+nvfp4_quantize_batch, aqn_sigma, rmsnorm_aqn, rmsnorm_aqn_quantize, nvfp4_lora_linear,
+nvfp4_lora_linear_w4a4.
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ LIB_PATH = _build.LIB
 
 OK = 0
 BF16, F32 = 0, 1
-OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH = 0, 1, 2, 3
+OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH, OP_RMSNORM_QUANTIZE = 0, 1, 2, 3, 4
 
 _lock = threading.Lock()
 _lib = None
@@ -41,6 +42,7 @@ def _signatures():
         "nvfp4_quantize_batch": (c.c_int, [i32, p, p, p, i32, p, p, p, p, sz, p]),
         "aqn_sigma": (f64, [f64, f64, i64, i64]),
         "rmsnorm_aqn": (c.c_int, [p, i64, i64, p, p, f32, f32, p, p]),
+        "rmsnorm_aqn_quantize": (c.c_int, [p, i64, i64, p, p, f32, f32, p, p, p, p, p, sz, p]),
         "nvfp4_lora_linear": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
         "nvfp4_lora_linear_w4a4": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
         "nvfp4_lora_linear_noalloc": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, p]),
@@ -233,6 +235,28 @@ def rmsnorm_aqn(x, w, eps=None, sigma: float = 0.0, delta: float = 1e-6, out=Non
     st = lib().rmsnorm_aqn(_ptr(x), M, H, _ptr(w), _ptr(eps), float(sigma), float(delta), _ptr(out), _stream(x, stream))
     _check(st, "rmsnorm_aqn")
     return out
+
+
+def rmsnorm_aqn_quantize(x, w, eps=None, sigma: float = 0.0, delta: float = 1e-6, out=None, codes=None, scales=None,
+                         g=None, workspace=None, stream=None):
+    """rmsnorm_aqn of bf16 x [M, H] and the NVFP4 quantization of its output in one call
+    -> (y bf16 [M, H], codes u8 [M, H/2], scales u8 [M, H/16], g f32 [1])."""
+    import torch
+    _require_cuda(x, w, eps)
+    _bits16(x)
+    M, H = x.shape
+    dev = x.device
+    out = _empty((M, H), torch.bfloat16, dev) if out is None else out
+    codes = _empty((M, H // 2), torch.uint8, dev) if codes is None else codes
+    scales = _empty((M, H // 16), torch.uint8, dev) if scales is None else scales
+    g = _empty((1,), torch.float32, dev) if g is None else g
+    if workspace is None:
+        workspace = _empty((workspace_bytes(OP_RMSNORM_QUANTIZE, 0, 0, 0),), torch.uint8, dev)
+    st = lib().rmsnorm_aqn_quantize(_ptr(x), M, H, _ptr(w), _ptr(eps), float(sigma), float(delta), _ptr(out),
+                                    _ptr(codes), _ptr(scales), _ptr(g), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(x, stream))
+    _check(st, "rmsnorm_aqn_quantize")
+    return out, codes, scales, g
 
 
 def _linear(fn_name, op, x, codes, scales, g, A, B, s, group_offsets, num_groups, out, workspace, stream):

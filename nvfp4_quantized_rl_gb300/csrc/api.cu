@@ -251,6 +251,36 @@ nvfp4rl_status rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float*
   return launch_rmsnorm_aqn(x, M, H, w, eps, sigma, delta, y, dev, static_cast<cudaStream_t>(stream));
 }
 
+nvfp4rl_status rmsnorm_aqn_quantize(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
+                                    float sigma, float delta, uint16_t* y, uint8_t* codes, uint8_t* scales, float* g,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || H <= 0 || !std::isfinite(sigma) || !(delta >= 0.0f) || !std::isfinite(delta))
+    return NVFP4RL_ERR_INVALID_ARG;
+  if (M == 0) return NVFP4RL_OK;
+  if (!x || !w || !y || !codes || !scales || !g) return NVFP4RL_ERR_INVALID_ARG;
+  if (H % 16 != 0 || H > rmsnorm_max_h() || M > 2147483647LL) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (eps && !aligned16(eps)) || !aligned16(codes) ||
+      !aligned16(scales) || (reinterpret_cast<uintptr_t>(g) & 3u))
+    return NVFP4RL_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < kQuantizeWorkspace) return NVFP4RL_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NVFP4RL_ERR_MISALIGNED;
+  const size_t n = static_cast<size_t>(M) * H;
+  const void* outs[4] = {y, codes, scales, g};
+  const size_t osz[4] = {n * 2, n / 2, n / 16, 4};
+  for (int i = 0; i < 4; ++i) {
+    if (overlap(outs[i], osz[i], x, n * 2) || overlap(outs[i], osz[i], w, H * 4) ||
+        (eps && overlap(outs[i], osz[i], eps, H * 4)) || overlap(outs[i], osz[i], workspace, kQuantizeWorkspace))
+      return NVFP4RL_ERR_ALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], osz[i], outs[j], osz[j])) return NVFP4RL_ERR_ALIAS;
+  }
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_rmsnorm_quantize(x, M, H, w, eps, sigma, delta, y, codes, scales, g, static_cast<uint32_t*>(workspace),
+                                 dev, static_cast<cudaStream_t>(stream));
+}
+
 nvfp4rl_status nvfp4_lora_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
                                  const uint8_t* w_scales, const float* w_g, int64_t N, const uint16_t* lora_A,
                                  const uint16_t* lora_B, int32_t r, float s, const int32_t* group_offsets,
@@ -274,6 +304,7 @@ size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int3
   switch (op) {
     case NVFP4RL_OP_QUANTIZE: return kQuantizeWorkspace;
     case NVFP4RL_OP_QUANTIZE_BATCH: return M <= kQuantizeBatchMax ? quantize_batch_workspace_bytes(M) : 0;
+    case NVFP4RL_OP_RMSNORM_QUANTIZE: return kQuantizeWorkspace;
     case NVFP4RL_OP_LINEAR_W4A16: return linear_workspace_bytes(false, M, N, K, r, 1);
     case NVFP4RL_OP_LINEAR_W4A4: return linear_workspace_bytes(true, M, N, K, r, num_groups > 0 ? num_groups : 1);
     default: return 0;

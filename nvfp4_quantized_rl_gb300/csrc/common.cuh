@@ -136,6 +136,12 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
 nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
                                   float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st);
 
+// RMSNorm-AQN of x into y and the NVFP4 quantization of y (quantize.cu); sync: two zeroable
+// words 16 bytes apart (kQuantizeWorkspace bytes).
+nvfp4rl_status launch_rmsnorm_quantize(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
+                                      float sigma, float delta, uint16_t* y, uint8_t* codes, uint8_t* scales,
+                                      float* g, uint32_t* sync, const DeviceInfo& dev, cudaStream_t st);
+
 struct LinearArgs {
   const uint16_t* x;
   int64_t M, K, N;

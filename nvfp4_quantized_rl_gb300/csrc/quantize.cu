@@ -666,6 +666,142 @@ __global__ void __launch_bounds__(kFusedThreads, 2)
   if (threadIdx.x == 0) atomicMax(amax_next, max(red[0], red[1]));
 }
 
+// RMSNorm-AQN fused with the NVFP4 quantization of its output, for outputs that fit in shared
+// memory across the grid (one CTA per SM, launched cooperatively so that all CTAs are resident):
+//   phase 1  four warps per row, eight rows at a time: y = bf16((w + sigma eps) x /
+//            sqrt(mean x^2 + delta)) as in
+//            rmsnorm_aqn_kernel, written to y and kept in this CTA's shared memory; the running
+//            max of |y| (bf16 patterns) is reduced per CTA and folded into sync[0];
+//   barrier  every CTA arrives on the counter sync[4] and waits (bounded) for all the others:
+//            then sync[0] holds amax over all of y, so g = amax / 2688 is known;
+//   phase 2  this CTA's rows are encoded from shared memory with quantize_kernel's bf16 code
+//            (same blocks, tables and results as nvfp4_quantize of y).
+// y is read from HBM never: x in, y and the codes out. sync[0] and sync[4] start at zero.
+constexpr int kFuseThreads = 1024;
+constexpr int kFuseGroup = 128;  // threads per row (four warps)
+constexpr int kFuseVec = 4;      // 128-bit words of a row per thread: H <= 128 * 4 * 8 = 4096
+
+__global__ void __launch_bounds__(kFuseThreads, 1)
+    rmsnorm_quant_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t H, const float* __restrict__ w,
+                         const float* __restrict__ eps, float sigma, float delta, uint16_t* __restrict__ y,
+                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ g_out,
+                         uint32_t* __restrict__ sync, uint32_t* __restrict__ status) {
+  extern __shared__ __align__(16) uint8_t ysm[];  // row slot i: H bf16 values
+  __shared__ EncodeTables tab;
+  __shared__ float part[2][kFuseThreads / 32];    // per-warp sums of squares, by iteration parity
+  __shared__ uint32_t red[kFuseThreads / 32];
+  __shared__ int good;
+  constexpr int kGroups = kFuseThreads / kFuseGroup;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = threadIdx.x / kFuseGroup, t = threadIdx.x % kFuseGroup;
+  const int64_t G = gridDim.x, cta = blockIdx.x;
+  const int nrows = cta < M ? static_cast<int>((M - 1 - cta) / G + 1) : 0;
+  const int nvec = static_cast<int>(H / 8);
+  uint32_t am2 = 0;
+  // rows i = grp + kGroups * it of this CTA; all groups step together (block barriers)
+  for (int it = 0; it * kGroups < nrows; ++it) {
+    const int i = grp + kGroups * it;
+    const bool live = i < nrows;
+    const int64_t row = cta + static_cast<int64_t>(i) * G;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? row : 0) * H);
+    uint4 v[kFuseVec];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kFuseVec; ++k) {
+      const int j = t + kFuseGroup * k;
+      v[k] = live && j < nvec ? ld_nc_v4(xr + j) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kFuseVec; ++k) {
+      const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a = __uint_as_float(bf16_lo_bits(q[u])), b = __uint_as_float(bf16_hi_bits(q[u]));
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) part[it & 1][warp] = ss;
+    __syncthreads();
+    if (!live) continue;
+    const float* pg = &part[it & 1][grp * (kFuseGroup / 32)];
+    const float r = rsqrtf((pg[0] + pg[1] + pg[2] + pg[3]) / static_cast<float>(H) + delta);
+    uint4* yr = reinterpret_cast<uint4*>(y + row * H);
+    uint4* ys = reinterpret_cast<uint4*>(ysm + static_cast<size_t>(i) * H * 2);
+#pragma unroll
+    for (int k = 0; k < kFuseVec; ++k) {
+      const int j = t + kFuseGroup * k;
+      if (j < nvec) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j);
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j + 1);
+        float wt[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        if (eps) {
+          const float4 e0 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j);
+          const float4 e1 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j + 1);
+          const float et[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u) wt[u] = fmaf(sigma, et[u], wt[u]);
+        }
+        const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = __uint_as_float(bf16_lo_bits(q[u])) * r * wt[2 * u];
+          const float b = __uint_as_float(bf16_hi_bits(q[u])) * r * wt[2 * u + 1];
+          o[u] = f32_to_bf16_bits(a) | (f32_to_bf16_bits(b) << 16);
+          am2 = __vmaxu2(am2, o[u] & 0x7FFF7FFFu);
+        }
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        yr[j] = ov;
+        ys[j] = ov;
+      }
+    }
+  }
+  uint32_t m = max(am2 & 0xFFFFu, am2 >> 16) << 16;
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t cm = 0;
+    for (int i = 0; i < kFuseThreads / 32; ++i) cm = max(cm, red[i]);
+    atomicMax(sync, cm);
+    __threadfence();
+    atomicAdd(sync + 4, 1u);
+    // grid barrier: all CTAs are resident (cooperative launch); the wait is bounded all the same
+    const uint64_t t0 = globaltimer();
+    int ok = 1;
+    while (*reinterpret_cast<volatile uint32_t*>(sync + 4) < static_cast<uint32_t>(G)) {
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        atomicOr(status, kStatusTimeoutProducer);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    good = ok;
+  }
+  __syncthreads();
+  if (!good) return;
+  const float amax = __uint_as_float(*reinterpret_cast<volatile uint32_t*>(sync));
+  const float g = __fdiv_rn(amax, 2688.0f);
+  if (cta == 0 && threadIdx.x == 0) *g_out = g;
+  const bool tiny = g < 0x1p-60f;
+  const float est_scale = tiny ? 0x1p64f : 1.0f;
+  const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
+  build_encode_tables(tab, g);
+  __syncthreads();
+  const int nb_row = static_cast<int>(H / 16);
+  const int total = nrows * nb_row;
+  for (int b = threadIdx.x; b < total; b += kFuseThreads) {
+    const int i = b / nb_row, cb = b - i * nb_row;
+    const uint4* src = reinterpret_cast<const uint4*>(ysm + static_cast<size_t>(i) * H * 2 + static_cast<size_t>(cb) * 32);
+    const uint4 vv[2] = {src[0], src[1]};
+    encode_block_bf16(vv, (cta + i * G) * nb_row + cb, g, inv_g6, est_scale, tab, codes, scales);
+  }
+}
+
 // Clears the amax accumulator word (a kernel rather than a memset, so that it chains with the
 // neighbouring kernels by programmatic dependent launch).
 __global__ void zero_word_kernel(uint32_t* __restrict__ p) {
@@ -834,6 +970,38 @@ nvfp4rl_status launch_quantize_batch(int count, const void* const* x, const int6
   const int last = order.back();
   return launch_quantize(x[last], dtype, rows[last], cols[last], nullptr, codes[last], scales[last], g[last], nullptr,
                          word + 4 * last, dev, st, /*amax_done=*/true);
+}
+
+nvfp4rl_status launch_rmsnorm_quantize(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
+                                      float sigma, float delta, uint16_t* y, uint8_t* codes, uint8_t* scales,
+                                      float* g, uint32_t* sync, const DeviceInfo& dev, cudaStream_t st) {
+  if (M == 0) return NVFP4RL_OK;
+  if (launch_pdl(zero_words_kernel, dim3(1), dim3(32), 0, st, sync, 2) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  if (launch_status() != NVFP4RL_OK) return NVFP4RL_ERR_CUDA;
+  // fused path: every CTA's rows of y fit in its shared memory, one CTA per SM
+  const int64_t G = std::min<int64_t>(M, dev.sm_count);
+  const int64_t rows_per_cta = (M + G - 1) / G;
+  const size_t smem = static_cast<size_t>(rows_per_cta) * H * 2;
+  if (H / 8 <= kFuseGroup * kFuseVec && smem + 8 * 1024 <= dev.smem_optin) {
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int per_sm = 0;
+    if (cudaFuncSetAttribute(rmsnorm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
+            cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_quant_kernel, kFuseThreads, smem) == cudaSuccess &&
+        per_sm >= 1) {
+      void* args[] = {const_cast<uint16_t**>(&x), &M, &H, const_cast<float**>(&w), const_cast<float**>(&eps), &sigma,
+                      &delta, &y, &codes, &scales, &g, &sync, const_cast<uint32_t**>(&dev.status)};
+      if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(rmsnorm_quant_kernel), dim3(static_cast<unsigned>(G)),
+                                      dim3(kFuseThreads), args, smem, st) == cudaSuccess)
+        return launch_status();
+    }
+    cudaGetLastError();  // fall back below
+  }
+  // otherwise: RMSNorm-AQN, then the amax and the encoding of y (its words were cleared above)
+  const nvfp4rl_status s1 = launch_rmsnorm_aqn(x, M, H, w, eps, sigma, delta, y, dev, st);
+  if (s1 != NVFP4RL_OK) return s1;
+  return launch_quantize(y, NVFP4RL_BF16, M, H, nullptr, codes, scales, g, nullptr, sync, dev, st);
 }
 
 }  // namespace nvfp4rl

@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
-    for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "nvfp4_quantize_batch", "rmsnorm_aqn", "nvfp4_lora_linear",
+    for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "nvfp4_quantize_batch", "rmsnorm_aqn",
+                     "rmsnorm_aqn_quantize", "nvfp4_lora_linear",
                      "nvfp4_lora_linear_w4a4", "aqn_sigma"):
         assert required in names
 
@@ -135,6 +136,22 @@ def test_rmsnorm_validation(nv):
     assert L.rmsnorm_aqn(A0, 4, 64, A1, None, 0.0, -1.0, A2, None) == 1
     assert L.rmsnorm_aqn(A0, 4, 64, A1 + 4, None, 0.0, 1e-6, A2, None) == 2
     assert L.rmsnorm_aqn(A0, 4, 64, A1, None, 0.0, 1e-6, A0, None) == 7
+
+
+def test_rmsnorm_quantize_validation(nv):
+    L = nv.lib()
+    def call(x=A0, M=4, H=64, w=A1, eps=None, y=A2, c=A3, sc=A4, g=0x60000, ws=0x70000, wsb=256):
+        return L.rmsnorm_aqn_quantize(x, M, H, w, eps, 0.0, 1e-6, y, c, sc, g, ws, wsb, None)
+    assert nv.workspace_bytes(nv.OP_RMSNORM_QUANTIZE, 0, 0, 0) >= 8
+    assert call(x=None) == 1
+    assert call(H=40) == 3                       # not a multiple of 16
+    assert call(H=16384) == 3                    # above the largest row
+    assert call(y=A2 + 8) == 2                   # misaligned
+    assert call(ws=None) == 4
+    assert call(wsb=4) == 4
+    assert call(y=A0) == 7                       # y over x
+    assert call(c=A2) == 7                       # codes over y
+    assert call(g=0x70000) == 7                  # g over the workspace
 
 
 def test_binding_refuses_cpu_tensors(nv):

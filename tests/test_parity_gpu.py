@@ -240,6 +240,25 @@ def _weights(n, k, seed, *stream, std=0.02, outliers=0.01, mask=None):
     return oracle.quantize(W, mask=mask)
 
 
+@pytest.mark.parametrize("noise", [True, False], ids=["aqn", "plain"])
+@pytest.mark.parametrize("shape", [(1, 16), (3, 528), (64, 3584), (4096, 3584), (300, 4096), (8192, 5120)])
+def test_rmsnorm_quantize(nv, shape, noise):
+    """rmsnorm_aqn_quantize: y within the RMSNorm tolerance of the oracle, and codes, scales and g
+    exactly the oracle's quantization of that y (4096 x 3584 and 300 x 4096 take the fused
+    on-chip kernel, 8192 x 5120 the fallback)."""
+    M, H = shape
+    x = synth.heavy_tail_activation_bf16(M, H, 41, M) if M >= 64 else synth.activation_bf16(M, H, 41, M)
+    w = synth.aqn_weight(H, 41, 2)
+    eps = synth.aqn_eps(H, 41, 3) if noise else None
+    sig = np.float32(3e-3) if noise else np.float32(0.0)
+    y, c, sc, g = nv.rmsnorm_aqn_quantize(P.dev_bf16(x), P.dev(w), None if eps is None else P.dev(eps), sig, 1e-6)
+    torch.cuda.synchronize()
+    yb = P.host_bits(y)
+    P.assert_rmsnorm_close(yb, oracle.rmsnorm_aqn(x, w, eps, sig, 1e-6), f"{shape} y")
+    got = (c.cpu().numpy(), sc.cpu().numpy(), np.float32(g.cpu().numpy()[0]))
+    assert_quant_equal(got, oracle.quantize(yb), f"{shape} quantized y")
+
+
 def gpu_linear(nv, w4a4, x, q, A, B, s, offsets=None):
     codes, scales, g = q
     fn = nv.nvfp4_lora_linear_w4a4 if w4a4 else nv.nvfp4_lora_linear
