@@ -668,9 +668,11 @@ __global__ void __launch_bounds__(kFusedThreads, 2)
 
 // RMSNorm-AQN fused with the NVFP4 quantization of its output, for outputs that fit in shared
 // memory across the grid (one CTA per SM, launched cooperatively so that all CTAs are resident):
-//   phase 1  four warps per row, eight rows at a time: y = bf16((w + sigma eps) x /
+//   phase 1  every row of the CTA is requested at once (one bulk copy per row into its slot),
+//            then eight warps per row, four rows at a time (each thread keeps the noised
+//            weight of its own columns in registers for all its rows): y = bf16((w + sigma eps) x /
 //            sqrt(mean x^2 + delta)) as in
-//            rmsnorm_aqn_kernel, written to y and kept in this CTA's shared memory; the running
+//            rmsnorm_aqn_kernel, written to y and over the row's slot; the running
 //            max of |y| (bf16 patterns) is reduced per CTA and folded into sync[0];
 //   barrier  every CTA arrives on the counter sync[4] and waits (bounded) for all the others:
 //            then sync[0] holds amax over all of y, so g = amax / 2688 is known;
@@ -678,15 +680,15 @@ __global__ void __launch_bounds__(kFusedThreads, 2)
 //            (same blocks, tables and results as nvfp4_quantize of y).
 // y is read from HBM never: x in, y and the codes out. sync[0] and sync[4] start at zero.
 constexpr int kFuseThreads = 1024;
-constexpr int kFuseGroup = 128;  // threads per row (four warps)
-constexpr int kFuseVec = 4;      // 128-bit words of a row per thread: H <= 128 * 4 * 8 = 4096
+constexpr int kFuseGroup = 256;  // threads per row (eight warps)
+constexpr int kFuseVec = 2;      // 128-bit words of a row per thread: H <= 256 * 2 * 8 = 4096
 
 __global__ void __launch_bounds__(kFuseThreads, 1)
     rmsnorm_quant_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t H, const float* __restrict__ w,
                          const float* __restrict__ eps, float sigma, float delta, uint16_t* __restrict__ y,
                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ g_out,
                          uint32_t* __restrict__ sync, uint32_t* __restrict__ status) {
-  extern __shared__ __align__(16) uint8_t ysm[];  // row slot i: H bf16 values
+  extern __shared__ __align__(16) uint8_t ysm[];  // row slot i: H bf16 values; then one mbarrier per slot
   __shared__ EncodeTables tab;
   __shared__ float part[2][kFuseThreads / 32];    // per-warp sums of squares, by iteration parity
   __shared__ uint32_t red[kFuseThreads / 32];
@@ -696,20 +698,59 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
   const int grp = threadIdx.x / kFuseGroup, t = threadIdx.x % kFuseGroup;
   const int64_t G = gridDim.x, cta = blockIdx.x;
   const int nrows = cta < M ? static_cast<int>((M - 1 - cta) / G + 1) : 0;
+  const int rmax = static_cast<int>((M + G - 1) / G);
   const int nvec = static_cast<int>(H / 8);
+  const uint32_t row_bytes = static_cast<uint32_t>(H * 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ysm + static_cast<size_t>(rmax) * row_bytes);
+  for (int i = threadIdx.x; i < nrows; i += kFuseThreads) mbar_init(smem_addr(&bars[i]), 1);
+  fence_barrier_init();
+  __syncthreads();
+  // every row of this CTA is requested at once (one bulk copy per row, lane 0 of each warp
+  // issuing rows warp, warp + 32, ...), so the loads of all rows are in flight together
+  if (lane == 0) {
+    for (int i = warp; i < nrows; i += kFuseThreads / 32) {
+      mbar_arrive_expect_tx(smem_addr(&bars[i]), row_bytes);
+      bulk_load(smem_addr(ysm + static_cast<size_t>(i) * row_bytes), x + (cta + static_cast<int64_t>(i) * G) * H,
+                row_bytes, smem_addr(&bars[i]));
+    }
+  }
+  // the noised weight w + sigma eps of this thread's columns (the same in every row), as rmsnorm_aqn forms it
+  float wt[kFuseVec][8];
+#pragma unroll
+  for (int k = 0; k < kFuseVec; ++k) {
+    const int j = t + kFuseGroup * k;
+    if (j < nvec) {
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j);
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j + 1);
+      wt[k][0] = w0.x; wt[k][1] = w0.y; wt[k][2] = w0.z; wt[k][3] = w0.w;
+      wt[k][4] = w1.x; wt[k][5] = w1.y; wt[k][6] = w1.z; wt[k][7] = w1.w;
+      if (eps) {
+        const float4 e0 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j);
+        const float4 e1 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j + 1);
+        const float et[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wt[k][u] = fmaf(sigma, et[u], wt[k][u]);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) wt[k][u] = 0.0f;
+    }
+  }
   uint32_t am2 = 0;
-  // rows i = grp + kGroups * it of this CTA; all groups step together (block barriers)
-  for (int it = 0; it * kGroups < nrows; ++it) {
+  // rows i = grp + kGroups * it of this CTA, each group of eight warps on its own (named barrier 1 + grp)
+  for (int it = 0; grp + kGroups * it < nrows; ++it) {
     const int i = grp + kGroups * it;
-    const bool live = i < nrows;
     const int64_t row = cta + static_cast<int64_t>(i) * G;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? row : 0) * H);
+    uint4* ys = reinterpret_cast<uint4*>(ysm + static_cast<size_t>(i) * row_bytes);
+    // a timeout is recorded in the status word; the row is then processed as it stands, so that
+    // the grid barrier below is still reached by every CTA
+    mbar_wait(smem_addr(&bars[i]), 0u, status, kStatusTimeoutDequant);
     uint4 v[kFuseVec];
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < kFuseVec; ++k) {
       const int j = t + kFuseGroup * k;
-      v[k] = live && j < nvec ? ld_nc_v4(xr + j) : make_uint4(0, 0, 0, 0);
+      v[k] = j < nvec ? ys[j] : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int k = 0; k < kFuseVec; ++k) {
@@ -723,32 +764,23 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
     }
     ss = warp_sum(ss);
     if (lane == 0) part[it & 1][warp] = ss;
-    __syncthreads();
-    if (!live) continue;
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(kFuseGroup) : "memory");
     const float* pg = &part[it & 1][grp * (kFuseGroup / 32)];
-    const float r = rsqrtf((pg[0] + pg[1] + pg[2] + pg[3]) / static_cast<float>(H) + delta);
+    float sum = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kFuseGroup / 32; ++u) sum += pg[u];
+    const float r = rsqrtf(sum / static_cast<float>(H) + delta);
     uint4* yr = reinterpret_cast<uint4*>(y + row * H);
-    uint4* ys = reinterpret_cast<uint4*>(ysm + static_cast<size_t>(i) * H * 2);
 #pragma unroll
     for (int k = 0; k < kFuseVec; ++k) {
       const int j = t + kFuseGroup * k;
       if (j < nvec) {
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j);
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j + 1);
-        float wt[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        if (eps) {
-          const float4 e0 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j);
-          const float4 e1 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j + 1);
-          const float et[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-          for (int u = 0; u < 8; ++u) wt[u] = fmaf(sigma, et[u], wt[u]);
-        }
         const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
         uint32_t o[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float a = __uint_as_float(bf16_lo_bits(q[u])) * r * wt[2 * u];
-          const float b = __uint_as_float(bf16_hi_bits(q[u])) * r * wt[2 * u + 1];
+          const float a = __uint_as_float(bf16_lo_bits(q[u])) * r * wt[k][2 * u];
+          const float b = __uint_as_float(bf16_hi_bits(q[u])) * r * wt[k][2 * u + 1];
           o[u] = f32_to_bf16_bits(a) | (f32_to_bf16_bits(b) << 16);
           am2 = __vmaxu2(am2, o[u] & 0x7FFF7FFFu);
         }
@@ -981,22 +1013,39 @@ nvfp4rl_status launch_rmsnorm_quantize(const uint16_t* x, int64_t M, int64_t H, 
   // fused path: every CTA's rows of y fit in its shared memory, one CTA per SM
   const int64_t G = std::min<int64_t>(M, dev.sm_count);
   const int64_t rows_per_cta = (M + G - 1) / G;
-  const size_t smem = static_cast<size_t>(rows_per_cta) * H * 2;
+  const size_t smem = static_cast<size_t>(rows_per_cta) * (H * 2 + 8);
   if (H / 8 <= kFuseGroup * kFuseVec && smem + 8 * 1024 <= dev.smem_optin) {
+    // per device: the largest dynamic shared-memory size set so far, and whether one CTA of that
+    // size is resident per SM
+    struct FuseState {
+      size_t smem_set = 0;
+      bool resident = false;
+    };
     static std::mutex mu;
+    static std::map<int, FuseState> states;
     std::lock_guard<std::mutex> lock(mu);
-    int per_sm = 0;
-    if (cudaFuncSetAttribute(rmsnorm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
-            cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_quant_kernel, kFuseThreads, smem) == cudaSuccess &&
-        per_sm >= 1) {
+    FuseState& fs = states[dev.device];
+    if (smem > fs.smem_set) {
+      int per_sm = 0;
+      fs.resident = false;
+      if (cudaFuncSetAttribute(rmsnorm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_quant_kernel, kFuseThreads, smem) ==
+              cudaSuccess &&
+          per_sm >= 1) {
+        fs.smem_set = smem;
+        fs.resident = true;
+      }
+      cudaGetLastError();
+    }
+    if (fs.resident) {
       void* args[] = {const_cast<uint16_t**>(&x), &M, &H, const_cast<float**>(&w), const_cast<float**>(&eps), &sigma,
                       &delta, &y, &codes, &scales, &g, &sync, const_cast<uint32_t**>(&dev.status)};
       if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(rmsnorm_quant_kernel), dim3(static_cast<unsigned>(G)),
                                       dim3(kFuseThreads), args, smem, st) == cudaSuccess)
         return launch_status();
+      cudaGetLastError();  // fall back below
     }
-    cudaGetLastError();  // fall back below
   }
   // otherwise: RMSNorm-AQN, then the amax and the encoding of y (its words were cleared above)
   const nvfp4rl_status s1 = launch_rmsnorm_aqn(x, M, H, w, eps, sigma, delta, y, dev, st);

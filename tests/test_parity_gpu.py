@@ -245,16 +245,20 @@ def _weights(n, k, seed, *stream, std=0.02, outliers=0.01, mask=None):
 def test_rmsnorm_quantize(nv, shape, noise):
     """rmsnorm_aqn_quantize: y within the RMSNorm tolerance of the oracle, and codes, scales and g
     exactly the oracle's quantization of that y (4096 x 3584 and 300 x 4096 take the fused
-    on-chip kernel, 8192 x 5120 the fallback)."""
+    on-chip kernel, 8192 x 5120 the fallback). Both paths also give rmsnorm_aqn's y bit for bit
+    (same per-row partition and summation order)."""
     M, H = shape
     x = synth.heavy_tail_activation_bf16(M, H, 41, M) if M >= 64 else synth.activation_bf16(M, H, 41, M)
     w = synth.aqn_weight(H, 41, 2)
     eps = synth.aqn_eps(H, 41, 3) if noise else None
     sig = np.float32(3e-3) if noise else np.float32(0.0)
-    y, c, sc, g = nv.rmsnorm_aqn_quantize(P.dev_bf16(x), P.dev(w), None if eps is None else P.dev(eps), sig, 1e-6)
+    xd, wd, ed = P.dev_bf16(x), P.dev(w), None if eps is None else P.dev(eps)
+    y, c, sc, g = nv.rmsnorm_aqn_quantize(xd, wd, ed, sig, 1e-6)
+    y_alone = nv.rmsnorm_aqn(xd, wd, ed, sig, 1e-6)
     torch.cuda.synchronize()
     yb = P.host_bits(y)
     P.assert_rmsnorm_close(yb, oracle.rmsnorm_aqn(x, w, eps, sig, 1e-6), f"{shape} y")
+    assert np.array_equal(yb, P.host_bits(y_alone)), f"{shape}: y differs from rmsnorm_aqn"
     got = (c.cpu().numpy(), sc.cpu().numpy(), np.float32(g.cpu().numpy()[0]))
     assert_quant_equal(got, oracle.quantize(yb), f"{shape} quantized y")
 
