@@ -7,10 +7,18 @@
 // z = sigma * eps with eps standard-normal draws passed in and sigma from the
 // exponential schedule (section "AQNの仕組み").
 //
-// One CTA per row: the row (H bf16) is read once with 128-bit loads into registers,
-// the sum of squares is reduced with warp shuffles, and (w + sigma*eps) * x * r is
-// written as bf16. w + sigma*eps is formed in fp32: late in the schedule sigma is far
-// below a bf16 ulp of w, so a 16-bit weight would lose the noise.
+// Rows are spread over a grid of resident CTAs of 256 threads (row = cta, cta + G, ...). Each
+// thread owns the columns 8j .. 8j + 7 for j = thread, thread + 256, ... in every row, so it forms
+// w + sigma*eps of those columns once, in fp32 registers, for all its rows: late in the schedule
+// sigma is far below a bf16 ulp of w, so a 16-bit weight would lose the noise, and re-reading the
+// fp32 weight for every row would move four times the bytes of x through L2. A row (H bf16) is read
+// with 128-bit loads into registers, the next row's load is issued before this row's reduction,
+// the sum of squares is reduced with warp shuffles and then over the eight warps in order, and
+// (w + sigma*eps) * x * r is written as bf16.
+#include <algorithm>
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace nvfp4rl {
@@ -19,79 +27,135 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxVecPerThread = 4;  // H <= 4 * 8 * 256 = 8192 keeps the row in registers
 
-template <bool kNoise>
-__global__ void __launch_bounds__(kThreads) rmsnorm_aqn_kernel(const uint16_t* __restrict__ x, int64_t H,
+template <bool kNoise, int kVec>
+__global__ void __launch_bounds__(kThreads) rmsnorm_aqn_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t H,
                                                                const float* __restrict__ w,
                                                                const float* __restrict__ eps, float sigma,
                                                                float delta, uint16_t* __restrict__ y) {
-  griddep_wait();
+  __shared__ float red[2][kThreads / 32];  // per-warp sums of squares, by row parity
+  griddep_wait();  // the preceding kernel's writes (x, or even w or eps) are visible from here on
   griddep_launch_dependents();
-  const int64_t row = blockIdx.x;
   const int nvec = static_cast<int>(H / 8);
-  const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
-  uint4 v[kMaxVecPerThread];
-  float ss = 0.0f;
+  float wt[kVec][8];
 #pragma unroll
-  for (int i = 0; i < kMaxVecPerThread; ++i) {
+  for (int i = 0; i < kVec; ++i) {
     const int j = threadIdx.x + i * kThreads;
-    if (j < nvec) {
-      v[i] = ld_nc_v4(xr + j);
-      const uint32_t q[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float a = __uint_as_float(bf16_lo_bits(q[t])), b = __uint_as_float(bf16_hi_bits(q[t]));
-        ss = fmaf(a, a, ss);
-        ss = fmaf(b, b, ss);
-      }
-    }
-  }
-  ss = warp_sum(ss);
-  __shared__ float red[kThreads / 32];
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kThreads / 32; ++i) tot += red[i];
-  const float r = rsqrtf(tot / static_cast<float>(H) + delta);
-
-  uint4* yr = reinterpret_cast<uint4*>(y + row * H);
-#pragma unroll
-  for (int i = 0; i < kMaxVecPerThread; ++i) {
-    const int j = threadIdx.x + i * kThreads;
+    for (int t = 0; t < 8; ++t) wt[i][t] = 0.0f;
     if (j < nvec) {
       const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j);
       const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * j + 1);
-      float wt[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      wt[i][0] = w0.x; wt[i][1] = w0.y; wt[i][2] = w0.z; wt[i][3] = w0.w;
+      wt[i][4] = w1.x; wt[i][5] = w1.y; wt[i][6] = w1.z; wt[i][7] = w1.w;
       if (kNoise) {
         const float4 e0 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j);
         const float4 e1 = __ldg(reinterpret_cast<const float4*>(eps) + 2 * j + 1);
         const float et[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) wt[t] = fmaf(sigma, et[t], wt[t]);
+        for (int t = 0; t < 8; ++t) wt[i][t] = fmaf(sigma, et[t], wt[i][t]);
       }
-      const uint32_t q[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float a = __uint_as_float(bf16_lo_bits(q[t])) * r * wt[2 * t];
-        const float b = __uint_as_float(bf16_hi_bits(q[t])) * r * wt[2 * t + 1];
-        o[t] = f32_to_bf16_bits(a) | (f32_to_bf16_bits(b) << 16);
-      }
-      yr[j] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
+  const int64_t G = gridDim.x;
+  int64_t row = blockIdx.x;
+  uint4 v[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const int j = threadIdx.x + i * kThreads;
+    v[i] = row < M && j < nvec ? ld_nc_v4(reinterpret_cast<const uint4*>(x + row * H) + j) : make_uint4(0, 0, 0, 0);
+  }
+  for (int par = 0; row < M; row += G, par ^= 1) {
+    const int64_t next = row + G;
+    uint4 nx[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const int j = threadIdx.x + i * kThreads;
+      nx[i] = next < M && j < nvec ? ld_nc_v4(reinterpret_cast<const uint4*>(x + next * H) + j)
+                                   : make_uint4(0, 0, 0, 0);
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const int j = threadIdx.x + i * kThreads;
+      if (j < nvec) {
+        const uint32_t q[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float a = __uint_as_float(bf16_lo_bits(q[t])), b = __uint_as_float(bf16_hi_bits(q[t]));
+          ss = fmaf(a, a, ss);
+          ss = fmaf(b, b, ss);
+        }
+      }
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[par][threadIdx.x >> 5] = ss;
+    __syncthreads();  // red[par] is rewritten two rows later, after the next row's barrier
+    float tot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) tot += red[par][i];
+    const float r = rsqrtf(tot / static_cast<float>(H) + delta);
+    uint4* yr = reinterpret_cast<uint4*>(y + row * H);
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const int j = threadIdx.x + i * kThreads;
+      if (j < nvec) {
+        const uint32_t q[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float a = __uint_as_float(bf16_lo_bits(q[t])) * r * wt[i][2 * t];
+          const float b = __uint_as_float(bf16_hi_bits(q[t])) * r * wt[i][2 * t + 1];
+          o[t] = f32_to_bf16_bits(a) | (f32_to_bf16_bits(b) << 16);
+        }
+        yr[j] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      v[i] = nx[i];
+    }
+  }
+}
+
+// Resident CTAs per SM of one instance (occupancy query, once per device and instance).
+template <bool kNoise, int kVec>
+int resident_ctas(const DeviceInfo& dev) {
+  static std::mutex mu;
+  static std::map<int, int> per_dev;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = per_dev.find(dev.device);
+  if (it != per_dev.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_aqn_kernel<kNoise, kVec>, kThreads, 0) != cudaSuccess)
+    n = 0;
+  cudaGetLastError();
+  n = std::max(n, 1);
+  per_dev[dev.device] = n;
+  return n;
+}
+
+template <bool kNoise, int kVec>
+cudaError_t launch_rows(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps, float sigma,
+                        float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st) {
+  const int64_t G = std::min<int64_t>(M, static_cast<int64_t>(dev.sm_count) * resident_ctas<kNoise, kVec>(dev));
+  return launch_pdl(rmsnorm_aqn_kernel<kNoise, kVec>, dim3(static_cast<unsigned>(G)), dim3(kThreads), 0, st, x, M, H,
+                    w, eps, sigma, delta, y);
+}
+
+template <bool kNoise>
+cudaError_t launch_vec(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps, float sigma,
+                       float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st) {
+  const int64_t vec = (H / 8 + kThreads - 1) / kThreads;
+  if (vec <= 1) return launch_rows<kNoise, 1>(x, M, H, w, eps, sigma, delta, y, dev, st);
+  if (vec == 2) return launch_rows<kNoise, 2>(x, M, H, w, eps, sigma, delta, y, dev, st);
+  if (vec == 3) return launch_rows<kNoise, 3>(x, M, H, w, eps, sigma, delta, y, dev, st);
+  return launch_rows<kNoise, 4>(x, M, H, w, eps, sigma, delta, y, dev, st);
 }
 
 }  // namespace
 
 nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
-                                  float sigma, float delta, uint16_t* y, const DeviceInfo&, cudaStream_t st) {
+                                  float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st) {
   if (M == 0) return NVFP4RL_OK;
-  const cudaError_t e =
-      eps ? launch_pdl(rmsnorm_aqn_kernel<true>, dim3(static_cast<unsigned>(M)), dim3(kThreads), 0, st, x, H, w, eps,
-                       sigma, delta, y)
-          : launch_pdl(rmsnorm_aqn_kernel<false>, dim3(static_cast<unsigned>(M)), dim3(kThreads), 0, st, x, H, w, eps,
-                       sigma, delta, y);
+  const cudaError_t e = eps ? launch_vec<true>(x, M, H, w, eps, sigma, delta, y, dev, st)
+                            : launch_vec<false>(x, M, H, w, eps, sigma, delta, y, dev, st);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }
