@@ -56,6 +56,9 @@ def _declare(lib):
         "oracle_quantize_rows": (None, [p, i, i64, i64, i64, f, p, p]),
         "oracle_quantize_guided_rows": (None, [p, i, i64, i64, i64, f, p, p, p]),
         "oracle_dequantize_rows": (None, [p, p, f, i64, i64, i64, p]),
+        "oracle_quantize_record_rows": (None, [p, i, i64, i64, i64, f, p, p, p]),
+        "oracle_e2m1_round_up": (i, [d, d]),
+        "oracle_quantize_cached_rows": (None, [p, i, i64, i64, i64, f, p, p, p]),
         "oracle_aqn_sigma": (d, [d, d, i64, i64]),
         "oracle_rmsnorm_aqn_rows": (None, [p, i64, i64, i64, p, p, f, f, p]),
         "oracle_lora_down": (None, [p, i64, i64, p, i32, p]),
@@ -169,6 +172,60 @@ def quantize(x: np.ndarray, mask: np.ndarray | None = None, amax_in: float | Non
                                                           _ptr(codes), _ptr(scales))
     _parallel(fn, rows, nthreads)
     return codes, scales, g
+
+
+def e2m1_round_up(x: float, S: float, L=None) -> int:
+    return (L or lib()).oracle_e2m1_round_up(float(x), float(S))
+
+
+def _rows_per_part(rows: int, cols: int, nthreads):
+    """Row split whose part boundaries fall on 32-element mask words (each part owns whole words)."""
+    step = 32 // np.gcd(cols, 32)
+    parts = _split((rows + step - 1) // step, nthreads or threads())
+    return [(a * step, min(rows, b * step)) for a, b in parts]
+
+
+def quantize_record(x: np.ndarray, amax_in: float | None = None, L=None, nthreads=None):
+    """Plain NVFP4 encoding plus the record of its rounding directions (TRACE rollout side):
+    (codes, scales, g, mask) with mask bit i%32 of word i/32 set when element i was rounded up in
+    magnitude."""
+    L = L or lib()
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    dt = _dtype_code(x)
+    a = amax(x, L, nthreads) if amax_in is None else np.float32(amax_in)
+    g = global_scale(a, L)
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 16), np.uint8)
+    mask = np.zeros((rows * cols + 31) // 32, np.uint32)
+    chunks = _rows_per_part(rows, cols, nthreads)
+    fn = lambda r0, r1: L.oracle_quantize_record_rows(_ptr(x), dt, cols, r0, r1, float(g), _ptr(codes),
+                                                      _ptr(scales), _ptr(mask))
+    if len(chunks) <= 1:
+        for r0, r1 in chunks:
+            fn(r0, r1)
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            list(ex.map(lambda ab: fn(*ab), chunks))
+    return codes, scales, g, mask
+
+
+def quantize_cached(x: np.ndarray, mask: np.ndarray, scales: np.ndarray, g: float, L=None, nthreads=None):
+    """Codes of x from a TRACE cache: the recorded scale bytes and g, rounding directions from mask."""
+    L = L or lib()
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    dt = _dtype_code(x)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    mask = np.ascontiguousarray(mask, dtype=np.uint32)
+    assert scales.size == rows * cols // 16 and mask.size * 32 >= rows * cols
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    fn = lambda r0, r1: L.oracle_quantize_cached_rows(_ptr(x), dt, cols, r0, r1, float(np.float32(g)),
+                                                      _ptr(scales), _ptr(mask), _ptr(codes))
+    _parallel(fn, rows, nthreads)
+    return codes
 
 
 def quantize_rows_given_g(x: np.ndarray, g: float, rows, mask: np.ndarray | None = None, L=None):

@@ -36,6 +36,16 @@
 //  * Guided rounding: with a = |x| / (dec(s) g): a >= 6 gives 6; an exact grid
 //    point is kept; otherwise mask bit 1 takes the larger-magnitude neighbour and
 //    bit 0 the smaller one. The scale byte is the plain one.
+//  * Recording (the rollout side of TRACE, section "仕組みの工学的な理解": the
+//    rollout engine quantizes and keeps a record of the result, which the training
+//    side later consults to take the same rounding decisions): the record bit of an
+//    element is 1 when the plain code's magnitude exceeds |x| / S (the value was
+//    rounded up in magnitude) and 0 otherwise (rounded down, on the grid, saturated,
+//    or a zero scale). Guided rounding with that mask gives the plain codes back.
+//  * Replay from the cache (section "TRACE の中心的なアイデア": the scale information
+//    is kept with the rounding bits): codes are the guided codes against the recorded
+//    scale byte and g, with no amax and no scale search. A recorded byte above 0x7E
+//    (the quantizer never writes one) is read as 0x7E; g <= 0 or NaN gives sign|0.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -98,6 +108,14 @@ int e2m1_encode_guided(double x, double S, int up) {
   return sign | (up ? k + 1 : k);
 }
 
+// Record bit of x under the real scale S: 1 when the plain code rounds |x| / S up
+// in magnitude.
+int e2m1_round_up(double x, double S) {
+  if (S == 0.0) return 0;
+  const int c = e2m1_encode(x, S);
+  return kGrid[c & 7] * S > std::fabs(x) ? 1 : 0;
+}
+
 double load_elem(const void* x, int dtype, int64_t i) {
   if (dtype == 0) {  // bf16 bit pattern
     const uint32_t u = static_cast<uint32_t>(static_cast<const uint16_t*>(x)[i]) << 16;
@@ -116,7 +134,7 @@ double bf16_value(uint16_t b) {
 }
 
 void quantize_rows(const void* x, int dtype, int64_t cols, int64_t row0, int64_t row1, float g,
-                   const uint32_t* mask, uint8_t* codes, uint8_t* scales) {
+                   const uint32_t* mask, uint8_t* codes, uint8_t* scales, uint32_t* record = nullptr) {
   const int64_t nblk = cols / 16;
   for (int64_t r = row0; r < row1; ++r) {
     for (int64_t b = 0; b < nblk; ++b) {
@@ -135,6 +153,10 @@ void quantize_rows(const void* x, int dtype, int64_t cols, int64_t row0, int64_t
           c = e2m1_encode_guided(v, S, up);
         } else {
           c = e2m1_encode(v, S);
+        }
+        if (record) {
+          const uint32_t bit = static_cast<uint32_t>(e2m1_round_up(v, S)) << (idx % 32);
+          record[idx / 32] = (record[idx / 32] & ~(1u << (idx % 32))) | bit;
         }
         uint8_t& byte = codes[idx / 2];
         if ((idx & 1) == 0) byte = static_cast<uint8_t>((byte & 0xF0) | c);
@@ -177,6 +199,35 @@ void oracle_quantize_rows(const void* x, int dtype, int64_t cols, int64_t row0, 
 void oracle_quantize_guided_rows(const void* x, int dtype, int64_t cols, int64_t row0, int64_t row1,
                                  float g, const uint32_t* mask, uint8_t* codes, uint8_t* scales) {
   quantize_rows(x, dtype, cols, row0, row1, g, mask, codes, scales);
+}
+
+// Plain encoding of rows [row0, row1) as oracle_quantize_rows, and the record bit of every
+// element written to bit (i % 32) of record[i / 32], i the flat row-major index.
+void oracle_quantize_record_rows(const void* x, int dtype, int64_t cols, int64_t row0, int64_t row1, float g,
+                                 uint8_t* codes, uint8_t* scales, uint32_t* record) {
+  quantize_rows(x, dtype, cols, row0, row1, g, nullptr, codes, scales, record);
+}
+
+int oracle_e2m1_round_up(double x, double S) { return e2m1_round_up(x, S); }
+
+// Codes of rows [row0, row1) from a cache: scale byte scales[r * cols/16 + b] and g as
+// recorded, rounding direction from the mask (same layout as the guided encoding).
+void oracle_quantize_cached_rows(const void* x, int dtype, int64_t cols, int64_t row0, int64_t row1, float g,
+                                 const uint8_t* scales, const uint32_t* mask, uint8_t* codes) {
+  const int64_t nblk = cols / 16;
+  for (int64_t r = row0; r < row1; ++r)
+    for (int64_t b = 0; b < nblk; ++b) {
+      const int s = scales[r * nblk + b] > 0x7E ? 0x7E : scales[r * nblk + b];
+      const double S = (g > 0.0f) ? e4m3_value(s) * static_cast<double>(g) : 0.0;
+      for (int i = 0; i < 16; ++i) {
+        const int64_t idx = r * cols + b * 16 + i;
+        const int up = (mask[idx / 32] >> (idx % 32)) & 1;
+        const int c = e2m1_encode_guided(load_elem(x, dtype, idx), S, up);
+        uint8_t& byte = codes[idx / 2];
+        if ((idx & 1) == 0) byte = static_cast<uint8_t>((byte & 0xF0) | c);
+        else byte = static_cast<uint8_t>((byte & 0x0F) | (c << 4));
+      }
+    }
 }
 
 // deq(code, s, g) = e2m1(code) * e4m3(s) * g, exact in double; rows [row0, row1).

@@ -40,6 +40,13 @@ MUTANTS = {
     "lora_B_transposed": ("U[m * r + j] * bf16_value(B[n * r + j])", "U[m * r + j] * bf16_value(B[(j * 5 + n) % 10])"),
     "dequant_block_index": ("scales[n * (K / 16) + k / 16]", "scales[n * (K / 16) + (k / 16 + 1) % (K / 16)]"),
     "gemm_operand_transposed": ("acc += xq[m * K + k] * wrow[k];", "acc += xq[m * K + k] * wrow[K - 1 - k];"),
+    "record_bit_inverted": ("return kGrid[c & 7] * S > std::fabs(x) ? 1 : 0;", "return kGrid[c & 7] * S > std::fabs(x) ? 0 : 1;"),
+    "record_grid_points_up": ("return kGrid[c & 7] * S > std::fabs(x) ? 1 : 0;", "return kGrid[c & 7] * S >= std::fabs(x) ? 1 : 0;"),
+    "cached_scale_of_next_block": ("scales[r * nblk + b] > 0x7E ? 0x7E : scales[r * nblk + b]",
+                                   "scales[r * nblk + (b + 1) % nblk] > 0x7E ? 0x7E : scales[r * nblk + (b + 1) % nblk]"),
+    "cached_g_dropped": ("(g > 0.0f) ? e4m3_value(s) * static_cast<double>(g) : 0.0", "(g > 0.0f) ? e4m3_value(s) : 0.0"),
+    "cached_mask_shifted": ("        const int up = (mask[idx / 32] >> (idx % 32)) & 1;\n        const int c = e2m1_encode_guided(load_elem",
+                            "        const int up = (mask[idx / 32] >> ((idx + 1) % 32)) & 1;\n        const int c = e2m1_encode_guided(load_elem"),
 }
 
 
@@ -122,6 +129,26 @@ def _battery(L):
                          eps=float(np.float32(1e-2))).numpy()
         return np.allclose(y, ref, rtol=1e-6, atol=1e-9)
     check("rmsnorm", rmsnorm)
+
+    def record_hand():
+        from tests.test_oracle_trace import HAND_ROWS, HAND_UP
+        _, _, _, m = oracle.quantize_record(np.array(HAND_ROWS, np.float32), amax_in=2688.0, L=L)
+        return np.unpackbits(m.view(np.uint8), bitorder="little")[:32].tolist() == HAND_UP
+    check("record_hand", record_hand)
+
+    def record_exact():
+        x = synth.weight_f32(8, 64, 0.02, 3, 7, outlier_frac=0.05)
+        c, s, g, m = oracle.quantize_record(x, L=L)
+        up = np.abs(ex.dequant_torch(c, s, g)) > np.abs(x.astype(np.float64))
+        return np.array_equal(np.unpackbits(m.view(np.uint8), bitorder="little")[: x.size].astype(bool),
+                              up.reshape(-1))
+    check("record_exact", record_exact)
+
+    def cached_roundtrip():
+        x = synth.weight_f32(6, 64, 0.02, 4, 7, outlier_frac=0.05)
+        c, s, g, m = oracle.quantize_record(x, L=L)
+        return np.array_equal(oracle.quantize_cached(x, m, s, g, L=L), c)
+    check("cached_roundtrip", cached_roundtrip)
 
     def linear():
         N, K, M, r = 5, 64, 3, 2
