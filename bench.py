@@ -640,7 +640,17 @@ def run_suite(args):
         us_p = timed(lambda: nv.nvfp4_quantize(W, codes=c, scales=sc, g=g, workspace=wsq), 10)
         emit("quantize_plain_7b_gate", us_p, 0, n * k * (2 + 0.5625), "hbm",
              {"shape": [n, k], "note": "amax + plain encode, same weight"})
-        del W, mask, c, sc, g
+        rec = torch.empty((n * k + 31) // 32, dtype=torch.int32, device=dev)
+        us_r = timed(lambda: nv.nvfp4_quantize_record(W, codes=c, scales=sc, g=g, record=rec, workspace=wsq), 10)
+        emit("quantize_record_7b_gate", us_r, 0, n * k * (2 + 0.5625 + 0.125), "hbm",
+             {"shape": [n, k], "note": "TRACE rollout side: amax + plain encode + the rounding-direction record; "
+                                       "bytes: 2 B in, 0.5625 B out, 0.125 B of record per element"})
+        c2 = torch.empty_like(c)
+        us_c = timed(lambda: nv.nvfp4_quantize_cached(W, rec, sc, g, codes=c2), 10)
+        emit("quantize_cached_7b_gate", us_c, 0, n * k * (2 + 0.125 + 0.0625 + 0.5), "hbm",
+             {"shape": [n, k], "note": "TRACE training side: one pass from the cached record, scales and g; "
+                                       "bytes: 2 B in, 0.125 B record + 0.0625 B scales in, 0.5 B codes out"})
+        del W, mask, c, sc, g, rec, c2
         torch.cuda.empty_cache()
     # ---- RMSNorm-AQN fused with the NVFP4 quantization of its output (the W4A4 activation operand)
     if want("rmsnorm_quantize"):

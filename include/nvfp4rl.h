@@ -151,6 +151,45 @@ NVFP4RL_API nvfp4rl_status nvfp4_quantize_guided(const void* x, int32_t dtype, i
                                      void* stream);
 
 /*
+ * nvfp4_quantize_record -- nvfp4_quantize that also records the direction of every
+ *   rounding: the rollout side of TRACE (TRACE summary, "仕組みの工学的な理解": the rollout
+ *   engine quantizes and keeps a record of the result, which the training side consults to
+ *   round the same way).
+ * Codes, scales and g are exactly those of nvfp4_quantize. In addition:
+ *   record   out, [ceil(rows*cols/32)] uint32 words, 16-byte aligned; element i (flat row-major
+ *            index) sets bit (i % 32) of word i / 32 to 1 when its plain code's magnitude exceeds
+ *            |x| / (E4M3(s_b) g) (rounded up in magnitude), else 0 (rounded down, on the grid,
+ *            saturated at 6, or a zero scale). The call writes the first rows*cols/8 bytes: when
+ *            rows*cols/16 is odd the upper 16 bits of the last word are left as they were.
+ *   nvfp4_quantize_guided(x, mask = record) then gives these codes again, and so does
+ *   nvfp4_quantize_cached(x, record, scales, g).
+ * Other arguments, workspace and errors as nvfp4_quantize; record may overlap nothing else.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_quantize_record(const void* x, int32_t dtype, int64_t rows, int64_t cols,
+                                                 uint8_t* codes, uint8_t* scales, float* g, uint32_t* record,
+                                                 const float* amax_in, void* workspace, size_t workspace_bytes,
+                                                 void* stream);
+
+/*
+ * nvfp4_quantize_cached -- the training side of TRACE: codes of x rounded as a cache says
+ *   (TRACE summary, "TRACE の中心的なアイデア": rounding decisions guided by the rollout's cached
+ *   mantissa and scale information), in one pass over x: no amax, no scale search.
+ *   codes[i] = guided code of x[i] (nvfp4_quantize_guided's rule) for the real scale
+ *   E4M3(s_b) g with s_b = scales[block of i] and g = *g as given; a byte above 0x7E (never
+ *   written by the quantizer) is read as 0x7E, and g <= 0 or NaN gives sign|0 everywhere.
+ *   x        [rows][cols] bf16 bits or fp32 (dtype), 16-byte aligned; cols multiple of 16.
+ *   mask     [ceil(rows*cols/32)] uint32 words (record layout), 16-byte aligned.
+ *   scales   [rows][cols/16] E4M3 bytes, 16-byte aligned (e.g. from nvfp4_quantize_record).
+ *   g        device fp32 (e.g. from nvfp4_quantize_record), 4-byte aligned.
+ *   codes    out, [rows][cols/2] bytes, 16-byte aligned; may overlap no input.
+ * No workspace. Errors: NVFP4RL_ERR_INVALID_ARG (bad dtype, negative rows, NULL pointer),
+ *   NVFP4RL_ERR_UNSUPPORTED_SHAPE (cols % 16), NVFP4RL_ERR_MISALIGNED, NVFP4RL_ERR_ALIAS.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_quantize_cached(const void* x, int32_t dtype, int64_t rows, int64_t cols,
+                                                 const uint32_t* mask, const uint8_t* scales, const float* g,
+                                                 uint8_t* codes, void* stream);
+
+/*
  * aqn_sigma -- AQN exponential noise schedule (QeRL explainer, "AQNの仕組み":
  *   large noise early, small noise late): sigma_k = sigma0 * (sigmaK/sigma0)^(k/K),
  *   k = 0..K. Host function, no device work. Returns NaN for K <= 0 or

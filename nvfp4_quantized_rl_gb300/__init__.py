@@ -8,7 +8,7 @@ importing the binding does not build it, and every call fails loudly when the
 library or a GPU is missing -- there is no CPU fallback.
 
 Functions carry the C names: nvfp4_amax, nvfp4_quantize, nvfp4_quantize_guided,
-nvfp4_quantize_batch, aqn_sigma, rmsnorm_aqn, rmsnorm_aqn_quantize, nvfp4_lora_linear,
+nvfp4_quantize_record, nvfp4_quantize_cached, nvfp4_quantize_batch, aqn_sigma, rmsnorm_aqn, rmsnorm_aqn_quantize, nvfp4_lora_linear,
 nvfp4_lora_linear_w4a4.
 """
 from __future__ import annotations
@@ -39,6 +39,8 @@ def _signatures():
         "nvfp4_amax": (c.c_int, [p, i32, i64, p, p]),
         "nvfp4_quantize": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, sz, p]),
         "nvfp4_quantize_guided": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
+        "nvfp4_quantize_record": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
+        "nvfp4_quantize_cached": (c.c_int, [p, i32, i64, i64, p, p, p, p, p]),
         "nvfp4_quantize_batch": (c.c_int, [i32, p, p, p, i32, p, p, p, p, sz, p]),
         "aqn_sigma": (f64, [f64, f64, i64, i64]),
         "rmsnorm_aqn": (c.c_int, [p, i64, i64, p, p, f32, f32, p, p]),
@@ -163,6 +165,35 @@ def nvfp4_quantize_guided(x, mask, amax_in=None, codes=None, scales=None, g=None
     return _quantize(x, mask, amax_in, codes, scales, g, workspace, stream)
 
 
+def nvfp4_quantize_record(x, amax_in=None, codes=None, scales=None, g=None, record=None, workspace=None,
+                          stream=None):
+    """nvfp4_quantize plus the record of its rounding directions -> (codes, scales, g, record int32
+    [ceil(R*C/32)]): bit i%32 of word i//32 is 1 where element i was rounded up in magnitude."""
+    import torch
+    rows, cols = x.shape if x.dim() == 2 else (0, 0)
+    record = _empty(((rows * cols + 31) // 32,), torch.int32, x.device) if record is None else record
+    codes, scales, g = _quantize(x, None, amax_in, codes, scales, g, workspace, stream, record=record)
+    return codes, scales, g, record
+
+
+def nvfp4_quantize_cached(x, mask, scales, g, codes=None, stream=None):
+    """Codes of x from a cache: the given scale bytes and g (CUDA tensors) with the rounding
+    directions of mask, in one pass -> codes u8 [R, C/2]."""
+    import torch
+    _require_cuda(x, mask, scales, g)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    dt = {torch.bfloat16: BF16, torch.float32: F32}.get(x.dtype)
+    if dt is None:
+        raise TypeError("x must be bf16 or fp32")
+    rows, cols = x.shape
+    codes = _empty((rows, cols // 2), torch.uint8, x.device) if codes is None else codes
+    st = lib().nvfp4_quantize_cached(_ptr(x), dt, rows, cols, _ptr(mask), _ptr(scales), _ptr(g), _ptr(codes),
+                                     _stream(x, stream))
+    _check(st, "nvfp4_quantize_cached")
+    return codes
+
+
 def nvfp4_quantize_batch(xs, codes=None, scales=None, g=None, workspace=None, stream=None):
     """NVFP4 quantization of a list of contiguous 2-D CUDA tensors of one dtype (bf16 or fp32) in one
     call, each with its own g -> (codes list, scales list, g list); outputs may be given as lists."""
@@ -194,9 +225,9 @@ def nvfp4_quantize_batch(xs, codes=None, scales=None, g=None, workspace=None, st
     return codes, scales, g
 
 
-def _quantize(x, mask, amax_in, codes, scales, g, workspace, stream):
+def _quantize(x, mask, amax_in, codes, scales, g, workspace, stream, record=None):
     import torch
-    _require_cuda(x, mask, amax_in)
+    _require_cuda(x, mask, amax_in, record)
     if x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D tensor")
     if x.dtype == torch.bfloat16:
@@ -214,7 +245,11 @@ def _quantize(x, mask, amax_in, codes, scales, g, workspace, stream):
         workspace = _empty((workspace_bytes(OP_QUANTIZE, 0, 0, 0),), torch.uint8, dev)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     L = lib()
-    if mask is None:
+    if record is not None:
+        st = L.nvfp4_quantize_record(_ptr(x), dt, rows, cols, _ptr(codes), _ptr(scales), _ptr(g), _ptr(record),
+                                     _ptr(amax_in), _ptr(workspace), wsb, _stream(x, stream))
+        _check(st, "nvfp4_quantize_record")
+    elif mask is None:
         st = L.nvfp4_quantize(_ptr(x), dt, rows, cols, _ptr(codes), _ptr(scales), _ptr(g), _ptr(amax_in),
                               _ptr(workspace), wsb, _stream(x, stream))
         _check(st, "nvfp4_quantize")

@@ -69,16 +69,19 @@ using namespace nvfp4rl;
 
 namespace {
 
+// record (nvfp4_quantize_record only): the rounding-direction bits, one per element.
 nvfp4rl_status quantize_common(const void* x, int32_t dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                bool guided, uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
-                               void* ws, size_t ws_bytes, void* stream) {
+                               void* ws, size_t ws_bytes, void* stream, uint32_t* record = nullptr,
+                               bool recording = false) {
   if (dtype != NVFP4RL_BF16 && dtype != NVFP4RL_F32) return NVFP4RL_ERR_INVALID_ARG;
   if (rows < 0 || cols <= 0) return NVFP4RL_ERR_INVALID_ARG;
   if (cols % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   if (rows == 0) return NVFP4RL_OK;  // empty tensor: nothing to read or write (g is left as is)
-  if (!x || !codes || !scales || !g || (guided && !mask)) return NVFP4RL_ERR_INVALID_ARG;
+  if (!x || !codes || !scales || !g || (guided && !mask) || (recording && !record)) return NVFP4RL_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (mask && !aligned16(mask)) ||
-      (reinterpret_cast<uintptr_t>(g) & 3u) || (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)))
+      (record && !aligned16(record)) || (reinterpret_cast<uintptr_t>(g) & 3u) ||
+      (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)))
     return NVFP4RL_ERR_MISALIGNED;
   if (!amax_in) {
     if (!ws || ws_bytes < kQuantizeWorkspace) return NVFP4RL_ERR_WORKSPACE;
@@ -87,20 +90,22 @@ nvfp4rl_status quantize_common(const void* x, int32_t dtype, int64_t rows, int64
   const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
   const size_t xbytes = n * (dtype == NVFP4RL_BF16 ? 2 : 4);
   const size_t mbytes = guided ? (n + 31) / 32 * 4 : 0;
-  const void* outs[3] = {codes, scales, g};
-  const size_t osz[3] = {n / 2, n / 16, 4};
-  for (int i = 0; i < 3; ++i) {
+  const int nouts = recording ? 4 : 3;
+  const void* outs[4] = {codes, scales, g, record};
+  const size_t osz[4] = {n / 2, n / 16, 4, n / 8};  // the record: 16 bits per block
+  for (int i = 0; i < nouts; ++i) {
     if (overlap(outs[i], osz[i], x, xbytes) || (guided && overlap(outs[i], osz[i], mask, mbytes)) ||
         (amax_in && overlap(outs[i], osz[i], amax_in, 4)) || (!amax_in && overlap(outs[i], osz[i], ws, kQuantizeWorkspace)))
       return NVFP4RL_ERR_ALIAS;
-    for (int j = i + 1; j < 3; ++j)
+    for (int j = i + 1; j < nouts; ++j)
       if (overlap(outs[i], osz[i], outs[j], osz[j])) return NVFP4RL_ERR_ALIAS;
   }
   DeviceInfo dev;
   nvfp4rl_status st = current_device(&dev);
   if (st != NVFP4RL_OK) return st;
   return launch_quantize(x, dtype, rows, cols, guided ? mask : nullptr, codes, scales, g, amax_in,
-                         static_cast<uint32_t*>(ws), dev, static_cast<cudaStream_t>(stream));
+                         static_cast<uint32_t*>(ws), dev, static_cast<cudaStream_t>(stream), false,
+                         recording ? record : nullptr);
 }
 
 // True when any two of the [begin, end) ranges overlap (n log n).
@@ -185,6 +190,33 @@ nvfp4rl_status nvfp4_quantize_guided(const void* x, int32_t dtype, int64_t rows,
                                      void* stream) {
   return quantize_common(x, dtype, rows, cols, mask, true, codes, scales, g, amax_in, workspace, workspace_bytes,
                          stream);
+}
+
+nvfp4rl_status nvfp4_quantize_record(const void* x, int32_t dtype, int64_t rows, int64_t cols, uint8_t* codes,
+                                     uint8_t* scales, float* g, uint32_t* record, const float* amax_in,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  return quantize_common(x, dtype, rows, cols, nullptr, false, codes, scales, g, amax_in, workspace, workspace_bytes,
+                         stream, record, true);
+}
+
+nvfp4rl_status nvfp4_quantize_cached(const void* x, int32_t dtype, int64_t rows, int64_t cols, const uint32_t* mask,
+                                     const uint8_t* scales, const float* g, uint8_t* codes, void* stream) {
+  if (dtype != NVFP4RL_BF16 && dtype != NVFP4RL_F32) return NVFP4RL_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0) return NVFP4RL_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return NVFP4RL_OK;
+  if (!x || !mask || !scales || !g || !codes) return NVFP4RL_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(mask) || !aligned16(scales) || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u))
+    return NVFP4RL_ERR_MISALIGNED;
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
+  if (overlap(codes, n / 2, x, n * (dtype == NVFP4RL_BF16 ? 2 : 4)) || overlap(codes, n / 2, mask, (n + 31) / 32 * 4) ||
+      overlap(codes, n / 2, scales, n / 16) || overlap(codes, n / 2, g, 4))
+    return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_quantize_cached(x, dtype, rows, cols, mask, scales, g, codes, dev, static_cast<cudaStream_t>(stream));
 }
 
 nvfp4rl_status nvfp4_quantize_batch(int32_t count, const void* const* x, const int64_t* rows, const int64_t* cols,

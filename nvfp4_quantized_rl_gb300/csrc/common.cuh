@@ -129,9 +129,17 @@ nvfp4rl_status launch_quantize_batch(int count, const void* const* x, const int6
                                      uint32_t* amax_words, const DeviceInfo& dev, cudaStream_t st);
 
 // amax_done: *amax_scratch already holds the tensor's amax bits (no amax pass is launched).
+// record (non-NULL only without mask): the plain encoding also writes its rounding directions,
+// 16 bits per 16-element block.
 nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
-                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done = false);
+                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done = false,
+                               uint32_t* record = nullptr);
+
+// Guided codes of x against the given scale bytes and g (device), in one pass (quantize.cu).
+nvfp4rl_status launch_quantize_cached(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
+                                      const uint8_t* scales, const float* g, uint8_t* codes, const DeviceInfo& dev,
+                                      cudaStream_t st);
 
 nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
                                   float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st);

@@ -88,6 +88,14 @@ __device__ __forceinline__ void guided_thresholds(float dec, float g, uint32_t g
   }
 }
 
+// Encodings of quantize_kernel.
+enum : int {
+  kModePlain = 0,   // nvfp4_quantize
+  kModeGuided = 1,  // nvfp4_quantize_guided: rounding directions from a mask
+  kModeRecord = 2,  // nvfp4_quantize_record: plain, and the record of its rounding directions
+  kModeCached = 3,  // nvfp4_quantize_cached: guided, against given scale bytes and g
+};
+
 // Two 16-bit maxima of |bf16| bit patterns over the eight values of a 128-bit word (the sign
 // bits are cleared before the unsigned compares).
 __device__ __forceinline__ uint32_t max4_abs_bf16(uint4 v) {
@@ -387,14 +395,15 @@ __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t b
   scales[blk] = static_cast<uint8_t>(b);
 }
 
-// Guided encoding of one block of bf16 values (finite), two elements per instruction: c_ge and
-// c_gt count the grid points below-or-at and strictly below |x| (bf16x2 compares against the
-// tables), x is on the grid when they differ or x = 0, and the magnitude is c_ge, plus one when
-// the element's mask bit is set, x is off the grid and c_ge < 7. The scale byte is the plain one.
-__device__ __forceinline__ void encode_block_bf16_guided(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
+// Plain encoding of one block of bf16 values, as encode_block_bf16, and the record of its rounding
+// directions: with c_ge the number of grid points at or below |x| (the guided tables' >=
+// thresholds), the plain magnitude is c_ge or c_ge + 1, and the element's bit is their difference
+// (1: rounded up in magnitude). Bit i of record16[blk] belongs to element i of the block.
+__device__ __forceinline__ void encode_block_bf16_record(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
                                                          float est_scale, const EncodeTables& tab,
-                                                         const GuidedTables& gtab, const uint32_t* __restrict__ mask,
-                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+                                                         const GuidedTables& gtab, uint8_t* __restrict__ codes,
+                                                         uint8_t* __restrict__ scales,
+                                                         uint16_t* __restrict__ record16) {
   const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
   uint32_t aw[8];
   uint32_t m2 = 0;
@@ -406,6 +415,59 @@ __device__ __forceinline__ void encode_block_bf16_guided(const uint4 (&v)[2], in
   const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
   uint32_t b = 0;
   if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, tab);
+  const uint4 ta = tab.thr[b][0], tb = tab.thr[b][1], ea = gtab.ge[b][0], eb = gtab.ge[b][1];
+  const uint32_t T2[7] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z};
+  const uint32_t GE[7] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z};
+  uint32_t byte[8];
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t acc = 0x43004300u, ce = 0x43004300u;  // bf16x2 (128, 128): the counts land in bits 0-2
+#pragma unroll
+    for (int k = 0; k < 7; ++k) {
+      acc = bf16x2_add(acc, bf16x2_gt(aw[i], T2[k]));
+      ce = bf16x2_add(ce, bf16x2_gt(aw[i], GE[k]));
+    }
+    const uint32_t m = acc & 0x00070007u;
+    const uint32_t d = (m - (ce & 0x00070007u)) & 0x00010001u;  // per half m >= c_ge: no borrow
+    bits |= ((d & 1u) | ((d >> 15) & 2u)) << (2 * i);
+    const uint32_t s = w[i] & 0x80008000u;
+    byte[i] = m | (m >> 12) | (s >> 12) | (s >> 24);
+  }
+  const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
+  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo, hi);
+  scales[blk] = static_cast<uint8_t>(b);
+  record16[blk] = static_cast<uint16_t>(bits);
+}
+
+// Guided encoding of one block of bf16 values (finite), two elements per instruction: c_ge and
+// c_gt count the grid points below-or-at and strictly below |x| (bf16x2 compares against the
+// tables), x is on the grid when they differ or x = 0, and the magnitude is c_ge, plus one when
+// the element's mask bit is set, x is off the grid and c_ge < 7. The scale byte is the plain one,
+// or, with kGivenScale, scales_in[blk] (above 0x7E read as 0x7E; 0 when g is not positive), and
+// then no scale byte is written.
+template <bool kGivenScale>
+__device__ __forceinline__ void encode_block_bf16_guided(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
+                                                         float est_scale, const EncodeTables* tab,
+                                                         const GuidedTables& gtab, const uint32_t* __restrict__ mask,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                         const uint8_t* __restrict__ scales_in) {
+  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+  uint32_t aw[8];
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    aw[i] = w[i] & 0x7FFF7FFFu;
+    m2 = __vmaxu2(m2, aw[i]);
+  }
+  uint32_t b = 0;
+  if (kGivenScale) {
+    if (g > 0.0f) b = min(static_cast<uint32_t>(scales_in[blk]), 0x7Eu);
+  } else {
+    const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+    if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, *tab);
+  }
   const uint4 ea = gtab.ge[b][0], eb = gtab.ge[b][1], ua = gtab.gt[b][0], ub = gtab.gt[b][1];
   const uint32_t GE[7] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z};
   const uint32_t GT[7] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z};
@@ -433,14 +495,19 @@ __device__ __forceinline__ void encode_block_bf16_guided(const uint4 (&v)[2], in
   const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
   const uint32_t hi = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
   *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo, hi);
-  scales[blk] = static_cast<uint8_t>(b);
+  if (!kGivenScale) scales[blk] = static_cast<uint8_t>(b);
 }
 
-// Scale byte and codes of one block, written to scales[blk] and codes[8 blk .. 8 blk + 7].
-template <int kDtype, bool kGuided>
+// Scale byte and codes of one block, written to scales[blk] and codes[8 blk .. 8 blk + 7], with
+// exact integer compares of fp32 bit patterns against per-block thresholds. kModeRecord also writes
+// the block's 16 rounding-direction bits to record16[blk]; kModeCached takes the scale byte from
+// scales_in[blk] (above 0x7E read as 0x7E; 0 when g is not positive) and writes none.
+template <int kDtype, int kMode>
 __device__ __forceinline__ void encode_block(const BlockWords<kDtype>& w, int64_t blk, float g, float est_scale,
                                              float g6, const uint32_t* __restrict__ mask,
-                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                             uint16_t* __restrict__ record16, const uint8_t* __restrict__ scales_in) {
+  constexpr bool kGuided = kMode == kModeGuided || kMode == kModeCached;
   uint32_t ax[16];
   uint32_t sgn = 0;
   if (kDtype == NVFP4RL_BF16) {
@@ -469,26 +536,39 @@ __device__ __forceinline__ void encode_block(const BlockWords<kDtype>& w, int64_
   const float bamax = __uint_as_float(mx);
 
   uint32_t b = 0;
-  if (g > 0.0f) b = scale_byte(bamax, g, __fdiv_rn(bamax * est_scale, g6));
+  if (kMode == kModeCached) {
+    if (g > 0.0f) b = min(static_cast<uint32_t>(scales_in[blk]), 0x7Eu);
+  } else if (g > 0.0f) {
+    b = scale_byte(bamax, g, __fdiv_rn(bamax * est_scale, g6));
+  }
   const float dec = e4m3_decode_pos(b);
 
   uint32_t lo32 = 0, hi32 = 0;
   if (!kGuided) {
-    uint32_t th[7];
+    uint32_t th[7], ge[7], gt[7];
     plain_thresholds(dec, g, th);
+    if (kMode == kModeRecord) guided_thresholds(dec, g, ge, gt);
     if (b == 0) {
 #pragma unroll
-      for (int k = 0; k < 7; ++k) th[k] = 0x7F800000u;  // zero scale: every code is sign|0
+      for (int k = 0; k < 7; ++k) th[k] = ge[k] = 0x7F800000u;  // zero scale: every code is sign|0
     }
+    uint32_t bits = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       uint32_t mag = 0;
 #pragma unroll
       for (int k = 0; k < 7; ++k) mag += ax[i] > th[k] ? 1u : 0u;
+      if (kMode == kModeRecord) {
+        uint32_t c_ge = 0;  // grid points at or below |x|: the plain magnitude is c_ge or c_ge + 1
+#pragma unroll
+        for (int k = 0; k < 7; ++k) c_ge += ax[i] > ge[k] ? 1u : 0u;
+        bits |= (mag - c_ge) << i;
+      }
       const uint32_t code = mag | (((sgn >> i) & 1u) << 3);
       if (i < 8) lo32 |= code << (4 * i);
       else hi32 |= code << (4 * (i - 8));
     }
+    if (kMode == kModeRecord) record16[blk] = static_cast<uint16_t>(bits);
   } else {
     uint32_t ge[7], gt[7];
     guided_thresholds(dec, g, ge, gt);
@@ -514,33 +594,43 @@ __device__ __forceinline__ void encode_block(const BlockWords<kDtype>& w, int64_
     }
   }
   *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo32, hi32);
-  scales[blk] = static_cast<uint8_t>(b);
+  if (kMode != kModeCached) scales[blk] = static_cast<uint8_t>(b);
 }
 
-template <int kDtype, bool kGuided>
+// kModeCached reads g from g_in and the scale bytes from scales_in, and writes the codes only;
+// the other modes take g = amax / 2688 (amax from amax_in, else the accumulated amax_bits) and
+// write g, the scale bytes and the codes (kModeRecord also the rounding-direction bits).
+template <int kDtype, int kMode>
 __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ x, int64_t nblocks,
                                                        const uint32_t* __restrict__ amax_bits,
                                                        const float* __restrict__ amax_in,
                                                        const uint32_t* __restrict__ mask,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                       float* __restrict__ g_out) {
+                                                       float* __restrict__ g_out, uint16_t* __restrict__ record16,
+                                                       const uint8_t* __restrict__ scales_in,
+                                                       const float* __restrict__ g_in) {
   griddep_wait();
   griddep_launch_dependents();
-  const float amax = amax_in ? *amax_in : __uint_as_float(*amax_bits);
-  const float g = __fdiv_rn(amax, 2688.0f);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  float g;
+  if (kMode == kModeCached) {
+    g = *g_in;
+  } else {
+    const float amax = amax_in ? *amax_in : __uint_as_float(*amax_bits);
+    g = __fdiv_rn(amax, 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  }
   // The estimate of bamax / (6 g) is taken on operands scaled by 2^64 when g is tiny,
   // so that 6 g keeps full precision; the exact correction uses the unscaled values.
   const bool tiny = g < 0x1p-60f;
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float g6 = 6.0f * (g * est_scale);
   const float inv_g6 = 1.0f / g6;
-  __shared__ EncodeTables tab;
-  // the guided tables exist only in the bf16 guided kernel
-  __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kGuided, GuidedTables, char> gtab;
+  // bf16 tables: the plain ones unless the scale bytes are given, the guided ones unless plain
+  __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kMode != kModeCached, EncodeTables, char> tab;
+  __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kMode != kModePlain, GuidedTables, char> gtab;
   if constexpr (kDtype == NVFP4RL_BF16) {
-    build_encode_tables(tab, g);
-    if constexpr (kGuided) build_guided_tables(gtab, g);
+    if constexpr (kMode != kModeCached) build_encode_tables(tab, g);
+    if constexpr (kMode != kModePlain) build_guided_tables(gtab, g);
     __syncthreads();
   }
 
@@ -555,15 +645,22 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
     BlockWords<kDtype> a, b;
     load_block<kDtype>(x, blk, a);
     if (two) load_block<kDtype>(x, blk2, b);
-    if constexpr (kDtype == NVFP4RL_BF16 && !kGuided) {
+    if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModePlain) {
       encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
       if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
+    } else if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModeRecord) {
+      encode_block_bf16_record(a.v, blk, g, inv_g6, est_scale, tab, gtab, codes, scales, record16);
+      if (two) encode_block_bf16_record(b.v, blk2, g, inv_g6, est_scale, tab, gtab, codes, scales, record16);
+    } else if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModeGuided) {
+      encode_block_bf16_guided<false>(a.v, blk, g, inv_g6, est_scale, &tab, gtab, mask, codes, scales, nullptr);
+      if (two) encode_block_bf16_guided<false>(b.v, blk2, g, inv_g6, est_scale, &tab, gtab, mask, codes, scales, nullptr);
     } else if constexpr (kDtype == NVFP4RL_BF16) {
-      encode_block_bf16_guided(a.v, blk, g, inv_g6, est_scale, tab, gtab, mask, codes, scales);
-      if (two) encode_block_bf16_guided(b.v, blk2, g, inv_g6, est_scale, tab, gtab, mask, codes, scales);
+      // the given scale bytes need no scale tables
+      encode_block_bf16_guided<true>(a.v, blk, g, inv_g6, est_scale, nullptr, gtab, mask, codes, nullptr, scales_in);
+      if (two) encode_block_bf16_guided<true>(b.v, blk2, g, inv_g6, est_scale, nullptr, gtab, mask, codes, nullptr, scales_in);
     } else {
-      encode_block<kDtype, kGuided>(a, blk, g, est_scale, g6, mask, codes, scales);
-      if (two) encode_block<kDtype, kGuided>(b, blk2, g, est_scale, g6, mask, codes, scales);
+      encode_block<kDtype, kMode>(a, blk, g, est_scale, g6, mask, codes, scales, record16, scales_in);
+      if (two) encode_block<kDtype, kMode>(b, blk2, g, est_scale, g6, mask, codes, scales, record16, scales_in);
     }
   }
 }
@@ -898,7 +995,7 @@ nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_b
 namespace {
 
 // CTAs of quantize_kernel resident per SM (once per device and variant).
-template <int kDtype, bool kGuided>
+template <int kDtype, int kMode>
 int quantize_ctas_per_sm(int device) {
   static std::mutex mu;
   static std::map<int, int> cache;
@@ -906,7 +1003,7 @@ int quantize_ctas_per_sm(int device) {
   auto it = cache.find(device);
   if (it != cache.end()) return it->second;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<kDtype, kGuided>, 256, 0) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<kDtype, kMode>, 256, 0) != cudaSuccess ||
       n < 1) {
     cudaGetLastError();
     n = 8;
@@ -917,37 +1014,66 @@ int quantize_ctas_per_sm(int device) {
 
 }  // namespace
 
+namespace {
+
+template <int kDtype, int kMode>
+cudaError_t launch_encode(int64_t nblocks, const DeviceInfo& dev, cudaStream_t st, const void* x,
+                          const uint32_t* amax_bits, const float* amax_in, const uint32_t* mask, uint8_t* codes,
+                          uint8_t* scales, float* g, uint16_t* record16, const uint8_t* scales_in, const float* g_in) {
+  // one wave: as many CTAs as can be resident at once (each loops over its share of the blocks)
+  const int threads = 256;
+  const int64_t want = (nblocks + threads - 1) / threads;
+  const int per_sm = quantize_ctas_per_sm<kDtype, kMode>(dev.device);
+  const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(dev.sm_count) * per_sm));
+  return launch_pdl(quantize_kernel<kDtype, kMode>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_bits, amax_in,
+                    mask, codes, scales, g, record16, scales_in, g_in);
+}
+
+template <int kMode>
+cudaError_t launch_encode_dtype(int dtype, int64_t nblocks, const DeviceInfo& dev, cudaStream_t st, const void* x,
+                                const uint32_t* amax_bits, const float* amax_in, const uint32_t* mask,
+                                uint8_t* codes, uint8_t* scales, float* g, uint16_t* record16,
+                                const uint8_t* scales_in, const float* g_in) {
+  return dtype == NVFP4RL_BF16
+             ? launch_encode<NVFP4RL_BF16, kMode>(nblocks, dev, st, x, amax_bits, amax_in, mask, codes, scales, g,
+                                                  record16, scales_in, g_in)
+             : launch_encode<NVFP4RL_F32, kMode>(nblocks, dev, st, x, amax_bits, amax_in, mask, codes, scales, g,
+                                                 record16, scales_in, g_in);
+}
+
+}  // namespace
+
 nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
-                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done) {
+                               uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done,
+                               uint32_t* record) {
   const int64_t n = rows * cols;
   const int64_t nblocks = n / 16;
   if (nblocks == 0) return NVFP4RL_OK;
-  const int threads = 256;
   if (amax_in == nullptr && !amax_done) {
     const nvfp4rl_status sa = launch_amax(x, dtype, n, amax_scratch, dev, st);
     if (sa != NVFP4RL_OK) return sa;
   }
-  // one wave: as many CTAs as can be resident at once (each loops over its share of the blocks)
-  const int64_t want = (nblocks + threads - 1) / threads;
-  const int per_sm = dtype == NVFP4RL_BF16 ? (mask ? quantize_ctas_per_sm<NVFP4RL_BF16, true>(dev.device)
-                                                   : quantize_ctas_per_sm<NVFP4RL_BF16, false>(dev.device))
-                                          : (mask ? quantize_ctas_per_sm<NVFP4RL_F32, true>(dev.device)
-                                                  : quantize_ctas_per_sm<NVFP4RL_F32, false>(dev.device));
-  const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(dev.sm_count) * per_sm));
-  cudaError_t e;
-  if (dtype == NVFP4RL_BF16) {
-    e = mask ? launch_pdl(quantize_kernel<NVFP4RL_BF16, true>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
-                          amax_in, mask, codes, scales, g)
-             : launch_pdl(quantize_kernel<NVFP4RL_BF16, false>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
-                          amax_in, mask, codes, scales, g);
-  } else {
-    e = mask ? launch_pdl(quantize_kernel<NVFP4RL_F32, true>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
-                          amax_in, mask, codes, scales, g)
-             : launch_pdl(quantize_kernel<NVFP4RL_F32, false>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_scratch,
-                          amax_in, mask, codes, scales, g);
-  }
+  uint16_t* record16 = reinterpret_cast<uint16_t*>(record);
+  const cudaError_t e =
+      record ? launch_encode_dtype<kModeRecord>(dtype, nblocks, dev, st, x, amax_scratch, amax_in, nullptr, codes,
+                                                scales, g, record16, nullptr, nullptr)
+      : mask ? launch_encode_dtype<kModeGuided>(dtype, nblocks, dev, st, x, amax_scratch, amax_in, mask, codes,
+                                                scales, g, nullptr, nullptr, nullptr)
+             : launch_encode_dtype<kModePlain>(dtype, nblocks, dev, st, x, amax_scratch, amax_in, nullptr, codes,
+                                               scales, g, nullptr, nullptr, nullptr);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  return launch_status();
+}
+
+nvfp4rl_status launch_quantize_cached(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
+                                      const uint8_t* scales, const float* g, uint8_t* codes, const DeviceInfo& dev,
+                                      cudaStream_t st) {
+  const int64_t nblocks = rows * cols / 16;
+  if (nblocks == 0) return NVFP4RL_OK;
+  if (launch_encode_dtype<kModeCached>(dtype, nblocks, dev, st, x, nullptr, nullptr, mask, codes, nullptr, nullptr,
+                                       nullptr, scales, g) != cudaSuccess)
+    return NVFP4RL_ERR_CUDA;
   return launch_status();
 }
 

@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "nvfp4_quantize_batch", "rmsnorm_aqn",
+                     "nvfp4_quantize_record", "nvfp4_quantize_cached",
                      "rmsnorm_aqn_quantize", "nvfp4_lora_linear",
                      "nvfp4_lora_linear_w4a4", "aqn_sigma"):
         assert required in names
@@ -82,6 +83,33 @@ def test_quantize_validation(nv):
     assert _q(nv, wsb=8) == 4                  # workspace too small
     g = nv.lib().nvfp4_quantize_guided(A0, 0, 4, 32, None, A1, A2, A3, None, A4, 256, None)
     assert g == 1                              # guided without a mask
+
+
+def test_quantize_record_validation(nv):
+    rec = nv.lib().nvfp4_quantize_record
+    A5 = A4 + 0x10000
+    assert rec(A0, 0, 4, 32, A1, A2, A3, None, None, A4, 256, None) == 1      # no record buffer
+    assert rec(A0, 0, 4, 32, A1, A2, A3, A5 + 4, None, A4, 256, None) == 2    # misaligned record
+    assert rec(A0, 0, 4, 32, A1, A2, A3, A1, None, A4, 256, None) == 7        # record over the codes
+    assert rec(A0, 0, 4, 32, A1, A2, A3, A0 + 16, None, A4, 256, None) == 7   # record over the input
+    assert rec(A0, 0, 4, 32, A1, A2, A3, A5, None, None, 0, None) == 4        # no workspace, no amax_in
+    assert rec(A0, 0, 4, 24, A1, A2, A3, A5, None, A4, 256, None) == 3
+    assert rec(A0, 0, 0, 32, A1, A2, A3, None, None, None, 0, None) == 0      # empty: nothing to do
+
+
+def test_quantize_cached_validation(nv):
+    cac = nv.lib().nvfp4_quantize_cached
+    A5 = A4 + 0x10000
+    assert cac(A0, 0, 4, 32, None, A2, A3, A1, None) == 1      # no mask
+    assert cac(A0, 0, 4, 32, A5, None, A3, A1, None) == 1      # no scales
+    assert cac(A0, 0, 4, 32, A5, A2, None, A1, None) == 1      # no g
+    assert cac(A0, 5, 4, 32, A5, A2, A3, A1, None) == 1        # bad dtype
+    assert cac(A0, 0, 4, 40, A5, A2, A3, A1, None) == 3        # cols not a multiple of 16
+    assert cac(A0, 0, 4, 32, A5 + 8, A2, A3, A1, None) == 2    # misaligned mask
+    assert cac(A0, 0, 4, 32, A5, A2, A3 + 2, A1, None) == 2    # misaligned g
+    assert cac(A0, 0, 4, 32, A5, A2, A3, A5, None) == 7        # codes over the mask
+    assert cac(A0, 0, 4, 32, A5, A2, A3, A2, None) == 7        # codes over the scales
+    assert cac(A0, 0, 0, 32, None, None, None, None, None) == 0  # empty: nothing to do
 
 
 def _qb(nv, n=2, xs=(A0, A0 + 0x1000), rows=(4, 8), cols=(32, 64), dtype=0, codes=(A1, A1 + 0x1000),

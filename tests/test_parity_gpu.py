@@ -196,6 +196,103 @@ def test_quantize_moe_experts_guided(nv):
             assert_quant_equal(gpu_quantize(nv, W), oracle.quantize(W), f"expert {e}.{j} plain")
 
 
+# ---------------------------------------------------------------- TRACE record and cached replay
+
+def _mask_bits(words, n):
+    return np.unpackbits(np.ascontiguousarray(words).view(np.uint8), bitorder="little")[:n]
+
+
+def gpu_record(nv, x_np, fill=0):
+    x = P.dev_bf16(x_np) if x_np.dtype == np.uint16 else P.dev(x_np)
+    rec = torch.full(((x_np.size + 31) // 32,), fill, dtype=torch.int32, device="cuda")
+    c, s, g, r = nv.nvfp4_quantize_record(x, record=rec)
+    torch.cuda.synchronize()
+    return (c.cpu().numpy(), s.cpu().numpy(), np.float32(g.cpu().numpy()[0])), r.cpu().numpy().view(np.uint32)
+
+
+def gpu_cached(nv, x_np, mask, scales, g):
+    x = P.dev_bf16(x_np) if x_np.dtype == np.uint16 else P.dev(x_np)
+    gd = torch.tensor([np.float32(g)], dtype=torch.float32, device="cuda")
+    c = nv.nvfp4_quantize_cached(x, P.dev(np.ascontiguousarray(mask).view(np.int32)), P.dev(scales), gd)
+    torch.cuda.synchronize()
+    return c.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(1, 16), (37, 48), (300, 1040), (129, 4096)])
+def test_quantize_record_ragged(nv, dtype, shape):
+    """Codes, scales and g as nvfp4_quantize; the record bit for bit; with an odd number of blocks
+    the upper half of the last record word keeps its previous contents."""
+    W = synth.weight_f32(*shape, 0.02, 12, shape[0], outlier_frac=0.02)
+    x = synth.bf16_bits(W) if dtype == "bf16" else W
+    got, rec = gpu_record(nv, x, fill=-0x5A5A5A5B)  # 0xA5A5A5A5
+    c, s, g, m = oracle.quantize_record(x)
+    assert_quant_equal(got, (c, s, g), f"record {dtype} {shape}")
+    n = x.size
+    assert np.array_equal(_mask_bits(rec, n), _mask_bits(m, n)), f"{dtype} {shape}: record bits differ"
+    if (n // 16) % 2:
+        assert rec[-1] >> 16 == 0xA5A5, "the unused half of the last record word was written"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_quantize_record_edge_values(nv, dtype):
+    """Exact grid points, every midpoint (ties both ways), +-0, zero and subnormal-scale blocks."""
+    e = _edge_tensor()
+    x = synth.bf16_bits(e) if dtype == "bf16" else e
+    got, rec = gpu_record(nv, x)
+    c, s, g, m = oracle.quantize_record(x)
+    assert_quant_equal(got, (c, s, g), f"record edge {dtype}")
+    assert np.array_equal(_mask_bits(rec, x.size), _mask_bits(m, x.size))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_quantize_cached_replay(nv, dtype):
+    """Replay from the rollout's cache: the same weights give the plain codes back; weights one
+    update later, and a random mask, give the oracle's cached codes; degenerate caches (g = 0,
+    negative g, bytes above 0x7E) follow the stated rules."""
+    W = synth.weight_f32(200, 768, 0.02, 13, 1, outlier_frac=0.01)
+    x = synth.bf16_bits(W) if dtype == "bf16" else W
+    c, s, g, m = oracle.quantize_record(x)
+    assert np.array_equal(gpu_cached(nv, x, m, s, g), c), "replay of the recorded weights"
+    W2 = (W + synth.normal_f32(W.shape, 0.002, 13, 2)).astype(np.float32)
+    x2 = synth.bf16_bits(W2) if dtype == "bf16" else W2
+    assert np.array_equal(gpu_cached(nv, x2, m, s, g), oracle.quantize_cached(x2, m, s, g)), "updated weights"
+    r = synth.guided_mask(W.size, 13, 3)
+    assert np.array_equal(gpu_cached(nv, x2, r, s, g), oracle.quantize_cached(x2, r, s, g)), "random mask"
+    s_odd = s.copy()
+    s_odd[::7] = 0xFF
+    s_odd[1::11] = 0x7F
+    s_odd[2::13] = 0x00
+    for gg in (g, np.float32(0.0), np.float32(-1.0)):
+        assert np.array_equal(gpu_cached(nv, x2, r, s_odd, gg), oracle.quantize_cached(x2, r, s_odd, gg)), f"g={gg}"
+    e = _edge_tensor()
+    xe = synth.bf16_bits(e) if dtype == "bf16" else e
+    ce, se, ge, me = oracle.quantize_record(xe)
+    assert np.array_equal(gpu_cached(nv, xe, me, se, ge), ce), "edge values"
+
+
+def test_trace_round_trip_gpu_only_qwen7b_gate(nv):
+    """The full 7B gate weight (18944 x 3584 bf16): record, then replay from the GPU's own cache,
+    gives the GPU's plain codes back; sampled rows of the record and of the codes match the oracle."""
+    n, k = synth.QWEN25_7B["linears"]["gate"]
+    W = synth.weight_bf16(n, k, 0.02, 14, 1, outlier_frac=0.01)
+    x = P.dev_bf16(W)
+    c, s, g, rec = nv.nvfp4_quantize_record(x)
+    plain, _, _ = nv.nvfp4_quantize(x)
+    replay = nv.nvfp4_quantize_cached(x, rec, s, g)
+    torch.cuda.synchronize()
+    assert torch.equal(replay, plain) and torch.equal(c, plain)
+    rows = np.sort(np.random.default_rng(14).choice(n, 24, replace=False))
+    gh = np.float32(g.cpu().numpy()[0])
+    assert gh == oracle.global_scale(oracle.amax(W))
+    rec_h = rec.cpu().numpy().view(np.uint32)
+    for r in rows:
+        cr, sr, gr, mr = oracle.quantize_record(W[r:r + 1], amax_in=oracle.amax(W))
+        assert gr == gh
+        assert np.array_equal(c[r].cpu().numpy(), cr[0]) and np.array_equal(s[r].cpu().numpy(), sr[0])
+        assert np.array_equal(rec_h[r * k // 32:(r + 1) * k // 32], mr), f"row {r}: record bits differ"
+
+
 # ---------------------------------------------------------------- RMSNorm with AQN
 
 def gpu_rmsnorm(nv, x, w, eps, sigma, delta):
