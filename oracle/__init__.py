@@ -59,6 +59,7 @@ def _declare(lib):
         "oracle_quantize_record_rows": (None, [p, i, i64, i64, i64, f, p, p, p]),
         "oracle_e2m1_round_up": (i, [d, d]),
         "oracle_quantize_cached_rows": (None, [p, i, i64, i64, i64, f, p, p, p]),
+        "oracle_ais": (None, [i64, p, p, p, d, d, d, d, p, p]),
         "oracle_aqn_sigma": (d, [d, d, i64, i64]),
         "oracle_rmsnorm_aqn_rows": (None, [p, i64, i64, i64, p, p, f, f, p]),
         "oracle_lora_down": (None, [p, i64, i64, p, i32, p]),
@@ -226,6 +227,24 @@ def quantize_cached(x: np.ndarray, mask: np.ndarray, scales: np.ndarray, g: floa
                                                       _ptr(scales), _ptr(mask), _ptr(codes))
     _parallel(fn, rows, nthreads)
     return codes
+
+
+AIS_STATS = ("alpha", "alpha_ess", "alpha_mis", "alpha_var", "dbar", "cv2", "dsigma", "mean_w")
+
+
+def ais(logp_rollout, logp_train, adv, C: float, delta: float, gamma: float, beta: float, L=None):
+    """AIS mixing coefficient over a batch of tokens (fp32 inputs): (stats dict, rectified weights f64)."""
+    L = L or lib()
+    lr = np.ascontiguousarray(logp_rollout, dtype=np.float32)
+    lt = np.ascontiguousarray(logp_train, dtype=np.float32)
+    a = np.ascontiguousarray(adv, dtype=np.float32)
+    n = lr.size
+    assert lt.size == n and a.size == n
+    stats = np.full(8, np.nan)
+    w = np.zeros(n)
+    L.oracle_ais(n, _ptr(lr), _ptr(lt), _ptr(a), float(C), float(delta), float(gamma), float(beta), _ptr(stats),
+                 _ptr(w))
+    return dict(zip(AIS_STATS, stats.tolist())), w
 
 
 def quantize_rows_given_g(x: np.ndarray, g: float, rows, mask: np.ndarray | None = None, L=None):

@@ -20,6 +20,12 @@
 //    an exponential noise schedule (section "AQNの仕組み").
 //  * LoRA linear: Y = x deq(W)^T + s (x A^T) B^T (QeRL explainer, section
 //    "NVFP4量子化とLoRA": frozen quantized base plus low-rank trainable factors).
+//  * AIS mixing coefficient (AIS summary, section 2.1 "混合係数": alpha_ess from the
+//    coefficient of variation of the truncated weights, alpha_mis from the mean
+//    absolute log-prob mismatch and a saturation threshold delta, alpha_var from a
+//    variance amplification ratio and a tolerance gamma, alpha = clip(alpha_ess -
+//    beta alpha_var, 0, 1) alpha_mis; section 2.2: the rectified weight
+//    w~ = 1 + alpha (min(rho, C) - 1)).
 //
 // Readings taken where the definition leaves a step open:
 //  * Both roundings (the E4M3 block scale and the E2M1 element code) apply to the
@@ -42,6 +48,13 @@
 //    element is 1 when the plain code's magnitude exceeds |x| / S (the value was
 //    rounded up in magnitude) and 0 otherwise (rounded down, on the grid, saturated,
 //    or a zero scale). Guided rounding with that mask gives the plain codes back.
+//  * AIS readings: one importance ratio per token, rho = exp(logp_train - logp_rollout)
+//    (training over rollout probability of the sampled token); w = min(rho, C); the
+//    CV, means and standard deviations are over the batch's N tokens with weight 1/N
+//    (population statistics); the variance amplification Delta sigma is the relative
+//    growth of the advantages' spread under the weights, std(w * A) / std(A) - 1 with A
+//    the per-token advantage (0 when the weights are all 1, so that a batch without
+//    mismatch is not penalised), and 0 when std(A) = 0.
 //  * Replay from the cache (section "TRACE の中心的なアイデア": the scale information
 //    is kept with the rounding bits): codes are the guided codes against the recorded
 //    scale byte and g, with no amax and no scale search. A recorded byte above 0x7E
@@ -240,6 +253,56 @@ void oracle_dequantize_rows(const uint8_t* codes, const uint8_t* scales, float g
       const int c = (codes[idx / 2] >> ((idx & 1) * 4)) & 15;
       out[idx] = e2m1_value(c) * e4m3_value(scales[r * nblk + k / 16]) * static_cast<double>(g);
     }
+}
+
+// AIS over a batch of n tokens. stats (8 doubles): alpha, alpha_ess, alpha_mis, alpha_var,
+// the mean |logp_train - logp_rollout|, CV^2 of the truncated weights, Delta sigma, and mean(w). w_out (n doubles, may be null): the rectified weights.
+void oracle_ais(int64_t n, const float* logp_rollout, const float* logp_train, const float* adv, double C,
+                double delta, double gamma, double beta, double* stats, double* w_out) {
+  if (n <= 0) return;
+  std::vector<double> w(n);
+  double sum_d = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    const double d = static_cast<double>(logp_train[i]) - static_cast<double>(logp_rollout[i]);
+    sum_d += std::fabs(d);
+    w[i] = std::fmin(std::exp(d), C);
+  }
+  const double N = static_cast<double>(n);
+  double mw = 0.0, ma = 0.0, mwa = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    mw += w[i];
+    ma += adv[i];
+    mwa += w[i] * adv[i];
+  }
+  mw /= N;
+  ma /= N;
+  mwa /= N;
+  double vw = 0.0, va = 0.0, vwa = 0.0;  // two-pass population variances
+  for (int64_t i = 0; i < n; ++i) {
+    vw += (w[i] - mw) * (w[i] - mw);
+    va += (adv[i] - ma) * (adv[i] - ma);
+    vwa += (w[i] * adv[i] - mwa) * (w[i] * adv[i] - mwa);
+  }
+  vw /= N;
+  va /= N;
+  vwa /= N;
+  const double cv2 = vw / (mw * mw);
+  const double a_ess = 1.0 / std::sqrt(1.0 + cv2);
+  const double dbar = sum_d / N;
+  const double a_mis = std::fmin(1.0, dbar / delta);
+  const double amp = va > 0.0 ? std::sqrt(vwa) / std::sqrt(va) - 1.0 : 0.0;
+  const double a_var = std::fmax(0.0, (amp - gamma) / gamma);
+  const double alpha = std::fmin(1.0, std::fmax(0.0, a_ess - beta * a_var)) * a_mis;
+  stats[0] = alpha;
+  stats[1] = a_ess;
+  stats[2] = a_mis;
+  stats[3] = a_var;
+  stats[4] = dbar;
+  stats[5] = cv2;
+  stats[6] = amp;
+  stats[7] = mw;
+  if (w_out)
+    for (int64_t i = 0; i < n; ++i) w_out[i] = 1.0 + alpha * (w[i] - 1.0);
 }
 
 // AQN noise schedule: sigma_k = sigma0 * (sigmaK / sigma0)^(k / K).

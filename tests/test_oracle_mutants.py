@@ -45,6 +45,15 @@ MUTANTS = {
     "cached_scale_of_next_block": ("scales[r * nblk + b] > 0x7E ? 0x7E : scales[r * nblk + b]",
                                    "scales[r * nblk + (b + 1) % nblk] > 0x7E ? 0x7E : scales[r * nblk + (b + 1) % nblk]"),
     "cached_g_dropped": ("(g > 0.0f) ? e4m3_value(s) * static_cast<double>(g) : 0.0", "(g > 0.0f) ? e4m3_value(s) : 0.0"),
+    "ais_ess_without_sqrt": ("const double a_ess = 1.0 / std::sqrt(1.0 + cv2);", "const double a_ess = 1.0 / (1.0 + cv2);"),
+    "ais_signed_mismatch": ("sum_d += std::fabs(d);", "sum_d += d;"),
+    "ais_ratio_inverted": ("static_cast<double>(logp_train[i]) - static_cast<double>(logp_rollout[i])",
+                           "static_cast<double>(logp_rollout[i]) - static_cast<double>(logp_train[i])"),
+    "ais_no_truncation": ("w[i] = std::fmin(std::exp(d), C);", "w[i] = std::exp(d);"),
+    "ais_no_clip": ("std::fmin(1.0, std::fmax(0.0, a_ess - beta * a_var)) * a_mis", "(a_ess - beta * a_var) * a_mis"),
+    "ais_mis_unsaturated": ("const double a_mis = std::fmin(1.0, dbar / delta);", "const double a_mis = dbar / delta;"),
+    "ais_dsigma_raw_ratio": ("std::sqrt(vwa) / std::sqrt(va) - 1.0", "std::sqrt(vwa) / std::sqrt(va)"),
+    "ais_rectified_weight": ("w_out[i] = 1.0 + alpha * (w[i] - 1.0);", "w_out[i] = alpha * w[i];"),
     "cached_mask_shifted": ("        const int up = (mask[idx / 32] >> (idx % 32)) & 1;\n        const int c = e2m1_encode_guided(load_elem",
                             "        const int up = (mask[idx / 32] >> ((idx + 1) % 32)) & 1;\n        const int c = e2m1_encode_guided(load_elem"),
 }
@@ -149,6 +158,21 @@ def _battery(L):
         c, s, g, m = oracle.quantize_record(x, L=L)
         return np.array_equal(oracle.quantize_cached(x, m, s, g, L=L), c)
     check("cached_roundtrip", cached_roundtrip)
+
+    def ais_cases():
+        from tests import test_oracle_ais as T
+        cases = [T.test_no_mismatch_is_vanilla_grpo, T.test_two_valued_weights_closed_form,
+                 T.test_truncation_and_saturation, T.test_penalty_clips_at_zero,
+                 lambda: T.test_variance_penalty_closed_form(3.0, 0.5, 0.25)]
+        real = oracle.ais
+        oracle.ais = lambda *a, **k: real(*a, **{**k, "L": L})
+        try:
+            for c in cases:
+                c()
+        finally:
+            oracle.ais = real
+        return True
+    check("ais", ais_cases)
 
     def linear():
         N, K, M, r = 5, 64, 3, 2
