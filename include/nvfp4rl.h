@@ -66,7 +66,8 @@ enum {
   NVFP4RL_OP_LINEAR_W4A16 = 1,
   NVFP4RL_OP_LINEAR_W4A4 = 2,
   NVFP4RL_OP_QUANTIZE_BATCH = 3, /* M = number of tensors */
-  NVFP4RL_OP_RMSNORM_QUANTIZE = 4
+  NVFP4RL_OP_RMSNORM_QUANTIZE = 4,
+  NVFP4RL_OP_AIS = 5
 };
 
 /*
@@ -188,6 +189,33 @@ NVFP4RL_API nvfp4rl_status nvfp4_quantize_record(const void* x, int32_t dtype, i
 NVFP4RL_API nvfp4rl_status nvfp4_quantize_cached(const void* x, int32_t dtype, int64_t rows, int64_t cols,
                                                  const uint32_t* mask, const uint8_t* scales, const float* g,
                                                  uint8_t* codes, void* stream);
+
+/*
+ * ais_mixing -- the adaptive importance-sampling correction of a batch of n tokens (AIS summary,
+ *   section 2.1 "混合係数" and section 2.2 "GRPO への統合"):
+ *     rho_i = exp(logp_train[i] - logp_rollout[i]),  w_i = min(rho_i, C),
+ *     alpha_ess = (1 + CV^2(w))^-1/2,  alpha_mis = min(1, mean|logp_train - logp_rollout| / delta),
+ *     dsigma = std(w A) / std(A) - 1 (0 when std(A) = 0),  alpha_var = max(0, (dsigma - gamma) / gamma),
+ *     alpha = clip(alpha_ess - beta alpha_var, 0, 1) alpha_mis,  w~_i = 1 + alpha (w_i - 1),
+ *   means and standard deviations over the n tokens with weight 1/n.
+ * Arguments:
+ *   logp_rollout, logp_train, adv  device fp32 [n], 16-byte aligned: the sampled tokens' log-probs
+ *            under the rollout and the training policy, and their advantages.
+ *   n        tokens (>= 0; 0: nothing is written).
+ *   C, delta, gamma  > 0 and finite; beta >= 0 and finite (else NVFP4RL_ERR_INVALID_ARG).
+ *   w_out    out, device fp32 [n], 16-byte aligned, or NULL (statistics only).
+ *   stats    out, device fp64 [8], 8-byte aligned: alpha, alpha_ess, alpha_mis, alpha_var,
+ *            mean |logp_train - logp_rollout|, CV^2(w), dsigma, mean(w).
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_AIS, 0, 0, 0, 0, 0) bytes, device, 16-byte
+ *            aligned; scratch.
+ * Outputs may overlap no input, each other or the workspace (NVFP4RL_ERR_ALIAS). The sums are
+ * compensated fp32 per thread and (hi, lo) fp32 pairs across threads and CTAs, added in a fixed
+ * order: the result does not depend on timing. alpha and the ratios are formed in fp32 from
+ * fp64 means. Three kernels chained by programmatic dependent launch; no device-side waits.
+ */
+NVFP4RL_API nvfp4rl_status ais_mixing(const float* logp_rollout, const float* logp_train, const float* adv,
+                                      int64_t n, float C, float delta, float gamma, float beta, float* w_out,
+                                      double* stats, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * aqn_sigma -- AQN exponential noise schedule (QeRL explainer, "AQNの仕組み":

@@ -8,7 +8,7 @@ importing the binding does not build it, and every call fails loudly when the
 library or a GPU is missing -- there is no CPU fallback.
 
 Functions carry the C names: nvfp4_amax, nvfp4_quantize, nvfp4_quantize_guided,
-nvfp4_quantize_record, nvfp4_quantize_cached, nvfp4_quantize_batch, aqn_sigma, rmsnorm_aqn, rmsnorm_aqn_quantize, nvfp4_lora_linear,
+nvfp4_quantize_record, nvfp4_quantize_cached, nvfp4_quantize_batch, ais_mixing, aqn_sigma, rmsnorm_aqn, rmsnorm_aqn_quantize, nvfp4_lora_linear,
 nvfp4_lora_linear_w4a4.
 """
 from __future__ import annotations
@@ -23,7 +23,7 @@ LIB_PATH = _build.LIB
 
 OK = 0
 BF16, F32 = 0, 1
-OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH, OP_RMSNORM_QUANTIZE = 0, 1, 2, 3, 4
+OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH, OP_RMSNORM_QUANTIZE, OP_AIS = 0, 1, 2, 3, 4, 5
 
 _lock = threading.Lock()
 _lib = None
@@ -41,6 +41,7 @@ def _signatures():
         "nvfp4_quantize_guided": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
         "nvfp4_quantize_record": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
         "nvfp4_quantize_cached": (c.c_int, [p, i32, i64, i64, p, p, p, p, p]),
+        "ais_mixing": (c.c_int, [p, p, p, i64, c.c_float, c.c_float, c.c_float, c.c_float, p, p, p, sz, p]),
         "nvfp4_quantize_batch": (c.c_int, [i32, p, p, p, i32, p, p, p, p, sz, p]),
         "aqn_sigma": (f64, [f64, f64, i64, i64]),
         "rmsnorm_aqn": (c.c_int, [p, i64, i64, p, p, f32, f32, p, p]),
@@ -192,6 +193,32 @@ def nvfp4_quantize_cached(x, mask, scales, g, codes=None, stream=None):
                                      _stream(x, stream))
     _check(st, "nvfp4_quantize_cached")
     return codes
+
+
+AIS_STATS = ("alpha", "alpha_ess", "alpha_mis", "alpha_var", "dbar", "cv2", "dsigma", "mean_w")
+
+
+def ais_mixing(logp_rollout, logp_train, adv, C: float, delta: float, gamma: float, beta: float, weights=True,
+               w_out=None, stats=None, workspace=None, stream=None):
+    """AIS correction of a token batch (fp32 CUDA tensors of n elements) -> (stats fp64 [8] in the order
+    of AIS_STATS, rectified weights fp32 [n] or None when weights is False)."""
+    import torch
+    _require_cuda(logp_rollout, logp_train, adv, w_out, stats, workspace)
+    for t in (logp_rollout, logp_train, adv):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != logp_rollout.numel():
+            raise ValueError("log-probs and advantages must be contiguous fp32 tensors of one size")
+    n = logp_rollout.numel()
+    dev = logp_rollout.device
+    if weights and w_out is None:
+        w_out = _empty((n,), torch.float32, dev)
+    stats = _empty((8,), torch.float64, dev) if stats is None else stats
+    if workspace is None:
+        workspace = _empty((workspace_bytes(OP_AIS, 0, 0, 0),), torch.uint8, dev)
+    st = lib().ais_mixing(_ptr(logp_rollout), _ptr(logp_train), _ptr(adv), n, float(C), float(delta), float(gamma),
+                          float(beta), _ptr(w_out) if weights else None, _ptr(stats), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(logp_rollout, stream))
+    _check(st, "ais_mixing")
+    return stats, (w_out if weights else None)
 
 
 def nvfp4_quantize_batch(xs, codes=None, scales=None, g=None, workspace=None, stream=None):

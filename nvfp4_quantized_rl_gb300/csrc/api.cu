@@ -219,6 +219,36 @@ nvfp4rl_status nvfp4_quantize_cached(const void* x, int32_t dtype, int64_t rows,
   return launch_quantize_cached(x, dtype, rows, cols, mask, scales, g, codes, dev, static_cast<cudaStream_t>(stream));
 }
 
+nvfp4rl_status ais_mixing(const float* lr, const float* lt, const float* adv, int64_t n, float C, float delta,
+                          float gamma, float beta, float* w_out, double* stats, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (n < 0) return NVFP4RL_ERR_INVALID_ARG;
+  if (!(C > 0.0f) || !(delta > 0.0f) || !(gamma > 0.0f) || !(beta >= 0.0f) || !std::isfinite(C) ||
+      !std::isfinite(delta) || !std::isfinite(gamma) || !std::isfinite(beta))
+    return NVFP4RL_ERR_INVALID_ARG;
+  if (n == 0) return NVFP4RL_OK;
+  if (!lr || !lt || !adv || !stats) return NVFP4RL_ERR_INVALID_ARG;
+  if (!aligned16(lr) || !aligned16(lt) || !aligned16(adv) || (w_out && !aligned16(w_out)) ||
+      (reinterpret_cast<uintptr_t>(stats) & 7u))
+    return NVFP4RL_ERR_MISALIGNED;
+  const size_t need = ais_workspace_bytes();
+  if (!workspace || workspace_bytes < need) return NVFP4RL_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NVFP4RL_ERR_MISALIGNED;
+  const size_t nb = static_cast<size_t>(n) * 4;
+  const void* ins[3] = {lr, lt, adv};
+  for (const void* in : ins)
+    if ((w_out && overlap(w_out, nb, in, nb)) || overlap(stats, 64, in, nb) || overlap(workspace, need, in, nb))
+      return NVFP4RL_ERR_ALIAS;
+  if ((w_out && (overlap(w_out, nb, stats, 64) || overlap(w_out, nb, workspace, need))) ||
+      overlap(stats, 64, workspace, need))
+    return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_ais(lr, lt, adv, n, C, delta, gamma, beta, w_out, stats, workspace, dev,
+                    static_cast<cudaStream_t>(stream));
+}
+
 nvfp4rl_status nvfp4_quantize_batch(int32_t count, const void* const* x, const int64_t* rows, const int64_t* cols,
                                     int32_t dtype, uint8_t* const* codes, uint8_t* const* scales, float* const* g,
                                     void* workspace, size_t workspace_bytes, void* stream) {
@@ -337,6 +367,7 @@ size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int3
     case NVFP4RL_OP_QUANTIZE: return kQuantizeWorkspace;
     case NVFP4RL_OP_QUANTIZE_BATCH: return M <= kQuantizeBatchMax ? quantize_batch_workspace_bytes(M) : 0;
     case NVFP4RL_OP_RMSNORM_QUANTIZE: return kQuantizeWorkspace;
+    case NVFP4RL_OP_AIS: return ais_workspace_bytes();
     case NVFP4RL_OP_LINEAR_W4A16: return linear_workspace_bytes(false, M, N, K, r, 1);
     case NVFP4RL_OP_LINEAR_W4A4: return linear_workspace_bytes(true, M, N, K, r, num_groups > 0 ? num_groups : 1);
     default: return 0;

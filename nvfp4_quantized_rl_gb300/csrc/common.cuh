@@ -136,6 +136,14 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
                                uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done = false,
                                uint32_t* record = nullptr);
 
+// AIS mixing coefficient and rectified weights of n tokens (ais.cu); workspace: a barrier counter
+// and one slot of partial sums per CTA (at most kAisMaxCtas CTAs).
+constexpr int kAisMaxCtas = 1024;
+size_t ais_workspace_bytes();
+nvfp4rl_status launch_ais(const float* lr, const float* lt, const float* adv, int64_t n, float C, float delta,
+                          float gamma, float beta, float* w_out, double* stats, void* workspace,
+                          const DeviceInfo& dev, cudaStream_t st);
+
 // Guided codes of x against the given scale bytes and g (device), in one pass (quantize.cu).
 nvfp4rl_status launch_quantize_cached(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                       const uint8_t* scales, const float* g, uint8_t* codes, const DeviceInfo& dev,

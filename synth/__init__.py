@@ -19,8 +19,8 @@ import numpy as np
 __all__ = [
     "rng", "bf16_bits", "bf16_to_f32", "normal_f32", "normal_bf16", "weight_bf16",
     "weight_f32", "activation_bf16", "heavy_tail_activation_bf16", "lora_factors",
-    "aqn_weight", "aqn_eps", "guided_mask", "moe_routing", "QWEN25_7B", "QWEN25_32B",
-    "MOE", "tiny_config",
+    "aqn_weight", "aqn_eps", "guided_mask", "moe_routing", "grpo_token_batch", "QWEN25_7B", "QWEN25_32B",
+    "MOE", "GRPO_BATCH", "tiny_config",
 ]
 
 
@@ -125,6 +125,34 @@ def moe_routing(tokens: int, experts: int, top_k: int, seed: int, *stream: int):
     offsets = np.zeros(experts + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
     return token_of[perm].astype(np.int64), offsets
+
+
+def grpo_token_batch(prompts: int, group: int, mean_len: int, seed: int, *stream: int, mismatch: float = 0.05,
+                     max_tokens: int | None = None):
+    """A GRPO training batch flattened to tokens: `prompts` prompts x `group` responses whose lengths
+    are log-normal around mean_len (16 .. 4 mean_len); per response a Bernoulli reward (success rate
+    uniform per prompt), normalised within its group, (r - mean) / (std + 1e-6), and broadcast to its
+    tokens as the advantage; per token the rollout log-prob of the sampled token, -Exponential(0.4)
+    (mostly confident tokens), and the training log-prob, that plus N(0, mismatch) noise capped at 0
+    (the low-precision rollout's mismatch). Returns fp32 (logp_rollout, logp_train, adv), optionally
+    cut to max_tokens."""
+    g = rng(seed, *stream)
+    n_resp = prompts * group
+    lens = np.clip(np.rint(g.lognormal(np.log(mean_len) - 0.18, 0.6, n_resp)), 16, 4 * mean_len).astype(np.int64)
+    p = np.repeat(g.uniform(0, 1, prompts), group)
+    r = (g.uniform(0, 1, n_resp) < p).astype(np.float64).reshape(prompts, group)
+    a = ((r - r.mean(axis=1, keepdims=True)) / (r.std(axis=1, keepdims=True) + 1e-6)).reshape(-1)
+    adv = np.repeat(a, lens).astype(np.float32)
+    n = adv.size
+    lr = (-g.exponential(0.4, n)).astype(np.float32)
+    lt = np.minimum(lr + g.normal(0.0, mismatch, n), 0.0).astype(np.float32)
+    if max_tokens is not None:
+        lr, lt, adv = lr[:max_tokens], lt[:max_tokens], adv[:max_tokens]
+    return lr, lt, adv
+
+
+# A GRPO batch of 64 prompts x 8 responses of ~8K tokens (about 4 M tokens; at most 4 Mi are kept).
+GRPO_BATCH = {"prompts": 64, "group": 8, "mean_len": 8192, "tokens": 4 * 1024 * 1024}
 
 
 # Model shapes (out_features, in_features) of one decoder layer's linears.

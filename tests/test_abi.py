@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "nvfp4_quantize_batch", "rmsnorm_aqn",
-                     "nvfp4_quantize_record", "nvfp4_quantize_cached",
+                     "nvfp4_quantize_record", "nvfp4_quantize_cached", "ais_mixing",
                      "rmsnorm_aqn_quantize", "nvfp4_lora_linear",
                      "nvfp4_lora_linear_w4a4", "aqn_sigma"):
         assert required in names
@@ -110,6 +110,29 @@ def test_quantize_cached_validation(nv):
     assert cac(A0, 0, 4, 32, A5, A2, A3, A5, None) == 7        # codes over the mask
     assert cac(A0, 0, 4, 32, A5, A2, A3, A2, None) == 7        # codes over the scales
     assert cac(A0, 0, 0, 32, None, None, None, None, None) == 0  # empty: nothing to do
+
+
+def test_ais_validation(nv):
+    ais = nv.lib().ais_mixing
+    W = 0x90000  # workspace
+    wsb = nv.workspace_bytes(nv.OP_AIS, 0, 0, 0)
+    assert wsb >= 1024 * 64
+    ok = dict(lr=A0, lt=A1, adv=A2, n=64, C=2.0, d=0.05, g=0.5, b=1.0, w=A3, st=A4, ws=W, wsb=wsb)
+
+    def call(**k):
+        a = {**ok, **k}
+        return ais(a["lr"], a["lt"], a["adv"], a["n"], a["C"], a["d"], a["g"], a["b"], a["w"], a["st"], a["ws"],
+                   a["wsb"], None)
+    assert call(n=-1) == 1
+    assert call(n=0, lr=None) == 0                  # empty batch: nothing to do
+    assert call(C=0.0) == 1 and call(d=-1.0) == 1 and call(g=0.0) == 1 and call(b=-0.5) == 1
+    assert call(C=float("inf")) == 1 and call(b=float("nan")) == 1
+    assert call(adv=None) == 1 and call(st=None) == 1
+    assert call(lt=A1 + 4) == 2 and call(w=A3 + 8) == 2 and call(st=A4 + 4) == 2
+    assert call(ws=None) == 4 and call(wsb=16) == 4
+    assert call(w=A0 + 64) == 7                     # weights over an input
+    assert call(st=A3 + 8) == 7                     # statistics over the weights
+    assert call(ws=A2) == 7                         # workspace over an input
 
 
 def _qb(nv, n=2, xs=(A0, A0 + 0x1000), rows=(4, 8), cols=(32, 64), dtype=0, codes=(A1, A1 + 0x1000),

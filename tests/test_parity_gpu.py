@@ -293,6 +293,63 @@ def test_trace_round_trip_gpu_only_qwen7b_gate(nv):
         assert np.array_equal(rec_h[r * k // 32:(r + 1) * k // 32], mr), f"row {r}: record bits differ"
 
 
+# ---------------------------------------------------------------- AIS mixing coefficient
+
+AIS_ABS = ("alpha", "alpha_ess", "alpha_mis", "alpha_var", "cv2", "dsigma")  # dimensionless: 1e-5 absolute
+AIS_REL = ("dbar", "mean_w")                                                 # 1e-5 relative
+
+
+def gpu_ais(nv, lr, lt, adv, C, delta, gamma, beta):
+    st, w = nv.ais_mixing(P.dev(lr), P.dev(lt), P.dev(adv), C, delta, gamma, beta)
+    torch.cuda.synchronize()
+    return dict(zip(nv.AIS_STATS, st.cpu().numpy().tolist())), w.cpu().numpy()
+
+
+def assert_ais_close(got, want, C, what=""):
+    (sg, wg), (sr, wr) = got, want
+    for k in AIS_ABS:
+        assert abs(sg[k] - sr[k]) <= 1e-5, f"{what}: {k} {sg[k]!r} vs {sr[k]!r}"
+    for k in AIS_REL:
+        assert abs(sg[k] - sr[k]) <= 1e-5 * abs(sr[k]) + 1e-12, f"{what}: {k} {sg[k]!r} vs {sr[k]!r}"
+    err = np.abs(wg.astype(np.float64) - wr)
+    assert err.max(initial=0.0) <= 1e-5 * (1 + C), f"{what}: weight error {err.max()}"
+
+
+@pytest.mark.parametrize("n", [1, 3, 5, 1000, 4099, 65537, 300001])
+def test_ais_sizes(nv, n):
+    lr, lt, adv = synth.grpo_token_batch(8, 8, 512, 21, n, max_tokens=n)
+    if lr.size < n:  # short batches: repeat the generated tokens
+        reps = -(-n // lr.size)
+        lr, lt, adv = (np.tile(a, reps)[:n].copy() for a in (lr, lt, adv))
+    args = (2.0, 0.05, 0.5, 1.0)
+    assert_ais_close(gpu_ais(nv, lr, lt, adv, *args), oracle.ais(lr, lt, adv, *args), 2.0, f"n={n}")
+
+
+def test_ais_grpo_batch_full(nv):
+    """The full GRPO batch (64 prompts x 8 responses of ~8K tokens, ~4 M tokens), every weight,
+    for parameters where each factor of alpha is active."""
+    b = synth.GRPO_BATCH
+    lr, lt, adv = synth.grpo_token_batch(b["prompts"], b["group"], b["mean_len"], 22, max_tokens=b["tokens"])
+    for args in [(2.0, 0.05, 0.5, 1.0), (1.05, 0.01, 1e-4, 0.5), (5.0, 1.0, 2e-3, 3.0)]:
+        assert_ais_close(gpu_ais(nv, lr, lt, adv, *args), oracle.ais(lr, lt, adv, *args), args[0], f"{args}")
+
+
+def test_ais_degenerate_batches(nv):
+    """No mismatch (alpha = 0: every weight exactly 1), constant advantages (dsigma = 0), every
+    ratio above C (all weights C), and a penalty that clips alpha to 0."""
+    lr, lt, adv = synth.grpo_token_batch(4, 8, 256, 23, max_tokens=5000)
+    st, w = gpu_ais(nv, lr, lr, adv, 2.0, 0.05, 0.5, 1.0)
+    assert st["alpha"] == 0.0 and st["dbar"] == 0.0 and np.all(w == 1.0)
+    const = np.full_like(adv, 0.75)
+    assert_ais_close(gpu_ais(nv, lr, lt, const, 2.0, 0.05, 0.5, 1.0), oracle.ais(lr, lt, const, 2.0, 0.05, 0.5, 1.0),
+                     2.0, "constant advantages")
+    hi = (lr + 3.0).astype(np.float32)
+    st, w = gpu_ais(nv, lr, hi, adv, 2.0, 0.05, 100.0, 1.0)
+    assert st["mean_w"] == 2.0 and st["cv2"] == 0.0 and np.all(w == np.float32(1 + st["alpha"] * 1.0))
+    clip = gpu_ais(nv, lr, (lr + np.float32(np.log(4.0))).astype(np.float32), adv, 100.0, 0.01, 0.5, 2.0)
+    assert clip[0]["alpha"] == 0.0 and np.all(clip[1] == 1.0)
+
+
 # ---------------------------------------------------------------- RMSNorm with AQN
 
 def gpu_rmsnorm(nv, x, w, eps, sigma, delta):
