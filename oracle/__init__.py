@@ -60,6 +60,7 @@ def _declare(lib):
         "oracle_e2m1_round_up": (i, [d, d]),
         "oracle_quantize_cached_rows": (None, [p, i, i64, i64, i64, f, p, p, p]),
         "oracle_ais": (None, [i64, p, p, p, d, d, d, d, p, p]),
+        "oracle_attention_decode": (None, [p, p, p, f, p, p, f, p, i64, i64, i64, i64, i64, d, p]),
         "oracle_aqn_sigma": (d, [d, d, i64, i64]),
         "oracle_rmsnorm_aqn_rows": (None, [p, i64, i64, i64, p, p, f, f, p]),
         "oracle_lora_down": (None, [p, i64, i64, p, i32, p]),
@@ -227,6 +228,40 @@ def quantize_cached(x: np.ndarray, mask: np.ndarray, scales: np.ndarray, g: floa
                                                       _ptr(scales), _ptr(mask), _ptr(codes))
     _parallel(fn, rows, nthreads)
     return codes
+
+
+def kv_quantize(x_bits: np.ndarray, g: float, L=None):
+    """NVFP4 encoding of KV rows (bf16 bits [..., D], D % 16 == 0) with a given per-tensor g:
+    (codes [..., D/2], scales [..., D/16])."""
+    L = L or lib()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    D = x.shape[-1]
+    rows = x.size // D
+    codes = np.zeros(x.shape[:-1] + (D // 2,), np.uint8)
+    scales = np.zeros(x.shape[:-1] + (D // 16,), np.uint8)
+    _parallel(lambda r0, r1: L.oracle_quantize_rows(_ptr(x), BF16, D, r0, r1, float(np.float32(g)), _ptr(codes),
+                                                    _ptr(scales)), rows)
+    return codes, scales
+
+
+def attention_decode(q_bits, k_codes, k_scales, gk, v_codes, v_scales, gv, lens, scale, L=None):
+    """Decode attention over an NVFP4 KV cache in fp64: q [B, Hq, D] bf16 bits; caches [B, Lmax, Hkv, D/2]
+    codes and [B, Lmax, Hkv, D/16] scales; lens [B] -> out [B, Hq, D] float64."""
+    L = L or lib()
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    B, Hq, D = q.shape
+    Lmax, Hkv = k_codes.shape[1], k_codes.shape[2]
+    kc, ks, vc, vs = (np.ascontiguousarray(a, dtype=np.uint8) for a in (k_codes, k_scales, v_codes, v_scales))
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    assert Hq % Hkv == 0 and D % 16 == 0 and lens.size == B and np.all((lens > 0) & (lens <= Lmax))
+    out = np.zeros((B, Hq, D))
+
+    def part(b0, b1):
+        L.oracle_attention_decode(_ptr(q[b0:b1]), _ptr(kc[b0:b1]), _ptr(ks[b0:b1]), float(np.float32(gk)),
+                                  _ptr(vc[b0:b1]), _ptr(vs[b0:b1]), float(np.float32(gv)), _ptr(lens[b0:b1]),
+                                  b1 - b0, Hq, Hkv, D, Lmax, float(scale), _ptr(out[b0:b1]))
+    _parallel(part, B)
+    return out
 
 
 AIS_STATS = ("alpha", "alpha_ess", "alpha_mis", "alpha_var", "dbar", "cv2", "dsigma", "mean_w")

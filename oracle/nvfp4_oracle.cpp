@@ -20,6 +20,12 @@
 //    an exponential noise schedule (section "AQNの仕組み").
 //  * LoRA linear: Y = x deq(W)^T + s (x A^T) B^T (QeRL explainer, section
 //    "NVFP4量子化とLoRA": frozen quantized base plus low-rank trainable factors).
+//  * FP4 KV cache (TRACE summary, section "実験結果と性能": rollouts with FP4 weights,
+//    activations and KV cache): every cached key/value row of a head is NVFP4-encoded
+//    like any tensor (16-element blocks along the head dimension, E4M3 block scales)
+//    with a per-tensor g given by the caller, and decode attention reads the dequantized
+//    rows: out = softmax(scale q K^T) V over the sequence's cached tokens, query head h
+//    reading KV head h / (Hq / Hkv) (grouped-query attention).
 //  * AIS mixing coefficient (AIS summary, section 2.1 "混合係数": alpha_ess from the
 //    coefficient of variation of the truncated weights, alpha_mis from the mean
 //    absolute log-prob mismatch and a saturation threshold delta, alpha_var from a
@@ -252,6 +258,42 @@ void oracle_dequantize_rows(const uint8_t* codes, const uint8_t* scales, float g
       const int64_t idx = r * cols + k;
       const int c = (codes[idx / 2] >> ((idx & 1) * 4)) & 15;
       out[idx] = e2m1_value(c) * e4m3_value(scales[r * nblk + k / 16]) * static_cast<double>(g);
+    }
+}
+
+// Decode attention over an NVFP4 KV cache, in fp64. q: [B][Hq][D] bf16 bits; caches: codes
+// [B][Lmax][Hkv][D/2], scales [B][Lmax][Hkv][D/16] for K and V, with per-tensor scales gk, gv;
+// lens[b] tokens of sequence b are attended (0 < lens[b] <= Lmax); out: [B][Hq][D] doubles.
+void oracle_attention_decode(const uint16_t* q, const uint8_t* kc, const uint8_t* ks, float gk, const uint8_t* vc,
+                             const uint8_t* vs, float gv, const int32_t* lens, int64_t B, int64_t Hq, int64_t Hkv,
+                             int64_t D, int64_t Lmax, double scale, double* out) {
+  const int64_t group = Hq / Hkv;
+  const auto deq = [&](const uint8_t* codes, const uint8_t* scales, float g, int64_t row, int64_t d) {
+    const int c = (codes[row * (D / 2) + d / 2] >> ((d & 1) * 4)) & 15;
+    return e2m1_value(c) * e4m3_value(scales[row * (D / 16) + d / 16]) * static_cast<double>(g);
+  };
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t h = 0; h < Hq; ++h) {
+      const int64_t kvh = h / group, L = lens[b];
+      std::vector<double> sc(L);
+      double mx = -INFINITY;
+      for (int64_t t = 0; t < L; ++t) {
+        const int64_t row = (b * Lmax + t) * Hkv + kvh;
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d) dot += bf16_value(q[(b * Hq + h) * D + d]) * deq(kc, ks, gk, row, d);
+        sc[t] = scale * dot;
+        mx = std::fmax(mx, sc[t]);
+      }
+      double den = 0.0;
+      for (int64_t t = 0; t < L; ++t) {
+        sc[t] = std::exp(sc[t] - mx);
+        den += sc[t];
+      }
+      for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < L; ++t) acc += sc[t] * deq(vc, vs, gv, (b * Lmax + t) * Hkv + kvh, d);
+        out[(b * Hq + h) * D + d] = acc / den;
+      }
     }
 }
 

@@ -54,6 +54,11 @@ MUTANTS = {
     "ais_mis_unsaturated": ("const double a_mis = std::fmin(1.0, dbar / delta);", "const double a_mis = dbar / delta;"),
     "ais_dsigma_raw_ratio": ("std::sqrt(vwa) / std::sqrt(va) - 1.0", "std::sqrt(vwa) / std::sqrt(va)"),
     "ais_rectified_weight": ("w_out[i] = 1.0 + alpha * (w[i] - 1.0);", "w_out[i] = alpha * w[i];"),
+    "attn_gqa_modulo": ("const int64_t kvh = h / group, L = lens[b];", "const int64_t kvh = h % Hkv, L = lens[b];"),
+    "attn_scale_dropped": ("sc[t] = scale * dot;", "sc[t] = dot;"),
+    "attn_length_off_by_one": ("for (int64_t t = 0; t < L; ++t) acc += sc[t]", "for (int64_t t = 1; t < L; ++t) acc += sc[t]"),
+    "attn_v_with_k_scales": ("acc += sc[t] * deq(vc, vs, gv,", "acc += sc[t] * deq(vc, ks, gv,"),
+    "attn_unnormalised": ("out[(b * Hq + h) * D + d] = acc / den;", "out[(b * Hq + h) * D + d] = acc;"),
     "cached_mask_shifted": ("        const int up = (mask[idx / 32] >> (idx % 32)) & 1;\n        const int c = e2m1_encode_guided(load_elem",
                             "        const int up = (mask[idx / 32] >> ((idx + 1) % 32)) & 1;\n        const int c = e2m1_encode_guided(load_elem"),
 }
@@ -173,6 +178,20 @@ def _battery(L):
             oracle.ais = real
         return True
     check("ais", ais_cases)
+
+    def attention():
+        from tests import test_oracle_attention as T
+        real_a, real_q = oracle.attention_decode, oracle.kv_quantize
+        oracle.attention_decode = lambda *a, **k: real_a(*a, **{**k, "L": L})
+        oracle.kv_quantize = lambda *a, **k: real_q(*a, **{**k, "L": L})
+        try:
+            T.test_matches_torch_sdpa_in_float64(2, 4, 2, 64, 9)
+            T.test_one_token_returns_its_value_row()
+            T.test_scale_and_per_tensor_scales_enter_as_stated()
+        finally:
+            oracle.attention_decode, oracle.kv_quantize = real_a, real_q
+        return True
+    check("attention", attention)
 
     def linear():
         N, K, M, r = 5, 64, 3, 2
