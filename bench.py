@@ -682,6 +682,31 @@ def run_suite(args):
                                        "counted, for comparison"})
         del x, w, z, y, c, sc, g, wsq
         torch.cuda.empty_cache()
+    # ---- decode attention over an NVFP4 KV cache (Qwen2.5-7B heads: 28 query / 4 KV, 128 dims)
+    if want("kv_attention"):
+        B_, Hq_, Hkv_, D_, L_ = 64, 28, 4, 128, 8192
+        gen = torch.Generator(device=dev).manual_seed(35)
+        kc_ = torch.randint(0, 256, (B_, L_, Hkv_, D_ // 2), generator=gen, device=dev, dtype=torch.int32).to(torch.uint8)
+        vc_ = torch.randint(0, 256, (B_, L_, Hkv_, D_ // 2), generator=gen, device=dev, dtype=torch.int32).to(torch.uint8)
+        ks_ = torch.randint(0x28, 0x40, (B_, L_, Hkv_, D_ // 16), generator=gen, device=dev,
+                            dtype=torch.int32).to(torch.uint8)
+        vs_ = torch.randint(0x28, 0x40, (B_, L_, Hkv_, D_ // 16), generator=gen, device=dev,
+                            dtype=torch.int32).to(torch.uint8)
+        lens_h = np.random.default_rng(35).integers(4096, L_ + 1, B_).astype(np.int32)
+        lens_d = torch.from_numpy(lens_h).to(dev)
+        q_ = (torch.randn(B_, Hq_, D_, generator=gen, device=dev)).to(torch.bfloat16)
+        g_ = torch.tensor([1.0 / 64], dtype=torch.float32, device=dev)
+        out_ = torch.empty(B_, Hq_, D_, dtype=torch.bfloat16, device=dev)
+        ws_ = torch.empty(max(16, nv.workspace_bytes(nv.OP_KV_ATTENTION, B_, Hkv_, L_)), dtype=torch.uint8, device=dev)
+        us_k = timed(lambda: nv.nvfp4_kv_decode_attention(q_, kc_, ks_, g_, vc_, vs_, g_, lens_d, 1.0 / np.sqrt(D_),
+                                                          out=out_, workspace=ws_), 10)
+        kv_bytes = int(lens_h.sum()) * Hkv_ * (D_ // 2 + D_ // 16) * 2 + 2 * B_ * Hq_ * D_ * 2
+        emit("kv_decode_attention_7b_b64_l8192", us_k, 0, kv_bytes, "hbm",
+             {"shape": {"B": B_, "Hq": Hq_, "Hkv": Hkv_, "D": D_, "Lmax": L_, "tokens": int(lens_h.sum())},
+              "note": "nvfp4_kv_decode_attention: random valid NVFP4 cache bytes, lengths 4096..8192; bytes: "
+                      "the attended K and V rows (codes + scales), q and out"})
+        del kc_, vc_, ks_, vs_, q_, out_, ws_
+        torch.cuda.empty_cache()
     # ---- AIS mixing coefficient and rectified weights of a GRPO training batch (~4 M tokens)
     if want("ais"):
         import synth

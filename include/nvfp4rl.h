@@ -67,7 +67,8 @@ enum {
   NVFP4RL_OP_LINEAR_W4A4 = 2,
   NVFP4RL_OP_QUANTIZE_BATCH = 3, /* M = number of tensors */
   NVFP4RL_OP_RMSNORM_QUANTIZE = 4,
-  NVFP4RL_OP_AIS = 5
+  NVFP4RL_OP_AIS = 5,
+  NVFP4RL_OP_KV_ATTENTION = 6 /* M = B, N = Hkv, K = Lmax */
 };
 
 /*
@@ -216,6 +217,55 @@ NVFP4RL_API nvfp4rl_status nvfp4_quantize_cached(const void* x, int32_t dtype, i
 NVFP4RL_API nvfp4rl_status ais_mixing(const float* logp_rollout, const float* logp_train, const float* adv,
                                       int64_t n, float C, float delta, float gamma, float beta, float* w_out,
                                       double* stats, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * nvfp4_kv_append -- writes one token's keys and values per sequence into an NVFP4 KV cache (TRACE
+ *   summary, "実験結果と性能": rollouts with FP4 weights, activations and KV cache). Each new row of
+ *   a head is encoded like nvfp4_quantize with the per-tensor scale *gk (keys) or *gv (values) as
+ *   given (a calibrated constant: a growing cache cannot re-derive g from its amax):
+ *   cache row (b, pos[b], h) = NVFP4(k[b][h][:]) and likewise for v.
+ * Arguments:
+ *   k, v     device bf16 [B][Hkv][D], 16-byte aligned; D a multiple of 16.
+ *   pos      device int32 [B]: the cache row of each sequence's new token; a sequence whose pos is
+ *            outside [0, Lmax) is skipped (nothing written for it).
+ *   gk, gv   device fp32 scalars (g <= 0 or NaN: every code is sign|0, every scale byte 0).
+ *   k_codes, v_codes   device [B][Lmax][Hkv][D/2] bytes; k_scales, v_scales [B][Lmax][Hkv][D/16]
+ *            E4M3 bytes; all 16-byte aligned. Only the rows (b, pos[b], *) are written.
+ * Errors: NVFP4RL_ERR_INVALID_ARG (negative sizes, NULL pointers), NVFP4RL_ERR_UNSUPPORTED_SHAPE
+ *   (D % 16), NVFP4RL_ERR_MISALIGNED, NVFP4RL_ERR_ALIAS (a cache overlapping an input or another
+ *   cache array).
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_kv_append(const uint16_t* k, const uint16_t* v, int64_t B, int64_t Hkv, int64_t D,
+                                           const int32_t* pos, const float* gk, const float* gv, uint8_t* k_codes,
+                                           uint8_t* k_scales, uint8_t* v_codes, uint8_t* v_scales, int64_t Lmax,
+                                           void* stream);
+
+/*
+ * nvfp4_kv_decode_attention -- one decode step of attention over an NVFP4 KV cache:
+ *   out[b][h] = softmax(scale * q[b][h] . K^[b, t, h / (Hq/Hkv)]) . V^[b, t, h / (Hq/Hkv)] over
+ *   t < lens[b], K^ and V^ the dequantized cache rows (E2M1 x E4M3(s) x g).
+ * Arguments:
+ *   q        device bf16 [B][Hq][D], 16-byte aligned; D must be 128; Hq a multiple of Hkv with
+ *            Hq / Hkv <= 16; B * Hkv <= 65535.
+ *   k_codes, k_scales, v_codes, v_scales  the cache as nvfp4_kv_append writes it; gk, gv its scales.
+ *   lens     device int32 [B]: tokens attended per sequence, clamped to [0, Lmax]; 0 gives zeros.
+ *   scale    softmax scale (typically 1/sqrt(D)), finite.
+ *   out      device bf16 [B][Hq][D], 16-byte aligned; may overlap no input.
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_KV_ATTENTION, B, Hkv, Lmax, 0, 0) bytes (may be 0
+ *            and NULL), device, 16-byte aligned; scratch.
+ * Scores and the softmax are fp32 (exp2 on scores prescaled by log2 e); the products P V take P
+ *   rounded to bf16; K and V are dequantized exactly (bf16). Long caches are split into spans
+ *   merged by a second kernel.
+ * Errors: NVFP4RL_ERR_INVALID_ARG, NVFP4RL_ERR_UNSUPPORTED_SHAPE, NVFP4RL_ERR_MISALIGNED,
+ *   NVFP4RL_ERR_WORKSPACE, NVFP4RL_ERR_ALIAS.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_kv_decode_attention(const uint16_t* q, const uint8_t* k_codes,
+                                                     const uint8_t* k_scales, const float* gk,
+                                                     const uint8_t* v_codes, const uint8_t* v_scales,
+                                                     const float* gv, const int32_t* lens, int64_t B, int64_t Hq,
+                                                     int64_t Hkv, int64_t D, int64_t Lmax, float scale,
+                                                     uint16_t* out, void* workspace, size_t workspace_bytes,
+                                                     void* stream);
 
 /*
  * aqn_sigma -- AQN exponential noise schedule (QeRL explainer, "AQNの仕組み":

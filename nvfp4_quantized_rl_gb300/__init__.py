@@ -8,7 +8,8 @@ importing the binding does not build it, and every call fails loudly when the
 library or a GPU is missing -- there is no CPU fallback.
 
 Functions carry the C names: nvfp4_amax, nvfp4_quantize, nvfp4_quantize_guided,
-nvfp4_quantize_record, nvfp4_quantize_cached, nvfp4_quantize_batch, ais_mixing, aqn_sigma, rmsnorm_aqn, rmsnorm_aqn_quantize, nvfp4_lora_linear,
+nvfp4_quantize_record, nvfp4_quantize_cached, nvfp4_quantize_batch, nvfp4_kv_append,
+nvfp4_kv_decode_attention, ais_mixing, aqn_sigma, rmsnorm_aqn, rmsnorm_aqn_quantize, nvfp4_lora_linear,
 nvfp4_lora_linear_w4a4.
 """
 from __future__ import annotations
@@ -23,7 +24,8 @@ LIB_PATH = _build.LIB
 
 OK = 0
 BF16, F32 = 0, 1
-OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH, OP_RMSNORM_QUANTIZE, OP_AIS = 0, 1, 2, 3, 4, 5
+OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH, OP_RMSNORM_QUANTIZE, OP_AIS, OP_KV_ATTENTION = (
+    0, 1, 2, 3, 4, 5, 6)
 
 _lock = threading.Lock()
 _lib = None
@@ -41,6 +43,9 @@ def _signatures():
         "nvfp4_quantize_guided": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
         "nvfp4_quantize_record": (c.c_int, [p, i32, i64, i64, p, p, p, p, p, p, sz, p]),
         "nvfp4_quantize_cached": (c.c_int, [p, i32, i64, i64, p, p, p, p, p]),
+        "nvfp4_kv_append": (c.c_int, [p, p, i64, i64, i64, p, p, p, p, p, p, p, i64, p]),
+        "nvfp4_kv_decode_attention": (c.c_int, [p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c.c_float, p, p,
+                                                 sz, p]),
         "ais_mixing": (c.c_int, [p, p, p, i64, c.c_float, c.c_float, c.c_float, c.c_float, p, p, p, sz, p]),
         "nvfp4_quantize_batch": (c.c_int, [i32, p, p, p, i32, p, p, p, p, sz, p]),
         "aqn_sigma": (f64, [f64, f64, i64, i64]),
@@ -193,6 +198,40 @@ def nvfp4_quantize_cached(x, mask, scales, g, codes=None, stream=None):
                                      _stream(x, stream))
     _check(st, "nvfp4_quantize_cached")
     return codes
+
+
+def nvfp4_kv_append(k, v, pos, gk, gv, k_codes, k_scales, v_codes, v_scales, stream=None):
+    """Writes one token's keys and values per sequence (bf16 [B, Hkv, D]) into an NVFP4 KV cache at
+    rows pos [B] (int32): caches are uint8 [B, Lmax, Hkv, D/2] codes and [B, Lmax, Hkv, D/16] scales;
+    gk, gv fp32 [1] CUDA tensors."""
+    _require_cuda(k, v, pos, gk, gv, k_codes, k_scales, v_codes, v_scales)
+    _bits16(k)
+    _bits16(v)
+    B, Hkv, D = k.shape
+    Lmax = k_codes.shape[1]
+    st = lib().nvfp4_kv_append(_ptr(k), _ptr(v), B, Hkv, D, _ptr(pos), _ptr(gk), _ptr(gv), _ptr(k_codes),
+                               _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), Lmax, _stream(k, stream))
+    _check(st, "nvfp4_kv_append")
+
+
+def nvfp4_kv_decode_attention(q, k_codes, k_scales, gk, v_codes, v_scales, gv, lens, scale, out=None,
+                              workspace=None, stream=None):
+    """One decode step of attention over an NVFP4 KV cache: q bf16 [B, Hq, 128] -> out bf16 [B, Hq, 128]."""
+    import torch
+    _require_cuda(q, k_codes, k_scales, gk, v_codes, v_scales, gv, lens, out, workspace)
+    _bits16(q)
+    B, Hq, D = q.shape
+    Lmax, Hkv = k_codes.shape[1], k_codes.shape[2]
+    out = _empty((B, Hq, D), torch.bfloat16, q.device) if out is None else out
+    need = workspace_bytes(OP_KV_ATTENTION, B, Hkv, Lmax)
+    if workspace is None and need > 0:
+        workspace = _empty((need,), torch.uint8, q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().nvfp4_kv_decode_attention(_ptr(q), _ptr(k_codes), _ptr(k_scales), _ptr(gk), _ptr(v_codes),
+                                         _ptr(v_scales), _ptr(gv), _ptr(lens), B, Hq, Hkv, D, Lmax, float(scale),
+                                         _ptr(out), _ptr(workspace), wsb, _stream(q, stream))
+    _check(st, "nvfp4_kv_decode_attention")
+    return out
 
 
 AIS_STATS = ("alpha", "alpha_ess", "alpha_mis", "alpha_var", "dbar", "cv2", "dsigma", "mean_w")

@@ -249,6 +249,66 @@ nvfp4rl_status ais_mixing(const float* lr, const float* lt, const float* adv, in
                     static_cast<cudaStream_t>(stream));
 }
 
+nvfp4rl_status nvfp4_kv_append(const uint16_t* k, const uint16_t* v, int64_t B, int64_t Hkv, int64_t D,
+                               const int32_t* pos, const float* gk, const float* gv, uint8_t* kc, uint8_t* ks,
+                               uint8_t* vc, uint8_t* vs, int64_t Lmax, void* stream) {
+  if (B < 0 || Hkv <= 0 || D <= 0 || Lmax <= 0) return NVFP4RL_ERR_INVALID_ARG;
+  if (D % 16 != 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return NVFP4RL_OK;
+  if (!k || !v || !pos || !gk || !gv || !kc || !ks || !vc || !vs) return NVFP4RL_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(ks) || !aligned16(vc) || !aligned16(vs) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u) || (reinterpret_cast<uintptr_t>(gk) & 3u) ||
+      (reinterpret_cast<uintptr_t>(gv) & 3u))
+    return NVFP4RL_ERR_MISALIGNED;
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(Lmax) * static_cast<size_t>(Hkv);
+  const size_t in_b = static_cast<size_t>(B) * Hkv * D * 2;
+  std::vector<std::pair<uintptr_t, uintptr_t>> outs, ins;
+  const auto rng = [](const void* p, size_t n) {
+    return std::make_pair(reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + n);
+  };
+  outs = {rng(kc, rows * (D / 2)), rng(ks, rows * (D / 16)), rng(vc, rows * (D / 2)), rng(vs, rows * (D / 16))};
+  ins = {rng(k, in_b), rng(v, in_b), rng(pos, static_cast<size_t>(B) * 4), rng(gk, 4), rng(gv, 4)};
+  if (any_overlap(outs)) return NVFP4RL_ERR_ALIAS;
+  std::sort(outs.begin(), outs.end());
+  for (const auto& r : ins)
+    if (hits(outs, r.first, r.second)) return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_kv_append(k, v, B, Hkv, D, pos, gk, gv, kc, ks, vc, vs, Lmax, dev, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4rl_status nvfp4_kv_decode_attention(const uint16_t* q, const uint8_t* kc, const uint8_t* ks, const float* gk,
+                                         const uint8_t* vc, const uint8_t* vs, const float* gv, const int32_t* lens,
+                                         int64_t B, int64_t Hq, int64_t Hkv, int64_t D, int64_t Lmax, float scale,
+                                         uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || !std::isfinite(scale)) return NVFP4RL_ERR_INVALID_ARG;
+  if (D != 128 || Hq % Hkv != 0 || Hq / Hkv > 16 || B * Hkv > 65535) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return NVFP4RL_OK;
+  if (!q || !kc || !ks || !gk || !vc || !vs || !gv || !lens || !out) return NVFP4RL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(ks) || !aligned16(vc) || !aligned16(vs) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(gk) & 3u) || (reinterpret_cast<uintptr_t>(gv) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lens) & 3u))
+    return NVFP4RL_ERR_MISALIGNED;
+  const size_t need = attention_workspace_bytes(B, Hkv, Lmax);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return NVFP4RL_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return NVFP4RL_ERR_MISALIGNED;
+  }
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(Lmax) * static_cast<size_t>(Hkv);
+  const size_t ob = static_cast<size_t>(B) * Hq * D * 2;
+  const void* ins[9] = {q, kc, ks, vc, vs, gk, gv, lens, workspace};
+  const size_t isz[9] = {ob, rows * (D / 2), rows * (D / 16), rows * (D / 2), rows * (D / 16), 4, 4,
+                         static_cast<size_t>(B) * 4, need};
+  for (int i = 0; i < 9; ++i)
+    if (ins[i] && isz[i] && overlap(out, ob, ins[i], isz[i])) return NVFP4RL_ERR_ALIAS;
+  DeviceInfo dev;
+  nvfp4rl_status st = current_device(&dev);
+  if (st != NVFP4RL_OK) return st;
+  return launch_kv_attention(q, kc, ks, gk, vc, vs, gv, lens, B, Hq, Hkv, Lmax, scale, out, workspace, dev,
+                             static_cast<cudaStream_t>(stream));
+}
+
 nvfp4rl_status nvfp4_quantize_batch(int32_t count, const void* const* x, const int64_t* rows, const int64_t* cols,
                                     int32_t dtype, uint8_t* const* codes, uint8_t* const* scales, float* const* g,
                                     void* workspace, size_t workspace_bytes, void* stream) {
@@ -368,6 +428,7 @@ size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int3
     case NVFP4RL_OP_QUANTIZE_BATCH: return M <= kQuantizeBatchMax ? quantize_batch_workspace_bytes(M) : 0;
     case NVFP4RL_OP_RMSNORM_QUANTIZE: return kQuantizeWorkspace;
     case NVFP4RL_OP_AIS: return ais_workspace_bytes();
+    case NVFP4RL_OP_KV_ATTENTION: return N > 0 && K > 0 ? attention_workspace_bytes(M, N, K) : 0;
     case NVFP4RL_OP_LINEAR_W4A16: return linear_workspace_bytes(false, M, N, K, r, 1);
     case NVFP4RL_OP_LINEAR_W4A4: return linear_workspace_bytes(true, M, N, K, r, num_groups > 0 ? num_groups : 1);
     default: return 0;

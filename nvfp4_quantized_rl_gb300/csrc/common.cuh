@@ -136,6 +136,18 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
                                uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done = false,
                                uint32_t* record = nullptr);
 
+// NVFP4 KV cache: append one token's rows per sequence (quantize.cu) and decode attention over the
+// cache (attention.cu, head dimension 128).
+nvfp4rl_status launch_kv_append(const uint16_t* k, const uint16_t* v, int64_t B, int64_t Hkv, int64_t D,
+                                const int32_t* pos, const float* gk, const float* gv, uint8_t* kc, uint8_t* ks,
+                                uint8_t* vc, uint8_t* vs, int64_t Lmax, const DeviceInfo& dev, cudaStream_t st);
+int attention_splits(int64_t B, int64_t Hkv, int64_t Lmax);
+size_t attention_workspace_bytes(int64_t B, int64_t Hkv, int64_t Lmax);
+nvfp4rl_status launch_kv_attention(const uint16_t* q, const uint8_t* kc, const uint8_t* ks, const float* gk,
+                                   const uint8_t* vc, const uint8_t* vs, const float* gv, const int32_t* lens,
+                                   int64_t B, int64_t Hq, int64_t Hkv, int64_t Lmax, float scale, uint16_t* out,
+                                   void* workspace, const DeviceInfo& dev, cudaStream_t st);
+
 // AIS mixing coefficient and rectified weights of n tokens (ais.cu); workspace: a barrier counter
 // and one slot of partial sums per CTA (at most kAisMaxCtas CTAs).
 constexpr int kAisMaxCtas = 1024;

@@ -931,6 +931,37 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
   }
 }
 
+// Appends one token's K and V rows per sequence to an NVFP4 KV cache: block i of the 2 B Hkv D/16
+// blocks (K first, then V) of the new rows [B][Hkv][D] is encoded with the given per-tensor g and
+// written to row (b, pos[b], h) of the cache ([B][Lmax][Hkv][D/2] codes, [B][Lmax][Hkv][D/16]
+// scales). Sequences whose pos is outside [0, Lmax) are skipped.
+__global__ void __launch_bounds__(256) kv_append_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                                                        int64_t B, int64_t Hkv, int64_t D,
+                                                        const int32_t* __restrict__ pos, const float* __restrict__ gk,
+                                                        const float* __restrict__ gv, uint8_t* __restrict__ kc,
+                                                        uint8_t* __restrict__ ks, uint8_t* __restrict__ vc,
+                                                        uint8_t* __restrict__ vs, int64_t Lmax) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t nb = D / 16, per = B * Hkv * nb;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < 2 * per; i += stride) {
+    const bool is_v = i >= per;
+    const int64_t j = is_v ? i - per : i;
+    const int64_t blk = j % nb, bh = j / nb, b = bh / Hkv, h = bh % Hkv;
+    const int64_t p = pos[b];
+    if (p < 0 || p >= Lmax) continue;
+    const float g = is_v ? *gv : *gk;
+    const float est_scale = g < 0x1p-60f ? 0x1p64f : 1.0f;  // as in quantize_kernel
+    const float g6 = 6.0f * (g * est_scale);
+    BlockWords<NVFP4RL_BF16> w;
+    load_block<NVFP4RL_BF16>((is_v ? v : k) + bh * D, blk, w);
+    const int64_t row = (b * Lmax + p) * Hkv + h;
+    encode_block<NVFP4RL_BF16, kModePlain>(w, blk, g, est_scale, g6, nullptr, (is_v ? vc : kc) + row * (D / 2),
+                                           (is_v ? vs : ks) + row * nb, nullptr, nullptr);
+  }
+}
+
 // Clears the amax accumulator word (a kernel rather than a memset, so that it chains with the
 // neighbouring kernels by programmatic dependent launch).
 __global__ void zero_word_kernel(uint32_t* __restrict__ p) {
@@ -1063,6 +1094,18 @@ nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t c
              : launch_encode_dtype<kModePlain>(dtype, nblocks, dev, st, x, amax_scratch, amax_in, nullptr, codes,
                                                scales, g, nullptr, nullptr, nullptr);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  return launch_status();
+}
+
+nvfp4rl_status launch_kv_append(const uint16_t* k, const uint16_t* v, int64_t B, int64_t Hkv, int64_t D,
+                                const int32_t* pos, const float* gk, const float* gv, uint8_t* kc, uint8_t* ks,
+                                uint8_t* vc, uint8_t* vs, int64_t Lmax, const DeviceInfo& dev, cudaStream_t st) {
+  const int64_t n = 2 * B * Hkv * (D / 16);
+  if (n == 0) return NVFP4RL_OK;
+  const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(dev.sm_count) * 8));
+  if (launch_pdl(kv_append_kernel, dim3(grid), dim3(256), 0, st, k, v, B, Hkv, D, pos, gk, gv, kc, ks, vc, vs, Lmax) !=
+      cudaSuccess)
+    return NVFP4RL_ERR_CUDA;
   return launch_status();
 }
 

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     for required in ("nvfp4_quantize", "nvfp4_quantize_guided", "nvfp4_quantize_batch", "rmsnorm_aqn",
-                     "nvfp4_quantize_record", "nvfp4_quantize_cached", "ais_mixing",
+                     "nvfp4_quantize_record", "nvfp4_quantize_cached", "ais_mixing", "nvfp4_kv_append",
+                     "nvfp4_kv_decode_attention",
                      "rmsnorm_aqn_quantize", "nvfp4_lora_linear",
                      "nvfp4_lora_linear_w4a4", "aqn_sigma"):
         assert required in names
@@ -133,6 +134,40 @@ def test_ais_validation(nv):
     assert call(w=A0 + 64) == 7                     # weights over an input
     assert call(st=A3 + 8) == 7                     # statistics over the weights
     assert call(ws=A2) == 7                         # workspace over an input
+
+
+def test_kv_validation(nv):
+    app, att = nv.lib().nvfp4_kv_append, nv.lib().nvfp4_kv_decode_attention
+    C0, C1, C2, C3 = 0x100000, 0x200000, 0x300000, 0x400000  # caches of 2 x 8 x 2 rows
+    ok = dict(k=A0, v=A1, B=2, H=2, D=128, pos=A2, gk=A3, gv=A3 + 4, kc=C0, ks=C1, vc=C2, vs=C3, L=8)
+
+    def ap(**kw):
+        a = {**ok, **kw}
+        return app(a["k"], a["v"], a["B"], a["H"], a["D"], a["pos"], a["gk"], a["gv"], a["kc"], a["ks"], a["vc"],
+                   a["vs"], a["L"], None)
+    assert ap(B=-1) == 1 and ap(H=0) == 1 and ap(L=0) == 1
+    assert ap(D=24) == 3
+    assert ap(B=0, k=None) == 0
+    assert ap(pos=None) == 1 and ap(gv=None) == 1
+    assert ap(k=A0 + 8) == 2 and ap(pos=A2 + 2) == 2 and ap(ks=C1 + 4) == 2
+    assert ap(vc=C0 + 16) == 7          # two caches overlap
+    assert ap(kc=A0) == 7               # a cache over an input
+    wsb = nv.workspace_bytes(nv.OP_KV_ATTENTION, 64, 4, 8192)
+    assert wsb > 0 and nv.workspace_bytes(nv.OP_KV_ATTENTION, 4096, 4, 64) == 0  # one span: no merge buffer
+    ok2 = dict(q=A0, kc=C0, ks=C1, gk=A3, vc=C2, vs=C3, gv=A3 + 4, lens=A2, B=2, Hq=4, H=2, D=128, L=8,
+               scale=0.1, out=A4, ws=None, wsb=0)
+
+    def at(**kw):
+        a = {**ok2, **kw}
+        return att(a["q"], a["kc"], a["ks"], a["gk"], a["vc"], a["vs"], a["gv"], a["lens"], a["B"], a["Hq"], a["H"],
+                   a["D"], a["L"], a["scale"], a["out"], a["ws"], a["wsb"], None)
+    assert at(D=64) == 3                # head dimension 128 only
+    assert at(Hq=5) == 3                # Hq not a multiple of Hkv
+    assert at(Hq=34, H=2) == 3          # more than 16 query heads per KV head
+    assert at(scale=float("inf")) == 1 and at(lens=None) == 1
+    assert at(out=A4 + 8) == 2
+    assert at(out=A0 + 64) == 7         # output over the query
+    assert at(B=64, H=4, Hq=28, L=8192, out=A4) == 4  # several spans need the merge buffer
 
 
 def _qb(nv, n=2, xs=(A0, A0 + 0x1000), rows=(4, 8), cols=(32, 64), dtype=0, codes=(A1, A1 + 0x1000),

@@ -293,6 +293,94 @@ def test_trace_round_trip_gpu_only_qwen7b_gate(nv):
         assert np.array_equal(rec_h[r * k // 32:(r + 1) * k // 32], mr), f"row {r}: record bits differ"
 
 
+# ---------------------------------------------------------------- FP4 KV cache and decode attention
+
+def _kv_cache_dev(B, Lmax, Hkv, D=128, fill=0x5A):
+    mk = lambda w: torch.full((B, Lmax, Hkv, w), fill, dtype=torch.uint8, device="cuda")
+    return mk(D // 2), mk(D // 16), mk(D // 2), mk(D // 16)
+
+
+def test_kv_append(nv):
+    """New rows land bit-exactly (the oracle's encoding at the given g) at each sequence's position;
+    a sequence whose position is outside the cache, and every other row, stay untouched."""
+    B, Hkv, D, Lmax = 5, 4, 128, 7
+    k = synth.activation_bf16(B * Hkv, D, 31, 1).reshape(B, Hkv, D)
+    v = synth.heavy_tail_activation_bf16(B * Hkv, D, 31, 2).reshape(B, Hkv, D)
+    pos = np.array([0, 6, 3, -1, 7], np.int32)  # the last two are outside [0, Lmax)
+    gk, gv = np.float32(0.0021), np.float32(0.0047)
+    kc, ks, vc, vs = _kv_cache_dev(B, Lmax, Hkv)
+    nv.nvfp4_kv_append(P.dev_bf16(k), P.dev_bf16(v), P.dev(pos), P.dev(np.array([gk])), P.dev(np.array([gv])),
+                       kc, ks, vc, vs)
+    torch.cuda.synchronize()
+    ck, sk = oracle.kv_quantize(k, gk)
+    cv, sv = oracle.kv_quantize(v, gv)
+    got = [t.cpu().numpy() for t in (kc, ks, vc, vs)]
+    for b in range(B):
+        for t in range(Lmax):
+            written = t == pos[b]
+            for arr, ref in zip(got, (ck, sk, cv, sv)):
+                if written:
+                    assert np.array_equal(arr[b, t], ref[b]), f"sequence {b} row {t}"
+                else:
+                    assert np.all(arr[b, t] == 0x5A), f"sequence {b} row {t} was written"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
+    (3, 7, 1, 200, [1, 77, 200]),
+    (4, 28, 4, 300, [300, 129, 64, 65]),
+    (2, 16, 1, 2000, [1999, 640]),
+    (2, 8, 2, 50, [0, 50]),
+])
+def test_kv_decode_attention(nv, B, Hq, Hkv, Lmax, lens):
+    """Cache built by nvfp4_kv_append one token at a time, attention against the oracle on the same
+    cache bytes (ragged lengths, a single token, a length of 0, spans split across CTAs)."""
+    D = 128
+    g = np.float32(0.003)
+    kc, ks, vc, vs = _kv_cache_dev(B, Lmax, Hkv, fill=0)
+    gd = P.dev(np.array([g]))
+    kall = synth.activation_bf16(B * Lmax * Hkv, D, 32, Hq).reshape(Lmax, B, Hkv, D)
+    vall = synth.activation_bf16(B * Lmax * Hkv, D, 33, Hq).reshape(Lmax, B, Hkv, D)
+    kd, vd = P.dev_bf16(kall), P.dev_bf16(vall)
+    for t in range(Lmax):
+        nv.nvfp4_kv_append(kd[t], vd[t], torch.full((B,), t, dtype=torch.int32, device="cuda"), gd, gd, kc, ks, vc, vs)
+    q = synth.activation_bf16(B * Hq, D, 34, Hq).reshape(B, Hq, D)
+    lens = np.array(lens, np.int32)
+    scale = 1.0 / np.sqrt(D)
+    out = nv.nvfp4_kv_decode_attention(P.dev_bf16(q), kc, ks, gd, vc, vs, gd, P.dev(lens), scale)
+    torch.cuda.synchronize()
+    caches = [t.cpu().numpy() for t in (kc, ks, vc, vs)]
+    ck, sk = oracle.kv_quantize(kall.transpose(1, 0, 2, 3), g)
+    assert np.array_equal(caches[0], ck) and np.array_equal(caches[1], sk), "cache bytes"
+    got = P.host_bits(out)
+    live = lens > 0
+    ref = oracle.attention_decode(q[live], *(c[live] for c in caches[:2]), g, *(c[live] for c in caches[2:]), g,
+                                  lens[live], scale)
+    P.assert_gemm_close(got[live], ref, f"attention {B}x{Hq}/{Hkv} L={Lmax}")
+    assert not got[~live].any(), "a sequence of length 0 gives zeros"
+
+
+def test_kv_decode_attention_qwen7b_sampled(nv):
+    """Qwen2.5-7B decode at full size: 64 sequences, 28 query / 4 KV heads, 128 dims, an 8192-token
+    cache of random valid NVFP4 bytes (scale bytes 0x28..0x3F), lengths 4096..8192; three sampled
+    sequences against the oracle."""
+    B, Hq, Hkv, D, Lmax = 64, 28, 4, 128, 8192
+    gen = torch.Generator(device="cuda").manual_seed(35)
+    codes = lambda: torch.randint(0, 256, (B, Lmax, Hkv, D // 2), generator=gen, device="cuda", dtype=torch.int32).to(torch.uint8)
+    scl = lambda: torch.randint(0x28, 0x40, (B, Lmax, Hkv, D // 16), generator=gen, device="cuda", dtype=torch.int32).to(torch.uint8)
+    kc, ks, vc, vs = codes(), scl(), codes(), scl()
+    g = np.float32(1.0 / 64)
+    gd = P.dev(np.array([g]))
+    lens = np.random.default_rng(35).integers(4096, Lmax + 1, B).astype(np.int32)
+    q = synth.activation_bf16(B * Hq, D, 36, 1).reshape(B, Hq, D)
+    out = nv.nvfp4_kv_decode_attention(P.dev_bf16(q), kc, ks, gd, vc, vs, gd, P.dev(lens), 1.0 / np.sqrt(D))
+    torch.cuda.synchronize()
+    got = P.host_bits(out)
+    for b in np.random.default_rng(36).choice(B, 3, replace=False):
+        cb = [t[b:b + 1].cpu().numpy() for t in (kc, ks, vc, vs)]
+        ref = oracle.attention_decode(q[b:b + 1], cb[0], cb[1], g, cb[2], cb[3], g, lens[b:b + 1], 1.0 / np.sqrt(D))
+        P.assert_gemm_close(got[b:b + 1], ref, f"sequence {b}")
+
+
 # ---------------------------------------------------------------- AIS mixing coefficient
 
 AIS_ABS = ("alpha", "alpha_ess", "alpha_mis", "alpha_var", "cv2", "dsigma")  # dimensionless: 1e-5 absolute
