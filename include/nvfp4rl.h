@@ -210,7 +210,8 @@ NVFP4RL_API nvfp4rl_status nvfp4_quantize_cached(const void* x, int32_t dtype, i
  *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_AIS, 0, 0, 0, 0, 0) bytes, device, 16-byte
  *            aligned; scratch.
  * Outputs may overlap no input, each other or the workspace (NVFP4RL_ERR_ALIAS). The sums are
- * compensated fp32 per thread and (hi, lo) fp32 pairs across threads and CTAs, added in a fixed
+ * fp32 over 16-token chunks folded into compensated fp32 sums per thread, and (hi, lo) fp32 pairs
+ * across threads and CTAs, added in a fixed
  * order: the result does not depend on timing. alpha and the ratios are formed in fp32 from
  * fp64 means. Three kernels chained by programmatic dependent launch; no device-side waits.
  */

@@ -12,7 +12,8 @@
 // Two kernels, chained by programmatic dependent launch (no grid-wide wait anywhere).
 // ais_reduce_kernel: each thread streams its tokens (128-bit loads) and sums seven quantities --
 // w', w'^2, |d|, A', A'^2, (wA)', (wA)'^2, each ' marking a shift by token 0's value, so that every
-// variance keeps its digits and constant data gives exactly zero -- with compensated (Kahan) fp32 additions; the warp and block
+// variance keeps its digits and constant data gives exactly zero -- in plain fp32 over chunks of 16
+// tokens, each chunk added to compensated (Kahan) fp32 sums; the warp and block
 // trees add (hi, lo) fp32 pairs with TwoSum (about 44 bits), and each CTA writes its pairs to its
 // slot of the workspace and takes a ticket. The CTA that takes the last ticket adds the slots in
 // slot order (one warp per quantity, again in pairs) and computes alpha and the statistics: the
@@ -76,19 +77,28 @@ struct Shift {
   float w, a, wa;
 };
 
-// One token's terms.
+// One token's terms, added in plain fp32 to a chunk sum c (at most 16 tokens per chunk).
 __device__ __forceinline__ void accumulate(float lr, float lt, float a, float C, const Shift& k,
-                                           Kahan (&s)[kAisSums]) {
+                                           float (&c)[kAisSums]) {
   const float d = lt - lr;
   const float w = fminf(expf(d), C);
   const float ws = w - k.w, as = a - k.a, was = w * a - k.wa;
-  s[0].add(ws);
-  s[1].add(ws * ws);
-  s[2].add(fabsf(d));
-  s[3].add(as);
-  s[4].add(as * as);
-  s[5].add(was);
-  s[6].add(was * was);
+  c[0] += ws;
+  c[1] = fmaf(ws, ws, c[1]);
+  c[2] += fabsf(d);
+  c[3] += as;
+  c[4] = fmaf(as, as, c[4]);
+  c[5] += was;
+  c[6] = fmaf(was, was, c[6]);
+}
+
+// A chunk's sums into the compensated running sums, the chunk restarted.
+__device__ __forceinline__ void fold(float (&c)[kAisSums], Kahan (&s)[kAisSums]) {
+#pragma unroll
+  for (int q = 0; q < kAisSums; ++q) {
+    s[q].add(c[q]);
+    c[q] = 0.0f;
+  }
 }
 
 __global__ void __launch_bounds__(kAisThreads, 1)
@@ -109,18 +119,25 @@ __global__ void __launch_bounds__(kAisThreads, 1)
   k0.a = __ldg(adv);
   k0.wa = k0.w * k0.a;
   Kahan s[kAisSums];
+  float c[kAisSums] = {0, 0, 0, 0, 0, 0, 0};
+  int in_chunk = 0;
 #pragma unroll 2
   for (int64_t j = tid; j < n4; j += nthreads) {
     const float4 r = __ldg(reinterpret_cast<const float4*>(lr) + j);
     const float4 t = __ldg(reinterpret_cast<const float4*>(lt) + j);
     const float4 a = __ldg(reinterpret_cast<const float4*>(adv) + j);
-    accumulate(r.x, t.x, a.x, p.C, k0, s);
-    accumulate(r.y, t.y, a.y, p.C, k0, s);
-    accumulate(r.z, t.z, a.z, p.C, k0, s);
-    accumulate(r.w, t.w, a.w, p.C, k0, s);
+    accumulate(r.x, t.x, a.x, p.C, k0, c);
+    accumulate(r.y, t.y, a.y, p.C, k0, c);
+    accumulate(r.z, t.z, a.z, p.C, k0, c);
+    accumulate(r.w, t.w, a.w, p.C, k0, c);
+    if (++in_chunk == 4) {  // 16 tokens
+      fold(c, s);
+      in_chunk = 0;
+    }
   }
   // the last n % 4 tokens: one per thread of the first threads of the grid
-  if (4 * n4 + tid < n) accumulate(lr[4 * n4 + tid], lt[4 * n4 + tid], adv[4 * n4 + tid], p.C, k0, s);
+  if (4 * n4 + tid < n) accumulate(lr[4 * n4 + tid], lt[4 * n4 + tid], adv[4 * n4 + tid], p.C, k0, c);
+  fold(c, s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 0; k < kAisSums; ++k) {
