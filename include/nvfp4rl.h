@@ -249,6 +249,8 @@ NVFP4RL_API nvfp4rl_status nvfp4_kv_append(const uint16_t* k, const uint16_t* v,
  *   q        device bf16 [B][Hq][D], 16-byte aligned; D must be 128; Hq a multiple of Hkv with
  *            Hq / Hkv <= 16; B * Hkv <= 65535.
  *   k_codes, k_scales, v_codes, v_scales  the cache as nvfp4_kv_append writes it; gk, gv its scales.
+ *            Scale bytes are 0x00 .. 0x7E as the encoder writes them; other bytes give unspecified
+ *            (finite or not) results but no fault.
  *   lens     device int32 [B]: tokens attended per sequence, clamped to [0, Lmax]; 0 gives zeros.
  *   scale    softmax scale (typically 1/sqrt(D)), finite.
  *   out      device bf16 [B][Hq][D], 16-byte aligned; may overlap no input.
