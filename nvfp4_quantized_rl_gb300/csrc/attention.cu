@@ -89,9 +89,13 @@ __device__ __forceinline__ uint32_t scale_bf16_2p119(uint32_t byte) {
   return __float_as_uint(e4m3_decode_pos(byte) * 0x1p119f) >> 16;
 }
 
-// Two code bytes' four elements (byte j's low nibble first) as bf16x2 patterns grid * 2^-126 with signs.
+// One code byte's two elements (low nibble first) as a bf16x2 pattern grid * 2^-126 with signs: with
+// u = byte + byte * 2^12 the high nibble also sits at bits 16..19, so one mask-and-shift pair places
+// both magnitudes (bits 6..8 of each half) and one places both signs (bit 15 of each half).
+// byte must be 0 .. 255.
 __device__ __forceinline__ uint32_t code_pair_bits(uint32_t byte) {
-  return ((byte & 7u) << 6) | ((byte & 8u) << 12) | ((byte & 0x70u) << 18) | ((byte & 0x80u) << 24);
+  const uint32_t u = byte * 4097u;
+  return ((u & 0x00070007u) << 6) | ((u & 0x00080008u) << 12);
 }
 
 // 16 code bytes (32 elements = two blocks) and their two scale bytes, dequantized to grid E4M3(s)
@@ -104,7 +108,7 @@ __device__ __forceinline__ void dequant32(uint4 codes, uint32_t s0, uint32_t s1,
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) o[4 * i + j] = bf16x2_mul(code_pair_bits(w[i] >> (8 * j)), i < 2 ? S0 : S1);
+    for (int j = 0; j < 4; ++j) o[4 * i + j] = bf16x2_mul(code_pair_bits((w[i] >> (8 * j)) & 0xFFu), i < 2 ? S0 : S1);
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < 4; ++i) d[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
