@@ -23,13 +23,10 @@
 // token's weight with that alpha (the log-probs are read again, from L2 at the sizes of a
 // training batch).
 #include "common.cuh"
-#include "sm100.cuh"
 
 
 namespace nvfp4rl {
 namespace {
-
-using namespace sm100;
 
 constexpr int kAisThreads = 1024;
 constexpr int kAisSums = 7;
