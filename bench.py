@@ -78,6 +78,28 @@ def step_bytes():
     return b
 
 
+# ----------------------------------------------------------------------------- replicas (N > 1)
+
+def max_over_ranks(ms, device, world, dist_mod):
+    """The slowest replica's time: the job's N replicas have all finished only then."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_replica_step, world, ms_per_step):
+    """Whole-job GB/s: every replica moves the same bytes per step (weak scaling)."""
+    return bytes_per_replica_step * world / (ms_per_step / 1e3) / 1e9
+
+
+def reference_runs_here(rank, world):
+    """Under torchrun the CPU reference arm runs and prints on rank 0 only."""
+    return world <= 1 or rank == 0
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -333,10 +355,7 @@ def run_gpu(args):
         dist.barrier()
     total_ms = float(sum(step_ms))
     op_ms = {name: float(np.mean(v)) for name, v in op_samples.items()}
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev, world, dist)
     ms_per_step = total_ms / args.steps
 
     # ---- end to end: host buffers in, host result out, through the same public API
@@ -349,7 +368,7 @@ def run_gpu(args):
         return
     hbm, bf16_tf, peak_src = peaks()
     sb = step_bytes()
-    value = sb * world / (total_ms / args.steps / 1e3) / 1e9
+    value = job_throughput(sb, world, total_ms / args.steps)
 
     # parts
     q_bytes = sum(bytes_quantize(n * k) for _, n, k in LINEARS)
@@ -801,10 +820,8 @@ def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, 
     ms = a.elapsed_time(b) / n
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": step_bytes() * world / (ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+        ms = max_over_ranks(ms, dev, world, dist)
+    return {"value": job_throughput(step_bytes(), world, ms), "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
@@ -868,7 +885,7 @@ def cpu_baseline(seconds_budget=20.0):
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    if world > 1 and rank != 0:
+    if not reference_runs_here(rank, world):
         return
     # each step is a sample sized so that warm-up and timed steps together take about two minutes
     den = sample_den(120.0 / max(1, args.steps + args.warmup))
