@@ -9,8 +9,8 @@
 // Per token rho = exp(logp_train - logp_rollout), w = min(rho, C); statistics over the n tokens
 // with weight 1/n; dsigma = std(w A) / std(A) - 1 (0 when std(A) = 0).
 //
-// Two kernels, chained by programmatic dependent launch (no grid-wide wait anywhere).
-// ais_reduce_kernel: each thread streams its tokens (128-bit loads) and sums seven quantities --
+// Three kernels, chained by programmatic dependent launch (no grid-wide wait anywhere): a
+// one-thread clear of the ticket word, then two that do the work. ais_reduce_kernel: each thread streams its tokens (128-bit loads) and sums seven quantities --
 // w', w'^2, |d|, A', A'^2, (wA)', (wA)'^2, each ' marking a shift by token 0's value, so that every
 // variance keeps its digits and constant data gives exactly zero -- in plain fp32 over chunks of 16
 // tokens, each chunk added to compensated (Kahan) fp32 sums; the warp and block
@@ -23,7 +23,6 @@
 // token's weight with that alpha (the log-probs are read again, from L2 at the sizes of a
 // training batch).
 #include "common.cuh"
-
 
 namespace nvfp4rl {
 namespace {
