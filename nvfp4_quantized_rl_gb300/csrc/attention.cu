@@ -8,17 +8,18 @@
 //
 // Split-KV ("flash decoding"): one CTA of four warps per (sequence, KV head, token span); warp w
 // takes tokens 16 w .. 16 w + 15 of every 64-token chunk of the span and works alone (its own
-// shared-memory region, __syncwarp only). The code and scale bytes of its 16 tokens stream into a
-// two-stage ring with cp.async; per group the warp dequantizes the K and V rows into bf16 tiles -- the sign and magnitude bits of
-// an E2M1 code placed as bf16 bits are grid * 2^-126 exactly, one bf16x2 FMA by E4M3(s) 2^119 makes
-// grid E4M3(s) 2^-7, exact (at most 6 significant bits); 2^7 g is applied as a scalar later -- and
-// each warp
-// takes 16 of the tokens: S = Q K^T with mma.sync m16n8k16 (the group's query heads are the rows,
-// padded to 16), an online softmax in exp2, and O += P V with the V fragments read transposed by
-// ldmatrix. The contraction is skinny (Hq / Hkv rows) and the cache read from HBM bounds the
-// kernel, so warp-level MMAs leave the tensor pipe mostly idle and need no tcgen05 machinery.
-// The four warps' states are merged in shared memory; with several spans per sequence a second
-// kernel merges the spans' (max, sum, O) partials.
+// shared-memory region, __syncwarp only). Per 16-token group the warp
+//   - streams the code and scale bytes of its tokens into a two-stage ring with cp.async;
+//   - dequantizes the K and V rows into bf16 tiles: the sign and magnitude bits of an E2M1 code
+//     placed as bf16 bits are grid * 2^-126 exactly, and one bf16x2 FMA by E4M3(s) 2^119 makes
+//     grid E4M3(s) 2^-7, exact (at most 6 significant bits); 2^7 g is applied as a scalar later;
+//   - computes S = Q K^T with mma.sync m16n8k16 (the group's query heads are the rows, padded to
+//     16), keeps an online softmax in exp2, and adds P V with the V fragments read transposed by
+//     ldmatrix.
+// The contraction is skinny (Hq / Hkv rows), so warp-level MMAs leave the tensor pipe mostly
+// idle and tcgen05 would add nothing; the dequantization's instructions, not the HBM read, bound
+// the kernel as it stands. The four warps' states are merged in shared memory; with several spans
+// per sequence a second kernel merges the spans' (max, sum, O) partials.
 #include <map>
 #include <mutex>
 
