@@ -1,4 +1,4 @@
-// NVFP4 block quantization, plain and rollout-guided (sm_103a).
+// NVFP4 block quantization: plain, rollout-guided, recorded and cached (sm_103a).
 //
 // Format: QeRL explainer, section "NVFP4量子化とLoRA" (4-bit weights with hardware
 // support); TRACE summary, section "仕組みの工学的な理解" (a few values share one
@@ -9,11 +9,19 @@
 // apply to the exact real quotient, ties to the even encoding, saturating.
 //
 // Kernels:
-//   amax_kernel      one HBM read of x, 128-bit non-caching loads, packed 16-bit max
-//                    for bf16, warp/CTA reduction, one atomicMax per CTA.
-//   quantize_kernel  one thread per 16-element block (two blocks in flight per thread):
-//                    two (bf16) or four (fp32) 128-bit loads, the exact E4M3 scale byte,
-//                    seven per-block thresholds, and per element seven unsigned compares.
+//   amax_kernel, amax_bulk_kernel  the tensor amax (grid-stride 128-bit loads, or for large
+//                    tensors a cp.async.bulk ring per SM), one atomicMax per CTA.
+//   quantize_kernel  one thread per 16-element block (two blocks in flight per thread), in four
+//                    modes: plain, guided (a mask picks the rounding direction), record (plain,
+//                    plus one rounding-direction bit per element: TRACE's rollout side), cached
+//                    (guided against given scale bytes and g, one pass: TRACE's training side).
+//                    bf16 input uses per-tensor threshold tables and two-element bf16 compares,
+//                    fp32 input per-block thresholds and integer compares.
+//   encode_amax_ring_kernel  the weight refresh: one tensor's encoding while the next tensor's
+//                    amax streams through a shared-memory ring.
+//   rmsnorm_quant_kernel  RMSNorm-AQN and the quantization of its output in one cooperative
+//                    kernel, the normalized rows kept in shared memory across a grid barrier.
+//   kv_append_kernel one decode step's K/V rows encoded at a given g into an NVFP4 KV cache.
 //
 // Exactness without division per element: for an fp32 value a and a real P,
 //   a > P  <=>  a > RD(P)      a >= P  <=>  a >= RU(P)
