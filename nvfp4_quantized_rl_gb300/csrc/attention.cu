@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(128) kv_attention_merge_kernel(const float* __
 
 int attention_splits(int64_t B, int64_t Hkv, int64_t Lmax) {
   const int64_t chunks = std::max<int64_t>(1, (Lmax + kChunk - 1) / kChunk);
-  const int64_t want = (4 * kNumSMsHint + B * Hkv - 1) / (B * Hkv);  // about four CTAs per SM
+  const int64_t want = (12 * kNumSMsHint + B * Hkv - 1) / (B * Hkv);  // several waves: a short tail
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({chunks, want, 256})));
 }
 
