@@ -1,22 +1,25 @@
 """Benchmark of the NVFP4 rollout linear layer on one GB300 (or N replicas).
 
-Workload (one step): a Qwen2.5-7B-shaped decoder layer in W4A16 decode --
-hidden 3584; q/o 3584x3584, gate/up 18944x3584, down 3584x18944 bf16 weights
-~N(0, 0.02) with 1% outlier columns x8; M = 64 bf16 tokens; LoRA r = 32 on every
-linear; AQN sigma schedule 1e-2 -> 5e-4 over K = 10. One step runs every stage of
-the path on that layer:
-  1. AQN sigma_k (host) and RMSNorm-AQN of the 64 tokens (input norm), then again
-     (post-attention norm);
-  2. the rollout weight refresh: the tensor amax and the NVFP4 encoding (codes,
-     E4M3 block scales, fp32 g) of all five weights, in one nvfp4_quantize_batch call;
-  3. the five W4A16 LoRA linears at M = 64.
-Inputs are synthetic, generated on the device from a seed, and larger than L2:
-every step streams the five bf16 weights (458 MB) and their NVFP4 codes (122 MB).
+Default workload (one step): 12 Qwen2.5-32B-shaped decoder layers, each with its own
+weights -- hidden 5120; q/o 5120x5120, k/v 1024x5120, gate/up 27648x5120,
+down 5120x27648 bf16 weights ~N(0, 0.015); LoRA r = 64, s = 2, on every linear;
+AQN sigma schedule 1e-2 -> 5e-4 over K = 10. Per layer the step runs every stage of
+the path:
+  1. the rollout weight refresh: the tensor amax and the NVFP4 encoding (codes, E4M3
+     block scales, fp32 g) of all seven weights, one nvfp4_quantize_batch call;
+  2. decode, M = 256 tokens: RMSNorm-AQN of the input and of the residual stream,
+     then the seven W4A16 LoRA linears;
+  3. prefill, M = 8192 tokens: RMSNorm-AQN twice, then the seven W4A4 LoRA linears
+     (activations quantized to NVFP4 on the fly, block-scaled FP4 MMA).
+One refresh thus serves 256 decode and 8192 prefill tokens per layer. `--config
+qwen7b-decode` runs the Qwen2.5-7B-shaped decode layer instead (M = 64, W4A16 only).
+Inputs are synthetic, generated on the device from a seed, and larger than L2: a
+step streams 37 GB of bf16 weights and 10 GB of NVFP4 codes.
 
-Prints one JSON line. `value` is algorithmic bytes per step (what the method must
-move, each tensor once) over the device time of a step, summed over ranks.
-`--impl reference` times the CPU oracle on a bounded sample of the same
-workload instead.
+Prints one JSON line. For the 32B step `value` is the LoRA-linear TFLOP/s of the whole
+step (every linear's 2MNK + 2Mr(K+N) over the device time of the step, including the
+refresh and the norms), summed over replicas; for the 7B decode step it is algorithmic
+GB/s. `--impl reference` times the CPU oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -35,22 +38,49 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 LoRA-linear TFLOP/s & HBM GB/s (% roofline); quantize GB/s, 1×GB300"
-WORKLOAD = ("qwen2.5-7b-shaped decode layer, W4A16: hidden 3584, q/o 3584x3584, gate/up 18944x3584, "
-            "down 3584x18944, M=64 tokens, LoRA r=32 s=2, AQN sigma 1e-2->5e-4 over K=10, "
-            "weight refresh (amax + NVFP4 encode) of all five weights each step")
-HIDDEN, INTER, M_TOK, RANK, S_LORA = 3584, 18944, 64, 32, 2.0
-LINEARS = [("q", 3584, 3584), ("o", 3584, 3584), ("gate", 18944, 3584), ("up", 18944, 3584), ("down", 3584, 18944)]
+S_LORA = 2.0
 SIGMA0, SIGMAK, KSCHED = 1e-2, 5e-4, 10
+FP4_PER_BF16 = 6.0  # nominal dense FP4 / BF16 tensor rate (13.5 / 2.25 PFLOP/s)
+
+LINEARS_32B = [("q", 5120, 5120), ("k", 1024, 5120), ("v", 1024, 5120), ("o", 5120, 5120), ("gate", 27648, 5120),
+               ("up", 27648, 5120), ("down", 5120, 27648)]
+LINEARS_7B = [("q", 3584, 3584), ("o", 3584, 3584), ("gate", 18944, 3584), ("up", 18944, 3584),
+              ("down", 3584, 18944)]
+
+CONFIGS = {
+    "qwen32b": {
+        "workload": "qwen2.5-32b-shaped decoder layers, decode + prefill: hidden 5120, q/o 5120x5120, k/v 1024x5120, "
+                    "gate/up 27648x5120, down 5120x27648 bf16 weights ~N(0,0.015); per layer: weight refresh (amax + "
+                    "NVFP4 encode) of all seven weights, RMSNorm-AQN x2 + W4A16 LoRA linears at M=256, RMSNorm-AQN x2 "
+                    "+ W4A4 LoRA linears at M=8192; LoRA r=64 s=2; AQN sigma 1e-2->5e-4 over K=10",
+        "hidden": 5120, "inter": 27648, "linears": LINEARS_32B, "std": 0.015, "outliers": 0.0, "rank": 64,
+        "decode_m": 256, "prefill_m": 8192, "layers": 12, "unit": "TFLOP/s", "probe_den": 256,
+    },
+    "qwen7b-decode": {
+        "workload": "qwen2.5-7b-shaped decode layer, W4A16: hidden 3584, q/o 3584x3584, gate/up 18944x3584, "
+                    "down 3584x18944 bf16 weights ~N(0,0.02) with 1% outlier columns x8, M=64 tokens, LoRA r=32 s=2, "
+                    "AQN sigma 1e-2->5e-4 over K=10, weight refresh (amax + NVFP4 encode) of all five weights each step",
+        "hidden": 3584, "inter": 18944, "linears": LINEARS_7B, "std": 0.02, "outliers": 0.01, "rank": 32,
+        "decode_m": 64, "prefill_m": 0, "layers": 1, "unit": "GB/s", "probe_den": 64,
+    },
+}
+
+# Which activation feeds each linear: q/k/v the normed input, o the attention output, gate/up the
+# normed residual stream, down the MLP activation (M x intermediate).
+INPUT_OF = {"q": "h1", "k": "h1", "v": "h1", "o": "attn", "gate": "h2", "up": "h2", "down": "act"}
 
 
 def peaks():
+    """(hbm GB/s, bf16 burst TFLOP/s, bf16 sustained TFLOP/s, source) from MEASURED_PEAKS.json, else the
+    fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+        bf = float(d["bf16_tflops"])
+        return float(d["hbm_gbs"]), bf, float(d.get("bf16_tflops_sustained", bf)), "measured"
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 # ----------------------------------------------------------------------------- byte / flop counts
@@ -67,15 +97,40 @@ def bytes_linear(M, N, K, r):
     return N * K * 0.5625 + 2 * M * K + 2 * M * N + 2 * r * (K + N)
 
 
+def bytes_linear_w4a4(M, N, K, r):
+    # the activation codes and scales written once by the on-the-fly quantizer and read by the GEMM
+    return bytes_linear(M, N, K, r) + 0.5625 * M * K
+
+
 def flops_linear(M, N, K, r):
     return 2 * M * N * K + 2 * M * r * (K + N)
 
 
-def step_bytes():
-    b = 2 * bytes_rmsnorm(M_TOK, HIDDEN)
-    b += sum(bytes_quantize(n * k) for _, n, k in LINEARS)
-    b += sum(bytes_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
-    return b
+def layer_counts(cfg):
+    """Algorithmic bytes and flops of one layer of the step, per part."""
+    H, r = cfg["hidden"], cfg["rank"]
+    md, mp = cfg["decode_m"], cfg["prefill_m"]
+    lin = cfg["linears"]
+    c = {
+        "refresh_bytes": sum(bytes_quantize(n * k) for _, n, k in lin),
+        "rms_d_bytes": 2 * bytes_rmsnorm(md, H),
+        "w4a16_bytes": sum(bytes_linear(md, n, k, r) for _, n, k in lin),
+        "w4a16_flops": sum(flops_linear(md, n, k, r) for _, n, k in lin),
+        "rms_p_bytes": 2 * bytes_rmsnorm(mp, H) if mp else 0.0,
+        "w4a4_bytes": sum(bytes_linear_w4a4(mp, n, k, r) for _, n, k in lin) if mp else 0.0,
+        "w4a4_flops": sum(flops_linear(mp, n, k, r) for _, n, k in lin) if mp else 0.0,
+    }
+    c["bytes"] = c["refresh_bytes"] + c["rms_d_bytes"] + c["w4a16_bytes"] + c["rms_p_bytes"] + c["w4a4_bytes"]
+    c["flops"] = c["w4a16_flops"] + c["w4a4_flops"]
+    return c
+
+
+def step_units(cfg, layers):
+    """Units of the step's metric (flops for TFLOP/s, bytes for GB/s) and the divisor to that unit."""
+    c = layer_counts(cfg)
+    if cfg["unit"] == "TFLOP/s":
+        return c["flops"] * layers, 1e12
+    return c["bytes"] * layers, 1e9
 
 
 # ----------------------------------------------------------------------------- replicas (N > 1)
@@ -90,9 +145,9 @@ def max_over_ranks(ms, device, world, dist_mod):
     return float(t.item())
 
 
-def job_throughput(bytes_per_replica_step, world, ms_per_step):
-    """Whole-job GB/s: every replica moves the same bytes per step (weak scaling)."""
-    return bytes_per_replica_step * world / (ms_per_step / 1e3) / 1e9
+def job_throughput(units_per_replica_step, world, ms_per_step, scale=1e9):
+    """Whole-job throughput (units / s / scale): every replica does the same work per step (weak scaling)."""
+    return units_per_replica_step * world / (ms_per_step / 1e3) / scale
 
 
 def reference_runs_here(rank, world):
@@ -207,11 +262,113 @@ def recorded_traffic(kernel):
         return None
 
 
+class Workload:
+    """Device buffers of the step: per-layer weights, their NVFP4 outputs and LoRA factors; activations,
+    outputs and workspaces per phase (decode / prefill), shared by the layers."""
+
+    def __init__(self, nv, torch, dev, cfg, layers, seed):
+        self.cfg, self.layers = cfg, layers
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+
+        def randn(*shape, std=1.0):
+            return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).mul_(std)
+
+        H, I, r = cfg["hidden"], cfg["inter"], cfg["rank"]
+        self.W, self.Q, self.lora = [], [], []
+        for _ in range(layers):
+            W, Q, lora = {}, {}, {}
+            for name, n, k in cfg["linears"]:
+                w = randn(n, k, std=cfg["std"])
+                if cfg["outliers"]:  # a seeded 1% of the input columns x8
+                    cols = torch.randperm(k, generator=gen, device=dev)[: round(cfg["outliers"] * k)]
+                    w[:, cols] *= 8
+                W[name] = w.to(torch.bfloat16)
+                del w
+                Q[name] = (torch.empty(n, k // 2, dtype=torch.uint8, device=dev),
+                           torch.empty(n, k // 16, dtype=torch.uint8, device=dev),
+                           torch.empty(1, dtype=torch.float32, device=dev))
+                lora[name] = (randn(r, k, std=0.02).to(torch.bfloat16), randn(n, r, std=0.02).to(torch.bfloat16))
+            self.W.append(W)
+            self.Q.append(Q)
+            self.lora.append(lora)
+        self.w1, self.w2 = (1 + randn(H, std=0.1)), (1 + randn(H, std=0.1))
+        self.eps = [randn(H) for _ in range(KSCHED + 1)]
+        self.phases = {}
+        for phase, M, w4a4 in (("d", cfg["decode_m"], False), ("p", cfg["prefill_m"], True)):
+            if not M:
+                continue
+            b = {"x_in": randn(M, H).to(torch.bfloat16), "x_res": randn(M, H).to(torch.bfloat16),
+                 "attn": randn(M, H).to(torch.bfloat16), "act": randn(M, I).to(torch.bfloat16),
+                 "h1": torch.empty(M, H, dtype=torch.bfloat16, device=dev),
+                 "h2": torch.empty(M, H, dtype=torch.bfloat16, device=dev)}
+            Y = {name: torch.empty(M, n, dtype=torch.bfloat16, device=dev) for name, n, k in cfg["linears"]}
+            op = nv.OP_LINEAR_W4A4 if w4a4 else nv.OP_LINEAR_W4A16
+            wsb = max(nv.workspace_bytes(op, M, n, k, r) for _, n, k in cfg["linears"])
+            self.phases[phase] = {"M": M, "w4a4": w4a4, "buf": b, "Y": Y,
+                                  "ws": torch.empty(wsb, dtype=torch.uint8, device=dev)}
+        self.wsq = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, len(cfg["linears"]), 0, 0),
+                               dtype=torch.uint8, device=dev)
+        self.wsa = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
+        self.amax = {name: torch.empty(1, dtype=torch.float32, device=dev) for name, _, _ in cfg["linears"]}
+
+    def ops(self):
+        """Names of the step's ops, per layer (the events of the per-op breakdown)."""
+        names = ["weight_refresh"]
+        for phase, P in self.phases.items():
+            kind = "w4a4" if P["w4a4"] else "w4a16"
+            names += [f"rmsnorm_{phase}"] + [f"{kind}_{n}" for n, _, _ in self.cfg["linears"]]
+        return names
+
+    def step(self, nv, k, ev=None, only=None, layer_sel=None):
+        """One step at noise-schedule index k. ev: {(layer, op): (start, end)} events recorded around every
+        op; only: run just these op names (single-op mode, layer 0 unless layer_sel)."""
+        sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
+        lin = self.cfg["linears"]
+        for l in (range(self.layers) if layer_sel is None else layer_sel):
+            def mark(name, fn):
+                if only is not None and name not in only:
+                    return
+                if ev is None:
+                    fn()
+                    return
+                a, b = ev[(l, name)]
+                a.record()
+                fn()
+                b.record()
+            W, Q, lora = self.W[l], self.Q[l], self.lora[l]
+            mark("weight_refresh", lambda: nv.nvfp4_quantize_batch(
+                [W[n] for n, _, _ in lin], codes=[Q[n][0] for n, _, _ in lin], scales=[Q[n][1] for n, _, _ in lin],
+                g=[Q[n][2] for n, _, _ in lin], workspace=self.wsq))
+            if only is not None:  # the single-weight amax and encode kernels (not part of the step)
+                for name, _, _ in lin:
+                    c, s, g = Q[name]
+                    if f"amax_{name}" in only:
+                        nv.nvfp4_amax(W[name], out=self.amax[name])
+                    if f"quantize_{name}" in only:
+                        nv.nvfp4_quantize(W[name], amax_in=self.amax[name], codes=c, scales=s, g=g)
+            for phase, P in self.phases.items():
+                b = P["buf"]
+                mark(f"rmsnorm_{phase}", lambda: (nv.rmsnorm_aqn(b["x_in"], self.w1, self.eps[k], sigma, 1e-6,
+                                                                 out=b["h1"]),
+                                                  nv.rmsnorm_aqn(b["x_res"], self.w2, self.eps[k], sigma, 1e-6,
+                                                                 out=b["h2"])))
+                fn = nv.nvfp4_lora_linear_w4a4 if P["w4a4"] else nv.nvfp4_lora_linear
+                kind = "w4a4" if P["w4a4"] else "w4a16"
+                for name, _, _ in lin:
+                    c, s, g = Q[name]
+                    A, B = lora[name]
+                    mark(f"{kind}_{name}", lambda: fn(b[INPUT_OF[name]], c, s, g, A, B, S_LORA, out=P["Y"][name],
+                                                      workspace=P["ws"]))
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
     import nvfp4_quantized_rl_gb300 as nv
 
+    cfg = CONFIGS[args.config]
+    layers = args.layers or cfg["layers"]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -220,111 +377,43 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1234 + rank)
-
-    def randn(*shape, std=1.0):
-        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).mul_(std)
-
-    # weights: bf16 ~N(0, 0.02), 1% of the input columns x8
-    W = {}
-    for name, n, k in LINEARS:
-        w = randn(n, k, std=0.02)
-        cols = torch.randperm(k, generator=gen, device=dev)[: round(0.01 * k)]
-        w[:, cols] *= 8
-        W[name] = w.to(torch.bfloat16)
-        del w
-    lora = {name: (randn(RANK, k, std=0.02).to(torch.bfloat16), randn(n, RANK, std=0.02).to(torch.bfloat16))
-            for name, n, k in LINEARS}
-    x_in = randn(M_TOK, HIDDEN).to(torch.bfloat16)
-    x_res = randn(M_TOK, HIDDEN).to(torch.bfloat16)
-    attn = randn(M_TOK, HIDDEN).to(torch.bfloat16)
-    act = randn(M_TOK, INTER).to(torch.bfloat16)
-    w1, w2 = (1 + randn(HIDDEN, std=0.1)), (1 + randn(HIDDEN, std=0.1))
-    eps = [randn(HIDDEN) for _ in range(KSCHED + 1)]
-
-    # outputs and workspaces, allocated once
-    Q = {name: (torch.empty(n, k // 2, dtype=torch.uint8, device=dev), torch.empty(n, k // 16, dtype=torch.uint8, device=dev),
-                torch.empty(1, dtype=torch.float32, device=dev), torch.empty(1, dtype=torch.float32, device=dev))
-         for name, n, k in LINEARS}
-    Y = {name: torch.empty(M_TOK, n, dtype=torch.bfloat16, device=dev) for name, n, k in LINEARS}
-    h1 = torch.empty(M_TOK, HIDDEN, dtype=torch.bfloat16, device=dev)
-    h2 = torch.empty_like(h1)
-    ws_bytes = max(nv.workspace_bytes(nv.OP_LINEAR_W4A16, M_TOK, n, k, RANK) for _, n, k in LINEARS)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    wsq = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, len(LINEARS), 0, 0), dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    refresh_args = ([W[n] for n, _, _ in LINEARS], [Q[n][0] for n, _, _ in LINEARS], [Q[n][1] for n, _, _ in LINEARS],
-                    [Q[n][2] for n, _, _ in LINEARS])
-    for name, _, _ in LINEARS:  # each weight's amax, the input of the single-op encode (quantize_<w>)
-        nv.nvfp4_amax(W[name], out=Q[name][3])
-    inputs = {"q": h1, "o": attn, "gate": h2, "up": h2, "down": act}
+    wl = Workload(nv, torch, dev, cfg, layers, 1234 + rank)
+    for name, _, _ in cfg["linears"]:  # each weight's amax, the input of the single-op encode (quantize_<w>)
+        nv.nvfp4_amax(wl.W[0][name], out=wl.amax[name])
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ops = wl.ops()
 
-    # per-op CUDA events (all launches go to the current stream)
-    ops = ["rmsnorm_aqn", "rmsnorm_aqn_2", "weight_refresh"] + [f"linear_{n}" for n, _, _ in LINEARS]
-    # single-op mode only (not part of the step): the per-weight amax and encode kernels alone
-    solo_ops = [f"amax_{n}" for n, _, _ in LINEARS] + [f"quantize_{n}" for n, _, _ in LINEARS]
-
-    def step(k, ev=None, only=None):
-        st = torch.cuda.current_stream(dev)
-
-        def mark(name, fn):
-            if only is not None and name not in only:
-                return
-            if ev is None:
-                fn()
-                return
-            a, b = ev[name]
-            a.record(st)
-            fn()
-            b.record(st)
-        sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
-        mark("rmsnorm_aqn", lambda: nv.rmsnorm_aqn(x_in, w1, eps[k], sigma, 1e-6, out=h1))
-        mark("weight_refresh", lambda: nv.nvfp4_quantize_batch(refresh_args[0], codes=refresh_args[1],
-                                                               scales=refresh_args[2], g=refresh_args[3], workspace=wsq))
-        if only is not None:
-            for name, n, kk in LINEARS:
-                c, s, g, a = Q[name]
-                if f"amax_{name}" in only:
-                    nv.nvfp4_amax(W[name], out=a)
-                if f"quantize_{name}" in only:
-                    nv.nvfp4_quantize(W[name], amax_in=a, codes=c, scales=s, g=g)
-        mark("rmsnorm_aqn_2", lambda: nv.rmsnorm_aqn(x_res, w2, eps[k], sigma, 1e-6, out=h2))
-        for name, n, kk in LINEARS:
-            c, s, g, _ = Q[name]
-            A, B = lora[name]
-            mark(f"linear_{name}", lambda: nv.nvfp4_lora_linear(inputs[name], c, s, g, A, B, S_LORA, out=Y[name],
-                                                                 workspace=ws))
-
-    # eager warm-up (initialises the library), then one CUDA graph per noise-schedule index k:
-    # a step replays the library's launches without host overhead between kernels
+    # eager warm-up (initialises the library), then one CUDA graph per noise-schedule index k: a step
+    # replays the library's launches without host overhead between kernels
     for i in range(2):
-        step(i % (KSCHED + 1))
+        wl.step(nv, i % (KSCHED + 1))
     torch.cuda.synchronize()
     if args.op:
-        return run_ops(args, torch, step, ops + solo_ops, flush, stream, rank)
+        return run_ops(args, torch, nv, wl, ops, flush, stream, rank)
     graphs, ev_graphs = [], []
     launches_per_step = None
-    for k in range(KSCHED + 1):
+    n_graphs = KSCHED + 1
+    for k in range(n_graphs):
         g = torch.cuda.CUDAGraph()
         l0 = nv.kernel_launches()
         with torch.cuda.graph(g):
-            step(k)
+            wl.step(nv, k)
         if launches_per_step is None:
             launches_per_step = nv.kernel_launches() - l0
         graphs.append(g)
-        # the same step with CUDA events around every op, replayed only for the per-op breakdown
-        ev = {name: (torch.cuda.Event(enable_timing=True, external=True),
-                     torch.cuda.Event(enable_timing=True, external=True)) for name in ops}
+    # the same step with CUDA events around every op of every layer, replayed only for the per-op
+    # breakdown (two noise indices suffice: the launches do not depend on k)
+    for k in range(2):
+        ev = {(l, name): (torch.cuda.Event(enable_timing=True, external=True),
+                          torch.cuda.Event(enable_timing=True, external=True)) for l in range(layers) for name in ops}
         ge = torch.cuda.CUDAGraph()
         with torch.cuda.graph(ge):
-            step(k, ev)
+            wl.step(nv, k, ev)
         ev_graphs.append((ge, ev))
     torch.cuda.synchronize()
     for i in range(args.warmup):
-        graphs[i % (KSCHED + 1)].replay()
+        graphs[i % n_graphs].replay()
     torch.cuda.synchronize()
 
     bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -333,98 +422,140 @@ def run_gpu(args):
     torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(dev)
     pci = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
-    # Steps run back to back: every step streams 458 MB of bf16 weights and 122 MB of codes,
-    # several times the 129 MB L2, so nothing one step leaves in L2 serves the next.
+    # Steps run back to back: every step streams each layer's bf16 weights and NVFP4 codes (several
+    # times the 129 MB L2 per layer), so nothing one step leaves in L2 serves the next.
     with ClockSampler(pci) as clocks:
         for i in range(args.steps):
             bounds[i][0].record(stream)
-            graphs[i % (KSCHED + 1)].replay()
+            graphs[i % n_graphs].replay()
             bounds[i][1].record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in bounds]
     # per-op breakdown (not part of the timed region): event-instrumented replays
     op_samples = {name: [] for name in ops}
-    for i in range(max(3, min(args.steps, 10))):
-        ge, ev = ev_graphs[i % (KSCHED + 1)]
+    for i in range(3):
+        ge, ev = ev_graphs[i % 2]
         ge.replay()
         torch.cuda.synchronize()
         for name in ops:
-            op_samples[name].append(ev[name][0].elapsed_time(ev[name][1]))
+            op_samples[name].append(sum(ev[(l, name)][0].elapsed_time(ev[(l, name)][1]) for l in range(layers)))
     launches = launches_per_step * args.steps
     if world > 1:
         dist.barrier()
     total_ms = float(sum(step_ms))
-    op_ms = {name: float(np.mean(v)) for name, v in op_samples.items()}
+    op_ms = {name: float(np.median(v)) for name, v in op_samples.items()}  # per step (all layers)
     total_ms = max_over_ranks(total_ms, dev, world, dist)
     ms_per_step = total_ms / args.steps
 
     # ---- end to end: host buffers in, host result out, through the same public API
-    e2e = run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, Q, Y, h1, h2, ws, flush,
-                  inputs, world)
+    e2e = run_e2e(args, nv, torch, dev, wl, world)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-    hbm, bf16_tf, peak_src = peaks()
-    sb = step_bytes()
-    value = job_throughput(sb, world, total_ms / args.steps)
-
-    # parts
-    q_bytes = sum(bytes_quantize(n * k) for _, n, k in LINEARS)
-    q_ms = op_ms["weight_refresh"]
-    l_bytes = sum(bytes_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
-    l_flops = sum(flops_linear(M_TOK, n, k, RANK) for _, n, k in LINEARS)
-    l_ms = sum(op_ms[f"linear_{n}"] for n, _, _ in LINEARS)
-    r_ms = op_ms["rmsnorm_aqn"] + op_ms["rmsnorm_aqn_2"]
-    parts = {
-        "rmsnorm_aqn": {"us": r_ms * 1e3, "GB/s": 2 * bytes_rmsnorm(M_TOK, HIDDEN) / r_ms / 1e6},
-        "weight_refresh": {"us": q_ms * 1e3, "GB/s": q_bytes / q_ms / 1e6,
-                           "note": "amax + NVFP4 encode of the five weights, one nvfp4_quantize_batch call; bytes: each "
-                                   "weight read once, codes and scales written (the amax pass reads each weight again)"},
-        "lora_linear_w4a16": {"us": l_ms * 1e3, "GB/s": l_bytes / l_ms / 1e6, "TFLOP/s": l_flops / l_ms / 1e9,
-                              "frac_hbm": l_bytes / l_ms / 1e6 / hbm},
-        "per_linear_us": {n: op_ms[f"linear_{n}"] * 1e3 for n, _, _ in LINEARS},
-    }
-    # dominant kernel by device time
-    groups = {"weight_refresh": q_ms, "lora_linear_w4a16": l_ms, "rmsnorm_aqn_kernel": op_ms["rmsnorm_aqn"]}
-    dom = max(groups, key=groups.get)
-    if dom == "weight_refresh":
-        ach = q_bytes / q_ms / 1e6
-        per_launch_bytes = q_bytes
-    elif dom == "lora_linear_w4a16":
-        ach = l_bytes / l_ms / 1e6
-        per_launch_bytes = l_bytes / len(LINEARS)
-    else:
-        ach = parts["rmsnorm_aqn"]["GB/s"]
-        per_launch_bytes = bytes_rmsnorm(M_TOK, HIDDEN)
-    tr = recorded_traffic(dom)
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
-                "algorithmic_bytes_per_launch": per_launch_bytes,
-                "traffic": None if tr is None else tr["dram_bytes_per_launch"]}
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, generated on device)",
-        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2: each step streams 458 MB of bf16 weights and 122 MB of NVFP4 codes (L2 129 MB); no flush",
-                   "replicas": world, "algorithmic_bytes_per_step": sb},
-        "parts": parts, "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
-        "clocks": clocks.summary(),
-    }
+    units, scale = step_units(cfg, layers)
+    value = job_throughput(units, world, ms_per_step, scale)
+    line = summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, launches, clocks, e2e)
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
 
 
+def summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, launches, clocks, e2e):
+    """The bench's JSON line: the step's throughput, the per-part breakdown with each part's fraction of its
+    binding roof, and the roofline of the op that takes the most device time."""
+    hbm, bf16_burst, bf16_sus, src = peaks()
+    fp4_sus = bf16_sus * FP4_PER_BF16
+    c = layer_counts(cfg)
+    lin = cfg["linears"]
+    L = layers
+    sus_note = f"{src} bf16_tflops_sustained (MEASURED_PEAKS.json): the op runs inside a long step"
+    parts, groups = {}, {}
+    q_ms = op_ms["weight_refresh"]
+    parts["weight_refresh"] = {
+        "us": q_ms * 1e3, "GB/s": c["refresh_bytes"] * L / q_ms / 1e6, "frac_hbm": c["refresh_bytes"] * L / q_ms / 1e6 / hbm,
+        "note": "amax + NVFP4 encode of every weight of every layer, one nvfp4_quantize_batch call per layer; bytes: "
+                "each weight read once, codes and scales written (the amax pass reads each weight again)"}
+    groups["weight_refresh"] = q_ms
+    for phase in ("d", "p"):
+        if f"rmsnorm_{phase}" not in op_ms:
+            continue
+        M = cfg["decode_m"] if phase == "d" else cfg["prefill_m"]
+        kind = "w4a16" if phase == "d" else "w4a4"
+        r_ms = op_ms[f"rmsnorm_{phase}"]
+        rb = c["rms_d_bytes" if phase == "d" else "rms_p_bytes"] * L
+        parts[f"rmsnorm_aqn_m{M}"] = {"us": r_ms * 1e3, "GB/s": rb / r_ms / 1e6, "frac_hbm": rb / r_ms / 1e6 / hbm}
+        l_ms = sum(op_ms[f"{kind}_{n}"] for n, _, _ in lin)
+        fl, by = c[f"{kind}_flops"] * L, c[f"{kind}_bytes"] * L
+        tf = fl / l_ms / 1e9
+        part = {"us": l_ms * 1e3, "TFLOP/s": tf, "GB/s": by / l_ms / 1e6, "frac_hbm": by / l_ms / 1e6 / hbm,
+                "per_linear_us": {n: op_ms[f"{kind}_{n}"] * 1e3 / L for n, _, _ in lin}}
+        if kind == "w4a16":
+            part["frac_bf16_tensor"] = tf / bf16_sus
+            part["note"] = ("fractions against the sustained bf16 tensor peak and the HBM copy rate; per_linear_us is "
+                            "per layer (LoRA-down + w4a16_tc_kernel)")
+            groups["lora_linear_w4a16"] = l_ms
+        else:
+            part["frac_fp4_tensor"] = tf / fp4_sus
+            part["note"] = (f"the full call (activation amax + NVFP4 encode, LoRA-down, w4a4_tc_kernel); fraction of "
+                            f"the dense FP4 peak = {FP4_PER_BF16:g} x sustained bf16 (the nominal 13.5 / 2.25 ratio)")
+            groups["lora_linear_w4a4"] = l_ms
+        parts[f"lora_linear_{kind}_m{M}"] = part
+    rms_ms = sum(op_ms[f"rmsnorm_{p}"] for p in ("d", "p") if f"rmsnorm_{p}" in op_ms)
+    groups["rmsnorm_aqn"] = rms_ms
+    dom = max(groups, key=groups.get)
+    n_lin = len(lin) * L
+    if dom == "lora_linear_w4a4":
+        ach = c["w4a4_flops"] * L / groups[dom] / 1e9
+        roofline = {"kernel": dom, "bound": "tensor", "dtype": "fp4", "achieved": ach, "peak": fp4_sus,
+                    "unit": "TFLOP/s", "frac": ach / fp4_sus,
+                    "peak_source": f"{FP4_PER_BF16:g} x {sus_note}",
+                    "algorithmic_flops_per_launch": c["w4a4_flops"] * L / n_lin, "launches_per_step": n_lin}
+    elif dom == "lora_linear_w4a16" and cfg["unit"] == "TFLOP/s":
+        ach = c["w4a16_flops"] * L / groups[dom] / 1e9
+        roofline = {"kernel": dom, "bound": "tensor", "dtype": "bf16", "achieved": ach, "peak": bf16_sus,
+                    "unit": "TFLOP/s", "frac": ach / bf16_sus, "peak_source": sus_note,
+                    "algorithmic_flops_per_launch": c["w4a16_flops"] * L / n_lin, "launches_per_step": n_lin}
+    else:
+        key = {"weight_refresh": "refresh_bytes", "lora_linear_w4a16": "w4a16_bytes"}.get(dom)
+        nb = c[key] * L if key else c["rms_d_bytes"] * L + c["rms_p_bytes"] * L
+        per = L if dom == "weight_refresh" else (n_lin if dom == "lora_linear_w4a16" else 2 * L * len(
+            [p for p in ("d", "p") if f"rmsnorm_{p}" in op_ms]))
+        ach = nb / groups[dom] / 1e6
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                    "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
+                    "algorithmic_bytes_per_launch": nb / per, "launches_per_step": per}
+    tr = recorded_traffic(f"{args.config}:{dom}")
+    roofline["traffic"] = None if tr is None else tr["dram_bytes_per_launch"]
+    units, _ = step_units(cfg, layers)
+    return {
+        "metric": METRIC, "value": value, "unit": cfg["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, generated on device)",
+        "config": {"workload": cfg["workload"], "layers_per_step": layers,
+                   "l2": "inputs larger than L2: every layer streams its own bf16 weights and NVFP4 codes (far more "
+                         "than the 129 MB L2); no flush",
+                   "replicas": world, "algorithmic_bytes_per_step": c["bytes"] * layers,
+                   "linear_flops_per_step": c["flops"] * layers,
+                   "tokens_per_refresh": {"decode": cfg["decode_m"], "prefill": cfg["prefill_m"]}},
+        "parts": parts, "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+
+
 def select_ops(spec, ops):
-    """--op names: op names of the step (e.g. linear_gate, weight_refresh, rmsnorm_aqn), the single-weight
-    amax_<w> / quantize_<w> (the per-tensor amax and encode kernels alone; not part of the step) or the
-    groups linears, refresh, rmsnorm, amax, quantize, all (= the step's ops); comma-separated."""
-    groups = {"linears": [o for o in ops if o.startswith("linear_")], "refresh": ["weight_refresh"],
-              "rmsnorm": [o for o in ops if "rmsnorm" in o], "amax": [o for o in ops if o.startswith("amax_")],
+    """--op names: op names of the step (weight_refresh, rmsnorm_d, w4a16_<w>, rmsnorm_p, w4a4_<w>), the
+    single-weight amax_<w> / quantize_<w> (the per-tensor amax and encode kernels alone; not part of the
+    step) or the groups w4a16, w4a4, linears, refresh, rmsnorm, amax, quantize, all (= the step's ops);
+    comma-separated. Single ops run on layer 0."""
+    groups = {"w4a16": [o for o in ops if o.startswith("w4a16_")], "w4a4": [o for o in ops if o.startswith("w4a4_")],
+              "linears": [o for o in ops if o.startswith(("w4a16_", "w4a4_"))], "refresh": ["weight_refresh"],
+              "rmsnorm": [o for o in ops if o.startswith("rmsnorm")], "amax": [o for o in ops if o.startswith("amax_")],
               "quantize": [o for o in ops if o.startswith("quantize_")],
               "all": [o for o in ops if not o.startswith(("amax_", "quantize_"))]}
     out = []
@@ -437,11 +568,12 @@ def select_ops(spec, ops):
     return out
 
 
-def run_ops(args, torch, step, ops, flush, stream, rank):
-    """Single-op timing (eager launches; before every op a 256 MB read evicts L2): W warm-up and K timed runs of
-    each selected op of the step; one JSON line of per-op device microseconds. Serves per-kernel
+def run_ops(args, torch, nv, wl, ops, flush, stream, rank):
+    """Single-op timing (eager launches on layer 0; before every op a 256 MB read evicts L2): W warm-up and
+    K timed runs of each selected op; one JSON line of per-op device microseconds. Serves per-kernel
     measurement and profiler captures of one op on the step's full-size inputs."""
-    sel = select_ops(args.op, ops)
+    solo = [f"amax_{n}" for n, _, _ in wl.cfg["linears"]] + [f"quantize_{n}" for n, _, _ in wl.cfg["linears"]]
+    sel = select_ops(args.op, ops + solo)
     flush64 = flush.view(torch.int64)
 
     def evict():  # read a buffer twice the L2 size: L2 then holds clean lines only (no write-backs later)
@@ -451,20 +583,21 @@ def run_ops(args, torch, step, ops, flush, stream, rank):
     for name in sel:
         for i in range(args.warmup):
             evict()
-            step(i % (KSCHED + 1), only={name})
+            wl.step(nv, i % (KSCHED + 1), only={name}, layer_sel=[0])
         torch.cuda.synchronize()
         ts = []
         for i in range(args.steps):
             evict()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            step(i % (KSCHED + 1), only={name})
+            wl.step(nv, i % (KSCHED + 1), only={name}, layer_sel=[0])
             b.record(stream)
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b) * 1e3)
         res[name] = {"us_median": float(np.median(ts)), "us_min": float(np.min(ts)), "runs": len(ts)}
     if rank == 0:
-        print(json.dumps({"mode": "ops", "workload": WORKLOAD, "steps": args.steps, "warmup": args.warmup, "ops": res}))
+        print(json.dumps({"mode": "ops", "workload": wl.cfg["workload"], "steps": args.steps, "warmup": args.warmup,
+                          "ops": res}))
 
 
 def run_suite(args):
@@ -480,7 +613,7 @@ def run_suite(args):
     torch.cuda.set_device(dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(4321)
-    hbm, bf16_tf, src = peaks()
+    hbm, bf16_tf, _, src = peaks()
     fp4_tf = bf16_tf * 6.0
     flush64 = torch.empty(256 << 20, dtype=torch.uint8, device=dev).view(torch.int64)
 
@@ -539,7 +672,7 @@ def run_suite(args):
             line.update(extra)
         print(json.dumps(line), flush=True)
 
-    r = RANK
+    r = 32  # LoRA rank of the 7B cases
     cases = set((args.suite or "all").split(","))
 
     def want(name):
@@ -758,58 +891,62 @@ def run_suite(args):
             torch.cuda.empty_cache()
 
 
-def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, Q, Y, h1, h2, ws, flush, inputs,
-            world):
-    """Same step through the public API, with each step's inputs copied from pinned host memory and every
-    output read back to pinned host memory inside the timed region. The copies are the step's bound (462 MB
-    over the host link), so they run on a copy stream, largest weights first, and each weight is quantized
-    (nvfp4_quantize: amax + encode) and its linear run as soon as it has landed; the step ends when the last
-    output is back in host memory."""
-    host_in = {name: W[name].cpu().pin_memory() for name, _, _ in LINEARS}
-    host_x = {"x_in": x_in.cpu().pin_memory(), "x_res": x_res.cpu().pin_memory(), "attn": attn.cpu().pin_memory(),
-              "act": act.cpu().pin_memory()}
-    dev_x = {"x_in": x_in, "x_res": x_res, "attn": attn, "act": act}
-    host_out = {name: torch.empty(Y[name].shape, dtype=torch.bfloat16).pin_memory() for name, _, _ in LINEARS}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+
+def run_e2e(args, nv, torch, dev, wl, world):
+    """The same step through the public API, with its inputs copied from pinned host memory and its result
+    read back to pinned host memory inside the timed region. Inputs: every layer's bf16 weights (the
+    refresh's input; one pinned host copy per weight shape is sent to every layer) and the step's
+    activations; the result: the outputs of every linear as they stand at the end of the step (the last
+    layer's). The copies are the bound (the host link), so they run on a copy stream, layer by layer, and
+    each layer is refreshed and run as soon as its weights have landed."""
+    cfg, L = wl.cfg, wl.layers
+    lin = cfg["linears"]
+    host_w = {name: wl.W[0][name].cpu().pin_memory() for name, _, _ in lin}
+    host_x, dev_x = {}, {}
+    for phase, P in wl.phases.items():
+        for key in ("x_in", "x_res", "attn", "act"):
+            host_x[(phase, key)] = P["buf"][key].cpu().pin_memory()
+            dev_x[(phase, key)] = P["buf"][key]
+    host_out = {(phase, name): torch.empty(P["Y"][name].shape, dtype=torch.bfloat16).pin_memory()
+                for phase, P in wl.phases.items() for name, _, _ in lin}
+    h2d = L * sum(t.numel() * t.element_size() for t in host_w.values()) + \
         sum(t.numel() * t.element_size() for t in host_x.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     stream = torch.cuda.current_stream(dev)
     copy_stream = torch.cuda.Stream(dev)
-    inputs_e2e = {"q": h1, "o": dev_x["attn"], "gate": h2, "up": h2, "down": dev_x["act"]}
-    wsq_e2e = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
-    order = [name for name, n, k in sorted(LINEARS, key=lambda t: -t[1] * t[2])]  # largest first
     ev_x = torch.cuda.Event()
-    ev_w = {name: torch.cuda.Event() for name in order}
+    ev_w = [torch.cuda.Event() for _ in range(L)]
+    read_w = [torch.cuda.Event() for _ in range(L)]  # layer l's weights have been read by its refresh
     done = torch.cuda.Event()
+    for e in read_w:
+        e.record(stream)
     done.record(stream)
 
     def step(k):
-        # inputs: the copy stream may overwrite them once the previous step has read them
-        copy_stream.wait_event(done)
         with torch.cuda.stream(copy_stream):
-            for key in host_x:
-                dev_x[key].copy_(host_x[key], non_blocking=True)
+            copy_stream.wait_event(done)  # the previous step has read its activations
+            for key, h in host_x.items():
+                dev_x[key].copy_(h, non_blocking=True)
             ev_x.record(copy_stream)
-            for name in order:
-                W[name].copy_(host_in[name], non_blocking=True)
-                ev_w[name].record(copy_stream)
+            for l in range(L):
+                copy_stream.wait_event(read_w[l])
+                for name, _, _ in lin:
+                    wl.W[l][name].copy_(host_w[name], non_blocking=True)
+                ev_w[l].record(copy_stream)
         stream.wait_event(ev_x)
-        sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
-        nv.rmsnorm_aqn(dev_x["x_in"], w1, eps[k], sigma, 1e-6, out=h1)
-        nv.rmsnorm_aqn(dev_x["x_res"], w2, eps[k], sigma, 1e-6, out=h2)
-        for name in order:
-            stream.wait_event(ev_w[name])
-            c, s, g, _ = Q[name]
-            nv.nvfp4_quantize(W[name], codes=c, scales=s, g=g, workspace=wsq_e2e)
-            A, B = lora[name]
-            nv.nvfp4_lora_linear(inputs_e2e[name], c, s, g, A, B, S_LORA, out=Y[name], workspace=ws)
-            host_out[name].copy_(Y[name], non_blocking=True)
+        for l in range(L):
+            stream.wait_event(ev_w[l])
+            wl.step(nv, k, only={"weight_refresh"}, layer_sel=[l])
+            read_w[l].record(stream)
+            wl.step(nv, k, only=set(wl.ops()) - {"weight_refresh"}, layer_sel=[l])
+        for (phase, name), h in host_out.items():
+            h.copy_(wl.phases[phase]["Y"][name], non_blocking=True)
         done.record(stream)
 
-    for i in range(max(1, args.warmup)):
+    for i in range(max(1, min(args.warmup, 2))):
         step(i % (KSCHED + 1))
     torch.cuda.synchronize()
-    n = max(1, args.steps)
+    n = max(1, min(args.steps, args.e2e_steps))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     done.record(stream)  # the first step's copies start after the timed region has begun
@@ -821,64 +958,93 @@ def run_e2e(args, nv, torch, dev, W, lora, x_in, x_res, attn, act, w1, w2, eps, 
     if world > 1:
         import torch.distributed as dist
         ms = max_over_ranks(ms, dev, world, dist)
-    return {"value": job_throughput(step_bytes(), world, ms), "unit": "GB/s", "ms_per_step": ms,
+    units, scale = step_units(cfg, L)
+    return {"value": job_throughput(units, world, ms, scale), "unit": cfg["unit"], "ms_per_step": ms, "steps": n,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
 
-def oracle_sample(den: int):
-    """A bounded sample of the same step, run by the CPU oracle: RMSNorm of all 64 tokens twice, the NVFP4
-    encoding of 1/den of each weight's rows, and every linear's outputs for those 1/den of its output rows
-    (all 64 tokens). Returns (algorithmic bytes of the sample, seconds, threads)."""
+_SAMPLE_INPUTS = {}
+
+
+def _sample_input(key, make):
+    """Seeded sample inputs, generated once per process (their generation is not part of the timing)."""
+    if key not in _SAMPLE_INPUTS:
+        _SAMPLE_INPUTS[key] = make()
+    return _SAMPLE_INPUTS[key]
+
+
+def oracle_sample(cfg, den: int):
+    """A bounded sample of one layer of the step, run by the CPU oracle: RMSNorm-AQN of 1/den of each
+    phase's tokens (twice), the NVFP4 encoding of 1/den of each weight's rows, and each linear's outputs
+    for those rows: W4A16 on every decode token, W4A4 on 1/32 of the prefill tokens (g_x over all of
+    them). Returns (metric units of the sample, seconds, threads, description)."""
     import oracle
     import synth
-    t_total, bytes_total = 0.0, 0.0
+    H, r = cfg["hidden"], cfg["rank"]
+    md, mp = cfg["decode_m"], cfg["prefill_m"]
+    t_total, flops, nbytes = 0.0, 0.0, 0.0
     nthreads = oracle.threads()
-    x = synth.activation_bf16(M_TOK, HIDDEN, 9, 0)
-    w = synth.aqn_weight(HIDDEN, 9, 1)
-    e = synth.aqn_eps(HIDDEN, 9, 2)
-    t0 = time.perf_counter()
-    oracle.rmsnorm_aqn(x, w, e, np.float32(SIGMA0), 1e-6)
-    oracle.rmsnorm_aqn(x, w, e, np.float32(SIGMA0), 1e-6)
-    t_total += time.perf_counter() - t0
-    bytes_total += 2 * bytes_rmsnorm(M_TOK, HIDDEN)
-    for i, (name, n, k) in enumerate(LINEARS):
-        rows = n // den
-        Wb = synth.weight_bf16(rows, k, 0.02, 9, 10 + i, outlier_frac=0.01)
+    w = synth.aqn_weight(H, 9, 1)
+    e = synth.aqn_eps(H, 9, 2)
+    for phase, M in (("d", md), ("p", mp)):
+        if not M:
+            continue
+        mr = max(1, M // den)
+        x = _sample_input(("x", mr, H, M), lambda: synth.activation_bf16(mr, H, 9, 3, M))
+        t0 = time.perf_counter()
+        oracle.rmsnorm_aqn(x, w, e, np.float32(SIGMA0), 1e-6)
+        oracle.rmsnorm_aqn(x, w, e, np.float32(SIGMA0), 1e-6)
+        t_total += time.perf_counter() - t0
+        nbytes += 2 * bytes_rmsnorm(mr, H)
+    for i, (name, n, k) in enumerate(cfg["linears"]):
+        rows = max(1, n // den)
+        Wb = _sample_input(("w", rows, k, cfg["std"], cfg["outliers"], i),
+                           lambda: synth.weight_bf16(rows, k, cfg["std"], 9, 10 + i, outlier_frac=cfg["outliers"]))
         t0 = time.perf_counter()
         codes, scales, g = oracle.quantize(Wb)
         t_total += time.perf_counter() - t0
-        bytes_total += bytes_quantize(rows * k)
-        A, B = synth.lora_factors(RANK, k, rows, 9, 20 + i)
-        xi = synth.activation_bf16(M_TOK, k, 9, 30 + i)
+        nbytes += bytes_quantize(rows * k)
+        A, B = _sample_input(("lora", r, k, rows, i), lambda: synth.lora_factors(r, k, rows, 9, 20 + i))
+        xi = _sample_input(("d", md, k), lambda: synth.activation_bf16(md, k, 9, 30, k))
         t0 = time.perf_counter()
         oracle.lora_linear_w4a16(xi, codes, scales, g, A, B, S_LORA)
         t_total += time.perf_counter() - t0
-        bytes_total += bytes_linear(M_TOK, rows, k, RANK)
-    return bytes_total, t_total, nthreads
-
-
-def sample_den(seconds_budget: float) -> int:
-    """The smallest sampling denominator (1/den of every weight) whose oracle run fits the budget,
-    extrapolated from a 1/64 probe run."""
-    _, t64, _ = oracle_sample(64)
-    for den in (1, 2, 4, 8, 16, 32):
-        if t64 * 64 / den <= seconds_budget:
-            return den
-    return 64
-
-
-def sample_desc(den: int) -> str:
+        flops += flops_linear(md, rows, k, r)
+        nbytes += bytes_linear(md, rows, k, r)
+        if mp:
+            xp = _sample_input(("p", mp, k), lambda: synth.heavy_tail_activation_bf16(mp, k, 9, 31, k))
+            sel = np.arange(0, mp, 32)
+            t0 = time.perf_counter()
+            oracle.lora_linear_w4a4(xp, codes, scales, g, A, B, S_LORA, rows=sel)
+            t_total += time.perf_counter() - t0
+            flops += flops_linear(len(sel), rows, k, r)
+            nbytes += bytes_linear_w4a4(len(sel), rows, k, r)
     frac = "all" if den == 1 else f"1/{den}"
-    return (f"RMSNorm-AQN of the 64x3584 tokens twice; NVFP4 encoding of {frac} of each weight's rows; "
-            f"each LoRA linear on those rows' outputs for all 64 tokens (fp64 oracle)")
+    desc = (f"one layer: RMSNorm-AQN of {frac} of the tokens twice; NVFP4 encoding of {frac} of each weight's rows; "
+            f"each LoRA linear on those rows' outputs for all {md} decode tokens (W4A16)"
+            + (f" and 1/32 of the {mp} prefill tokens (W4A4, g_x over all of them)" if mp else "") + " (fp64 oracle)")
+    units = flops if cfg["unit"] == "TFLOP/s" else nbytes
+    return units, t_total, nthreads, desc
 
 
-def cpu_baseline(seconds_budget=20.0):
-    den = sample_den(seconds_budget)
-    b, t, th = oracle_sample(den)
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": sample_desc(den),
+def sample_den(cfg, seconds_budget: float) -> int:
+    """The smallest sampling denominator whose oracle run fits the budget, extrapolated from a probe run at
+    the config's probe denominator."""
+    probe = cfg["probe_den"]
+    _, tp, _, _ = oracle_sample(cfg, probe)
+    den = 1
+    while den < probe and tp * probe / den > seconds_budget:
+        den *= 2
+    return den
+
+
+def cpu_baseline(cfg, seconds_budget=20.0):
+    den = sample_den(cfg, seconds_budget)
+    u, t, th, desc = oracle_sample(cfg, den)
+    scale = 1e12 if cfg["unit"] == "TFLOP/s" else 1e9
+    return {"value": u / t / scale, "unit": cfg["unit"], "cores": th, "kind": "oracle", "sample": desc,
             "sample_seconds": t}
 
 
@@ -887,24 +1053,25 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if not reference_runs_here(rank, world):
         return
+    cfg = CONFIGS[args.config]
     # each step is a sample sized so that warm-up and timed steps together take about two minutes
-    den = sample_den(120.0 / max(1, args.steps + args.warmup))
+    den = sample_den(cfg, 120.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(den)
-    tot_b, tot_t, th = 0.0, 0.0, 1
+        oracle_sample(cfg, den)
+    tot_u, tot_t, th, desc = 0.0, 0.0, 1, ""
     for _ in range(args.steps):
-        b, t, th = oracle_sample(den)
-        tot_b += b
+        u, t, th, desc = oracle_sample(cfg, den)
+        tot_u += u
         tot_t += t
-    v = tot_b / tot_t / 1e9
-    desc = sample_desc(den)
+    scale = 1e12 if cfg["unit"] == "TFLOP/s" else 1e9
+    v = tot_u / tot_t / scale
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "impl": "reference", "metric": METRIC, "value": v, "unit": cfg["unit"], "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_t / max(1, args.steps) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD, "sample": desc},
-        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": desc},
-        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": {"workload": cfg["workload"], "sample": desc},
+        "cpu_baseline": {"value": v, "unit": cfg["unit"], "cores": th, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": cfg["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
@@ -915,11 +1082,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="qwen32b", choices=sorted(CONFIGS))
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the config's)")
+    ap.add_argument("--e2e-steps", type=int, default=3, help="timed steps of the end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--op", default=None, help="time single ops of the step instead (see select_ops)")
     ap.add_argument("--suite", default=None, nargs="?", const="all",
-                    help="secondary measurements instead: all or any of w4a4_7b,w4a16_32b,w4a4_32b,moe,quantize_32b")
+                    help="secondary measurements instead: all or any of w4a4_7b,w4a16_32b,w4a4_32b,moe,quantize_32b,"
+                         "quantize_batch_32b,quantize_guided,rmsnorm_quantize,kv_attention,ais,rmsnorm_prefill")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -28,6 +28,15 @@
  *     NVFP4RL_ERR_CUDA. Inputs must be finite (not checked on the device).
  *   - Outputs must not overlap inputs (NVFP4RL_ERR_ALIAS).
  *   - Zero-sized problems (rows == 0, M == 0) are valid no-ops.
+ *   - Device state: on its first call on a device the library caches that device's attributes,
+ *     kernel attributes and the device addresses of its own __device__ variables (the status word,
+ *     the allocation-free scratch array). cudaDeviceReset() discards all of them on the GPU side:
+ *     after a reset of a device it has been used on, the library must not be called again in that
+ *     process.
+ *   - Device status: bounded device-side waits report through one status word per device, shared
+ *     by every stream and call on that device; nvfp4rl_device_status() synchronizes the device,
+ *     reads it and optionally clears it. A timeout is therefore attributed to the device, not to
+ *     one call or workspace.
  */
 #ifndef NVFP4RL_H_
 #define NVFP4RL_H_
@@ -314,14 +323,17 @@ NVFP4RL_API nvfp4rl_status rmsnorm_aqn_quantize(const uint16_t* x, int64_t M, in
  *   (QeRL explainer, "NVFP4量子化とLoRA": frozen NVFP4 base weights plus
  *   trainable low-rank factors):
  *   Y = x deq(W)^T + s (x A^T) B^T,  deq(W)[n][k] = e2m1(code) * E4M3(s_b) * w_g.
- *   x        [M][K] bf16 bits; K multiple of 256.
+ *   x        [M][K] bf16 bits; K multiple of 256 (one 256-K pipeline stage); M <= 65535.
  *   w_codes  [N][K/2], w_scales [N][K/16]: as written by nvfp4_quantize; N multiple of 128.
  *   w_g      one fp32 (device), the tensor's g.
- *   lora_A   [r][K] bf16 bits, lora_B [N][r] bf16 bits; r in [0, 256] (0: no LoRA,
- *            A and B may then be NULL).
+ *   lora_A   [r][K] bf16 bits, lora_B [N][r] bf16 bits; r = 0 (no LoRA, A and B may then be
+ *            NULL) or a multiple of 16 up to 128 (other ranks in [0, 256]:
+ *            NVFP4RL_ERR_UNSUPPORTED_SHAPE; outside it: NVFP4RL_ERR_INVALID_ARG).
  *   y        out, [M][N] bf16 bits.
  *   group_offsets, num_groups: must be NULL / 0 (grouped W4A16 is not provided).
- *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, M, N, K, r, 0).
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, M, N, K, r, 0): U = bf16(x A^T),
+ *            scratch, contents undefined between calls.
+ * Deterministic: split-K partial tiles are summed in a fixed order, so equal inputs give equal bits.
  */
 NVFP4RL_API nvfp4rl_status nvfp4_lora_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
                                  const uint8_t* w_scales, const float* w_g, int64_t N,
@@ -336,7 +348,7 @@ NVFP4RL_API nvfp4rl_status nvfp4_lora_linear(const uint16_t* x, int64_t M, int64
  *   unquantized bf16 x (TRACE summary, "論文が取り組む課題" and "実験結果と性能":
  *   FP4 weights and activations in the rollout):
  *   Y = deq(quant(x)) deq(W)^T + s (x A^T) B^T.
- *   Arguments as nvfp4_lora_linear, plus grouping:
+ *   Arguments, shape rules and determinism as nvfp4_lora_linear, plus grouping:
  *   group_offsets  NULL (dense) or device int32 [num_groups + 1], non-decreasing,
  *                  offsets[0] == 0, offsets[num_groups] == M: rows
  *                  [offsets[e], offsets[e+1]) use expert e's weights
@@ -380,13 +392,15 @@ NVFP4RL_API nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t cle
  *   planner, restricted runtimes that forbid cudaMalloc, code that must not grow its device
  *   footprint after start-up). The pages have no counterpart: this is a deployment entry
  *   point of this library, not part of the method.
- *   Same arguments and result as nvfp4_lora_linear (dense only). The scratch lives in a fixed
- *   array of nvfp4rl_noalloc_scratch_bytes() (16 MiB) that every GPU loading this library
- *   holds until the process exits. Nothing is allocated by the call.
+ *   Same arguments and result as nvfp4_lora_linear (dense only), bit for bit. The scratch lives
+ *   in a fixed array of nvfp4rl_noalloc_scratch_bytes() (4 MiB) that every GPU loading this
+ *   library holds until the process exits. Nothing is allocated by the call.
  *   - Returns NVFP4RL_ERR_WORKSPACE when the problem needs more scratch than the array
- *     (nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, ...) > 16 MiB).
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *     make that first call before any stream capture.
+ *     (nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, ...) > 4 MiB, i.e. M * r > 2^21).
+ *   - The first call on a device checks that it is a compute-capability 10.3 GPU
+ *     (NVFP4RL_ERR_DEVICE otherwise) and looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture. The address is
+ *     kept for the process: do not use this entry point after cudaDeviceReset() of that device.
  *   - All calls on a device share the array and each overwrites it: calls that may overlap
  *     on the GPU (unordered streams) race and must not be issued.
  */
@@ -395,7 +409,7 @@ NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_noalloc(const uint16_t* x, int64_t 
                                                      const uint16_t* lora_A, const uint16_t* lora_B, int32_t r,
                                                      float s, uint16_t* y, void* stream);
 
-/* Bytes of the fixed scratch array nvfp4_lora_linear_noalloc uses (16 MiB). Host only. */
+/* Bytes of the fixed scratch array nvfp4_lora_linear_noalloc uses (4 MiB). Host only. */
 NVFP4RL_API size_t nvfp4rl_noalloc_scratch_bytes(void);
 
 /*

@@ -393,7 +393,7 @@ def nvfp4_lora_linear_w4a4(x, codes, scales, g, A=None, B=None, s: float = 1.0, 
 
 def nvfp4_lora_linear_noalloc(x, codes, scales, g, A=None, B=None, s: float = 1.0, out=None, stream=None):
     """W4A16 LoRA linear without a workspace argument, for callers that cannot allocate device memory:
-    the library's fixed 16 MiB device array serves as scratch (see include/nvfp4rl.h). Outputs are still
+    the library's fixed 4 MiB device array serves as scratch (see include/nvfp4rl.h). Outputs are still
     the caller's (allocated here with torch only when `out` is None)."""
     import torch
     _require_cuda(x, codes, scales, g, A, B)

@@ -22,6 +22,22 @@ std::atomic<uint64_t> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups) {
+  if (w4a4) return w4a4_tc_supported(M, N, K, r) ? w4a4_tc_workspace_bytes(M, N, K, r, groups) : 0;
+  return w4a16_tc_supported(M, N, K, r) ? w4a16_tc_workspace_bytes(M, N, K, r, kPlanSMs) : 0;
+}
+
+// Both linears run on the tcgen05 kernels; the host checks admit only the shapes they take.
+nvfp4rl_status launch_linear(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
+  if (a.M == 0) return NVFP4RL_OK;
+  if (a.w4a4) {
+    if (!w4a4_tc_supported(a.M, a.N, a.K, a.r)) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+    return launch_w4a4_tc(a, ws, ws_bytes, dev, st);
+  }
+  if (!w4a16_tc_supported(a.M, a.N, a.K, a.r)) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  return launch_w4a16_tc(a, ws, ws_bytes, dev, st);
+}
+
 nvfp4rl_status current_device(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4RL_ERR_CUDA;
@@ -127,6 +143,7 @@ nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K,
                              const uint16_t* B, int32_t r, float s, const int32_t* offsets, int32_t groups,
                              uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
   if (M < 0 || K <= 0 || N <= 0 || r < 0 || r > 256) return NVFP4RL_ERR_INVALID_ARG;
+  if (r % 16 != 0 || r > kMaxLoraRank) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return NVFP4RL_OK;  // no activation rows: nothing to read or write
   if (!x || !w_codes || !w_scales || !w_g || !y) return NVFP4RL_ERR_INVALID_ARG;
   if (r > 0 && (!A || !B)) return NVFP4RL_ERR_INVALID_ARG;
@@ -144,7 +161,8 @@ nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K,
   if (reinterpret_cast<uintptr_t>(w_g) & 3u) return NVFP4RL_ERR_MISALIGNED;
   const int G = offsets ? groups : 1;
   const size_t need = linear_workspace_bytes(w4a4, M, N, K, r, G);
-  if (M > 0 && (!ws || ws_bytes < need)) return NVFP4RL_ERR_WORKSPACE;
+  if (need == 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (!ws || ws_bytes < need) return NVFP4RL_ERR_WORKSPACE;
   const size_t ybytes = static_cast<size_t>(M) * N * 2;
   const void* ins[] = {x, w_codes, w_scales, w_g, A, B, offsets, ws};
   const size_t isz[] = {static_cast<size_t>(M) * K * 2, static_cast<size_t>(G) * N * K / 2,

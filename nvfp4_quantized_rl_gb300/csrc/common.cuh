@@ -111,7 +111,7 @@ inline nvfp4rl_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? NVFP4RL_OK : NVFP4RL_ERR_CUDA;
 }
 
-// ---- internal launchers (quantize.cu, rmsnorm.cu, linear.cu) -------------------------------
+// ---- internal launchers (quantize.cu, rmsnorm.cu, linear_tc.cu, linear_w4a4_tc.cu, ...) -----------
 
 // Quantization scratch: one 32-bit word holding the running amax bits.
 constexpr size_t kQuantizeWorkspace = 256;
@@ -186,6 +186,11 @@ struct LinearArgs {
   bool w4a4;
 };
 
+// LoRA ranks the linears take: 0 (no LoRA) or a multiple of 16 up to this bound (the rank is the K
+// of the up-projection MMA, 16 per instruction; both LoRA tiles stay resident in shared memory).
+constexpr int kMaxLoraRank = 128;
+
+// Workspace bytes of a linear call (0 when the shape is not supported).
 size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups);
 
 // Split-K planning uses at most this many SMs, so workspace sizes do not depend on the device.

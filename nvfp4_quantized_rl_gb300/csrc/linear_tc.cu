@@ -634,18 +634,19 @@ struct TcPlan {
   size_t smem_bytes, ws_u, ws_total;
 };
 
-// Tile shape, shared-memory rings and workspace (U only). For decode tiles (64 tokens) the rings
-// leave room for one LoRA-down CTA on the same SM, so that kernel never delays a CTA of this one.
-// The activation ring has ring_depth stages; the weight ring takes the rest (at most 8 stages).
-TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
+// Tile shape, shared-memory rings and workspace (U only), for `mbox`-token tiles. With
+// reserve_down the rings leave room for one LoRA-down CTA on the same SM, so that kernel never
+// delays a CTA of this one. The activation ring has ring_depth stages; the weight ring takes the
+// rest (at most 8 stages).
+TcPlan plan_for(int64_t M, int64_t N, int r, int mbox, bool reserve_down) {
   TcPlan t{};
-  t.mbox = M <= 64 ? 64 : 128;
+  t.mbox = mbox;
   t.tiles_m = static_cast<int>((M + t.mbox - 1) / t.mbox);
   t.tiles_n = static_cast<int>(N / kRows);
   const size_t lora = r ? static_cast<size_t>(kRows + t.mbox) * 2 * r : 0;
   const size_t fixed = 1024 + lora + 512;
   const size_t xring = static_cast<size_t>(ring_depth(t.mbox)) * x_stage_bytes(t.mbox);
-  const size_t budget = 227 * 1024 - (r && t.mbox == 64 ? kDownSmem + 1024 : 0);
+  const size_t budget = 227 * 1024 - (reserve_down ? kDownSmem + 1024 : 0);
   t.w_stages = budget > fixed + xring ? static_cast<int>(std::min<size_t>(8, (budget - fixed - xring) / kWStageBytes)) : 0;
   t.smem_bytes = fixed + xring + t.w_stages * kWStageBytes;
   size_t o = 0;
@@ -653,6 +654,20 @@ TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
   t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
   t.ws_total = o;
   return t;
+}
+
+// 128-token tiles when M exceeds one 64-token tile and two weight stages still fit beside the
+// 128-token activation ring and the LoRA tiles; otherwise 64-token tiles (always the case for
+// r = 128 at M > 64), leaving room for a LoRA-down CTA where that still leaves two weight stages.
+TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
+  (void)K;
+  if (M > 64) {
+    const TcPlan t = plan_for(M, N, r, 128, false);
+    if (t.w_stages >= 2) return t;
+  }
+  const TcPlan t = plan_for(M, N, r, 64, r > 0);
+  if (t.w_stages >= 2) return t;
+  return plan_for(M, N, r, 64, false);
 }
 
 template <int MBOX>
@@ -789,7 +804,7 @@ nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const u
 
 // True when the tcgen05 W4A16 path takes this shape.
 bool w4a16_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
-  if (!(M > 0 && N % kRows == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= 128)))) return false;
+  if (!(M > 0 && N % kRows == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= kMaxLoraRank)))) return false;
   const TcPlan t = plan(M, N, K, r);
   return t.w_stages >= 2;
 }

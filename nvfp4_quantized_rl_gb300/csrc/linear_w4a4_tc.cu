@@ -488,7 +488,7 @@ CUtensorMapSwizzle lora_map_swizzle(int box_bytes) {
 }  // namespace
 
 bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
-  return M > 0 && N % kTile == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= 128)) &&
+  return M > 0 && N % kTile == 0 && K % kKStage == 0 && (r == 0 || (r % 16 == 0 && r <= kMaxLoraRank)) &&
          w4a4_plan(M, K, r, 1).stages >= 2;
 }
 

@@ -10,13 +10,17 @@
 // (on the first call on that device, with that device current) and passes it on as the
 // workspace. Every call on a device shares the one array; calls that overlap on the GPU (on
 // different streams without ordering) race on it.
+//
+// The W4A16 workspace holds only U = bf16(x A^T), M * max(r, 1) * 2 bytes rounded up to 256:
+// 4 MiB covers M * r up to 2^21 (e.g. 16384 tokens at rank 128, 65535 tokens at rank 32);
+// larger problems are rejected with NVFP4RL_ERR_WORKSPACE.
 #include <mutex>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;  // 4 MiB
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -32,20 +36,29 @@ extern "C" nvfp4rl_status nvfp4_lora_linear_noalloc(const uint16_t* x, int64_t M
   if (M < 0 || K <= 0 || N <= 0 || r < 0 || r > 256) return NVFP4RL_ERR_INVALID_ARG;
   if (M == 0) return NVFP4RL_OK;
   const size_t need = nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, M, N, K, r, 0);
-  if (need == 0) return NVFP4RL_ERR_INVALID_ARG;
+  // A shape the linear does not take: nvfp4_lora_linear reports which argument is wrong, and
+  // launches nothing.
+  if (need == 0)
+    return nvfp4_lora_linear(x, M, K, w_codes, w_scales, w_g, N, lora_A, lora_B, r, s, nullptr, 0, y, nullptr, 0,
+                             stream);
   if (need > kNoallocScratchBytes) return NVFP4RL_ERR_WORKSPACE;  // the problem needs more than the fixed array
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4RL_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return NVFP4RL_ERR_DEVICE;
+  // The current device must be one this library's kernels run on before its module is touched.
+  nvfp4rl::DeviceInfo dev;
+  const nvfp4rl_status ds = nvfp4rl::current_device(&dev);
+  if (ds != NVFP4RL_OK) return ds;
+  if (dev.device < 0 || dev.device >= 64) return NVFP4RL_ERR_DEVICE;
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_ptr[dev.device]) {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return NVFP4RL_ERR_CUDA;
-      g_noalloc_ptr[dev] = p;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();  // leave no error pending for the next call's launch check
+        return NVFP4RL_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev.device] = p;
     }
-    scratch = g_noalloc_ptr[dev];
+    scratch = g_noalloc_ptr[dev.device];
   }
   // Nothing in the workspace has to start at zero: every call writes what it later reads.
   return nvfp4_lora_linear(x, M, K, w_codes, w_scales, w_g, N, lora_A, lora_B, r, s, nullptr, 0, y, scratch,

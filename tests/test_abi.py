@@ -213,6 +213,17 @@ def test_linear_validation(nv):
     assert _lin(nv, fn="nvfp4_lora_linear_w4a4", off=0x90000, G=0) == 1
     assert _lin(nv, fn="nvfp4_lora_linear_w4a4", off=0x90000, G=4, r=16, A=0x70000, B=0x80000) == 1
     assert _lin(nv, s=float("nan")) == 1
+    # LoRA ranks: 0 or a multiple of 16 up to 128 (both tcgen05 kernels); others in [0, 256] are
+    # unsupported shapes, above 256 invalid
+    for fn in ("nvfp4_lora_linear", "nvfp4_lora_linear_w4a4"):
+        for bad_r in (8, 24, 136, 144, 256):
+            assert _lin(nv, fn=fn, r=bad_r, A=0x70000, B=0x80000) == 3, (fn, bad_r)
+    assert _lin(nv, M=65536) == 3              # above the largest M
+    for op in (nv.OP_LINEAR_W4A16, nv.OP_LINEAR_W4A4):
+        assert nv.workspace_bytes(op, 64, 256, 512, 8) == 0
+        assert nv.workspace_bytes(op, 64, 256, 512, 136) == 0
+        for r in (0, 16, 64, 128):
+            assert nv.workspace_bytes(op, 200, 256, 512, r) > 0, (op, r)
 
 
 def test_rmsnorm_validation(nv):

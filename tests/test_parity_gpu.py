@@ -196,6 +196,23 @@ def test_quantize_moe_experts_guided(nv):
             assert_quant_equal(gpu_quantize(nv, W), oracle.quantize(W), f"expert {e}.{j} plain")
 
 
+def test_quantize_moe_guided_layers_sampled(nv):
+    """Every guided layer of the MoE model (36..47 of 48): a seeded 1/32 of each layer's expert
+    tensors (4 experts x gate, up, down), guided with that tensor's Bernoulli(1/2) mask, every block
+    against the oracle."""
+    cfg = synth.MOE
+    H, I = cfg["hidden"], cfg["intermediate"]
+    shapes = [(I, H), (I, H), (H, I)]
+    for layer in cfg["guided_layers"]:
+        experts = np.random.default_rng(1000 + layer).choice(cfg["experts"], 4, replace=False)
+        for e in experts:
+            for j, (n, k) in enumerate(shapes):
+                W = synth.weight_bf16(n, k, 0.02, layer, int(e), j)
+                mask = synth.guided_mask(W.size, layer, int(e), j, 99)
+                assert_quant_equal(gpu_quantize(nv, W, mask=mask), oracle.quantize(W, mask=mask),
+                                   f"layer {layer} expert {e}.{j} guided")
+
+
 # ---------------------------------------------------------------- TRACE record and cached replay
 
 def _mask_bits(words, n):
@@ -534,7 +551,7 @@ def test_linear_tiny(nv, w4a4):
 
 @pytest.mark.parametrize("w4a4", [False, True], ids=["w4a16", "w4a4"])
 @pytest.mark.parametrize("M,N,K,r,s", [(100, 384, 768, 32, 2.0), (1, 128, 256, 0, 2.0), (65, 256, 512, 16, 0.0),
-                                       (200, 640, 1024, 64, 0.5)])
+                                       (200, 640, 1024, 64, 0.5), (200, 384, 1024, 128, 1.0), (64, 256, 512, 128, 2.0)])
 def test_linear_multi_tile_ragged(nv, w4a4, M, N, K, r, s):
     q = _weights(N, K, 11, M, N)
     x = synth.heavy_tail_activation_bf16(M, K, 12, M) if w4a4 else synth.activation_bf16(M, K, 12, M)
@@ -549,6 +566,45 @@ def test_linear_empty_is_a_noop(nv):
     y = nv.nvfp4_lora_linear(x, P.dev(q[0]), P.dev(q[1]), P.dev(np.atleast_1d(q[2])))
     torch.cuda.synchronize()
     assert y.shape == (0, 128)
+
+
+@pytest.mark.parametrize("w4a4", [False, True], ids=["w4a16", "w4a4"])
+@pytest.mark.parametrize("shift", [15, 17])
+def test_linear_small_scale_bytes(nv, w4a4, shift):
+    """Weights quantized against a per-tensor amax 2^shift above their own, so that almost every block
+    scale byte is zero or an E4M3 subnormal (0x00..0x07; the all-zero rows of W too), and the output
+    is made of those blocks alone: the dequantization of small scale bytes is what the GEMM bar sees."""
+    M, N, K, r = 96, 384, 1024, 32
+    W = synth.weight_bf16(N, K, 0.02, 81, shift)
+    W[5] = 0  # all-zero rows: scale byte 0
+    W[200] = 0
+    amax = float(np.abs(synth.bf16_to_f32(W)).max())
+    q = oracle.quantize(W, amax_in=amax * 2.0 ** shift)
+    sb = q[1]
+    assert (sb <= 7).all() and (sb == 0).any() and len(np.unique(sb)) >= 3, np.unique(sb)
+    x = synth.activation_bf16(M, K, 82, shift)
+    A, B = synth.lora_factors(r, K, N, 83, shift)
+    y = gpu_linear(nv, w4a4, x, q, A, B, 0.5)
+    P.assert_gemm_close(y, ref_linear(w4a4, x, q, A, B, 0.5), f"small weight scales (2^-{shift})")
+
+
+def test_w4a4_small_activation_scale_bytes(nv):
+    """W4A4 with activations whose per-tensor amax sits in row 0 while every other row is 2^16 smaller:
+    the activation quantizer gives those rows zero or subnormal block scale bytes, which the block-scaled
+    MMA must decode exactly. Rows 1.. are compared on their own (row 0 dominates the output's rms)."""
+    M, N, K = 130, 256, 512
+    x = synth.bf16_to_f32(synth.activation_bf16(M, K, 84, 0))
+    x[1:] *= np.float32(2.0 ** -16)
+    x[7] = 0.0
+    xb = synth.bf16_bits(x)
+    q = _weights(N, K, 85, 0)
+    gx = oracle.global_scale(oracle.amax(xb))
+    _, xs = oracle.quantize_rows_given_g(xb, gx, np.arange(M))
+    assert (xs[1:] <= 7).mean() > 0.99 and (xs[1:] == 0).any(), np.unique(xs[1:])
+    y = gpu_linear(nv, True, xb, q, None, None, 0.0)
+    ref = ref_linear(True, xb, q, None, None, 0.0)
+    P.assert_gemm_close(y[:1], ref[:1], "row 0 (normal scales)")
+    P.assert_gemm_close(y[1:], ref[1:], "rows 1.. (subnormal activation scales)")
 
 
 def test_linear_qwen7b_decode_full(nv):
@@ -578,14 +634,34 @@ def test_w4a4_qwen7b_prefill_sampled(nv):
         P.assert_gemm_close(y[rows], ref_linear(True, xi, q, A, B, 2.0, rows=rows), f"7B W4A4 {name}")
 
 
-def test_qwen32b_decode_and_prefill_sampled(nv):
+@pytest.fixture(scope="module")
+def qwen32b_layer():
+    """The seven bf16 weights of one Qwen2.5-32B-shaped layer (~N(0, 0.015)) and the oracle's NVFP4
+    encoding of each, shared by the quantization and the linear parity tests."""
+    out = {}
+    for i, (name, (n, k)) in enumerate(synth.QWEN25_32B["linears"].items()):
+        W = synth.weight_bf16(n, k, 0.015, 3, i)
+        out[name] = (W, oracle.quantize(W))
+    return out
+
+
+def test_quantize_qwen32b_layer_full(nv, qwen32b_layer):
+    """Standalone nvfp4_quantize of all seven 32B-shaped weights (q, k, v, o, gate, up, down), every
+    output byte against the oracle."""
+    for name, (W, want) in qwen32b_layer.items():
+        assert_quant_equal(gpu_quantize(nv, W), want, f"32B {name}")
+
+
+def test_qwen32b_decode_and_prefill_sampled(nv, qwen32b_layer):
+    """All seven 32B-shaped linears (r = 64): W4A16 at M = 256 and W4A4 at M = 8192, sampled rows."""
     rows256 = np.arange(0, 256, 8)
     rows8k = np.sort(np.random.default_rng(41).choice(8192, 24, replace=False))
-    x256 = synth.activation_bf16(256, 5120, 40, 0)
-    x8k = synth.heavy_tail_activation_bf16(8192, 5120, 40, 1)
-    for i, name in enumerate(["q", "k", "gate"]):
-        n, k = synth.QWEN25_32B["linears"][name]
-        q = _weights(n, k, 3, i, std=0.015, outliers=0.0)
+    xs = {}
+    for i, (name, (W, q)) in enumerate(qwen32b_layer.items()):
+        n, k = W.shape
+        if k not in xs:
+            xs[k] = (synth.activation_bf16(256, k, 40, k), synth.heavy_tail_activation_bf16(8192, k, 40, k + 1))
+        x256, x8k = xs[k]
         A, B = synth.lora_factors(64, k, n, 42, i)
         y = gpu_linear(nv, False, x256, q, A, B, 2.0)
         P.assert_gemm_close(y[rows256], ref_linear(False, x256, q, A, B, 2.0, rows=rows256), f"32B M=256 {name}")
