@@ -70,8 +70,13 @@ constexpr int kDownM = 64;        // activation rows per LoRA-down cluster
 constexpr int kDownPad = 8;       // bf16 row padding (conflict-free ldmatrix)
 constexpr int kDownStages = 3;    // chunks in flight (cp.async ring)
 constexpr int kDownCluster = 16;  // CTAs per LoRA-down cluster (K split); 8 where 16 is not available
-constexpr int kDownStageElems = (kDownM + 32) * (kDownK + kDownPad);
-constexpr int kDownSmem = kDownStages * kDownStageElems * 2 + kDownM * 32 * 4;
+// One pass of the kernel covers RP ranks (32, or 64 so that r = 64 reads x once).
+template <int RP>
+struct DownShape {
+  static constexpr int kStageElems = (kDownM + RP) * (kDownK + kDownPad);
+  static constexpr int kSmem = kDownStages * kStageElems * 2 + kDownM * RP * 4;
+};
+constexpr int kDownSmem = DownShape<32>::kSmem;  // the decode instance, which shares an SM with the main kernel
 
 struct TcParams {
   int64_t M, N, K;
@@ -502,11 +507,13 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // LoRA down-projection U = bf16(x A^T), [M][r]. A cluster of CTAs (blockIdx.x, 16 or 8) covers 64
 // rows of x (blockIdx.y); CTA q takes a contiguous range of the 64-K chunks. A ring of three
-// chunk buffers is filled with cp.async (x: 64 x 64, A: 32 x 64 bf16) while mma.sync m16n8k16
-// runs on the oldest (warp w: rows 16w..16w+15, 32 ranks per pass), accumulating in registers.
-// The fp32 partial [64][32] goes to shared memory; after a cluster barrier, CTA q sums its share
-// of the rows over all CTAs' partials in rank order (distributed shared memory) and writes U.
-// Rows past M read as zero and are not written.
+// chunk buffers is filled with cp.async (x: 64 x 64, A: RP x 64 bf16) while mma.sync m16n8k16
+// runs on the oldest (warp w: rows 16w..16w+15, RP ranks per pass over x), accumulating in
+// registers. The fp32 partial [64][RP] goes to shared memory; after a cluster barrier, CTA q sums
+// its share of the rows over all CTAs' partials in rank order (distributed shared memory) and
+// writes U. Rows past M read as zero and are not written. Each rank's sum runs through the same
+// chunks and instructions whatever RP is, so U does not depend on it.
+template <int RP>
 __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                               const uint16_t* __restrict__ A, int r,
                                                               uint16_t* __restrict__ U) {
@@ -516,8 +523,9 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
   griddep_wait();
   griddep_launch_dependents();
   extern __shared__ __align__(16) uint8_t down_smem[];
-  uint16_t* ring = reinterpret_cast<uint16_t*>(down_smem);  // [kDownStages][96][kDownK + kDownPad]
-  float(*part)[32] = reinterpret_cast<float(*)[32]>(down_smem + kDownStages * kDownStageElems * 2);
+  constexpr int kDownStageElems = DownShape<RP>::kStageElems;
+  uint16_t* ring = reinterpret_cast<uint16_t*>(down_smem);  // [kDownStages][64 + RP][kDownK + kDownPad]
+  float(*part)[RP] = reinterpret_cast<float(*)[RP]>(down_smem + kDownStages * kDownStageElems * 2);
   constexpr int kRow = kDownK + kDownPad;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kDownM;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -525,13 +533,13 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
   const int q = static_cast<int>(cluster_ctarank());
   const int nchunks = static_cast<int>(K / kDownK);
   const int cb = q * nchunks / C, n = (q + 1) * nchunks / C - cb;
-  for (int j0 = 0; j0 < r; j0 += 32) {
-    // one chunk: rows 0..63 of the buffer hold x, rows 64..95 hold A (ranks j0..j0+31)
+  for (int j0 = 0; j0 < r; j0 += RP) {
+    // one chunk: rows 0..63 of the buffer hold x, rows 64..63+RP hold A (ranks j0..j0+RP-1)
     auto load = [&](int i, int buf) {
       uint16_t* b = ring + buf * kDownStageElems;
       const int64_t k0 = static_cast<int64_t>(cb + i) * kDownK;
 #pragma unroll
-      for (int u = 0; u < (96 * kDownK / 8) / 128; ++u) {  // 96 rows x 8 vectors of 8 bf16
+      for (int u = 0; u < ((kDownM + RP) * kDownK / 8) / 128; ++u) {  // 64 + RP rows x 8 vectors of 8 bf16
         const int idx = tid + u * 128, row = idx >> 3, vec = idx & 7;
         uint16_t* dst = b + row * kRow + vec * 8;
         const uint16_t* src = nullptr;
@@ -544,7 +552,7 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
         else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
       }
     };
-    float c[4][4] = {};
+    float c[RP / 8][4] = {};
 #pragma unroll
     for (int st = 0; st < kDownStages - 1; ++st) {
       if (st < n) load(st, st);
@@ -563,7 +571,7 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
         ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(xs + (warp * 16 + (lane & 15)) * kRow + ks * 16 + (lane >> 4) * 8)),
                 a[0], a[1], a[2], a[3]);
 #pragma unroll
-        for (int jp = 0; jp < 2; ++jp) {
+        for (int jp = 0; jp < RP / 16; ++jp) {
           const int g8 = lane >> 3;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(as + (jp * 16 + (g8 >> 1) * 8 + (lane & 7)) * kRow + ks * 16 + (g8 & 1) * 8)),
@@ -576,15 +584,15 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
     cp_async_wait<0>();
     // C fragment: c0,c1 at (row lane/4, cols 2(lane%4), +1); c2,c3 at row + 8
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < RP / 8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         part[warp * 16 + (lane >> 2) + (e >> 1) * 8][nt * 8 + 2 * (lane & 3) + (e & 1)] = c[nt][e];
     cluster_sync_all();
     // CTA q: rows [q*64/C, (q+1)*64/C), four ranks per thread and step
     const int rb = q * kDownM / C, re = (q + 1) * kDownM / C;
-    for (int idx = tid; idx < (re - rb) * 8; idx += 128) {
-      const int row = rb + idx / 8, j4 = (idx % 8) * 4;
+    for (int idx = tid; idx < (re - rb) * (RP / 4); idx += 128) {
+      const int row = rb + idx / (RP / 4), j4 = (idx % (RP / 4)) * 4;
       const int64_t m = m0 + row;
       const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(&part[row][j4]));
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -724,26 +732,25 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
   return make_tensor_map_2d(m, dt, base, cols, rows, esize, box_cols, box_rows, sw);
 }
 
-// Cluster size of the LoRA-down kernel on this device: 16 (non-portable) where a 16-CTA cluster
-// of it can be resident, else 8. Also sets the kernel's attributes (once per device).
-int down_cluster_size(int device) {
+template <int RP>
+int down_cluster_size_for(int device) {
   static std::mutex mu;
   static std::map<int, int> cache;
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(device);
   if (it != cache.end()) return it->second;
   int c = 8;
+  const int smem = DownShape<RP>::kSmem;
+  auto* kern = w4a16_lora_down_kernel<RP>;
   const bool attrs =
-      cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDownSmem) ==
-          cudaSuccess &&
-      cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            static_cast<int>(cudaSharedmemCarveoutMaxShared)) == cudaSuccess;
-  if (attrs &&
-      cudaFuncSetAttribute(w4a16_lora_down_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+  if (attrs && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kDownCluster, 1, 1);
     cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = kDownSmem;
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kDownCluster;
@@ -752,14 +759,20 @@ int down_cluster_size(int device) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(w4a16_lora_down_kernel), &cfg) == cudaSuccess &&
-        n > 0)
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) == cudaSuccess && n > 0)
       c = kDownCluster;
   }
   cudaGetLastError();
   if (!attrs) c = 0;  // the kernel cannot be launched with its shared memory
   cache[device] = c;
   return c;
+}
+
+// Cluster size of the LoRA-down kernel (ranks-per-pass instance RP) on this device: 16
+// (non-portable) where a 16-CTA cluster of it can be resident, else 8; 0 when it cannot be
+// launched. Also sets the kernel's attributes (once per device).
+int down_cluster_size(int device, int rp) {
+  return rp == 64 ? down_cluster_size_for<64>(device) : down_cluster_size_for<32>(device);
 }
 
 }  // namespace
@@ -778,16 +791,25 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 }
 
 // LoRA down-projection: one cluster per 64 rows of x, K (a multiple of 64) split over the cluster.
+// Ranks per pass over x: 64 when r > 32 and M exceeds one decode tile (x is then read once for
+// r = 64); 32 otherwise, the instance whose shared memory leaves room beside a decode CTA of the
+// main kernel.
 nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
                                 const DeviceInfo& dev, cudaStream_t st) {
   const int nchunks = static_cast<int>(K / kDownK);
-  const int dc = down_cluster_size(dev.device);
+  const int rp = r > 32 && M > 64 ? 64 : 32;
+  const int dc = down_cluster_size(dev.device, rp);
   if (dc == 0) return NVFP4RL_ERR_CUDA;
-  const int cd = std::min(dc, nchunks);
+  // split K over a cluster only as far as the row blocks alone leave SMs idle (about three CTAs
+  // per SM in all)
+  const int64_t row_blocks = (M + kDownM - 1) / kDownM;
+  const int64_t want = std::max<int64_t>(1, (3 * static_cast<int64_t>(std::min(dev.sm_count, kPlanSMs)) + row_blocks - 1) /
+                                                row_blocks);
+  const int cd = static_cast<int>(std::min<int64_t>({static_cast<int64_t>(dc), static_cast<int64_t>(nchunks), want}));
   cudaLaunchConfig_t dcfg = {};
   dcfg.gridDim = dim3(cd, static_cast<unsigned>((M + kDownM - 1) / kDownM), 1);
   dcfg.blockDim = dim3(128);
-  dcfg.dynamicSmemBytes = kDownSmem;
+  dcfg.dynamicSmemBytes = rp == 64 ? DownShape<64>::kSmem : DownShape<32>::kSmem;
   dcfg.stream = st;
   cudaLaunchAttribute dattr[2];
   dattr[0].id = cudaLaunchAttributeClusterDimension;
@@ -798,7 +820,9 @@ nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const u
   dattr[1].val.programmaticStreamSerializationAllowed = 1;
   dcfg.attrs = dattr;
   dcfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel, x, M, K, A, r, U) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  const cudaError_t e = rp == 64 ? cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel<64>, x, M, K, A, r, U)
+                                 : cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel<32>, x, M, K, A, r, U);
+  if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }
 
