@@ -9,8 +9,10 @@ the path:
      block scales, fp32 g) of all seven weights, one nvfp4_quantize_batch call;
   2. decode, M = 256 tokens: RMSNorm-AQN of the input and of the residual stream,
      then the seven W4A16 LoRA linears;
-  3. prefill, M = 8192 tokens: RMSNorm-AQN twice, then the seven W4A4 LoRA linears
-     (activations quantized to NVFP4 on the fly, block-scaled FP4 MMA).
+  3. prefill, M = 8192 tokens: RMSNorm-AQN fused with the NVFP4 encoding of its output
+     (rmsnorm_aqn_quantize) for the input and the residual stream, then the seven W4A4 LoRA
+     linears (block-scaled FP4 MMA): q/k/v and gate/up on those shared NVFP4 activations
+     (nvfp4_lora_linear_w4a4_quantized), o and down quantizing theirs on the fly.
 One refresh thus serves 256 decode and 8192 prefill tokens per layer. `--config
 qwen7b-decode` runs the Qwen2.5-7B-shaped decode layer instead (M = 64, W4A16 only).
 Inputs are synthetic, generated on the device from a seed, and larger than L2: a
@@ -51,8 +53,9 @@ CONFIGS = {
     "qwen32b": {
         "workload": "qwen2.5-32b-shaped decoder layers, decode + prefill: hidden 5120, q/o 5120x5120, k/v 1024x5120, "
                     "gate/up 27648x5120, down 5120x27648 bf16 weights ~N(0,0.015); per layer: weight refresh (amax + "
-                    "NVFP4 encode) of all seven weights, RMSNorm-AQN x2 + W4A16 LoRA linears at M=256, RMSNorm-AQN x2 "
-                    "+ W4A4 LoRA linears at M=8192; LoRA r=64 s=2; AQN sigma 1e-2->5e-4 over K=10",
+                    "NVFP4 encode) of all seven weights, RMSNorm-AQN x2 + W4A16 LoRA linears at M=256, RMSNorm-AQN->NVFP4 "
+                    "x2 + W4A4 LoRA linears at M=8192 (q/k/v, gate/up on the shared NVFP4 activations); LoRA r=64 "
+                    "s=2; AQN sigma 1e-2->5e-4 over K=10",
         "hidden": 5120, "inter": 27648, "linears": LINEARS_32B, "std": 0.015, "outliers": 0.0, "rank": 64,
         "decode_m": 256, "prefill_m": 8192, "layers": 12, "unit": "TFLOP/s", "probe_den": 256,
     },
@@ -116,7 +119,7 @@ def layer_counts(cfg):
         "rms_d_bytes": 2 * bytes_rmsnorm(md, H),
         "w4a16_bytes": sum(bytes_linear(md, n, k, r) for _, n, k in lin),
         "w4a16_flops": sum(flops_linear(md, n, k, r) for _, n, k in lin),
-        "rms_p_bytes": 2 * bytes_rmsnorm(mp, H) if mp else 0.0,
+        "rms_p_bytes": 2 * (bytes_rmsnorm(mp, H) + 0.5625 * mp * H) if mp else 0.0,
         "w4a4_bytes": sum(bytes_linear_w4a4(mp, n, k, r) for _, n, k in lin) if mp else 0.0,
         "w4a4_flops": sum(flops_linear(mp, n, k, r) for _, n, k in lin) if mp else 0.0,
     }
@@ -302,6 +305,11 @@ class Workload:
                  "attn": randn(M, H).to(torch.bfloat16), "act": randn(M, I).to(torch.bfloat16),
                  "h1": torch.empty(M, H, dtype=torch.bfloat16, device=dev),
                  "h2": torch.empty(M, H, dtype=torch.bfloat16, device=dev)}
+            if w4a4:  # the normed inputs in NVFP4 as well (rmsnorm_aqn_quantize), shared by their linears
+                for h in ("h1", "h2"):
+                    b[h + "q"] = (torch.empty(M, H // 2, dtype=torch.uint8, device=dev),
+                                  torch.empty(M, H // 16, dtype=torch.uint8, device=dev),
+                                  torch.empty(1, dtype=torch.float32, device=dev))
             Y = {name: torch.empty(M, n, dtype=torch.bfloat16, device=dev) for name, n, k in cfg["linears"]}
             op = nv.OP_LINEAR_W4A4 if w4a4 else nv.OP_LINEAR_W4A16
             wsb = max(nv.workspace_bytes(op, M, n, k, r) for _, n, k in cfg["linears"])
@@ -310,6 +318,7 @@ class Workload:
         self.wsq = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE_BATCH, len(cfg["linears"]), 0, 0),
                                dtype=torch.uint8, device=dev)
         self.wsa = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
+        self.wsr = torch.empty(nv.workspace_bytes(nv.OP_RMSNORM_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
         self.amax = {name: torch.empty(1, dtype=torch.float32, device=dev) for name, _, _ in cfg["linears"]}
 
     def ops(self):
@@ -349,17 +358,31 @@ class Workload:
                         nv.nvfp4_quantize(W[name], amax_in=self.amax[name], codes=c, scales=s, g=g)
             for phase, P in self.phases.items():
                 b = P["buf"]
-                mark(f"rmsnorm_{phase}", lambda: (nv.rmsnorm_aqn(b["x_in"], self.w1, self.eps[k], sigma, 1e-6,
-                                                                 out=b["h1"]),
-                                                  nv.rmsnorm_aqn(b["x_res"], self.w2, self.eps[k], sigma, 1e-6,
-                                                                 out=b["h2"])))
-                fn = nv.nvfp4_lora_linear_w4a4 if P["w4a4"] else nv.nvfp4_lora_linear
+
+                def norms():
+                    for src, w, h in (("x_in", self.w1, "h1"), ("x_res", self.w2, "h2")):
+                        if P["w4a4"]:  # W4A4: RMSNorm-AQN and the NVFP4 encoding of its output in one call
+                            nv.rmsnorm_aqn_quantize(b[src], w, self.eps[k], sigma, 1e-6, out=b[h], codes=b[h + "q"][0],
+                                                    scales=b[h + "q"][1], g=b[h + "q"][2], workspace=self.wsr)
+                        else:
+                            nv.rmsnorm_aqn(b[src], w, self.eps[k], sigma, 1e-6, out=b[h])
+                mark(f"rmsnorm_{phase}", norms)
                 kind = "w4a4" if P["w4a4"] else "w4a16"
                 for name, _, _ in lin:
                     c, s, g = Q[name]
                     A, B = lora[name]
-                    mark(f"{kind}_{name}", lambda: fn(b[INPUT_OF[name]], c, s, g, A, B, S_LORA, out=P["Y"][name],
-                                                      workspace=P["ws"]))
+                    src = INPUT_OF[name]
+                    if not P["w4a4"]:
+                        fn = lambda: nv.nvfp4_lora_linear(b[src], c, s, g, A, B, S_LORA, out=P["Y"][name],
+                                                          workspace=P["ws"])
+                    elif src + "q" in b:  # activations already in NVFP4 (q/k/v, gate/up)
+                        xc, xs, xg = b[src + "q"]
+                        fn = lambda: nv.nvfp4_lora_linear_w4a4_quantized(b[src], xc, xs, xg, c, s, g, A, B, S_LORA,
+                                                                         out=P["Y"][name], workspace=P["ws"])
+                    else:  # o and down: quantized on the fly
+                        fn = lambda: nv.nvfp4_lora_linear_w4a4(b[src], c, s, g, A, B, S_LORA, out=P["Y"][name],
+                                                               workspace=P["ws"])
+                    mark(f"{kind}_{name}", fn)
 
 
 def run_gpu(args):
@@ -500,8 +523,10 @@ def summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, laun
             groups["lora_linear_w4a16"] = l_ms
         else:
             part["frac_fp4_tensor"] = tf / fp4_sus
-            part["note"] = (f"the full call (activation amax + NVFP4 encode, LoRA-down, w4a4_tc_kernel); fraction of "
-                            f"the dense FP4 peak = {FP4_PER_BF16:g} x sustained bf16 (the nominal 13.5 / 2.25 ratio)")
+            part["note"] = (f"the full calls: LoRA-down and the block-scaled GEMM; q/k/v and gate/up read the NVFP4 "
+                            f"activations rmsnorm_aqn_quantize wrote (timed under rmsnorm), o and down quantize theirs "
+                            f"(amax + encode) in the call; fraction of the dense FP4 peak = {FP4_PER_BF16:g} x "
+                            f"sustained bf16 (the nominal 13.5 / 2.25 ratio)")
             groups["lora_linear_w4a4"] = l_ms
         parts[f"lora_linear_{kind}_m{M}"] = part
     rms_ms = sum(op_ms[f"rmsnorm_{p}"] for p in ("d", "p") if f"rmsnorm_{p}" in op_ms)

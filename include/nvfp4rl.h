@@ -77,7 +77,8 @@ enum {
   NVFP4RL_OP_QUANTIZE_BATCH = 3, /* M = number of tensors */
   NVFP4RL_OP_RMSNORM_QUANTIZE = 4,
   NVFP4RL_OP_AIS = 5,
-  NVFP4RL_OP_KV_ATTENTION = 6 /* M = B, N = Hkv, K = Lmax */
+  NVFP4RL_OP_KV_ATTENTION = 6, /* M = B, N = Hkv, K = Lmax */
+  NVFP4RL_OP_LINEAR_W4A4_QUANTIZED = 7
 };
 
 /*
@@ -361,6 +362,27 @@ NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_w4a4(const uint16_t* x, int64_t M, 
                                       const uint16_t* lora_A, const uint16_t* lora_B, int32_t r, float s,
                                       const int32_t* group_offsets, int32_t num_groups, uint16_t* y,
                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * nvfp4_lora_linear_w4a4_quantized -- nvfp4_lora_linear_w4a4 on activations that are already in
+ *   NVFP4: the rollout's normalized activations quantized once (e.g. by rmsnorm_aqn_quantize) and
+ *   shared by every linear that reads them (TRACE summary, "論文が取り組む課題" and "実験結果と性能":
+ *   FP4 activations in the rollout; QeRL explainer, "NVFP4量子化とLoRA": the LoRA branch).
+ *   Y = deq(x_codes, x_scales, x_g) deq(W)^T + s (x A^T) B^T.
+ *   x_codes  [M][K/2], x_scales [M][K/16] (16-byte aligned), x_g one fp32 (4-byte aligned): the
+ *            NVFP4 encoding of the activations as nvfp4_quantize / rmsnorm_aqn_quantize write it.
+ *   x        [M][K] bf16 bits, the unquantized activations, read by the LoRA branch only; may be NULL
+ *            when r == 0.
+ *   Other arguments, shape rules, grouping and determinism as nvfp4_lora_linear_w4a4; given the codes
+ *   that nvfp4_lora_linear_w4a4 would compute from x, the result is the same bits.
+ *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A4_QUANTIZED, M, N, K, r, num_groups)
+ *            (U = bf16(x A^T) and the grouped tile map; no activation codes); it may overlap no input.
+ */
+NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_w4a4_quantized(
+    const uint16_t* x, const uint8_t* x_codes, const uint8_t* x_scales, const float* x_g, int64_t M, int64_t K,
+    const uint8_t* w_codes, const uint8_t* w_scales, const float* w_g, int64_t N, const uint16_t* lora_A,
+    const uint16_t* lora_B, int32_t r, float s, const int32_t* group_offsets, int32_t num_groups, uint16_t* y,
+    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes an operation needs for these sizes (0 on invalid sizes). */
 NVFP4RL_API size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r, int32_t num_groups);

@@ -24,8 +24,8 @@ LIB_PATH = _build.LIB
 
 OK = 0
 BF16, F32 = 0, 1
-OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH, OP_RMSNORM_QUANTIZE, OP_AIS, OP_KV_ATTENTION = (
-    0, 1, 2, 3, 4, 5, 6)
+(OP_QUANTIZE, OP_LINEAR_W4A16, OP_LINEAR_W4A4, OP_QUANTIZE_BATCH, OP_RMSNORM_QUANTIZE, OP_AIS, OP_KV_ATTENTION,
+ OP_LINEAR_W4A4_QUANTIZED) = (0, 1, 2, 3, 4, 5, 6, 7)
 
 _lock = threading.Lock()
 _lib = None
@@ -54,6 +54,8 @@ def _signatures():
         "nvfp4_lora_linear": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
         "nvfp4_lora_linear_w4a4": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p, p, sz, p]),
         "nvfp4_lora_linear_noalloc": (c.c_int, [p, i64, i64, p, p, p, i64, p, p, i32, f32, p, p]),
+        "nvfp4_lora_linear_w4a4_quantized": (c.c_int, [p, p, p, p, i64, i64, p, p, p, i64, p, p, i32, f32, p, i32, p,
+                                                       p, sz, p]),
         "nvfp4rl_noalloc_scratch_bytes": (sz, []),
         "nvfp4rl_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
         "nvfp4rl_status_string": (c.c_char_p, [c.c_int]),
@@ -389,6 +391,31 @@ def nvfp4_lora_linear_w4a4(x, codes, scales, g, A=None, B=None, s: float = 1.0, 
     with codes [G, N, K/2], scales [G, N, K/16], g [G]."""
     return _linear("nvfp4_lora_linear_w4a4", OP_LINEAR_W4A4, x, codes, scales, g, A, B, s, group_offsets,
                    num_groups, out, workspace, stream)
+
+
+def nvfp4_lora_linear_w4a4_quantized(x, x_codes, x_scales, x_g, codes, scales, g, A=None, B=None, s: float = 1.0,
+                                     group_offsets=None, num_groups: int = 0, out=None, workspace=None, stream=None):
+    """W4A4 on activations already in NVFP4 (x_codes [M, K/2], x_scales [M, K/16], x_g [1], e.g. from
+    rmsnorm_aqn_quantize); x is the bf16 activation the LoRA branch reads (may be None without LoRA)."""
+    import torch
+    _require_cuda(x_codes, x_scales, x_g, codes, scales, g, A, B, group_offsets, x)
+    _bits16(x), _bits16(A), _bits16(B)
+    M, K2 = x_codes.shape
+    K = 2 * K2
+    N = codes.shape[-2]
+    r = 0 if A is None else A.shape[0]
+    G = 0 if group_offsets is None else (num_groups if num_groups else group_offsets.numel() - 1)
+    out = _empty((M, N), torch.bfloat16, x_codes.device) if out is None else out
+    if workspace is None:
+        workspace = _empty((max(workspace_bytes(OP_LINEAR_W4A4_QUANTIZED, M, N, K, r, G), 16),), torch.uint8,
+                           x_codes.device)
+    wsb = workspace.numel() * workspace.element_size()
+    st = lib().nvfp4_lora_linear_w4a4_quantized(_ptr(x), _ptr(x_codes), _ptr(x_scales), _ptr(x_g), M, K, _ptr(codes),
+                                                _ptr(scales), _ptr(g), N, _ptr(A), _ptr(B), r, float(s),
+                                                _ptr(group_offsets), G, _ptr(out), _ptr(workspace), wsb,
+                                                _stream(x_codes, stream))
+    _check(st, "nvfp4_lora_linear_w4a4_quantized")
+    return out
 
 
 def nvfp4_lora_linear_noalloc(x, codes, scales, g, A=None, B=None, s: float = 1.0, out=None, stream=None):

@@ -22,8 +22,8 @@ std::atomic<uint64_t> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups) {
-  if (w4a4) return w4a4_tc_supported(M, N, K, r) ? w4a4_tc_workspace_bytes(M, N, K, r, groups) : 0;
+size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups, bool prequantized) {
+  if (w4a4) return w4a4_tc_supported(M, N, K, r) ? w4a4_tc_workspace_bytes(M, N, K, r, groups, prequantized) : 0;
   return w4a16_tc_supported(M, N, K, r) ? w4a16_tc_workspace_bytes(M, N, K, r, kPlanSMs) : 0;
 }
 
@@ -138,14 +138,19 @@ bool hits(const std::vector<std::pair<uintptr_t, uintptr_t>>& r, uintptr_t a, ui
   return it != r.begin() && std::prev(it)->second > a;
 }
 
+// xq_codes / xq_scales / xq_g: W4A4 on activations given in NVFP4 (x is then read by the LoRA
+// branch only and may be NULL without LoRA); all NULL: x is quantized by the call.
 nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
                              const uint8_t* w_scales, const float* w_g, int64_t N, const uint16_t* A,
                              const uint16_t* B, int32_t r, float s, const int32_t* offsets, int32_t groups,
-                             uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+                             uint16_t* y, void* ws, size_t ws_bytes, void* stream, const uint8_t* xq_codes = nullptr,
+                             const uint8_t* xq_scales = nullptr, const float* xq_g = nullptr) {
+  const bool pre = xq_codes || xq_scales || xq_g;
   if (M < 0 || K <= 0 || N <= 0 || r < 0 || r > 256) return NVFP4RL_ERR_INVALID_ARG;
   if (r % 16 != 0 || r > kMaxLoraRank) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return NVFP4RL_OK;  // no activation rows: nothing to read or write
-  if (!x || !w_codes || !w_scales || !w_g || !y) return NVFP4RL_ERR_INVALID_ARG;
+  if (pre && (!xq_codes || !xq_scales || !xq_g)) return NVFP4RL_ERR_INVALID_ARG;
+  if ((!x && !(pre && r == 0)) || !w_codes || !w_scales || !w_g || !y) return NVFP4RL_ERR_INVALID_ARG;
   if (r > 0 && (!A || !B)) return NVFP4RL_ERR_INVALID_ARG;
   if (!std::isfinite(s)) return NVFP4RL_ERR_INVALID_ARG;
   if (offsets) {
@@ -155,26 +160,34 @@ nvfp4rl_status linear_common(bool w4a4, const uint16_t* x, int64_t M, int64_t K,
     return NVFP4RL_ERR_INVALID_ARG;
   }
   if (K % 256 != 0 || N % 128 != 0 || M > 65535) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
-  const void* arrays[] = {x, w_codes, w_scales, A, B, offsets, y, ws};
+  const void* arrays[] = {x, w_codes, w_scales, A, B, offsets, y, ws, xq_codes, xq_scales};
   for (const void* p : arrays)
     if (p && !aligned16(p)) return NVFP4RL_ERR_MISALIGNED;
-  if (reinterpret_cast<uintptr_t>(w_g) & 3u) return NVFP4RL_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(w_g) & 3u) || (reinterpret_cast<uintptr_t>(xq_g) & 3u))
+    return NVFP4RL_ERR_MISALIGNED;
   const int G = offsets ? groups : 1;
-  const size_t need = linear_workspace_bytes(w4a4, M, N, K, r, G);
+  const size_t need = linear_workspace_bytes(w4a4, M, N, K, r, G, pre);
   if (need == 0) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
   if (!ws || ws_bytes < need) return NVFP4RL_ERR_WORKSPACE;
   const size_t ybytes = static_cast<size_t>(M) * N * 2;
-  const void* ins[] = {x, w_codes, w_scales, w_g, A, B, offsets, ws};
+  const void* ins[] = {x, w_codes, w_scales, w_g, A, B, offsets, ws, xq_codes, xq_scales, xq_g};
   const size_t isz[] = {static_cast<size_t>(M) * K * 2, static_cast<size_t>(G) * N * K / 2,
                         static_cast<size_t>(G) * N * K / 16, static_cast<size_t>(G) * 4,
                         A ? static_cast<size_t>(r) * K * 2 : 0, B ? static_cast<size_t>(N) * r * 2 : 0,
-                        offsets ? static_cast<size_t>(groups + 1) * 4 : 0, ws ? need : 0};
-  for (int i = 0; i < 8; ++i)
+                        offsets ? static_cast<size_t>(groups + 1) * 4 : 0, ws ? need : 0,
+                        static_cast<size_t>(M) * K / 2, static_cast<size_t>(M) * K / 16, 4};
+  for (int i = 0; i < 11; ++i)
     if (ins[i] && overlap(y, ybytes, ins[i], isz[i])) return NVFP4RL_ERR_ALIAS;
+  // the workspace (U, tile map) is written by the call: it may not overlap an input either
+  for (int i = 0; i < 11; ++i)
+    if (i != 7 && ins[i] && ws && overlap(ws, need, ins[i], isz[i])) return NVFP4RL_ERR_ALIAS;
   DeviceInfo dev;
   nvfp4rl_status st = current_device(&dev);
   if (st != NVFP4RL_OK) return st;
   LinearArgs a{x, M, K, N, w_codes, w_scales, w_g, A, B, r, s, offsets, G, y, w4a4};
+  a.xq_codes = xq_codes;
+  a.xq_scales = xq_scales;
+  a.xq_g = xq_g;
   return launch_linear(a, ws, ws_bytes, dev, static_cast<cudaStream_t>(stream));
 }
 
@@ -439,6 +452,17 @@ nvfp4rl_status nvfp4_lora_linear_w4a4(const uint16_t* x, int64_t M, int64_t K, c
                        y, workspace, workspace_bytes, stream);
 }
 
+nvfp4rl_status nvfp4_lora_linear_w4a4_quantized(const uint16_t* x, const uint8_t* x_codes, const uint8_t* x_scales,
+                                                const float* x_g, int64_t M, int64_t K, const uint8_t* w_codes,
+                                                const uint8_t* w_scales, const float* w_g, int64_t N,
+                                                const uint16_t* lora_A, const uint16_t* lora_B, int32_t r, float s,
+                                                const int32_t* group_offsets, int32_t num_groups, uint16_t* y,
+                                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x_codes || !x_scales || !x_g) return NVFP4RL_ERR_INVALID_ARG;
+  return linear_common(true, x, M, K, w_codes, w_scales, w_g, N, lora_A, lora_B, r, s, group_offsets, num_groups, y,
+                       workspace, workspace_bytes, stream, x_codes, x_scales, x_g);
+}
+
 size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r, int32_t num_groups) {
   if (M < 0 || N < 0 || K < 0 || r < 0 || r > 256 || num_groups < 0 || num_groups > 1024) return 0;
   switch (op) {
@@ -449,6 +473,8 @@ size_t nvfp4rl_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int3
     case NVFP4RL_OP_KV_ATTENTION: return N > 0 && K > 0 ? attention_workspace_bytes(M, N, K) : 0;
     case NVFP4RL_OP_LINEAR_W4A16: return linear_workspace_bytes(false, M, N, K, r, 1);
     case NVFP4RL_OP_LINEAR_W4A4: return linear_workspace_bytes(true, M, N, K, r, num_groups > 0 ? num_groups : 1);
+    case NVFP4RL_OP_LINEAR_W4A4_QUANTIZED:
+      return linear_workspace_bytes(true, M, N, K, r, num_groups > 0 ? num_groups : 1, true);
     default: return 0;
   }
 }

@@ -184,14 +184,20 @@ struct LinearArgs {
   int groups;
   uint16_t* y;
   bool w4a4;
+  // W4A4 with activations already in NVFP4 (codes, scales, g as the quantizer wrote them for x);
+  // null: the call quantizes x itself
+  const uint8_t* xq_codes = nullptr;
+  const uint8_t* xq_scales = nullptr;
+  const float* xq_g = nullptr;
 };
 
 // LoRA ranks the linears take: 0 (no LoRA) or a multiple of 16 up to this bound (the rank is the K
 // of the up-projection MMA, 16 per instruction; both LoRA tiles stay resident in shared memory).
 constexpr int kMaxLoraRank = 128;
 
-// Workspace bytes of a linear call (0 when the shape is not supported).
-size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups);
+// Workspace bytes of a linear call (0 when the shape is not supported); prequantized: W4A4 on
+// activations given in NVFP4 (the workspace then holds no activation codes).
+size_t linear_workspace_bytes(bool w4a4, int64_t M, int64_t N, int64_t K, int r, int groups, bool prequantized = false);
 
 // Split-K planning uses at most this many SMs, so workspace sizes do not depend on the device.
 constexpr int kPlanSMs = 152;
@@ -208,7 +214,7 @@ nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const u
 
 // tcgen05 W4A4 block-scaled path (linear_w4a4_tc.cu).
 bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r);
-size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups);
+size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups, bool prequantized);
 nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev,
                               cudaStream_t st);
 

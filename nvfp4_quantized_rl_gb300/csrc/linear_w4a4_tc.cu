@@ -847,7 +847,7 @@ struct W4a4Plan {
 
 // Wide tiles when three 48 KB code stages still fit beside the LoRA tiles (r <= 64), otherwise
 // 128 x 128 tiles.
-W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups) {
+W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups, bool prequantized = false) {
   W4a4Plan t{};
   const size_t wlora = r ? static_cast<size_t>(kTile + kWN) * 2 * r : 0;
   const size_t wfixed = 1024 + wlora + kWSfRing * kWSfStage + 512;
@@ -864,10 +864,11 @@ W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups) {
   }
   size_t o = 0;
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
-  t.ws_codes = take(static_cast<size_t>(M) * K / 2);
-  t.ws_scales = take(static_cast<size_t>(M) * K / 16);
-  t.ws_amax = take(kQuantizeWorkspace);
-  t.ws_gx = take(16);
+  // activation codes, scales, amax word and g_x, unless the caller passes them in NVFP4
+  t.ws_codes = take(prequantized ? 0 : static_cast<size_t>(M) * K / 2);
+  t.ws_scales = take(prequantized ? 0 : static_cast<size_t>(M) * K / 16);
+  t.ws_amax = take(prequantized ? 0 : kQuantizeWorkspace);
+  t.ws_gx = take(prequantized ? 0 : 16);
   t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
   t.ws_tiles = take(static_cast<size_t>(groups + 2) * 4);
   t.ws_total = o;
@@ -887,26 +888,31 @@ bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r) {
          w4a4_plan(M, K, r, 1).stages >= 2;
 }
 
-size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups) {
+size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups, bool prequantized) {
   (void)N;
-  return w4a4_plan(M, K, r, groups).ws_total;
+  return w4a4_plan(M, K, r, groups, prequantized).ws_total;
 }
 
 nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev,
                               cudaStream_t st) {
   const int groups = a.offsets ? a.groups : 1;
-  const W4a4Plan t = w4a4_plan(a.M, a.K, a.r, groups);
+  const bool pre = a.xq_codes != nullptr;
+  const W4a4Plan t = w4a4_plan(a.M, a.K, a.r, groups, pre);
   if (ws_bytes < t.ws_total) return NVFP4RL_ERR_WORKSPACE;
   char* base = static_cast<char*>(ws);
-  uint8_t* xc = reinterpret_cast<uint8_t*>(base + t.ws_codes);
-  uint8_t* xs = reinterpret_cast<uint8_t*>(base + t.ws_scales);
-  float* gx = reinterpret_cast<float*>(base + t.ws_gx);
+  const uint8_t* xc = pre ? a.xq_codes : reinterpret_cast<uint8_t*>(base + t.ws_codes);
+  const uint8_t* xs = pre ? a.xq_scales : reinterpret_cast<uint8_t*>(base + t.ws_scales);
+  const float* gx = pre ? a.xq_g : reinterpret_cast<float*>(base + t.ws_gx);
   uint16_t* U = reinterpret_cast<uint16_t*>(base + t.ws_u);
   int32_t* tiles = reinterpret_cast<int32_t*>(base + t.ws_tiles);
 
-  nvfp4rl_status sq = launch_quantize(a.x, NVFP4RL_BF16, a.M, a.K, nullptr, xc, xs, gx, nullptr,
-                                      reinterpret_cast<uint32_t*>(base + t.ws_amax), dev, st);
-  if (sq != NVFP4RL_OK) return sq;
+  if (!pre) {
+    nvfp4rl_status sq = launch_quantize(a.x, NVFP4RL_BF16, a.M, a.K, nullptr, reinterpret_cast<uint8_t*>(base + t.ws_codes),
+                                        reinterpret_cast<uint8_t*>(base + t.ws_scales),
+                                        reinterpret_cast<float*>(base + t.ws_gx), nullptr,
+                                        reinterpret_cast<uint32_t*>(base + t.ws_amax), dev, st);
+    if (sq != NVFP4RL_OK) return sq;
+  }
   if (a.r) {
     const nvfp4rl_status sd = launch_lora_down(a.x, a.M, a.K, a.A, a.r, U, dev, st);
     if (sd != NVFP4RL_OK) return sd;

@@ -226,6 +226,28 @@ def test_linear_validation(nv):
             assert nv.workspace_bytes(op, 200, 256, 512, r) > 0, (op, r)
 
 
+def _linq(nv, x=A0, xc=0x90000, xs=0xA0000, xg=0xB0000, M=8, K=512, codes=A1, scales=A2, g=A3, N=256, A=None,
+          B=None, r=0, s=2.0, off=None, G=0, y=A4, ws=0x60000, wsb=1 << 30):
+    return nv.lib().nvfp4_lora_linear_w4a4_quantized(x, xc, xs, xg, M, K, codes, scales, g, N, A, B, r, s, off, G, y,
+                                                     ws, wsb, None)
+
+
+def test_linear_w4a4_quantized_validation(nv):
+    assert _linq(nv, xc=None) == 1                  # the activation codes are required
+    assert _linq(nv, xg=None) == 1
+    assert _linq(nv, x=None, r=16, A=0x70000, B=0x80000) == 1  # the LoRA branch reads x
+    assert _linq(nv, xs=0xA0000 + 8) == 2           # misaligned scales
+    assert _linq(nv, xg=0xB0000 + 2) == 2           # misaligned g_x
+    assert _linq(nv, y=0x90000) == 7                # y over the activation codes
+    assert _linq(nv, ws=0xA0000) == 7               # the workspace over the activation scales
+    assert _linq(nv, K=500) == 3 and _linq(nv, r=8, A=0x70000, B=0x80000) == 3
+    assert _linq(nv, wsb=16) == 4
+    # without activation codes to hold, the workspace is smaller than the quantize-on-the-fly call's
+    for r in (0, 32):
+        q = nv.workspace_bytes(nv.OP_LINEAR_W4A4_QUANTIZED, 4096, 3584, 3584, r)
+        assert 0 < q < nv.workspace_bytes(nv.OP_LINEAR_W4A4, 4096, 3584, 3584, r) - 4096 * 3584 // 2
+
+
 def test_rmsnorm_validation(nv):
     L = nv.lib()
     assert L.rmsnorm_aqn(None, 4, 64, A1, None, 0.0, 1e-6, A2, None) == 1

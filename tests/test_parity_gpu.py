@@ -607,6 +607,32 @@ def test_w4a4_small_activation_scale_bytes(nv):
     P.assert_gemm_close(y[1:], ref[1:], "rows 1.. (subnormal activation scales)")
 
 
+@pytest.mark.parametrize("M,N,K,r", [(300, 384, 1024, 32), (130, 256, 512, 0), (200, 640, 1024, 128),
+                                     (4096, 3584, 3584, 32)])
+def test_w4a4_quantized_activations(nv, M, N, K, r):
+    """nvfp4_lora_linear_w4a4_quantized on the NVFP4 output of rmsnorm_aqn_quantize: within the GEMM bar
+    of the oracle's W4A4 on the normalized activations y, and the same bits as nvfp4_lora_linear_w4a4(y)
+    (which quantizes y itself, to the same codes)."""
+    x = synth.heavy_tail_activation_bf16(M, K, 91, M)
+    w = synth.aqn_weight(K, 91, 2)
+    eps = synth.aqn_eps(K, 91, 3)
+    q = _weights(N, K, 92, M)
+    A, B = synth.lora_factors(r, K, N, 93, M) if r else (None, None)
+    yd, xc, xs, xg = nv.rmsnorm_aqn_quantize(P.dev_bf16(x), P.dev(w), P.dev(eps), np.float32(3e-3), 1e-6)
+    gd = P.dev(np.atleast_1d(np.asarray(q[2], np.float32)))
+    Ad, Bd = (None, None) if not r else (P.dev_bf16(A), P.dev_bf16(B))
+    cd, sd = P.dev(q[0]), P.dev(q[1])
+    out = nv.nvfp4_lora_linear_w4a4_quantized(yd if r else None, xc, xs, xg, cd, sd, gd, Ad, Bd, 2.0)
+    ref_call = nv.nvfp4_lora_linear_w4a4(yd, cd, sd, gd, Ad, Bd, 2.0)
+    torch.cuda.synchronize()
+    got = P.host_bits(out)
+    assert np.array_equal(got, P.host_bits(ref_call)), "differs from the quantize-on-the-fly call"
+    y = P.host_bits(yd)
+    rows = None if M <= 512 else np.sort(np.random.default_rng(94).choice(M, 48, replace=False))
+    want = ref_linear(True, y, q, A, B, 2.0, rows=rows)
+    P.assert_gemm_close(got if rows is None else got[rows], want, f"{M}x{N}x{K} r={r}")
+
+
 def test_linear_qwen7b_decode_full(nv):
     """The 7B decode layer the benchmark times: M=64 bf16 tokens, every linear, r=32, every output."""
     x = synth.activation_bf16(64, 3584, 21, 0)
