@@ -70,6 +70,7 @@ constexpr uint32_t kD0 = 0, kD1 = 128, kDL = 256, kSF = 384;  // TMEM columns
 struct W4a4Params {
   int64_t M, N, K;
   int tiles_n;
+  int tiles_m;             // dense row tiles
   int total_tiles;         // dense: tiles_m * tiles_n; grouped: read from tile_start[groups] * tiles_n
   int r, lora_box_bytes;
   float s;
@@ -100,9 +101,30 @@ struct TileInfo {
   int n0;         // first weight row within the expert
 };
 
+// Dense tiles are visited in groups of kGroupRows row tiles; within a group consecutive tiles step
+// through the row tiles first. A wave of CTAs then covers a block of a few weight tiles times those
+// row tiles, whose operands stay in L2 while the wave runs (visiting all weight tiles of one row tile
+// first would stream the whole weight matrix through L2 once per wave). Grouped (MoE) tiles keep the
+// row-major order: their row tiles belong to different experts.
+constexpr int kGroupRows = 32;
+
+__device__ __forceinline__ void tile_coords(const W4a4Params& p, int t, int& tm, int& tn) {
+  if (p.offsets) {
+    tm = t / p.tiles_n;
+    tn = t % p.tiles_n;
+  } else {
+    const int per_group = kGroupRows * p.tiles_n;
+    const int first = (t / per_group) * kGroupRows, rem = t % per_group;
+    const int rows = min(kGroupRows, p.tiles_m - first);
+    tm = first + rem % rows;
+    tn = rem / rows;
+  }
+}
+
 __device__ __forceinline__ TileInfo tile_info(const W4a4Params& p, int t) {
   TileInfo ti;
-  const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+  int tm, tn;
+  tile_coords(p, t, tm, tn);
   ti.n0 = tn * kTile;
   if (p.offsets) {
     ti.e = find_group(p.tile_start, p.groups, tm);
@@ -119,7 +141,7 @@ __device__ __forceinline__ TileInfo tile_info(const W4a4Params& p, int t) {
 // Tile t of a kernel whose tiles cover `tile_n` weight rows (tiles_n tiles per row tile).
 __device__ __forceinline__ TileInfo tile_info_n(const W4a4Params& p, int t, int tile_n) {
   TileInfo ti = tile_info(p, t);
-  ti.n0 = (t % p.tiles_n) * tile_n;
+  ti.n0 = ti.n0 / kTile * tile_n;
   return ti;
 }
 
@@ -948,7 +970,8 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
   p.K = a.K;
   p.tiles_n = static_cast<int>((a.N + wbox - 1) / wbox);
   const int64_t tiles_m_bound = a.offsets ? (a.M + kTile - 1) / kTile + groups : (a.M + kTile - 1) / kTile;
-  p.total_tiles = static_cast<int>(((a.M + kTile - 1) / kTile) * p.tiles_n);
+  p.tiles_m = static_cast<int>((a.M + kTile - 1) / kTile);
+  p.total_tiles = p.tiles_m * p.tiles_n;
   p.r = a.r;
   p.lora_box_bytes = lbox;
   p.s = a.s;
