@@ -63,7 +63,9 @@ typedef enum nvfp4rl_status {
   NVFP4RL_ERR_CUDA = 5,              /* a CUDA runtime call or a kernel launch failed */
   NVFP4RL_ERR_TIMEOUT = 6,           /* a bounded device-side wait ran out (reported by nvfp4rl_device_status) */
   NVFP4RL_ERR_ALIAS = 7,             /* an output buffer overlaps an input buffer */
-  NVFP4RL_ERR_DEVICE = 8             /* the current device is not a compute-capability 10.3 GPU */
+  NVFP4RL_ERR_DEVICE = 8,            /* the current device is not a compute-capability 10.3 GPU */
+  NVFP4RL_ERR_RANGE = 9              /* a W4A4 call's LoRA scale s / (g_x g_w) exceeded 2^100
+                                        (reported by nvfp4rl_device_status) */
 } nvfp4rl_status;
 
 /* Element types of quantizer inputs. */
@@ -356,6 +358,13 @@ NVFP4RL_API nvfp4rl_status nvfp4_lora_linear(const uint16_t* x, int64_t M, int64
  *                  w_codes + e*N*K/2, w_scales + e*N*K/16, w_g[e].
  *                  Grouped calls take r == 0 (no LoRA). num_groups in [1, 1024].
  *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A4, M, N, K, r, num_groups).
+ *   The LoRA branch is added inside the FP4 product's fp32 accumulator: with alpha = g_x w_g,
+ *   c = s / alpha and P the product of the E2M1 codes times their E4M3 block scales (deq without
+ *   the two g's), Y = alpha (P + (c U) B^T), where c U (U = bf16(x A^T)) enters as the sum of two
+ *   bf16 parts (~2^-17 relative). alpha == 0 (an all-zero x or weight) gives Y = s U B^T. If |c| > 2^100
+ *   (the product of the two tensors' amax below ~1e-23 times |s|) the result may overflow and the
+ *   call sets the range bit of the device status word (nvfp4rl_device_status ->
+ *   NVFP4RL_ERR_RANGE).
  */
 NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_w4a4(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
                                       const uint8_t* w_scales, const float* w_g, int64_t N,
@@ -376,7 +385,7 @@ NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_w4a4(const uint16_t* x, int64_t M, 
  *   Other arguments, shape rules, grouping and determinism as nvfp4_lora_linear_w4a4; given the codes
  *   that nvfp4_lora_linear_w4a4 would compute from x, the result is the same bits.
  *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A4_QUANTIZED, M, N, K, r, num_groups)
- *            (U = bf16(x A^T) and the grouped tile map; no activation codes); it may overlap no input.
+ *            (the two bf16 parts of c U and the grouped tile map; no activation codes); it may overlap no input.
  */
 NVFP4RL_API nvfp4rl_status nvfp4_lora_linear_w4a4_quantized(
     const uint16_t* x, const uint8_t* x_codes, const uint8_t* x_scales, const float* x_g, int64_t M, int64_t K,
@@ -403,8 +412,9 @@ NVFP4RL_API const char* nvfp4rl_status_string(nvfp4rl_status status);
 /*
  * nvfp4rl_device_status -- synchronizes the current device and reports the
  *   library's device-side error word: NVFP4RL_ERR_TIMEOUT if a bounded wait in
- *   a kernel ran out since the last clear, else NVFP4RL_OK. *word_out (may be
- *   NULL) receives the raw word; clear != 0 resets it.
+ *   a kernel ran out since the last clear, else NVFP4RL_ERR_RANGE if a W4A4 call's
+ *   LoRA scale was out of range, else NVFP4RL_OK. *word_out (may be NULL) receives
+ *   the raw word (bits 0-4: timeouts, bit 5: range); clear != 0 resets it.
  */
 NVFP4RL_API nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t clear);
 

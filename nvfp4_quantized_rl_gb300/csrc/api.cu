@@ -490,6 +490,7 @@ const char* nvfp4rl_status_string(nvfp4rl_status status) {
     case NVFP4RL_ERR_TIMEOUT: return "device-side wait timed out";
     case NVFP4RL_ERR_ALIAS: return "output overlaps an input";
     case NVFP4RL_ERR_DEVICE: return "device is not compute capability 10.3";
+    case NVFP4RL_ERR_RANGE: return "W4A4 LoRA scale s / (g_x g_w) out of range";
   }
   return "unknown status";
 }
@@ -513,7 +514,8 @@ nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t clear) {
     const uint32_t z = 0;
     if (cudaMemcpyToSymbol(g_device_status, &z, sizeof(z)) != cudaSuccess) return NVFP4RL_ERR_CUDA;
   }
-  return w ? NVFP4RL_ERR_TIMEOUT : NVFP4RL_OK;
+  if (w & sm100::kStatusTimeoutMask) return NVFP4RL_ERR_TIMEOUT;
+  return w ? NVFP4RL_ERR_RANGE : NVFP4RL_OK;
 }
 
 }  // extern "C"

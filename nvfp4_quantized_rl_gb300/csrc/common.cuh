@@ -206,11 +206,23 @@ constexpr int kPlanSMs = 152;
 bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                         int esize, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
 
+// W4A4 form of the LoRA down-projection's output: instead of U = bf16(x A^T), the two bf16 parts
+// of c U with c = s / (g_x w_g) (c = s when g_x w_g = 0): hi = bf16(c U) into U, lo =
+// bf16(c U - hi) into `lo`. |c| above 2^100 sets the range bit of `status`.
+struct LoraDownScale {
+  const float* g_x = nullptr;  // null: plain U
+  const float* w_g = nullptr;
+  float s = 0.f;
+  uint16_t* lo = nullptr;  // [M][r]
+  uint32_t* status = nullptr;
+};
+
 // LoRA down-projection U = bf16(x A^T), [M][r] row-major, K a multiple of 64 (linear_tc.cu):
 // clusters of CTAs split K and reduce in distributed shared memory. Launched as a programmatic
-// dependent of the previous kernel on the stream; it waits for that kernel before reading x.
+// dependent of the previous kernel on the stream; it waits for that kernel before reading x
+// (and g_x).
 nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
-                                const DeviceInfo& dev, cudaStream_t st);
+                                const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale = {});
 
 // tcgen05 W4A4 block-scaled path (linear_w4a4_tc.cu).
 bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r);

@@ -512,16 +512,24 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // registers. The fp32 partial [64][RP] goes to shared memory; after a cluster barrier, CTA q sums
 // its share of the rows over all CTAs' partials in rank order (distributed shared memory) and
 // writes U. Rows past M read as zero and are not written. Each rank's sum runs through the same
-// chunks and instructions whatever RP is, so U does not depend on it.
+// chunks and instructions whatever RP is, so U does not depend on it. With a LoraDownScale (the
+// W4A4 path) the kernel writes hi and lo of c U instead.
 template <int RP>
 __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                               const uint16_t* __restrict__ A, int r,
-                                                              uint16_t* __restrict__ U) {
-  // Earlier kernels on the stream (which may have written x) have completed once griddep_wait
-  // returns; only then may the main kernel start: it reads x and the weights without waiting,
-  // and waits (griddepcontrol.wait) for this kernel before reading U.
+                                                              uint16_t* __restrict__ U, const LoraDownScale ls) {
+  // Earlier kernels on the stream (which may have written x, or g_x) have completed once
+  // griddep_wait returns; only then may the main kernel start: it reads x and the weights
+  // without waiting, and waits (griddepcontrol.wait) for this kernel before reading U.
   griddep_wait();
   griddep_launch_dependents();
+  float cu = 1.f;  // c of the W4A4 form
+  if (ls.g_x) {
+    const float alpha = *ls.g_x * *ls.w_g;
+    cu = alpha == 0.f ? ls.s : ls.s / alpha;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && !(fabsf(cu) <= 0x1p100f))
+      atomicOr(ls.status, kStatusRange);
+  }
   extern __shared__ __align__(16) uint8_t down_smem[];
   constexpr int kDownStageElems = DownShape<RP>::kStageElems;
   uint16_t* ring = reinterpret_cast<uint16_t*>(down_smem);  // [kDownStages][64 + RP][kDownK + kDownPad]
@@ -603,8 +611,20 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
       if (m < M) {
         const float av[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (j0 + j4 + e < r) U[m * r + j0 + j4 + e] = static_cast<uint16_t>(f32_to_bf16_bits(av[e]));
+        for (int e = 0; e < 4; ++e) {
+          if (j0 + j4 + e >= r) continue;
+          const uint32_t u = f32_to_bf16_bits(av[e]);
+          const int64_t at = m * r + j0 + j4 + e;
+          if (ls.g_x) {
+            // c U = hi + lo: hi = bf16(c U), lo = bf16(c U - hi) (c U - hi is exact in fp32)
+            const float cuv = __uint_as_float(u << 16) * cu;
+            const uint32_t hi = f32_to_bf16_bits(cuv);
+            U[at] = static_cast<uint16_t>(hi);
+            ls.lo[at] = static_cast<uint16_t>(f32_to_bf16_bits(cuv - __uint_as_float(hi << 16)));
+          } else {
+            U[at] = static_cast<uint16_t>(u);
+          }
+        }
       }
     }
     cluster_sync_all();  // partials read by every peer before the next pass overwrites them
@@ -795,7 +815,7 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 // r = 64); 32 otherwise, the instance whose shared memory leaves room beside a decode CTA of the
 // main kernel.
 nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
-                                const DeviceInfo& dev, cudaStream_t st) {
+                                const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale) {
   const int nchunks = static_cast<int>(K / kDownK);
   const int rp = r > 32 && M > 64 ? 64 : 32;
   const int dc = down_cluster_size(dev.device, rp);
@@ -820,8 +840,8 @@ nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const u
   dattr[1].val.programmaticStreamSerializationAllowed = 1;
   dcfg.attrs = dattr;
   dcfg.numAttrs = 2;
-  const cudaError_t e = rp == 64 ? cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel<64>, x, M, K, A, r, U)
-                                 : cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel<32>, x, M, K, A, r, U);
+  const cudaError_t e = rp == 64 ? cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel<64>, x, M, K, A, r, U, scale)
+                                 : cudaLaunchKernelEx(&dcfg, w4a16_lora_down_kernel<32>, x, M, K, A, r, U, scale);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }

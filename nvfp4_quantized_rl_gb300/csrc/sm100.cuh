@@ -24,6 +24,8 @@ enum : uint32_t {
   kStatusTimeoutMma = 1u << 2,
   kStatusTimeoutEpilogue = 1u << 3,
   kStatusTimeoutDrain = 1u << 4,
+  kStatusTimeoutMask = (1u << 5) - 1u,
+  kStatusRange = 1u << 5,  // not a wait: a W4A4 LoRA scale s / (g_x g_w) out of range
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {

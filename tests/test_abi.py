@@ -53,7 +53,7 @@ def test_aqn_sigma_matches_the_oracle(nv):
 
 
 def test_status_strings(nv):
-    for s in range(9):
+    for s in range(10):
         assert nv.status_string(s) and nv.status_string(s) != "unknown status"
 
 

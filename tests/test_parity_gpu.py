@@ -607,6 +607,67 @@ def test_w4a4_small_activation_scale_bytes(nv):
     P.assert_gemm_close(y[1:], ref[1:], "rows 1.. (subnormal activation scales)")
 
 
+@pytest.mark.parametrize("r", [48, 96])
+def test_w4a4_lora_rank_not_a_multiple_of_64(nv, r):
+    """The W4A4 kernel runs the LoRA up-projection in 64-rank slices; ranks that leave the last slice
+    partly empty (its columns past r read as zeros) over several row and column tiles."""
+    M, N, K, s = 150, 512, 768, 1.5
+    q = _weights(N, K, 86, r)
+    x = synth.heavy_tail_activation_bf16(M, K, 87, r)
+    A, B = synth.lora_factors(r, K, N, 88, r)
+    y = gpu_linear(nv, True, x, q, A, B, s)
+    P.assert_gemm_close(y, ref_linear(True, x, q, A, B, s), f"r={r}")
+
+
+def test_w4a4_lora_with_zero_alpha(nv):
+    """alpha = g_x g_w = 0 with a LoRA branch. An all-zero weight tensor (g_w = 0): Y = s (x A^T) B^T
+    alone. An all-zero activation tensor (g_x = 0, U = 0): Y = 0."""
+    M, N, K, r, s = 140, 256, 512, 32, 2.0
+    q = oracle.quantize(np.zeros((N, K), np.uint16))
+    assert np.float32(q[2]) == 0
+    x = synth.activation_bf16(M, K, 89, 0)
+    A, B = synth.lora_factors(r, K, N, 89, 1)
+    y = gpu_linear(nv, True, x, q, A, B, s)
+    P.assert_gemm_close(y, ref_linear(True, x, q, A, B, s), "zero weights: LoRA branch alone")
+    q2 = _weights(N, K, 89, 2)
+    y0 = gpu_linear(nv, True, np.zeros((M, K), np.uint16), q2, A, B, s)
+    assert not (y0 & 0x7FFF).any(), "zero activations must give zero outputs"
+
+
+def _clear_status(nv):
+    st, word = nv.device_status(clear=True)
+    return st, word
+
+
+def test_w4a4_lora_tiny_alpha_in_range(nv):
+    """Weights ~1e-20 (g_w ~1e-23): the LoRA branch enters the accumulator scaled by s / alpha ~1e25,
+    still within range; the result stays within the GEMM bar and no status bit is set."""
+    M, N, K, r, s = 130, 384, 512, 32, 2.0
+    assert _clear_status(nv)[0] == 0
+    q = _weights(N, K, 90, 0, std=1e-20)
+    x = synth.activation_bf16(M, K, 90, 1)
+    A, B = synth.lora_factors(r, K, N, 90, 2)
+    y = gpu_linear(nv, True, x, q, A, B, s)
+    P.assert_gemm_close(y, ref_linear(True, x, q, A, B, s), "weights ~1e-20")
+    assert _clear_status(nv) == (0, 0)
+
+
+def test_w4a4_lora_scale_out_of_range_sets_status(nv):
+    """Weights ~1e-30 put s / alpha above 2^100: the call sets the range bit of the device status word
+    (NVFP4RL_ERR_RANGE, bit 5) and the context keeps working."""
+    M, N, K, r = 130, 256, 512, 16
+    assert _clear_status(nv)[0] == 0
+    q = _weights(N, K, 95, 0, std=1e-30, outliers=0.0)
+    x = synth.activation_bf16(M, K, 95, 1)
+    A, B = synth.lora_factors(r, K, N, 95, 2)
+    gpu_linear(nv, True, x, q, A, B, 2.0)
+    assert _clear_status(nv) == (9, 32)
+    assert _clear_status(nv) == (0, 0)
+    q2 = _weights(N, K, 95, 3)
+    y = gpu_linear(nv, True, x, q2, A, B, 2.0)
+    P.assert_gemm_close(y, ref_linear(True, x, q2, A, B, 2.0), "after the range report")
+
+
 @pytest.mark.parametrize("M,N,K,r", [(300, 384, 1024, 32), (130, 256, 512, 0), (200, 640, 1024, 128),
                                      (4096, 3584, 3584, 32)])
 def test_w4a4_quantized_activations(nv, M, N, K, r):
