@@ -19,10 +19,18 @@ constexpr int kNumSMsHint = 152;  // GB300: 2 dies x 76 SMs; the real count is q
 __device__ __forceinline__ uint32_t bf16_lo_bits(uint32_t pair) { return pair << 16; }
 __device__ __forceinline__ uint32_t bf16_hi_bits(uint32_t pair) { return pair & 0xFFFF0000u; }
 
-// fp32 -> bf16 bits, round to nearest even (finite inputs)
+// fp32 -> bf16 bits, round to nearest even (finite inputs; one cvt instruction)
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
-  uint32_t u = __float_as_uint(f);
-  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+// Two fp32 values -> a bf16 pair (lo in bits 0-15, hi in bits 16-31), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // E4M3 (OCP FP8 E4M3FN) value of a non-negative byte 0x00..0x7E, built from its bits.

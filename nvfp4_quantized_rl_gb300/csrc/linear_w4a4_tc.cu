@@ -38,7 +38,9 @@
 //               stages: an FP4 stage's scale bytes go to one of four TMEM scale slots with
 //               tcgen05.st; on a LoRA stage the group only passes the landed slices on
 //   warps 12-27 epilogue (quarter = warp % 4, 64 columns each): TMEM -> registers, scaled by
-//               alpha, packed to bf16 and stored 16 columns at a time; D is released once read
+//               alpha and packed to bf16 (cvt.rn.bf16x2); D is released to the next tile's MMAs
+//               as soon as it has been read, then the rows are stored, 128-byte pieces at a time
+//               after a shuffle transpose within groups of 8 lanes
 // TMEM: the accumulator D in columns 0..255; scale slot j in 256 + 64 j: activation scales in
 // its first 16 columns (4 per K step: the MMA reads column 4t + w in lane quarter w, so each
 // quarter writes its own rows there), weight scales in the next 32 (8 per K step: column 8t + w
@@ -164,13 +166,6 @@ __device__ __forceinline__ void mma_stage_nvf4(uint32_t d_tmem, uint64_t a_desc,
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
-}
-
-// One 32-byte store (16 bf16 outputs of a row; the address is 32-byte aligned).
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* o) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-               "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-               : "memory");
 }
 
 // 16 columns from four words: column 4t + w holds word t, for every w (the MMA reads only column
@@ -422,26 +417,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = tile_info(p, t);
       const float alpha = gx * p.w_g[ti.e];
       const float out = nl && alpha == 0.f ? 1.f : alpha;
-      // this thread's row (TMEM lane 32q + lane), columns 64 part .. + 63, 16 at a time. (Reading all
-      // 64 first and releasing D before the stores measured slower: the stores then compete with
-      // the next tile's scale and MMA warps.)
-      const int64_t m = ti.m0 + q * 32 + lane;
-      const bool live = m < ti.m_end;
-      uint16_t* yrow = p.y + m * p.N + ti.n0;
-#pragma unroll 1
-      for (int c = part * 64; c < part * 64 + 64; c += 16) {
-        uint32_t d[16], o[8];
-        tmem_ld16(tmem + lane_base + c, d);
+      // this thread's row (TMEM lane 32q + lane), columns 64 part .. + 63, scaled and packed: unit u
+      // (16 bytes) = o[4u .. 4u + 3] = columns 8u .. 8u + 7
+      uint32_t o[32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t d[16];
+        tmem_ld16(tmem + lane_base + part * 64 + cc * 16, d);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          o[i] = f32_to_bf16_bits(__uint_as_float(d[2 * i]) * out) |
-                 (f32_to_bf16_bits(__uint_as_float(d[2 * i + 1]) * out) << 16);
-        if (live && ti.n0 + c < p.N) st_global_v8(yrow + c, o);
+          o[cc * 8 + i] = pack_bf16x2(__uint_as_float(d[2 * i]) * out, __uint_as_float(d[2 * i + 1]) * out);
       }
+      // D has been read: the next tile's MMAs may start while this warp stores
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(dfree));
+      // 8 x 8 transpose of 16-byte units within each group of 8 lanes: afterwards lane 8G + k holds
+      // unit k of rows 8G .. 8G + 7 of the warp's 32 (in o[4j .. 4j + 3] for row 8G + j), so that
+      // each store instruction writes four whole 128-byte row pieces instead of 32 scattered 32-byte
+      // ones
+#pragma unroll
+      for (int dd = 1; dd < 8; dd <<= 1) {
+        const bool hi = (lane & dd) != 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (u & dd) continue;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t send = hi ? o[4 * u + e] : o[4 * (u ^ dd) + e];
+            const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, dd);
+            if (hi) o[4 * u + e] = recv;
+            else o[4 * (u ^ dd) + e] = recv;
+          }
+        }
+      }
+      const int kk = lane & 7, grp = lane >> 3;
+      if (ti.n0 + part * 64 < p.N) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int64_t m = ti.m0 + q * 32 + grp * 8 + j;
+          if (m < ti.m_end)
+            *reinterpret_cast<uint4*>(p.y + m * p.N + ti.n0 + part * 64 + kk * 8) =
+                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+      }
     }
   }
   tc_fence_before();
