@@ -9,7 +9,17 @@
 // MoE expert over that expert's contiguous block of routed rows. U = bf16(x A^T) comes from the
 // cluster LoRA-down kernel that the W4A16 path uses (linear_tc.cu), launched before this one.
 //
-// One persistent kernel, one CTA per SM, tiles of 128 activation rows x 256 weight rows.
+// One persistent kernel, one CTA per SM, in two forms. Dense calls with more than 128 rows run on
+// CTA pairs (a cluster of two, tcgen05 cta_group::2): a pair tile is 256 activation rows x 256
+// weight rows; each CTA loads its own 128 activation rows and half of the weight rows (so a ring
+// stage is 32 KB and six fit), keeps the scales of its rows and of all 256 weight rows in its own
+// TMEM, and holds its 128 rows of the accumulator; the even CTA issues the MMAs, its commits
+// arrive in both CTAs, and the odd CTA's scale and epilogue warps arrive on the even CTA's
+// barriers. Grouped (MoE) calls, whose row tiles may belong to different experts, and calls of
+// at most 128 rows run one CTA per tile of 128 x 256 (48 KB stages, four of them). A pair's
+// tensor cores move the same FP4 work per SM as a lone CTA (measured: 65 ns per 128 x 256 x 64
+// MMA either way, resident operands) but it reads two thirds of the operand bytes per flop from
+// L2, which bounds the lone CTA's ring.
 //
 // The LoRA branch shares the FP4 product's fp32 accumulator. With c = s / alpha,
 //   y = alpha * (x_q W_q^T + c U B^T),
@@ -18,20 +28,22 @@
 // slice x B_lora slice^T, then lo slice x B_lora slice^T) as the first stages of its K loop,
 // through the same operand ring as the codes: 64 ranks of U (128 rows x 128 bytes) and of B_lora
 // (256 rows x 128 bytes) fill a ring stage exactly as 256 K of activation and weight codes do. The
-// accumulator receives c U B^T to ~2^-17 relative, as if U = bf16(x A^T) were scaled in fp32. There is then no second accumulator, no LoRA buffer of its own in shared memory, and no
+// accumulator receives c U B^T to ~2^-17 relative, as if U = bf16(x A^T) were scaled
+// in fp32. There is then no second accumulator, no LoRA buffer of its own in shared memory, and no
 // hand-over between the epilogue and a late LoRA MMA. When alpha = 0 (an all-zero weight or
 // activation tensor) the FP4 MMAs are skipped and the tile computes s U B^T with an output scale
 // of 1. c above 2^100 (s / alpha so large that c U or c U B^T could leave the fp32 range: the
 // product of the two tensors' amax below about 1e-23 for s = 2) sets a range bit in the device
 // status word.
 //
-// A stage's four FP4 MMAs (128 x 256 x 64 each) take ~0.2 us, while a trip through the operand
-// ring (MMA completion -> TMA refill of the slot -> data landed -> scales in TMEM -> MMA issue)
-// takes over 1 us, so four 48 KB stages are in flight. Roles (28 warps: the 72 registers a thread
+// A stage's four FP4 MMAs take ~0.26 us, while a trip through the operand ring (MMA completion ->
+// TMA refill of the slot -> data landed -> scales in TMEM -> MMA issue) takes over 1 us, so
+// several stages are in flight. Roles (28 warps: the 72 registers a thread
 // gets at that size hold every role without spilling; 29 warps would leave 64):
 //   warp 0      activation code producer (TMA, 128 x 128 B per stage; a U slice on LoRA stages)
 //   warp 1      TMEM allocation; one thread issues the MMAs
-//   warp 2      weight code producer (TMA, 256 x 128 B per stage; a B_lora slice on LoRA stages)
+//   warp 2      weight code producer (TMA, 256 x 128 B per stage, 128 x 128 B in a pair; a B_lora
+//               slice on LoRA stages)
 //   warp 3      scale producers, FP4 stages only: lane 0 the activation (128 x 16 B), lane 1 the
 //               weight (256 x 16 B) scale tiles
 //   warps 4-11  two groups of four scale warps (one per TMEM lane quarter) taking alternate
@@ -50,6 +62,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -64,13 +79,10 @@ constexpr int kWN = 256;                          // weight rows per tile (MMA N
 constexpr int kKStage = 256;                      // K per FP4 stage
 constexpr int kLoraK = 64;                        // ranks per LoRA slice (128 bytes of bf16), two stages each
 constexpr int kACode = kTile * kKStage / 2;       // 16 KB: activation codes or a U slice
-constexpr int kBCode = kWN * kKStage / 2;         // 32 KB: weight codes or a B_lora slice
-constexpr int kStage = kACode + kBCode;           // 48 KB operand ring stage
 constexpr int kSfA = kTile * kKStage / 16;        // 2 KB activation scales per stage
 constexpr int kSfB = kWN * kKStage / 16;          // 4 KB weight scales per stage
 constexpr int kSfStage = kSfA + kSfB;
 constexpr int kSfRing = 4;                        // scale ring stages
-constexpr int kMaxStages = 4;                     // operand ring stages
 constexpr int kSlots = 4;                         // TMEM scale slots
 constexpr int kDone = 16;                         // commit ring, > operand stages and scale slots
 constexpr int kThreads = 28 * 32;
@@ -177,25 +189,110 @@ __device__ __forceinline__ void tmem_st16_rep4(uint32_t taddr, uint32_t a0, uint
       : "memory");
 }
 
+// ---- CTA pairs (tcgen05 cta_group::2) --------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrives once on `bar` in both CTAs of the pair when every tcgen05 operation this thread issued
+// before has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(static_cast<uint16_t>(3))
+               : "memory");
+}
+// Arrival on a barrier of another CTA of the cluster (address from dsmem_map). Relaxed: what the
+// arrival announces (TMEM stores waited for with tcgen05.wait::st, operand tiles whose TMA
+// completion this thread observed) is complete before it, and a release at cluster scope measured
+// ~1 us of extra latency per arrival on the critical path.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// mma_stage_nvf4 for a CTA pair: M = 256 (128 rows in each CTA's shared memory and TMEM), each
+// CTA holding half of the 256 weight rows and the full weight scales.
+__device__ __forceinline__ void mma_stage_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 a1, b1;\n\t.reg .b32 s1, s2;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t"
+      "add.u64 a1, %1, 2;\n\tadd.u64 b1, %2, 2;\n\tadd.u32 s1, %4, 4;\n\tadd.u32 s2, %5, 8;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [s1], [s2], t;\n\t"
+      "add.u64 a1, %1, 4;\n\tadd.u64 b1, %2, 4;\n\tadd.u32 s1, %4, 8;\n\tadd.u32 s2, %5, 16;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [s1], [s2], t;\n\t"
+      "add.u64 a1, %1, 6;\n\tadd.u64 b1, %2, 6;\n\tadd.u32 s1, %4, 12;\n\tadd.u32 s2, %5, 24;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [s1], [s2], t;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Operand ring geometry: a CTA of a pair holds half of the tile's 256 weight rows.
+template <bool kPair>
+struct Ring {
+  static constexpr int kBRows = kPair ? kWN / 2 : kWN;     // weight rows in this CTA's shared memory
+  static constexpr int kBBytes = kBRows * kKStage / 2;    // 16 or 32 KB per stage
+  static constexpr int kStageBytes = kACode + kBBytes;    // 32 or 48 KB
+  static constexpr int kMaxStages = kPair ? 6 : 4;
+};
+constexpr int kRingBarriers = 6;  // cfull barriers, >= either ring's stages
+
+// The tile a CTA works on in round t of its persistent loop: a CTA alone takes tile t (128 x 256);
+// a CTA pair takes pair tile t (256 x 256), rank r of the pair its row tile 2 pm + r.
+template <bool kPair>
+__device__ __forceinline__ TileInfo tile_of(const W4a4Params& p, int t, uint32_t rank) {
+  if constexpr (!kPair) {
+    return tile_info(p, t);
+  } else {
+    const int rows2 = (p.tiles_m + 1) >> 1;  // pair rows
+    const int per_group = (kGroupRows / 2) * p.tiles_n;
+    const int first = (t / per_group) * (kGroupRows / 2), rem = t % per_group;
+    const int rows = min(kGroupRows / 2, rows2 - first);
+    TileInfo ti;
+    ti.e = 0;
+    ti.m0 = static_cast<int64_t>(2 * (first + rem % rows) + static_cast<int>(rank)) * kTile;
+    ti.m_end = p.M;
+    ti.n0 = (rem / rows) * kWN;
+    return ti;
+  }
+}
+
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a4_wide_kernel(const __grid_constant__ CUtensorMap map_xc, const __grid_constant__ CUtensorMap map_xs,
                      const __grid_constant__ CUtensorMap map_wc, const __grid_constant__ CUtensorMap map_ws,
                      const __grid_constant__ CUtensorMap map_uh, const __grid_constant__ CUtensorMap map_ul,
                      const __grid_constant__ CUtensorMap map_bl, const W4a4Params p) {
+  using R = Ring<kPair>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;                                  // operand ring stages
-  uint8_t* sfring = smem + S * kStage;                     // kSfRing x kSfStage
+  uint8_t* sfring = smem + S * R::kStageBytes;             // kSfRing x kSfStage
   // mdone[i % kDone]: one tcgen05.commit per stage i (of every tile, LoRA stages included). The
   // operand producers wait for stage i - S before refilling a ring slot, the scale warps for stage
   // i - kSlots before rewriting a TMEM scale slot. Neither can fall kDone stages behind the MMAs
   // (those would need operands the waiter has not provided yet), so the parity a waiter looks for
-  // is never ambiguous.
-  uint64_t* cfull = reinterpret_cast<uint64_t*>(sfring + kSfRing * kSfStage);  // [kMaxStages] operands landed
-  uint64_t* mdone = cfull + kMaxStages;                   // [kDone]
+  // is never ambiguous. In a pair the leader's commits arrive in both CTAs.
+  uint64_t* cfull = reinterpret_cast<uint64_t*>(sfring + kSfRing * kSfStage);  // operands landed
+  uint64_t* mdone = cfull + kRingBarriers;                // [kDone]
   uint64_t* ffull = mdone + kDone;                        // [kSfRing] scale tiles landed
   uint64_t* fempty = ffull + kSfRing;                     // [kSfRing] scale tiles read
-  uint64_t* sfready = fempty + kSfRing;                   // [kSlots] stage ready for its MMAs
+  uint64_t* sfready = fempty + kSfRing;                   // [kSlots] stage ready for its MMAs (leader's)
   uint64_t* dfull = sfready + kSlots;                     // the tile's accumulator is complete
   uint64_t* dfree = dfull + 1;                            // ... and has been read by every epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfree + 1);
@@ -205,6 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nl = 2 * ((p.r + kLoraK - 1) / kLoraK);        // LoRA stages per tile (hi, lo per slice), first
   const int ns = nl + ksteps;
   const int ntiles = total_tiles(p);
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);  // CTA or pair
+  const int units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  constexpr int kPeers = kPair ? 2 : 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) mbar_init(smem_addr(&cfull[i]), 2);  // activation + weight producer
@@ -213,14 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&ffull[i]), 2);
       mbar_init(smem_addr(&fempty[i]), 4);
     }
-    for (int i = 0; i < kSlots; ++i) mbar_init(smem_addr(&sfready[i]), 4);
+    for (int i = 0; i < kSlots; ++i) mbar_init(smem_addr(&sfready[i]), 4 * kPeers);
     mbar_init(smem_addr(dfull), 1);
-    mbar_init(smem_addr(dfree), 16);
+    mbar_init(smem_addr(dfree), 16 * kPeers);
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 512);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_alloc_pair(smem_addr(tmem_slot), 512);
+    else tmem_alloc(smem_addr(tmem_slot), 512);
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // the peer's barriers exist before anything signals them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
@@ -236,12 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wside) prefetch_tensormap(&map_ul);
       }
       const uint32_t off = wside ? kACode : 0;
-      const uint32_t bytes = wside ? kBCode : kACode;
+      const uint32_t bytes = wside ? R::kBBytes : kACode;
+      const int half = static_cast<int>(rank) * R::kBRows;  // this CTA's weight rows of the tile
       int c = 0, issued = 0;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const TileInfo ti = tile_info(p, t);
-        const int row = wside ? ti.e * static_cast<int>(p.N) + ti.n0 : static_cast<int>(ti.m0);
-        const int lrow = wside ? ti.n0 : static_cast<int>(ti.m0);  // B_lora is shared by the experts
+      for (int t = unit; t < ntiles && ok; t += units) {
+        const TileInfo ti = tile_of<kPair>(p, t, rank);
+        const int row = wside ? ti.e * static_cast<int>(p.N) + ti.n0 + half : static_cast<int>(ti.m0);
+        const int lrow = wside ? ti.n0 + half : static_cast<int>(ti.m0);  // B_lora is shared by the experts
         for (int k = 0; k < ns; ++k) {
           const int prev = issued - S;  // the stage that last used ring slot c
           if (prev >= 0 && !mbar_wait(smem_addr(&mdone[prev % kDone]), (prev / kDone) & 1, p.status,
@@ -250,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t bar = smem_addr(&cfull[c]);
-          const uint32_t dst = smem_addr(smem + c * kStage + off);
+          const uint32_t dst = smem_addr(smem + c * R::kStageBytes + off);
           mbar_arrive_expect_tx(bar, bytes);
           if (k < nl)  // slice k / 2 of hi (k even) or lo (k odd), and of B_lora
             tma_load_2d(dst, wside ? &map_bl : (k & 1) ? &map_ul : &map_uh, (k >> 1) * kLoraK, lrow, bar);
@@ -259,9 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++c == S) c = 0;
         }
       }
-      // do not exit with copies in flight: wait for the last S stages to land
-      for (int j = max(0, issued - S); j < issued; ++j)
+      // do not exit with copies in flight (the last S stages to land), nor before the last S
+      // stages' commits have arrived here
+      for (int j = max(0, issued - S); j < issued; ++j) {
         mbar_wait(smem_addr(&cfull[j % S]), (j / S) & 1, p.status, kStatusTimeoutDrain);
+        if (wside) mbar_wait(smem_addr(&mdone[j % kDone]), (j / kDone) & 1, p.status, kStatusTimeoutDrain);
+      }
     }
   } else if (warp == 3) {
     // ---------------------------------------------------------------- scale producers (FP4 stages)
@@ -271,8 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(map);
       int f = 0, issued = 0;
       uint32_t ph = 0;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const TileInfo ti = tile_info(p, t);
+      for (int t = unit; t < ntiles && ok; t += units) {
+        const TileInfo ti = tile_of<kPair>(p, t, rank);
+        // the weight scales of all 256 rows of the tile, in both CTAs of a pair
         const int row = wside ? ti.e * static_cast<int>(p.N) + ti.n0 : static_cast<int>(ti.m0);
         for (int k = 0; k < ksteps; ++k) {
           if (!mbar_wait(smem_addr(&fempty[f]), ph ^ 1u, p.status, kStatusTimeoutProducer)) {
@@ -293,24 +403,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_addr(&ffull[j % kSfRing]), (j / kSfRing) & 1, p.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer (one thread)
-    if (lane == 0) {
-      const uint32_t idesc = idesc_nvf4_f32(kTile, kWN);
-      const uint32_t idesc_l = idesc_bf16_f32(kTile, kWN);
-      // ring slot c's operand descriptors add c * kStage to the start address field; a K step
+    // ---------------------------------------------------------------- MMA issuer (one thread; a pair's leader)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_nvf4_f32(kTile * kPeers, kWN);
+      const uint32_t idesc_l = idesc_bf16_f32(kTile * kPeers, kWN);
+      // ring slot c's operand descriptors add c * stage bytes to the start address field; a K step
       // (64 E2M1 codes or 16 bf16 values: 32 bytes of a swizzled row) adds 2
       const uint64_t adesc0 = smem_desc(smem_addr(smem), 16, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_addr(smem + kACode), 16, 1024, 2);
       const float gx = *p.g_x;
       int c = 0, li = 0, it = 0;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
-        // the previous tile's epilogue has read D
+      for (int t = unit; t < ntiles && ok; t += units, ++li) {
+        // the previous tile's epilogue has read D (in both CTAs of a pair)
         if (!mbar_wait(smem_addr(dfree), (li & 1) ^ 1, p.status, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const TileInfo ti = tile_info(p, t);
+        const TileInfo ti = tile_of<kPair>(p, t, 0);
         // alpha = 0 with a LoRA branch: D = s U B^T alone (the FP4 product would be scaled by 0)
         const bool fp4 = !(nl && gx * p.w_g[ti.e] == 0.f);
         for (int k = 0; k < ns; ++k) {
@@ -320,35 +430,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t soff = static_cast<uint64_t>(c * (kStage >> 4));
-          if (k < nl) {
+          const uint64_t soff = static_cast<uint64_t>(c * (R::kStageBytes >> 4));
+          const uint32_t sf = tmem + kSlot0 + kSlotCols * j;
+          if constexpr (kPair) {
+            if (k < nl) {
 #pragma unroll
-            for (int kk = 0; kk < kLoraK / 16; ++kk)
-              mma_f16_ss(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
-          } else if (fp4) {
-            const uint32_t sf = tmem + kSlot0 + kSlotCols * j;
-            mma_stage_nvf4(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+              for (int kk = 0; kk < kLoraK / 16; ++kk)
+                mma_f16_pair(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
+            } else if (fp4) {
+              mma_stage_nvf4_pair(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+            }
+            mma_commit_pair(smem_addr(&mdone[it % kDone]));
+          } else {
+            if (k < nl) {
+#pragma unroll
+              for (int kk = 0; kk < kLoraK / 16; ++kk)
+                mma_f16_ss(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
+            } else if (fp4) {
+              mma_stage_nvf4(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+            }
+            mma_commit(smem_addr(&mdone[it % kDone]));
           }
-          mma_commit(smem_addr(&mdone[it % kDone]));
           ++it;
           if (++c == S) c = 0;
         }
         if (!ok) break;
-        mma_commit(smem_addr(dfull));
+        if constexpr (kPair) mma_commit_pair(smem_addr(dfull));
+        else mma_commit(smem_addr(dfull));
       }
     }
     __syncwarp();
   } else if (warp >= kFirstSf && warp < kFirstEpi) {
     // ---------------------------------------------------------------- scale warps
-    // Group g (warps 5-8: g = 0, 9-12: g = 1) takes the stages it with it % 2 == g; stage it uses
+    // Group g (warps 4-7: g = 0, 8-11: g = 1) takes the stages it with it % 2 == g; stage it uses
     // TMEM scale slot it % kSlots. FP4 stage: lane i of quarter q reads activation row 32q + i (its
     // four K-step words) and writes them to columns 4t + w (for every w; the MMA reads 4t + q), and
-    // reads weight rows 32w + i, w = 0..7, writing column 16 + 8t + w = row 32w + i, K step t.
-    // LoRA stage: the slices have landed (the MMA issuer then waits on sfready alone).
+    // reads weight rows 32w + i, w = 0..7, writing column 16 + 8t + w = row 32w + i, K step t (all
+    // 256 rows, in each CTA of a pair). LoRA stage: the slices have landed. Either way the group
+    // then arrives on sfready (a pair's leader's), which the MMA issuer waits on alone.
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int g = (warp - kFirstSf) >> 2;
-    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int my_tiles = unit < ntiles ? (ntiles - 1 - unit) / units + 1 : 0;
     const int total = my_tiles * ns;
     for (int it = g; it < total && ok; it += 2) {
       const int li = it / ns, k = it - li * ns;
@@ -361,46 +484,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                kStatusTimeoutMma));
         if (!ok) break;
       }
-      if (k < nl) {
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&cfull[it % S]), static_cast<uint32_t>((it / S) & 1),
+      if (k >= nl) {
+        const int fi = li * ksteps + (k - nl);  // FP4 stage count: the scale ring's index
+        const int f = fi % kSfRing;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&ffull[f]), static_cast<uint32_t>((fi / kSfRing) & 1),
                                                p.status, kStatusTimeoutMma));
         if (!ok) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sfready[j]));
-        continue;
-      }
-      const int fi = li * ksteps + (k - nl);  // FP4 stage count: the scale ring's index
-      const int f = fi % kSfRing;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&ffull[f]), static_cast<uint32_t>((fi / kSfRing) & 1),
-                                             p.status, kStatusTimeoutMma));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t slot = tmem + lane_base + kSlot0 + kSlotCols * j;
-      const uint8_t* st = sfring + f * kSfStage;
-      const uint4 a = reinterpret_cast<const uint4*>(st)[q * 32 + lane];
-      tmem_st16_rep4(slot, a.x, a.y, a.z, a.w);
-      // weight scales in two halves of 16 columns: K steps 0-1, then 2-3
+        tc_fence_after();
+        const uint32_t slot = tmem + lane_base + kSlot0 + kSlotCols * j;
+        const uint8_t* st = sfring + f * kSfStage;
+        const uint4 a = reinterpret_cast<const uint4*>(st)[q * 32 + lane];
+        tmem_st16_rep4(slot, a.x, a.y, a.z, a.w);
+        // weight scales in two halves of 16 columns: K steps 0-1, then 2-3
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t b[16];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t b[16];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const uint2 r = reinterpret_cast<const uint2*>(st + kSfA)[(w * 32 + lane) * 2 + hh];
-          b[w] = r.x;
-          b[8 + w] = r.y;
+          for (int w = 0; w < 8; ++w) {
+            const uint2 r = reinterpret_cast<const uint2*>(st + kSfA)[(w * 32 + lane) * 2 + hh];
+            b[w] = r.x;
+            b[8 + w] = r.y;
+          }
+          tmem_st16(slot + 16 + 16 * hh, b);
         }
-        tmem_st16(slot + 16 + 16 * hh, b);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&fempty[f]));  // the scale tiles have been read
+        tmem_st_wait();
+        tc_fence_before();
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&fempty[f]));  // the scale tiles have been read
-      tmem_st_wait();
-      tc_fence_before();
-      // the stage's code tiles have landed too (the MMA issuer then waits on sfready alone)
+      // the stage's operand tiles have landed too
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&cfull[it % S]), static_cast<uint32_t>((it / S) & 1),
                                              p.status, kStatusTimeoutMma));
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sfready[j]));
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(smem_addr(&sfready[j]));
+        else mbar_arrive_remote(dsmem_map(smem_addr(&sfready[j]), 0));
+      }
     }
   } else if (warp >= kFirstEpi) {
     // ---------------------------------------------------------------- epilogue (16 warps)
@@ -409,12 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const float gx = *p.g_x;
     int li = 0;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++li) {
+    for (int t = unit; t < ntiles && ok; t += units, ++li) {
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(dfull), static_cast<uint32_t>(li & 1), p.status,
                                              kStatusTimeoutEpilogue));
       if (!ok) break;
       tc_fence_after();
-      const TileInfo ti = tile_info(p, t);
+      const TileInfo ti = tile_of<kPair>(p, t, rank);
       const float alpha = gx * p.w_g[ti.e];
       const float out = nl && alpha == 0.f ? 1.f : alpha;
       // this thread's row (TMEM lane 32q + lane), columns 64 part .. + 63, scaled and packed: unit u
@@ -432,7 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // D has been read: the next tile's MMAs may start while this warp stores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(dfree));
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(smem_addr(dfree));
+        else mbar_arrive_remote(dsmem_map(smem_addr(dfree), 0));
+      }
       // 8 x 8 transpose of 16-byte units within each group of 8 lanes: afterwards lane 8G + k holds
       // unit k of rows 8G .. 8G + 7 of the warp's 32 (in o[4j .. 4j + 3] for row 8G + j), so that
       // each store instruction writes four whole 128-byte row pieces instead of 32 scattered 32-byte
@@ -466,10 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // neither CTA leaves while the other may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
@@ -491,15 +616,19 @@ __global__ void __launch_bounds__(1024) tile_map128_kernel(const int32_t* __rest
 }
 
 struct W4a4Plan {
+  bool pair;   // CTA pairs (dense calls with at least two row tiles)
   int stages;
   size_t smem, ws_codes, ws_scales, ws_amax, ws_gx, ws_uh, ws_ul, ws_tiles, ws_total;
 };
 
-W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups, bool prequantized = false) {
+W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups, bool prequantized = false, bool grouped = false) {
   W4a4Plan t{};
+  t.pair = !grouped && M > kTile;
   const size_t fixed = 1024 + kSfRing * kSfStage + 512;
-  t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (227 * 1024 - fixed) / kStage));
-  t.smem = fixed + t.stages * kStage;
+  const size_t stage = t.pair ? Ring<true>::kStageBytes : Ring<false>::kStageBytes;
+  const size_t max_stages = t.pair ? Ring<true>::kMaxStages : Ring<false>::kMaxStages;
+  t.stages = static_cast<int>(std::min<size_t>(max_stages, (227 * 1024 - fixed) / stage));
+  t.smem = fixed + t.stages * stage;
   size_t o = 0;
   auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
   // activation codes, scales, amax word and g_x, unless the caller passes them in NVFP4
@@ -513,6 +642,36 @@ W4a4Plan w4a4_plan(int64_t M, int64_t K, int r, int groups, bool prequantized = 
   t.ws_tiles = take(static_cast<size_t>(groups + 2) * 4);
   t.ws_total = o;
   return t;
+}
+
+// CTA pairs of the pair kernel that fit on the device at once (cached per device and shared-memory size).
+int pair_clusters(int device, int smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(device, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaFuncSetAttribute(w4a4_wide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+      cudaFuncSetAttribute(w4a4_wide_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(w4a4_wide_kernel<true>), &cfg) != cudaSuccess)
+      n = 0;
+  }
+  if (n <= 0) cudaGetLastError();
+  cache[key] = n;
+  return n;
 }
 
 }  // namespace
@@ -531,8 +690,9 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
                               cudaStream_t st) {
   const int groups = a.offsets ? a.groups : 1;
   const bool pre = a.xq_codes != nullptr;
-  const W4a4Plan t = w4a4_plan(a.M, a.K, a.r, groups, pre);
+  const W4a4Plan t = w4a4_plan(a.M, a.K, a.r, groups, pre, a.offsets != nullptr);
   if (ws_bytes < t.ws_total) return NVFP4RL_ERR_WORKSPACE;
+  const uint32_t brows = t.pair ? Ring<true>::kBRows : Ring<false>::kBRows;  // weight rows per CTA
   char* base = static_cast<char*>(ws);
   const uint8_t* xc = pre ? a.xq_codes : reinterpret_cast<uint8_t*>(base + t.ws_codes);
   const uint8_t* xs = pre ? a.xq_scales : reinterpret_cast<uint8_t*>(base + t.ws_scales);
@@ -566,7 +726,7 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
   const uint64_t wrows = static_cast<uint64_t>(groups) * a.N;
   if (!make_tensor_map_2d(&mxc, CU_TENSOR_MAP_DATA_TYPE_UINT8, xc, a.K / 2, a.M, 1, 128, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tensor_map_2d(&mxs, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, a.K / 16, a.M, 1, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_tensor_map_2d(&mwc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, a.K / 2, wrows, 1, 128, kWN,
+      !make_tensor_map_2d(&mwc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, a.K / 2, wrows, 1, 128, brows,
                           CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tensor_map_2d(&mws, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_scales, a.K / 16, wrows, 1, 16, kWN,
                           CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -578,7 +738,7 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_2d(&mul, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ul, a.r, a.M, 2, kLoraK, kTile,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, a.r, a.N, 2, kLoraK, kWN,
+        !make_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, a.r, a.N, 2, kLoraK, brows,
                             CU_TENSOR_MAP_SWIZZLE_128B))
       return NVFP4RL_ERR_CUDA;
   } else {
@@ -591,7 +751,7 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
   p.tiles_n = static_cast<int>((a.N + kWN - 1) / kWN);
   const int64_t tiles_m_bound = a.offsets ? (a.M + kTile - 1) / kTile + groups : (a.M + kTile - 1) / kTile;
   p.tiles_m = static_cast<int>((a.M + kTile - 1) / kTile);
-  p.total_tiles = p.tiles_m * p.tiles_n;
+  p.total_tiles = (t.pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;  // pair tiles for a pair
   p.r = a.r;
   p.s = a.s;
   p.g_x = gx;
@@ -602,12 +762,31 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
   p.y = a.y;
   p.status = dev.status;
   p.stages = t.stages;
-  const int64_t max_tiles = tiles_m_bound * p.tiles_n;
-  const int grid = static_cast<int>(std::min<int64_t>(max_tiles, dev.sm_count));
-  if (cudaFuncSetAttribute(w4a4_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(t.smem)) != cudaSuccess)
+  if (!t.pair) {
+    const int64_t max_tiles = tiles_m_bound * p.tiles_n;
+    const int grid = static_cast<int>(std::min<int64_t>(max_tiles, dev.sm_count));
+    if (cudaFuncSetAttribute(w4a4_wide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(t.smem)) != cudaSuccess)
+      return NVFP4RL_ERR_CUDA;
+    w4a4_wide_kernel<false><<<grid, kThreads, t.smem, st>>>(mxc, mxs, mwc, mws, muh, mul, mb, p);
+    return launch_status();
+  }
+  const int clusters = pair_clusters(dev.device, static_cast<int>(t.smem));
+  if (clusters <= 0) return NVFP4RL_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min<int64_t>(p.total_tiles, clusters)), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = t.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, w4a4_wide_kernel<true>, mxc, mxs, mwc, mws, muh, mul, mb, p) != cudaSuccess)
     return NVFP4RL_ERR_CUDA;
-  w4a4_wide_kernel<<<grid, kThreads, t.smem, st>>>(mxc, mxs, mwc, mws, muh, mul, mb, p);
   return launch_status();
 }
 
