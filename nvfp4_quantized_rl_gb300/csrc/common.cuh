@@ -232,6 +232,13 @@ struct LoraDownScale {
 nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
                                 const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale = {});
 
+// The same on tcgen05 for prefill-sized M (lora_down_tc.cu); launch_lora_down takes it for
+// M >= kLoraDownTcMinRows.
+constexpr int64_t kLoraDownTcMinRows = 1024;
+bool lora_down_tc_supported(int64_t M, int64_t K, int r);
+nvfp4rl_status launch_lora_down_tc(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
+                                   const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale);
+
 // tcgen05 W4A4 block-scaled path (linear_w4a4_tc.cu).
 bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r);
 size_t w4a4_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int groups, bool prequantized);

@@ -83,7 +83,7 @@ struct TcParams {
   int stages_per_split;  // 256-K stages per CTA
   int splits;            // CTAs per cluster along K (1: no split)
   int r;                 // LoRA rank (0 or a multiple of 16)
-  int lora_box_bytes;    // min(2r, 128)
+  int lora_box_bytes;    // lora_box_bytes_for(r)
   float s;
   const float* w_g;
   uint16_t* y;
@@ -96,6 +96,12 @@ __host__ __device__ constexpr int x_stage_bytes(int mbox) { return 4 * mbox * 12
 // depth of the A-buffer / activation / stage-ready rings
 __host__ __device__ constexpr int ring_depth(int mbox) { return mbox <= 64 ? 3 : 2; }
 __host__ __device__ constexpr int threads_for(int deq_warps) { return 32 * (kFirstDeqWarp + deq_warps); }
+
+// LoRA operand tiles (B_lora rows, U rows) are loaded in boxes of 2r bytes for r <= 32 and of 128
+// bytes (64 ranks) otherwise; a rank that is not a multiple of 64 then leaves the last box partly
+// beyond r, which the copy fills with zeros. Shared memory holds lora_padded_rank(r) ranks per row.
+__host__ __device__ constexpr int lora_box_bytes_for(int r) { return r <= 32 ? 2 * r : 128; }
+__host__ __device__ constexpr int lora_padded_rank(int r) { return r <= 32 ? r : (r + 63) / 64 * 64; }
 
 __device__ __forceinline__ uint32_t swizzle_mode_for(int box_bytes) {
   return box_bytes == 128 ? 2u : box_bytes == 64 ? 4u : 6u;
@@ -222,9 +228,9 @@ __global__ void __maxnreg__(88)
   uint8_t* xring = smem;
   uint8_t* wring = xring + R * kXBytes;
   uint8_t* lora_a = wring + SW * kWStageBytes;
-  const int lora_a_bytes = p.r ? kRows * 2 * p.r : 0;
+  const int lora_a_bytes = p.r ? kRows * 2 * lora_padded_rank(p.r) : 0;
   uint8_t* lora_u = lora_a + lora_a_bytes;
-  const int lora_u_bytes = p.r ? MBOX * 2 * p.r : 0;
+  const int lora_u_bytes = p.r ? MBOX * 2 * lora_padded_rank(p.r) : 0;
   uint64_t* bars = reinterpret_cast<uint64_t*>(lora_u + lora_u_bytes);
   uint64_t* wfull = bars;             // [SW] weight stage landed
   uint64_t* wempty = wfull + SW;      // [SW] weight stage dequantized (DW arrivals)
@@ -299,7 +305,7 @@ __global__ void __maxnreg__(88)
     // ------------------------------------------------------------------ activation + LoRA producer
     if (lane == 0) {
       prefetch_tensormap(&map_x);
-      const int nbox = do_lora ? 2 * p.r / p.lora_box_bytes : 0;
+      const int nbox = do_lora ? 2 * lora_padded_rank(p.r) / p.lora_box_bytes : 0;
       const int box_el = p.lora_box_bytes / 2;
       if (do_lora) {
         // B_lora is an input of the call; U comes from the LoRA-down kernel (loaded at the end)
@@ -671,7 +677,7 @@ TcPlan plan_for(int64_t M, int64_t N, int r, int mbox, bool reserve_down) {
   t.mbox = mbox;
   t.tiles_m = static_cast<int>((M + t.mbox - 1) / t.mbox);
   t.tiles_n = static_cast<int>(N / kRows);
-  const size_t lora = r ? static_cast<size_t>(kRows + t.mbox) * 2 * r : 0;
+  const size_t lora = r ? static_cast<size_t>(kRows + t.mbox) * 2 * lora_padded_rank(r) : 0;
   const size_t fixed = 1024 + lora + 512;
   const size_t xring = static_cast<size_t>(ring_depth(t.mbox)) * x_stage_bytes(t.mbox);
   const size_t budget = 227 * 1024 - (reserve_down ? kDownSmem + 1024 : 0);
@@ -816,6 +822,7 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 // main kernel.
 nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
                                 const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale) {
+  if (lora_down_tc_supported(M, K, r)) return launch_lora_down_tc(x, M, K, A, r, U, dev, st, scale);
   const int nchunks = static_cast<int>(K / kDownK);
   const int rp = r > 32 && M > 64 ? 64 : 32;
   const int dc = down_cluster_size(dev.device, rp);
@@ -877,7 +884,7 @@ nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, c
   }
 
   CUtensorMap mc, ms, mx, mb, mu;
-  const int lbox = a.r ? std::min(2 * a.r, 128) : 128;
+  const int lbox = a.r ? lora_box_bytes_for(a.r) : 128;
   if (!make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, a.K / 2, a.N, 1, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_scales, a.K / 16, a.N, 1, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, 2, 64, t.mbox, CU_TENSOR_MAP_SWIZZLE_128B))

@@ -551,7 +551,8 @@ def test_linear_tiny(nv, w4a4):
 
 @pytest.mark.parametrize("w4a4", [False, True], ids=["w4a16", "w4a4"])
 @pytest.mark.parametrize("M,N,K,r,s", [(100, 384, 768, 32, 2.0), (1, 128, 256, 0, 2.0), (65, 256, 512, 16, 0.0),
-                                       (200, 640, 1024, 64, 0.5), (200, 384, 1024, 128, 1.0), (64, 256, 512, 128, 2.0)])
+                                       (200, 640, 1024, 64, 0.5), (200, 384, 1024, 128, 1.0), (64, 256, 512, 128, 2.0),
+                                       (130, 384, 768, 48, 1.0), (70, 256, 512, 112, 0.5)])
 def test_linear_multi_tile_ragged(nv, w4a4, M, N, K, r, s):
     q = _weights(N, K, 11, M, N)
     x = synth.heavy_tail_activation_bf16(M, K, 12, M) if w4a4 else synth.activation_bf16(M, K, 12, M)
@@ -605,6 +606,21 @@ def test_w4a4_small_activation_scale_bytes(nv):
     ref = ref_linear(True, xb, q, None, None, 0.0)
     P.assert_gemm_close(y[:1], ref[:1], "row 0 (normal scales)")
     P.assert_gemm_close(y[1:], ref[1:], "rows 1.. (subnormal activation scales)")
+
+
+@pytest.mark.parametrize("w4a4", [False, True], ids=["w4a16", "w4a4"])
+@pytest.mark.parametrize("M,K,r", [(1300, 1280, 16), (1300, 1280, 112), (2048, 768, 48), (1025, 512, 128)])
+def test_linear_prefill_sized_lora_down(nv, w4a4, M, K, r):
+    """From 1024 rows the LoRA down-projection runs on the tensor cores in 128-row tiles with K split
+    over a cluster; ragged row tiles, ranks from 16 to 128, plain U (W4A16) and hi/lo (W4A4) outputs.
+    Sampled rows, the first and last included."""
+    N = 256
+    q = _weights(N, K, 96, M, r)
+    x = synth.heavy_tail_activation_bf16(M, K, 97, r) if w4a4 else synth.activation_bf16(M, K, 97, r)
+    A, B = synth.lora_factors(r, K, N, 98, M)
+    y = gpu_linear(nv, w4a4, x, q, A, B, 1.5)
+    rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(99).choice(M, 62, replace=False)]))
+    P.assert_gemm_close(y[rows], ref_linear(w4a4, x, q, A, B, 1.5, rows=rows), f"M={M} K={K} r={r}")
 
 
 @pytest.mark.parametrize("r", [48, 96])
