@@ -170,7 +170,8 @@ nvfp4rl_status launch_quantize_cached(const void* x, int dtype, int64_t rows, in
                                       cudaStream_t st);
 
 nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
-                                  float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st);
+                                  float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st,
+                                  uint32_t* amax = nullptr);
 
 // RMSNorm-AQN of x into y and the NVFP4 quantization of y (quantize.cu); sync: two zeroable
 // words 16 bytes apart (kQuantizeWorkspace bytes).

@@ -1224,10 +1224,11 @@ nvfp4rl_status launch_rmsnorm_quantize(const uint16_t* x, int64_t M, int64_t H, 
       cudaGetLastError();  // fall back below
     }
   }
-  // otherwise: RMSNorm-AQN, then the amax and the encoding of y (its words were cleared above)
-  const nvfp4rl_status s1 = launch_rmsnorm_aqn(x, M, H, w, eps, sigma, delta, y, dev, st);
+  // otherwise: RMSNorm-AQN accumulating max |y| into the amax word (cleared above), then the
+  // encoding of y
+  const nvfp4rl_status s1 = launch_rmsnorm_aqn(x, M, H, w, eps, sigma, delta, y, dev, st, sync);
   if (s1 != NVFP4RL_OK) return s1;
-  return launch_quantize(y, NVFP4RL_BF16, M, H, nullptr, codes, scales, g, nullptr, sync, dev, st);
+  return launch_quantize(y, NVFP4RL_BF16, M, H, nullptr, codes, scales, g, nullptr, sync, dev, st, true);
 }
 
 }  // namespace nvfp4rl

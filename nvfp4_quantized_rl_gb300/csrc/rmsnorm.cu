@@ -14,7 +14,9 @@
 // fp32 weight for every row would move four times the bytes of x through L2. A row (H bf16) is read
 // with 128-bit loads into registers, the next row's load is issued before this row's reduction,
 // the sum of squares is reduced with warp shuffles and then over the eight warps in order, and
-// (w + sigma*eps) * x * r is written as bf16.
+// (w + sigma*eps) * x * r is written as bf16. With `amax_bits` the kernel also accumulates max |y| over
+// the bf16 values it writes (fp32 bit pattern, one atomicMax per CTA): the amax pass that the NVFP4
+// encoding of y would otherwise make.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -31,8 +33,11 @@ template <bool kNoise, int kVec>
 __global__ void __launch_bounds__(kThreads) rmsnorm_aqn_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t H,
                                                                const float* __restrict__ w,
                                                                const float* __restrict__ eps, float sigma,
-                                                               float delta, uint16_t* __restrict__ y) {
+                                                               float delta, uint16_t* __restrict__ y,
+                                                               uint32_t* __restrict__ amax_bits) {
   __shared__ float red[2][kThreads / 32];  // per-warp sums of squares, by row parity
+  __shared__ uint32_t mred[kThreads / 32];
+  uint32_t m2 = 0;  // max |y| of this thread, both bf16 halves
   griddep_wait();  // the preceding kernel's writes (x, or even w or eps) are visible from here on
   griddep_launch_dependents();
   const int nvec = static_cast<int>(H / 8);
@@ -106,10 +111,22 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_aqn_kernel(const uint16_t* _
           const float a = __uint_as_float(bf16_lo_bits(q[t])) * r * wt[i][2 * t];
           const float b = __uint_as_float(bf16_hi_bits(q[t])) * r * wt[i][2 * t + 1];
           o[t] = f32_to_bf16_bits(a) | (f32_to_bf16_bits(b) << 16);
+          m2 = __vmaxu2(m2, o[t] & 0x7FFF7FFFu);
         }
         yr[j] = make_uint4(o[0], o[1], o[2], o[3]);
       }
       v[i] = nx[i];
+    }
+  }
+  if (amax_bits) {
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) mred[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t r = 0;
+      for (int i = 0; i < kThreads / 32; ++i) r = max(r, mred[i]);
+      atomicMax(amax_bits, r);
     }
   }
 }
@@ -133,29 +150,30 @@ int resident_ctas(const DeviceInfo& dev) {
 
 template <bool kNoise, int kVec>
 cudaError_t launch_rows(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps, float sigma,
-                        float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st) {
+                        float delta, uint16_t* y, uint32_t* amax, const DeviceInfo& dev, cudaStream_t st) {
   const int64_t G = std::min<int64_t>(M, static_cast<int64_t>(dev.sm_count) * resident_ctas<kNoise, kVec>(dev));
   return launch_pdl(rmsnorm_aqn_kernel<kNoise, kVec>, dim3(static_cast<unsigned>(G)), dim3(kThreads), 0, st, x, M, H,
-                    w, eps, sigma, delta, y);
+                    w, eps, sigma, delta, y, amax);
 }
 
 template <bool kNoise>
 cudaError_t launch_vec(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps, float sigma,
-                       float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st) {
+                       float delta, uint16_t* y, uint32_t* amax, const DeviceInfo& dev, cudaStream_t st) {
   const int64_t vec = (H / 8 + kThreads - 1) / kThreads;
-  if (vec <= 1) return launch_rows<kNoise, 1>(x, M, H, w, eps, sigma, delta, y, dev, st);
-  if (vec == 2) return launch_rows<kNoise, 2>(x, M, H, w, eps, sigma, delta, y, dev, st);
-  if (vec == 3) return launch_rows<kNoise, 3>(x, M, H, w, eps, sigma, delta, y, dev, st);
-  return launch_rows<kNoise, 4>(x, M, H, w, eps, sigma, delta, y, dev, st);
+  if (vec <= 1) return launch_rows<kNoise, 1>(x, M, H, w, eps, sigma, delta, y, amax, dev, st);
+  if (vec == 2) return launch_rows<kNoise, 2>(x, M, H, w, eps, sigma, delta, y, amax, dev, st);
+  if (vec == 3) return launch_rows<kNoise, 3>(x, M, H, w, eps, sigma, delta, y, amax, dev, st);
+  return launch_rows<kNoise, 4>(x, M, H, w, eps, sigma, delta, y, amax, dev, st);
 }
 
 }  // namespace
 
 nvfp4rl_status launch_rmsnorm_aqn(const uint16_t* x, int64_t M, int64_t H, const float* w, const float* eps,
-                                  float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st) {
+                                  float sigma, float delta, uint16_t* y, const DeviceInfo& dev, cudaStream_t st,
+                                  uint32_t* amax) {
   if (M == 0) return NVFP4RL_OK;
-  const cudaError_t e = eps ? launch_vec<true>(x, M, H, w, eps, sigma, delta, y, dev, st)
-                            : launch_vec<false>(x, M, H, w, eps, sigma, delta, y, dev, st);
+  const cudaError_t e = eps ? launch_vec<true>(x, M, H, w, eps, sigma, delta, y, amax, dev, st)
+                            : launch_vec<false>(x, M, H, w, eps, sigma, delta, y, amax, dev, st);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
   return launch_status();
 }
