@@ -139,6 +139,8 @@ nvfp4rl_status launch_quantize_batch(int count, const void* const* x, const int6
 // amax_done: *amax_scratch already holds the tensor's amax bits (no amax pass is launched).
 // record (non-NULL only without mask): the plain encoding also writes its rounding directions,
 // 16 bits per 16-element block.
+// Clears one word (the amax accumulator) with a one-thread kernel chained by programmatic dependent launch.
+nvfp4rl_status launch_zero_word(uint32_t* p, cudaStream_t st);
 nvfp4rl_status launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, const uint32_t* mask,
                                uint8_t* codes, uint8_t* scales, float* g, const float* amax_in,
                                uint32_t* amax_scratch, const DeviceInfo& dev, cudaStream_t st, bool amax_done = false,
@@ -237,8 +239,14 @@ nvfp4rl_status launch_lora_down(const uint16_t* x, int64_t M, int64_t K, const u
 // M >= kLoraDownTcMinRows.
 constexpr int64_t kLoraDownTcMinRows = 1024;
 bool lora_down_tc_supported(int64_t M, int64_t K, int r);
+// amax (or null): accumulates max |x| into that word (atomicMax of the fp32 bit pattern; the caller
+// clears it first), the amax the NVFP4 encoding of x needs.
 nvfp4rl_status launch_lora_down_tc(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
-                                   const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale);
+                                   const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale,
+                                   uint32_t* amax = nullptr);
+// U (plain, [M][r] bf16) -> hi and lo of c U in place (hi over U, lo into scale.lo).
+nvfp4rl_status launch_lora_scale(uint16_t* U, int64_t M, int r, const LoraDownScale& scale, const DeviceInfo& dev,
+                                 cudaStream_t st);
 
 // tcgen05 W4A4 block-scaled path (linear_w4a4_tc.cu).
 bool w4a4_tc_supported(int64_t M, int64_t N, int64_t K, int r);

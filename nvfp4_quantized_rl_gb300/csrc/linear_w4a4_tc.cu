@@ -701,22 +701,35 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
   uint16_t* Ul = reinterpret_cast<uint16_t*>(base + t.ws_ul);
   int32_t* tiles = reinterpret_cast<int32_t*>(base + t.ws_tiles);
 
-  if (!pre) {
-    nvfp4rl_status sq = launch_quantize(a.x, NVFP4RL_BF16, a.M, a.K, nullptr, reinterpret_cast<uint8_t*>(base + t.ws_codes),
-                                        reinterpret_cast<uint8_t*>(base + t.ws_scales),
-                                        reinterpret_cast<float*>(base + t.ws_gx), nullptr,
-                                        reinterpret_cast<uint32_t*>(base + t.ws_amax), dev, st);
-    if (sq != NVFP4RL_OK) return sq;
-  }
-  if (a.r) {
-    LoraDownScale ls;
-    ls.g_x = gx;
-    ls.w_g = a.w_g;
-    ls.s = a.s;
-    ls.lo = Ul;
-    ls.status = dev.status;
-    const nvfp4rl_status sd = launch_lora_down(a.x, a.M, a.K, a.A, a.r, Uh, dev, st, ls);
-    if (sd != NVFP4RL_OK) return sd;
+  LoraDownScale ls;  // hi and lo of c U
+  ls.g_x = gx;
+  ls.w_g = a.w_g;
+  ls.s = a.s;
+  ls.lo = Ul;
+  ls.status = dev.status;
+  uint8_t* qcodes = reinterpret_cast<uint8_t*>(base + t.ws_codes);
+  uint8_t* qscales = reinterpret_cast<uint8_t*>(base + t.ws_scales);
+  float* qg = reinterpret_cast<float*>(base + t.ws_gx);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(base + t.ws_amax);
+  if (!pre && a.r && lora_down_tc_supported(a.M, a.K, a.r)) {
+    // x is read twice instead of three times: the tensor-core LoRA-down takes max |x| from the tiles it
+    // streams, the encoding then needs no amax pass; U is scaled to hi/lo once g_x is known
+    nvfp4rl_status e = launch_zero_word(amax, st);
+    if (e == NVFP4RL_OK) e = launch_lora_down_tc(a.x, a.M, a.K, a.A, a.r, Uh, dev, st, LoraDownScale{}, amax);
+    if (e == NVFP4RL_OK)
+      e = launch_quantize(a.x, NVFP4RL_BF16, a.M, a.K, nullptr, qcodes, qscales, qg, nullptr, amax, dev, st, true);
+    if (e == NVFP4RL_OK) e = launch_lora_scale(Uh, a.M, a.r, ls, dev, st);
+    if (e != NVFP4RL_OK) return e;
+  } else {
+    if (!pre) {
+      const nvfp4rl_status sq = launch_quantize(a.x, NVFP4RL_BF16, a.M, a.K, nullptr, qcodes, qscales, qg, nullptr,
+                                                amax, dev, st);
+      if (sq != NVFP4RL_OK) return sq;
+    }
+    if (a.r) {
+      const nvfp4rl_status sd = launch_lora_down(a.x, a.M, a.K, a.A, a.r, Uh, dev, st, ls);
+      if (sd != NVFP4RL_OK) return sd;
+    }
   }
   if (a.offsets) {
     tile_map128_kernel<<<1, 1024, 0, st>>>(a.offsets, groups, tiles);

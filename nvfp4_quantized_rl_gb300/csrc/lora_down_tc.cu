@@ -11,8 +11,11 @@
 // 128 / ks) over all partials in rank order (distributed shared memory) and writes U, or, for the
 // W4A4 path, hi and lo of c U (LoraDownScale). The sums run through the same K ranges and rank
 // order on every call, so U is deterministic.
+// With `amax` the kernel also accumulates max |x| over every element it loads (fp32 bit pattern, an
+// atomicMax per warp): the tensor amax that the NVFP4 encoding of x needs, without a pass of its own.
 //   warp 0   TMA producer (one thread)
 //   warp 1   TMEM allocation; one thread issues the MMAs
+//   warps 2-3 with `amax`: each scans half of every landed x tile
 //   warps 0-3 after the K loop: TMEM -> shared-memory partials, then the cluster reduction
 
 #include <cuda.h>
@@ -46,6 +49,7 @@ struct DownParams {
   int nchunks;
   uint16_t* U;
   LoraDownScale ls;
+  uint32_t* amax;  // or null
   uint32_t* status;
 };
 
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
-      mbar_init(smem_addr(&empty[i]), 1);
+      mbar_init(smem_addr(&empty[i]), p.amax ? 3 : 1);  // the MMAs' commit (+ the two scanning warps)
     }
     mbar_init(smem_addr(done), 1);
     fence_barrier_init();
@@ -128,6 +132,27 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
       mma_commit(smem_addr(&empty[s]));
     }
     mma_commit(smem_addr(done));  // every MMA above has completed (also when there were none)
+  } else if (p.amax && (warp == 2 || warp == 3)) {
+    // ---------------------------------------------------------------- max |x| of the landed tiles
+    uint32_t m2 = 0;
+    const int half = warp - 2;  // bytes [half 8 KB, half 8 KB + 8 KB) of the x tile
+    for (int i = 0; i < n && ok; ++i) {
+      const int s = i % kStages;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (i / kStages) & 1, p.status, kStatusTimeoutMma));
+      if (!ok) break;
+      const uint4* t = reinterpret_cast<const uint4*>(smem + s * stage_bytes + half * (kXBytes / 2));
+#pragma unroll 4
+      for (int e = lane; e < kXBytes / 2 / 16; e += 32) {
+        const uint4 v = t[e];
+        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                   __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) atomicMax(p.amax, m);
   }
   __syncwarp();
   // ---------------------------------------------------------------- partial tile -> shared memory
@@ -207,6 +232,35 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
 
 namespace {
 
+// U (bf16) -> hi and lo of c U in place (hi over U, lo into `lo`), c = s / (g_x w_g) (s when that
+// is 0): the form the W4A4 GEMM consumes, for a LoRA-down that ran before g_x was known.
+__global__ void __launch_bounds__(256) lora_scale_kernel(uint16_t* __restrict__ U, uint16_t* __restrict__ lo,
+                                                         int64_t n8, LoraDownScale ls) {
+  const float alpha = *ls.g_x * *ls.w_g;
+  const float cu = alpha == 0.f ? ls.s : ls.s / alpha;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && !(fabsf(cu) <= 0x1p100f)) atomicOr(ls.status, kStatusRange);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(U)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t hh[2], ll[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float cuv = __uint_as_float(k ? (w[e] & 0xFFFF0000u) : (w[e] << 16)) * cu;
+        hh[k] = f32_to_bf16_bits(cuv);
+        ll[k] = f32_to_bf16_bits(cuv - __uint_as_float(hh[k] << 16));
+      }
+      h[e] = hh[0] | (hh[1] << 16);
+      l[e] = ll[0] | (ll[1] << 16);
+    }
+    reinterpret_cast<uint4*>(U)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+    reinterpret_cast<uint4*>(lo)[i] = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
 size_t down_smem_bytes(int r) {
   return 1024 + static_cast<size_t>(kStages) * (kXBytes + static_cast<size_t>(r) * kChunk * 2) + 256;
 }
@@ -253,7 +307,7 @@ bool lora_down_tc_supported(int64_t M, int64_t K, int r) {
 }
 
 nvfp4rl_status launch_lora_down_tc(const uint16_t* x, int64_t M, int64_t K, const uint16_t* A, int r, uint16_t* U,
-                                   const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale) {
+                                   const DeviceInfo& dev, cudaStream_t st, const LoraDownScale& scale, uint32_t* amax) {
   const int maxc = down_tc_max_cluster(dev.device, r);
   if (maxc == 0) return NVFP4RL_ERR_CUDA;
   const int nchunks = static_cast<int>(K / kChunk);
@@ -275,6 +329,7 @@ nvfp4rl_status launch_lora_down_tc(const uint16_t* x, int64_t M, int64_t K, cons
   p.chunks_per_cta = (nchunks + ks - 1) / ks;
   p.U = U;
   p.ls = scale;
+  p.amax = amax;
   p.status = dev.status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ks), static_cast<unsigned>(row_tiles), 1);
@@ -291,6 +346,15 @@ nvfp4rl_status launch_lora_down_tc(const uint16_t* x, int64_t M, int64_t K, cons
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, lora_down_tc_kernel, mx, ma, p) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  return launch_status();
+}
+
+nvfp4rl_status launch_lora_scale(uint16_t* U, int64_t M, int r, const LoraDownScale& scale, const DeviceInfo& dev,
+                                 cudaStream_t st) {
+  const int64_t n8 = M * r / 8;
+  if (n8 == 0) return NVFP4RL_OK;
+  const int grid = static_cast<int>(std::min<int64_t>((n8 + 255) / 256, static_cast<int64_t>(dev.sm_count) * 4));
+  lora_scale_kernel<<<grid, 256, 0, st>>>(U, scale.lo, n8, scale);
   return launch_status();
 }
 

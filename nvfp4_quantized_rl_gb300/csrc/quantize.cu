@@ -1024,6 +1024,11 @@ nvfp4rl_status launch_amax_accumulate(const void* x, int dtype, int64_t n, uint3
 
 }  // namespace
 
+nvfp4rl_status launch_zero_word(uint32_t* p, cudaStream_t st) {
+  if (launch_pdl(zero_word_kernel, dim3(1), dim3(32), 0, st, p) != cudaSuccess) return NVFP4RL_ERR_CUDA;
+  return launch_status();
+}
+
 nvfp4rl_status launch_amax(const void* x, int dtype, int64_t n, uint32_t* amax_bits, const DeviceInfo& dev,
                            cudaStream_t st) {
   if (launch_pdl(zero_word_kernel, dim3(1), dim3(32), 0, st, amax_bits) != cudaSuccess) return NVFP4RL_ERR_CUDA;
