@@ -269,8 +269,9 @@ NVFP4RL_API nvfp4rl_status nvfp4_kv_append(const uint16_t* k, const uint16_t* v,
  *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_KV_ATTENTION, B, Hkv, Lmax, 0, 0) bytes (may be 0
  *            and NULL), device, 16-byte aligned; scratch.
  * Scores and the softmax are fp32 (exp2 on scores prescaled by log2 e); the products P V take P
- *   rounded to bf16; K and V are dequantized exactly (bf16). Long caches are split into spans
- *   merged by a second kernel.
+ *   rounded to f16; K and V are dequantized exactly (f16), q enters as f16 scaled by a power of two
+ *   (exact for every element above 2^-31 of the group's max |q|). Long caches are split into spans
+ *   merged by a second kernel. B * Lmax must stay below 2^31 - 64 (32-bit copy coordinates).
  * Errors: NVFP4RL_ERR_INVALID_ARG, NVFP4RL_ERR_UNSUPPORTED_SHAPE, NVFP4RL_ERR_MISALIGNED,
  *   NVFP4RL_ERR_WORKSPACE, NVFP4RL_ERR_ALIAS.
  */

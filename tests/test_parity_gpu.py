@@ -347,6 +347,8 @@ def test_kv_append(nv):
     (4, 28, 4, 300, [300, 129, 64, 65]),
     (2, 16, 1, 2000, [1999, 640]),
     (2, 8, 2, 50, [0, 50]),
+    (2, 40, 8, 130, [130, 66]),     # 5 query heads per KV head (Qwen2.5-32B grouping)
+    (3, 9, 1, 257, [257, 1, 128]),  # 9 heads: two head tiles, the second nearly empty
 ])
 def test_kv_decode_attention(nv, B, Hq, Hkv, Lmax, lens):
     """Cache built by nvfp4_kv_append one token at a time, attention against the oracle on the same
@@ -374,6 +376,59 @@ def test_kv_decode_attention(nv, B, Hq, Hkv, Lmax, lens):
                                   lens[live], scale)
     P.assert_gemm_close(got[live], ref, f"attention {B}x{Hq}/{Hkv} L={Lmax}")
     assert not got[~live].any(), "a sequence of length 0 gives zeros"
+
+
+def _random_cache(B, Lmax, Hkv, lens, seed, fill):
+    """Valid random NVFP4 rows (codes any byte, scale bytes 0x28..0x3F) below each length, `fill`
+    bytes at and past it (0xFF: NaN scale bytes, -6 codes)."""
+    rng = np.random.default_rng(seed)
+    kc = rng.integers(0, 256, (B, Lmax, Hkv, 64), dtype=np.uint8)
+    vc = rng.integers(0, 256, (B, Lmax, Hkv, 64), dtype=np.uint8)
+    ks = rng.integers(0x28, 0x40, (B, Lmax, Hkv, 8), dtype=np.uint8)
+    vs = rng.integers(0x28, 0x40, (B, Lmax, Hkv, 8), dtype=np.uint8)
+    for b, n in enumerate(lens):
+        for arr in (kc, vc, ks, vs):
+            arr[b, n:] = fill
+    return kc, ks, vc, vs
+
+
+def test_kv_decode_attention_ignores_rows_past_length(nv):
+    """Rows at and past each sequence's length hold NaN scale bytes and -6 codes (never written by
+    nvfp4_kv_append): they must not reach the output, in full groups, ragged tails and spans."""
+    B, Hq, Hkv, Lmax, D = 4, 28, 4, 300, 128
+    lens = np.array([300, 129, 1, 64], np.int32)
+    caches = _random_cache(B, Lmax, Hkv, lens, 37, 0xFF)
+    g = np.float32(1.0 / 64)
+    gd = P.dev(np.array([g]))
+    q = synth.activation_bf16(B * Hq, D, 38, 1).reshape(B, Hq, D)
+    dev = [torch.from_numpy(c).cuda() for c in caches]
+    out = nv.nvfp4_kv_decode_attention(P.dev_bf16(q), dev[0], dev[1], gd, dev[2], dev[3], gd, P.dev(lens),
+                                       1.0 / np.sqrt(D))
+    torch.cuda.synchronize()
+    got = P.host_bits(out)
+    ref = oracle.attention_decode(q, caches[0], caches[1], g, caches[2], caches[3], g, lens, 1.0 / np.sqrt(D))
+    assert np.all(np.isfinite(P.bf16_f64(got))), "rows past the length leaked into the output"
+    P.assert_gemm_close(got, ref, "NaN-filled rows past the lengths")
+
+
+@pytest.mark.parametrize("qmag", [2.0 ** -60, 2.0 ** 40, 0.0])
+def test_kv_decode_attention_query_magnitudes(nv, qmag):
+    """q scaled far from 1 (scores near 0: a near-uniform average; scores huge: one token wins) and
+    q = 0 (the exact average of V): the power-of-two scaling of q must keep every result."""
+    B, Hq, Hkv, Lmax, D = 2, 7, 1, 200, 128
+    lens = np.array([200, 77], np.int32)
+    caches = _random_cache(B, Lmax, Hkv, lens, 39, 0)
+    g = np.float32(1.0 / 64)
+    gd = P.dev(np.array([g]))
+    q = synth.bf16_bits((P.bf16_f64(synth.activation_bf16(B * Hq, D, 40, 1)) * qmag).astype(np.float32))
+    q = q.reshape(B, Hq, D)
+    dev = [torch.from_numpy(c).cuda() for c in caches]
+    out = nv.nvfp4_kv_decode_attention(P.dev_bf16(q), dev[0], dev[1], gd, dev[2], dev[3], gd, P.dev(lens),
+                                       1.0 / np.sqrt(D))
+    torch.cuda.synchronize()
+    got = P.host_bits(out)
+    ref = oracle.attention_decode(q, caches[0], caches[1], g, caches[2], caches[3], g, lens, 1.0 / np.sqrt(D))
+    P.assert_gemm_close(got, ref, f"q x {qmag}")
 
 
 def test_kv_decode_attention_qwen7b_sampled(nv):
