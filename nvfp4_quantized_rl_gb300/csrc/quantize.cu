@@ -265,6 +265,21 @@ __device__ __forceinline__ uint32_t bf16x2_gt(uint32_t a, uint32_t b) {  // per 
   return d;
 }
 
+// Four code bytes from eight fp32 values (y[2i] the low nibble of byte i): E2M1 codes by the
+// hardware conversion (round to nearest, ties to even, saturating; the sign of zero kept).
+__device__ __forceinline__ uint32_t e2m1_word(const float (&y)[8]) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(d)
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -276,23 +291,79 @@ __device__ __forceinline__ uint32_t bf16_rd(float v) { return __float_as_uint(v)
 // bf16 pattern of the smallest bf16 >= v (v >= 0 finite fp32).
 __device__ __forceinline__ uint32_t bf16_ru(float v) { return (__float_as_uint(v) + 0xFFFFu) >> 16; }
 
+// bar.sync on a named barrier among `threads` threads (whole warps) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Per-tensor lookup tables for the bf16 plain encoding, built in shared memory by every CTA
 // (they depend only on g):
 //   mid[i]  = (RD, RU) of 3 g (E4M3(i) + E4M3(i + 1)): six times the midpoint between scale
 //             bytes i and i + 1, rounded down and up (i = 0 .. 0x7D), for the exact scale byte;
 //   thr[b]  = for scale byte b, the seven element thresholds as bf16 patterns in both halves of a
-//             word, ready for the two-element compares (b = 0: +inf).
+//             word, ready for the two-element compares (b = 0: +inf);
+//   rcp[b]  = a reciprocal of E4M3(b) g with which the hardware conversion of fl32(x) * rcp[b] to
+//             E2M1 gives every element's exact code (cvt_reciprocal), else -1; 0 for a zero scale.
 struct EncodeTables {
   float2 mid[0x7E];
   uint4 thr[0x7F][2];
+  float rcp[0x7F];
 };
 
-__device__ void build_encode_tables(EncodeTables& t, float g) {
-  for (int i = threadIdx.x; i < 0x7E; i += blockDim.x) {
+// A reciprocal r of d = E4M3(b) g for the conversion form of the plain encoding, or -1.
+// cvt.rn.satfinite.e2m1x2 rounds y = fl32(x r) to E2M1 (nearest, ties to the even code,
+// saturating at 6), which is the exact rounding of |x|/d unless y and x/d fall on different sides
+// of a midpoint m (or y lands on m while x/d does not). With r within 3.5 fp32 ulps of 1/d, y is
+// within 2^-21.2 of x/d (relative), so only a bf16 x within 2^-20 of m d can be misrounded, and
+// there is at most one such bf16 value B per midpoint (their spacing is 2^-8 relative). All in
+// fp32: m d = ph + pl exactly (an FMA gives the product's rounding error), so for each such B the
+// exact side of m d it lies on (above, below, or on it: then the even code) is known, and
+// fl32(B r) is one multiply; r is taken as RN(1/fl32(d)) or one of its four nearest fp32
+// neighbours, the first for which every such B goes to its exact side. Zero scale (b = 0, or g
+// not positive): 0, so x 0 = +-0 and every code is sign|0, as the compares give.
+__device__ float cvt_reciprocal(int b, float g) {
+  if (b == 0 || !(g > 0.0f)) return 0.0f;
+  const float dec = e4m3_decode_pos(b);
+  const float dh = __fmul_rn(dec, g);
+  if (!(dh > 0x1p-120f)) return -1.0f;  // 1/d near the fp32 range: the compare form
+  const float r0 = __frcp_rn(dh);
+  const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+  float B[7];
+  bool near[7], up[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    const float md = mids[k] * dec;  // exact: at most 7 significant bits
+    const float ph = __fmul_rn(md, g), pl = __fmaf_rn(md, g, -ph);
+    const uint32_t t = __float_as_uint(ph) & 0xFFFF0000u;  // the bf16 grid points around m d
+    const float lo = __uint_as_float(t), hi = __uint_as_float(t + 0x10000u);
+    const float dlo = (lo - ph) - pl, dhi = (hi - ph) - pl;  // B - m d, with its exact sign
+    const float tol = 0x1p-20f * ph;
+    near[k] = fabsf(dlo) <= tol || fabsf(dhi) <= tol;
+    B[k] = fabsf(dlo) <= tol ? lo : hi;
+    const float dB = fabsf(dlo) <= tol ? dlo : dhi;
+    up[k] = dB > 0.0f || (dB == 0.0f && (k & 1));  // exact side; a tie at odd k goes up to the even code
+  }
+  const int step[5] = {0, -1, 1, -2, 2};
+#pragma unroll 1
+  for (int i = 0; i < 5; ++i) {
+    const float r = __uint_as_float(__float_as_uint(r0) + step[i]);
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < 7; ++k) {
+      const float y = __fmul_rn(B[k], r);
+      ok = ok && (!near[k] || (y > mids[k] || (y == mids[k] && (k & 1))) == up[k]);
+    }
+    if (ok) return r;
+  }
+  return -1.0f;
+}
+
+__device__ void build_encode_tables(EncodeTables& t, float g, bool with_rcp, int tid, int nthreads) {
+  for (int i = tid; i < 0x7E; i += nthreads) {
     const float m3 = 3.0f * (e4m3_decode_pos(i) + e4m3_decode_pos(i + 1));  // exact in fp32
     t.mid[i] = make_float2(__fmul_rd(m3, g), __fmul_ru(m3, g));
   }
-  for (int b = threadIdx.x; b < 0x7F; b += blockDim.x) {
+  for (int b = tid; b < 0x7F; b += nthreads) {
     uint32_t tk[8];
     if (b == 0 || !(g > 0.0f)) {
 #pragma unroll
@@ -309,6 +380,7 @@ __device__ void build_encode_tables(EncodeTables& t, float g) {
     }
     t.thr[b][0] = make_uint4(tk[0], tk[1], tk[2], tk[3]);
     t.thr[b][1] = make_uint4(tk[4], tk[5], tk[6], tk[7]);
+    t.rcp[b] = with_rcp ? cvt_reciprocal(b, g) : -1.0f;
   }
 }
 
@@ -363,35 +435,26 @@ __device__ __forceinline__ uint32_t scale_byte_tab(float bamax, float est, const
   return b - dec + inc;
 }
 
-// Plain encoding of one block of bf16 values (finite), two elements per instruction. For bf16 x and a
-// real P: x > P <=> x > RD_bf16(P) and x >= P <=> x > pred(RU_bf16(P)), with RD_bf16(P) =
+// The compare form of the plain bf16 encoding (scale byte b already chosen): for bf16 x and a real
+// P, x > P <=> x > RD_bf16(P) and x >= P <=> x > pred(RU_bf16(P)), with RD_bf16(P) =
 // RD_bf16(RD_fp32(P)) and RU_bf16(P) = RU_bf16(RU_fp32(P)); so the seven midpoint thresholds
 // become bf16 values compared with set.gt.bf16x2, and the magnitude code is the number of
 // thresholds exceeded, accumulated with add.bf16x2 on 128.0 (128 + c is exact and its low
-// three bits are c). The scale byte's midpoint products and the thresholds of every scale
-// byte come from per-tensor tables in shared memory.
-__device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
-                                                  float est_scale, const EncodeTables& tab,
-                                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
-  uint32_t aw[8];
-  uint32_t m2 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    aw[i] = w[i] & 0x7FFF7FFFu;
-    m2 = __vmaxu2(m2, aw[i]);
-  }
-  const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-  uint32_t b = 0;
-  if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, tab);
+// three bits are c). Taken for the blocks the conversion form cannot round exactly (rare);
+// not inlined, so the common form's warps branch around it.
+__device__ __noinline__ void encode_block_bf16_compare(uint4 v0, uint4 v1, int64_t blk, uint32_t b,
+                                                       const EncodeTables& tab, uint8_t* __restrict__ codes,
+                                                       uint8_t* __restrict__ scales) {
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   const uint4 ta = tab.thr[b][0], tb = tab.thr[b][1];
   const uint32_t T2[7] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z};
   uint32_t byte[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
+    const uint32_t aw = w[i] & 0x7FFF7FFFu;
     uint32_t acc = 0x43004300u;  // bf16x2 (128, 128)
 #pragma unroll
-    for (int k = 0; k < 7; ++k) acc = bf16x2_add(acc, bf16x2_gt(aw[i], T2[k]));
+    for (int k = 0; k < 7; ++k) acc = bf16x2_add(acc, bf16x2_gt(aw, T2[k]));
     const uint32_t m = acc & 0x00070007u;
     const uint32_t s = w[i] & 0x80008000u;
     // low byte: magnitude of element 2i in bits 0-2, its sign in bit 3, element 2i+1 in bits 4-7
@@ -400,6 +463,41 @@ __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t b
   const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
   const uint32_t hi = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
   *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo, hi);
+  scales[blk] = static_cast<uint8_t>(b);
+}
+
+// Plain encoding of one block of bf16 values: the exact scale byte from the block amax, then the
+// codes by the hardware conversion of fl32(x) / (E4M3(s) g) where cvt_reciprocal shows that
+// exact, else by the compare form. The scale byte's midpoint products come from the per-tensor
+// tables in shared memory.
+__device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
+                                                  float est_scale, const EncodeTables& tab,
+                                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+  const uint32_t bamax_bits = max(m2 & 0xFFFFu, m2 >> 16);
+  const float bamax = __uint_as_float(bamax_bits << 16);
+  uint32_t b = 0;
+  if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, tab);
+  const float rcp = tab.rcp[b];
+  if (!(rcp >= 0.0f && bamax_bits < 0x7F80u)) {
+    encode_block_bf16_compare(v[0], v[1], blk, b, tab, codes, scales);
+    return;
+  }
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      y[2 * i] = __fmul_rn(__uint_as_float(w[4 * h + i] << 16), rcp);
+      y[2 * i + 1] = __fmul_rn(__uint_as_float(w[4 * h + i] & 0xFFFF0000u), rcp);
+    }
+    out[h] = e2m1_word(y);
+  }
+  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(out[0], out[1]);
   scales[blk] = static_cast<uint8_t>(b);
 }
 
@@ -637,22 +735,27 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kMode != kModeCached, EncodeTables, char> tab;
   __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kMode != kModePlain, GuidedTables, char> gtab;
   if constexpr (kDtype == NVFP4RL_BF16) {
-    if constexpr (kMode != kModeCached) build_encode_tables(tab, g);
+    if constexpr (kMode != kModeCached) build_encode_tables(tab, g, kMode == kModePlain, threadIdx.x, blockDim.x);
     if constexpr (kMode != kModePlain) build_guided_tables(gtab, g);
     __syncthreads();
   }
 
-  // Two blocks per iteration, both loaded before either is encoded (more bytes in flight).
+  // Two blocks per iteration, both loaded before either is encoded, and the next iteration's
+  // two loaded before this one's are encoded (software pipelining: more bytes in flight).
   // The blocks are visited from the end of the tensor to its start: the amax pass that
   // precedes this kernel reads from start to end, so the tensor's tail is still in L2.
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < nblocks; j += 2 * stride) {
+  BlockWords<kDtype> na, nb;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j0 < nblocks) load_block<kDtype>(x, nblocks - 1 - j0, na);
+  if (j0 + stride < nblocks) load_block<kDtype>(x, nblocks - 1 - j0 - stride, nb);
+  for (int64_t j = j0; j < nblocks; j += 2 * stride) {
     const int64_t blk = nblocks - 1 - j;
     const bool two = j + stride < nblocks;
     const int64_t blk2 = blk - stride;
-    BlockWords<kDtype> a, b;
-    load_block<kDtype>(x, blk, a);
-    if (two) load_block<kDtype>(x, blk2, b);
+    const BlockWords<kDtype> a = na, b = nb;
+    if (j + 2 * stride < nblocks) load_block<kDtype>(x, blk - 2 * stride, na);
+    if (j + 3 * stride < nblocks) load_block<kDtype>(x, blk - 3 * stride, nb);
     if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModePlain) {
       encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
       if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
@@ -669,6 +772,97 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
     } else {
       encode_block<kDtype, kMode>(a, blk, g, est_scale, g6, mask, codes, scales, record16, scales_in);
       if (two) encode_block<kDtype, kMode>(b, blk2, g, est_scale, g6, mask, codes, scales, record16, scales_in);
+    }
+  }
+}
+
+// Plain encoding of one bf16 tensor fed through shared memory: warp 0 streams the tensor in 16 KB
+// chunks with cp.async.bulk into a ring of kEncRingStages stages (bulk copies keep far more bytes
+// in flight than per-thread loads), and warps 1-8 encode the chunk's 512 blocks from shared memory,
+// two per thread, with the same tables and block encoder as quantize_kernel (so the same bytes).
+// Chunks are visited from the end of the tensor to its start, like quantize_kernel's blocks.
+constexpr int kEncRingWarps = 8;
+constexpr int kEncRingThreads = 32 * (kEncRingWarps + 1);
+constexpr int kEncRingStages = 4;
+constexpr int kEncRingSmem = kAmaxChunk * kEncRingStages;
+constexpr int kChunkBlocks = kAmaxChunk / 32;  // bf16 blocks of 16 elements per chunk
+
+__global__ void __launch_bounds__(kEncRingThreads, 3)
+    encode_ring_kernel(const uint8_t* __restrict__ x, int64_t nblocks, const uint32_t* __restrict__ amax_bits,
+                       const float* __restrict__ amax_in, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                       float* __restrict__ g_out, uint32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kEncRingStages], empty[kEncRingStages];
+  __shared__ EncodeTables tab;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float amax = amax_in ? *amax_in : __uint_as_float(*amax_bits);
+  const float g = __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  const bool tiny = g < 0x1p-60f;  // as in quantize_kernel
+  const float est_scale = tiny ? 0x1p64f : 1.0f;
+  const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kEncRingStages; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&empty[i]), kEncRingWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // the encode warps build the tables (named barrier 1) while warp 0 starts the stream
+  if (warp > 0) {
+    build_encode_tables(tab, g, true, threadIdx.x - 32, 32 * kEncRingWarps);
+    named_barrier_sync(1, 32 * kEncRingWarps);
+  }
+  const int64_t bytes = nblocks * 32;
+  const int64_t nchunks = (bytes + kAmaxChunk - 1) / kAmaxChunk;
+  const int64_t mine = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t j = 0; j < mine; ++j) {
+        const int s = static_cast<int>(j % kEncRingStages);
+        if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>((j / kEncRingStages) & 1) ^ 1u, status,
+                       kStatusTimeoutProducer))
+          break;
+        const int64_t c = nchunks - 1 - (blockIdx.x + j * gridDim.x);
+        const int64_t off = c * kAmaxChunk;
+        const uint32_t size = static_cast<uint32_t>(min(static_cast<int64_t>(kAmaxChunk), bytes - off));
+        mbar_arrive_expect_tx(smem_addr(&full[s]), size);
+        bulk_load(smem_addr(ring + s * kAmaxChunk), x + off, size, smem_addr(&full[s]));
+        issued = j + 1;
+      }
+      // every issued copy has landed before the CTA exits
+      for (int64_t j = max(int64_t(0), issued - kEncRingStages); j < issued; ++j)
+        mbar_wait(smem_addr(&full[j % kEncRingStages]), static_cast<uint32_t>((j / kEncRingStages) & 1), status,
+                  kStatusTimeoutDrain);
+    }
+  } else {
+    const int t = threadIdx.x - 32;
+    for (int64_t j = 0; j < mine; ++j) {
+      const int s = static_cast<int>(j % kEncRingStages);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((j / kEncRingStages) & 1),
+                                             status, kStatusTimeoutDequant)))
+        break;
+      const int64_t c = nchunks - 1 - (blockIdx.x + j * gridDim.x);
+      const int nblk = static_cast<int>(min(static_cast<int64_t>(kChunkBlocks), nblocks - c * kChunkBlocks));
+      const uint4* v = reinterpret_cast<const uint4*>(ring + s * kAmaxChunk);
+      uint4 a[2], b[2];
+      const bool two = t + 32 * kEncRingWarps < nblk;
+      if (t < nblk) {
+        a[0] = v[2 * t];
+        a[1] = v[2 * t + 1];
+      }
+      if (two) {
+        b[0] = v[2 * (t + 32 * kEncRingWarps)];
+        b[1] = v[2 * (t + 32 * kEncRingWarps) + 1];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));  // this warp has read the stage
+      if (t < nblk) encode_block_bf16(a, c * kChunkBlocks + t, g, inv_g6, est_scale, tab, codes, scales);
+      if (two) encode_block_bf16(b, c * kChunkBlocks + t + 32 * kEncRingWarps, g, inv_g6, est_scale, tab, codes, scales);
     }
   }
 }
@@ -702,7 +896,6 @@ __global__ void __launch_bounds__(kFusedThreads, 2)
   const bool tiny = g < 0x1p-60f;
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
-  build_encode_tables(tab, g);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kFusedStages; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
@@ -711,6 +904,11 @@ __global__ void __launch_bounds__(kFusedThreads, 2)
     fence_barrier_init();
   }
   __syncthreads();
+  // the encode warps build the tables (named barrier 1) while warps 0-2 start the amax stream
+  if (warp >= 3) {
+    build_encode_tables(tab, g, true, threadIdx.x - 96, 32 * kFusedEncodeWarps);
+    named_barrier_sync(1, 32 * kFusedEncodeWarps);
+  }
   const int64_t nchunks = (bytes_n + kAmaxChunk - 1) / kAmaxChunk;
   const int64_t mine = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   if (warp == 0) {
@@ -927,7 +1125,7 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
   const bool tiny = g < 0x1p-60f;
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
-  build_encode_tables(tab, g);
+  build_encode_tables(tab, g, true, threadIdx.x, blockDim.x);
   __syncthreads();
   const int nb_row = static_cast<int>(H / 16);
   const int total = nrows * nb_row;
@@ -1060,10 +1258,38 @@ int quantize_ctas_per_sm(int device) {
 
 namespace {
 
+// CTAs of encode_ring_kernel resident per SM (once per device; sets its shared-memory size).
+int encode_ring_ctas_per_sm(int device) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(device);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaFuncSetAttribute(encode_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncRingSmem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_ring_kernel, kEncRingThreads, kEncRingSmem) !=
+          cudaSuccess ||
+      n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[device] = n;
+  return n;
+}
+
 template <int kDtype, int kMode>
 cudaError_t launch_encode(int64_t nblocks, const DeviceInfo& dev, cudaStream_t st, const void* x,
                           const uint32_t* amax_bits, const float* amax_in, const uint32_t* mask, uint8_t* codes,
                           uint8_t* scales, float* g, uint16_t* record16, const uint8_t* scales_in, const float* g_in) {
+  if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModePlain) {
+    const int per_sm = encode_ring_ctas_per_sm(dev.device);
+    if (per_sm == 0) return cudaErrorLaunchFailure;
+    const int64_t nchunks = (nblocks * 32 + kAmaxChunk - 1) / kAmaxChunk;
+    const int grid = static_cast<int>(std::min<int64_t>(nchunks, static_cast<int64_t>(dev.sm_count) * per_sm));
+    return launch_pdl(encode_ring_kernel, dim3(grid), dim3(kEncRingThreads), kEncRingSmem, st,
+                      static_cast<const uint8_t*>(x), nblocks, amax_bits, amax_in, codes, scales, g, dev.status);
+  }
   // one wave: as many CTAs as can be resident at once (each loops over its share of the blocks)
   const int threads = 256;
   const int64_t want = (nblocks + threads - 1) / threads;
