@@ -833,6 +833,21 @@ def run_suite(args):
                                        "bytes: 2 B in, 0.125 B record + 0.0625 B scales in, 0.5 B codes out"})
         del W, mask, c, sc, g, rec, c2
         torch.cuda.empty_cache()
+    # ---- plain encode of the 7B gate weight with its amax given (the single encode pass alone)
+    if want("quantize_amax_given"):
+        n, k = 18944, 3584
+        W = weight(n, k)
+        am = W.float().abs().amax().reshape(1)
+        c = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(n, k // 16, dtype=torch.uint8, device=dev)
+        g = torch.empty(1, dtype=torch.float32, device=dev)
+        wsq = torch.empty(nv.workspace_bytes(nv.OP_QUANTIZE, 0, 0, 0), dtype=torch.uint8, device=dev)
+        us_a = timed(lambda: nv.nvfp4_quantize(W, amax_in=am, codes=c, scales=sc, g=g, workspace=wsq), 10)
+        emit("quantize_amax_given_7b_gate", us_a, 0, n * k * (2 + 0.5625), "hbm",
+             {"shape": [n, k], "note": "one encode pass, amax given (nvfp4_quantize amax_in); bytes: 2 B in, "
+                                       "0.5625 B out per element"})
+        del W, c, sc, g, wsq
+        torch.cuda.empty_cache()
     # ---- RMSNorm-AQN fused with the NVFP4 quantization of its output (the W4A4 activation operand)
     if want("rmsnorm_quantize"):
         m, h = 4096, 3584

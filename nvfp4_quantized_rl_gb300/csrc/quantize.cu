@@ -1125,7 +1125,9 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
   const bool tiny = g < 0x1p-60f;
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
-  build_encode_tables(tab, g, true, threadIdx.x, blockDim.x);
+  // no reciprocals here: built after the grid barrier they cost more than the conversion saves at
+  // the sizes that fit on chip
+  build_encode_tables(tab, g, false, threadIdx.x, blockDim.x);
   __syncthreads();
   const int nb_row = static_cast<int>(H / 16);
   const int total = nrows * nb_row;

@@ -111,6 +111,41 @@ def test_quantize_midpoints_with_general_scales(nv):
     assert_quant_equal(gpu_quantize(nv, xb), oracle.quantize(xb), "midpoint ties, general scales")
 
 
+@pytest.mark.parametrize("M", [137, 150, 161, 231])
+def test_quantize_bf16_next_to_midpoints(nv, M):
+    """bf16 values next to every midpoint m E4M3(s) g (the three bf16 values nearest to it) in blocks of
+    every normal scale byte s, with g = amax / 2688 for amax mantissas M: 231 = 11 * 21 makes g exact
+    (m E4M3(s) g can then be a bf16 value: exact ties), 150 and 161 carry the factors 3 and 7 of 2688 / 2^7
+    that put bf16 values within an fp32 rounding of m E4M3(s) g, 137 neither. The bf16 encoding rounds
+    x times a reciprocal of E4M3(s) g with the hardware conversion: these are the values it must still
+    decide exactly (codes, scales and g bit-exact against the oracle)."""
+    rng = np.random.default_rng(M)
+    amax = np.float32(M * 2.0 ** -4)
+    g = float(np.float32(amax / np.float32(2688.0)))
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    blocks = []
+    for b in range(0x08, 0x78):  # 6 E4M3(s) g stays below amax
+        d = float(oracle.e4m3_value(b)) * g
+        near = []
+        for m in mids:
+            c = int(synth.bf16_bits(np.array([m * d], np.float32))[0])
+            near += [c - 1, c, c + 1]
+        top = int(synth.bf16_bits(np.array([6.0 * d], np.float32))[0])
+        vals = np.array(near + [top, top], np.uint16)  # 23 values: the block maximum in both blocks
+        a, bb = np.concatenate([[top], vals[:15]]), np.concatenate([[top], vals[15:22], vals[:8]])
+        for blk in (a, bb):
+            blk = blk.astype(np.uint16) | (rng.integers(0, 2, 16) << 15).astype(np.uint16)
+            blocks.append(rng.permutation(blk))
+    amax_block = np.zeros(16, np.uint16)
+    amax_block[3] = synth.bf16_bits(np.array([amax], np.float32))[0]
+    blocks.append(amax_block)
+    x = np.stack(blocks).reshape(-1, 64) if len(blocks) % 4 == 0 else np.stack(blocks + [np.zeros(16, np.uint16)] *
+                                                                              (4 - len(blocks) % 4)).reshape(-1, 64)
+    want = oracle.quantize(x)
+    assert float(want[2]) == g
+    assert_quant_equal(gpu_quantize(nv, x), want, f"bf16 next to midpoints, amax mantissa {M}")
+
+
 def test_quantize_zero_tiny_and_huge(nv):
     z = np.zeros((8, 64), np.float32)
     z[2, 5] = -0.0
