@@ -22,11 +22,10 @@
 //   warp 2      activation producer (TMA): per 128-K sub-stage two boxes of 64 bf16 x tokens
 //               (128-byte swizzle, read straight from x) into a separate, shallower ring;
 //               plus the LoRA tiles.
-//   warps 3-18  dequantize: thread = one weight row and a quarter of the stage's K; 4-bit codes
-//               are expanded to bf16 with integer ops (a nibble swap, sign and magnitude bits
-//               moved into a bf16 bit pattern, one bf16x2 FMA by E4M3(s) * 2^94), written to
-//               TMEM with tcgen05.st; then the epilogue: TMEM -> registers, g and s applied,
-//               bf16 stores.
+//   warps 3-18  dequantize: thread = one weight row and a quarter of the stage's K; each code
+//               byte is converted to f16x2 by the hardware, moved to a bf16 pattern (one shift
+//               and mask) and scaled by one bf16x2 FMA by E4M3(s) * 2^80, written to TMEM with
+//               tcgen05.st; then the epilogue: TMEM -> registers, g and s applied, bf16 stores.
 // The weight ring is released by the dequant warps and the activation ring by the MMAs, so
 // the HBM weight stream runs ahead independently of the L2-resident activation tiles. Each
 // output tile starts its K range at a different stage (the CTAs then read different
@@ -35,12 +34,11 @@
 // fp32 partial tile in its own shared memory, and after a cluster barrier each CTA sums one
 // slice of the tokens over all partials (in split order) through distributed shared memory.
 //
-// The bf16 pattern of a code magnitude m = (e1 e0 m0) placed in bits 8..6 is the value
-// grid(m) * 2^-126 (a subnormal when e = 0), so multiplying by E4M3(s) * 2^94 gives
-// grid(m) * E4M3(s) * 2^-32 exactly (at most 6 significant bits); the epilogue multiplies
-// the fp32 accumulator by 2^32 and then by g. Two codes 16 bits apart in a code word share
-// their shifts and are expanded together; one delta swap of nibbles beforehand makes those
-// two codes K-adjacent, the pair (2c, 2c+1) of TMEM column c.
+// Dequant: each code byte becomes an f16x2 by the hardware conversion (cvt.rn.f16x2.e2m1x2); the
+// f16 pattern shifted right by 3 (sign kept) is the bf16 pattern of the value times 2^-112, and
+// one bf16x2 FMA by E4M3(s) * 2^80 gives grid(m) * E4M3(s) * 2^-32 exactly (at most 6 significant
+// bits); the epilogue multiplies the fp32 accumulator by 2^32 and then by g. Byte c of a code
+// word holds the K pair (2c, 2c+1) of TMEM column c.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -114,28 +112,38 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Four TMEM columns from one word of 8 codes (K order e0..e7): column c = (e_2c, e_2c+1),
-// each a bf16 of grid(m) * E4M3(s) * 2^-32 with the code's sign (scale2 = E4M3(s) * 2^94).
-__device__ __forceinline__ void expand_word(uint32_t w, uint32_t scale2, uint32_t* out) {
-  // swap nibbles 1<->4 and 3<->6 (one delta swap): nibbles p and p+4 of v, 16 bits apart,
-  // are then the K-adjacent pairs (e0, e1), (e4, e5), (e2, e3), (e6, e7) for p = 0..3
-  const uint32_t t = (w ^ (w >> 12)) & 0x0000F0F0u;
-  const uint32_t v = w ^ t ^ (t << 12);
-  const uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u;
-  out[0] = bf16x2_mul(((v << 6) & kMag) | ((v << 12) & kSign), scale2);  // (e0, e1)
-  out[2] = bf16x2_mul(((v << 2) & kMag) | ((v << 8) & kSign), scale2);   // (e4, e5)
-  out[1] = bf16x2_mul(((v >> 2) & kMag) | ((v << 4) & kSign), scale2);   // (e2, e3)
-  out[3] = bf16x2_mul(((v >> 6) & kMag) | (v & kSign), scale2);          // (e6, e7)
+// Four code bytes (two E2M1 elements each, low nibble first) -> four f16x2 (low half = low nibble).
+__device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t (&d)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(w));
 }
 
-// bf16x2 of E4M3(s) * 2^94 for a normal scale byte s (8 <= s <= 0x7E): the bf16 bits are
-// (s << 4) + (214 << 7), i.e. exponent e + 214 and mantissa m << 4; one multiply-add writes
-// both halves.
-__device__ __forceinline__ uint32_t scale_bf16x2_normal(uint32_t s) { return (s & 0x7Fu) * 0x00100010u + 0x6B006B00u; }
+// Four TMEM columns from one word of 8 codes (K order e0..e7): column c = (e_2c, e_2c+1), each a
+// bf16 of grid(m) * E4M3(s) * 2^-32 with the code's sign (scale2 = E4M3(s) * 2^80). Byte c of the
+// word is converted to f16x2 by the hardware; an E2M1 value as f16 has its mantissa in the top
+// bit, so the f16 pattern shifted right by 3 (sign kept in place) is the bf16 pattern of the same
+// value times 2^-112; the bf16x2 FMA by E4M3(s) * 2^80 is then exact (at most 6 significant bits).
+__device__ __forceinline__ void expand_word(uint32_t w, uint32_t scale2, uint32_t* out) {
+  uint32_t h[4];
+  e2m1x8_f16x2(w, h);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) out[c] = bf16x2_mul(((h[c] >> 3) & 0x0FFF0FFFu) | (h[c] & 0x80008000u), scale2);
+}
 
-// bf16x2 of E4M3(s) * 2^94 for any scale byte (exact: at most 4 significant bits).
+// bf16x2 of E4M3(s) * 2^80 for a normal scale byte s (8 <= s <= 0x7E): the bf16 bits are
+// (s << 4) + (200 << 7), i.e. exponent e + 200 and mantissa m << 4; one multiply-add writes
+// both halves.
+__device__ __forceinline__ uint32_t scale_bf16x2_normal(uint32_t s) { return (s & 0x7Fu) * 0x00100010u + 0x64006400u; }
+
+// bf16x2 of E4M3(s) * 2^80 for any scale byte (exact: at most 4 significant bits).
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t s) {
-  const uint32_t b = __float_as_uint(e4m3_decode_pos(s & 0x7Fu) * 0x1p94f) >> 16;
+  const uint32_t b = __float_as_uint(e4m3_decode_pos(s & 0x7Fu) * 0x1p80f) >> 16;
   return b | (b << 16);
 }
 
