@@ -30,9 +30,12 @@
 // the HBM weight stream runs ahead independently of the L2-resident activation tiles. Each
 // output tile starts its K range at a different stage (the CTAs then read different
 // activation tiles at any one time).
-// When K is split across CTAs, the CTAs of one output tile form a cluster: each leaves its
-// fp32 partial tile in its own shared memory, and after a cluster barrier each CTA sums one
-// slice of the tokens over all partials (in split order) through distributed shared memory.
+// When K is split across CTAs, the CTAs of one output tile form a cluster; each CTA owns a slice
+// of the tile's tokens. After a cluster barrier every CTA pushes its fp32 partial of each token
+// into the owner's shared memory (remote stores into the free activation ring); after a second
+// barrier each owner sums its slice over the partials in split order and writes it.
+// The thread that initializes the barriers also requests the first ring stages, before the
+// block's set-up (TMEM allocation, the block barrier) completes.
 //
 // Dequant: each code byte becomes an f16x2 by the hardware conversion (cvt.rn.f16x2.e2m1x2); the
 // f16 pattern shifted right by 3 (sign kept) is the bf16 pattern of the value times 2^-112, and
@@ -230,6 +233,8 @@ __global__ void __maxnreg__(88)
   constexpr int kChunks = 8 / kWarpsPerQuarter;      // 16-byte code chunks per thread and stage
   constexpr uint32_t kDcol = 0, kLcol = MBOX, kAcol0 = 2 * MBOX;
   constexpr int kXBytes = x_stage_bytes(MBOX);
+  constexpr int kEpiTok = MBOX / kWarpsPerQuarter;  // tokens per epilogue warp (multiple of 16)
+  static_assert((MBOX + kMaxSplits - 1) * kRows * 4 <= R * kXBytes, "split-K partials fit the activation ring");
 
   // layout: activation ring (reused as the fp32 partial tile after the K loop) | weight ring |
   //         lora A tile | lora U tile | barriers
@@ -250,7 +255,6 @@ __global__ void __maxnreg__(88)
   uint64_t* dfull = consumed + R;
   uint64_t* lfull = dfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lfull + 1);
-  float* part = reinterpret_cast<float*>(xring);  // [MBOX][kRows] fp32 partial tile (split K)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, split = blockIdx.y, tile_m = blockIdx.z;
@@ -273,25 +277,59 @@ __global__ void __maxnreg__(88)
     mbar_init(smem_addr(lfull), 1);
     fence_barrier_init();
   }
+  // Each output tile starts its K range at a different stage, so that the CTAs do not all read
+  // the same activation tile from L2 at the same time. Producers and consumers all walk the
+  // stages in this order.
+  auto kstage = [&](int j) { return st0 + (j + tile_n) % nst; };
+  // The first weight and activation stages (as many as the rings hold) are requested by the
+  // thread that initialized their barriers, before TMEM is allocated and the block meets; the
+  // producers continue from there. (x and the weights are complete when this kernel starts: it
+  // is launched after, or as the programmatic dependent of a kernel that waited for, their
+  // producers.)
+  const int w_pre = min(SW, nst), x_pre = min(R, nst);
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < w_pre; ++j) {
+      uint8_t* st = wring + j * kWStageBytes;
+      const uint32_t bar = smem_addr(&wfull[j]);
+      mbar_arrive_expect_tx(bar, kWStageBytes);
+      tma_load_2d(smem_addr(st), &map_codes, kstage(j) * (kKStage / 2), n0, bar);
+      tma_load_2d(smem_addr(st + kCodeBytes), &map_scales, kstage(j) * (kKStage / 16), n0, bar);
+    }
+    for (int j = 0; j < x_pre; ++j) {
+      uint8_t* st = xring + j * kXBytes;
+      const uint32_t bar = smem_addr(&ready[j]);
+      mbar_arrive_expect_tx(bar, kXBytes);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        tma_load_2d(smem_addr(st + q * MBOX * 128), &map_x, kstage(j) * kKStage + q * 64, m0, bar);
+    }
+  }
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Each output tile starts its K range at a different stage, so that the CTAs do not all read
-  // the same activation tile from L2 at the same time. Producers and consumers all walk the
-  // stages in this order.
-  auto kstage = [&](int j) { return st0 + (j + tile_n) % nst; };
+  // Sixteen tokens of this thread's weight row (TMEM lane) from the accumulators, starting at
+  // token col: the base product times 2^32 g, plus s times the LoRA accumulator.
+  auto epilogue16 = [&](uint32_t tlane, int col, bool lora, float g, float s_lora, float(&v)[16]) {
+    uint32_t d[16], l[16];
+    tmem_ld16(tlane + kDcol + col, d);
+    if (lora) tmem_ld16(tlane + kLcol + col, l);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[i] = (__uint_as_float(d[i]) * 0x1p32f) * g;
+      if (lora) v[i] = fmaf(s_lora, __uint_as_float(l[i]), v[i]);
+    }
+  };
 
   bool ok = true;
   if (warp == 0) {
     // ------------------------------------------------------------------ weight producer
     if (lane == 0) {
-      prefetch_tensormap(&map_codes);
-      prefetch_tensormap(&map_scales);
-      int issued = 0;
-      for (int j = 0; j < nst && ok; ++j) {
+      int issued = w_pre;
+      for (int j = w_pre; j < nst && ok; ++j) {
         const int s = j % SW;
         if (!mbar_wait(smem_addr(&wempty[s]), ((j / SW) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
           ok = false;
@@ -312,7 +350,6 @@ __global__ void __maxnreg__(88)
   } else if (warp == 2) {
     // ------------------------------------------------------------------ activation + LoRA producer
     if (lane == 0) {
-      prefetch_tensormap(&map_x);
       const int nbox = do_lora ? 2 * lora_padded_rank(p.r) / p.lora_box_bytes : 0;
       const int box_el = p.lora_box_bytes / 2;
       if (do_lora) {
@@ -323,8 +360,8 @@ __global__ void __maxnreg__(88)
         for (int b = 0; b < nbox; ++b)
           tma_load_2d(smem_addr(lora_a + b * kRows * p.lora_box_bytes), &map_blora, b * box_el, n0, smem_addr(lfull));
       }
-      int issued = 0;
-      for (int j = 0; j < nst && ok; ++j) {
+      int issued = x_pre;
+      for (int j = x_pre; j < nst && ok; ++j) {
         const int s = j % R;
         if (!mbar_wait(smem_addr(&consumed[s]), ((j / R) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
           ok = false;
@@ -351,25 +388,29 @@ __global__ void __maxnreg__(88)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kRows, MBOX);
-      for (int j = 0; j < nst && ok; ++j) {
-        const int a = j % R;
-        if (!mbar_wait(smem_addr(&ready[a]), (j / R) & 1, p.status, kStatusTimeoutMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    // The whole warp walks the stages and waits; one elected lane issues each stage's MMAs
+    // and commit (the same lane every time).
+    const uint32_t idesc = idesc_bf16_f32(kRows, MBOX);
+    for (int j = 0; j < nst && ok; ++j) {
+      const int a = j % R;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&ready[a]), (j / R) & 1, p.status, kStatusTimeoutMma));
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
         mma_stage16<MBOX>(tmem + kDcol, tmem + kAcol0 + a * 128, smem_desc(smem_addr(xring + a * kXBytes), 16, 1024, 2),
                           idesc, j ? 1u : 0u);
         mma_commit(smem_addr(&consumed[a]));
       }
-      if (ok && do_lora) {
-        if (mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutMma)) {
-          tc_fence_after();
-          const uint32_t sw = swizzle_mode_for(p.lora_box_bytes);
-          const uint32_t sbo = 8 * p.lora_box_bytes;
-          const uint32_t la = smem_addr(lora_a), lu = smem_addr(lora_u);
+      __syncwarp();
+    }
+    if (ok && do_lora) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutMma));
+      if (ok) {
+        tc_fence_after();
+        const uint32_t sw = swizzle_mode_for(p.lora_box_bytes);
+        const uint32_t sbo = 8 * p.lora_box_bytes;
+        const uint32_t la = smem_addr(lora_a), lu = smem_addr(lora_u);
+        if (elect_one()) {
           for (int kk = 0; kk < p.r / 16; ++kk) {
             const int off = kk * 32;
             const int box = off / p.lora_box_bytes, in = off % p.lora_box_bytes;
@@ -377,12 +418,12 @@ __global__ void __maxnreg__(88)
             const uint64_t bd = smem_desc(lu + box * MBOX * p.lora_box_bytes + in, 16, sbo, sw);
             mma_f16_ss(tmem + kLcol, ad, bd, idesc, kk ? 1u : 0u);
           }
-        } else {
-          ok = false;
         }
+        __syncwarp();
       }
-      mma_commit(smem_addr(dfull));  // also the completion point of every MMA issued above
     }
+    if (elect_one()) mma_commit(smem_addr(dfull));  // also the completion point of every MMA issued above
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
     const int dw = warp - kFirstDeqWarp;  // 0..DW-1
@@ -420,63 +461,70 @@ __global__ void __maxnreg__(88)
     // ---------------------------------------------------------------- epilogue
     ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait(smem_addr(dfull), 0, p.status, kStatusTimeoutEpilogue));
     tc_fence_after();
-    if (ok) {
+    if (ok && p.splits == 1) {
       const float g = *p.w_g;
       const int64_t n = n0 + row;
-      constexpr int kTok = MBOX / kWarpsPerQuarter;  // tokens per warp (multiple of 16)
-      const int t0 = part_k * kTok;
+      const int t0 = part_k * kEpiTok;
 #pragma unroll
-      for (int c = 0; c < kTok; c += 16) {
-        uint32_t d[16], l[16];
-        tmem_ld16(tmem + lane_base + kDcol + t0 + c, d);
-        if (do_lora) tmem_ld16(tmem + lane_base + kLcol + t0 + c, l);
-        tmem_ld_wait();
+      for (int c = 0; c < kEpiTok; c += 16) {
+        float v[16];
+        epilogue16(tmem + lane_base, t0 + c, do_lora, g, p.s, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float v = (__uint_as_float(d[i]) * 0x1p32f) * g;
-          if (do_lora) v = fmaf(p.s, __uint_as_float(l[i]), v);
-          if (p.splits > 1) {
-            part[(t0 + c + i) * kRows + row] = v;  // every token of the tile, rows in lanes
-          } else {
-            const int64_t m = m0 + t0 + c + i;
-            if (m < p.M) p.y[m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(v));
-          }
+          const int64_t m = m0 + t0 + c + i;
+          if (m < p.M) p.y[m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(v[i]));
         }
       }
     }
   }
   if (p.splits > 1) {
     // ---------------------------------------------------------------- split-K reduction
-    // All threads of the cluster meet twice: the partial tiles are complete before any CTA
-    // reads them, and no CTA leaves (its shared memory) while a peer may still read it.
+    // CTA q of the cluster owns the tokens [q slice, (q + 1) slice) of the tile. After a cluster
+    // barrier (every CTA has finished its K loop, so every activation ring is free), each CTA
+    // pushes its fp32 partial of every token to the owner's ring area (red[q][token][row], remote
+    // stores); after a second barrier each owner sums its tokens over the splits in split order
+    // from its own shared memory and writes them. No CTA reads another's memory, so none waits
+    // for its peers before leaving.
+    const int C = p.splits;
+    const int q = static_cast<int>(cluster_ctarank());
+    const int slice = (MBOX + C - 1) / C;
+    float* red = reinterpret_cast<float*>(xring);  // [C][slice][kRows]
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= kFirstDeqWarp && ok) {
+      tc_fence_after();
+      const int quarter = warp & 3, row = quarter * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      const float g = *p.w_g;
+      const int t0 = ((warp - kFirstDeqWarp) >> 2) * kEpiTok;
+#pragma unroll
+      for (int c = 0; c < kEpiTok; c += 16) {
+        float v[16];
+        epilogue16(tmem + lane_base, t0 + c, do_lora, g, p.s, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = t0 + c + i;
+          const int owner = t / slice;
+          const uint32_t local = smem_addr(red + (q * slice + (t - owner * slice)) * kRows + row);
+          dsmem_st_f32(dsmem_map(local, static_cast<uint32_t>(owner)), v[i]);
+        }
+      }
+    }
     __syncwarp();
     cluster_sync_all();
     if (warp >= kFirstDeqWarp) {
-      const int C = p.splits;
-      const int q = static_cast<int>(cluster_ctarank());
-      const int tb = q * MBOX / C, te = (q + 1) * MBOX / C;  // this CTA's slice of the tokens
-      constexpr int kPerTok = kRows / 8;                    // 8 rows (two float4) per item
+      const int tb = q * slice, te = min(MBOX, tb + slice);
+      constexpr int kPerTok = kRows / 8;  // 8 rows (two float4) per item
       for (int idx = (warp - kFirstDeqWarp) * 32 + lane; idx < (te - tb) * kPerTok; idx += DW * 32) {
-        const int tok = tb + idx / kPerTok, r8 = (idx % kPerTok) * 8;
-        const int64_t m = m0 + tok;
+        const int lt = idx / kPerTok, r8 = (idx % kPerTok) * 8;
+        const int64_t m = m0 + tb + lt;
         if (m >= p.M) continue;
-        const uint32_t local = smem_addr(part + tok * kRows + r8);
-        float4 va[kMaxSplits], vb[kMaxSplits];
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplits; ++sp) {
-          if (sp < C) {
-            const uint32_t ra = dsmem_map(local, static_cast<uint32_t>(sp));
-            va[sp] = dsmem_ld_v4(ra);
-            vb[sp] = dsmem_ld_v4(ra + 16);
-          }
-        }
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplits; ++sp) {
-          if (sp < C) {
-            acc[0] += va[sp].x; acc[1] += va[sp].y; acc[2] += va[sp].z; acc[3] += va[sp].w;
-            acc[4] += vb[sp].x; acc[5] += vb[sp].y; acc[6] += vb[sp].z; acc[7] += vb[sp].w;
-          }
+        for (int sp = 0; sp < C; ++sp) {
+          const float4* src = reinterpret_cast<const float4*>(red + (sp * slice + lt) * kRows + r8);
+          const float4 va = src[0], vb = src[1];
+          acc[0] += va.x; acc[1] += va.y; acc[2] += va.z; acc[3] += va.w;
+          acc[4] += vb.x; acc[5] += vb.y; acc[6] += vb.z; acc[7] += vb.w;
         }
         uint32_t o[4];
 #pragma unroll
@@ -484,8 +532,6 @@ __global__ void __maxnreg__(88)
         *reinterpret_cast<uint4*>(p.y + m * p.N + n0 + r8) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
-    __syncwarp();
-    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();

@@ -403,8 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_addr(&ffull[j % kSfRing]), (j / kSfRing) & 1, p.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer (one thread; a pair's leader)
-    if (lane == 0 && rank == 0) {
+    // ---------------------------------------------------------------- MMA issuer (a pair's leader)
+    // The whole warp walks the tiles and stages and waits; one elected lane issues the MMAs and
+    // commits (the same lane every time).
+    if (rank == 0) {
       const uint32_t idesc = idesc_nvf4_f32(kTile * kPeers, kWN);
       const uint32_t idesc_l = idesc_bf16_f32(kTile * kPeers, kWN);
       // ring slot c's operand descriptors add c * stage bytes to the start address field; a K step
@@ -415,48 +417,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c = 0, li = 0, it = 0;
       for (int t = unit; t < ntiles && ok; t += units, ++li) {
         // the previous tile's epilogue has read D (in both CTAs of a pair)
-        if (!mbar_wait(smem_addr(dfree), (li & 1) ^ 1, p.status, kStatusTimeoutMma)) {
-          ok = false;
-          break;
-        }
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(dfree), (li & 1) ^ 1, p.status, kStatusTimeoutMma));
+        if (!ok) break;
         tc_fence_after();
         const TileInfo ti = tile_of<kPair>(p, t, 0);
         // alpha = 0 with a LoRA branch: D = s U B^T alone (the FP4 product would be scaled by 0)
         const bool fp4 = !(nl && gx * p.w_g[ti.e] == 0.f);
         for (int k = 0; k < ns; ++k) {
           const int j = it % kSlots;
-          if (!mbar_wait(smem_addr(&sfready[j]), (it / kSlots) & 1, p.status, kStatusTimeoutMma)) {
-            ok = false;
-            break;
-          }
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sfready[j]), (it / kSlots) & 1, p.status, kStatusTimeoutMma));
+          if (!ok) break;
           tc_fence_after();
           const uint64_t soff = static_cast<uint64_t>(c * (R::kStageBytes >> 4));
           const uint32_t sf = tmem + kSlot0 + kSlotCols * j;
-          if constexpr (kPair) {
-            if (k < nl) {
+          if (elect_one()) {
+            if constexpr (kPair) {
+              if (k < nl) {
 #pragma unroll
-              for (int kk = 0; kk < kLoraK / 16; ++kk)
-                mma_f16_pair(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
-            } else if (fp4) {
-              mma_stage_nvf4_pair(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
-            }
-            mma_commit_pair(smem_addr(&mdone[it % kDone]));
-          } else {
-            if (k < nl) {
+                for (int kk = 0; kk < kLoraK / 16; ++kk)
+                  mma_f16_pair(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
+              } else if (fp4) {
+                mma_stage_nvf4_pair(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+              }
+              mma_commit_pair(smem_addr(&mdone[it % kDone]));
+            } else {
+              if (k < nl) {
 #pragma unroll
-              for (int kk = 0; kk < kLoraK / 16; ++kk)
-                mma_f16_ss(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
-            } else if (fp4) {
-              mma_stage_nvf4(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+                for (int kk = 0; kk < kLoraK / 16; ++kk)
+                  mma_f16_ss(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
+              } else if (fp4) {
+                mma_stage_nvf4(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+              }
+              mma_commit(smem_addr(&mdone[it % kDone]));
             }
-            mma_commit(smem_addr(&mdone[it % kDone]));
           }
+          __syncwarp();
           ++it;
           if (++c == S) c = 0;
         }
         if (!ok) break;
-        if constexpr (kPair) mma_commit_pair(smem_addr(dfull));
-        else mma_commit(smem_addr(dfull));
+        if (elect_one()) {
+          if constexpr (kPair) mma_commit_pair(smem_addr(dfull));
+          else mma_commit(smem_addr(dfull));
+        }
+        __syncwarp();
       }
     }
     __syncwarp();

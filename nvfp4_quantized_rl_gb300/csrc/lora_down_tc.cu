@@ -115,23 +115,26 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
     // do not leave with copies in flight
     for (int i = max(0, issued - kStages); i < issued; ++i)
       mbar_wait(smem_addr(&full[i % kStages]), (i / kStages) & 1, p.status, kStatusTimeoutDrain);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
+    // The whole warp walks the chunks and waits; one elected lane issues the MMAs and commits.
     const uint32_t idesc = idesc_bf16_f32(kRows, static_cast<uint32_t>(p.r));
     for (int i = 0; i < n && ok; ++i) {
       const int s = i % kStages;
-      if (!mbar_wait(smem_addr(&full[s]), (i / kStages) & 1, p.status, kStatusTimeoutMma)) {
-        ok = false;
-        break;
-      }
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (i / kStages) & 1, p.status, kStatusTimeoutMma));
+      if (!ok) break;
       tc_fence_after();
       const uint64_t xd = smem_desc(smem_addr(smem + s * stage_bytes), 16, 1024, 2);
       const uint64_t ad = smem_desc(smem_addr(smem + s * stage_bytes + kXBytes), 16, 1024, 2);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < kChunk / 16; ++kk) mma_f16_ss(tmem, xd + 2 * kk, ad + 2 * kk, idesc, (i | kk) ? 1u : 0u);
-      mma_commit(smem_addr(&empty[s]));
+        for (int kk = 0; kk < kChunk / 16; ++kk) mma_f16_ss(tmem, xd + 2 * kk, ad + 2 * kk, idesc, (i | kk) ? 1u : 0u);
+        mma_commit(smem_addr(&empty[s]));
+      }
+      __syncwarp();
     }
-    mma_commit(smem_addr(done));  // every MMA above has completed (also when there were none)
+    if (elect_one()) mma_commit(smem_addr(done));  // every MMA above has completed (also when there were none)
+    __syncwarp();
   } else if (p.amax && (warp == 2 || warp == 3)) {
     // ---------------------------------------------------------------- max |x| of the landed tiles
     uint32_t m2 = 0;

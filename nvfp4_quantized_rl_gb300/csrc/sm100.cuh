@@ -66,6 +66,9 @@ __device__ __forceinline__ float4 dsmem_ld_v4(uint32_t cluster_addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ void dsmem_st_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
 // Every thread of every CTA of the cluster: shared-memory writes before it are visible to
 // the cluster's reads after it. Executed by whole warps (converged).
 __device__ __forceinline__ void cluster_sync_all() {
@@ -160,6 +163,21 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// True in exactly one lane of the calling warp, which must be converged: the lowest active lane,
+// so repeated calls elect the same lane. tcgen05.mma and tcgen05.commit are issued from such a
+// lane of a converged warp. The warp then keeps its operands warp-uniform; issued from a
+// single-lane branch instead, a stream of small MMAs runs at a fraction of the tensor pipe's rate
+// whenever other warps keep the schedulers busy.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // Arrives once on `bar` when every tcgen05 operation this thread issued before has completed.
