@@ -329,16 +329,17 @@ class Workload:
             names += [f"rmsnorm_{phase}"] + [f"{kind}_{n}" for n, _, _ in self.cfg["linears"]]
         return names
 
-    def step(self, nv, k, ev=None, only=None, layer_sel=None):
-        """One step at noise-schedule index k. ev: {(layer, op): (start, end)} events recorded around every
-        op; only: run just these op names (single-op mode, layer 0 unless layer_sel)."""
+    def step(self, nv, k, ev=None, only=None, layer_sel=None, grp=None):
+        """One step at noise-schedule index k. ev: {(layer, op): (start, end)} events recorded around the ops
+        it names; grp: {(layer, "linears_<phase>"): (start, end)} events around all linears of a phase;
+        only: run just these op names (single-op mode, layer 0 unless layer_sel)."""
         sigma = nv.aqn_sigma(SIGMA0, SIGMAK, k, KSCHED)
         lin = self.cfg["linears"]
         for l in (range(self.layers) if layer_sel is None else layer_sel):
             def mark(name, fn):
                 if only is not None and name not in only:
                     return
-                if ev is None:
+                if ev is None or (l, name) not in ev:
                     fn()
                     return
                 a, b = ev[(l, name)]
@@ -368,6 +369,9 @@ class Workload:
                             nv.rmsnorm_aqn(b[src], w, self.eps[k], sigma, 1e-6, out=b[h])
                 mark(f"rmsnorm_{phase}", norms)
                 kind = "w4a4" if P["w4a4"] else "w4a16"
+                span = grp.get((l, f"linears_{phase}")) if grp else None
+                if span:
+                    span[0].record()
                 for name, _, _ in lin:
                     c, s, g = Q[name]
                     A, B = lora[name]
@@ -383,6 +387,8 @@ class Workload:
                         fn = lambda: nv.nvfp4_lora_linear_w4a4(b[src], c, s, g, A, B, S_LORA, out=P["Y"][name],
                                                                workspace=P["ws"])
                     mark(f"{kind}_{name}", fn)
+                if span:
+                    span[1].record()
 
 
 def run_gpu(args):
@@ -434,6 +440,15 @@ def run_gpu(args):
         with torch.cuda.graph(ge):
             wl.step(nv, k, ev)
         ev_graphs.append((ge, ev))
+    # and with events only at the ends of each op group (the refresh, each phase's RMSNorms, each
+    # phase's linears as one span): the parts' times, free of the per-call event boundaries
+    group_names = ["weight_refresh"] + [f"rmsnorm_{p}" for p in wl.phases] + [f"linears_{p}" for p in wl.phases]
+    evg = {(l, name): (torch.cuda.Event(enable_timing=True, external=True),
+                       torch.cuda.Event(enable_timing=True, external=True)) for l in range(layers) for name in group_names}
+    gg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gg):
+        wl.step(nv, 0, ev={key: v for key, v in evg.items() if not key[1].startswith("linears_")},
+                grp={key: v for key, v in evg.items() if key[1].startswith("linears_")})
     torch.cuda.synchronize()
     for i in range(args.warmup):
         graphs[i % n_graphs].replay()
@@ -462,6 +477,13 @@ def run_gpu(args):
         torch.cuda.synchronize()
         for name in ops:
             op_samples[name].append(sum(ev[(l, name)][0].elapsed_time(ev[(l, name)][1]) for l in range(layers)))
+    group_samples = {name: [] for name in group_names}
+    for i in range(3):
+        gg.replay()
+        torch.cuda.synchronize()
+        for name in group_names:
+            group_samples[name].append(sum(evg[(l, name)][0].elapsed_time(evg[(l, name)][1]) for l in range(layers)))
+    group_ms = {name: float(np.median(v)) for name, v in group_samples.items()}
     launches = launches_per_step * args.steps
     if world > 1:
         dist.barrier()
@@ -479,7 +501,7 @@ def run_gpu(args):
         return
     units, scale = step_units(cfg, layers)
     value = job_throughput(units, world, ms_per_step, scale)
-    line = summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, launches, clocks, e2e)
+    line = summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, group_ms, launches, clocks, e2e)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     print(json.dumps(line))
@@ -487,9 +509,11 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, launches, clocks, e2e):
+def summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, group_ms, launches, clocks, e2e):
     """The bench's JSON line: the step's throughput, the per-part breakdown with each part's fraction of its
-    binding roof, and the roofline of the op that takes the most device time."""
+    binding roof, and the roofline of the op that takes the most device time. Part times come from the
+    replays with events only at the group ends (group_ms); per_linear_us from the replays with events
+    around every call (op_ms)."""
     hbm, bf16_burst, bf16_sus, src = peaks()
     fp4_sus = bf16_sus * FP4_PER_BF16
     c = layer_counts(cfg)
@@ -497,7 +521,7 @@ def summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, laun
     L = layers
     sus_note = f"{src} bf16_tflops_sustained (MEASURED_PEAKS.json): the op runs inside a long step"
     parts, groups = {}, {}
-    q_ms = op_ms["weight_refresh"]
+    q_ms = group_ms["weight_refresh"]
     parts["weight_refresh"] = {
         "us": q_ms * 1e3, "GB/s": c["refresh_bytes"] * L / q_ms / 1e6, "frac_hbm": c["refresh_bytes"] * L / q_ms / 1e6 / hbm,
         "note": "amax + NVFP4 encode of every weight of every layer, one nvfp4_quantize_batch call per layer; bytes: "
@@ -508,28 +532,30 @@ def summarize(args, cfg, layers, world, value, ms_per_step, step_ms, op_ms, laun
             continue
         M = cfg["decode_m"] if phase == "d" else cfg["prefill_m"]
         kind = "w4a16" if phase == "d" else "w4a4"
-        r_ms = op_ms[f"rmsnorm_{phase}"]
+        r_ms = group_ms[f"rmsnorm_{phase}"]
         rb = c["rms_d_bytes" if phase == "d" else "rms_p_bytes"] * L
         parts[f"rmsnorm_aqn_m{M}"] = {"us": r_ms * 1e3, "GB/s": rb / r_ms / 1e6, "frac_hbm": rb / r_ms / 1e6 / hbm}
-        l_ms = sum(op_ms[f"{kind}_{n}"] for n, _, _ in lin)
+        l_ms = group_ms[f"linears_{phase}"]
         fl, by = c[f"{kind}_flops"] * L, c[f"{kind}_bytes"] * L
         tf = fl / l_ms / 1e9
         part = {"us": l_ms * 1e3, "TFLOP/s": tf, "GB/s": by / l_ms / 1e6, "frac_hbm": by / l_ms / 1e6 / hbm,
                 "per_linear_us": {n: op_ms[f"{kind}_{n}"] * 1e3 / L for n, _, _ in lin}}
         if kind == "w4a16":
             part["frac_bf16_tensor"] = tf / bf16_sus
-            part["note"] = ("fractions against the sustained bf16 tensor peak and the HBM copy rate; per_linear_us is "
-                            "per layer (LoRA-down + w4a16_tc_kernel)")
+            part["note"] = ("fractions against the sustained bf16 tensor peak and the HBM copy rate; us: the phase's "
+                            "linears as one span; per_linear_us: per layer (LoRA-down + w4a16_tc_kernel), with events "
+                            "around every call (each call boundary then adds its own gap)")
             groups["lora_linear_w4a16"] = l_ms
         else:
             part["frac_fp4_tensor"] = tf / fp4_sus
-            part["note"] = (f"the full calls: LoRA-down and the block-scaled GEMM; q/k/v and gate/up read the NVFP4 "
+            part["note"] = (f"us: the phase's linears as one span; per_linear_us: events around every call; "
+                            f"the full calls: LoRA-down and the block-scaled GEMM; q/k/v and gate/up read the NVFP4 "
                             f"activations rmsnorm_aqn_quantize wrote (timed under rmsnorm), o and down quantize theirs "
                             f"(amax + encode) in the call; fraction of the dense FP4 peak = {FP4_PER_BF16:g} x "
                             f"sustained bf16 (the nominal 13.5 / 2.25 ratio)")
             groups["lora_linear_w4a4"] = l_ms
         parts[f"lora_linear_{kind}_m{M}"] = part
-    rms_ms = sum(op_ms[f"rmsnorm_{p}"] for p in ("d", "p") if f"rmsnorm_{p}" in op_ms)
+    rms_ms = sum(group_ms[f"rmsnorm_{p}"] for p in ("d", "p") if f"rmsnorm_{p}" in group_ms)
     groups["rmsnorm_aqn"] = rms_ms
     dom = max(groups, key=groups.get)
     n_lin = len(lin) * L
