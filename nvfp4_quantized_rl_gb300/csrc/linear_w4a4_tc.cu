@@ -53,10 +53,12 @@
 //               alpha and packed to bf16 (cvt.rn.bf16x2); D is released to the next tile's MMAs
 //               as soon as it has been read, then the rows are stored, 128-byte pieces at a time
 //               after a shuffle transpose within groups of 8 lanes
-// TMEM: the accumulator D in columns 0..255; scale slot j in 256 + 64 j: activation scales in
-// its first 16 columns (4 per K step: the MMA reads column 4t + w in lane quarter w, so each
-// quarter writes its own rows there), weight scales in the next 32 (8 per K step: column 8t + w
-// holds rows 32w .. 32w + 31, the same in every lane quarter).
+// TMEM: the accumulator D in columns 0..255; five scale slots: slot j's activation scales in
+// columns 256 + 16 j .. + 15 (4 per K step: the MMA reads column 4t + w in lane quarter w, so each
+// quarter writes its own rows there), its weight scales in 352 + 32 j .. + 31 (8 per K step:
+// column 8t + w holds rows 32w .. 32w + 31, the same in every lane quarter). A slot is rewritten
+// only after the MMAs of the stage five earlier have completed, so four stages of MMAs stay
+// queued while the scale warps refill it.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -83,11 +85,14 @@ constexpr int kSfA = kTile * kKStage / 16;        // 2 KB activation scales per 
 constexpr int kSfB = kWN * kKStage / 16;          // 4 KB weight scales per stage
 constexpr int kSfStage = kSfA + kSfB;
 constexpr int kSfRing = 4;                        // scale ring stages
-constexpr int kSlots = 4;                         // TMEM scale slots
+constexpr int kSlots = 5;                         // TMEM scale slots
 constexpr int kDone = 16;                         // commit ring, > operand stages and scale slots
 constexpr int kThreads = 28 * 32;
 constexpr int kFirstSf = 4, kFirstEpi = 12;
-constexpr uint32_t kSlot0 = 256, kSlotCols = 64;  // TMEM columns of scale slot j: kSlot0 + kSlotCols j
+// TMEM columns of scale slot j: activation scales at kSfACol + 16 j (16 columns), weight scales at
+// kSfBCol + 32 j (32 columns); five slots fill columns 256..511 with D in 0..255.
+constexpr uint32_t kSfACol = 256, kSfBCol = 352;
+static_assert(kSfACol + 16 * kSlots <= kSfBCol && kSfBCol + 32 * kSlots <= 512, "scale slots fit TMEM");
 
 struct W4a4Params {
   int64_t M, N, K;
@@ -429,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint64_t soff = static_cast<uint64_t>(c * (R::kStageBytes >> 4));
-          const uint32_t sf = tmem + kSlot0 + kSlotCols * j;
+          const uint32_t sfa = tmem + kSfACol + 16 * j, sfb = tmem + kSfBCol + 32 * j;
           if (elect_one()) {
             if constexpr (kPair) {
               if (k < nl) {
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kLoraK / 16; ++kk)
                   mma_f16_pair(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
               } else if (fp4) {
-                mma_stage_nvf4_pair(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+                mma_stage_nvf4_pair(tmem, adesc0 + soff, bdesc0 + soff, idesc, sfa, sfb, k ? 1u : 0u);
               }
               mma_commit_pair(smem_addr(&mdone[it % kDone]));
             } else {
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kLoraK / 16; ++kk)
                   mma_f16_ss(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
               } else if (fp4) {
-                mma_stage_nvf4(tmem, adesc0 + soff, bdesc0 + soff, idesc, sf, sf + 16, k ? 1u : 0u);
+                mma_stage_nvf4(tmem, adesc0 + soff, bdesc0 + soff, idesc, sfa, sfb, k ? 1u : 0u);
               }
               mma_commit(smem_addr(&mdone[it % kDone]));
             }
@@ -468,9 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- scale warps
     // Group g (warps 4-7: g = 0, 8-11: g = 1) takes the stages it with it % 2 == g; stage it uses
     // TMEM scale slot it % kSlots. FP4 stage: lane i of quarter q reads activation row 32q + i (its
-    // four K-step words) and writes them to columns 4t + w (for every w; the MMA reads 4t + q), and
-    // reads weight rows 32w + i, w = 0..7, writing column 16 + 8t + w = row 32w + i, K step t (all
-    // 256 rows, in each CTA of a pair). LoRA stage: the slices have landed. Either way the group
+    // four K-step words) and writes them to columns 4t + w of the slot's activation part (for every
+    // w; the MMA reads 4t + q), and reads weight rows 32w + i, w = 0..7, writing column 8t + w of the
+    // slot's weight part = row 32w + i, K step t (all 256 rows, in each CTA of a pair). LoRA stage: the slices have landed. Either way the group
     // then arrives on sfready (a pair's leader's), which the MMA issuer waits on alone.
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -495,10 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                p.status, kStatusTimeoutMma));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t slot = tmem + lane_base + kSlot0 + kSlotCols * j;
+        const uint32_t slot_a = tmem + lane_base + kSfACol + 16 * j, slot_b = tmem + lane_base + kSfBCol + 32 * j;
         const uint8_t* st = sfring + f * kSfStage;
         const uint4 a = reinterpret_cast<const uint4*>(st)[q * 32 + lane];
-        tmem_st16_rep4(slot, a.x, a.y, a.z, a.w);
+        tmem_st16_rep4(slot_a, a.x, a.y, a.z, a.w);
         // weight scales in two halves of 16 columns: K steps 0-1, then 2-3
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -509,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             b[w] = r.x;
             b[8 + w] = r.y;
           }
-          tmem_st16(slot + 16 + 16 * hh, b);
+          tmem_st16(slot_b + 16 * hh, b);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&fempty[f]));  // the scale tiles have been read
@@ -543,15 +548,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float out = nl && alpha == 0.f ? 1.f : alpha;
       // this thread's row (TMEM lane 32q + lane), columns 64 part .. + 63, scaled and packed: unit u
       // (16 bytes) = o[4u .. 4u + 3] = columns 8u .. 8u + 7
+      // 32 columns per load, each waited and packed: two waits instead of four
       uint32_t o[32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t d[16];
-        tmem_ld16(tmem + lane_base + part * 64 + cc * 16, d);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t d[32];
+        tmem_ld32(tmem + lane_base + part * 64 + hh * 32, d);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          o[cc * 8 + i] = pack_bf16x2(__uint_as_float(d[2 * i]) * out, __uint_as_float(d[2 * i + 1]) * out);
+        for (int i = 0; i < 16; ++i)
+          o[hh * 16 + i] = pack_bf16x2(__uint_as_float(d[2 * i]) * out, __uint_as_float(d[2 * i + 1]) * out);
       }
       // D has been read: the next tile's MMAs may start while this warp stores
       tc_fence_before();
