@@ -504,17 +504,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* st = sfring + f * kSfStage;
         const uint4 a = reinterpret_cast<const uint4*>(st)[q * 32 + lane];
         tmem_st16_rep4(slot_a, a.x, a.y, a.z, a.w);
-        // weight scales in two halves of 16 columns: K steps 0-1, then 2-3
+        // weight scales: row 32w + lane whole (16 bytes, one conflict-free load per row), then two
+        // stores of 16 columns: K steps 0-1 (words x, y), then 2-3 (words z, w)
+        uint4 r[8];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int w = 0; w < 8; ++w) r[w] = reinterpret_cast<const uint4*>(st + kSfA)[w * 32 + lane];
+        {
           uint32_t b[16];
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
-            const uint2 r = reinterpret_cast<const uint2*>(st + kSfA)[(w * 32 + lane) * 2 + hh];
-            b[w] = r.x;
-            b[8 + w] = r.y;
+            b[w] = r[w].x;
+            b[8 + w] = r[w].y;
           }
-          tmem_st16(slot_b + 16 * hh, b);
+          tmem_st16(slot_b, b);
+        }
+        {
+          uint32_t b[16];
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            b[w] = r[w].z;
+            b[8 + w] = r[w].w;
+          }
+          tmem_st16(slot_b + 16, b);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&fempty[f]));  // the scale tiles have been read
