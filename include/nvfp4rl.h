@@ -64,7 +64,8 @@ typedef enum nvfp4rl_status {
   NVFP4RL_ERR_TIMEOUT = 6,           /* a bounded device-side wait ran out (reported by nvfp4rl_device_status) */
   NVFP4RL_ERR_ALIAS = 7,             /* an output buffer overlaps an input buffer */
   NVFP4RL_ERR_DEVICE = 8,            /* the current device is not a compute-capability 10.3 GPU */
-  NVFP4RL_ERR_RANGE = 9              /* a W4A4 call's LoRA scale s / (g_x g_w) exceeded 2^100
+  NVFP4RL_ERR_RANGE = 9              /* a folded LoRA scale (W4A4: s / (g_x g_w); W4A16 at
+                                        M > 128, r <= 64: s / (2^32 g_w)) exceeded 2^100
                                         (reported by nvfp4rl_device_status) */
 } nvfp4rl_status;
 
@@ -336,7 +337,14 @@ NVFP4RL_API nvfp4rl_status rmsnorm_aqn_quantize(const uint16_t* x, int64_t M, in
  *   y        out, [M][N] bf16 bits.
  *   group_offsets, num_groups: must be NULL / 0 (grouped W4A16 is not provided).
  *   workspace >= nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, M, N, K, r, 0): U = bf16(x A^T),
- *            scratch, contents undefined between calls.
+ *            or on 256-token tiles (below) the two bf16 parts of c U, scratch, contents undefined
+ *            between calls.
+ * For M > 128 with r <= 64, where 256-token tiles fill half the SMs or K / 256 >= 64, the call
+ *   works on 256-token tiles and folds the LoRA branch into the base product's accumulator: U
+ *   (x A^T as accumulated in fp32, not rounded to bf16) enters as the two bf16 parts
+ *   hi = bf16(c U), lo = bf16(c U - hi) of c U, c = s / (2^32 w_g) (c = s when w_g = 0), i.e. to
+ *   ~2^-17 relative of c U, as the W4A4 call does. |c| above 2^100 (weights with amax below ~1e-36) sets the range bit of the device
+ *   status word (NVFP4RL_ERR_RANGE from nvfp4rl_device_status).
  * Deterministic: split-K partial tiles are summed in a fixed order, so equal inputs give equal bits.
  */
 NVFP4RL_API nvfp4rl_status nvfp4_lora_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w_codes,
@@ -413,8 +421,8 @@ NVFP4RL_API const char* nvfp4rl_status_string(nvfp4rl_status status);
 /*
  * nvfp4rl_device_status -- synchronizes the current device and reports the
  *   library's device-side error word: NVFP4RL_ERR_TIMEOUT if a bounded wait in
- *   a kernel ran out since the last clear, else NVFP4RL_ERR_RANGE if a W4A4 call's
- *   LoRA scale was out of range, else NVFP4RL_OK. *word_out (may be NULL) receives
+ *   a kernel ran out since the last clear, else NVFP4RL_ERR_RANGE if a folded LoRA
+ *   scale was out of range, else NVFP4RL_OK. *word_out (may be NULL) receives
  *   the raw word (bits 0-4: timeouts, bit 5: range); clear != 0 resets it.
  */
 NVFP4RL_API nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t clear);
@@ -429,7 +437,8 @@ NVFP4RL_API nvfp4rl_status nvfp4rl_device_status(uint32_t* word_out, int32_t cle
  *   in a fixed array of nvfp4rl_noalloc_scratch_bytes() (4 MiB) that every GPU loading this
  *   library holds until the process exits. Nothing is allocated by the call.
  *   - Returns NVFP4RL_ERR_WORKSPACE when the problem needs more scratch than the array
- *     (nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, ...) > 4 MiB, i.e. M * r > 2^21).
+ *     (nvfp4rl_workspace_bytes(NVFP4RL_OP_LINEAR_W4A16, ...) > 4 MiB, i.e. M * r > 2^21, or
+ *     M * r > 2^20 on 256-token tiles, where the workspace holds two parts of U).
  *   - The first call on a device checks that it is a compute-capability 10.3 GPU
  *     (NVFP4RL_ERR_DEVICE otherwise) and looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture. The address is

@@ -490,7 +490,7 @@ const char* nvfp4rl_status_string(nvfp4rl_status status) {
     case NVFP4RL_ERR_TIMEOUT: return "device-side wait timed out";
     case NVFP4RL_ERR_ALIAS: return "output overlaps an input";
     case NVFP4RL_ERR_DEVICE: return "device is not compute capability 10.3";
-    case NVFP4RL_ERR_RANGE: return "W4A4 LoRA scale s / (g_x g_w) out of range";
+    case NVFP4RL_ERR_RANGE: return "folded LoRA scale (s / (g_x g_w), or s / (2^32 g_w)) out of range";
   }
   return "unknown status";
 }

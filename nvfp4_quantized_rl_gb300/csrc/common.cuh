@@ -217,15 +217,21 @@ constexpr int kPlanSMs = 152;
 bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                         int esize, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
 
-// W4A4 form of the LoRA down-projection's output: instead of U = bf16(x A^T), the two bf16 parts
-// of c U with c = s / (g_x w_g) (c = s when g_x w_g = 0): hi = bf16(c U) into U, lo =
-// bf16(c U - hi) into `lo`. |c| above 2^100 sets the range bit of `status`.
+// Folded form of the LoRA down-projection's output (the W4A4 path, and W4A16 with 256-token
+// tiles): instead of U = bf16(x A^T), the two bf16 parts of c U with c = s / (g_x w_g) (c = s
+// when g_x w_g = 0): hi = bf16(c U) into U, lo = bf16(c U - hi) into `lo`. g_x comes from device
+// memory (W4A4: the activations' g; U is then bf16(x A^T)) or by value (W4A16: 2^32, the
+// dequantized weights' offset; U is then x A^T as accumulated in fp32). |c| above 2^100 sets the
+// range bit of `status`.
 struct LoraDownScale {
-  const float* g_x = nullptr;  // null: plain U
+  const float* g_x = nullptr;  // null: g_x_value, or plain U when that is 0 too
   const float* w_g = nullptr;
   float s = 0.f;
   uint16_t* lo = nullptr;  // [M][r]
   uint32_t* status = nullptr;
+  float g_x_value = 0.f;
+  __host__ __device__ bool folded() const { return g_x != nullptr || g_x_value != 0.f; }
+  __device__ float gx() const { return g_x ? *g_x : g_x_value; }
 };
 
 // LoRA down-projection U = bf16(x A^T), [M][r] row-major, K a multiple of 64 (linear_tc.cu):

@@ -218,6 +218,64 @@ __device__ __forceinline__ void dequant_chunks(const uint8_t* crow, int row, int
   }
 }
 
+// Split-K reduction over distributed shared memory, for a cluster of C CTAs that computed the same
+// output tile over C ranges of K. CTA q owns the tile's tokens [q slice, (q + 1) slice), slice =
+// ceil(MBOX / C). After a cluster barrier (every CTA's MMAs done: `red` is free in every CTA) each
+// CTA writes its fp32 partial of every token into the owner's buffer, red[q][token - slice owner]
+// [row] (remote stores, rows in lanes); after a second barrier each owner sums its tokens over the
+// splits in split order from its own shared memory and writes them, 8 rows (16 bytes) per store.
+// No CTA reads another's memory, so none has to wait for its peers before leaving. load16(col, v):
+// this thread's 16 partial values of its row (TMEM lane) from token col on.
+template <int MBOX, int DW, class Load16>
+__device__ __forceinline__ void splitk_push_reduce(float* red, const TcParams& p, bool have, int warp, int lane,
+                                                   int64_t m0, int n0, Load16 load16) {
+  constexpr int kEpiTok = MBOX / (DW / 4);  // tokens per epilogue warp
+  const int C = p.splits;
+  const int q = static_cast<int>(cluster_ctarank());
+  const int slice = (MBOX + C - 1) / C;
+  __syncwarp();
+  cluster_sync_all();
+  if (warp >= kFirstDeqWarp && have) {
+    tc_fence_after();
+    const int row = (warp & 3) * 32 + lane;
+    const int t0 = ((warp - kFirstDeqWarp) >> 2) * kEpiTok;
+#pragma unroll 1
+    for (int c = 0; c < kEpiTok; c += 16) {
+      float v[16];
+      load16(t0 + c, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int t = t0 + c + i;
+        const int owner = t / slice;
+        const uint32_t local = smem_addr(red + (q * slice + (t - owner * slice)) * kRows + row);
+        dsmem_st_f32(dsmem_map(local, static_cast<uint32_t>(owner)), v[i]);
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();
+  if (warp >= kFirstDeqWarp) {
+    const int tb = q * slice, te = min(MBOX, tb + slice);
+    constexpr int kPerTok = kRows / 8;  // 8 rows (two float4) per item
+    for (int idx = (warp - kFirstDeqWarp) * 32 + lane; idx < (te - tb) * kPerTok; idx += DW * 32) {
+      const int lt = idx / kPerTok, r8 = (idx % kPerTok) * 8;
+      const int64_t m = m0 + tb + lt;
+      if (m >= p.M) continue;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int sp = 0; sp < C; ++sp) {
+        const float4* src = reinterpret_cast<const float4*>(red + (sp * slice + lt) * kRows + r8);
+        const float4 va = src[0], vb = src[1];
+        acc[0] += va.x; acc[1] += va.y; acc[2] += va.z; acc[3] += va.w;
+        acc[4] += vb.x; acc[5] += vb.y; acc[6] += vb.z; acc[7] += vb.w;
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = f32_to_bf16_bits(acc[2 * i]) | (f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+      *reinterpret_cast<uint4*>(p.y + m * p.N + n0 + r8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // 88 registers per thread: 608 threads of this kernel and a 128-thread LoRA-down CTA (72 registers)
 // fit the 64K-register file of one SM together.
 template <int MBOX, int DW>
@@ -479,59 +537,294 @@ __global__ void __maxnreg__(88)
   }
   if (p.splits > 1) {
     // ---------------------------------------------------------------- split-K reduction
-    // CTA q of the cluster owns the tokens [q slice, (q + 1) slice) of the tile. After a cluster
-    // barrier (every CTA has finished its K loop, so every activation ring is free), each CTA
-    // pushes its fp32 partial of every token to the owner's ring area (red[q][token][row], remote
-    // stores); after a second barrier each owner sums its tokens over the splits in split order
-    // from its own shared memory and writes them. No CTA reads another's memory, so none waits
-    // for its peers before leaving.
-    const int C = p.splits;
-    const int q = static_cast<int>(cluster_ctarank());
-    const int slice = (MBOX + C - 1) / C;
-    float* red = reinterpret_cast<float*>(xring);  // [C][slice][kRows]
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float g = *p.w_g;
+    splitk_push_reduce<MBOX, DW>(reinterpret_cast<float*>(xring), p, ok, warp, lane, m0, n0,
+                                 [&](int col, float(&v)[16]) { epilogue16(tmem + lane_base, col, do_lora, g, p.s, v); });
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
     __syncwarp();
-    cluster_sync_all();
-    if (warp >= kFirstDeqWarp && ok) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---- 256-token tiles ---------------------------------------------------------------------------
+//
+// w4a16_tc256_kernel: one CTA = 128 weight rows x one K range x 256 tokens, for calls with more
+// than 128 tokens and a LoRA rank of at most 64. The fp32 accumulator D (128 x 256) takes TMEM
+// columns 0..255 and two A buffers (one 256-K stage each) the other 256, so there is no room for a
+// LoRA accumulator of its own: the LoRA branch is folded into D. The LoRA-down kernel writes c U as
+// two bf16 matrices hi = bf16(c U) and lo = bf16(c U - hi) with c = s / (2^32 g) (c = s when
+// g = 0); after its K loop the tile adds B_lora hi^T + B_lora lo^T to D, and the epilogue's scale
+// 2^32 g (1 when g = 0) turns D into x deq(W)^T + s U B^T, the LoRA term to ~2^-17 relative of
+// c U (the hi + lo sum). Each weight tile is dequantized once for all 256 tokens and every MMA is
+// 128 x 256 x 16. A stage's activations (256 K x 256 tokens, 128 KB) stream in 64-K slots of 32 KB
+// (one 128-byte swizzled box of 256 rows), five slots in flight; after the K loop the slots hold
+// the LoRA tiles (B_lora, hi, lo), and with split K the partials.
+constexpr int kQ = 64;              // K per activation slot
+constexpr int kQBytes = 256 * 128;  // one slot: 64 bf16 K x 256 tokens
+constexpr int kQPerStage = 4;       // slots per 256-K stage
+constexpr int kQSlots = 5;          // slots in flight
+constexpr int kMaxFoldRank = 64;    // the B_lora, hi and lo tiles are one 128-byte box each
+static_assert(kKStage == kQPerStage * kQ, "a stage is four activation slots");
+static_assert((256 + kMaxSplits - 1) * kRows * 4 <= kQSlots * kQBytes + 2 * kWStageBytes,
+              "split-K partials fit the activation slots and two weight stages");
+
+__host__ __device__ constexpr size_t smem256_fixed() { return 1024 + static_cast<size_t>(kQSlots) * kQBytes + 512; }
+
+template <int DW>
+__global__ void __maxnreg__(88)
+    w4a16_tc256_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
+                       const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_blora,
+                       const __grid_constant__ CUtensorMap map_uhi, const __grid_constant__ CUtensorMap map_ulo,
+                       const TcParams p) {
+  constexpr int MBOX = 256;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int SW = p.w_stages;
+  constexpr int kWarpsPerQuarter = DW / 4;       // dequant warps sharing one TMEM lane quarter
+  constexpr int kChunks = 8 / kWarpsPerQuarter;  // 16-byte code chunks per thread and stage
+  constexpr uint32_t kAcol0 = 256;               // A buffer a: TMEM columns 256 + 128 a
+  constexpr int kEpiTok = MBOX / kWarpsPerQuarter;
+
+  // layout: activation slots (then the LoRA tiles, then split-K partials) | weight ring | barriers
+  uint8_t* xring = smem;
+  uint8_t* wring = xring + kQSlots * kQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wring + SW * kWStageBytes);
+  uint64_t* wfull = bars;             // [SW] weight stage landed
+  uint64_t* wempty = wfull + SW;      // [SW] weight stage dequantized (DW arrivals)
+  uint64_t* xfull = wempty + SW;      // [kQSlots] activation slot landed
+  uint64_t* xempty = xfull + kQSlots; // [kQSlots] its MMAs have completed (commit)
+  uint64_t* aready = xempty + kQSlots;  // [2] A buffer written (DW arrivals)
+  uint64_t* afree = aready + 2;       // [2] the stage's MMAs have completed (commit)
+  uint64_t* lfull = afree + 2;        // LoRA tiles landed
+  uint64_t* dfull = lfull + 1;        // every MMA has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x, split = blockIdx.y, tile_m = blockIdx.z;
+  const int n0 = tile_n * kRows;
+  const int m0 = tile_m * MBOX;
+  const int st0 = split * p.stages_per_split;
+  const int nst = min(p.stages_per_split, static_cast<int>(p.K / kKStage) - st0);
+  const int nq = kQPerStage * nst;  // activation slot loads of the K loop
+  const bool do_lora = p.r > 0 && split == 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(smem_addr(&wfull[i]), 1);
+      mbar_init(smem_addr(&wempty[i]), DW);
+    }
+    for (int i = 0; i < kQSlots; ++i) {
+      mbar_init(smem_addr(&xfull[i]), 1);
+      mbar_init(smem_addr(&xempty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&aready[i]), DW);
+      mbar_init(smem_addr(&afree[i]), 1);
+    }
+    mbar_init(smem_addr(lfull), 1);
+    mbar_init(smem_addr(dfull), 1);
+    fence_barrier_init();
+  }
+  // stage order: each output tile starts its K range at a different stage (see w4a16_tc_kernel)
+  auto kstage = [&](int j) { return st0 + (j + tile_n) % nst; };
+  auto load_x = [&](int i) {  // activation slot load i (slot i % kQSlots): stage i / 4, K quarter i % 4
+    const int sl = i % kQSlots;
+    const uint32_t bar = smem_addr(&xfull[sl]);
+    mbar_arrive_expect_tx(bar, kQBytes);
+    tma_load_2d(smem_addr(xring + sl * kQBytes), &map_x, kstage(i / kQPerStage) * kKStage + (i % kQPerStage) * kQ, m0,
+                bar);
+  };
+  // the first weight stages and activation slots are requested before the block's set-up completes
+  const int w_pre = min(SW, nst), x_pre = min(kQSlots, nq);
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < w_pre; ++j) {
+      uint8_t* st = wring + j * kWStageBytes;
+      const uint32_t bar = smem_addr(&wfull[j]);
+      mbar_arrive_expect_tx(bar, kWStageBytes);
+      tma_load_2d(smem_addr(st), &map_codes, kstage(j) * (kKStage / 2), n0, bar);
+      tma_load_2d(smem_addr(st + kCodeBytes), &map_scales, kstage(j) * (kKStage / 16), n0, bar);
+    }
+    for (int i = 0; i < x_pre; ++i) load_x(i);
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  bool ok = true;
+  if (warp == 0) {
+    // ------------------------------------------------------------------ weight producer
+    if (lane == 0) {
+      int issued = w_pre;
+      for (int j = w_pre; j < nst && ok; ++j) {
+        const int s = j % SW;
+        if (!mbar_wait(smem_addr(&wempty[s]), ((j / SW) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = wring + s * kWStageBytes;
+        const uint32_t bar = smem_addr(&wfull[s]);
+        mbar_arrive_expect_tx(bar, kWStageBytes);
+        const int kst = kstage(j);
+        tma_load_2d(smem_addr(st), &map_codes, kst * (kKStage / 2), n0, bar);
+        tma_load_2d(smem_addr(st + kCodeBytes), &map_scales, kst * (kKStage / 16), n0, bar);
+        issued = j + 1;
+      }
+      for (int j = max(0, issued - SW); j < issued; ++j)
+        mbar_wait(smem_addr(&wfull[j % SW]), (j / SW) & 1, p.status, kStatusTimeoutDrain);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ activation + LoRA producer
+    if (lane == 0) {
+      int issued = x_pre;
+      for (int i = x_pre; i < nq && ok; ++i) {
+        const int sl = i % kQSlots;
+        if (!mbar_wait(smem_addr(&xempty[sl]), ((i / kQSlots) & 1) ^ 1, p.status, kStatusTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        load_x(i);
+        issued = i + 1;
+      }
+      if (do_lora && ok) {
+        // slots 0..2 take the LoRA tiles once the K loop's MMAs have read them
+        for (int sl = 0; sl < 3 && ok; ++sl) {
+          const int uses = sl < nq ? (nq - sl + kQSlots - 1) / kQSlots : 0;
+          if (uses > 0)
+            ok = mbar_wait(smem_addr(&xempty[sl]), (uses - 1) & 1, p.status, kStatusTimeoutProducer);
+        }
+        if (ok) {
+          griddep_wait();  // the LoRA-down kernel has completed and its hi and lo are visible
+          const int lb = p.lora_box_bytes;
+          mbar_arrive_expect_tx(smem_addr(lfull), static_cast<uint32_t>(kRows * lb + 2 * MBOX * lb));
+          tma_load_2d(smem_addr(xring), &map_blora, 0, n0, smem_addr(lfull));
+          tma_load_2d(smem_addr(xring + kQBytes), &map_uhi, 0, m0, smem_addr(lfull));
+          tma_load_2d(smem_addr(xring + 2 * kQBytes), &map_ulo, 0, m0, smem_addr(lfull));
+          mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutDrain);
+        }
+      }
+      // drain: the last activation copies have landed before the CTA exits
+      for (int i = max(0, issued - kQSlots); i < issued; ++i)
+        mbar_wait(smem_addr(&xfull[i % kQSlots]), (i / kQSlots) & 1, p.status, kStatusTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    // The whole warp walks the stages and waits; one elected lane issues the MMAs and commits.
+    const uint32_t idesc = idesc_bf16_f32(kRows, MBOX);
+    for (int j = 0; j < nst && ok; ++j) {
+      const int a = j & 1;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&aready[a]), (j >> 1) & 1, p.status, kStatusTimeoutMma));
+      if (!ok) break;
       tc_fence_after();
-      const int quarter = warp & 3, row = quarter * 32 + lane;
-      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-      const float g = *p.w_g;
-      const int t0 = ((warp - kFirstDeqWarp) >> 2) * kEpiTok;
+      for (int q = 0; q < kQPerStage && ok; ++q) {
+        const int i = j * kQPerStage + q, sl = i % kQSlots;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&xfull[sl]), (i / kQSlots) & 1, p.status, kStatusTimeoutMma));
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t bd = smem_desc(smem_addr(xring + sl * kQBytes), 16, 1024, 2);
+          const uint32_t at = tmem + kAcol0 + a * 128 + q * 32;
 #pragma unroll
+          for (int kk = 0; kk < kQ / 16; ++kk)
+            mma_f16_ts(tmem, at + 8 * kk, bd + 2 * kk, idesc, (j | q | kk) ? 1u : 0u);
+          mma_commit(smem_addr(&xempty[sl]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (elect_one()) mma_commit(smem_addr(&afree[a]));
+      __syncwarp();
+    }
+    if (ok && do_lora) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(lfull), 0, p.status, kStatusTimeoutMma));
+      if (ok) {
+        tc_fence_after();
+        const int lb = p.lora_box_bytes;
+        const uint32_t sw = swizzle_mode_for(lb), sbo = 8 * lb;
+        if (elect_one()) {
+          for (int part = 0; part < 2; ++part)
+            for (int kk = 0; kk < p.r / 16; ++kk) {
+              const uint64_t ad = smem_desc(smem_addr(xring) + kk * 32, 16, sbo, sw);
+              const uint64_t bd = smem_desc(smem_addr(xring + (1 + part) * kQBytes) + kk * 32, 16, sbo, sw);
+              mma_f16_ss(tmem, ad, bd, idesc, 1u);
+            }
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) mma_commit(smem_addr(dfull));  // also the completion point of every MMA issued above
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ dequant + epilogue
+    const int dw = warp - kFirstDeqWarp;
+    const int quarter = warp & 3;
+    const int part_k = dw >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    for (int j = 0; j < nst && ok; ++j) {
+      const int s = j % SW, a = j & 1;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&wfull[s]), (j / SW) & 1, p.status, kStatusTimeoutDequant) &&
+                                       mbar_wait(smem_addr(&afree[a]), ((j >> 1) & 1) ^ 1, p.status,
+                                                 kStatusTimeoutDequant));
+      if (!ok) break;
+      const uint8_t* st = wring + s * kWStageBytes;
+      const uint8_t* crow = st + row * 128;
+      const uint32_t* srow = reinterpret_cast<const uint32_t*>(st + kCodeBytes + row * 16);
+      const uint32_t taddr = tmem + lane_base + kAcol0 + a * 128;
+      const uint2 sc = kChunks == 4 ? *reinterpret_cast<const uint2*>(srow + part_k * 2)
+                                    : make_uint2(srow[part_k], 0x08080808u);
+      if (__any_sync(0xFFFFFFFFu, has_small_scale(sc)))
+        dequant_chunks<true, kChunks>(crow, row, part_k * kChunks, sc, taddr);
+      else
+        dequant_chunks<false, kChunks>(crow, row, part_k * kChunks, sc, taddr);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&aready[a]));
+        mbar_arrive(smem_addr(&wempty[s]));
+      }
+    }
+    // ---------------------------------------------------------------- epilogue
+    ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait(smem_addr(dfull), 0, p.status, kStatusTimeoutEpilogue));
+    tc_fence_after();
+    if (ok && p.splits == 1) {
+      const float g = *p.w_g;
+      const float out = p.r > 0 && g == 0.f ? 1.f : 0x1p32f * g;
+      const int64_t n = n0 + row;
+      const int t0 = part_k * kEpiTok;
+#pragma unroll 1
       for (int c = 0; c < kEpiTok; c += 16) {
-        float v[16];
-        epilogue16(tmem + lane_base, t0 + c, do_lora, g, p.s, v);
+        uint32_t d[16];
+        tmem_ld16(tmem + lane_base + t0 + c, d);
+        tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int t = t0 + c + i;
-          const int owner = t / slice;
-          const uint32_t local = smem_addr(red + (q * slice + (t - owner * slice)) * kRows + row);
-          dsmem_st_f32(dsmem_map(local, static_cast<uint32_t>(owner)), v[i]);
+          const int64_t m = m0 + t0 + c + i;
+          if (m < p.M) p.y[m * p.N + n] = static_cast<uint16_t>(f32_to_bf16_bits(__uint_as_float(d[i]) * out));
         }
       }
     }
-    __syncwarp();
-    cluster_sync_all();
-    if (warp >= kFirstDeqWarp) {
-      const int tb = q * slice, te = min(MBOX, tb + slice);
-      constexpr int kPerTok = kRows / 8;  // 8 rows (two float4) per item
-      for (int idx = (warp - kFirstDeqWarp) * 32 + lane; idx < (te - tb) * kPerTok; idx += DW * 32) {
-        const int lt = idx / kPerTok, r8 = (idx % kPerTok) * 8;
-        const int64_t m = m0 + tb + lt;
-        if (m >= p.M) continue;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int sp = 0; sp < C; ++sp) {
-          const float4* src = reinterpret_cast<const float4*>(red + (sp * slice + lt) * kRows + r8);
-          const float4 va = src[0], vb = src[1];
-          acc[0] += va.x; acc[1] += va.y; acc[2] += va.z; acc[3] += va.w;
-          acc[4] += vb.x; acc[5] += vb.y; acc[6] += vb.z; acc[7] += vb.w;
-        }
-        uint32_t o[4];
+  }
+  if (p.splits > 1) {
+    // ---------------------------------------------------------------- split-K reduction
+    // (the partials take the activation slots, and the weight ring behind them where needed)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float g = *p.w_g;
+    const float out = p.r > 0 && g == 0.f ? 1.f : 0x1p32f * g;
+    splitk_push_reduce<MBOX, DW>(reinterpret_cast<float*>(xring), p, ok, warp, lane, m0, n0, [&](int col, float(&v)[16]) {
+      uint32_t d[16];
+      tmem_ld16(tmem + lane_base + col, d);
+      tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = f32_to_bf16_bits(acc[2 * i]) | (f32_to_bf16_bits(acc[2 * i + 1]) << 16);
-        *reinterpret_cast<uint4*>(p.y + m * p.N + n0 + r8) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
+      for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(d[i]) * out;
+    });
   }
   tc_fence_before();
   __syncthreads();
@@ -584,8 +877,8 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
   griddep_wait();
   griddep_launch_dependents();
   float cu = 1.f;  // c of the W4A4 form
-  if (ls.g_x) {
-    const float alpha = *ls.g_x * *ls.w_g;
+  if (ls.folded()) {
+    const float alpha = ls.gx() * *ls.w_g;
     cu = alpha == 0.f ? ls.s : ls.s / alpha;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && !(fabsf(cu) <= 0x1p100f))
       atomicOr(ls.status, kStatusRange);
@@ -675,9 +968,12 @@ __global__ void __launch_bounds__(128) w4a16_lora_down_kernel(const uint16_t* __
           if (j0 + j4 + e >= r) continue;
           const uint32_t u = f32_to_bf16_bits(av[e]);
           const int64_t at = m * r + j0 + j4 + e;
-          if (ls.g_x) {
-            // c U = hi + lo: hi = bf16(c U), lo = bf16(c U - hi) (c U - hi is exact in fp32)
-            const float cuv = __uint_as_float(u << 16) * cu;
+          if (ls.folded()) {
+            // c U = hi + lo: hi = bf16(c U), lo = bf16(c U - hi) (c U - hi is exact in fp32). U
+            // is bf16(x A^T) when g_x comes from memory (W4A4: the same U as the calls that learn
+            // g_x after the LoRA-down), x A^T as accumulated in fp32 when it is given by value
+            // (W4A16 on 256-token tiles).
+            const float cuv = (ls.g_x ? __uint_as_float(u << 16) : av[e]) * cu;
             const uint32_t hi = f32_to_bf16_bits(cuv);
             U[at] = static_cast<uint16_t>(hi);
             ls.lo[at] = static_cast<uint16_t>(f32_to_bf16_bits(cuv - __uint_as_float(hi << 16)));
@@ -719,7 +1015,7 @@ constexpr int kDW = 16;  // dequant warps of the tcgen05 kernel (4 per TMEM lane
 
 struct TcPlan {
   int mbox, tiles_m, tiles_n, w_stages;
-  size_t smem_bytes, ws_u, ws_total;
+  size_t smem_bytes, ws_u, ws_lo, ws_total;  // ws_lo: the lo part of c U (256-token tiles with LoRA)
 };
 
 // Tile shape, shared-memory rings and workspace (U only), for `mbox`-token tiles. With
@@ -744,11 +1040,37 @@ TcPlan plan_for(int64_t M, int64_t N, int r, int mbox, bool reserve_down) {
   return t;
 }
 
-// 128-token tiles when M exceeds one 64-token tile and two weight stages still fit beside the
-// 128-token activation ring and the LoRA tiles; otherwise 64-token tiles (always the case for
-// r = 128 at M > 64), leaving room for a LoRA-down CTA where that still leaves two weight stages.
+// 256-token tiles (w4a16_tc256_kernel): four activation slots, the rest of shared memory for the
+// weight ring; the workspace holds hi and lo of c U.
+TcPlan plan256(int64_t M, int64_t N, int r) {
+  TcPlan t{};
+  t.mbox = 256;
+  t.tiles_m = static_cast<int>((M + 255) / 256);
+  t.tiles_n = static_cast<int>(N / kRows);
+  const size_t fixed = smem256_fixed();
+  const size_t budget = 227 * 1024;
+  t.w_stages = static_cast<int>(std::min<size_t>(8, (budget - fixed) / kWStageBytes));
+  t.smem_bytes = fixed + t.w_stages * kWStageBytes;
+  size_t o = 0;
+  auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
+  t.ws_u = take(static_cast<size_t>(M) * std::max(r, 1) * 2);
+  t.ws_lo = r ? take(static_cast<size_t>(M) * r * 2) : 0;
+  t.ws_total = o;
+  return t;
+}
+
+// 256-token tiles for more than 128 tokens at LoRA ranks up to 64 when they fill at least half the
+// SMs or K has 64 stages or more (measured on the 32B-shaped layer at 256 tokens: gate 79 -> 66 us
+// and down 104 -> 72 us per call, while q and k, 40 and 8 such tiles over 20 stages, are faster on
+// twice as many 128-token CTAs); else 128-token tiles when M exceeds one 64-token tile and two
+// weight stages still fit beside the 128-token activation ring and the LoRA tiles; otherwise
+// 64-token tiles (always the case for r = 128 at M > 64), leaving room for a LoRA-down CTA where
+// that still leaves two weight stages.
 TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
-  (void)K;
+  if (M > 128 && r <= kMaxFoldRank) {
+    const int64_t tiles256 = (N / kRows) * ((M + 255) / 256);
+    if (2 * tiles256 >= kPlanSMs || K / kKStage >= 64) return plan256(M, N, r);
+  }
   if (M > 64) {
     const TcPlan t = plan_for(M, N, r, 128, false);
     if (t.w_stages >= 2) return t;
@@ -758,9 +1080,10 @@ TcPlan plan(int64_t M, int64_t N, int64_t K, int r) {
   return plan_for(M, N, r, 64, false);
 }
 
-template <int MBOX>
-void* tc_kernel_ptr() {
-  return reinterpret_cast<void*>(w4a16_tc_kernel<MBOX, kDW>);
+void* tc_kernel_ptr(int mbox) {
+  return mbox == 256 ? reinterpret_cast<void*>(w4a16_tc256_kernel<kDW>)
+         : mbox == 128 ? reinterpret_cast<void*>(w4a16_tc_kernel<128, kDW>)
+                       : reinterpret_cast<void*>(w4a16_tc_kernel<64, kDW>);
 }
 
 // Clusters of `c` CTAs of the tcgen05 kernel that can be resident at once on this device.
@@ -783,7 +1106,7 @@ int cluster_capacity(int device, int mbox, size_t smem, int c) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  const void* fn = mbox == 64 ? tc_kernel_ptr<64>() : tc_kernel_ptr<128>();
+  const void* fn = tc_kernel_ptr(mbox);
   if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
@@ -792,19 +1115,28 @@ int cluster_capacity(int device, int mbox, size_t smem, int c) {
   return n;
 }
 
-// Split-K factor: 1 when the output tiles alone fill half the SMs; otherwise the largest
-// cluster size (<= 8, <= the number of 256-K stages) whose clusters all fit at once.
-int choose_splits(int device, const TcPlan& t, int64_t K, int sm_count) {
+// Split-K factor: the cluster size c (<= 8, <= the number of 256-K stages, the stages dividing
+// into exactly c splits) that minimises waves(c) x (stages per CTA + 1 + 4 [c > 1]), where waves(c)
+// is the number of rounds of resident clusters that tiles x c CTAs take, the + 1 stands for a CTA's
+// fixed cost (set-up, pipeline fill, epilogue) and the + 4 for the split-K reduction through
+// distributed shared memory (measured: ~4 stages' time).
+int choose_splits_waves(int device, const TcPlan& t, int64_t K) {
   const int tiles = t.tiles_n * t.tiles_m;
   const int kst = static_cast<int>(K / kKStage);
-  if (2 * tiles > sm_count) return 1;
-  for (int c = std::min(kMaxSplits, kst); c >= 2; --c) {
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int c = 1; c <= std::min(kMaxSplits, kst); ++c) {
     const int sps = (kst + c - 1) / c;
-    const int used = (kst + sps - 1) / sps;  // splits after rounding the stages per split
-    if (used != c) continue;
-    if (tiles <= cluster_capacity(device, t.mbox, t.smem_bytes, c)) return c;
+    if ((kst + sps - 1) / sps != c) continue;
+    const int cap = cluster_capacity(device, t.mbox, t.smem_bytes, c);
+    if (cap <= 0) continue;
+    const int64_t cost = static_cast<int64_t>((tiles + cap - 1) / cap) * (sps + 1 + (c > 1 ? 4 : 0));
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c;
+    }
   }
-  return 1;
+  return best;
 }
 
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows, int esize,
@@ -918,18 +1250,86 @@ size_t w4a16_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int r, int) {
   return plan(M, N, K, r).ws_total;
 }
 
+// 256-token tiles: the LoRA-down writes hi and lo of c U, c = s / (2^32 g), and the main kernel
+// folds them into its accumulator.
+nvfp4rl_status launch_w4a16_tc256(const LinearArgs& a, const TcPlan& t, void* ws, const DeviceInfo& dev,
+                                  cudaStream_t st) {
+  uint16_t* U = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + t.ws_u);
+  uint16_t* Ulo = a.r ? reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + t.ws_lo) : nullptr;
+  if (cudaFuncSetAttribute(w4a16_tc256_kernel<kDW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(t.smem_bytes)) != cudaSuccess)
+    return NVFP4RL_ERR_CUDA;
+  const int splits = choose_splits_waves(dev.device, t, a.K);
+  const int kst = static_cast<int>(a.K / kKStage);
+  if (a.r) {
+    LoraDownScale ls;
+    ls.g_x_value = 0x1p32f;  // the dequantized weights carry 2^-32 of their value
+    ls.w_g = a.w_g;
+    ls.s = a.s;
+    ls.lo = Ulo;
+    ls.status = dev.status;
+    const nvfp4rl_status sd = launch_lora_down(a.x, a.M, a.K, a.A, a.r, U, dev, st, ls);
+    if (sd != NVFP4RL_OK) return sd;
+  }
+  CUtensorMap mc, ms, mx, mb, mh, ml;
+  const int lbox = a.r ? lora_box_bytes_for(a.r) : 128;
+  if (!make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, a.K / 2, a.N, 1, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_scales, a.K / 16, a.N, 1, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, 2, kQ, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+    return NVFP4RL_ERR_CUDA;
+  if (a.r) {
+    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, a.r, a.N, 2, lbox / 2, kRows, swizzle_for(lbox)) ||
+        !make_map(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, U, a.r, a.M, 2, lbox / 2, 256, swizzle_for(lbox)) ||
+        !make_map(&ml, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ulo, a.r, a.M, 2, lbox / 2, 256, swizzle_for(lbox)))
+      return NVFP4RL_ERR_CUDA;
+  } else {
+    mb = mh = ml = mc;
+  }
+  TcParams p{};
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.stages_per_split = (kst + splits - 1) / splits;
+  p.splits = splits;
+  p.r = a.r;
+  p.lora_box_bytes = lbox;
+  p.s = a.s;
+  p.w_g = a.w_g;
+  p.y = a.y;
+  p.status = dev.status;
+  p.w_stages = t.w_stages;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(t.tiles_n, splits, t.tiles_m);
+  cfg.blockDim = dim3(threads_for(kDW));
+  cfg.dynamicSmemBytes = t.smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = splits;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as in launch_w4a16_tc
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.r ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, w4a16_tc256_kernel<kDW>, mc, ms, mx, mb, mh, ml, p) != cudaSuccess)
+    return NVFP4RL_ERR_CUDA;
+  return launch_status();
+}
+
 nvfp4rl_status launch_w4a16_tc(const LinearArgs& a, void* ws, size_t ws_bytes, const DeviceInfo& dev,
                                cudaStream_t st) {
   const TcPlan t = plan(a.M, a.N, a.K, a.r);
   if (ws_bytes < t.ws_total) return NVFP4RL_ERR_WORKSPACE;
   if (t.w_stages < 2) return NVFP4RL_ERR_UNSUPPORTED_SHAPE;
+  if (t.mbox == 256) return launch_w4a16_tc256(a, t, ws, dev, st);
   uint16_t* U = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + t.ws_u);
   const int smem = static_cast<int>(t.smem_bytes);
   cudaError_t e =
       t.mbox == 64 ? cudaFuncSetAttribute(w4a16_tc_kernel<64, kDW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
                    : cudaFuncSetAttribute(w4a16_tc_kernel<128, kDW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return NVFP4RL_ERR_CUDA;
-  const int splits = choose_splits(dev.device, t, a.K, std::min(dev.sm_count, kPlanSMs));
+  const int splits = choose_splits_waves(dev.device, t, a.K);
   const int kst = static_cast<int>(a.K / kKStage);
 
   if (a.r) {

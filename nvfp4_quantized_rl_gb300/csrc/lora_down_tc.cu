@@ -184,8 +184,8 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
   cluster_sync_all();  // every CTA's partial is in its shared memory
   // ---------------------------------------------------------------- reduction over the cluster, U
   float cu = 1.f;  // c of the W4A4 form
-  if (p.ls.g_x) {
-    const float alpha = *p.ls.g_x * *p.ls.w_g;
+  if (p.ls.folded()) {
+    const float alpha = p.ls.gx() * *p.ls.w_g;
     cu = alpha == 0.f ? p.ls.s : p.ls.s / alpha;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && !(fabsf(cu) <= 0x1p100f))
       atomicOr(p.ls.status, kStatusRange);
@@ -210,9 +210,11 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t u = f32_to_bf16_bits(av[e]);
-      if (p.ls.g_x) {
-        // c U = hi + lo: hi = bf16(c U), lo = bf16(c U - hi) (c U - hi is exact in fp32)
-        const float cuv = __uint_as_float(u << 16) * cu;
+      if (p.ls.folded()) {
+        // c U = hi + lo: hi = bf16(c U), lo = bf16(c U - hi) (c U - hi is exact in fp32). U is
+        // bf16(x A^T) when g_x comes from memory (W4A4: the same U as the calls that learn g_x
+        // after the LoRA-down), x A^T as accumulated in fp32 when it is given by value (W4A16).
+        const float cuv = (p.ls.g_x ? __uint_as_float(u << 16) : av[e]) * cu;
         o[e] = f32_to_bf16_bits(cuv);
         lo[e] = f32_to_bf16_bits(cuv - __uint_as_float(o[e] << 16));
       } else {
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
     }
     const int64_t at = m * p.r + j4;  // 8-byte aligned: r and j4 are multiples of 4
     *reinterpret_cast<uint2*>(p.U + at) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
-    if (p.ls.g_x)
+    if (p.ls.folded())
       *reinterpret_cast<uint2*>(p.ls.lo + at) = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
   }
   cluster_sync_all();  // partials read by every peer before any CTA leaves
@@ -239,7 +241,7 @@ namespace {
 // is 0): the form the W4A4 GEMM consumes, for a LoRA-down that ran before g_x was known.
 __global__ void __launch_bounds__(256) lora_scale_kernel(uint16_t* __restrict__ U, uint16_t* __restrict__ lo,
                                                          int64_t n8, LoraDownScale ls) {
-  const float alpha = *ls.g_x * *ls.w_g;
+  const float alpha = ls.gx() * *ls.w_g;
   const float cu = alpha == 0.f ? ls.s : ls.s / alpha;
   if (blockIdx.x == 0 && threadIdx.x == 0 && !(fabsf(cu) <= 0x1p100f)) atomicOr(ls.status, kStatusRange);
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;

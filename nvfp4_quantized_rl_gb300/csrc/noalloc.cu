@@ -11,9 +11,10 @@
 // workspace. Every call on a device shares the one array; calls that overlap on the GPU (on
 // different streams without ordering) race on it.
 //
-// The W4A16 workspace holds only U = bf16(x A^T), M * max(r, 1) * 2 bytes rounded up to 256:
-// 4 MiB covers M * r up to 2^21 (e.g. 16384 tokens at rank 128, 65535 tokens at rank 32);
-// larger problems are rejected with NVFP4RL_ERR_WORKSPACE.
+// The W4A16 workspace holds only U = bf16(x A^T), M * max(r, 1) * 2 bytes rounded up to 256 (for
+// more than 128 tokens at rank <= 64, the two bf16 parts of the scaled U: twice that): 4 MiB covers
+// M * r up to 2^21, or 2^20 in the two-part case (e.g. 16384 tokens at rank 128, 16384 tokens at
+// rank 64); larger problems are rejected with NVFP4RL_ERR_WORKSPACE.
 #include <mutex>
 
 #include "common.cuh"

@@ -25,7 +25,7 @@ enum : uint32_t {
   kStatusTimeoutEpilogue = 1u << 3,
   kStatusTimeoutDrain = 1u << 4,
   kStatusTimeoutMask = (1u << 5) - 1u,
-  kStatusRange = 1u << 5,  // not a wait: a W4A4 LoRA scale s / (g_x g_w) out of range
+  kStatusRange = 1u << 5,  // not a wait: a folded LoRA scale (s / (g_x g_w), or s / (2^32 g_w)) out of range
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -155,6 +155,17 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // D(tmem) (+)= A(smem) * B(smem)^T, kind::f16.
+// D (TMEM) = / += A (TMEM columns from a_tmem) x B (shared-memory descriptor), kind::f16.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
   asm volatile(

@@ -651,6 +651,41 @@ def test_linear_multi_tile_ragged(nv, w4a4, M, N, K, r, s):
     P.assert_gemm_close(y, ref_linear(w4a4, x, q, A, B, s), f"{M}x{N}x{K} r={r}")
 
 
+@pytest.mark.parametrize("M,N,K,r,s", [(300, 9728, 512, 64, 2.0), (256, 9728, 512, 0, 1.0), (200, 9728, 256, 48, 0.5),
+                                       (260, 256, 16384, 32, 1.0), (129, 384, 16384, 16, 2.0)])
+def test_linear_256_token_tiles(nv, M, N, K, r, s):
+    """W4A16 with more than 128 tokens at LoRA ranks up to 64 on 256-token tiles (taken when those
+    fill half the SMs, 76 column tiles here, or K has 64 stages or more, split over a cluster here):
+    the LoRA branch folded into the accumulator as hi + lo of c U, token tiles past M, r = 48 in a
+    zero-padded 64-rank box, no LoRA at all."""
+    q = _weights(N, K, 21, M, N)
+    x = synth.activation_bf16(M, K, 22, M)
+    A, B = synth.lora_factors(r, K, N, 23, M) if r else (None, None)
+    y = gpu_linear(nv, False, x, q, A, B, s)
+    P.assert_gemm_close(y, ref_linear(False, x, q, A, B, s), f"{M}x{N}x{K} r={r}")
+
+
+@pytest.mark.parametrize("case", ["zero_weight", "small_scales"])
+def test_linear_256_token_tiles_edge_weights(nv, case):
+    """256-token tiles on an all-zero weight tensor (g = 0: the folded LoRA term enters with c = s and
+    the output scale is 1, Y = s (x A^T) B^T) and on weights whose block scale bytes are zero or E4M3
+    subnormals (the general dequant branch)."""
+    M, N, K, r, s = 200, 9728, 256, 32, 2.0
+    if case == "zero_weight":
+        q = oracle.quantize(np.zeros((N, K), np.uint16))
+        assert q[2] == 0.0
+    else:
+        W = synth.weight_bf16(N, K, 0.02, 91, 15)
+        W[5] = 0
+        amax = float(np.abs(synth.bf16_to_f32(W)).max())
+        q = oracle.quantize(W, amax_in=amax * 2.0 ** 15)
+        assert (q[1] <= 7).all() and (q[1] == 0).any()
+    x = synth.activation_bf16(M, K, 92, 0)
+    A, B = synth.lora_factors(r, K, N, 93, 0)
+    y = gpu_linear(nv, False, x, q, A, B, s)
+    P.assert_gemm_close(y, ref_linear(False, x, q, A, B, s), case)
+
+
 def test_linear_empty_is_a_noop(nv):
     q = _weights(128, 256, 1)
     x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
