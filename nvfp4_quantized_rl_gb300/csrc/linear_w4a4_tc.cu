@@ -25,7 +25,7 @@
 //   y = alpha * (x_q W_q^T + c U B^T),
 // and c U is not a bf16 value, so the LoRA-down kernel writes it as two bf16 matrices, hi =
 // bf16(c U) and lo = bf16(c U - hi), and each tile runs the up-projection (kind::f16 MMAs, hi
-// slice x B_lora slice^T, then lo slice x B_lora slice^T) as the first stages of its K loop,
+// slice x B_lora slice^T, then lo slice x B_lora slice^T) as the last stages of its K loop,
 // through the same operand ring as the codes: 64 ranks of U (128 rows x 128 bytes) and of B_lora
 // (256 rows x 128 bytes) fill a ring stage exactly as 256 K of activation and weight codes do. The
 // accumulator receives c U B^T to ~2^-17 relative, as if U = bf16(x A^T) were scaled
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ksteps = static_cast<int>(p.K / kKStage);     // FP4 stages per tile
-  const int nl = 2 * ((p.r + kLoraK - 1) / kLoraK);        // LoRA stages per tile (hi, lo per slice), first
+  const int nl = 2 * ((p.r + kLoraK - 1) / kLoraK);        // LoRA stages per tile (hi, lo per slice), last
   const int ns = nl + ksteps;
   const int ntiles = total_tiles(p);
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = wside ? R::kBBytes : kACode;
       const int half = static_cast<int>(rank) * R::kBRows;  // this CTA's weight rows of the tile
       int c = 0, issued = 0;
+      bool u_ready = wside;  // B_lora is an input of the call; U is the LoRA-down kernel's output
       for (int t = unit; t < ntiles && ok; t += units) {
         const TileInfo ti = tile_of<kPair>(p, t, rank);
         const int row = wside ? ti.e * static_cast<int>(p.N) + ti.n0 + half : static_cast<int>(ti.m0);
@@ -362,10 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t bar = smem_addr(&cfull[c]);
           const uint32_t dst = smem_addr(smem + c * R::kStageBytes + off);
+          if (k >= ksteps && !u_ready) {
+            griddep_wait();  // the LoRA-down kernel has completed and its hi and lo are visible
+            u_ready = true;
+          }
           mbar_arrive_expect_tx(bar, bytes);
-          if (k < nl)  // slice k / 2 of hi (k even) or lo (k odd), and of B_lora
-            tma_load_2d(dst, wside ? &map_bl : (k & 1) ? &map_ul : &map_uh, (k >> 1) * kLoraK, lrow, bar);
-          else tma_load_2d(dst, map, (k - nl) * (kKStage / 2), row, bar);
+          const int kl = k - ksteps;
+          if (kl >= 0)  // slice kl / 2 of hi (kl even) or lo (kl odd), and of B_lora
+            tma_load_2d(dst, wside ? &map_bl : (kl & 1) ? &map_ul : &map_uh, (kl >> 1) * kLoraK, lrow, bar);
+          else tma_load_2d(dst, map, k * (kKStage / 2), row, bar);
           ++issued;
           if (++c == S) c = 0;
         }
@@ -435,21 +441,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t soff = static_cast<uint64_t>(c * (R::kStageBytes >> 4));
           const uint32_t sfa = tmem + kSfACol + 16 * j, sfb = tmem + kSfBCol + 32 * j;
+          const int kl = k - ksteps;  // LoRA stages come last
           if (elect_one()) {
             if constexpr (kPair) {
-              if (k < nl) {
+              if (kl >= 0) {
 #pragma unroll
                 for (int kk = 0; kk < kLoraK / 16; ++kk)
-                  mma_f16_pair(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
+                  mma_f16_pair(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l,
+                               (fp4 || kl || kk) ? 1u : 0u);
               } else if (fp4) {
                 mma_stage_nvf4_pair(tmem, adesc0 + soff, bdesc0 + soff, idesc, sfa, sfb, k ? 1u : 0u);
               }
               mma_commit_pair(smem_addr(&mdone[it % kDone]));
             } else {
-              if (k < nl) {
+              if (kl >= 0) {
 #pragma unroll
                 for (int kk = 0; kk < kLoraK / 16; ++kk)
-                  mma_f16_ss(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (k | kk) ? 1u : 0u);
+                  mma_f16_ss(tmem, adesc0 + soff + 2 * kk, bdesc0 + soff + 2 * kk, idesc_l, (fp4 || kl || kk) ? 1u : 0u);
               } else if (fp4) {
                 mma_stage_nvf4(tmem, adesc0 + soff, bdesc0 + soff, idesc, sfa, sfb, k ? 1u : 0u);
               }
@@ -493,8 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                kStatusTimeoutMma));
         if (!ok) break;
       }
-      if (k >= nl) {
-        const int fi = li * ksteps + (k - nl);  // FP4 stage count: the scale ring's index
+      if (k < ksteps) {
+        const int fi = li * ksteps + k;  // FP4 stage count: the scale ring's index
         const int f = fi % kSfRing;
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&ffull[f]), static_cast<uint32_t>((fi / kSfRing) & 1),
                                                p.status, kStatusTimeoutMma));
@@ -796,13 +804,30 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
   p.y = a.y;
   p.status = dev.status;
   p.stages = t.stages;
+  // With LoRA, the GEMM is a programmatic dependent of the kernel before it (the LoRA-down, or the
+  // hi/lo split): it runs its FP4 stages while that kernel finishes and waits for it
+  // (griddepcontrol.wait) only before loading U, for the LoRA stages at the end of a tile. What it
+  // reads before that (activation codes, scales and g_x, the weights, B_lora) was complete before
+  // that kernel's own wait returned. Without LoRA the kernel before it may be the activation encode,
+  // so the launch is an ordinary one.
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
   if (!t.pair) {
     const int64_t max_tiles = tiles_m_bound * p.tiles_n;
     const int grid = static_cast<int>(std::min<int64_t>(max_tiles, dev.sm_count));
     if (cudaFuncSetAttribute(w4a4_wide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(t.smem)) != cudaSuccess)
       return NVFP4RL_ERR_CUDA;
-    w4a4_wide_kernel<false><<<grid, kThreads, t.smem, st>>>(mxc, mxs, mwc, mws, muh, mul, mb, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = t.smem;
+    cfg.stream = st;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = a.r ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, w4a4_wide_kernel<false>, mxc, mxs, mwc, mws, muh, mul, mb, p) != cudaSuccess)
+      return NVFP4RL_ERR_CUDA;
     return launch_status();
   }
   const int clusters = pair_clusters(dev.device, static_cast<int>(t.smem));
@@ -812,13 +837,14 @@ nvfp4rl_status launch_w4a4_tc(const LinearArgs& a, void* ws, size_t ws_bytes, co
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = t.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.r ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, w4a4_wide_kernel<true>, mxc, mxs, mwc, mws, muh, mul, mb, p) != cudaSuccess)
     return NVFP4RL_ERR_CUDA;
   return launch_status();
