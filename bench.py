@@ -872,7 +872,20 @@ def run_suite(args):
         emit("quantize_amax_given_7b_gate", us_a, 0, n * k * (2 + 0.5625), "hbm",
              {"shape": [n, k], "note": "one encode pass, amax given (nvfp4_quantize amax_in); bytes: 2 B in, "
                                        "0.5625 B out per element"})
-        del W, c, sc, g, wsq
+        mask = torch.randint(-2 ** 31, 2 ** 31 - 1, ((n * k + 31) // 32,), generator=gen, device=dev,
+                             dtype=torch.int64).to(torch.int32)  # Bernoulli(1/2) bits
+        us_ga = timed(lambda: nv.nvfp4_quantize_guided(W, mask, amax_in=am, codes=c, scales=sc, g=g, workspace=wsq),
+                      10)
+        emit("quantize_guided_amax_given_7b_gate", us_ga, 0, n * k * (2 + 0.5625 + 0.125), "hbm",
+             {"shape": [n, k], "note": "one guided encode pass, amax given; bytes: 2 B in, 0.5625 B out, 0.125 B "
+                                       "of mask per element"})
+        rec = torch.empty((n * k + 31) // 32, dtype=torch.int32, device=dev)
+        us_ra = timed(lambda: nv.nvfp4_quantize_record(W, amax_in=am, codes=c, scales=sc, g=g, record=rec,
+                                                       workspace=wsq), 10)
+        emit("quantize_record_amax_given_7b_gate", us_ra, 0, n * k * (2 + 0.5625 + 0.125), "hbm",
+             {"shape": [n, k], "note": "one record encode pass, amax given; bytes: 2 B in, 0.5625 B out, 0.125 B "
+                                       "of record per element"})
+        del W, c, sc, g, wsq, mask, rec
         torch.cuda.empty_cache()
     # ---- RMSNorm-AQN fused with the NVFP4 quantization of its output (the W4A4 activation operand)
     if want("rmsnorm_quantize"):

@@ -11,12 +11,15 @@
 // Kernels:
 //   amax_kernel, amax_bulk_kernel  the tensor amax (grid-stride 128-bit loads, or for large
 //                    tensors a cp.async.bulk ring per SM), one atomicMax per CTA.
-//   quantize_kernel  one thread per 16-element block (two blocks in flight per thread), in four
-//                    modes: plain, guided (a mask picks the rounding direction), record (plain,
-//                    plus one rounding-direction bit per element: TRACE's rollout side), cached
-//                    (guided against given scale bytes and g, one pass: TRACE's training side).
-//                    bf16 input uses per-tensor threshold tables and two-element bf16 compares,
-//                    fp32 input per-block thresholds and integer compares.
+//   Four modes: plain, guided (a mask picks the rounding direction), record (plain, plus one
+//   rounding-direction bit per element: TRACE's rollout side), cached (guided against given scale
+//   bytes and g, one pass: TRACE's training side).
+//   encode_ring_kernel  bf16 input, every mode: a cp.async.bulk ring per CTA feeds encode warps
+//                    that take the codes from the hardware E2M1 conversion of x times a reciprocal
+//                    of the scale, chosen per scale byte so that the result is exact (else the
+//                    compare form below for that byte's blocks).
+//   quantize_kernel  fp32 input: one thread per 16-element block (two blocks in flight per
+//                    thread), per-block thresholds and integer compares.
 //   encode_amax_ring_kernel  the weight refresh: one tensor's encoding while the next tensor's
 //                    amax streams through a shared-memory ring.
 //   rmsnorm_quant_kernel  RMSNorm-AQN and the quantization of its output in one cooperative
@@ -96,7 +99,7 @@ __device__ __forceinline__ void guided_thresholds(float dec, float g, uint32_t g
   }
 }
 
-// Encodings of quantize_kernel.
+// Encoding modes.
 enum : int {
   kModePlain = 0,   // nvfp4_quantize
   kModeGuided = 1,  // nvfp4_quantize_guided: rounding directions from a mask
@@ -310,7 +313,7 @@ struct EncodeTables {
   float rcp[0x7F];
 };
 
-// A reciprocal r of d = E4M3(b) g for the conversion form of the plain encoding, or -1.
+// A reciprocal r of d = E4M3(b) g for the conversion forms of the encodings, or -1.
 // cvt.rn.satfinite.e2m1x2 rounds y = fl32(x r) to E2M1 (nearest, ties to the even code,
 // saturating at 6), which is the exact rounding of |x|/d unless y and x/d fall on different sides
 // of a midpoint m (or y lands on m while x/d does not). With r within 3.5 fp32 ulps of 1/d, y is
@@ -319,20 +322,29 @@ struct EncodeTables {
 // fp32: m d = ph + pl exactly (an FMA gives the product's rounding error), so for each such B the
 // exact side of m d it lies on (above, below, or on it: then the even code) is known, and
 // fl32(B r) is one multiply; r is taken as RN(1/fl32(d)) or one of its four nearest fp32
-// neighbours, the first for which every such B goes to its exact side. Zero scale (b = 0, or g
-// not positive): 0, so x 0 = +-0 and every code is sign|0, as the compares give.
-__device__ float cvt_reciprocal(int b, float g) {
+// neighbours, the first for which every such B goes to its exact side. With `grid` the seven grid
+// points G (0.5 .. 6) are checked the same way, strictly: y must lie on the side of G that x/d lies
+// on and never on G itself, and a bf16 value exactly on G d rejects the byte; then y is on the
+// grid only for x = 0. `mids` false skips the midpoints (the guided encodings need only the grid
+// points). Zero scale (b = 0, or g not positive): 0, so x 0 = +-0 and every code is sign|0, as the
+// compares give.
+__device__ float cvt_reciprocal(int b, float g, bool mids = true, bool grid = false) {
   if (b == 0 || !(g > 0.0f)) return 0.0f;
   const float dec = e4m3_decode_pos(b);
   const float dh = __fmul_rn(dec, g);
-  if (!(dh > 0x1p-120f)) return -1.0f;  // 1/d near the fp32 range: the compare form
+  if (!(dh > 0x1p-120f) || !(dh <= 0x1.fffffep127f)) return -1.0f;  // 1/d near the fp32 range: the compare form
   const float r0 = __frcp_rn(dh);
-  const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
-  float B[7];
-  bool near[7], up[7];
+  // points 0-6: the midpoints (a tie goes to the even code: up at odd k); 7-13: the grid points
+  const float pts[14] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+  float B[14];
+  bool near[14], up[14];
 #pragma unroll
-  for (int k = 0; k < 7; ++k) {
-    const float md = mids[k] * dec;  // exact: at most 7 significant bits
+  for (int k = 0; k < 14; ++k) {
+    near[k] = false;
+    B[k] = 0.0f;
+    up[k] = false;
+    if (k < 7 ? !mids : !grid) continue;
+    const float md = pts[k] * dec;  // exact: at most 7 significant bits
     const float ph = __fmul_rn(md, g), pl = __fmaf_rn(md, g, -ph);
     const uint32_t t = __float_as_uint(ph) & 0xFFFF0000u;  // the bf16 grid points around m d
     const float lo = __uint_as_float(t), hi = __uint_as_float(t + 0x10000u);
@@ -341,7 +353,8 @@ __device__ float cvt_reciprocal(int b, float g) {
     near[k] = fabsf(dlo) <= tol || fabsf(dhi) <= tol;
     B[k] = fabsf(dlo) <= tol ? lo : hi;
     const float dB = fabsf(dlo) <= tol ? dlo : dhi;
-    up[k] = dB > 0.0f || (dB == 0.0f && (k & 1));  // exact side; a tie at odd k goes up to the even code
+    if (k >= 7 && near[k] && dB == 0.0f) return -1.0f;  // a bf16 value on a grid point
+    up[k] = dB > 0.0f || (dB == 0.0f && (k & 1));  // exact side; a midpoint tie at odd k goes up to the even code
   }
   const int step[5] = {0, -1, 1, -2, 2};
 #pragma unroll 1
@@ -349,9 +362,10 @@ __device__ float cvt_reciprocal(int b, float g) {
     const float r = __uint_as_float(__float_as_uint(r0) + step[i]);
     bool ok = true;
 #pragma unroll
-    for (int k = 0; k < 7; ++k) {
+    for (int k = 0; k < 14; ++k) {
       const float y = __fmul_rn(B[k], r);
-      ok = ok && (!near[k] || (y > mids[k] || (y == mids[k] && (k & 1))) == up[k]);
+      const bool side = k < 7 ? (y > pts[k] || (y == pts[k] && (k & 1))) : y > pts[k];
+      ok = ok && (!near[k] || (side == up[k] && (k < 7 || y != pts[k])));
     }
     if (ok) return r;
   }
@@ -384,42 +398,29 @@ __device__ void build_encode_tables(EncodeTables& t, float g, bool with_rcp, int
   }
 }
 
-// Per-tensor thresholds of the guided encoding for bf16 input, built in shared memory like
-// EncodeTables: for scale byte b and grid point G_k (0.5, 1, 1.5, 2, 3, 4, 6), in both halves of
-// a word, ge: x >= G_k E4M3(b) g <=> x > ge (pred of the bf16 rounded up), gt: x > G_k E4M3(b) g
-// <=> x > gt (the bf16 rounded down); b = 0: +inf.
-struct GuidedTables {
-  uint4 ge[0x7F][2];
-  uint4 gt[0x7F][2];
+// Per-tensor tables of the guided, record and cached bf16 encodings, built in shared memory by
+// every CTA: mid as in EncodeTables (the scale byte; not built for cached), and rcp[b] a reciprocal
+// of E4M3(b) g checked against the grid points (and for the record against the midpoints too)
+// by cvt_reciprocal, else -1 (those scale bytes take the compare form).
+struct ModeTables {
+  float2 mid[0x7E];
+  float rcp[0x7F];
 };
 
-__device__ void build_guided_tables(GuidedTables& t, float g) {
-  const float grid[7] = {0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-  for (int b = threadIdx.x; b < 0x7F; b += blockDim.x) {
-    uint32_t e[8], u[8];
-    if (b == 0 || !(g > 0.0f)) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) e[k] = u[k] = 0x7F807F80u;
-    } else {
-      const float dec = e4m3_decode_pos(b);
-#pragma unroll
-      for (int k = 0; k < 7; ++k) {
-        const uint32_t te = bf16_ru(__fmul_ru(grid[k] * dec, g)) - 1u, tu = bf16_rd(__fmul_rd(grid[k] * dec, g));
-        e[k] = te | (te << 16);
-        u[k] = tu | (tu << 16);
-      }
-      e[7] = u[7] = 0u;
+__device__ void build_mode_tables(ModeTables& t, float g, bool with_mid, bool mids, int tid, int nthreads) {
+  if (with_mid) {
+    for (int i = tid; i < 0x7E; i += nthreads) {
+      const float m3 = 3.0f * (e4m3_decode_pos(i) + e4m3_decode_pos(i + 1));  // exact in fp32
+      t.mid[i] = make_float2(__fmul_rd(m3, g), __fmul_ru(m3, g));
     }
-    t.ge[b][0] = make_uint4(e[0], e[1], e[2], e[3]);
-    t.ge[b][1] = make_uint4(e[4], e[5], e[6], e[7]);
-    t.gt[b][0] = make_uint4(u[0], u[1], u[2], u[3]);
-    t.gt[b][1] = make_uint4(u[4], u[5], u[6], u[7]);
   }
+  for (int b = tid; b < 0x7F; b += nthreads) t.rcp[b] = cvt_reciprocal(b, g, mids, true);
 }
 
 // Exact E4M3 scale byte of bamax / (6 g) from the estimate `est` and the midpoint table: the
 // same decision as scale_byte, with the midpoint products looked up instead of computed.
-__device__ __forceinline__ uint32_t scale_byte_tab(float bamax, float est, const EncodeTables& t) {
+template <class Tables>
+__device__ __forceinline__ uint32_t scale_byte_tab(float bamax, float est, const Tables& t) {
   const uint32_t b = min(e4m3_estimate(est), 0x7Eu);
   uint32_t dec = 0, inc = 0;
   if (b > 0) {
@@ -499,109 +500,6 @@ __device__ __forceinline__ void encode_block_bf16(const uint4 (&v)[2], int64_t b
   }
   *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(out[0], out[1]);
   scales[blk] = static_cast<uint8_t>(b);
-}
-
-// Plain encoding of one block of bf16 values, as encode_block_bf16, and the record of its rounding
-// directions: with c_ge the number of grid points at or below |x| (the guided tables' >=
-// thresholds), the plain magnitude is c_ge or c_ge + 1, and the element's bit is their difference
-// (1: rounded up in magnitude). Bit i of record16[blk] belongs to element i of the block.
-__device__ __forceinline__ void encode_block_bf16_record(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
-                                                         float est_scale, const EncodeTables& tab,
-                                                         const GuidedTables& gtab, uint8_t* __restrict__ codes,
-                                                         uint8_t* __restrict__ scales,
-                                                         uint16_t* __restrict__ record16) {
-  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
-  uint32_t aw[8];
-  uint32_t m2 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    aw[i] = w[i] & 0x7FFF7FFFu;
-    m2 = __vmaxu2(m2, aw[i]);
-  }
-  const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-  uint32_t b = 0;
-  if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, tab);
-  const uint4 ta = tab.thr[b][0], tb = tab.thr[b][1], ea = gtab.ge[b][0], eb = gtab.ge[b][1];
-  const uint32_t T2[7] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z};
-  const uint32_t GE[7] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z};
-  uint32_t byte[8];
-  uint32_t bits = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t acc = 0x43004300u, ce = 0x43004300u;  // bf16x2 (128, 128): the counts land in bits 0-2
-#pragma unroll
-    for (int k = 0; k < 7; ++k) {
-      acc = bf16x2_add(acc, bf16x2_gt(aw[i], T2[k]));
-      ce = bf16x2_add(ce, bf16x2_gt(aw[i], GE[k]));
-    }
-    const uint32_t m = acc & 0x00070007u;
-    const uint32_t d = (m - (ce & 0x00070007u)) & 0x00010001u;  // per half m >= c_ge: no borrow
-    bits |= ((d & 1u) | ((d >> 15) & 2u)) << (2 * i);
-    const uint32_t s = w[i] & 0x80008000u;
-    byte[i] = m | (m >> 12) | (s >> 12) | (s >> 24);
-  }
-  const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
-  const uint32_t hi = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
-  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo, hi);
-  scales[blk] = static_cast<uint8_t>(b);
-  record16[blk] = static_cast<uint16_t>(bits);
-}
-
-// Guided encoding of one block of bf16 values (finite), two elements per instruction: c_ge and
-// c_gt count the grid points below-or-at and strictly below |x| (bf16x2 compares against the
-// tables), x is on the grid when they differ or x = 0, and the magnitude is c_ge, plus one when
-// the element's mask bit is set, x is off the grid and c_ge < 7. The scale byte is the plain one,
-// or, with kGivenScale, scales_in[blk] (above 0x7E read as 0x7E; 0 when g is not positive), and
-// then no scale byte is written.
-template <bool kGivenScale>
-__device__ __forceinline__ void encode_block_bf16_guided(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
-                                                         float est_scale, const EncodeTables* tab,
-                                                         const GuidedTables& gtab, const uint32_t* __restrict__ mask,
-                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                         const uint8_t* __restrict__ scales_in) {
-  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
-  uint32_t aw[8];
-  uint32_t m2 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    aw[i] = w[i] & 0x7FFF7FFFu;
-    m2 = __vmaxu2(m2, aw[i]);
-  }
-  uint32_t b = 0;
-  if (kGivenScale) {
-    if (g > 0.0f) b = min(static_cast<uint32_t>(scales_in[blk]), 0x7Eu);
-  } else {
-    const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-    if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, *tab);
-  }
-  const uint4 ea = gtab.ge[b][0], eb = gtab.ge[b][1], ua = gtab.gt[b][0], ub = gtab.gt[b][1];
-  const uint32_t GE[7] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z};
-  const uint32_t GT[7] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z};
-  const uint32_t up_bits = (mask[blk >> 1] >> ((blk & 1) * 16)) & (b ? 0xFFFFu : 0u);
-  uint32_t byte[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t ce = 0x43004300u, cu = 0x43004300u;  // bf16x2 (128, 128): the counts land in bits 0-2
-#pragma unroll
-    for (int k = 0; k < 7; ++k) {
-      ce = bf16x2_add(ce, bf16x2_gt(aw[i], GE[k]));
-      cu = bf16x2_add(cu, bf16x2_gt(aw[i], GT[k]));
-    }
-    const uint32_t c = ce & 0x00070007u;
-    // per 16-bit half, as 0/1 in bit 0: on the grid (the counts differ), x != 0, c == 7
-    const uint32_t on = (((ce ^ cu) & 0x00070007u) + 0x00070007u) >> 3 & 0x00010001u;
-    const uint32_t nz = ((aw[i] + 0x7FFF7FFFu) >> 15) & 0x00010001u;
-    const uint32_t c7 = ((c + 0x00010001u) >> 3) & 0x00010001u;
-    const uint32_t t = up_bits >> (2 * i);
-    const uint32_t up = (t & 1u) | ((t & 2u) << 15);
-    const uint32_t m = c + (up & nz & ~on & ~c7 & 0x00010001u);
-    const uint32_t s = w[i] & 0x80008000u;
-    byte[i] = m | (m >> 12) | (s >> 12) | (s >> 24);
-  }
-  const uint32_t lo = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
-  const uint32_t hi = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
-  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(lo, hi);
-  if (!kGivenScale) scales[blk] = static_cast<uint8_t>(b);
 }
 
 // Scale byte and codes of one block, written to scales[blk] and codes[8 blk .. 8 blk + 7], with
@@ -703,6 +601,163 @@ __device__ __forceinline__ void encode_block(const BlockWords<kDtype>& w, int64_
   if (kMode != kModeCached) scales[blk] = static_cast<uint8_t>(b);
 }
 
+// Four code bytes (two E2M1 codes each, low nibble first) -> four f16x2 grid values (low half =
+// low nibble).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&d)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(w));
+}
+
+// f16x2 of (hi, lo), each rounded toward zero.
+__device__ __forceinline__ uint32_t f16x2_rz(float hi, float lo) {
+  uint32_t d;
+  asm("cvt.rz.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Per 16-bit half: 0xFFFF where a < b (f16), else 0.
+__device__ __forceinline__ uint32_t f16x2_lt_mask(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("set.lt.u32.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Per 16-bit half: 0xFFFF where a == b (f16), else 0.
+__device__ __forceinline__ uint32_t f16x2_eq_mask(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("set.eq.u32.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Per 16-bit half: 0xFFFF where the bf16 value is not +-0 (finite input), else 0.
+__device__ __forceinline__ uint32_t bf16x2_nonzero_mask(uint32_t a) {
+  uint32_t d;
+  asm("set.ne.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(0u));
+  return d;
+}
+
+// a b + c (low 32 bits) and the high 32 bits of the signed 64-bit product a b, plus c.
+__device__ __forceinline__ uint32_t mad_lo_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t mad_hi_s32(uint32_t a, int32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.hi.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Guided, cached or record encoding of one bf16 block (kMode != kModePlain) in the conversion
+// form. The scale byte is the plain one (scale_byte_tab), or for kModeCached the given byte
+// (above 0x7E read as 0x7E; 0 when g is not positive). With r = tab.rcp[b] (cvt_reciprocal with
+// the grid points) and y = fl32(x r): c, the nearest code of y (cvt.rn.satfinite.e2m1x2), is the
+// floor or the ceiling of |x| / d on the E2M1 grid, and lt = (|y| < G_c) decides which, exactly
+// (y is on the side of every grid point that |x| / d is on; the compare runs on f16 values
+// rounded toward zero, G_c being a short f16 value). So, per element:
+//   plain code c, rounding-direction bit lt (kModeRecord);
+//   floor c - lt, ceiling c + 1 - lt for x != 0, capped at code 7 (guided: the ceiling where the
+//   mask bit is set, the scale byte nonzero and x off the grid, which is every x != 0 here: no
+//   bf16 value lies on a grid point for the bytes the table accepts).
+// Non-finite blocks and bytes the table rejects take encode_block's compare form, which writes
+// the same bytes. `mask_word` is mask[blk >> 1] (guided and cached).
+template <int kMode, class Tables>
+__device__ __forceinline__ void encode_block_bf16_conv(const uint4 (&v)[2], int64_t blk, float g, float inv_g6,
+                                                       float est_scale, float g6, const Tables& tab,
+                                                       uint32_t mask_word, uint32_t given_scale,
+                                                       const uint32_t* __restrict__ mask, uint8_t* __restrict__ codes,
+                                                       uint8_t* __restrict__ scales, uint16_t* __restrict__ record16,
+                                                       const uint8_t* __restrict__ scales_in) {
+  constexpr bool kGuided = kMode == kModeGuided || kMode == kModeCached;
+  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+  const uint32_t bamax_bits = max(m2 & 0xFFFFu, m2 >> 16);
+  uint32_t b = 0;
+  if constexpr (kMode == kModeCached) {
+    if (g > 0.0f) b = min(given_scale, 0x7Eu);
+  } else {
+    const float bamax = __uint_as_float(bamax_bits << 16);
+    if (g > 0.0f) b = scale_byte_tab(bamax, (bamax * est_scale) * inv_g6, tab);
+  }
+  const float r = tab.rcp[b];
+  if (!(r >= 0.0f && bamax_bits < 0x7F80u)) {
+    BlockWords<NVFP4RL_BF16> bw;
+    bw.v[0] = v[0];
+    bw.v[1] = v[1];
+    encode_block<NVFP4RL_BF16, kMode>(bw, blk, g, est_scale, g6, mask, codes, scales, record16, scales_in);
+    return;
+  }
+  // up bits of elements 8h .. 8h + 7 at bits 0, 4, .., 28 of upn[h]: the nibble layout of the codes
+  uint32_t upn[2] = {0u, 0u};
+  if constexpr (kGuided) {
+    const uint32_t up16 = b ? (mask_word >> ((blk & 1) * 16)) & 0xFFFFu : 0u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t x = (up16 >> (8 * h)) & 0xFFu;
+      x = (x | (x << 12)) & 0x000F000Fu;
+      x = (x | (x << 6)) & 0x03030303u;
+      upn[h] = (x | (x << 3)) & 0x11111111u;
+    }
+  }
+  uint32_t out[2], rec = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      y[2 * j] = __fmul_rn(__uint_as_float(w[4 * h + j] << 16), r);
+      y[2 * j + 1] = __fmul_rn(__uint_as_float(w[4 * h + j] & 0xFFFF0000u), r);
+    }
+    uint32_t q = e2m1_word(y);  // nearest codes, signed
+    uint32_t G[4];
+    e2m1x8_to_f16x2(q & 0x77777777u, G);  // |G_c|
+    uint32_t ltn = 0, xn = 0;  // per element, in the nibble layout: |y| < G_c; x != 0 and c < 7
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t z = f16x2_rz(fabsf(y[2 * j + 1]), fabsf(y[2 * j]));
+      const uint32_t lt = f16x2_lt_mask(z, G[j]);  // |y| < G_c: c is the ceiling
+      if constexpr (kMode == kModeRecord) {
+        rec |= lt & (0x00010001u << (4 * h + j));
+      } else {
+        const uint32_t c7 = f16x2_eq_mask(G[j], 0x46004600u);
+        const uint32_t nz = bf16x2_nonzero_mask(w[4 * h + j]);
+        // bit 12 (low half) and bit 16 (high half) of each mask, moved to this pair's two nibbles
+        // (bits 8j and 8j + 4) by integer multiply-adds, which run beside the logic ops
+        const uint32_t lt_b = lt & 0x00011000u, x_b = nz & ~c7 & 0x00011000u;
+        if (j < 2) {
+          ltn = mad_hi_s32(lt_b, 1 << (20 + 8 * j), ltn);  // (lt_b << (20 + 8j)) >> 32 = lt_b >> (12 - 8j)
+          xn = mad_hi_s32(x_b, 1 << (20 + 8 * j), xn);
+        } else {
+          ltn = mad_lo_u32(lt_b, 1u << (8 * j - 12), ltn);
+          xn = mad_lo_u32(x_b, 1u << (8 * j - 12), xn);
+        }
+      }
+    }
+    // floor = c - lt; the ceiling adds one where c is the ceiling already (lt) or x != 0 lies above
+    // G_c below the top of the grid: code = c - lt + (up & (lt | (x != 0 & c < 7)))
+    if constexpr (kGuided) q = q + (upn[h] & (ltn | xn)) - ltn;
+    out[h] = q;
+  }
+  *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(out[0], out[1]);
+  if constexpr (kMode != kModeCached) scales[blk] = static_cast<uint8_t>(b);
+  if constexpr (kMode == kModeRecord) {
+    // element 2p's bit at p, element 2p + 1's at 16 + p -> bits 2p and 2p + 1
+    uint32_t x = rec;
+    x = (x | (x << 4)) & 0x0F0F0F0Fu;
+    x = (x | (x << 2)) & 0x33333333u;
+    x = (x | (x << 1)) & 0x55555555u;
+    record16[blk] = static_cast<uint16_t>((x & 0xFFFFu) | ((x >> 16) << 1));
+  }
+}
+
 // kModeCached reads g from g_in and the scale bytes from scales_in, and writes the codes only;
 // the other modes take g = amax / 2688 (amax from amax_in, else the accumulated amax_bits) and
 // write g, the scale bytes and the codes (kModeRecord also the rounding-direction bits).
@@ -730,16 +785,6 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   const bool tiny = g < 0x1p-60f;
   const float est_scale = tiny ? 0x1p64f : 1.0f;
   const float g6 = 6.0f * (g * est_scale);
-  const float inv_g6 = 1.0f / g6;
-  // bf16 tables: the plain ones unless the scale bytes are given, the guided ones unless plain
-  __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kMode != kModeCached, EncodeTables, char> tab;
-  __shared__ std::conditional_t<kDtype == NVFP4RL_BF16 && kMode != kModePlain, GuidedTables, char> gtab;
-  if constexpr (kDtype == NVFP4RL_BF16) {
-    if constexpr (kMode != kModeCached) build_encode_tables(tab, g, kMode == kModePlain, threadIdx.x, blockDim.x);
-    if constexpr (kMode != kModePlain) build_guided_tables(gtab, g);
-    __syncthreads();
-  }
-
   // Two blocks per iteration, both loaded before either is encoded, and the next iteration's
   // two loaded before this one's are encoded (software pipelining: more bytes in flight).
   // The blocks are visited from the end of the tensor to its start: the amax pass that
@@ -756,53 +801,52 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
     const BlockWords<kDtype> a = na, b = nb;
     if (j + 2 * stride < nblocks) load_block<kDtype>(x, blk - 2 * stride, na);
     if (j + 3 * stride < nblocks) load_block<kDtype>(x, blk - 3 * stride, nb);
-    if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModePlain) {
-      encode_block_bf16(a.v, blk, g, inv_g6, est_scale, tab, codes, scales);
-      if (two) encode_block_bf16(b.v, blk2, g, inv_g6, est_scale, tab, codes, scales);
-    } else if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModeRecord) {
-      encode_block_bf16_record(a.v, blk, g, inv_g6, est_scale, tab, gtab, codes, scales, record16);
-      if (two) encode_block_bf16_record(b.v, blk2, g, inv_g6, est_scale, tab, gtab, codes, scales, record16);
-    } else if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModeGuided) {
-      encode_block_bf16_guided<false>(a.v, blk, g, inv_g6, est_scale, &tab, gtab, mask, codes, scales, nullptr);
-      if (two) encode_block_bf16_guided<false>(b.v, blk2, g, inv_g6, est_scale, &tab, gtab, mask, codes, scales, nullptr);
-    } else if constexpr (kDtype == NVFP4RL_BF16) {
-      // the given scale bytes need no scale tables
-      encode_block_bf16_guided<true>(a.v, blk, g, inv_g6, est_scale, nullptr, gtab, mask, codes, nullptr, scales_in);
-      if (two) encode_block_bf16_guided<true>(b.v, blk2, g, inv_g6, est_scale, nullptr, gtab, mask, codes, nullptr, scales_in);
-    } else {
-      encode_block<kDtype, kMode>(a, blk, g, est_scale, g6, mask, codes, scales, record16, scales_in);
-      if (two) encode_block<kDtype, kMode>(b, blk2, g, est_scale, g6, mask, codes, scales, record16, scales_in);
-    }
+    encode_block<kDtype, kMode>(a, blk, g, est_scale, g6, mask, codes, scales, record16, scales_in);
+    if (two) encode_block<kDtype, kMode>(b, blk2, g, est_scale, g6, mask, codes, scales, record16, scales_in);
   }
 }
 
-// Plain encoding of one bf16 tensor fed through shared memory: warp 0 streams the tensor in 16 KB
-// chunks with cp.async.bulk into a ring of kEncRingStages stages (bulk copies keep far more bytes
-// in flight than per-thread loads), and warps 1-8 encode the chunk's 512 blocks from shared memory,
-// two per thread, with the same tables and block encoder as quantize_kernel (so the same bytes).
-// Chunks are visited from the end of the tensor to its start, like quantize_kernel's blocks.
+// Encoding of one bf16 tensor fed through shared memory: warp 0 streams the tensor in 16 KB chunks
+// with cp.async.bulk into a ring of kEncRingStages stages (bulk copies keep far more bytes in
+// flight than per-thread loads), and warps 1-8 encode the chunk's 512 blocks from shared memory,
+// two per thread. Plain: EncodeTables and encode_block_bf16; guided, record and cached:
+// ModeTables and encode_block_bf16_conv (each thread loads its blocks' mask words and given
+// scale bytes before it waits for the chunk). Chunks are visited from the end of the tensor to its
+// start (the amax pass before it reads from start to end, so the tail is still in L2). kModeCached
+// takes g from g_in and writes codes only; the other modes take g = amax / 2688 and write g, the
+// scale bytes and the codes (kModeRecord also the rounding-direction bits).
 constexpr int kEncRingWarps = 8;
 constexpr int kEncRingThreads = 32 * (kEncRingWarps + 1);
 constexpr int kEncRingStages = 4;
 constexpr int kEncRingSmem = kAmaxChunk * kEncRingStages;
 constexpr int kChunkBlocks = kAmaxChunk / 32;  // bf16 blocks of 16 elements per chunk
 
+template <int kMode>
 __global__ void __launch_bounds__(kEncRingThreads, 3)
     encode_ring_kernel(const uint8_t* __restrict__ x, int64_t nblocks, const uint32_t* __restrict__ amax_bits,
-                       const float* __restrict__ amax_in, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                       float* __restrict__ g_out, uint32_t* __restrict__ status) {
+                       const float* __restrict__ amax_in, const uint32_t* __restrict__ mask,
+                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ g_out,
+                       uint16_t* __restrict__ record16, const uint8_t* __restrict__ scales_in,
+                       const float* __restrict__ g_in, uint32_t* __restrict__ status) {
+  constexpr bool kPlain = kMode == kModePlain;
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kEncRingStages], empty[kEncRingStages];
-  __shared__ EncodeTables tab;
+  __shared__ std::conditional_t<kPlain, EncodeTables, ModeTables> tab;
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float amax = amax_in ? *amax_in : __uint_as_float(*amax_bits);
-  const float g = __fdiv_rn(amax, 2688.0f);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  float g;
+  if constexpr (kMode == kModeCached) {
+    g = *g_in;
+  } else {
+    const float amax = amax_in ? *amax_in : __uint_as_float(*amax_bits);
+    g = __fdiv_rn(amax, 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  }
   const bool tiny = g < 0x1p-60f;  // as in quantize_kernel
   const float est_scale = tiny ? 0x1p64f : 1.0f;
-  const float inv_g6 = 1.0f / (6.0f * (g * est_scale));
+  const float g6 = 6.0f * (g * est_scale);
+  const float inv_g6 = 1.0f / g6;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kEncRingStages; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
@@ -813,7 +857,8 @@ __global__ void __launch_bounds__(kEncRingThreads, 3)
   __syncthreads();
   // the encode warps build the tables (named barrier 1) while warp 0 starts the stream
   if (warp > 0) {
-    build_encode_tables(tab, g, true, threadIdx.x - 32, 32 * kEncRingWarps);
+    if constexpr (kPlain) build_encode_tables(tab, g, true, threadIdx.x - 32, 32 * kEncRingWarps);
+    else build_mode_tables(tab, g, kMode != kModeCached, kMode == kModeRecord, threadIdx.x - 32, 32 * kEncRingWarps);
     named_barrier_sync(1, 32 * kEncRingWarps);
   }
   const int64_t bytes = nblocks * 32;
@@ -843,15 +888,25 @@ __global__ void __launch_bounds__(kEncRingThreads, 3)
     const int t = threadIdx.x - 32;
     for (int64_t j = 0; j < mine; ++j) {
       const int s = static_cast<int>(j % kEncRingStages);
+      const int64_t c = nchunks - 1 - (blockIdx.x + j * gridDim.x);
+      const int nblk = static_cast<int>(min(static_cast<int64_t>(kChunkBlocks), nblocks - c * kChunkBlocks));
+      const bool one = t < nblk, two = t + 32 * kEncRingWarps < nblk;
+      const int64_t blk_a = c * kChunkBlocks + t, blk_b = blk_a + 32 * kEncRingWarps;
+      uint32_t mw_a = 0, mw_b = 0, sb_a = 0, sb_b = 0;
+      if constexpr (kMode == kModeGuided || kMode == kModeCached) {
+        if (one) mw_a = __ldg(mask + (blk_a >> 1));
+        if (two) mw_b = __ldg(mask + (blk_b >> 1));
+      }
+      if constexpr (kMode == kModeCached) {
+        if (one) sb_a = __ldg(scales_in + blk_a);
+        if (two) sb_b = __ldg(scales_in + blk_b);
+      }
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((j / kEncRingStages) & 1),
                                              status, kStatusTimeoutDequant)))
         break;
-      const int64_t c = nchunks - 1 - (blockIdx.x + j * gridDim.x);
-      const int nblk = static_cast<int>(min(static_cast<int64_t>(kChunkBlocks), nblocks - c * kChunkBlocks));
       const uint4* v = reinterpret_cast<const uint4*>(ring + s * kAmaxChunk);
       uint4 a[2], b[2];
-      const bool two = t + 32 * kEncRingWarps < nblk;
-      if (t < nblk) {
+      if (one) {
         a[0] = v[2 * t];
         a[1] = v[2 * t + 1];
       }
@@ -861,8 +916,17 @@ __global__ void __launch_bounds__(kEncRingThreads, 3)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));  // this warp has read the stage
-      if (t < nblk) encode_block_bf16(a, c * kChunkBlocks + t, g, inv_g6, est_scale, tab, codes, scales);
-      if (two) encode_block_bf16(b, c * kChunkBlocks + t + 32 * kEncRingWarps, g, inv_g6, est_scale, tab, codes, scales);
+      if constexpr (kPlain) {
+        if (one) encode_block_bf16(a, blk_a, g, inv_g6, est_scale, tab, codes, scales);
+        if (two) encode_block_bf16(b, blk_b, g, inv_g6, est_scale, tab, codes, scales);
+      } else {
+        if (one)
+          encode_block_bf16_conv<kMode>(a, blk_a, g, inv_g6, est_scale, g6, tab, mw_a, sb_a, mask, codes, scales,
+                                        record16, scales_in);
+        if (two)
+          encode_block_bf16_conv<kMode>(b, blk_b, g, inv_g6, est_scale, g6, tab, mw_b, sb_b, mask, codes, scales,
+                                        record16, scales_in);
+      }
     }
   }
 }
@@ -979,7 +1043,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2)
 //            max of |y| (bf16 patterns) is reduced per CTA and folded into sync[0];
 //   barrier  every CTA arrives on the counter sync[4] and waits (bounded) for all the others:
 //            then sync[0] holds amax over all of y, so g = amax / 2688 is known;
-//   phase 2  this CTA's rows are encoded from shared memory with quantize_kernel's bf16 code
+//   phase 2  this CTA's rows are encoded from shared memory with the plain bf16 block encoder
 //            (same blocks, tables and results as nvfp4_quantize of y).
 // y is read from HBM never: x in, y and the codes out. sync[0] and sync[4] start at zero.
 constexpr int kFuseThreads = 1024;
@@ -1260,7 +1324,8 @@ int quantize_ctas_per_sm(int device) {
 
 namespace {
 
-// CTAs of encode_ring_kernel resident per SM (once per device; sets its shared-memory size).
+// CTAs of encode_ring_kernel<kMode> resident per SM (once per device; sets its shared-memory size).
+template <int kMode>
 int encode_ring_ctas_per_sm(int device) {
   static std::mutex mu;
   static std::map<int, int> cache;
@@ -1268,9 +1333,9 @@ int encode_ring_ctas_per_sm(int device) {
   auto it = cache.find(device);
   if (it != cache.end()) return it->second;
   int n = 0;
-  if (cudaFuncSetAttribute(encode_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncRingSmem) !=
+  if (cudaFuncSetAttribute(encode_ring_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncRingSmem) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_ring_kernel, kEncRingThreads, kEncRingSmem) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_ring_kernel<kMode>, kEncRingThreads, kEncRingSmem) !=
           cudaSuccess ||
       n < 1) {
     cudaGetLastError();
@@ -1280,25 +1345,28 @@ int encode_ring_ctas_per_sm(int device) {
   return n;
 }
 
+// bf16 input: every mode through encode_ring_kernel; fp32 input: quantize_kernel.
 template <int kDtype, int kMode>
 cudaError_t launch_encode(int64_t nblocks, const DeviceInfo& dev, cudaStream_t st, const void* x,
                           const uint32_t* amax_bits, const float* amax_in, const uint32_t* mask, uint8_t* codes,
                           uint8_t* scales, float* g, uint16_t* record16, const uint8_t* scales_in, const float* g_in) {
-  if constexpr (kDtype == NVFP4RL_BF16 && kMode == kModePlain) {
-    const int per_sm = encode_ring_ctas_per_sm(dev.device);
+  if constexpr (kDtype == NVFP4RL_BF16) {
+    const int per_sm = encode_ring_ctas_per_sm<kMode>(dev.device);
     if (per_sm == 0) return cudaErrorLaunchFailure;
     const int64_t nchunks = (nblocks * 32 + kAmaxChunk - 1) / kAmaxChunk;
     const int grid = static_cast<int>(std::min<int64_t>(nchunks, static_cast<int64_t>(dev.sm_count) * per_sm));
-    return launch_pdl(encode_ring_kernel, dim3(grid), dim3(kEncRingThreads), kEncRingSmem, st,
-                      static_cast<const uint8_t*>(x), nblocks, amax_bits, amax_in, codes, scales, g, dev.status);
+    return launch_pdl(encode_ring_kernel<kMode>, dim3(grid), dim3(kEncRingThreads), kEncRingSmem, st,
+                      static_cast<const uint8_t*>(x), nblocks, amax_bits, amax_in, mask, codes, scales, g, record16,
+                      scales_in, g_in, dev.status);
+  } else {
+    // one wave: as many CTAs as can be resident at once (each loops over its share of the blocks)
+    const int threads = 256;
+    const int64_t want = (nblocks + threads - 1) / threads;
+    const int per_sm = quantize_ctas_per_sm<kDtype, kMode>(dev.device);
+    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(dev.sm_count) * per_sm));
+    return launch_pdl(quantize_kernel<kDtype, kMode>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_bits,
+                      amax_in, mask, codes, scales, g, record16, scales_in, g_in);
   }
-  // one wave: as many CTAs as can be resident at once (each loops over its share of the blocks)
-  const int threads = 256;
-  const int64_t want = (nblocks + threads - 1) / threads;
-  const int per_sm = quantize_ctas_per_sm<kDtype, kMode>(dev.device);
-  const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(dev.sm_count) * per_sm));
-  return launch_pdl(quantize_kernel<kDtype, kMode>, dim3(grid), dim3(threads), 0, st, x, nblocks, amax_bits, amax_in,
-                    mask, codes, scales, g, record16, scales_in, g_in);
 }
 
 template <int kMode>

@@ -323,6 +323,60 @@ def test_quantize_cached_replay(nv, dtype):
     assert np.array_equal(gpu_cached(nv, xe, me, se, ge), ce), "edge values"
 
 
+def _blocks_next_to_grid(M, seed):
+    """bf16 blocks of every normal scale byte s whose elements are the three bf16 values nearest to each
+    grid point G E4M3(s) g and each midpoint m E4M3(s) g, the block maximum 6 E4M3(s) g, random signs;
+    g = amax / 2688 for the amax mantissa M (as in test_quantize_bf16_next_to_midpoints)."""
+    rng = np.random.default_rng(seed)
+    amax = np.float32(M * 2.0 ** -4)
+    g = float(np.float32(amax / np.float32(2688.0)))
+    pts = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    blocks = []
+    for b in range(0x08, 0x78):  # 6 E4M3(s) g stays below amax
+        d = float(oracle.e4m3_value(b)) * g
+        near = []
+        for p in pts:
+            c = int(synth.bf16_bits(np.array([p * d], np.float32))[0])
+            near += [c - 1, c, c + 1]
+        top = int(synth.bf16_bits(np.array([6.0 * d], np.float32))[0])
+        vals = np.array(near + near[:3], np.uint16)  # 45 values: three blocks of 15 beside the maximum
+        for i in range(3):
+            blk = np.concatenate([[top], vals[15 * i:15 * i + 15]]).astype(np.uint16)
+            blk = blk | (rng.integers(0, 2, 16) << 15).astype(np.uint16)
+            blocks.append(rng.permutation(blk))
+    amax_block = np.zeros(16, np.uint16)
+    amax_block[3] = synth.bf16_bits(np.array([amax], np.float32))[0]
+    blocks.append(amax_block)
+    blocks += [np.zeros(16, np.uint16)] * (-len(blocks) % 4)
+    return np.stack(blocks).reshape(-1, 64), g
+
+
+@pytest.mark.parametrize("M", [137, 150, 161, 231])
+def test_quantize_guided_record_cached_next_to_grid_points(nv, M):
+    """Guided, record and cached encodings of bf16 values next to every grid point and midpoint of
+    every normal scale byte (see _blocks_next_to_grid): the bf16 path decides floor and ceiling from the
+    hardware conversion of x times a reciprocal of E4M3(s) g, checked per scale byte against exactly
+    these values (with M = 231 some of them lie on a grid point and the byte takes the compare form);
+    codes, scales, g and record bits bit-exact against the oracle."""
+    x, g = _blocks_next_to_grid(M, 40 + M)
+    mask = synth.guided_mask(x.size, M, 1)
+    want = oracle.quantize(x, mask=mask)
+    assert float(want[2]) == g
+    assert_quant_equal(gpu_quantize(nv, x, mask=mask), want, f"guided next to grid points, M {M}")
+    got, rec = gpu_record(nv, x)
+    c, s, gr, m = oracle.quantize_record(x)
+    assert_quant_equal(got, (c, s, gr), f"record next to grid points, M {M}")
+    assert np.array_equal(_mask_bits(rec, x.size), _mask_bits(m, x.size)), f"record bits, M {M}"
+    assert np.array_equal(gpu_cached(nv, x, mask, s, gr), oracle.quantize_cached(x, mask, s, gr)), "cached"
+    # given scale bytes one step off for a third of the blocks: the values then sit elsewhere on the grid
+    s2 = s.copy().reshape(-1)
+    rng = np.random.default_rng(M)
+    pick = rng.random(s2.size) < 1 / 3
+    s2[pick] = np.clip(s2[pick].astype(np.int32) + rng.choice([-1, 1], int(pick.sum())), 0, 0x7E).astype(np.uint8)
+    s2 = s2.reshape(s.shape)
+    assert np.array_equal(gpu_cached(nv, x, mask, s2, gr), oracle.quantize_cached(x, mask, s2, gr)), "cached, moved"
+
+
 def test_trace_round_trip_gpu_only_qwen7b_gate(nv):
     """The full 7B gate weight (18944 x 3584 bf16): record, then replay from the GPU's own cache,
     gives the GPU's plain codes back; sampled rows of the record and of the codes match the oracle."""
