@@ -654,6 +654,14 @@ __device__ __forceinline__ uint32_t mad_hi_s32(uint32_t a, int32_t b, uint32_t c
   return d;
 }
 
+// Per bf16 half: max(|a|, |b|) (sign bits: the XOR of the inputs'; the canonical NaN 0x7FFF if
+// either input is NaN).
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Guided, cached or record encoding of one bf16 block (kMode != kModePlain) in the conversion
 // form. The scale byte is the plain one (scale_byte_tab), or for kModeCached the given byte
 // (above 0x7E read as 0x7E; 0 when g is not positive). With r = tab.rcp[b] (cvt_reciprocal with
@@ -676,10 +684,10 @@ __device__ __forceinline__ void encode_block_bf16_conv(const uint4 (&v)[2], int6
                                                        const uint8_t* __restrict__ scales_in) {
   constexpr bool kGuided = kMode == kModeGuided || kMode == kModeCached;
   const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
-  uint32_t m2 = 0;
+  uint32_t m2 = w[0];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
-  const uint32_t bamax_bits = max(m2 & 0xFFFFu, m2 >> 16);
+  for (int i = 1; i < 8; ++i) m2 = bf16x2_max_abs(m2, w[i]);
+  const uint32_t bamax_bits = max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu);  // 0x7FFF if any x is NaN
   uint32_t b = 0;
   if constexpr (kMode == kModeCached) {
     if (g > 0.0f) b = min(given_scale, 0x7Eu);
