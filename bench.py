@@ -1109,12 +1109,18 @@ def oracle_sample(cfg, den: int):
 
 
 def sample_den(cfg, seconds_budget: float) -> int:
-    """The smallest sampling denominator whose oracle run fits the budget, extrapolated from a probe run at
-    the config's probe denominator."""
+    """The smallest sampling denominator whose oracle run fits the budget: two probe runs (at the config's
+    probe denominator and half of it) fit t(den) = a + b / den (a: the work that does not shrink with den,
+    such as the activation amax over all tokens), which is then extrapolated."""
     probe = cfg["probe_den"]
-    _, tp, _, _ = oracle_sample(cfg, probe)
+    _, t1, _, _ = oracle_sample(cfg, probe)
+    _, t2, _, _ = oracle_sample(cfg, probe // 2)
+    b = max(0.0, (t2 - t1) * probe)
+    a = max(0.0, t1 - b / probe)
+    if b == 0.0:  # timing noise: proportional extrapolation from the larger probe
+        a, b = 0.0, t2 * probe / 2
     den = 1
-    while den < probe and tp * probe / den > seconds_budget:
+    while den < probe and a + b / den > seconds_budget:
         den *= 2
     return den
 
