@@ -377,6 +377,32 @@ def test_quantize_guided_record_cached_next_to_grid_points(nv, M):
     assert np.array_equal(gpu_cached(nv, x, mask, s2, gr), oracle.quantize_cached(x, mask, s2, gr)), "cached, moved"
 
 
+def test_quantize_guided_record_cached_subnormal_elements(nv):
+    """Blocks that take the bf16 conversion form (a general g) whose other elements are bf16
+    subnormals (2^-133 .. 2^-127), tiny normals and +-0 beside a normal block maximum: every nonzero
+    element lies below the first grid point, so its floor is code 0 and its ceiling code 1, and the
+    guided encoding must tell a subnormal from zero. Codes, scales, g and record bits bit-exact
+    against the oracle; the cached mode with the recorded scales and a random mask."""
+    rng = np.random.default_rng(77)
+    rows, cols = 96, 512
+    bits = np.zeros((rows, cols), np.uint16)
+    sub = np.array([0x0001, 0x0002, 0x0007, 0x0040, 0x007F, 0x0080, 0x0081, 0x00FF, 0x0000], np.uint16)
+    for r in range(rows):
+        for b in range(cols // 16):
+            top = synth.bf16_bits(np.array([rng.uniform(0.01, 1.5)], np.float32))[0]
+            blk = np.concatenate([[top], rng.choice(sub, 15)]).astype(np.uint16)
+            blk = blk | (rng.integers(0, 2, 16) << 15).astype(np.uint16)
+            bits[r, 16 * b:16 * b + 16] = rng.permutation(blk)
+    bits[0, 0] = synth.bf16_bits(np.array([1.7], np.float32))[0]  # amax 1.7: g = 1.7 / 2688, not a power of two
+    mask = synth.guided_mask(bits.size, 77, 1)
+    assert_quant_equal(gpu_quantize(nv, bits, mask=mask), oracle.quantize(bits, mask=mask), "guided, subnormals")
+    got, rec = gpu_record(nv, bits)
+    c, s, g, m = oracle.quantize_record(bits)
+    assert_quant_equal(got, (c, s, g), "record, subnormals")
+    assert np.array_equal(_mask_bits(rec, bits.size), _mask_bits(m, bits.size)), "record bits, subnormals"
+    assert np.array_equal(gpu_cached(nv, bits, mask, s, g), oracle.quantize_cached(bits, mask, s, g)), "cached"
+
+
 def test_trace_round_trip_gpu_only_qwen7b_gate(nv):
     """The full 7B gate weight (18944 x 3584 bf16): record, then replay from the GPU's own cache,
     gives the GPU's plain codes back; sampled rows of the record and of the codes match the oracle."""
