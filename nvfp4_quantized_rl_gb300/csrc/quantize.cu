@@ -709,10 +709,10 @@ __device__ __forceinline__ void encode_block_bf16_conv(const uint4 (&v)[2], int6
     const uint32_t up16 = b ? (mask_word >> ((blk & 1) * 16)) & 0xFFFFu : 0u;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      uint32_t x = (up16 >> (8 * h)) & 0xFFu;
-      x = (x | (x << 12)) & 0x000F000Fu;
-      x = (x | (x << 6)) & 0x03030303u;
-      upn[h] = (x | (x << 3)) & 0x11111111u;
+      uint32_t x = (up16 >> (8 * h)) & 0xFFu;  // pair j's two bits to nibble j, then a byte lookup:
+      x = (x | (x << 4)) & 0x0F0Fu;            // 0 -> 0x00, 1 -> 0x01, 2 -> 0x10, 3 -> 0x11
+      x = (x | (x << 2)) & 0x3333u;
+      upn[h] = __byte_perm(0x11100100u, 0u, x);
     }
   }
   uint32_t out[2], rec = 0;
