@@ -819,7 +819,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
 // flight than per-thread loads), and warps 1-8 encode the chunk's 512 blocks from shared memory,
 // two per thread. Plain: EncodeTables and encode_block_bf16; guided, record and cached:
 // ModeTables and encode_block_bf16_conv (each thread loads its blocks' mask words and given
-// scale bytes before it waits for the chunk). Chunks are visited from the end of the tensor to its
+// scale bytes one chunk ahead). Chunks are visited from the end of the tensor to its
 // start (the amax pass before it reads from start to end, so the tail is still in L2). kModeCached
 // takes g from g_in and writes codes only; the other modes take g = amax / 2688 and write g, the
 // scale bytes and the codes (kModeRecord also the rounding-direction bits).
@@ -894,21 +894,36 @@ __global__ void __launch_bounds__(kEncRingThreads, 3)
     }
   } else {
     const int t = threadIdx.x - 32;
+    // this thread's blocks of chunk j: the mask words and given scale bytes are loaded one chunk
+    // ahead, while the previous chunk is encoded
+    const auto side = [&](int64_t jj, uint32_t (&sv)[4]) {
+      const int64_t cc = nchunks - 1 - (blockIdx.x + jj * gridDim.x);
+      const int nb = static_cast<int>(min(static_cast<int64_t>(kChunkBlocks), nblocks - cc * kChunkBlocks));
+      const int64_t ba = cc * kChunkBlocks + t, bb = ba + 32 * kEncRingWarps;
+      sv[0] = sv[1] = sv[2] = sv[3] = 0u;
+      if constexpr (kMode == kModeGuided || kMode == kModeCached) {
+        if (t < nb) sv[0] = __ldg(mask + (ba >> 1));
+        if (t + 32 * kEncRingWarps < nb) sv[1] = __ldg(mask + (bb >> 1));
+      }
+      if constexpr (kMode == kModeCached) {
+        if (t < nb) sv[2] = __ldg(scales_in + ba);
+        if (t + 32 * kEncRingWarps < nb) sv[3] = __ldg(scales_in + bb);
+      }
+    };
+    uint32_t cur[4] = {0u, 0u, 0u, 0u}, nxt[4] = {0u, 0u, 0u, 0u};
+    if constexpr (!kPlain) {
+      if (mine > 0) side(0, cur);
+    }
     for (int64_t j = 0; j < mine; ++j) {
       const int s = static_cast<int>(j % kEncRingStages);
       const int64_t c = nchunks - 1 - (blockIdx.x + j * gridDim.x);
       const int nblk = static_cast<int>(min(static_cast<int64_t>(kChunkBlocks), nblocks - c * kChunkBlocks));
       const bool one = t < nblk, two = t + 32 * kEncRingWarps < nblk;
       const int64_t blk_a = c * kChunkBlocks + t, blk_b = blk_a + 32 * kEncRingWarps;
-      uint32_t mw_a = 0, mw_b = 0, sb_a = 0, sb_b = 0;
-      if constexpr (kMode == kModeGuided || kMode == kModeCached) {
-        if (one) mw_a = __ldg(mask + (blk_a >> 1));
-        if (two) mw_b = __ldg(mask + (blk_b >> 1));
+      if constexpr (!kPlain) {
+        if (j + 1 < mine) side(j + 1, nxt);
       }
-      if constexpr (kMode == kModeCached) {
-        if (one) sb_a = __ldg(scales_in + blk_a);
-        if (two) sb_b = __ldg(scales_in + blk_b);
-      }
+      const uint32_t mw_a = cur[0], mw_b = cur[1], sb_a = cur[2], sb_b = cur[3];
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((j / kEncRingStages) & 1),
                                              status, kStatusTimeoutDequant)))
         break;
@@ -934,6 +949,8 @@ __global__ void __launch_bounds__(kEncRingThreads, 3)
         if (two)
           encode_block_bf16_conv<kMode>(b, blk_b, g, inv_g6, est_scale, g6, tab, mw_b, sb_b, mask, codes, scales,
                                         record16, scales_in);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
       }
     }
   }
