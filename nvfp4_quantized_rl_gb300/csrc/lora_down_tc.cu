@@ -38,8 +38,7 @@ constexpr int kRows = 128;                 // rows of x per CTA (MMA M)
 constexpr int kChunk = 64;                 // K per stage (128 bytes of bf16)
 constexpr int kXBytes = kRows * kChunk * 2;  // 16 KB
 constexpr int kMaxRank = 128;
-constexpr int kMaxStagesDown = 12;      // ring stages: as many as fit the shared-memory limit, at most this
-constexpr int kSmemLimit = 232448;      // dynamic shared memory per CTA on this GPU
+constexpr int kStages = 6;
 constexpr int kThreadsDown = 128;
 constexpr int kPartStride = kMaxRank + 4;  // fp32 words per partial row (+4: fewer bank conflicts)
 
@@ -52,7 +51,6 @@ struct DownParams {
   LoraDownScale ls;
   uint32_t* amax;  // or null
   uint32_t* status;
-  int stages;      // ring stages (down_stages(r))
 };
 
 __device__ __forceinline__ uint32_t tmem_cols_for(int r) { return r <= 32 ? 32u : r <= 64 ? 64u : 128u; }
@@ -64,10 +62,9 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int abytes = p.r * kChunk * 2;          // A rows of one stage
   const int stage_bytes = kXBytes + abytes;      // multiple of 1024 (r a multiple of 16 -> 2 KB steps)
-  const int stages = p.stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
-  uint64_t* empty = full + stages;
-  uint64_t* done = empty + stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* done = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   float* part = reinterpret_cast<float*>(smem);  // [kRows][kPartStride] after the K loop
 
@@ -83,7 +80,7 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
   griddep_wait();
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int i = 0; i < stages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
       mbar_init(smem_addr(&empty[i]), p.amax ? 3 : 1);  // the MMAs' commit (+ the two scanning warps)
     }
@@ -103,8 +100,8 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
     prefetch_tensormap(&map_a);
     int issued = 0;
     for (int i = 0; i < n && ok; ++i) {
-      const int s = i % stages;
-      if (i >= stages && !mbar_wait(smem_addr(&empty[s]), ((i / stages) - 1) & 1, p.status, kStatusTimeoutProducer)) {
+      const int s = i % kStages;
+      if (i >= kStages && !mbar_wait(smem_addr(&empty[s]), ((i / kStages) - 1) & 1, p.status, kStatusTimeoutProducer)) {
         ok = false;
         break;
       }
@@ -116,15 +113,15 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
       ++issued;
     }
     // do not leave with copies in flight
-    for (int i = max(0, issued - stages); i < issued; ++i)
-      mbar_wait(smem_addr(&full[i % stages]), (i / stages) & 1, p.status, kStatusTimeoutDrain);
+    for (int i = max(0, issued - kStages); i < issued; ++i)
+      mbar_wait(smem_addr(&full[i % kStages]), (i / kStages) & 1, p.status, kStatusTimeoutDrain);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     // The whole warp walks the chunks and waits; one elected lane issues the MMAs and commits.
     const uint32_t idesc = idesc_bf16_f32(kRows, static_cast<uint32_t>(p.r));
     for (int i = 0; i < n && ok; ++i) {
-      const int s = i % stages;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (i / stages) & 1, p.status, kStatusTimeoutMma));
+      const int s = i % kStages;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (i / kStages) & 1, p.status, kStatusTimeoutMma));
       if (!ok) break;
       tc_fence_after();
       const uint64_t xd = smem_desc(smem_addr(smem + s * stage_bytes), 16, 1024, 2);
@@ -143,8 +140,8 @@ __global__ void __launch_bounds__(kThreadsDown, 1)
     uint32_t m2 = 0;
     const int half = warp - 2;  // bytes [half 8 KB, half 8 KB + 8 KB) of the x tile
     for (int i = 0; i < n && ok; ++i) {
-      const int s = i % stages;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (i / stages) & 1, p.status, kStatusTimeoutMma));
+      const int s = i % kStages;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[s]), (i / kStages) & 1, p.status, kStatusTimeoutMma));
       if (!ok) break;
       const uint4* t = reinterpret_cast<const uint4*>(smem + s * stage_bytes + half * (kXBytes / 2));
 #pragma unroll 4
@@ -269,15 +266,8 @@ __global__ void __launch_bounds__(256) lora_scale_kernel(uint16_t* __restrict__ 
   }
 }
 
-// Ring stages for rank r: as many as the shared-memory limit allows (r = 64: 9 stages of 24 KB), up to
-// kMaxStagesDown; more bytes of x in flight per SM than a fixed six-stage ring.
-int down_stages(int r) {
-  const int stage = kXBytes + r * kChunk * 2;
-  return std::min(kMaxStagesDown, (kSmemLimit - 1024 - 256) / stage);
-}
-
 size_t down_smem_bytes(int r) {
-  return 1024 + static_cast<size_t>(down_stages(r)) * (kXBytes + static_cast<size_t>(r) * kChunk * 2) + 256;
+  return 1024 + static_cast<size_t>(kStages) * (kXBytes + static_cast<size_t>(r) * kChunk * 2) + 256;
 }
 
 // Largest cluster size (<= 8) whose clusters of this kernel fit on the device at once, per device
@@ -346,7 +336,6 @@ nvfp4rl_status launch_lora_down_tc(const uint16_t* x, int64_t M, int64_t K, cons
   p.ls = scale;
   p.amax = amax;
   p.status = dev.status;
-  p.stages = down_stages(r);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ks), static_cast<unsigned>(row_tiles), 1);
   cfg.blockDim = dim3(kThreadsDown, 1, 1);
